@@ -1,0 +1,175 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) DeepSeek-style Mixture-of-Experts layer forward.
+ *
+ * The layer, as the pages describe it:
+ *   "Lower latency and higher throughput with multi-node DeepSeek deployment" (Perplexity),
+ *     section "Expert Parallelism": 256 routed experts and 1 shared expert; every token is
+ *     sent to 8 distinct routed experts whose results are combined by a weighted sum, and
+ *     the shared expert's result is added.  Dispatch sends tokens to their experts before
+ *     the expert GEMMs; Combine gathers the results and forms the weighted sum.
+ *     section "MoE Router": a sort that keeps the indices produces the top-k; a dense
+ *     dispatch/combine needs per-expert aggregated routing information, not per-token.
+ *     section "Cuda Graph" / "Quantization": kernels read the routing counts on the device
+ *     instead of sizing work from buffer sizes, so a call can be captured in a CUDA graph.
+ *   "DeepSeek-V4.1-Flash" vLLM article, section "Kernels", Mega-Gate: the router (gate
+ *     GEMM, expert scoring, bias, top-k selection) runs as one fused kernel.
+ *   "GRACE-MoE" notes, "Core Idea 1. Expert Grouping": the expert affinity matrix A of
+ *     co-activations that grouping starts from; "2. Expert Replication": per-expert load W.
+ *
+ * Readings taken where the pages are silent (scoring = logistic sigmoid; the bias only
+ * selects; ties go to the lower expert index; weights are the selected unbiased scores
+ * divided by their sum; SwiGLU h = silu(x W1) * (x W3), y = h W2; shared expert weight 1)
+ * are stated again at each entry point below.
+ *
+ * Conventions for every entry point
+ *   - Every array argument is a DEVICE pointer owned by the caller, 16-byte aligned.
+ *     Host structs (moe_shape_t, moe_weights_t) are read during the call only.
+ *   - Row-major layouts; "bf16" arrays hold IEEE bfloat16 values (2 bytes each).
+ *   - `stream` is a cudaStream_t (0 = legacy default stream).  All work is enqueued on it;
+ *     no call synchronises the host, allocates or frees memory, so calls can be captured
+ *     in a CUDA graph.  Outputs are valid once the stream reaches them.
+ *   - `ws` is a caller-owned device workspace of at least moe_workspace_bytes() bytes
+ *     (256-byte aligned).  Calls that share a workspace must be serialised by the caller.
+ *   - Arguments are validated on the host before anything is enqueued: an invalid call
+ *     returns a negative moe_status_t and has no effect.  A failing launch returns
+ *     MOE_ERR_CUDA.  Conditions found on the device (a bounded wait that ran out) are
+ *     recorded in the workspace's status word; read them with moe_read_status().
+ *   - Supported shapes: 1 <= E <= 1024, 1 <= K <= min(E, 32), H and I multiples of 64,
+ *     T >= 0 (T == 0 enqueues nothing and returns MOE_OK), T*K < 2^31.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,        /* null pointer, negative size, K > E, ...            */
+    MOE_ERR_UNSUPPORTED_SHAPE = -2,  /* H or I not a multiple of 64, E > 1024, K > 32, ... */
+    MOE_ERR_MISALIGNED = -3,         /* a pointer is not 16-byte aligned (ws: 256-byte)     */
+    MOE_ERR_WORKSPACE_TOO_SMALL = -4,
+    MOE_ERR_CUDA = -5,               /* a CUDA runtime/driver call failed                  */
+    MOE_ERR_DEVICE_TIMEOUT = -6,     /* a bounded device-side wait ran out (status word)   */
+    MOE_ERR_NOT_IMPLEMENTED = -7
+} moe_status_t;
+
+/* Layer shape.  T tokens, hidden size H, E routed experts, top-K, expert intermediate
+ * size I, shared-expert intermediate size I_shared (0 = no shared expert). */
+typedef struct moe_shape {
+    int32_t T, H, E, K, I, I_shared;
+} moe_shape_t;
+
+/* Layer weights (device pointers).
+ *   W_gate bf16 [E, H]      router gate rows
+ *   bias   fp32 [E]         per-expert selection bias (selection only, not in the weights)
+ *   W1     bf16 [E, H, I]   gate projection of each routed expert (I contiguous)
+ *   W3     bf16 [E, H, I]   up projection
+ *   W2     bf16 [E, I, H]   down projection (H contiguous)
+ *   W1s, W3s bf16 [H, I_shared], W2s bf16 [I_shared, H]: the shared expert (NULL when
+ *   I_shared == 0). */
+typedef struct moe_weights {
+    const void *W_gate;
+    const float *bias;
+    const void *W1, *W3, *W2;
+    const void *W1s, *W3s, *W2s;
+} moe_weights_t;
+
+/* Bytes of workspace that moe_layer_forward needs for `shape`; it also suffices for every
+ * other entry point called with the same or smaller sizes.  Returns 0 for an invalid shape. */
+size_t moe_workspace_bytes(const moe_shape_t *shape);
+
+/* Static, NUL-terminated description of a moe_status_t value. */
+const char *moe_error_string(int status);
+
+/* Reads the device status word of workspace `ws` (synchronising `stream`), resets it to
+ * MOE_OK and returns what it held: MOE_OK or MOE_ERR_DEVICE_TIMEOUT; MOE_ERR_CUDA if the
+ * copy itself failed. */
+int moe_read_status(void *ws, void *stream);
+
+/* Router: gate GEMM, sigmoid scoring, selection bias, top-K, renormalised weights, fused
+ * in one kernel ("DeepSeek-V4.1-Flash", Kernels, Mega-Gate; "Lower latency and higher
+ * throughput...", MoE Router).
+ *   X      bf16 [T, H]      token activations
+ *   W_gate bf16 [E, H]
+ *   bias   fp32 [E]
+ *   out topk_idx int32 [T, K]: the K experts with the largest sel = sigmoid(X W_gate^T) +
+ *       bias, in descending sel order, equal sel -> lower index first.  The selection is
+ *       the one exact arithmetic gives: fp32 scores carry a rigorous error bound and any
+ *       token whose order the bound cannot certify is re-scored in double-word arithmetic.
+ *   out topk_w fp32 [T, K]: s_j / sum_j s_j over the selected unbiased scores s.
+ *   ws / ws_bytes: workspace (split-K partial logits, completion counters). */
+int moe_router_topk(const void *X, const void *W_gate, const float *bias,
+                    int T, int H, int E, int K,
+                    int32_t *topk_idx, float *topk_w,
+                    void *ws, size_t ws_bytes, void *stream);
+
+/* Dispatch: the single-GPU counterpart of the AllToAll Dispatch ("Lower latency and higher
+ * throughput...", Expert Parallelism; MoE Router: per-expert aggregated routing info).
+ *   X        bf16 [T, H], topk_idx int32 [T, K] (values in [0, E), distinct per token)
+ *   out counts   int32 [E]      tokens routed to each expert (the per-expert load W of
+ *                               "GRACE-MoE", Expert Replication)
+ *   out offsets  int32 [E + 1]  exclusive prefix sum of counts; offsets[E] = T*K
+ *   out perm     int32 [T*K]    token of permuted row r; rows are ordered by
+ *                               (expert ascending, token ascending) -- deterministic
+ *   out slot_pos int32 [T, K]   permuted row that holds (token t, slot j)
+ *   out Xp       bf16 [T*K, H]  Xp[r] = X[perm[r]]
+ *   out affinity int32 [E, E]   (nullable) tokens whose top-K holds both i and j, zero
+ *                               diagonal ("GRACE-MoE", Expert Grouping, matrix A)
+ *   ws / ws_bytes: workspace (per-token-group expert bit masks and counts). */
+int moe_dispatch(const void *X, const int32_t *topk_idx, int T, int H, int E, int K,
+                 int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *slot_pos,
+                 void *Xp, int32_t *affinity,
+                 void *ws, size_t ws_bytes, void *stream);
+
+/* Grouped SwiGLU expert FFN over expert-contiguous rows ("Lower latency and higher
+ * throughput...", Roofline / GroupGEMM: group i has m_i rows, [m_i, k] x [k, n];
+ * Quantization: SiLU-and-multiply activation).  For group g, rows r in
+ * [offsets[g], offsets[g+1]):
+ *     Yp[r] = ( silu(Xp[r] W1[g]) * (Xp[r] W3[g]) ) W2[g]
+ * tcgen05 tensor cores with fp32 accumulation; the activation h is rounded to bf16.
+ *   Xp      bf16 [rows, H]
+ *   offsets int32 [n_groups + 1] on the device, non-decreasing, offsets[0] = 0,
+ *           offsets[n_groups] <= rows; read by the kernels, never by the host
+ *   W1, W3  bf16 [n_groups, H, I];  W2 bf16 [n_groups, I, H]
+ *   out Yp  [rows, H], bf16 (out_fp32 == 0) or fp32 (out_fp32 == 1)
+ *   rows    upper bound of offsets[n_groups] (sizes the tensor maps and the workspace)
+ *   ws / ws_bytes: workspace (holds the bf16 activation h [rows, I]).
+ * The shared expert is the case n_groups = 1, offsets = {0, T}. */
+int moe_expert_ffn(const void *Xp, const int32_t *offsets, int n_groups, int rows,
+                   int H, int I,
+                   const void *W1, const void *W3, const void *W2,
+                   void *Yp, int out_fp32,
+                   void *ws, size_t ws_bytes, void *stream);
+
+/* Combine: the single-GPU counterpart of the AllToAll Combine ("Lower latency and higher
+ * throughput...", Expert Parallelism: weighted sum of the routed results plus the shared
+ * expert's result).
+ *     Y[t] = sum_j topk_w[t, j] * Yp[slot_pos[t, j]]  (+ Ysh[t] when Ysh != NULL)
+ *   Yp bf16 [T*K, H], slot_pos int32 [T, K], topk_w fp32 [T, K], Ysh fp32 [T, H] or NULL
+ *   out Y fp32 [T, H].  Summation order is fixed (j ascending, then Ysh). */
+int moe_combine(const void *Yp, const int32_t *slot_pos, const float *topk_w,
+                const float *Ysh, int T, int H, int K, float *Y, void *stream);
+
+/* Whole layer: router -> dispatch -> grouped expert FFN and shared expert -> combine.
+ *   X bf16 [T, H]; out Y fp32 [T, H]
+ *   out topk_idx int32 [T, K], topk_w fp32 [T, K], counts int32 [E] (required)
+ *   out affinity int32 [E, E] (nullable: skipped when NULL)
+ *   ws / ws_bytes: at least moe_workspace_bytes(shape). */
+int moe_layer_forward(const moe_shape_t *shape, const moe_weights_t *weights,
+                      const void *X, float *Y,
+                      int32_t *topk_idx, float *topk_w, int32_t *counts,
+                      int32_t *affinity,
+                      void *ws, size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */
