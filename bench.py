@@ -1,0 +1,407 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE layer forward (router -> dispatch -> grouped SwiGLU FFN + shared
+expert -> combine) on GB300, through the C ABI.
+
+Default workload: the DeepSeek-V3-shaped decode step, T = 128 tokens (64 requests x query
+length 2), H = 7168, E = 256 routed experts, top-8, I = 2048, one shared expert I = 2048,
+bf16 weights (22.5 GB of routed experts) and activations, fp32 output.  Inputs are seeded
+synthetic tensors already resident in HBM; the active experts' weights (~22 GB per step)
+are far larger than L2, so every step streams them from HBM.
+
+One JSON line on rank 0.  `--impl reference` times the fp64 CPU oracle instead (the
+reference arm), on a bounded sample of the same workload.
+Multi-GPU (torchrun): independent replicas, one per GPU, each with its own tokens; no
+collective on the data path (the timing is reduced with a max over ranks).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s on 1 GB300 (DeepSeek-V3 shape)"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+STAGES = ("router", "dispatch", "ffn_up", "ffn_down", "combine")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the GPU is busy."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        win = [p for (t, p) in self.samples if t0 <= t <= t1] or [p for (_, p) in self.samples]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in win if num(p[0]) is not None]
+        mx = [num(p[1]) for p in win if num(p[1]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for p in win for i in range(4) if p[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(win)}
+
+
+# ------------------------------------------------------------------------ accounting
+def algorithmic(w, n_act: int):
+    """Per-launch algorithmic bytes and FLOPs of each stage (what the method must move or
+    compute: the weights of the activated experts, the activations in and out)."""
+    T, H, E, K, I, Is = w.T, w.H, w.E, w.K, w.I, w.Is
+    TK = T * K
+    b = {
+        "router": E * H * 2 + T * H * 2 + T * K * 8,
+        "dispatch": T * H * 2 + TK * H * 2 + T * K * 4 * 3,
+        "ffn_up": (n_act * 2 * H * I + (2 * H * Is if Is else 0)) * 2 + (TK + T) * H * 2
+                  + (TK * I + T * Is) * 2,
+        "ffn_down": (n_act * I * H + Is * H) * 2 + (TK * I + T * Is) * 2 + TK * H * 2
+                    + (T * H * 4 if Is else 0),
+        "combine": TK * H * 2 + (T * H * 4 if Is else 0) + T * H * 4 + T * K * 8,
+    }
+    f = {
+        "router": 2 * T * E * H,
+        "dispatch": 0,
+        "ffn_up": 2 * (TK * 2 * H * I + T * 2 * H * Is),
+        "ffn_down": 2 * (TK * I * H + T * Is * H),
+        "combine": 2 * TK * H,
+    }
+    layer_bytes = (n_act + (1 if Is else 0)) * 3 * H * I * 2 + E * H * 2 + T * H * 2 + T * H * 4
+    layer_flops = 2 * T * (K * 3 * H * I + 3 * H * Is) + 2 * T * E * H
+    return b, f, layer_bytes, layer_flops
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    from expert_routed_ffn_router_gb300 import binding as B
+    from expert_routed_ffn_router_gb300 import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    B.load()
+    w = synth.workload(args.workload)
+    if rank:
+        w = synth.workload(args.workload, x_seed=w.x_seed + 7919 * rank)
+    routing = synth.routing_inputs(w)
+    weights = synth.expert_weights_device(w, dev)
+    weights["W_gate"] = torch.from_numpy(routing["W_gate"].view(np.int16)).view(torch.bfloat16).to(dev)
+    weights["bias"] = torch.from_numpy(routing["bias"]).to(dev)
+    X_host = torch.from_numpy(routing["X"].view(np.int16)).view(torch.bfloat16)
+    X = X_host.to(dev)
+    layer = B.MoELayer(weights, w.T, w.K, with_affinity=True)
+    peaks, peak_src = load_peaks()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank]))
+    sampler.start()
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        layer.forward(X)
+    torch.cuda.synchronize()
+    if layer.status() != 0:
+        raise RuntimeError("device status word reported an error during warm-up")
+
+    # ---- device-resident timed region (per-stage events recorded inside every step)
+    K = args.steps
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for evs in stage_ev:
+        for ev in evs:
+            ev.record(stream)          # materialise the handles
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for k in range(K):
+        B.moe_debug_set_stage_events(stage_ev[k])
+        layer.forward(X)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t_wall1 = time.time()
+    B.moe_debug_set_stage_events(None)
+    ms = ev0.elapsed_time(ev1) / K
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    stage_ms = {name: statistics.fmean(stage_ev[k][i].elapsed_time(stage_ev[k][i + 1])
+                                       for k in range(K))
+                for i, name in enumerate(STAGES)}
+    if layer.status() != 0:
+        raise RuntimeError("device status word reported an error in the timed region")
+
+    # ---- end to end: pinned host input -> layer -> pinned host output, every step
+    Xh = X_host.pin_memory()
+    Yh = torch.empty(w.T, w.H, dtype=torch.float32).pin_memory()
+    Xd = torch.empty_like(X)
+    for _ in range(max(1, args.warmup // 2)):
+        Xd.copy_(Xh, non_blocking=True)
+        layer.forward(Xd)
+        Yh.copy_(layer.Y, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(K):
+        Xd.copy_(Xh, non_blocking=True)
+        layer.forward(Xd)
+        Yh.copy_(layer.Y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    sampler.stop()
+    ms_e2e = e0.elapsed_time(e1) / K
+    if world > 1:
+        t = torch.tensor([ms_e2e], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+
+    counts = layer.counts.cpu().numpy()
+    n_act = int((counts > 0).sum())
+    b, f, layer_bytes, layer_flops = algorithmic(w, n_act)
+    dom = max(("ffn_up", "ffn_down", "router", "combine", "dispatch"), key=lambda s: stage_ms[s])
+    t_dom = stage_ms[dom] / 1e3
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if f[dom] / max(b[dom], 1) > ridge and dom.startswith("ffn"):
+        ach = f[dom] / t_dom / 1e12
+        roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    else:
+        ach = b[dom] / t_dom / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = None
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
+    roof["algorithmic_bytes_per_launch"] = int(b[dom])
+    roof["launch_ms"] = round(stage_ms[dom], 4)
+
+    total_tokens = w.T * world
+    value = total_tokens / (ms / 1e3)
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; random-init weights of the DeepSeek-V3 MoE shape)",
+        "config": {"workload": f"{w.name}: DeepSeek-V3-shaped MoE layer forward, T={w.T} "
+                               f"tokens, H={w.H}, E={w.E}, top-{w.K}, I={w.I}, shared I={w.Is}",
+                   "tokens_per_gpu": w.T, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: the activated experts' weights "
+                         f"({layer_bytes / 1e9:.1f} GB) stream from HBM every step",
+                   "n_active_experts": n_act},
+        "e2e": {"value": round(total_tokens / (ms_e2e / 1e3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": int(Xh.numel() * Xh.element_size()),
+                "d2h_bytes_per_step": int(Yh.numel() * Yh.element_size())},
+        "gpu_launches": K * 9,
+        "roofline": roof,
+        "layer_roofline": {"algorithmic_bytes": int(layer_bytes),
+                           "hbm_frac": round(layer_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                           "hbm_frac_of_8TBs": round(layer_bytes / (ms / 1e3) / 8e12, 4),
+                           "tensor_frac": round(layer_flops / (ms / 1e3) / 1e12 /
+                                                peaks["bf16_tflops"], 4)},
+        "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "clocks": sampler.summary(t_wall0, t_wall1),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, routing, weights, budget_s=args.cpu_budget)
+    return out
+
+
+# --------------------------------------------------------------------- oracle (CPU)
+def _oracle_step(w, routing, weights, tokens, host_cache):
+    """One oracle pass over `tokens`: router for those tokens + their experts + shared."""
+    import numpy as np
+
+    import oracle
+    from expert_routed_ffn_router_gb300 import synth
+    X = routing["X"][tokens]
+    idx, wt = oracle.router(X, routing["W_gate"], routing["bias"], w.K)
+    used = sorted({int(e) for e in idx.ravel()})
+    for e in used:
+        if e not in host_cache:
+            host_cache[e] = tuple(synth.bf16_tensor_to_bits(weights[n][e]) for n in ("W1", "W3", "W2"))
+    if "shared" not in host_cache and w.Is:
+        host_cache["shared"] = tuple(synth.bf16_tensor_to_bits(weights[n]) for n in ("W1s", "W3s", "W2s"))
+    return X, idx, wt, used
+
+
+def _oracle_timed(w, routing, weights, tokens, host_cache):
+    import numpy as np
+
+    import oracle
+    X, idx, wt, used = _oracle_step(w, routing, weights, tokens, host_cache)
+    t0 = time.perf_counter()
+    idx, wt = oracle.router(X, routing["W_gate"], routing["bias"], w.K)
+    sh = host_cache.get("shared", (None, None, None))
+    oracle.layer_tokens(X, idx, wt, {e: host_cache[e][0] for e in used},
+                        {e: host_cache[e][1] for e in used}, {e: host_cache[e][2] for e in used},
+                        *sh, np.arange(len(tokens)), w.I, w.Is)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, routing, weights, budget_s=12.0):
+    import numpy as np
+
+    import oracle
+    cores = oracle.num_threads()
+    cache = {}
+    n1 = cores
+    t1 = _oracle_timed(w, routing, weights, np.arange(n1) % w.T, cache)
+    per_tok = t1 / n1
+    n = int(min(w.T, max(n1, round(budget_s / max(per_tok, 1e-6)))))
+    tokens = np.arange(n) % w.T
+    t = _oracle_timed(w, routing, weights, tokens, cache)
+    return {"value": round(n / t, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"first {n} of the {w.T} tokens of the workload: fp64 router over all "
+                      f"{w.E} experts + the {w.K} routed experts and the shared expert of each "
+                      f"token ({t:.1f} s)"}
+
+
+def run_reference(args):
+    import numpy as np
+    import torch
+
+    import oracle
+    from expert_routed_ffn_router_gb300 import synth
+    w = synth.workload(args.workload)
+    routing = synth.routing_inputs(w)
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    weights = synth.expert_weights_device(w, dev)
+    cores = oracle.num_threads()
+    cache = {}
+    # size each step so that warm-up + timed steps take about two minutes
+    t1 = _oracle_timed(w, routing, weights, np.arange(cores) % w.T, cache)
+    per_tok = t1 / cores
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(w.T, round(budget / max(per_tok, 1e-6)))))
+    rng = np.random.default_rng(0)
+    steps_tok = [rng.choice(w.T, size=n, replace=False) for _ in range(args.warmup + args.steps)]
+    for k in range(args.warmup):
+        _oracle_timed(w, routing, weights, steps_tok[k], cache)
+    tt = 0.0
+    for k in range(args.steps):
+        tt += _oracle_timed(w, routing, weights, steps_tok[args.warmup + k], cache)
+    value = n * args.steps / tt
+    return {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tt / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "impl": "reference",
+        "config": {"workload": f"{w.name}: DeepSeek-V3-shaped MoE layer forward, T={w.T}"},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{n} random tokens of the {w.T}-token workload per step"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="decode",
+                    help="decode (default), tiny, sweep2..sweep256, prefill, skewed")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group("nccl")
+    out = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,195 @@
+"""Thin ctypes binding of the C ABI in include/moe.h.
+
+Argument marshalling only: torch tensors supply device pointers (``data_ptr()``) and the
+current CUDA stream; every step of the layer runs in the library's CUDA kernels.  The
+functions carry the C names.  A missing or unbuildable library raises -- there is no
+fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+MOE_OK = 0
+MOE_ERR_DEVICE_TIMEOUT = -6
+
+_lib = None
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status} ({moe_error_string(status)})")
+        self.status = status
+
+
+class MoeShape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("T", "H", "E", "K", "I", "I_shared")]
+
+
+class MoeWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("W_gate", "bias", "W1", "W3", "W2", "W1s",
+                                               "W3s", "W2s")]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libmoe_gb300.so (building it first when it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.build() if build_if_missing else _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library {path} is missing; run the package build first")
+    lib = ctypes.CDLL(path)
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    sig = {
+        "moe_workspace_bytes": ([ctypes.POINTER(MoeShape)], Z),
+        "moe_error_string": ([I], ctypes.c_char_p),
+        "moe_read_status": ([P, P], I),
+        "moe_debug_set_wait_limit": ([ctypes.c_ulonglong, I], None),
+        "moe_debug_set_stage_events": ([P, I], None),
+        "moe_router_topk": ([P, P, P, I, I, I, I, P, P, P, Z, P], I),
+        "moe_dispatch": ([P, P, I, I, I, I, P, P, P, P, P, P, P, Z, P], I),
+        "moe_expert_ffn": ([P, P, I, I, I, I, P, P, P, P, I, P, Z, P], I),
+        "moe_combine": ([P, P, P, P, I, I, I, P, P], I),
+        "moe_layer_forward": ([ctypes.POINTER(MoeShape), ctypes.POINTER(MoeWeights), P, P, P,
+                               P, P, P, P, Z, P], I),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("device tensors are required")
+    if not t.is_contiguous():
+        raise ValueError("contiguous tensors are required")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn, rc):
+    if rc != MOE_OK:
+        raise MoeError(fn, rc)
+
+
+# ------------------------------------------------------------------------- C entry points
+def moe_error_string(status: int) -> str:
+    return load().moe_error_string(int(status)).decode()
+
+
+def moe_workspace_bytes(T, H, E, K, I, I_shared) -> int:
+    s = MoeShape(T, H, E, K, I, I_shared)
+    return int(load().moe_workspace_bytes(ctypes.byref(s)))
+
+
+def moe_read_status(ws, stream=None) -> int:
+    return int(load().moe_read_status(_ptr(ws), _stream(stream)))
+
+
+def moe_debug_set_wait_limit(limit_ns: int, inject_stall: int = 0) -> None:
+    load().moe_debug_set_wait_limit(int(limit_ns), int(inject_stall))
+
+
+def moe_debug_set_stage_events(events) -> None:
+    """events: list of >= 6 recorded torch.cuda.Event (timing enabled), or None."""
+    if events is None:
+        load().moe_debug_set_stage_events(None, 0)
+        return
+    arr = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
+    load().moe_debug_set_stage_events(ctypes.cast(arr, ctypes.c_void_p), len(events))
+
+
+def moe_router_topk(X, W_gate, bias, K, topk_idx, topk_w, ws, stream=None):
+    T, H = X.shape
+    E = W_gate.shape[0]
+    _check("moe_router_topk", load().moe_router_topk(
+        _ptr(X), _ptr(W_gate), _ptr(bias), T, H, E, int(K), _ptr(topk_idx), _ptr(topk_w),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_dispatch(X, topk_idx, E, counts, offsets, perm, slot_pos, Xp, affinity, ws,
+                 stream=None):
+    T, H = X.shape
+    K = topk_idx.shape[1]
+    _check("moe_dispatch", load().moe_dispatch(
+        _ptr(X), _ptr(topk_idx), T, H, int(E), K, _ptr(counts), _ptr(offsets), _ptr(perm),
+        _ptr(slot_pos), _ptr(Xp), _ptr(affinity), _ptr(ws), ws.numel() * ws.element_size(),
+        _stream(stream)))
+
+
+def moe_expert_ffn(Xp, offsets, n_groups, W1, W3, W2, Yp, ws, stream=None):
+    rows, H = Xp.shape
+    I = W1.shape[-1]
+    out_fp32 = 1 if Yp.dtype == torch.float32 else 0
+    _check("moe_expert_ffn", load().moe_expert_ffn(
+        _ptr(Xp), _ptr(offsets), int(n_groups), rows, H, I, _ptr(W1), _ptr(W3), _ptr(W2),
+        _ptr(Yp), out_fp32, _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_combine(Yp, slot_pos, topk_w, Ysh, Y, stream=None):
+    T, K = slot_pos.shape
+    H = Y.shape[1]
+    _check("moe_combine", load().moe_combine(
+        _ptr(Yp), _ptr(slot_pos), _ptr(topk_w), _ptr(Ysh), T, H, K, _ptr(Y), _stream(stream)))
+
+
+def moe_layer_forward(shape: MoeShape, weights: dict, X, Y, topk_idx, topk_w, counts,
+                      affinity, ws, stream=None):
+    w = MoeWeights(*[None if weights.get(n) is None else weights[n].data_ptr()
+                     for n in ("W_gate", "bias", "W1", "W3", "W2", "W1s", "W3s", "W2s")])
+    _check("moe_layer_forward", load().moe_layer_forward(
+        ctypes.byref(shape), ctypes.byref(w), _ptr(X), _ptr(Y), _ptr(topk_idx), _ptr(topk_w),
+        _ptr(counts), _ptr(affinity), _ptr(ws), ws.numel() * ws.element_size(),
+        _stream(stream)))
+
+
+# ------------------------------------------------------------------- convenience wrapper
+class MoELayer:
+    """Holds a layer's weights, outputs and workspace (torch allocations) and runs
+    moe_layer_forward.  weights: dict of device tensors W_gate, bias, W1, W3, W2 and
+    (optionally) W1s, W3s, W2s."""
+
+    def __init__(self, weights: dict, T: int, K: int, with_affinity: bool = True):
+        self.w = weights
+        E, H = weights["W_gate"].shape
+        I = weights["W1"].shape[-1]
+        Is = 0 if weights.get("W1s") is None else weights["W1s"].shape[-1]
+        self.shape = MoeShape(T, H, E, K, I, Is)
+        dev = weights["W_gate"].device
+        self.Y = torch.empty(T, H, dtype=torch.float32, device=dev)
+        self.topk_idx = torch.empty(T, K, dtype=torch.int32, device=dev)
+        self.topk_w = torch.empty(T, K, dtype=torch.float32, device=dev)
+        self.counts = torch.empty(E, dtype=torch.int32, device=dev)
+        self.affinity = (torch.empty(E, E, dtype=torch.int32, device=dev)
+                         if with_affinity else None)
+        nbytes = moe_workspace_bytes(T, H, E, K, I, Is)
+        if nbytes == 0:
+            raise MoeError("moe_workspace_bytes", -2)
+        self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+
+    def forward(self, X, stream=None):
+        moe_layer_forward(self.shape, self.w, X, self.Y, self.topk_idx, self.topk_w,
+                          self.counts, self.affinity, self.ws, stream)
+        return self.Y
+
+    def status(self, stream=None) -> int:
+        return moe_read_status(self.ws, stream)

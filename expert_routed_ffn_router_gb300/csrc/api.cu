@@ -1,0 +1,356 @@
+// api.cu -- the C ABI of include/moe.h: argument validation, workspace layout and the
+// kernel sequence of each entry point.  Everything is enqueued on the caller's stream;
+// nothing here allocates, frees or synchronises (moe_read_status excepted).
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/moe.h"
+#include "kernels.h"
+
+namespace moe {
+
+int num_sms()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+cudaError_t ensure_smem(const void *func, size_t bytes)
+{
+    // small table of (function, device) -> largest limit set so far
+    struct Entry { const void *f; int dev; size_t bytes; };
+    static Entry tab[64];
+    static int n = 0;
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    for (int i = 0; i < n; ++i)
+        if (tab[i].f == func && tab[i].dev == dev && tab[i].bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(bytes));
+    if (e != cudaSuccess) return e;
+    for (int i = 0; i < n; ++i)
+        if (tab[i].f == func && tab[i].dev == dev) { tab[i].bytes = bytes; return cudaSuccess; }
+    if (n < 64) tab[n++] = Entry{func, dev, bytes};
+    return cudaSuccess;
+}
+
+namespace {
+
+constexpr size_t kHeader = 256;   // status word + reserved
+unsigned long long g_wait_limit_ns = 1000000000ull;
+int g_inject_stall = 0;
+cudaEvent_t g_stage_events[6] = {};
+bool g_stage_events_on = false;
+
+void record_stage(int i, cudaStream_t s)
+{
+    if (g_stage_events_on && g_stage_events[i]) cudaEventRecord(g_stage_events[i], s);
+}
+
+size_t al256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_common(int T, int H, int E, int K)
+{
+    if (T < 0 || H <= 0 || E <= 0 || K <= 0 || K > E) return MOE_ERR_INVALID_ARG;
+    if (E > 1024 || K > 32 || H % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (static_cast<long long>(T) * K >= (1ll << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    return MOE_OK;
+}
+
+int check_ptrs(std::initializer_list<const void *> ps)
+{
+    for (const void *p : ps) {
+        if (!p) return MOE_ERR_INVALID_ARG;
+        if (!aligned(p, 16)) return MOE_ERR_MISALIGNED;
+    }
+    return MOE_OK;
+}
+
+int check_opt(const void *p) { return (p && !aligned(p, 16)) ? MOE_ERR_MISALIGNED : MOE_OK; }
+
+int check_ws(const void *ws, size_t have, size_t need)
+{
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    if (!aligned(ws, 256)) return MOE_ERR_MISALIGNED;
+    if (have < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    return MOE_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+struct RouterLayout {
+    RouterPlan plan;
+    RouterScratch scr;
+    size_t bytes;
+};
+RouterLayout router_layout(int T, int H, int E, unsigned char *base)
+{
+    RouterLayout L{};
+    L.plan = router_plan(T, H, E);
+    size_t o = 0;
+    L.scr.part = reinterpret_cast<float *>(base + o); o += L.plan.part_bytes;
+    L.scr.xsq = reinterpret_cast<float *>(base + o); o += L.plan.xsq_bytes;
+    L.scr.wsq = reinterpret_cast<float *>(base + o); o += L.plan.wsq_bytes;
+    L.scr.cnt = reinterpret_cast<unsigned *>(base + o); o += L.plan.cnt_bytes;
+    L.bytes = o;
+    return L;
+}
+
+struct DispatchLayout {
+    DispatchPlan plan;
+    DispatchScratch scr;
+    size_t bytes;
+};
+DispatchLayout dispatch_layout(int T, int E, unsigned char *base)
+{
+    DispatchLayout L{};
+    L.plan = dispatch_plan(T, E);
+    size_t o = 0;
+    L.scr.smask = reinterpret_cast<uint32_t *>(base + o); o += L.plan.smask_bytes;
+    L.scr.chunk_cnt = reinterpret_cast<int32_t *>(base + o); o += L.plan.ccnt_bytes;
+    L.scr.chunk_base = reinterpret_cast<int32_t *>(base + o); o += L.plan.cbase_bytes;
+    L.bytes = o;
+    return L;
+}
+
+struct LayerLayout {
+    RouterLayout r;
+    DispatchLayout d;
+    int32_t *offsets, *perm, *slot_pos;
+    void *Xp, *h, *Yp, *hs;
+    float *Ysh;
+    size_t bytes;
+};
+LayerLayout layer_layout(const moe_shape_t &s, unsigned char *ws)
+{
+    LayerLayout L{};
+    const size_t TK = static_cast<size_t>(s.T) * s.K;
+    size_t o = kHeader;
+    L.r = router_layout(s.T, s.H, s.E, ws ? ws + o : nullptr); o += L.r.bytes;
+    L.d = dispatch_layout(s.T, s.E, ws ? ws + o : nullptr); o += L.d.bytes;
+    auto take = [&](size_t b) { unsigned char *p = ws ? ws + o : nullptr; o += al256(b); return p; };
+    L.offsets = reinterpret_cast<int32_t *>(take((s.E + 1) * sizeof(int32_t)));
+    L.perm = reinterpret_cast<int32_t *>(take(TK * sizeof(int32_t)));
+    L.slot_pos = reinterpret_cast<int32_t *>(take(TK * sizeof(int32_t)));
+    L.Xp = take(TK * s.H * 2);
+    L.h = take(TK * s.I * 2);
+    L.Yp = take(TK * s.H * 2);
+    L.hs = take(static_cast<size_t>(s.T) * s.I_shared * 2);
+    L.Ysh = reinterpret_cast<float *>(take(s.I_shared > 0 ? static_cast<size_t>(s.T) * s.H * 4 : 0));
+    L.bytes = o;
+    return L;
+}
+
+int check_shape(const moe_shape_t *s)
+{
+    if (!s) return MOE_ERR_INVALID_ARG;
+    int rc = check_common(s->T, s->H, s->E, s->K);
+    if (rc) return rc;
+    if (s->I <= 0 || s->I_shared < 0) return MOE_ERR_INVALID_ARG;
+    if (s->I % 64 != 0 || s->I_shared % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_shape_t *shape)
+{
+    if (check_shape(shape) != MOE_OK) return 0;
+    return layer_layout(*shape, nullptr).bytes;
+}
+
+const char *moe_error_string(int status)
+{
+    switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_MISALIGNED: return "misaligned pointer";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "bounded device-side wait ran out";
+    case MOE_ERR_NOT_IMPLEMENTED: return "not implemented";
+    default: return "unknown status";
+    }
+}
+
+int moe_read_status(void *ws, void *stream)
+{
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(ws, 0, sizeof v, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return v;
+}
+
+void moe_debug_set_wait_limit(unsigned long long limit_ns, int inject_stall)
+{
+    g_wait_limit_ns = limit_ns ? limit_ns : 1000000000ull;
+    g_inject_stall = inject_stall;
+}
+
+void moe_debug_set_stage_events(void *const *events, int n)
+{
+    g_stage_events_on = events != nullptr && n >= 6;
+    for (int i = 0; i < 6; ++i)
+        g_stage_events[i] = g_stage_events_on ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+}
+
+int moe_router_topk(const void *X, const void *W_gate, const float *bias, int T, int H, int E,
+                    int K, int32_t *topk_idx, float *topk_w, void *ws, size_t ws_bytes,
+                    void *stream)
+{
+    int rc = check_common(T, H, E, K);
+    if (rc) return rc;
+    if ((rc = check_ptrs({X, W_gate, bias, topk_idx, topk_w}))) return rc;
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    const RouterLayout L = router_layout(T, H, E, w ? w + kHeader : nullptr);
+    if ((rc = check_ws(ws, ws_bytes, kHeader + L.bytes))) return rc;
+    if (T == 0) return MOE_OK;
+    return cuda_status(launch_router(X, W_gate, bias, T, H, E, K, topk_idx, topk_w, L.plan,
+                                     L.scr, static_cast<int *>(ws),
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+int moe_dispatch(const void *X, const int32_t *topk_idx, int T, int H, int E, int K,
+                 int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *slot_pos, void *Xp,
+                 int32_t *affinity, void *ws, size_t ws_bytes, void *stream)
+{
+    int rc = check_common(T, H, E, K);
+    if (rc) return rc;
+    if ((rc = check_ptrs({X, topk_idx, counts, offsets, perm, slot_pos, Xp}))) return rc;
+    if ((rc = check_opt(affinity))) return rc;
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    const DispatchLayout L = dispatch_layout(T, E, w ? w + kHeader : nullptr);
+    if ((rc = check_ws(ws, ws_bytes, kHeader + L.bytes))) return rc;
+    if (T == 0) return MOE_OK;
+    return cuda_status(launch_dispatch(X, topk_idx, T, H, E, K, counts, offsets, perm, slot_pos,
+                                       Xp, affinity, L.plan, L.scr, static_cast<int *>(ws),
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+int moe_expert_ffn(const void *Xp, const int32_t *offsets, int n_groups, int rows, int H, int I,
+                   const void *W1, const void *W3, const void *W2, void *Yp, int out_fp32,
+                   void *ws, size_t ws_bytes, void *stream)
+{
+    if (n_groups <= 0 || rows < 0 || H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+    if (n_groups > 1024 || H % 64 != 0 || I % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (out_fp32 != 0 && out_fp32 != 1) return MOE_ERR_INVALID_ARG;
+    int rc = check_ptrs({Xp, offsets, W1, W3, W2, Yp});
+    if (rc) return rc;
+    const size_t hbytes = al256(static_cast<size_t>(rows) * I * 2);
+    if ((rc = check_ws(ws, ws_bytes, kHeader + hbytes))) return rc;
+    if (rows == 0) return MOE_OK;
+    FfnProblem P{};
+    P.act = Xp;
+    P.offsets = offsets;
+    P.n_groups = n_groups;
+    P.rows = rows;
+    P.W1 = W1; P.W3 = W3; P.W2 = W2;
+    P.h = static_cast<unsigned char *>(ws) + kHeader;
+    P.out = Yp;
+    P.out_fp32 = out_fp32;
+    const int hint = rows / n_groups > 0 ? rows / n_groups : 1;
+    return cuda_status(launch_ffn(&P, 1, H, &I, hint, static_cast<int *>(ws),
+                                  static_cast<cudaStream_t>(stream), g_wait_limit_ns,
+                                  g_inject_stall, nullptr));
+}
+
+int moe_combine(const void *Yp, const int32_t *slot_pos, const float *topk_w, const float *Ysh,
+                int T, int H, int K, float *Y, void *stream)
+{
+    if (T < 0 || H <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+    if (H % 64 != 0 || K > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+    int rc = check_ptrs({Yp, slot_pos, topk_w, Y});
+    if (rc) return rc;
+    if ((rc = check_opt(Ysh))) return rc;
+    if (T == 0) return MOE_OK;
+    return cuda_status(launch_combine(Yp, slot_pos, topk_w, Ysh, T, H, K, Y,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int moe_layer_forward(const moe_shape_t *shape, const moe_weights_t *wt, const void *X, float *Y,
+                      int32_t *topk_idx, float *topk_w, int32_t *counts, int32_t *affinity,
+                      void *ws, size_t ws_bytes, void *stream)
+{
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if (!wt) return MOE_ERR_INVALID_ARG;
+    const moe_shape_t s = *shape;
+    if ((rc = check_ptrs({X, Y, topk_idx, topk_w, counts, wt->W_gate, wt->bias, wt->W1, wt->W3,
+                          wt->W2})))
+        return rc;
+    if (s.I_shared > 0 && (rc = check_ptrs({wt->W1s, wt->W3s, wt->W2s}))) return rc;
+    if ((rc = check_opt(affinity))) return rc;
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    const LayerLayout L = layer_layout(s, w);
+    if ((rc = check_ws(ws, ws_bytes, L.bytes))) return rc;
+    if (s.T == 0) return MOE_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int *status = static_cast<int *>(ws);
+
+    record_stage(0, st);
+    cudaError_t e = launch_router(X, wt->W_gate, wt->bias, s.T, s.H, s.E, s.K, topk_idx, topk_w,
+                                  L.r.plan, L.r.scr, status, st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    record_stage(1, st);
+    e = launch_dispatch(X, topk_idx, s.T, s.H, s.E, s.K, counts, L.offsets, L.perm, L.slot_pos,
+                        L.Xp, affinity, L.d.plan, L.d.scr, status, st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    record_stage(2, st);
+
+    FfnProblem P[2]{};
+    int Ipp[2] = {s.I, s.I_shared};
+    P[0].act = L.Xp;
+    P[0].offsets = L.offsets;
+    P[0].n_groups = s.E;
+    P[0].rows = s.T * s.K;
+    P[0].W1 = wt->W1; P[0].W3 = wt->W3; P[0].W2 = wt->W2;
+    P[0].h = L.h;
+    P[0].out = L.Yp;
+    P[0].out_fp32 = 0;
+    int n_probs = 1;
+    if (s.I_shared > 0) {
+        P[1].act = X;
+        P[1].offsets = nullptr;
+        P[1].n_groups = 1;
+        P[1].rows = s.T;
+        P[1].dense_rows = s.T;
+        P[1].W1 = wt->W1s; P[1].W3 = wt->W3s; P[1].W2 = wt->W2s;
+        P[1].h = L.hs;
+        P[1].out = L.Ysh;
+        P[1].out_fp32 = 1;
+        n_probs = 2;
+    }
+    long long hint = static_cast<long long>(s.T) * s.K / s.E;
+    if (hint < 1) hint = 1;
+    e = launch_ffn(P, n_probs, s.H, Ipp, static_cast<int>(hint), status, st, g_wait_limit_ns,
+                   g_inject_stall, g_stage_events_on ? g_stage_events[3] : nullptr);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    record_stage(4, st);
+    e = launch_combine(L.Yp, L.slot_pos, topk_w, s.I_shared > 0 ? L.Ysh : nullptr, s.T, s.H,
+                       s.K, Y, st);
+    record_stage(5, st);
+    return cuda_status(e);
+}
+
+}  // extern "C"

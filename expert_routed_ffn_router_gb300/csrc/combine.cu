@@ -1,0 +1,71 @@
+// combine.cu -- the single-GPU counterpart of the AllToAll Combine: the weighted sum of a
+// token's routed expert outputs plus the shared expert's output.
+//
+// Method: "Lower latency and higher throughput with multi-node DeepSeek deployment",
+// section "Expert Parallelism": the results of a token's 8 routed experts are summed with
+// their routing weights, and the shared expert's result is added.
+//
+//   Y[t, :] = sum_{j<K} topk_w[t, j] * Yp[slot_pos[t, j], :]  (+ Ysh[t, :])
+//
+// One CTA of 128 threads covers 1024 columns of one token; each thread owns 8 consecutive
+// columns (a 16-byte bf16 vector of every routed row, two float4 of Ysh and Y).  The order
+// of the additions is fixed (j ascending, then Ysh), so Y is bitwise reproducible.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int CT = 128;          // threads per CTA
+constexpr int COLS = CT * 8;     // columns per CTA
+
+__global__ void __launch_bounds__(CT) combine_kernel(const uint4 *__restrict__ Yp,
+                                                     const int32_t *__restrict__ slot_pos,
+                                                     const float *__restrict__ topk_w,
+                                                     const float4 *__restrict__ Ysh, int H,
+                                                     int K, float4 *__restrict__ Y)
+{
+    const int t = blockIdx.x;
+    const int c = blockIdx.y * COLS + threadIdx.x * 8;
+    if (c >= H) return;
+    const int vec = H / 8;
+    const int cv = c / 8;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int j = 0; j < K; ++j) {
+        const int r = __ldg(slot_pos + static_cast<size_t>(t) * K + j);
+        const float w = __ldg(topk_w + static_cast<size_t>(t) * K + j);
+        const uint4 v = __ldg(Yp + static_cast<size_t>(r) * vec + cv);
+        acc[0] = fmaf(w, bf16_lo(v.x), acc[0]);
+        acc[1] = fmaf(w, bf16_hi(v.x), acc[1]);
+        acc[2] = fmaf(w, bf16_lo(v.y), acc[2]);
+        acc[3] = fmaf(w, bf16_hi(v.y), acc[3]);
+        acc[4] = fmaf(w, bf16_lo(v.z), acc[4]);
+        acc[5] = fmaf(w, bf16_hi(v.z), acc[5]);
+        acc[6] = fmaf(w, bf16_lo(v.w), acc[6]);
+        acc[7] = fmaf(w, bf16_hi(v.w), acc[7]);
+    }
+    const size_t o = (static_cast<size_t>(t) * H + c) / 4;
+    if (Ysh) {
+        const float4 s0 = __ldg(Ysh + o), s1 = __ldg(Ysh + o + 1);
+        acc[0] += s0.x; acc[1] += s0.y; acc[2] += s0.z; acc[3] += s0.w;
+        acc[4] += s1.x; acc[5] += s1.y; acc[6] += s1.z; acc[7] += s1.w;
+    }
+    Y[o] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    Y[o + 1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const void *Yp, const int32_t *slot_pos, const float *topk_w,
+                           const float *Ysh, int T, int H, int K, float *Y, cudaStream_t s)
+{
+    dim3 grid(T, (H + COLS - 1) / COLS);
+    combine_kernel<<<grid, CT, 0, s>>>(static_cast<const uint4 *>(Yp), slot_pos, topk_w,
+                                       reinterpret_cast<const float4 *>(Ysh), H, K,
+                                       reinterpret_cast<float4 *>(Y));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,244 @@
+// dispatch.cu -- the single-GPU counterpart of the AllToAll Dispatch: per-expert counts,
+// exclusive scan, a deterministic stable permutation of the (token, slot) pairs into
+// expert-contiguous rows, the row gather, and the expert co-activation (affinity) matrix.
+//
+// Method: "Lower latency and higher throughput with multi-node DeepSeek deployment",
+// section "Expert Parallelism" (tokens are sent to the GPUs of their experts before the
+// expert computation) and section "MoE Router" (a dense dispatch/combine needs routing
+// information aggregated per expert, not per token).  The affinity matrix is the expert
+// co-activation matrix A of "GRACE-MoE", Core Idea 1 (Expert Grouping).
+//
+// Representation: the 0/1 selection matrix S[T, E] is stored as 32-token bit masks,
+// smask[w][e] = bit l set iff token 32w + l chose expert e.  Every quantity is a popcount of
+// these words, so nothing depends on the order in which atomics land:
+//   counts[e]         = sum_w popc(smask[w][e])
+//   rank of token t   = #{t' < t : t' chose e}  (prefix popcount -> stable order)
+//   affinity[i][j]    = sum_w popc(smask[w][i] & smask[w][j]),  i != j
+// The masks of a warp are built with warp-aggregated shared-memory atomics
+// (__match_any_sync groups the lanes that picked the same expert).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int CHUNK = 256;            // tokens per chunk (8 warps x 32)
+constexpr int CW = CHUNK / 32;        // mask rows per chunk
+
+__global__ void __launch_bounds__(CHUNK) masks_kernel(const int32_t *__restrict__ idx, int T,
+                                                      int E, int K, uint32_t *smask,
+                                                      int32_t *chunk_cnt, int *status)
+{
+    extern __shared__ uint32_t m_s[];    // [CW][E]
+    const int c = blockIdx.x, tid = threadIdx.x;
+    const int w = tid >> 5, lane = tid & 31;
+    for (int i = tid; i < CW * E; i += CHUNK) m_s[i] = 0u;
+    __syncthreads();
+    const int t = c * CHUNK + tid;
+    const bool valid = t < T;
+    for (int j = 0; j < K; ++j) {
+        int e = valid ? idx[static_cast<size_t>(t) * K + j] : -1;
+        if (valid && (e < 0 || e >= E)) {
+            report(status, MOE_ERR_INVALID_ARG);
+            e = -1;
+        }
+        const uint32_t peers = __match_any_sync(kFullMask, e);
+        if (e >= 0 && lane == __ffs(peers) - 1) atomicOr(&m_s[w * E + e], peers);
+    }
+    __syncthreads();
+    const int rows = min(CW, (T - c * CHUNK + 31) / 32);
+    for (int i = tid; i < rows * E; i += CHUNK)
+        smask[static_cast<size_t>(c * CW) * E + i] = m_s[i];
+    for (int e = tid; e < E; e += CHUNK) {
+        int n = 0;
+        for (int r = 0; r < CW; ++r) n += __popc(m_s[r * E + e]);
+        chunk_cnt[static_cast<size_t>(c) * E + e] = n;
+    }
+}
+
+// One CTA: per-expert totals, exclusive scan over experts, per-chunk bases.
+__global__ void __launch_bounds__(1024) scan_kernel(int E, int n_chunks,
+                                                    const int32_t *chunk_cnt,
+                                                    int32_t *chunk_base, int32_t *counts,
+                                                    int32_t *offsets)
+{
+    __shared__ int warp_sums[32];
+    const int e = threadIdx.x, lane = e & 31, w = e >> 5;
+    int total = 0;
+    if (e < E)
+        for (int c = 0; c < n_chunks; ++c) {
+            const int n = chunk_cnt[static_cast<size_t>(c) * E + e];
+            chunk_base[static_cast<size_t>(c) * E + e] = total;
+            total += n;
+        }
+    // block-wide exclusive scan of `total` over experts
+    int incl = total;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(kFullMask, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) warp_sums[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+        int v = lane < blockDim.x / 32 ? warp_sums[lane] : 0;
+        int inc = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(kFullMask, inc, off);
+            if (lane >= off) inc += u;
+        }
+        warp_sums[lane] = inc - v;
+    }
+    __syncthreads();
+    const int excl = warp_sums[w] + incl - total;
+    if (e < E) {
+        counts[e] = total;
+        offsets[e] = excl;
+        for (int c = 0; c < n_chunks; ++c) chunk_base[static_cast<size_t>(c) * E + e] += excl;
+    }
+    if (e == E - 1) offsets[E] = excl + total;
+}
+
+__global__ void __launch_bounds__(CHUNK) scatter_kernel(const int32_t *__restrict__ idx, int T,
+                                                        int E, int K, const uint32_t *smask,
+                                                        const int32_t *chunk_base, int32_t *perm,
+                                                        int32_t *slot_pos)
+{
+    extern __shared__ uint32_t sh[];
+    uint32_t *m_s = sh;                                  // [CW][E]
+    int32_t *base = reinterpret_cast<int32_t *>(sh + CW * E);  // [CW][E]
+    const int c = blockIdx.x, tid = threadIdx.x;
+    const int w = tid >> 5, lane = tid & 31;
+    const int rows = min(CW, (T - c * CHUNK + 31) / 32);
+    for (int i = tid; i < CW * E; i += CHUNK)
+        m_s[i] = i < rows * E ? smask[static_cast<size_t>(c * CW) * E + i] : 0u;
+    __syncthreads();
+    for (int e = tid; e < E; e += CHUNK) {
+        int run = chunk_base[static_cast<size_t>(c) * E + e];
+        for (int r = 0; r < CW; ++r) {
+            base[r * E + e] = run;
+            run += __popc(m_s[r * E + e]);
+        }
+    }
+    __syncthreads();
+    const int t = c * CHUNK + tid;
+    if (t >= T) return;
+    const uint32_t below = (1u << lane) - 1u;
+    for (int j = 0; j < K; ++j) {
+        const int e = idx[static_cast<size_t>(t) * K + j];
+        if (e < 0 || e >= E) continue;   // reported by masks_kernel
+        const int r = base[w * E + e] + __popc(m_s[w * E + e] & below);
+        slot_pos[static_cast<size_t>(t) * K + j] = r;
+        perm[r] = t;
+    }
+}
+
+// Xp[r] = X[perm[r]] for r < offsets[E]; one warp per row, 16-byte vectors.
+__global__ void __launch_bounds__(256) gather_kernel(const uint4 *__restrict__ X, int H,
+                                                     const int32_t *__restrict__ perm,
+                                                     const int32_t *__restrict__ offsets,
+                                                     int E, uint4 *__restrict__ Xp)
+{
+    const int n_rows = offsets[E];
+    const int vec = H / 8;
+    const int lane = threadIdx.x & 31;
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int nw = (gridDim.x * blockDim.x) >> 5;
+    for (int r = gw; r < n_rows; r += nw) {
+        const uint4 *src = X + static_cast<size_t>(perm[r]) * vec;
+        uint4 *dst = Xp + static_cast<size_t>(r) * vec;
+        int v = lane;
+        for (; v + 96 < vec; v += 128) {
+            const uint4 a0 = __ldg(src + v), a1 = __ldg(src + v + 32);
+            const uint4 a2 = __ldg(src + v + 64), a3 = __ldg(src + v + 96);
+            dst[v] = a0; dst[v + 32] = a1; dst[v + 64] = a2; dst[v + 96] = a3;
+        }
+        for (; v < vec; v += 32) dst[v] = __ldg(src + v);
+    }
+}
+
+// affinity[i][j] = sum_w popc(smask[w][i] & smask[w][j]) for i != j, 0 on the diagonal.
+__global__ void __launch_bounds__(256) affinity_kernel(const uint32_t *__restrict__ smask,
+                                                       int n_words, int E, int32_t *aff)
+{
+    __shared__ uint32_t A[64][33];
+    __shared__ uint32_t B[64][33];
+    const int i0 = blockIdx.y * 32, j0 = blockIdx.x * 32;
+    const int tid = threadIdx.x;
+    const int ti = tid >> 3, tj = (tid & 7) * 4;
+    int acc[4] = {0, 0, 0, 0};
+    for (int w0 = 0; w0 < n_words; w0 += 64) {
+        for (int q = tid; q < 64 * 32; q += 256) {
+            const int r = q >> 5, col = q & 31;
+            const int w = w0 + r;
+            const bool ok = w < n_words;
+            A[r][col] = (ok && i0 + col < E) ? smask[static_cast<size_t>(w) * E + i0 + col] : 0u;
+            B[r][col] = (ok && j0 + col < E) ? smask[static_cast<size_t>(w) * E + j0 + col] : 0u;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int r = 0; r < 64; ++r) {
+            const uint32_t a = A[r][ti];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[q] += __popc(a & B[r][tj + q]);
+        }
+        __syncthreads();
+    }
+    const int i = i0 + ti;
+    if (i >= E) return;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int j = j0 + tj + q;
+        if (j < E) aff[static_cast<size_t>(i) * E + j] = (i == j) ? 0 : acc[q];
+    }
+}
+
+}  // namespace
+
+DispatchPlan dispatch_plan(int T, int E)
+{
+    DispatchPlan p{};
+    p.n_chunks = (T + CHUNK - 1) / CHUNK;
+    p.n_words = (T + 31) / 32;
+    auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
+    p.smask_bytes = al(static_cast<size_t>(p.n_chunks) * CW * E * sizeof(uint32_t));
+    p.ccnt_bytes = al(static_cast<size_t>(p.n_chunks) * E * sizeof(int32_t));
+    p.cbase_bytes = al(static_cast<size_t>(p.n_chunks) * E * sizeof(int32_t));
+    return p;
+}
+
+cudaError_t launch_dispatch(const void *X, const int32_t *topk_idx, int T, int H, int E,
+                            int K, int32_t *counts, int32_t *offsets, int32_t *perm,
+                            int32_t *slot_pos, void *Xp, int32_t *affinity,
+                            const DispatchPlan &plan, const DispatchScratch &scr,
+                            int *status, cudaStream_t s)
+{
+    const size_t m_smem = static_cast<size_t>(CW) * E * sizeof(uint32_t);
+    cudaError_t err;
+    err = ensure_smem(reinterpret_cast<const void *>(masks_kernel), m_smem);
+    if (err != cudaSuccess) return err;
+    err = ensure_smem(reinterpret_cast<const void *>(scatter_kernel), 2 * m_smem);
+    if (err != cudaSuccess) return err;
+    masks_kernel<<<plan.n_chunks, CHUNK, m_smem, s>>>(topk_idx, T, E, K, scr.smask,
+                                                      scr.chunk_cnt, status);
+    scan_kernel<<<1, 1024, 0, s>>>(E, plan.n_chunks, scr.chunk_cnt, scr.chunk_base,
+                                   counts, offsets);
+    scatter_kernel<<<plan.n_chunks, CHUNK, 2 * m_smem, s>>>(topk_idx, T, E, K, scr.smask,
+                                                            scr.chunk_base, perm, slot_pos);
+    if (affinity) {
+        dim3 g((E + 31) / 32, (E + 31) / 32);
+        affinity_kernel<<<g, 256, 0, s>>>(scr.smask, plan.n_words, E, affinity);
+    }
+    if (Xp) {
+        const long long rows = static_cast<long long>(T) * K;
+        long long blocks = (rows + 7) / 8;
+        const long long cap = static_cast<long long>(num_sms()) * 8;
+        if (blocks > cap) blocks = cap;
+        gather_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(
+            static_cast<const uint4 *>(X), H, perm, offsets, E, static_cast<uint4 *>(Xp));
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace moe

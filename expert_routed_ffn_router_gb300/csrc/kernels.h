@@ -1,0 +1,80 @@
+// kernels.h -- host-side launchers of the library's kernels and the workspace plan.
+// Internal to the library: the public boundary is include/moe.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+// ------------------------------------------------------------------------- device info
+int num_sms();                 // SMs of the current device (cached per device)
+
+// --------------------------------------------------------------------------- router
+struct RouterPlan {
+    int TT, TE, nTT, nET, KS, S;  // token tile, expert tile, tiles, split-K, 32-wide stages
+    size_t part_bytes, xsq_bytes, wsq_bytes, cnt_bytes, smem_bytes;
+    size_t total() const { return part_bytes + xsq_bytes + wsq_bytes + cnt_bytes; }
+};
+RouterPlan router_plan(int T, int H, int E);
+
+struct RouterScratch {
+    float *part, *xsq, *wsq;
+    unsigned *cnt;
+};
+cudaError_t launch_router(const void *X, const void *Wg, const float *bias, int T, int H,
+                          int E, int K, int32_t *topk_idx, float *topk_w,
+                          const RouterPlan &plan, const RouterScratch &scr, int *status,
+                          cudaStream_t s);
+
+// ------------------------------------------------------------------------- dispatch
+struct DispatchPlan {
+    int n_chunks, n_words;             // 256-token chunks, 32-token mask rows
+    size_t smask_bytes, ccnt_bytes, cbase_bytes;
+    size_t total() const { return smask_bytes + ccnt_bytes + cbase_bytes; }
+};
+DispatchPlan dispatch_plan(int T, int E);
+
+struct DispatchScratch {
+    uint32_t *smask;
+    int32_t *chunk_cnt, *chunk_base;
+};
+cudaError_t launch_dispatch(const void *X, const int32_t *topk_idx, int T, int H, int E,
+                            int K, int32_t *counts, int32_t *offsets, int32_t *perm,
+                            int32_t *slot_pos, void *Xp, int32_t *affinity,
+                            const DispatchPlan &plan, const DispatchScratch &scr,
+                            int *status, cudaStream_t s);
+
+// -------------------------------------------------------------------------- combine
+cudaError_t launch_combine(const void *Yp, const int32_t *slot_pos, const float *topk_w,
+                           const float *Ysh, int T, int H, int K, float *Y, cudaStream_t s);
+
+// ------------------------------------------------------------------------------ FFN
+// One grouped problem of the expert FFN: rows of group g are [offsets[g], offsets[g+1])
+// (or one dense group of `dense_rows` rows when offsets == nullptr).
+struct FfnProblem {
+    const void *act;        // bf16 [rows, H] (up) -- the B operand rows
+    const int32_t *offsets; // device [n_groups + 1] or nullptr
+    int n_groups;
+    int rows;               // extent of `act` / the outputs (tensor-map size)
+    int dense_rows;         // used when offsets == nullptr
+    const void *W1, *W3, *W2;  // bf16 [n_groups, H, I], [n_groups, H, I], [n_groups, I, H]
+    void *h;                // bf16 [rows, I] activation scratch
+    void *out;              // [rows, H] bf16 or fp32
+    int out_fp32;
+};
+
+// Enqueues the up projection (+SwiGLU) and the down projection of up to two problems
+// (the routed experts and the shared expert) that share H; I may differ per problem.
+// `mid_event` (nullable) is recorded on `s` between the up and the down launch.
+cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I_per_prob,
+                       int token_hint, int *status, cudaStream_t s,
+                       unsigned long long timeout_ns, int inject, cudaEvent_t mid_event);
+
+// Raises the dynamic shared-memory limit of `func` to `bytes` once per process and size
+// (a no-op afterwards, so launches stay capturable).
+cudaError_t ensure_smem(const void *func, size_t bytes);
+
+}  // namespace moe

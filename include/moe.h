@@ -29,7 +29,9 @@
  *     no call synchronises the host, allocates or frees memory, so calls can be captured
  *     in a CUDA graph.  Outputs are valid once the stream reaches them.
  *   - `ws` is a caller-owned device workspace of at least moe_workspace_bytes() bytes
- *     (256-byte aligned).  Calls that share a workspace must be serialised by the caller.
+ *     (256-byte aligned).  Its first 4 bytes are the status word: zero them once after
+ *     allocating (e.g. cudaMemset); moe_read_status() resets the word after reading it.
+ *     Calls that share a workspace must be serialised by the caller.
  *   - Arguments are validated on the host before anything is enqueued: an invalid call
  *     returns a negative moe_status_t and has no effect.  A failing launch returns
  *     MOE_ERR_CUDA.  Conditions found on the device (a bounded wait that ran out) are
@@ -92,6 +94,20 @@ const char *moe_error_string(int status);
  * MOE_OK and returns what it held: MOE_OK or MOE_ERR_DEVICE_TIMEOUT; MOE_ERR_CUDA if the
  * copy itself failed. */
 int moe_read_status(void *ws, void *stream);
+
+/* Testing hook: sets the limit of the bounded device-side waits of the tensor-core FFN
+ * kernels (0 restores the default of one second) and, with inject_stall = 1, makes their
+ * TMA producer skip its work so that the waits run out and MOE_ERR_DEVICE_TIMEOUT is
+ * recorded in the status word (no fault, no hang).  Affects later moe_expert_ffn and
+ * moe_layer_forward calls of the process; not for production use. */
+void moe_debug_set_wait_limit(unsigned long long limit_ns, int inject_stall);
+
+/* Profiling hook: with `events` pointing at n >= 6 cudaEvent_t handles, every later
+ * moe_layer_forward records them on its stream: [0] before the router, [1] after the
+ * router, [2] after dispatch, [3] after the FFN up-projection launch, [4] after the FFN
+ * down-projection launch, [5] after combine.  events == NULL switches recording off.  The
+ * handles stay owned by the caller and must outlive the recording calls. */
+void moe_debug_set_stage_events(void *const *events, int n);
 
 /* Router: gate GEMM, sigmoid scoring, selection bias, top-K, renormalised weights, fused
  * in one kernel ("DeepSeek-V4.1-Flash", Kernels, Mega-Gate; "Lower latency and higher

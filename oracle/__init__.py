@@ -4,5 +4,5 @@ Only the tests, ``__graft_entry__.smoke()`` and the benchmark's ``cpu_baseline``
 import this package.  It shares no code with the CUDA library in
 ``expert_routed_ffn_router_gb300``.
 """
-from .oracle import (build_oracle, dispatch, expert_rows, forward, layer_tokens,  # noqa: F401
+from .oracle import (build_oracle, combine, dispatch, expert_rows, forward, layer_tokens,  # noqa: F401
                      num_threads, router)

@@ -263,6 +263,27 @@ int oracle_layer_tokens(const uint16_t *X, int H, int I, int Is, int K,
     return rc;
 }
 
+/* Combine on its own ([LLHT] "Expert Parallelism": weighted sum of the routed results,
+ * shared result added):  Y[t] = sum_j topk_w[t,j] * Yp[slot_pos[t,j]] (+ Ysh[t]).
+ * Yp is bf16 [rows, H], Ysh is double [T, H] or NULL, Y is double [T, H]. */
+int oracle_combine(const uint16_t *Yp, const int32_t *slot_pos, const double *topk_w,
+                   const double *Ysh, int T, int H, int K, double *Y)
+{
+    if (T < 0 || H <= 0 || K <= 0) return -1;
+    for (int t = 0; t < T; ++t) {
+        double *y = Y + (size_t)t * H;
+        for (int c = 0; c < H; ++c) y[c] = 0.0;
+        for (int j = 0; j < K; ++j) {
+            const uint16_t *row = Yp + (size_t)slot_pos[(size_t)t * K + j] * H;
+            double w = topk_w[(size_t)t * K + j];
+            for (int c = 0; c < H; ++c) y[c] += w * bf16_value(row[c]);
+        }
+        if (Ysh)
+            for (int c = 0; c < H; ++c) y[c] += Ysh[(size_t)t * H + c];
+    }
+    return 0;
+}
+
 /* Number of threads the OpenMP runtime will use (1 without OpenMP). */
 int oracle_num_threads(void)
 {

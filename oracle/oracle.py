@@ -56,6 +56,8 @@ def _load():
         lib.oracle_expert_rows.restype = i
         lib.oracle_layer_tokens.argtypes = [P, i, i, i, i, P, P, P, P, P, P, P, P, P, i, P]
         lib.oracle_layer_tokens.restype = i
+        lib.oracle_combine.argtypes = [P, P, P, P, i, i, i, P]
+        lib.oracle_combine.restype = i
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i
         _lib = lib
@@ -165,6 +167,23 @@ def layer_tokens(X: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray,
     if rc != 0:
         raise ValueError(f"oracle_layer_tokens rejected its arguments ({rc})")
     del keep
+    return Y
+
+
+def combine(Yp: np.ndarray, slot_pos: np.ndarray, topk_w: np.ndarray,
+            Ysh: np.ndarray | None = None) -> np.ndarray:
+    """Y[t] = sum_j topk_w[t,j] * Yp[slot_pos[t,j]] (+ Ysh[t]); Yp bf16 bits [rows,H]."""
+    Yp = _u16(Yp)
+    slot_pos = np.ascontiguousarray(slot_pos, dtype=np.int32)
+    topk_w = np.ascontiguousarray(topk_w, dtype=np.float64)
+    T, K = slot_pos.shape
+    H = Yp.shape[1]
+    if Ysh is not None:
+        Ysh = np.ascontiguousarray(Ysh, dtype=np.float64)
+    Y = np.zeros((T, H), np.float64)
+    rc = _load().oracle_combine(_p(Yp), _p(slot_pos), _p(topk_w), _p(Ysh), T, H, K, _p(Y))
+    if rc != 0:
+        raise ValueError(f"oracle_combine rejected its arguments ({rc})")
     return Y
 
 

@@ -1,0 +1,75 @@
+"""The C-ABI library builds, loads and exports every function include/moe.h declares, and
+its host-side argument validation rejects bad calls before anything reaches a GPU.
+(CPU only: no call here launches a kernel.)"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from expert_routed_ffn_router_gb300 import _build, binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(moe_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return ctypes.CDLL(_build.LIB)
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("moe_router_topk", "moe_dispatch", "moe_expert_ffn", "moe_combine",
+              "moe_layer_forward", "moe_workspace_bytes", "moe_error_string",
+              "moe_read_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_error_strings_and_workspace_size():
+    assert binding.moe_error_string(0) == "ok"
+    assert "timeout" in binding.moe_error_string(-6) or "ran out" in binding.moe_error_string(-6)
+    n = binding.moe_workspace_bytes(128, 7168, 256, 8, 2048, 2048)
+    # at least the permuted activations, h, Yp (bf16) and the shared output (fp32)
+    TK = 128 * 8
+    assert n >= TK * 7168 * 2 * 2 + TK * 2048 * 2 + 128 * 7168 * 4
+    assert binding.moe_workspace_bytes(1, 100, 16, 2, 128, 0) == 0        # H % 64 != 0
+    assert binding.moe_workspace_bytes(1, 256, 2048, 2, 128, 0) == 0      # E > 1024
+    assert binding.moe_workspace_bytes(1, 256, 16, 17, 128, 0) == 0       # K > E
+    assert binding.moe_workspace_bytes(0, 256, 16, 2, 128, 128) > 0
+
+
+def test_validation_rejects_before_launch(lib):
+    lib.moe_router_topk.restype = ctypes.c_int
+    lib.moe_combine.restype = ctypes.c_int
+    P = ctypes.c_void_p
+    ok = P(0x10000)            # never dereferenced: every call below fails validation
+    bad = P(0x10001)
+    ws = P(0x100000)
+    f = lib.moe_router_topk
+    f.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P,
+                  ctypes.c_size_t, P]
+    assert f(ok, ok, ok, 4, 256, 16, 17, ok, ok, ws, 1 << 20, None) == -1   # K > E
+    assert f(ok, ok, ok, 4, 96, 16, 2, ok, ok, ws, 1 << 20, None) == -2     # H % 64
+    assert f(bad, ok, ok, 4, 256, 16, 2, ok, ok, ws, 1 << 20, None) == -3   # misaligned
+    assert f(None, ok, ok, 4, 256, 16, 2, ok, ok, ws, 1 << 20, None) == -1  # null
+    assert f(ok, ok, ok, 4, 256, 16, 2, ok, ok, ws, 16, None) == -4         # small ws
+    assert f(ok, ok, ok, -1, 256, 16, 2, ok, ok, ws, 1 << 20, None) == -1   # T < 0
+    g = lib.moe_combine
+    g.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P]
+    assert g(ok, ok, ok, bad, 4, 256, 2, ok, None) == -3                    # Ysh misaligned
+    assert g(ok, ok, ok, None, 4, 256, 33, ok, None) == -2                  # K > 32
+    assert g(ok, ok, ok, None, 0, 256, 2, ok, None) == 0                    # T == 0: no-op

@@ -1,0 +1,190 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the same seeded
+inputs.  Integer outputs (top-k indices, counts, offsets, permutation, slot positions,
+affinity) must be bit-exact; routing weights within 1e-5; Y within relative Frobenius
+5e-3 and max-abs 3e-2."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from expert_routed_ffn_router_gb300 import binding as B
+from expert_routed_ffn_router_gb300 import synth
+
+from gpu_common import (DEV, W_MAX_ABS, Y_MAX_ABS, Y_REL_FROB, Problem, bits, check_layer,
+                        host_to_device_bf16, rel_frob)
+
+pytestmark = pytest.mark.gpu
+
+
+def _ws(nbytes):
+    return torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+
+
+# --------------------------------------------------------------------------- whole layer
+def test_tiny_layer():
+    r = check_layer(Problem(synth.workload("tiny")))
+    assert r["rel_frob"] < 2e-3
+
+
+@pytest.mark.parametrize("T,H,E,K,I,Is", [
+    (1, 256, 16, 2, 128, 128),      # a single token: 14 experts receive nothing
+    (37, 256, 16, 2, 128, 128),     # ragged token tail
+    (300, 192, 40, 5, 192, 64),     # H % 128 == 64, E not a multiple of 32, K = 5
+    (130, 128, 8, 8, 64, 0),        # K == E (every expert, order only), no shared expert
+    (513, 256, 64, 6, 256, 128),    # several dispatch chunks
+])
+def test_ragged_shapes(T, H, E, K, I, Is):
+    w = synth.Workload("rag", T=T, H=H, E=E, K=K, I=I, Is=Is, seed=T, x_seed=T + 1)
+    check_layer(Problem(w))
+
+
+def test_exact_ties_duplicate_gate_rows():
+    w = synth.workload("tiny", T=64)
+    r = synth.routing_inputs(w)
+    for a, b in ((1, 9), (4, 5), (0, 15)):
+        r["W_gate"][b] = r["W_gate"][a]
+        r["bias"][b] = r["bias"][a]
+    res = check_layer(Problem(w, routing=r))
+    both = [row for row in res["idx"].tolist() if 4 in row and 5 in row]
+    assert both and all(row.index(4) < row.index(5) for row in both)
+
+
+def test_near_ties_take_the_refine_path():
+    # gate rows that differ in one bf16 ulp of one element: selection scores a few 1e-6
+    # apart, far inside the fp32 error bound, so the exact order must come from the refine
+    w = synth.workload("tiny", T=96)
+    r = synth.routing_inputs(w)
+    for a, b in ((2, 3), (7, 11), (12, 13)):
+        r["W_gate"][b] = r["W_gate"][a]
+        r["W_gate"][b, 17] = r["W_gate"][a, 17] + 1
+        r["bias"][b] = r["bias"][a]
+    check_layer(Problem(w, routing=r))
+
+
+def test_one_expert_takes_every_token():
+    w = synth.workload("tiny", T=200)
+    r = synth.routing_inputs(w)
+    r["bias"][3] = 10.0
+    res = check_layer(Problem(w, routing=r))
+    assert res["disp"]["counts"][3] == w.T
+
+
+def test_deterministic_and_graph_capture():
+    p = Problem(synth.workload("tiny", T=77))
+    layer = B.MoELayer(p.dev, p.w.T, p.w.K)
+    layer.forward(p.X)
+    torch.cuda.synchronize()
+    y1 = layer.Y.clone()
+    layer.forward(p.X)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, layer.Y)
+    # capture the whole layer in a CUDA graph and replay it on new activations
+    s = torch.cuda.Stream()
+    X2 = p.X.clone()
+    with torch.cuda.stream(s):
+        layer.forward(X2, stream=s)            # warm-up on the capture stream
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            layer.forward(X2, stream=s)
+    torch.cuda.synchronize()
+    Xn = host_to_device_bf16(synth.f32_to_bf16_bits(
+        np.random.default_rng(5).standard_normal((p.w.T, p.w.H)).astype(np.float32)))
+    X2.copy_(Xn)
+    g.replay()
+    torch.cuda.synchronize()
+    y_graph = layer.Y.clone()
+    layer.forward(Xn)
+    torch.cuda.synchronize()
+    assert torch.equal(y_graph, layer.Y)
+    assert layer.status() == 0
+
+
+# --------------------------------------------------------------------- separate stages
+def test_stages_separately_tiny():
+    w = synth.workload("tiny", T=45)
+    p = Problem(w)
+    T, H, E, K, I = w.T, w.H, w.E, w.K, w.I
+    ws = _ws(B.moe_workspace_bytes(T, H, E, K, I, w.Is))
+    idx = torch.empty(T, K, dtype=torch.int32, device=DEV)
+    wt = torch.empty(T, K, dtype=torch.float32, device=DEV)
+    B.moe_router_topk(p.X, p.dev["W_gate"], p.dev["bias"], K, idx, wt, ws)
+    idx_o, w_o = p.oracle_routing()
+    assert np.array_equal(idx.cpu().numpy(), idx_o)
+    assert np.abs(wt.cpu().numpy() - w_o).max() <= W_MAX_ABS
+
+    # dispatch fed the oracle's routing (no GPU-made input reaches the oracle)
+    idx_in = torch.from_numpy(idx_o).to(DEV)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(T * K, dtype=torch.int32, device=DEV)
+    slot = torch.empty(T, K, dtype=torch.int32, device=DEV)
+    Xp = torch.empty(T * K, H, dtype=torch.bfloat16, device=DEV)
+    aff = torch.empty(E, E, dtype=torch.int32, device=DEV)
+    B.moe_dispatch(p.X, idx_in, E, counts, offsets, perm, slot, Xp, aff, ws)
+    d = oracle.dispatch(idx_o, E)
+    for name, t in (("counts", counts), ("offsets", offsets), ("perm", perm),
+                    ("slot_pos", slot), ("affinity", aff)):
+        assert np.array_equal(t.cpu().numpy().reshape(d[name].shape), d[name]), name
+    assert np.array_equal(bits(Xp), p.routing["X"][d["perm"]])
+
+    # expert FFN on the oracle's permutation of X
+    Xp_h = p.routing["X"][d["perm"]]
+    Xp_in = host_to_device_bf16(Xp_h)
+    off_in = torch.from_numpy(d["offsets"]).to(DEV)
+    Yp = torch.empty(T * K, H, dtype=torch.float32, device=DEV)
+    B.moe_expert_ffn(Xp_in, off_in, E, p.dev["W1"], p.dev["W3"], p.dev["W2"], Yp, ws)
+    torch.cuda.synchronize()
+    rows_e = np.searchsorted(d["offsets"], np.arange(T * K), side="right") - 1
+    y_o = oracle.expert_rows(list(Xp_h), [p.host_w["W1"][e] for e in rows_e],
+                             [p.host_w["W3"][e] for e in rows_e],
+                             [p.host_w["W2"][e] for e in rows_e], H, I)
+    y_g = Yp.cpu().numpy().astype(np.float64)
+    assert rel_frob(y_g, y_o) <= Y_REL_FROB and np.abs(y_g - y_o).max() <= Y_MAX_ABS
+
+    # combine on a synthetic Yp and the oracle's slots, weights rounded to fp32 on both sides
+    rng = np.random.default_rng(3)
+    Yp_h = synth.f32_to_bf16_bits(rng.standard_normal((T * K, H)).astype(np.float32))
+    Ysh_h = rng.standard_normal((T, H)).astype(np.float32)
+    w32 = w_o.astype(np.float32)
+    Y = torch.empty(T, H, dtype=torch.float32, device=DEV)
+    B.moe_combine(host_to_device_bf16(Yp_h), torch.from_numpy(d["slot_pos"]).to(DEV),
+                  torch.from_numpy(w32).to(DEV), torch.from_numpy(Ysh_h).to(DEV), Y)
+    Y_o = oracle.combine(Yp_h, d["slot_pos"], w32.astype(np.float64), Ysh_h.astype(np.float64))
+    assert np.abs(Y.cpu().numpy() - Y_o).max() <= 1e-5
+    assert B.moe_read_status(ws) == 0
+
+
+def test_shared_expert_alone_is_a_dense_group():
+    w = synth.workload("tiny", T=70)
+    p = Problem(w)
+    T, H, Is = w.T, w.H, w.Is
+    ws = _ws(B.moe_workspace_bytes(T, H, 1, 1, Is, 0))
+    off = torch.tensor([0, T], dtype=torch.int32, device=DEV)
+    Y = torch.empty(T, H, dtype=torch.float32, device=DEV)
+    B.moe_expert_ffn(p.X, off, 1, p.dev["W1s"].unsqueeze(0).contiguous(),
+                     p.dev["W3s"].unsqueeze(0).contiguous(),
+                     p.dev["W2s"].unsqueeze(0).contiguous(), Y, ws)
+    torch.cuda.synchronize()
+    X = p.routing["X"]
+    y_o = oracle.expert_rows(list(X), [p.host_w["W1s"]] * T, [p.host_w["W3s"]] * T,
+                             [p.host_w["W2s"]] * T, H, Is)
+    assert rel_frob(Y.cpu().numpy().astype(np.float64), y_o) <= Y_REL_FROB
+
+
+# ------------------------------------------------------------------ bounded waits
+def test_bounded_wait_reports_timeout_and_context_survives():
+    w = synth.workload("tiny", T=40)
+    p = Problem(w)
+    layer = B.MoELayer(p.dev, w.T, w.K)
+    try:
+        B.moe_debug_set_wait_limit(50_000_000, inject_stall=1)    # 50 ms
+        layer.forward(p.X)
+        torch.cuda.synchronize()
+        assert layer.status() == B.MOE_ERR_DEVICE_TIMEOUT
+    finally:
+        B.moe_debug_set_wait_limit(0, 0)
+    layer.forward(p.X)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    idx_o, w_o = p.oracle_routing()
+    assert np.array_equal(layer.topk_idx.cpu().numpy(), idx_o)

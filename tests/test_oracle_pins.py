@@ -247,3 +247,19 @@ def test_bf16_encoding_round_to_nearest_even():
     assert b[0] == 0x3F80 and b[1] == 0x3F82 and b[2] == 0xC020 and b[3] == 0
     np.testing.assert_array_equal(_val(b)[:4], [1.0, 1 + 2 ** -6, -2.5, 0.0])
     assert math.isclose(_val(b)[4], 3e-30, rel_tol=2 ** -8)
+
+
+def test_combine_one_hot_and_linearity():
+    r = np.random.default_rng(9)
+    T, K, H = 6, 3, 32
+    Yp = _bits(r.standard_normal((T * K, H)))
+    slot = r.permutation(T * K).reshape(T, K).astype(np.int32)
+    onehot = np.zeros((T, K))
+    onehot[:, 1] = 1.0
+    Y = oracle.combine(Yp, slot, onehot)
+    np.testing.assert_array_equal(Y, _val(Yp)[slot[:, 1]])       # picks one row exactly
+    w = r.uniform(0, 1, (T, K))
+    sh = r.standard_normal((T, H))
+    Y1 = oracle.combine(Yp, slot, w, sh)
+    ref = np.einsum("tk,tkh->th", w, _val(Yp)[slot]) + sh      # library contraction
+    np.testing.assert_allclose(Y1, ref, rtol=1e-14, atol=1e-14)
