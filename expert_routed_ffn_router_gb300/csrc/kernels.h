@@ -15,6 +15,7 @@ int num_sms();                 // SMs of the current device (cached per device)
 // --------------------------------------------------------------------------- router
 struct RouterPlan {
     int TT, TE, nTT, nET, KS, S;  // token tile, expert tile, tiles, split-K, 32-wide stages
+    int max_pairs;                // shared-memory refine list capacity
     size_t part_bytes, xsq_bytes, wsq_bytes, cnt_bytes, smem_bytes;
     size_t total() const { return part_bytes + xsq_bytes + wsq_bytes + cnt_bytes; }
 };

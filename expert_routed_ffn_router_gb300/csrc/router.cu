@@ -22,10 +22,11 @@
 // (error-free TwoSum accumulation of the exact products, ~2^-48 relative) with an fp64
 // sigmoid, and the top-k is taken again among those candidates.
 //
-// Structure.  Grid (expert tiles, token tiles, K splits).  Each CTA computes a 64x64
-// tile of fp32 logits over its slice of H on the CUDA cores and writes it to the
-// workspace; the last CTA of a token tile (completion counter) sums the split-K partials in
-// a fixed order, scores, selects and writes the outputs -- one launch, no host sync.
+// Structure.  Grid (expert tiles, token tiles, K splits).  Each CTA computes a TT x 64
+// tile of fp32 logits (TT = 16 tokens for small batches, 64 for large ones) over its slice
+// of H on the CUDA cores and writes it to the workspace; the last CTA of a token tile
+// (completion counter) sums the split-K partials in a fixed order, scores, selects and
+// writes the outputs -- one launch, no host sync.
 #include <cfloat>
 #include <climits>
 
@@ -35,7 +36,6 @@
 namespace moe {
 namespace {
 
-constexpr int TT = 64;     // tokens per CTA tile
 constexpr int TE = 64;     // experts per CTA tile
 constexpr int KST = 32;    // k per shared-memory stage
 constexpr int NT = 256;    // threads
@@ -53,6 +53,7 @@ struct RouterArgs {
     int32_t *topk_idx;
     float *topk_w;
     int *status;
+    int max_pairs;   // capacity of the shared-memory refine list
 };
 
 __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
@@ -82,40 +83,113 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &err)
     err = __fadd_rn(__fsub_rn(a, ap), __fsub_rn(b, bp));
 }
 
+// Double-word accumulation of an exact fp32 product into (hi, lo).
+__device__ __forceinline__ void dw_add(float &hi, float &lo, float p)
+{
+    float s, e;
+    two_sum(hi, p, s, e);
+    hi = s;
+    lo = __fadd_rn(lo, e);
+}
+
+// (hi, lo) += (ohi, olo) in double-word arithmetic.
+__device__ __forceinline__ void dw_merge(float &hi, float &lo, float ohi, float olo)
+{
+    float s, e;
+    two_sum(hi, ohi, s, e);
+    hi = s;
+    lo = __fadd_rn(__fadd_rn(lo, olo), e);
+}
+
 // Double-word dot product of a bf16 token row and a bf16 gate row, reduced over the warp
-// in a fixed order; every lane returns the same value.
+// in a fixed order; every lane returns the same value.  Four independent accumulators per
+// lane keep four 16-byte loads of each row in flight.
 __device__ double dot_double_word(const uint16_t *x, const uint16_t *w, int H, int lane)
 {
     const uint4 *xr = reinterpret_cast<const uint4 *>(x);
     const uint4 *wr = reinterpret_cast<const uint4 *>(w);
-    float hi = 0.f, lo = 0.f;
-    for (int v = lane; v < H / 8; v += 32) {
-        float xf[8], wf[8];
-        unpack8(xr[v], xf);
-        unpack8(wr[v], wf);
+    const int nv = H / 8;
+    float hi[4] = {0.f, 0.f, 0.f, 0.f}, lo[4] = {0.f, 0.f, 0.f, 0.f};
+    int v = lane;
+    for (; v + 96 < nv; v += 128) {
+        uint4 xa[4], wa[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float p = __fmul_rn(xf[i], wf[i]);  // exact: 8-bit x 8-bit significands
-            float s, e;
-            two_sum(hi, p, s, e);
-            hi = s;
-            lo = __fadd_rn(lo, e);
+        for (int u = 0; u < 4; ++u) {
+            xa[u] = __ldg(xr + v + 32 * u);
+            wa[u] = __ldg(wr + v + 32 * u);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            float xf[8], wf[8];
+            unpack8(xa[u], xf);
+            unpack8(wa[u], wf);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dw_add(hi[u], lo[u], __fmul_rn(xf[i], wf[i]));  // exact product
         }
     }
+    for (; v < nv; v += 32) {
+        float xf[8], wf[8];
+        unpack8(__ldg(xr + v), xf);
+        unpack8(__ldg(wr + v), wf);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dw_add(hi[0], lo[0], __fmul_rn(xf[i], wf[i]));
+    }
+    dw_merge(hi[0], lo[0], hi[1], lo[1]);
+    dw_merge(hi[2], lo[2], hi[3], lo[3]);
+    dw_merge(hi[0], lo[0], hi[2], lo[2]);
+    float h = hi[0], l = lo[0];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-        float ohi = __shfl_xor_sync(kFullMask, hi, off);
-        float olo = __shfl_xor_sync(kFullMask, lo, off);
-        float s, e;
-        two_sum(hi, ohi, s, e);
-        hi = s;
-        lo = __fadd_rn(__fadd_rn(lo, olo), e);
+        const float ohi = __shfl_xor_sync(kFullMask, h, off);
+        const float olo = __shfl_xor_sync(kFullMask, l, off);
+        dw_merge(h, l, ohi, olo);
     }
-    return static_cast<double>(hi) + static_cast<double>(lo);
+    return static_cast<double>(h) + static_cast<double>(l);
 }
 
+// Top-K of a token among `n` candidate (expert, sel64) pairs by (sel64 desc, expert asc);
+// writes the experts and their renormalised weights.  Warp-wide; pairs live in shared memory.
+__device__ void select_refined(const int *pe, const double *pv, int n, int K,
+                               const float *bias, int32_t *oi, float *ow, int *ord, int lane)
+{
+    for (int j = 0; j < K; ++j) {
+        double bs = -DBL_MAX;
+        int be = INT_MAX, bp = -1;
+        for (int q = lane; q < n; q += 32) {
+            const int e = pe[q];
+            if (e < 0) continue;                 // already taken
+            const double v = pv[q];
+            if (be == INT_MAX || before64(v, e, bs, be)) { bs = v; be = e; bp = q; }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const double os = __shfl_xor_sync(kFullMask, bs, off);
+            const int oe = __shfl_xor_sync(kFullMask, be, off);
+            const int op = __shfl_xor_sync(kFullMask, bp, off);
+            if (oe != INT_MAX && (be == INT_MAX || before64(os, oe, bs, be))) { bs = os; be = oe; bp = op; }
+        }
+        if (lane == 0) ord[j] = bp;
+        __syncwarp();
+        if (lane == (bp & 31)) const_cast<int *>(pe)[bp] = -1 - be;   // mark taken, keep expert
+        __syncwarp();
+    }
+    double den = 0.0;
+    for (int j = 0; j < K; ++j) {
+        const int q = ord[j], e = -1 - pe[q];
+        den += pv[q] - static_cast<double>(bias[e]);
+    }
+    for (int j = lane; j < K; j += 32) {
+        const int q = ord[j], e = -1 - pe[q];
+        oi[j] = e;
+        ow[j] = static_cast<float>((pv[q] - static_cast<double>(bias[e])) / den);
+    }
+    __syncwarp();
+}
+
+template <int TT>
 __global__ void __launch_bounds__(NT, 2) router_kernel(const RouterArgs a)
 {
+    constexpr int TPT = TT / 16;                   // tokens per thread in the tile GEMM
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_last;
 
@@ -130,18 +204,21 @@ __global__ void __launch_bounds__(NT, 2) router_kernel(const RouterArgs a)
     float *xs = reinterpret_cast<float *>(smem);   // [2][KST][TT]
     float *wsm = xs + 2 * KST * TT;                // [2][KST][TE]
 
-    const int lr = tid & 63, lv = tid >> 6;        // loader: row, 8-element vector
-    const int xrow = t0 + lr, wrow = e0 + lr;
-    const bool xok = xrow < a.T, wok = wrow < a.E;
-    const uint4 *xp = reinterpret_cast<const uint4 *>(a.X + static_cast<size_t>(xok ? xrow : 0) * a.H) + lv;
-    const uint4 *wp = reinterpret_cast<const uint4 *>(a.Wg + static_cast<size_t>(wok ? wrow : 0) * a.H) + lv;
+    // loaders: X tile = TT rows x 4 vectors of 8 bf16, W tile = 64 rows x 4 vectors
+    const bool xload = tid < TT * 4;
+    const int xr_row = tid % TT, xr_vec = tid / TT;
+    const int wr_row = tid & 63, wr_vec = tid >> 6;
+    const int xrow = t0 + xr_row, wrow = e0 + wr_row;
+    const bool xok = xload && xrow < a.T, wok = wrow < a.E;
+    const uint4 *xp = reinterpret_cast<const uint4 *>(a.X + static_cast<size_t>(xok ? xrow : 0) * a.H) + xr_vec;
+    const uint4 *wp = reinterpret_cast<const uint4 *>(a.Wg + static_cast<size_t>(wok ? wrow : 0) * a.H) + wr_vec;
     float xsq = 0.f, wsq = 0.f;
     uint4 xr = make_uint4(0, 0, 0, 0), wr = make_uint4(0, 0, 0, 0);
 
-    const int tx = tid & 15, ty = tid >> 4;        // compute: experts 4tx.., tokens 4ty..
-    float acc_mid[16], acc_out[16];
+    const int tx = tid & 15, ty = tid >> 4;        // compute: experts 4tx.., tokens TPT*ty..
+    float acc_mid[TPT * 4], acc_out[TPT * 4];
 #pragma unroll
-    for (int p = 0; p < 16; ++p) { acc_mid[p] = 0.f; acc_out[p] = 0.f; }
+    for (int p = 0; p < TPT * 4; ++p) { acc_mid[p] = 0.f; acc_out[p] = 0.f; }
 
     auto gload = [&](int s) {
         xr = xok ? __ldg(xp + s * 4) : make_uint4(0, 0, 0, 0);
@@ -151,14 +228,19 @@ __global__ void __launch_bounds__(NT, 2) router_kernel(const RouterArgs a)
         float xf[8], wf[8];
         unpack8(xr, xf);
         unpack8(wr, wf);
-        float *xd = xs + buf * KST * TT + (lv * 8) * TT + lr;
-        float *wd = wsm + buf * KST * TE + (lv * 8) * TE + lr;
+        float *wd = wsm + buf * KST * TE + (wr_vec * 8) * TE + wr_row;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            xd[i * TT] = xf[i];
             wd[i * TE] = wf[i];
-            xsq = fmaf(xf[i], xf[i], xsq);
             wsq = fmaf(wf[i], wf[i], wsq);
+        }
+        if (xload) {
+            float *xd = xs + buf * KST * TT + (xr_vec * 8) * TT + xr_row;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                xd[i * TT] = xf[i];
+                xsq = fmaf(xf[i], xf[i], xsq);
+            }
         }
     };
 
@@ -170,27 +252,32 @@ __global__ void __launch_bounds__(NT, 2) router_kernel(const RouterArgs a)
     int buf = 0, nmid = 0;
     for (int s = s_beg; s < s_end; ++s) {
         if (s + 1 < s_end) gload(s + 1);
-        float acc_in[16];
+        float acc_in[TPT * 4];
 #pragma unroll
-        for (int p = 0; p < 16; ++p) acc_in[p] = 0.f;
-        const float *xb = xs + buf * KST * TT + 4 * ty;
+        for (int p = 0; p < TPT * 4; ++p) acc_in[p] = 0.f;
+        const float *xb = xs + buf * KST * TT + TPT * ty;
         const float *wb = wsm + buf * KST * TE + 4 * tx;
 #pragma unroll 8
         for (int kk = 0; kk < KST; ++kk) {
-            const float4 xv = *reinterpret_cast<const float4 *>(xb + kk * TT);
+            float xa[TPT];
+            if constexpr (TPT == 4) {
+                const float4 xv = *reinterpret_cast<const float4 *>(xb + kk * TT);
+                xa[0] = xv.x; xa[1] = xv.y; xa[2] = xv.z; xa[3] = xv.w;
+            } else {
+                xa[0] = xb[kk * TT];
+            }
             const float4 wv = *reinterpret_cast<const float4 *>(wb + kk * TE);
-            const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
             const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < TPT; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) acc_in[i * 4 + j] = fmaf(xa[i], wa[j], acc_in[i * 4 + j]);
         }
 #pragma unroll
-        for (int p = 0; p < 16; ++p) acc_mid[p] += acc_in[p];
+        for (int p = 0; p < TPT * 4; ++p) acc_mid[p] += acc_in[p];
         if (++nmid == 8) {
 #pragma unroll
-            for (int p = 0; p < 16; ++p) { acc_out[p] += acc_mid[p]; acc_mid[p] = 0.f; }
+            for (int p = 0; p < TPT * 4; ++p) { acc_out[p] += acc_mid[p]; acc_mid[p] = 0.f; }
             nmid = 0;
         }
         if (s + 1 < s_end) sstore(buf ^ 1);
@@ -198,11 +285,11 @@ __global__ void __launch_bounds__(NT, 2) router_kernel(const RouterArgs a)
         buf ^= 1;
     }
 #pragma unroll
-    for (int p = 0; p < 16; ++p) acc_out[p] += acc_mid[p];
+    for (int p = 0; p < TPT * 4; ++p) acc_out[p] += acc_mid[p];
 
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int t = t0 + 4 * ty + i;
+    for (int i = 0; i < TPT; ++i) {
+        const int t = t0 + TPT * ty + i;
         if (t >= a.T) continue;
         float *dst = a.part + (static_cast<size_t>(ks) * a.T + t) * a.E;
 #pragma unroll
@@ -214,15 +301,17 @@ __global__ void __launch_bounds__(NT, 2) router_kernel(const RouterArgs a)
 
     // squared norms of this slice, reduced over the 4 loader threads of a row in order
     {
-        float *rx = xs;            // [4][64]
-        float *rw = xs + 4 * 64;   // [4][64]
-        rx[lv * 64 + lr] = xsq;
-        rw[lv * 64 + lr] = wsq;
+        float *rx = xs;            // [4][TT]
+        float *rw = xs + 4 * TT;   // [4][64]
+        if (xload) rx[xr_vec * TT + xr_row] = xsq;
+        rw[wr_vec * 64 + wr_row] = wsq;
         __syncthreads();
-        if (tid < 64) {
-            const float sx = ((rx[tid] + rx[64 + tid]) + rx[128 + tid]) + rx[192 + tid];
-            const float sw = ((rw[tid] + rw[64 + tid]) + rw[128 + tid]) + rw[192 + tid];
+        if (tid < TT) {
+            const float sx = ((rx[tid] + rx[TT + tid]) + rx[2 * TT + tid]) + rx[3 * TT + tid];
             if (et == 0 && t0 + tid < a.T) a.xsq[static_cast<size_t>(ks) * a.T + t0 + tid] = sx;
+        }
+        if (tid < 64) {
+            const float sw = ((rw[tid] + rw[64 + tid]) + rw[128 + tid]) + rw[192 + tid];
             if (e0 + tid < a.E)
                 a.wsq[(static_cast<size_t>(tt) * a.KS + ks) * a.E + e0 + tid] = sw;
         }
@@ -242,21 +331,36 @@ __global__ void __launch_bounds__(NT, 2) router_kernel(const RouterArgs a)
     const int warp = tid >> 5, lane = tid & 31;
     const int E = a.E, K = a.K, KS = a.KS;
     const int NI = (E + 31) / 32;
-    // per-warp arrays: sel[E], bnd[E], sc[E] (fp32) and sel64[E] (fp64)
-    float *w_sel = reinterpret_cast<float *>(smem) + static_cast<size_t>(warp) * 3 * E;
-    float *w_bnd = w_sel + E;
-    float *w_sc = w_bnd + E;
-    double *w_s64 = reinterpret_cast<double *>(
-        smem + static_cast<size_t>(NW) * 3 * E * sizeof(float)) + static_cast<size_t>(warp) * E;
-    int *w_ord = reinterpret_cast<int *>(
-        smem + static_cast<size_t>(NW) * 3 * E * sizeof(float) +
-        static_cast<size_t>(NW) * E * sizeof(double)) + warp * 32;
-
     // depth of the summation tree (see the file comment) and the norm inflation
     const int ns_max = (a.S + KS - 1) / KS;
     const float depth = static_cast<float>(KST + 8 + (ns_max + 7) / 8 + 1 + KS + 2);
     const float gam = depth * kU / (1.f - depth * kU) * 1.0001f;
     const float infl = 1.f + static_cast<float>(a.H + 16 + KS) * (2.f * kU) + 4.f * kU;
+
+    // shared: nw[E] | per warp sel[E], bnd[E], sc[E] | per warp ord[32] | pair list
+    // (expert, sel64) of the tokens to refine | per warp sel64 scratch for overflow
+    float *nw = reinterpret_cast<float *>(smem);
+    float *w_sel = nw + E + static_cast<size_t>(warp) * 3 * E;
+    float *w_bnd = w_sel + E;
+    float *w_sc = w_bnd + E;
+    int *w_ord = reinterpret_cast<int *>(nw + E + static_cast<size_t>(NW) * 3 * E) + warp * 32;
+    int *p_e = reinterpret_cast<int *>(nw + E + static_cast<size_t>(NW) * 3 * E) + NW * 32;
+    int *p_tok = p_e + a.max_pairs;
+    unsigned char *after_i = reinterpret_cast<unsigned char *>(p_tok + a.max_pairs);
+    after_i = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(after_i) + 7) & ~static_cast<uintptr_t>(7));
+    double *p_val = reinterpret_cast<double *>(after_i);
+    double *w_s64 = p_val + a.max_pairs + static_cast<size_t>(warp) * E;   // overflow only
+    __shared__ int s_npairs, s_npend;
+    __shared__ int s_pend[3 * 64];      // (token, first pair, pair count) per pending token
+    if (tid == 0) { s_npairs = 0; s_npend = 0; }
+
+    // gate-row norms once per CTA (the K-split partial sums, added in order)
+    for (int e = tid; e < E; e += NT) {
+        float nw2 = 0.f;
+        for (int q = 0; q < KS; ++q) nw2 += a.wsq[(static_cast<size_t>(tt) * KS + q) * E + e];
+        nw[e] = sqrtf(nw2) * infl;
+    }
+    __syncthreads();
 
     for (int tl = warp; tl < TT; tl += NW) {
         const int t = t0 + tl;
@@ -265,14 +369,8 @@ __global__ void __launch_bounds__(NT, 2) router_kernel(const RouterArgs a)
         for (int q = 0; q < KS; ++q) nx2 += a.xsq[static_cast<size_t>(q) * a.T + t];
         const float nx = sqrtf(nx2) * infl;
 
-        for (int i = 0; i < NI; ++i) {
-            const int e = lane + 32 * i;
-            if (e >= E) break;
-            float l = a.part[static_cast<size_t>(t) * E + e];
-            for (int q = 1; q < KS; ++q) l += a.part[(static_cast<size_t>(q) * a.T + t) * E + e];
-            float nw2 = 0.f;
-            for (int q = 0; q < KS; ++q) nw2 += a.wsq[(static_cast<size_t>(tt) * KS + q) * E + e];
-            const float bl = gam * nx * (sqrtf(nw2) * infl) + 1e-30f;
+        auto score = [&](int e, float l) {
+            const float bl = gam * nx * nw[e] + 1e-30f;
             const float s = 1.f / (1.f + expf(-l));
             const float sel = s + a.bias[e];
             const float al = fabsf(l);
@@ -280,10 +378,35 @@ __global__ void __launch_bounds__(NT, 2) router_kernel(const RouterArgs a)
             w_sel[e] = sel;
             w_bnd[e] = bl * D + 4.f * kU + fabsf(sel) * (2.f * kU);
             w_sc[e] = s;
+        };
+        if ((E & 3) == 0) {
+            // coalesced float4 reads of the K-split partials, all issued before the sum
+            for (int g = lane; g < E / 4; g += 32) {
+                float4 v[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    if (q < KS)
+                        v[q] = __ldcg(reinterpret_cast<const float4 *>(
+                                   a.part + (static_cast<size_t>(q) * a.T + t) * E) + g);
+                float4 l = v[0];
+#pragma unroll
+                for (int q = 1; q < 16; ++q)
+                    if (q < KS) { l.x += v[q].x; l.y += v[q].y; l.z += v[q].z; l.w += v[q].w; }
+                score(4 * g, l.x);
+                score(4 * g + 1, l.y);
+                score(4 * g + 2, l.z);
+                score(4 * g + 3, l.w);
+            }
+        } else {
+            for (int e = lane; e < E; e += 32) {
+                float l = __ldcg(a.part + static_cast<size_t>(t) * E + e);
+                for (int q = 1; q < KS; ++q) l += __ldcg(a.part + (static_cast<size_t>(q) * a.T + t) * E + e);
+                score(e, l);
+            }
         }
         __syncwarp();
 
-        // top-K by (sel desc, index asc)
+        // top-K by (sel desc, index asc); lane owns experts lane + 32 i
         uint32_t taken = 0;
         float lower_min = FLT_MAX;
         bool order_ok = true;
@@ -336,48 +459,71 @@ __global__ void __launch_bounds__(NT, 2) router_kernel(const RouterArgs a)
             continue;
         }
 
-        // refine the candidates in double-word arithmetic
-        const uint16_t *xrow_p = a.X + static_cast<size_t>(t) * a.H;
-        for (int i = 0; i < NI; ++i) {
-            uint32_t m = __ballot_sync(kFullMask, (cand >> i) & 1u);
-            while (m) {
-                const int src = __ffs(m) - 1;
-                m &= m - 1;
-                const int e = src + 32 * i;
-                const double l64 = dot_double_word(xrow_p, a.Wg + static_cast<size_t>(e) * a.H, a.H, lane);
-                const double s64 = 1.0 / (1.0 + exp(-l64));
-                if (lane == src) w_s64[e] = s64 + static_cast<double>(a.bias[e]);
-            }
-        }
-        __syncwarp();
-        uint32_t taken2 = 0;
-        for (int j = 0; j < K; ++j) {
-            double bs = -DBL_MAX;
-            int be = INT_MAX;
+        // not certified: queue the candidates for the CTA-wide double-word refine
+        int base = 0;
+        if (lane == 0) base = atomicAdd(&s_npairs, n_cand);
+        base = __shfl_sync(kFullMask, base, 0);
+        if (base + n_cand <= a.max_pairs) {
+            int pos = base;
             for (int i = 0; i < NI; ++i) {
-                if (!((cand >> i) & 1u) || ((taken2 >> i) & 1u)) continue;
-                const int e = lane + 32 * i;
-                const double v = w_s64[e];
-                if (be == INT_MAX || before64(v, e, bs, be)) { bs = v; be = e; }
+                const bool c = (cand >> i) & 1u;
+                const uint32_t m = __ballot_sync(kFullMask, c);
+                if (c) {
+                    const int q = pos + __popc(m & ((1u << lane) - 1u));
+                    p_e[q] = lane + 32 * i;
+                    p_tok[q] = tl;
+                }
+                pos += __popc(m);
             }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const double os = __shfl_xor_sync(kFullMask, bs, off);
-                const int oe = __shfl_xor_sync(kFullMask, be, off);
-                if (oe != INT_MAX && (be == INT_MAX || before64(os, oe, bs, be))) { bs = os; be = oe; }
+            if (lane == 0) {
+                const int pi = atomicAdd(&s_npend, 1);
+                s_pend[3 * pi] = tl;
+                s_pend[3 * pi + 1] = base;
+                s_pend[3 * pi + 2] = n_cand;
             }
-            if ((be & 31) == lane) taken2 |= 1u << (be >> 5);
-            if (lane == 0) w_ord[j] = be;
+            __syncwarp();
+            continue;
+        }
+        // list full (pathological ties): retire the reserved in-range slots, then refine
+        // this token with the warp alone
+        for (int q = base + lane; q < a.max_pairs; q += 32) p_e[q] = -1;
+        const uint16_t *xrow_p = a.X + static_cast<size_t>(t) * a.H;
+        int nc = 0;
+        int *ce = reinterpret_cast<int *>(w_bnd);      // reuse: candidate experts
+        for (int i = 0; i < NI; ++i) {
+            const bool c = (cand >> i) & 1u;
+            const uint32_t m = __ballot_sync(kFullMask, c);
+            if (c) ce[nc + __popc(m & ((1u << lane) - 1u))] = lane + 32 * i;
+            nc += __popc(m);
         }
         __syncwarp();
-        double den = 0.0;
-        for (int j = 0; j < K; ++j) den += w_s64[w_ord[j]] - static_cast<double>(a.bias[w_ord[j]]);
-        for (int j = lane; j < K; j += 32) {
-            const int e = w_ord[j];
-            oi[j] = e;
-            ow[j] = static_cast<float>((w_s64[e] - static_cast<double>(a.bias[e])) / den);
+        for (int q = 0; q < nc; ++q) {
+            const int e = ce[q];
+            const double l64 = dot_double_word(xrow_p, a.Wg + static_cast<size_t>(e) * a.H, a.H, lane);
+            if (lane == 0) w_s64[q] = 1.0 / (1.0 + exp(-l64)) + static_cast<double>(a.bias[e]);
         }
         __syncwarp();
+        select_refined(ce, w_s64, nc, K, a.bias, oi, ow, w_ord, lane);
+    }
+    __syncthreads();
+
+    // CTA-wide refine: every warp takes (token, expert) pairs of the queued tokens
+    const int npairs = min(s_npairs, a.max_pairs);
+    for (int q = warp; q < npairs; q += NW) {
+        const int e = p_e[q];
+        if (e < 0) continue;
+        const int t = t0 + p_tok[q];
+        const double l64 = dot_double_word(a.X + static_cast<size_t>(t) * a.H,
+                                           a.Wg + static_cast<size_t>(e) * a.H, a.H, lane);
+        if (lane == 0) p_val[q] = 1.0 / (1.0 + exp(-l64)) + static_cast<double>(a.bias[e]);
+    }
+    __syncthreads();
+    for (int pi = warp; pi < s_npend; pi += NW) {
+        const int tl = s_pend[3 * pi], first = s_pend[3 * pi + 1], cnt = s_pend[3 * pi + 2];
+        const int t = t0 + tl;
+        select_refined(p_e + first, p_val + first, cnt, K, a.bias,
+                       a.topk_idx + static_cast<size_t>(t) * K, a.topk_w + static_cast<size_t>(t) * K,
+                       w_ord, lane);
     }
 }
 
@@ -386,23 +532,27 @@ __global__ void __launch_bounds__(NT, 2) router_kernel(const RouterArgs a)
 RouterPlan router_plan(int T, int H, int E)
 {
     RouterPlan p{};
-    p.TT = TT;
+    p.TT = T <= 4096 ? 16 : 64;
     p.TE = TE;
-    p.nTT = (T + TT - 1) / TT;
+    p.nTT = (T + p.TT - 1) / p.TT;
     p.nET = (E + TE - 1) / TE;
     p.S = H / KST;
     const int base = p.nTT * p.nET;
     const int target = 2 * num_sms();
     p.KS = 1;
-    while (p.KS * 2 <= p.S && p.KS < 16 && base * p.KS < target) p.KS *= 2;
+    while (p.KS * 2 <= p.S && p.KS < 8 && base * p.KS < target) p.KS *= 2;
     auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
     p.part_bytes = al(static_cast<size_t>(p.KS) * T * E * sizeof(float));
     p.xsq_bytes = al(static_cast<size_t>(p.KS) * T * sizeof(float));
     p.wsq_bytes = al(static_cast<size_t>(p.nTT) * p.KS * E * sizeof(float));
     p.cnt_bytes = al(static_cast<size_t>(p.nTT) * sizeof(unsigned));
-    const size_t gemm_smem = 2 * KST * (TT + TE) * sizeof(float);
-    const size_t fin_smem = static_cast<size_t>(NW) * E * (3 * sizeof(float) + sizeof(double)) +
-                            NW * 32 * sizeof(int);
+    const size_t gemm_smem = 2 * KST * (p.TT + TE) * sizeof(float);
+    p.max_pairs = 1024;
+    const size_t fin_smem = static_cast<size_t>(E) * sizeof(float) +
+                            static_cast<size_t>(NW) * 3 * E * sizeof(float) +
+                            NW * 32 * sizeof(int) + 2 * p.max_pairs * sizeof(int) + 16 +
+                            p.max_pairs * sizeof(double) +
+                            static_cast<size_t>(NW) * E * sizeof(double);
     p.smem_bytes = gemm_smem > fin_smem ? gemm_smem : fin_smem;
     return p;
 }
@@ -414,7 +564,9 @@ cudaError_t launch_router(const void *X, const void *Wg, const float *bias, int 
 {
     cudaError_t err = cudaMemsetAsync(scr.cnt, 0, static_cast<size_t>(plan.nTT) * sizeof(unsigned), s);
     if (err != cudaSuccess) return err;
-    err = ensure_smem(reinterpret_cast<const void *>(router_kernel), plan.smem_bytes);
+    const void *fn = plan.TT == 16 ? reinterpret_cast<const void *>(router_kernel<16>)
+                                   : reinterpret_cast<const void *>(router_kernel<64>);
+    err = ensure_smem(fn, plan.smem_bytes);
     if (err != cudaSuccess) return err;
     RouterArgs a{};
     a.X = static_cast<const uint16_t *>(X);
@@ -423,8 +575,12 @@ cudaError_t launch_router(const void *X, const void *Wg, const float *bias, int 
     a.T = T; a.H = H; a.E = E; a.K = K; a.KS = plan.KS; a.S = plan.S;
     a.part = scr.part; a.xsq = scr.xsq; a.wsq = scr.wsq; a.cnt = scr.cnt;
     a.topk_idx = topk_idx; a.topk_w = topk_w; a.status = status;
+    a.max_pairs = plan.max_pairs;
     dim3 grid(plan.nET, plan.nTT, plan.KS);
-    router_kernel<<<grid, NT, plan.smem_bytes, s>>>(a);
+    if (plan.TT == 16)
+        router_kernel<16><<<grid, NT, plan.smem_bytes, s>>>(a);
+    else
+        router_kernel<64><<<grid, NT, plan.smem_bytes, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -19,6 +19,7 @@ Workloads (DeepSeek-V3 shape: H=7168, E=256, K=8, I=I_shared=2048):
   skewed   T=8192, DeepSeek-V3 shape, 8 clusters of 32 co-activating experts with Zipf
            popularity (gate rows and tokens share cluster directions)
   prefill  T=16384, DeepSeek-V3 shape, bias = 0 (near-uniform routing), seed 0
+  profile  T=32, H=7168, E=32, K=8, I=I_shared=2048 (2.8 GB of experts; profiler captures)
 """
 from __future__ import annotations
 
@@ -55,6 +56,8 @@ WORKLOADS = {
     "skewed": Workload("skewed", T=8192, recipe="skewed", **DSV3),
     "prefill": Workload("prefill", T=16384, bias_range=0.0, **DSV3),
 }
+# small DeepSeek-V3-width case for profiler captures: 32 experts (2.8 GB), same tiles as decode
+WORKLOADS["profile"] = Workload("profile", T=32, H=7168, E=32, K=8, I=2048, Is=2048)
 SWEEP_T = (2, 4, 8, 16, 32, 64, 128, 256)
 for _t in SWEEP_T:
     WORKLOADS[f"sweep{_t}"] = Workload(f"sweep{_t}", T=_t, x_seed=_t, **DSV3)
@@ -159,7 +162,8 @@ def expert_weights_host(w: Workload) -> dict:
 
 
 def expert_weights_device(w: Workload, device):
-    """The same tensors drawn on the GPU with torch's generator (bf16 torch tensors)."""
+    """Tensors of the same shapes and distribution drawn on the GPU with torch's Philox
+    generator (bf16 torch tensors); the values differ from expert_weights_host."""
     import torch
     g = torch.Generator(device=device)
     out = {}

@@ -44,6 +44,7 @@ def test_exact_ties_duplicate_gate_rows():
     for a, b in ((1, 9), (4, 5), (0, 15)):
         r["W_gate"][b] = r["W_gate"][a]
         r["bias"][b] = r["bias"][a]
+    r["bias"][4] = r["bias"][5] = 2.0     # the tied pair is the top-2 of every token
     res = check_layer(Problem(w, routing=r))
     both = [row for row in res["idx"].tolist() if 4 in row and 5 in row]
     assert both and all(row.index(4) < row.index(5) for row in both)
