@@ -126,6 +126,26 @@ int moe_router_topk(const void *X, const void *W_gate, const float *bias,
                     int32_t *topk_idx, float *topk_w,
                     void *ws, size_t ws_bytes, void *stream);
 
+/* Router for callers that cannot allocate device memory.  No counterpart on the pages:
+ * this is a convenience of this library.  Same inputs, outputs and results as
+ * moe_router_topk, but without a workspace argument: the scratch lives in a fixed 4 MiB
+ * array that the library holds on every GPU that loads it, until the process exits.
+ * Meant for code that may not call cudaMalloc or a framework allocator -- a plug-in
+ * whose host application owns all device memory and hands out only the input and output
+ * buffers, or a path whose allocator is frozen after start-up.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current) and caches it; make that first call before any stream capture.
+ *   - Allocates and frees nothing.  Shapes whose router scratch does not fit in 4 MiB
+ *     return MOE_ERR_UNSUPPORTED_SHAPE before anything is enqueued (every T <= 2048 with
+ *     E <= 256 fits).
+ *   - All calls on a device share the one array and it keeps what the last call left;
+ *     the part that must start at zero is cleared on `stream` by every call.  Calls whose
+ *     work overlaps on the GPU (other streams, other host threads) race on the array:
+ *     serialise them. */
+int moe_router_topk_noalloc(const void *X, const void *W_gate, const float *bias,
+                            int T, int H, int E, int K,
+                            int32_t *topk_idx, float *topk_w, void *stream);
+
 /* Dispatch: the single-GPU counterpart of the AllToAll Dispatch ("Lower latency and higher
  * throughput...", Expert Parallelism; MoE Router: per-expert aggregated routing info).
  *   X        bf16 [T, H], topk_idx int32 [T, K] (values in [0, E), distinct per token)
