@@ -1,5 +1,5 @@
 // router.cu -- fused MoE router: gate GEMM -> sigmoid scoring -> selection bias -> top-k
-// -> renormalised weights, in one kernel.
+// -> renormalised weights.
 //
 // Method: "DeepSeek-V4.1-Flash" (vLLM article), section "Kernels", Mega-Gate: the gate
 // GEMM, expert scoring, bias and top-k selection run in one kernel instead of a GEMM plus
@@ -13,7 +13,8 @@
 //
 // Exactness.  The selection must be the one exact arithmetic gives.  bf16 x bf16 products
 // are exact in fp32, so the only error of the fp32 logit is the rounding of its sums.  The
-// summation here is a fixed tree in which every product passes through at most d
+// summation is a fixed tree in which every product passes through at most
+//     d = 32 (one 32-deep chain per shared-memory stage) + stages per split + splits + 2
 // additions, so |l_fp32 - l| <= gamma_d * sum|x_h w_h| <= gamma_d * ||x|| * ||w||
 // (Cauchy-Schwarz), gamma_d = d u / (1 - d u), u = 2^-24.  Propagating that bound through
 // the sigmoid and the bias add gives an interval per expert.  When the intervals certify
@@ -22,11 +23,14 @@
 // (error-free TwoSum accumulation of the exact products, ~2^-48 relative) with an fp64
 // sigmoid, and the top-k is taken again among those candidates.
 //
-// Structure.  Grid (expert tiles, token tiles, K splits).  Each CTA computes a TT x 64
-// tile of fp32 logits (TT = 16 tokens for small batches, 64 for large ones) over its slice
-// of H on the CUDA cores and writes it to the workspace; the last CTA of a token tile
-// (completion counter) sums the split-K partials in a fixed order, scores, selects and
-// writes the outputs -- one launch, no host sync.
+// Structure.  A grid (expert tiles, token tiles, K splits) of 256-thread CTAs computes
+// fp32 logit tiles on the CUDA cores into the workspace:
+//   small batches (T <= 4096): 16 tokens x 256 experts per CTA, 4x4 per thread;
+//   large batches:             128 tokens x 64 experts per CTA, 8x4 per thread.
+// Small batches: the last CTA of a token tile (completion counter) sums the split-K
+// partials in a fixed order, scores, selects and writes the outputs -- one launch.
+// Large batches: a second launch finalises, one warp per token, so the selection of
+// thousands of tokens is spread over the whole GPU instead of one CTA per token tile.
 #include <cfloat>
 #include <climits>
 
@@ -36,10 +40,10 @@
 namespace moe {
 namespace {
 
-constexpr int TE = 64;     // experts per CTA tile
 constexpr int KST = 32;    // k per shared-memory stage
 constexpr int NT = 256;    // threads
 constexpr int NW = NT / 32;
+constexpr int CH = 16;     // tokens per finalise chunk (two per warp)
 constexpr float kU = 5.9604644775390625e-8f;  // 2^-24
 
 struct RouterArgs {
@@ -56,6 +60,21 @@ struct RouterArgs {
     int max_pairs;   // capacity of the shared-memory refine list
 };
 
+// CTA tile: TT tokens x TE experts, TPT x EPT per thread, PF stages of loads in flight.
+template <int TT_, int TE_, int TPT_, int EPT_, int PF_>
+struct Cfg {
+    static constexpr int TT = TT_, TE = TE_, TPT = TPT_, EPT = EPT_, PF = PF_;
+    static constexpr int NTY = TT / TPT, NTX = TE / EPT;
+    static constexpr int LY = 4;                          // token groups per warp
+    static constexpr int XV = TT * 4, WV = TE * 4;        // 8-element vectors per stage
+    static constexpr int XPT = (XV + NT - 1) / NT, WPT = (WV + NT - 1) / NT;
+    static_assert(NTX * NTY == NT, "one output micro-tile per thread");
+    static_assert(NTY % LY == 0 && NTX % (32 / LY) == 0, "warp layout");
+    static_assert(EPT == 4 && TPT % 4 == 0, "float4 operand reads");
+};
+using SmallCfg = Cfg<16, 256, 4, 4, 2>;
+using LargeCfg = Cfg<128, 64, 8, 4, 2>;
+
 __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
 {
     f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
@@ -64,14 +83,17 @@ __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
     f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
 }
 
-// (sel, e) ranks before (sel2, e2): larger sel, then lower index.
-__device__ __forceinline__ bool before(float a, int ea, float b, int eb)
-{
-    return a > b || (a == b && ea < eb);
-}
 __device__ __forceinline__ bool before64(double a, int ea, double b, int eb)
 {
     return a > b || (a == b && ea < eb);
+}
+
+// Total order key of (sel, e): larger sel first, then lower expert index.
+__device__ __forceinline__ unsigned long long rank_key(float sel, int e)
+{
+    uint32_t u = __float_as_uint(sel + 0.0f);            // -0 -> +0
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);       // monotone float -> uint
+    return (static_cast<unsigned long long>(u) << 32) | static_cast<uint32_t>(~e);
 }
 
 // Error-free transformation: s + err == a + b exactly (Knuth's TwoSum).
@@ -102,24 +124,27 @@ __device__ __forceinline__ void dw_merge(float &hi, float &lo, float ohi, float 
 }
 
 // Double-word dot product of a bf16 token row and a bf16 gate row, reduced over the warp
-// in a fixed order; every lane returns the same value.  Four independent accumulators per
-// lane keep four 16-byte loads of each row in flight.
+// in a fixed order; every lane returns the same value.  Eight independent accumulators
+// per lane keep eight 16-byte loads of each row in flight.
 __device__ double dot_double_word(const uint16_t *x, const uint16_t *w, int H, int lane)
 {
+    constexpr int U = 8;
     const uint4 *xr = reinterpret_cast<const uint4 *>(x);
     const uint4 *wr = reinterpret_cast<const uint4 *>(w);
     const int nv = H / 8;
-    float hi[4] = {0.f, 0.f, 0.f, 0.f}, lo[4] = {0.f, 0.f, 0.f, 0.f};
-    int v = lane;
-    for (; v + 96 < nv; v += 128) {
-        uint4 xa[4], wa[4];
+    float hi[U], lo[U];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < U; ++u) { hi[u] = 0.f; lo[u] = 0.f; }
+    int v = lane;
+    for (; v + 32 * (U - 1) < nv; v += 32 * U) {
+        uint4 xa[U], wa[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
             xa[u] = __ldg(xr + v + 32 * u);
             wa[u] = __ldg(wr + v + 32 * u);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < U; ++u) {
             float xf[8], wf[8];
             unpack8(xa[u], xf);
             unpack8(wa[u], wf);
@@ -127,16 +152,27 @@ __device__ double dot_double_word(const uint16_t *x, const uint16_t *w, int H, i
             for (int i = 0; i < 8; ++i) dw_add(hi[u], lo[u], __fmul_rn(xf[i], wf[i]));  // exact product
         }
     }
-    for (; v < nv; v += 32) {
-        float xf[8], wf[8];
-        unpack8(__ldg(xr + v), xf);
-        unpack8(__ldg(wr + v), wf);
+    if (v < nv) {                          // tail: one predicated batch of loads
+        uint4 xa[U], wa[U];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) dw_add(hi[0], lo[0], __fmul_rn(xf[i], wf[i]));
+        for (int u = 0; u < U; ++u) {
+            const bool ok = v + 32 * u < nv;
+            xa[u] = ok ? __ldg(xr + v + 32 * u) : make_uint4(0, 0, 0, 0);
+            wa[u] = ok ? __ldg(wr + v + 32 * u) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float xf[8], wf[8];
+            unpack8(xa[u], xf);
+            unpack8(wa[u], wf);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dw_add(hi[u], lo[u], __fmul_rn(xf[i], wf[i]));
+        }
     }
-    dw_merge(hi[0], lo[0], hi[1], lo[1]);
-    dw_merge(hi[2], lo[2], hi[3], lo[3]);
-    dw_merge(hi[0], lo[0], hi[2], lo[2]);
+#pragma unroll
+    for (int step = 1; step < U; step <<= 1)
+#pragma unroll
+        for (int u = 0; u + step < U; u += 2 * step) dw_merge(hi[u], lo[u], hi[u + step], lo[u + step]);
     float h = hi[0], l = lo[0];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -148,16 +184,17 @@ __device__ double dot_double_word(const uint16_t *x, const uint16_t *w, int H, i
 }
 
 // Top-K of a token among `n` candidate (expert, sel64) pairs by (sel64 desc, expert asc);
-// writes the experts and their renormalised weights.  Warp-wide; pairs live in shared memory.
-__device__ void select_refined(const int *pe, const double *pv, int n, int K,
-                               const float *bias, int32_t *oi, float *ow, int *ord, int lane)
+// writes the experts and their renormalised weights.  Warp-wide; pairs live in shared
+// memory; taken pairs are marked by storing -1 - expert.
+__device__ void select_refined(int *pe, const double *pv, int n, int K, const float *bias,
+                               int32_t *oi, float *ow, int *ord, int lane)
 {
     for (int j = 0; j < K; ++j) {
         double bs = -DBL_MAX;
         int be = INT_MAX, bp = -1;
         for (int q = lane; q < n; q += 32) {
             const int e = pe[q];
-            if (e < 0) continue;                 // already taken
+            if (e < 0) continue;
             const double v = pv[q];
             if (be == INT_MAX || before64(v, e, bs, be)) { bs = v; be = e; bp = q; }
         }
@@ -170,7 +207,7 @@ __device__ void select_refined(const int *pe, const double *pv, int n, int K,
         }
         if (lane == 0) ord[j] = bp;
         __syncwarp();
-        if (lane == (bp & 31)) const_cast<int *>(pe)[bp] = -1 - be;   // mark taken, keep expert
+        if (lane == (bp & 31)) pe[bp] = -1 - be;
         __syncwarp();
     }
     double den = 0.0;
@@ -186,345 +223,570 @@ __device__ void select_refined(const int *pe, const double *pv, int n, int K,
     __syncwarp();
 }
 
-template <int TT>
-__global__ void __launch_bounds__(NT, 2) router_kernel(const RouterArgs a)
-{
-    constexpr int TPT = TT / 16;                   // tokens per thread in the tile GEMM
-    extern __shared__ __align__(16) unsigned char smem[];
-    __shared__ int s_last;
+// Bound constants of the summation tree: gamma_d and the inflation of computed norms.
+struct Bounds {
+    float gam, infl;
+    __device__ Bounds(int S, int KS, int H)
+    {
+        const int ns_max = (S + KS - 1) / KS;
+        const float depth = static_cast<float>(KST + ns_max + KS + 2);
+        gam = depth * kU / (1.f - depth * kU) * 1.0001f;
+        infl = 1.f + static_cast<float>(H + 16 + KS) * (2.f * kU) + 4.f * kU;
+    }
+};
 
+// Compare-and-swap for a descending order of 64-bit keys.
+__device__ __forceinline__ void cas_desc(unsigned long long &a, unsigned long long &b)
+{
+    const unsigned long long hi = a > b ? a : b, lo = a > b ? b : a;
+    a = hi;
+    b = lo;
+}
+
+// Sorts eight keys in descending order (Batcher's odd-even merge network, 19 comparators).
+__device__ __forceinline__ void sort8_desc(unsigned long long (&k)[8])
+{
+    cas_desc(k[0], k[1]); cas_desc(k[2], k[3]); cas_desc(k[4], k[5]); cas_desc(k[6], k[7]);
+    cas_desc(k[0], k[2]); cas_desc(k[1], k[3]); cas_desc(k[4], k[6]); cas_desc(k[5], k[7]);
+    cas_desc(k[1], k[2]); cas_desc(k[5], k[6]);
+    cas_desc(k[0], k[4]); cas_desc(k[1], k[5]); cas_desc(k[2], k[6]); cas_desc(k[3], k[7]);
+    cas_desc(k[2], k[4]); cas_desc(k[3], k[5]);
+    cas_desc(k[1], k[2]); cas_desc(k[3], k[4]); cas_desc(k[5], k[6]);
+}
+
+// Scores one token held by one warp and selects its top-K in fp32 with the certified
+// error bound.  `w_sel` holds the token's fp32 logits on entry (lane owns e = lane + 32i);
+// it is overwritten with sel, and w_bnd / w_sc receive the bound and the sigmoid.
+// Returns true when the result is certified and written; otherwise `cand` holds the
+// lane's candidate bits and `n_cand` their warp-wide count.
+__device__ bool score_select(int E, int K, float nx, const float *nw, const float *bias,
+                             float gam, float *w_sel, float *w_bnd, float *w_sc,
+                             int32_t *oi, float *ow, uint32_t &cand, int &n_cand, int lane)
+{
+    const int NI = (E + 31) / 32;
+    const bool fast = NI <= 8;                // keys of <= 256 experts fit in registers
+    unsigned long long key[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) key[i] = 0ull;
+    unsigned long long best = 0ull;           // generic path: lane's best untaken key
+    for (int i = 0; i < NI; ++i) {
+        const int e = lane + 32 * i;
+        if (e >= E) break;
+        const float l = w_sel[e];
+        const float bl = gam * nx * nw[e] + 1e-30f;
+        const float s = 1.f / (1.f + expf(-l));
+        const float sel = s + bias[e];
+        const float al = fabsf(l);
+        const float D = (al > bl) ? fminf(0.25f, __expf(-(al - bl)) * 1.01f) : 0.25f;
+        w_sel[e] = sel;
+        w_bnd[e] = bl * D + 4.f * kU + fabsf(sel) * (2.f * kU);
+        w_sc[e] = s;
+        const unsigned long long k = rank_key(sel, e);
+        if (fast) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (u == i) key[u] = k;
+        }
+        best = k > best ? k : best;
+    }
+    if (fast) sort8_desc(key);
+    __syncwarp();
+
+    uint32_t taken = 0;
+    float lower_min = FLT_MAX, prev_lo = 0.f, my_s = 0.f;
+    int my_e = 0;
+    bool order_ok = true;
+    for (int j = 0; j < K; ++j) {
+        // tournament over the lanes' heads (fast path: a lane's keys are kept sorted)
+        const unsigned long long head = fast ? key[0] : best;
+        unsigned long long win = head;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const unsigned long long o = __shfl_xor_sync(kFullMask, win, off);
+            win = o > win ? o : win;
+        }
+        const int e = static_cast<int>(~static_cast<uint32_t>(win));
+        if (fast) {
+            if (head == win) {                 // pop the winner's head
+#pragma unroll
+                for (int u = 0; u < 7; ++u) key[u] = key[u + 1];
+                key[7] = 0ull;
+            }
+        } else if ((e & 31) == lane) {         // generic: the owner rescans its entries
+            taken |= 1u << (e >> 5);
+            best = 0ull;
+            for (int i = 0; i < NI; ++i) {
+                const int f = lane + 32 * i;
+                if (f >= E) break;
+                if (taken & (1u << i)) continue;
+                const unsigned long long k = rank_key(w_sel[f], f);
+                best = k > best ? k : best;
+            }
+        }
+        const float ws = w_sel[e], wb = w_bnd[e];
+        if (lane == j) { my_e = e; my_s = w_sc[e]; }
+        const float lo = __fsub_rd(ws, wb), hi = __fadd_ru(ws, wb);
+        if (j > 0 && !(prev_lo > hi)) order_ok = false;
+        prev_lo = lo;
+        lower_min = fminf(lower_min, lo);
+    }
+    // candidates: every expert whose upper bound reaches the k-th lower bound
+    n_cand = 0;
+    cand = 0;
+    for (int i = 0; i < NI; ++i) {
+        const int e = lane + 32 * i;
+        const bool c = e < E && __fadd_ru(w_sel[e], w_bnd[e]) >= lower_min;
+        if (c) cand |= 1u << i;
+        n_cand += __popc(__ballot_sync(kFullMask, c));
+    }
+    if (n_cand == K && order_ok) {
+        float den = 0.f;
+        for (int j = 0; j < K; ++j) den += __shfl_sync(kFullMask, my_s, j);
+        if (lane < K) {
+            oi[lane] = my_e;
+            ow[lane] = my_s / den;
+        }
+        __syncwarp();
+        return true;
+    }
+    __syncwarp();
+    return false;
+}
+
+// Writes the lane-distributed candidate bits of a token as a compact expert list.
+__device__ int list_candidates(uint32_t cand, int E, int *out, int lane)
+{
+    const int NI = (E + 31) / 32;
+    int pos = 0;
+    for (int i = 0; i < NI; ++i) {
+        const bool c = (cand >> i) & 1u;
+        const uint32_t m = __ballot_sync(kFullMask, c);
+        if (c) out[pos + __popc(m & ((1u << lane) - 1u))] = lane + 32 * i;
+        pos += __popc(m);
+    }
+    __syncwarp();
+    return pos;
+}
+
+// ------------------------------------------------------------------------ tile GEMM
+// Computes the fp32 logit tile of CTA (et, tt, ks) and the squared norms of its slices.
+template <class C>
+__device__ void gemm_tile(const RouterArgs &a, unsigned char *smem)
+{
     const int et = blockIdx.x, tt = blockIdx.y, ks = blockIdx.z;
-    const int nET = gridDim.x;
-    const int tid = threadIdx.x;
-    const int t0 = tt * TT, e0 = et * TE;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = tt * C::TT, e0 = et * C::TE;
     const int s_beg = static_cast<int>(static_cast<long long>(ks) * a.S / a.KS);
     const int s_end = static_cast<int>(static_cast<long long>(ks + 1) * a.S / a.KS);
 
-    // ------------------------------------------------------------------ tile GEMM
     float *xs = reinterpret_cast<float *>(smem);   // [2][KST][TT]
-    float *wsm = xs + 2 * KST * TT;                // [2][KST][TE]
+    float *wsm = xs + 2 * KST * C::TT;             // [2][KST][TE]
 
-    // loaders: X tile = TT rows x 4 vectors of 8 bf16, W tile = 64 rows x 4 vectors
-    const bool xload = tid < TT * 4;
-    const int xr_row = tid % TT, xr_vec = tid / TT;
-    const int wr_row = tid & 63, wr_vec = tid >> 6;
-    const int xrow = t0 + xr_row, wrow = e0 + wr_row;
-    const bool xok = xload && xrow < a.T, wok = wrow < a.E;
-    const uint4 *xp = reinterpret_cast<const uint4 *>(a.X + static_cast<size_t>(xok ? xrow : 0) * a.H) + xr_vec;
-    const uint4 *wp = reinterpret_cast<const uint4 *>(a.Wg + static_cast<size_t>(wok ? wrow : 0) * a.H) + wr_vec;
-    float xsq = 0.f, wsq = 0.f;
-    uint4 xr = make_uint4(0, 0, 0, 0), wr = make_uint4(0, 0, 0, 0);
-
-    const int tx = tid & 15, ty = tid >> 4;        // compute: experts 4tx.., tokens TPT*ty..
-    float acc_mid[TPT * 4], acc_out[TPT * 4];
+    // loaders: vector q -> (row q % ROWS, 8-element group q / ROWS); consecutive threads
+    // take consecutive rows, so the transposed shared-memory stores do not conflict
+    const uint4 *xp[C::XPT];
+    bool xok[C::XPT];
 #pragma unroll
-    for (int p = 0; p < TPT * 4; ++p) { acc_mid[p] = 0.f; acc_out[p] = 0.f; }
+    for (int i = 0; i < C::XPT; ++i) {
+        const int q = tid + NT * i;
+        const int row = t0 + q % C::TT;
+        xok[i] = q < C::XV && row < a.T;
+        xp[i] = reinterpret_cast<const uint4 *>(a.X + static_cast<size_t>(xok[i] ? row : 0) * a.H) + q / C::TT;
+    }
+    const uint4 *wp[C::WPT];
+    bool wok[C::WPT];
+#pragma unroll
+    for (int i = 0; i < C::WPT; ++i) {
+        const int q = tid + NT * i;
+        const int row = e0 + q % C::TE;
+        wok[i] = q < C::WV && row < a.E;
+        wp[i] = reinterpret_cast<const uint4 *>(a.Wg + static_cast<size_t>(wok[i] ? row : 0) * a.H) + q / C::TE;
+    }
+    float xsq[C::XPT], wsq[C::WPT];
+#pragma unroll
+    for (int i = 0; i < C::XPT; ++i) xsq[i] = 0.f;
+#pragma unroll
+    for (int i = 0; i < C::WPT; ++i) wsq[i] = 0.f;
 
-    auto gload = [&](int s) {
-        xr = xok ? __ldg(xp + s * 4) : make_uint4(0, 0, 0, 0);
-        wr = wok ? __ldg(wp + s * 4) : make_uint4(0, 0, 0, 0);
+    uint4 rx[C::PF][C::XPT], rw[C::PF][C::WPT];    // register ring of prefetched stages
+    auto gload = [&](int j, int st) {
+#pragma unroll
+        for (int i = 0; i < C::XPT; ++i) rx[j][i] = xok[i] ? __ldg(xp[i] + st * 4) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int i = 0; i < C::WPT; ++i) rw[j][i] = wok[i] ? __ldg(wp[i] + st * 4) : make_uint4(0, 0, 0, 0);
     };
-    auto sstore = [&](int buf) {
-        float xf[8], wf[8];
-        unpack8(xr, xf);
-        unpack8(wr, wf);
-        float *wd = wsm + buf * KST * TE + (wr_vec * 8) * TE + wr_row;
+    auto sstore = [&](int j, int buf) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            wd[i * TE] = wf[i];
-            wsq = fmaf(wf[i], wf[i], wsq);
+        for (int i = 0; i < C::XPT; ++i) {
+            const int q = tid + NT * i;
+            if (q < C::XV) {
+                float f[8];
+                unpack8(rx[j][i], f);
+                float *d = xs + buf * KST * C::TT + ((q / C::TT) * 8) * C::TT + q % C::TT;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) { d[e * C::TT] = f[e]; xsq[i] = fmaf(f[e], f[e], xsq[i]); }
+            }
         }
-        if (xload) {
-            float *xd = xs + buf * KST * TT + (xr_vec * 8) * TT + xr_row;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                xd[i * TT] = xf[i];
-                xsq = fmaf(xf[i], xf[i], xsq);
+        for (int i = 0; i < C::WPT; ++i) {
+            const int q = tid + NT * i;
+            if (q < C::WV) {
+                float f[8];
+                unpack8(rw[j][i], f);
+                float *d = wsm + buf * KST * C::TE + ((q / C::TE) * 8) * C::TE + q % C::TE;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) { d[e * C::TE] = f[e]; wsq[i] = fmaf(f[e], f[e], wsq[i]); }
             }
         }
     };
 
-    if (s_beg < s_end) {
-        gload(s_beg);
-        sstore(0);
-    }
-    __syncthreads();
-    int buf = 0, nmid = 0;
-    for (int s = s_beg; s < s_end; ++s) {
-        if (s + 1 < s_end) gload(s + 1);
-        float acc_in[TPT * 4];
+    // output micro-tile of this thread: tokens TPT*ty.., experts EPT*tx..
+    constexpr int WY = C::NTY / C::LY;
+    const int ty = (warp % WY) * C::LY + (lane % C::LY);
+    const int tx = (warp / WY) * (32 / C::LY) + lane / C::LY;
+    float acc[C::TPT * C::EPT];
 #pragma unroll
-        for (int p = 0; p < TPT * 4; ++p) acc_in[p] = 0.f;
-        const float *xb = xs + buf * KST * TT + TPT * ty;
-        const float *wb = wsm + buf * KST * TE + 4 * tx;
-#pragma unroll 8
-        for (int kk = 0; kk < KST; ++kk) {
-            float xa[TPT];
-            if constexpr (TPT == 4) {
-                const float4 xv = *reinterpret_cast<const float4 *>(xb + kk * TT);
-                xa[0] = xv.x; xa[1] = xv.y; xa[2] = xv.z; xa[3] = xv.w;
-            } else {
-                xa[0] = xb[kk * TT];
-            }
-            const float4 wv = *reinterpret_cast<const float4 *>(wb + kk * TE);
-            const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-            for (int i = 0; i < TPT; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc_in[i * 4 + j] = fmaf(xa[i], wa[j], acc_in[i * 4 + j]);
-        }
-#pragma unroll
-        for (int p = 0; p < TPT * 4; ++p) acc_mid[p] += acc_in[p];
-        if (++nmid == 8) {
-#pragma unroll
-            for (int p = 0; p < TPT * 4; ++p) { acc_out[p] += acc_mid[p]; acc_mid[p] = 0.f; }
-            nmid = 0;
-        }
-        if (s + 1 < s_end) sstore(buf ^ 1);
-        __syncthreads();
-        buf ^= 1;
-    }
-#pragma unroll
-    for (int p = 0; p < TPT * 4; ++p) acc_out[p] += acc_mid[p];
+    for (int p = 0; p < C::TPT * C::EPT; ++p) acc[p] = 0.f;
 
 #pragma unroll
-    for (int i = 0; i < TPT; ++i) {
-        const int t = t0 + TPT * ty + i;
+    for (int j = 0; j < C::PF; ++j)
+        if (s_beg + j < s_end) gload(j, s_beg + j);
+    for (int s0 = s_beg; s0 < s_end; s0 += C::PF) {
+#pragma unroll
+        for (int j = 0; j < C::PF; ++j) {
+            const int st = s0 + j;
+            if (st < s_end) {
+                const int buf = st & 1;
+                sstore(j, buf);
+                if (st + C::PF < s_end) gload(j, st + C::PF);
+                __syncthreads();
+                // one 32-deep fp32 chain per (token, expert) for this stage, then added to
+                // the running sum of the split
+                float acc_in[C::TPT * C::EPT];
+#pragma unroll
+                for (int p = 0; p < C::TPT * C::EPT; ++p) acc_in[p] = 0.f;
+                const float *xb = xs + buf * KST * C::TT + C::TPT * ty;
+                const float *wb = wsm + buf * KST * C::TE + C::EPT * tx;
+#pragma unroll 4
+                for (int kk = 0; kk < KST; ++kk) {
+                    float xa[C::TPT];
+#pragma unroll
+                    for (int i4 = 0; i4 < C::TPT / 4; ++i4) {
+                        const float4 v = *reinterpret_cast<const float4 *>(xb + kk * C::TT + 4 * i4);
+                        xa[4 * i4] = v.x; xa[4 * i4 + 1] = v.y; xa[4 * i4 + 2] = v.z; xa[4 * i4 + 3] = v.w;
+                    }
+                    const float4 wv = *reinterpret_cast<const float4 *>(wb + kk * C::TE);
+                    const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                    for (int i = 0; i < C::TPT; ++i)
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj)
+                            acc_in[i * 4 + jj] = fmaf(xa[i], wa[jj], acc_in[i * 4 + jj]);
+                }
+#pragma unroll
+                for (int p = 0; p < C::TPT * C::EPT; ++p) acc[p] += acc_in[p];
+            }
+        }
+    }
+
+#pragma unroll
+    for (int i = 0; i < C::TPT; ++i) {
+        const int t = t0 + C::TPT * ty + i;
         if (t >= a.T) continue;
         float *dst = a.part + (static_cast<size_t>(ks) * a.T + t) * a.E;
+        const int e = e0 + C::EPT * tx;
+        if ((a.E & 3) == 0 && e + 3 < a.E) {
+            *reinterpret_cast<float4 *>(dst + e) =
+                make_float4(acc[i * 4], acc[i * 4 + 1], acc[i * 4 + 2], acc[i * 4 + 3]);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = e0 + 4 * tx + j;
-            if (e < a.E) dst[e] = acc_out[i * 4 + j];
+            for (int jj = 0; jj < 4; ++jj)
+                if (e + jj < a.E) dst[e + jj] = acc[i * 4 + jj];
         }
     }
 
-    // squared norms of this slice, reduced over the 4 loader threads of a row in order
+    // squared norms of this slice, reduced over the four 8-element groups of a row in order
+    __syncthreads();
+    float *rxs = xs;                   // [4][TT]
+    float *rws = xs + 4 * C::TT;       // [4][TE]
+#pragma unroll
+    for (int i = 0; i < C::XPT; ++i) {
+        const int q = tid + NT * i;
+        if (q < C::XV) rxs[q] = xsq[i];
+    }
+#pragma unroll
+    for (int i = 0; i < C::WPT; ++i) {
+        const int q = tid + NT * i;
+        if (q < C::WV) rws[q] = wsq[i];
+    }
+    __syncthreads();
+    for (int r = tid; r < C::TT; r += NT) {
+        const float sx = ((rxs[r] + rxs[C::TT + r]) + rxs[2 * C::TT + r]) + rxs[3 * C::TT + r];
+        if (et == 0 && t0 + r < a.T) a.xsq[static_cast<size_t>(ks) * a.T + t0 + r] = sx;
+    }
+    for (int r = tid; r < C::TE; r += NT) {
+        const float sw = ((rws[r] + rws[C::TE + r]) + rws[2 * C::TE + r]) + rws[3 * C::TE + r];
+        if (e0 + r < a.E) a.wsq[(static_cast<size_t>(tt) * a.KS + ks) * a.E + e0 + r] = sw;
+    }
+}
+
+// Shared-memory layout of the finalise step (after the GEMM tile is done with smem).
+struct FinSmem {
+    float *nw, *bias, *nxs, *L;        // [E], [E], [CH], [CH][E]
+    float *sel, *bnd, *sc;             // per warp [E] each
+    int *ord, *ce;                     // per warp [32], [E]
+    int *p_e, *p_tok;                  // refine list [max_pairs]
+    double *p_val, *s64;               // [max_pairs], per warp [E]
+
+    __device__ FinSmem(unsigned char *smem, int E, int max_pairs, int warp)
     {
-        float *rx = xs;            // [4][TT]
-        float *rw = xs + 4 * TT;   // [4][64]
-        if (xload) rx[xr_vec * TT + xr_row] = xsq;
-        rw[wr_vec * 64 + wr_row] = wsq;
-        __syncthreads();
-        if (tid < TT) {
-            const float sx = ((rx[tid] + rx[TT + tid]) + rx[2 * TT + tid]) + rx[3 * TT + tid];
-            if (et == 0 && t0 + tid < a.T) a.xsq[static_cast<size_t>(ks) * a.T + t0 + tid] = sx;
-        }
-        if (tid < 64) {
-            const float sw = ((rw[tid] + rw[64 + tid]) + rw[128 + tid]) + rw[192 + tid];
-            if (e0 + tid < a.E)
-                a.wsq[(static_cast<size_t>(tt) * a.KS + ks) * a.E + e0 + tid] = sw;
-        }
+        float *f = reinterpret_cast<float *>(smem);
+        nw = f; f += E;
+        bias = f; f += E;
+        nxs = f; f += CH;
+        L = f; f += CH * E;
+        sel = f + static_cast<size_t>(warp) * 3 * E;
+        bnd = sel + E;
+        sc = bnd + E;
+        f += NW * 3 * E;
+        int *i = reinterpret_cast<int *>(f);
+        ord = i + warp * 32; i += NW * 32;
+        ce = i + static_cast<size_t>(warp) * E; i += NW * E;
+        p_e = i; i += max_pairs;
+        p_tok = i; i += max_pairs;
+        const uintptr_t d = (reinterpret_cast<uintptr_t>(i) + 7) & ~static_cast<uintptr_t>(7);
+        p_val = reinterpret_cast<double *>(d);
+        s64 = p_val + max_pairs + static_cast<size_t>(warp) * E;
     }
+    static size_t bytes(int E, int max_pairs)
+    {
+        return (2 * static_cast<size_t>(E) + CH + static_cast<size_t>(CH) * E +
+                static_cast<size_t>(NW) * 3 * E) * 4 +
+               (NW * 32 + static_cast<size_t>(NW) * E + 2 * static_cast<size_t>(max_pairs)) * 4 + 8 +
+               (static_cast<size_t>(max_pairs) + static_cast<size_t>(NW) * E) * 8;
+    }
+};
 
-    // ------------------------------------------------------------ last CTA finalises
+// Refines one token with its warp alone (used when the shared list is full, and by the
+// one-warp-per-token finaliser).
+__device__ void refine_token_warp(const RouterArgs &a, int t, uint32_t cand, int *ce,
+                                  double *s64, int *ord, int lane)
+{
+    const int nc = list_candidates(cand, a.E, ce, lane);
+    const uint16_t *xrow = a.X + static_cast<size_t>(t) * a.H;
+    for (int q = 0; q < nc; ++q) {
+        const int e = ce[q];
+        const double l64 = dot_double_word(xrow, a.Wg + static_cast<size_t>(e) * a.H, a.H, lane);
+        if (lane == 0) s64[q] = 1.0 / (1.0 + exp(-l64)) + static_cast<double>(a.bias[e]);
+    }
+    __syncwarp();
+    select_refined(ce, s64, nc, a.K, a.bias, a.topk_idx + static_cast<size_t>(t) * a.K,
+                   a.topk_w + static_cast<size_t>(t) * a.K, ord, lane);
+}
+
+// ------------------------------------------------------- fused kernel (small batches)
+template <class C>
+__global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ int s_last, s_npairs, s_npend;
+    __shared__ int s_pend[3 * C::TT];     // (token, first pair, pair count) to refine
+
+    gemm_tile<C>(a, smem);
+
+    // ---------------------------------------------------------- last CTA finalises
+    const int tt = blockIdx.y, tid = threadIdx.x;
     __threadfence();
     __syncthreads();
     if (tid == 0) {
         const unsigned prev = atomicAdd(&a.cnt[tt], 1u);
-        s_last = (prev == static_cast<unsigned>(nET * a.KS - 1));
+        s_last = (prev == static_cast<unsigned>(gridDim.x * a.KS - 1));
+        s_npairs = 0;
+        s_npend = 0;
     }
     __syncthreads();
     if (!s_last) return;
     __threadfence();
 
     const int warp = tid >> 5, lane = tid & 31;
-    const int E = a.E, K = a.K, KS = a.KS;
-    const int NI = (E + 31) / 32;
-    // depth of the summation tree (see the file comment) and the norm inflation
-    const int ns_max = (a.S + KS - 1) / KS;
-    const float depth = static_cast<float>(KST + 8 + (ns_max + 7) / 8 + 1 + KS + 2);
-    const float gam = depth * kU / (1.f - depth * kU) * 1.0001f;
-    const float infl = 1.f + static_cast<float>(a.H + 16 + KS) * (2.f * kU) + 4.f * kU;
-
-    // shared: nw[E] | per warp sel[E], bnd[E], sc[E] | per warp ord[32] | pair list
-    // (expert, sel64) of the tokens to refine | per warp sel64 scratch for overflow
-    float *nw = reinterpret_cast<float *>(smem);
-    float *w_sel = nw + E + static_cast<size_t>(warp) * 3 * E;
-    float *w_bnd = w_sel + E;
-    float *w_sc = w_bnd + E;
-    int *w_ord = reinterpret_cast<int *>(nw + E + static_cast<size_t>(NW) * 3 * E) + warp * 32;
-    int *p_e = reinterpret_cast<int *>(nw + E + static_cast<size_t>(NW) * 3 * E) + NW * 32;
-    int *p_tok = p_e + a.max_pairs;
-    unsigned char *after_i = reinterpret_cast<unsigned char *>(p_tok + a.max_pairs);
-    after_i = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(after_i) + 7) & ~static_cast<uintptr_t>(7));
-    double *p_val = reinterpret_cast<double *>(after_i);
-    double *w_s64 = p_val + a.max_pairs + static_cast<size_t>(warp) * E;   // overflow only
-    __shared__ int s_npairs, s_npend;
-    __shared__ int s_pend[3 * 64];      // (token, first pair, pair count) per pending token
-    if (tid == 0) { s_npairs = 0; s_npend = 0; }
-
-    // gate-row norms once per CTA (the K-split partial sums, added in order)
-    for (int e = tid; e < E; e += NT) {
+    const int E = a.E, KS = a.KS, t0 = tt * C::TT;
+    FinSmem S(smem, E, a.max_pairs, warp);
+    const Bounds bd(a.S, KS, a.H);
+    for (int e = tid; e < E; e += NT) {        // gate-row norms and biases, once per CTA
+        float w[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+            if (q < KS) w[q] = __ldcg(a.wsq + (static_cast<size_t>(tt) * KS + q) * E + e);
         float nw2 = 0.f;
-        for (int q = 0; q < KS; ++q) nw2 += a.wsq[(static_cast<size_t>(tt) * KS + q) * E + e];
-        nw[e] = sqrtf(nw2) * infl;
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+            if (q < KS) nw2 += w[q];
+        S.nw[e] = sqrtf(nw2) * bd.infl;
+        S.bias[e] = a.bias[e];
     }
-    __syncthreads();
 
-    for (int tl = warp; tl < TT; tl += NW) {
-        const int t = t0 + tl;
-        if (t >= a.T) break;
-        float nx2 = 0.f;
-        for (int q = 0; q < KS; ++q) nx2 += a.xsq[static_cast<size_t>(q) * a.T + t];
-        const float nx = sqrtf(nx2) * infl;
-
-        auto score = [&](int e, float l) {
-            const float bl = gam * nx * nw[e] + 1e-30f;
-            const float s = 1.f / (1.f + expf(-l));
-            const float sel = s + a.bias[e];
-            const float al = fabsf(l);
-            const float D = (al > bl) ? fminf(0.25f, expf(-(al - bl)) * 1.01f) : 0.25f;
-            w_sel[e] = sel;
-            w_bnd[e] = bl * D + 4.f * kU + fabsf(sel) * (2.f * kU);
-            w_sc[e] = s;
-        };
-        if ((E & 3) == 0) {
-            // coalesced float4 reads of the K-split partials, all issued before the sum
-            for (int g = lane; g < E / 4; g += 32) {
-                float4 v[16];
+    for (int c0 = 0; c0 < C::TT; c0 += CH) {
+        __syncthreads();
+        // K-split partials of the chunk's tokens -> shared logits (fixed order over splits)
+        const int n4 = (E & 3) == 0 ? E / 4 : 0;
+        if (n4) {
+            // up to 16 independent loads in flight per thread, added in split order
+            const size_t stride = static_cast<size_t>(a.T) * E / 4;
+            for (int it = tid; it < CH * n4; it += NT) {
+                const int tl = it / n4, g = it - tl * n4, t = t0 + c0 + tl;
+                if (t >= a.T) continue;
+                const float4 *src = reinterpret_cast<const float4 *>(a.part + static_cast<size_t>(t) * E) + g;
+                float4 w[16];
 #pragma unroll
                 for (int q = 0; q < 16; ++q)
-                    if (q < KS)
-                        v[q] = __ldcg(reinterpret_cast<const float4 *>(
-                                   a.part + (static_cast<size_t>(q) * a.T + t) * E) + g);
-                float4 l = v[0];
+                    if (q < KS) w[q] = __ldcg(src + q * stride);
+                float4 v = w[0];
 #pragma unroll
                 for (int q = 1; q < 16; ++q)
-                    if (q < KS) { l.x += v[q].x; l.y += v[q].y; l.z += v[q].z; l.w += v[q].w; }
-                score(4 * g, l.x);
-                score(4 * g + 1, l.y);
-                score(4 * g + 2, l.z);
-                score(4 * g + 3, l.w);
+                    if (q < KS) { v.x += w[q].x; v.y += w[q].y; v.z += w[q].z; v.w += w[q].w; }
+                *reinterpret_cast<float4 *>(S.L + tl * E + 4 * g) = v;
             }
         } else {
-            for (int e = lane; e < E; e += 32) {
-                float l = __ldcg(a.part + static_cast<size_t>(t) * E + e);
-                for (int q = 1; q < KS; ++q) l += __ldcg(a.part + (static_cast<size_t>(q) * a.T + t) * E + e);
-                score(e, l);
+            for (int it = tid; it < CH * E; it += NT) {
+                const int tl = it / E, e = it - tl * E, t = t0 + c0 + tl;
+                if (t >= a.T) continue;
+                float v = __ldcg(a.part + static_cast<size_t>(t) * E + e);
+                for (int q = 1; q < KS; ++q) v += __ldcg(a.part + (static_cast<size_t>(q) * a.T + t) * E + e);
+                S.L[tl * E + e] = v;
             }
         }
-        __syncwarp();
+        for (int tl = tid; tl < CH; tl += NT) {
+            const int t = t0 + c0 + tl;
+            if (t >= a.T) continue;
+            float n2 = 0.f;
+            for (int q = 0; q < KS; ++q) n2 += __ldcg(a.xsq + static_cast<size_t>(q) * a.T + t);
+            S.nxs[tl] = sqrtf(n2) * bd.infl;
+        }
+        __syncthreads();
 
-        // top-K by (sel desc, index asc); lane owns experts lane + 32 i
-        uint32_t taken = 0;
-        float lower_min = FLT_MAX;
-        bool order_ok = true;
-        float prev_lo = 0.f;
-        for (int j = 0; j < K; ++j) {
-            float bs = -FLT_MAX;
-            int be = INT_MAX;
-            for (int i = 0; i < NI; ++i) {
-                const int e = lane + 32 * i;
-                if (e >= E) break;
-                if (taken & (1u << i)) continue;
-                const float v = w_sel[e];
-                if (be == INT_MAX || before(v, e, bs, be)) { bs = v; be = e; }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float os = __shfl_xor_sync(kFullMask, bs, off);
-                const int oe = __shfl_xor_sync(kFullMask, be, off);
-                if (oe != INT_MAX && (be == INT_MAX || before(os, oe, bs, be))) { bs = os; be = oe; }
-            }
-            if ((be & 31) == lane) taken |= 1u << (be >> 5);
-            if (lane == 0) w_ord[j] = be;
-            const float bb = w_bnd[be];
-            const float lo = __fsub_rd(bs, bb), hi = __fadd_ru(bs, bb);
-            if (j > 0 && !(prev_lo > hi)) order_ok = false;
-            prev_lo = lo;
-            lower_min = fminf(lower_min, lo);
-        }
-        // candidates: every expert whose upper bound reaches the k-th lower bound
-        int n_cand = 0;
-        uint32_t cand = 0;
-        for (int i = 0; i < NI; ++i) {
-            const int e = lane + 32 * i;
-            const bool c = e < E && __fadd_ru(w_sel[e], w_bnd[e]) >= lower_min;
-            if (c) cand |= 1u << i;
-            n_cand += __popc(__ballot_sync(kFullMask, c));
-        }
-        __syncwarp();
-
-        int32_t *oi = a.topk_idx + static_cast<size_t>(t) * K;
-        float *ow = a.topk_w + static_cast<size_t>(t) * K;
-        if (n_cand == K && order_ok) {
-            float den = 0.f;
-            for (int j = 0; j < K; ++j) den += w_sc[w_ord[j]];
-            for (int j = lane; j < K; j += 32) {
-                oi[j] = w_ord[j];
-                ow[j] = w_sc[w_ord[j]] / den;
-            }
+        for (int tl = warp; tl < CH; tl += NW) {
+            const int t = t0 + c0 + tl;
+            if (t >= a.T) break;
+            for (int e = lane; e < E; e += 32) S.sel[e] = S.L[tl * E + e];
             __syncwarp();
-            continue;
-        }
-
-        // not certified: queue the candidates for the CTA-wide double-word refine
-        int base = 0;
-        if (lane == 0) base = atomicAdd(&s_npairs, n_cand);
-        base = __shfl_sync(kFullMask, base, 0);
-        if (base + n_cand <= a.max_pairs) {
-            int pos = base;
-            for (int i = 0; i < NI; ++i) {
-                const bool c = (cand >> i) & 1u;
-                const uint32_t m = __ballot_sync(kFullMask, c);
-                if (c) {
-                    const int q = pos + __popc(m & ((1u << lane) - 1u));
-                    p_e[q] = lane + 32 * i;
-                    p_tok[q] = tl;
+            uint32_t cand;
+            int n_cand;
+            int32_t *oi = a.topk_idx + static_cast<size_t>(t) * a.K;
+            float *ow = a.topk_w + static_cast<size_t>(t) * a.K;
+            if (score_select(E, a.K, S.nxs[tl], S.nw, S.bias, bd.gam, S.sel, S.bnd, S.sc,
+                             oi, ow, cand, n_cand, lane))
+                continue;
+            // not certified: queue the candidates for the CTA-wide double-word refine
+            int base = 0;
+            if (lane == 0) base = atomicAdd(&s_npairs, n_cand);
+            base = __shfl_sync(kFullMask, base, 0);
+            if (base + n_cand <= a.max_pairs) {
+                list_candidates(cand, E, S.p_e + base, lane);
+                for (int q = lane; q < n_cand; q += 32) S.p_tok[base + q] = c0 + tl;
+                if (lane == 0) {
+                    const int pi = atomicAdd(&s_npend, 1);
+                    s_pend[3 * pi] = c0 + tl;
+                    s_pend[3 * pi + 1] = base;
+                    s_pend[3 * pi + 2] = n_cand;
                 }
-                pos += __popc(m);
+                __syncwarp();
+                continue;
             }
-            if (lane == 0) {
-                const int pi = atomicAdd(&s_npend, 1);
-                s_pend[3 * pi] = tl;
-                s_pend[3 * pi + 1] = base;
-                s_pend[3 * pi + 2] = n_cand;
-            }
+            // list full (pathological ties): retire the reserved in-range slots, then
+            // refine this token with the warp alone
+            for (int q = base + lane; q < a.max_pairs; q += 32) S.p_e[q] = -1;
             __syncwarp();
-            continue;
+            refine_token_warp(a, t, cand, S.ce, S.s64, S.ord, lane);
         }
-        // list full (pathological ties): retire the reserved in-range slots, then refine
-        // this token with the warp alone
-        for (int q = base + lane; q < a.max_pairs; q += 32) p_e[q] = -1;
-        const uint16_t *xrow_p = a.X + static_cast<size_t>(t) * a.H;
-        int nc = 0;
-        int *ce = reinterpret_cast<int *>(w_bnd);      // reuse: candidate experts
-        for (int i = 0; i < NI; ++i) {
-            const bool c = (cand >> i) & 1u;
-            const uint32_t m = __ballot_sync(kFullMask, c);
-            if (c) ce[nc + __popc(m & ((1u << lane) - 1u))] = lane + 32 * i;
-            nc += __popc(m);
-        }
-        __syncwarp();
-        for (int q = 0; q < nc; ++q) {
-            const int e = ce[q];
-            const double l64 = dot_double_word(xrow_p, a.Wg + static_cast<size_t>(e) * a.H, a.H, lane);
-            if (lane == 0) w_s64[q] = 1.0 / (1.0 + exp(-l64)) + static_cast<double>(a.bias[e]);
-        }
-        __syncwarp();
-        select_refined(ce, w_s64, nc, K, a.bias, oi, ow, w_ord, lane);
     }
     __syncthreads();
 
     // CTA-wide refine: every warp takes (token, expert) pairs of the queued tokens
     const int npairs = min(s_npairs, a.max_pairs);
     for (int q = warp; q < npairs; q += NW) {
-        const int e = p_e[q];
+        const int e = S.p_e[q];
         if (e < 0) continue;
-        const int t = t0 + p_tok[q];
+        const int t = t0 + S.p_tok[q];
         const double l64 = dot_double_word(a.X + static_cast<size_t>(t) * a.H,
                                            a.Wg + static_cast<size_t>(e) * a.H, a.H, lane);
-        if (lane == 0) p_val[q] = 1.0 / (1.0 + exp(-l64)) + static_cast<double>(a.bias[e]);
+        if (lane == 0) S.p_val[q] = 1.0 / (1.0 + exp(-l64)) + static_cast<double>(a.bias[e]);
     }
     __syncthreads();
     for (int pi = warp; pi < s_npend; pi += NW) {
         const int tl = s_pend[3 * pi], first = s_pend[3 * pi + 1], cnt = s_pend[3 * pi + 2];
         const int t = t0 + tl;
-        select_refined(p_e + first, p_val + first, cnt, K, a.bias,
-                       a.topk_idx + static_cast<size_t>(t) * K, a.topk_w + static_cast<size_t>(t) * K,
-                       w_ord, lane);
+        select_refined(S.p_e + first, S.p_val + first, cnt, a.K, a.bias,
+                       a.topk_idx + static_cast<size_t>(t) * a.K,
+                       a.topk_w + static_cast<size_t>(t) * a.K, S.ord, lane);
     }
+}
+
+// ------------------------------------------- GEMM-only kernel + finaliser (large batches)
+template <class C>
+__global__ void __launch_bounds__(NT, 2) router_gemm_kernel(const RouterArgs a)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    gemm_tile<C>(a, smem);
+}
+
+// One warp per token: split-K sum, scoring, certified top-K, refine when needed.
+__global__ void __launch_bounds__(NT) router_finalize_kernel(const RouterArgs a, int TT)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * NW + warp;
+    const int E = a.E, KS = a.KS;
+    float *fb = reinterpret_cast<float *>(smem);
+    float *w_sel = fb + static_cast<size_t>(warp) * 4 * E;
+    float *w_bnd = w_sel + E, *w_sc = w_bnd + E, *w_nw = w_sc + E;
+    int *ib = reinterpret_cast<int *>(fb + static_cast<size_t>(NW) * 4 * E);
+    int *ce = ib + static_cast<size_t>(warp) * E;
+    int *ord = ib + static_cast<size_t>(NW) * E + warp * 32;
+    const uintptr_t d = reinterpret_cast<uintptr_t>(ib + static_cast<size_t>(NW) * E + NW * 32);
+    double *s64 = reinterpret_cast<double *>((d + 7) & ~static_cast<uintptr_t>(7)) +
+                  static_cast<size_t>(warp) * E;
+    if (t >= a.T) return;
+    const Bounds bd(a.S, KS, a.H);
+    const int tt = t / TT;
+    const float part_sq = lane < KS ? __ldcg(a.xsq + static_cast<size_t>(lane) * a.T + t) : 0.f;
+    float n2 = 0.f;
+    for (int q = 0; q < KS; ++q) n2 += __shfl_sync(kFullMask, part_sq, q);
+    const float nx = sqrtf(n2) * bd.infl;
+    for (int e = lane; e < E; e += 32) {
+        float pv[16], pn[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+            if (q < KS) {
+                pv[q] = __ldcg(a.part + (static_cast<size_t>(q) * a.T + t) * E + e);
+                pn[q] = __ldcg(a.wsq + (static_cast<size_t>(tt) * KS + q) * E + e);
+            }
+        float v = pv[0], n = pn[0];
+#pragma unroll
+        for (int q = 1; q < 16; ++q)
+            if (q < KS) { v += pv[q]; n += pn[q]; }
+        w_sel[e] = v;
+        w_nw[e] = sqrtf(n) * bd.infl;
+    }
+    __syncwarp();
+    uint32_t cand;
+    int n_cand;
+    int32_t *oi = a.topk_idx + static_cast<size_t>(t) * a.K;
+    float *ow = a.topk_w + static_cast<size_t>(t) * a.K;
+    if (score_select(E, a.K, nx, w_nw, a.bias, bd.gam, w_sel, w_bnd, w_sc, oi, ow, cand, n_cand, lane))
+        return;
+    refine_token_warp(a, t, cand, ce, s64, ord, lane);
+}
+
+size_t fused_smem(int TT, int TE, int E, int max_pairs)
+{
+    const size_t g = 2 * KST * static_cast<size_t>(TT + TE) * sizeof(float);
+    const size_t f = FinSmem::bytes(E, max_pairs);
+    return (g > f ? g : f) + 16;
+}
+
+size_t finalize_smem(int E)
+{
+    return static_cast<size_t>(NW) * 5 * E * 4 + NW * 32 * 4 + 8 + static_cast<size_t>(NW) * E * 8;
 }
 
 }  // namespace
@@ -532,28 +794,26 @@ __global__ void __launch_bounds__(NT, 2) router_kernel(const RouterArgs a)
 RouterPlan router_plan(int T, int H, int E)
 {
     RouterPlan p{};
-    p.TT = T <= 4096 ? 16 : 64;
-    p.TE = TE;
+    const bool small = T <= 4096;
+    p.TT = small ? SmallCfg::TT : LargeCfg::TT;
+    p.TE = small ? SmallCfg::TE : LargeCfg::TE;
     p.nTT = (T + p.TT - 1) / p.TT;
-    p.nET = (E + TE - 1) / TE;
+    p.nET = (E + p.TE - 1) / p.TE;
     p.S = H / KST;
     const int base = p.nTT * p.nET;
     const int target = 2 * num_sms();
-    p.KS = 1;
-    while (p.KS * 2 <= p.S && p.KS < 8 && base * p.KS < target) p.KS *= 2;
+    // at most 32 stages per split keeps the summation depth (and the error bound) small
+    p.KS = (p.S + 31) / 32;
+    if (p.KS > 16) p.KS = 16;
+    while (p.KS * 2 <= p.S && p.KS * 2 <= 16 && base * p.KS < target) p.KS *= 2;
+    p.max_pairs = 1024;
     auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
     p.part_bytes = al(static_cast<size_t>(p.KS) * T * E * sizeof(float));
     p.xsq_bytes = al(static_cast<size_t>(p.KS) * T * sizeof(float));
     p.wsq_bytes = al(static_cast<size_t>(p.nTT) * p.KS * E * sizeof(float));
     p.cnt_bytes = al(static_cast<size_t>(p.nTT) * sizeof(unsigned));
-    const size_t gemm_smem = 2 * KST * (p.TT + TE) * sizeof(float);
-    p.max_pairs = 1024;
-    const size_t fin_smem = static_cast<size_t>(E) * sizeof(float) +
-                            static_cast<size_t>(NW) * 3 * E * sizeof(float) +
-                            NW * 32 * sizeof(int) + 2 * p.max_pairs * sizeof(int) + 16 +
-                            p.max_pairs * sizeof(double) +
-                            static_cast<size_t>(NW) * E * sizeof(double);
-    p.smem_bytes = gemm_smem > fin_smem ? gemm_smem : fin_smem;
+    p.smem_bytes = small ? fused_smem(p.TT, p.TE, E, p.max_pairs)
+                         : 2 * KST * static_cast<size_t>(p.TT + p.TE) * sizeof(float) + 16;
     return p;
 }
 
@@ -562,12 +822,6 @@ cudaError_t launch_router(const void *X, const void *Wg, const float *bias, int 
                           const RouterPlan &plan, const RouterScratch &scr, int *status,
                           cudaStream_t s)
 {
-    cudaError_t err = cudaMemsetAsync(scr.cnt, 0, static_cast<size_t>(plan.nTT) * sizeof(unsigned), s);
-    if (err != cudaSuccess) return err;
-    const void *fn = plan.TT == 16 ? reinterpret_cast<const void *>(router_kernel<16>)
-                                   : reinterpret_cast<const void *>(router_kernel<64>);
-    err = ensure_smem(fn, plan.smem_bytes);
-    if (err != cudaSuccess) return err;
     RouterArgs a{};
     a.X = static_cast<const uint16_t *>(X);
     a.Wg = static_cast<const uint16_t *>(Wg);
@@ -577,10 +831,23 @@ cudaError_t launch_router(const void *X, const void *Wg, const float *bias, int 
     a.topk_idx = topk_idx; a.topk_w = topk_w; a.status = status;
     a.max_pairs = plan.max_pairs;
     dim3 grid(plan.nET, plan.nTT, plan.KS);
-    if (plan.TT == 16)
-        router_kernel<16><<<grid, NT, plan.smem_bytes, s>>>(a);
-    else
-        router_kernel<64><<<grid, NT, plan.smem_bytes, s>>>(a);
+    cudaError_t err;
+    if (plan.TT == SmallCfg::TT) {
+        err = cudaMemsetAsync(scr.cnt, 0, static_cast<size_t>(plan.nTT) * sizeof(unsigned), s);
+        if (err != cudaSuccess) return err;
+        err = ensure_smem(reinterpret_cast<const void *>(router_fused_kernel<SmallCfg>), plan.smem_bytes);
+        if (err != cudaSuccess) return err;
+        router_fused_kernel<SmallCfg><<<grid, NT, plan.smem_bytes, s>>>(a);
+        return cudaGetLastError();
+    }
+    err = ensure_smem(reinterpret_cast<const void *>(router_gemm_kernel<LargeCfg>), plan.smem_bytes);
+    if (err != cudaSuccess) return err;
+    router_gemm_kernel<LargeCfg><<<grid, NT, plan.smem_bytes, s>>>(a);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    const size_t fs = finalize_smem(E);
+    err = ensure_smem(reinterpret_cast<const void *>(router_finalize_kernel), fs);
+    if (err != cudaSuccess) return err;
+    router_finalize_kernel<<<(T + NW - 1) / NW, NT, fs, s>>>(a, plan.TT);
     return cudaGetLastError();
 }
 

@@ -22,7 +22,7 @@
 namespace moe {
 namespace {
 
-constexpr size_t kRouterScratchBytes = size_t(4) << 20;  // 4 MiB per GPU
+constexpr size_t kRouterScratchBytes = size_t(16) << 20;  // 16 MiB per GPU
 constexpr size_t kStatusBytes = 256;                      // status word + padding
 constexpr int kMaxDevices = 64;
 

@@ -128,16 +128,16 @@ int moe_router_topk(const void *X, const void *W_gate, const float *bias,
 
 /* Router for callers that cannot allocate device memory.  No counterpart on the pages:
  * this is a convenience of this library.  Same inputs, outputs and results as
- * moe_router_topk, but without a workspace argument: the scratch lives in a fixed 4 MiB
+ * moe_router_topk, but without a workspace argument: the scratch lives in a fixed 16 MiB
  * array that the library holds on every GPU that loads it, until the process exits.
  * Meant for code that may not call cudaMalloc or a framework allocator -- a plug-in
  * whose host application owns all device memory and hands out only the input and output
  * buffers, or a path whose allocator is frozen after start-up.
  *   - The first call on a device looks up the array's device address (with that device
  *     current) and caches it; make that first call before any stream capture.
- *   - Allocates and frees nothing.  Shapes whose router scratch does not fit in 4 MiB
+ *   - Allocates and frees nothing.  Shapes whose router scratch does not fit in 16 MiB
  *     return MOE_ERR_UNSUPPORTED_SHAPE before anything is enqueued (every T <= 2048 with
- *     E <= 256 fits).
+ *     E <= 256 and H <= 7168 fits).
  *   - All calls on a device share the one array and it keeps what the last call left;
  *     the part that must start at zero is cleared on `stream` by every call.  Calls whose
  *     work overlaps on the GPU (other streams, other host threads) race on the array:

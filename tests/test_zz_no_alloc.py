@@ -59,8 +59,8 @@ def _without_workspace(f, w, X, Wg, bias):
 
 def test_noalloc_router_matches_workspace_router_twice():
     f = _noalloc()
-    # two calls in a row on different batches: the second must not see the first's scratch
-    for T, x_seed in ((128, 0), (77, 5)):
+    # calls in a row on different batches: a call must not see an earlier call's scratch
+    for T, x_seed in ((128, 0), (77, 5), (2048, 9)):   # 2048: the documented upper end
         w, X, Wg, bias = _inputs(T, x_seed)
         ref_idx, ref_w = _with_workspace(w, X, Wg, bias)
         idx, wt = _without_workspace(f, w, X, Wg, bias)
@@ -72,7 +72,7 @@ def test_noalloc_router_matches_workspace_router_twice():
 def test_noalloc_router_rejects_shapes_beyond_its_scratch():
     f = _noalloc()
     w, X, Wg, bias = _inputs(128, 0)
-    # 65536 tokens need far more than the fixed 4 MiB of router scratch; rejected on the
+    # 65536 tokens need far more than the fixed 16 MiB of router scratch; rejected on the
     # host before anything is enqueued (the pointers are never dereferenced)
     rc = f(ctypes.c_void_p(X.data_ptr()), ctypes.c_void_p(Wg.data_ptr()),
            ctypes.c_void_p(bias.data_ptr()), 65536, w.H, w.E, w.K,
