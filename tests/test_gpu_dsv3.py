@@ -38,3 +38,9 @@ def test_batch_sweep(dsv3_weights, T):
 def test_prefill_T16384(dsv3_weights):
     w = synth.workload("prefill")
     check_layer(Problem(w, weights_dev=dsv3_weights), tokens=_sample(w.T, 2))
+
+
+def test_skewed_T8192(dsv3_weights):
+    w = synth.workload("skewed")
+    r = check_layer(Problem(w, weights_dev=dsv3_weights), tokens=_sample(w.T, 2))
+    assert r["disp"]["counts"].max() >= 0.95 * w.T  # the most popular experts: nearly every token
