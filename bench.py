@@ -5,8 +5,8 @@ expert -> combine) on GB300, through the C ABI.
 Default workload: the DeepSeek-V3-shaped decode step, T = 128 tokens (64 requests x query
 length 2), H = 7168, E = 256 routed experts, top-8, I = 2048, one shared expert I = 2048,
 bf16 weights (22.5 GB of routed experts) and activations, fp32 output.  Inputs are seeded
-synthetic tensors already resident in HBM; the active experts' weights (~22 GB per step)
-are far larger than L2, so every step streams them from HBM.
+synthetic tensors already resident in HBM; the activated experts' weights (13.2 GB per
+step at T=128) are far larger than L2, so every step streams them from HBM.
 
 One JSON line on rank 0.  `--impl reference` times the fp64 CPU oracle instead (the
 reference arm), on a bounded sample of the same workload.
@@ -132,6 +132,26 @@ def algorithmic(w, n_act: int):
     return b, f, layer_bytes, layer_flops
 
 
+# ------------------------------------------------------------------- replica helpers
+def replica_workload(name: str, rank: int):
+    """The workload a replica runs: rank 0 runs the canonical batch, rank r > 0 the same
+    shapes and weights with its own tokens (X seed shifted by 7919 r)."""
+    from expert_routed_ffn_router_gb300 import synth
+    w = synth.workload(name)
+    return w if rank == 0 else synth.workload(name, x_seed=w.x_seed + 7919 * rank)
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank timing over the process group (identity without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ----------------------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local_rank):
     import numpy as np
@@ -143,9 +163,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     B.load()
-    w = synth.workload(args.workload)
-    if rank:
-        w = synth.workload(args.workload, x_seed=w.x_seed + 7919 * rank)
+    w = replica_workload(args.workload, rank)
     routing = synth.routing_inputs(w)
     weights = synth.expert_weights_device(w, dev)
     weights["W_gate"] = torch.from_numpy(routing["W_gate"].view(np.int16)).view(torch.bfloat16).to(dev)
@@ -189,11 +207,7 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     t_wall1 = time.time()
     B.moe_debug_set_stage_events(None)
-    ms = ev0.elapsed_time(ev1) / K
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / K, dev)
     stage_ms = {name: statistics.fmean(stage_ev[k][i].elapsed_time(stage_ev[k][i + 1])
                                        for k in range(K))
                 for i, name in enumerate(STAGES)}
@@ -220,11 +234,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     sampler.stop()
-    ms_e2e = e0.elapsed_time(e1) / K
-    if world > 1:
-        t = torch.tensor([ms_e2e], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / K, dev)
 
     counts = layer.counts.cpu().numpy()
     n_act = int((counts > 0).sum())

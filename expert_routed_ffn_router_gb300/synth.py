@@ -20,6 +20,7 @@ Workloads (DeepSeek-V3 shape: H=7168, E=256, K=8, I=I_shared=2048):
            popularity (gate rows and tokens share cluster directions)
   prefill  T=16384, DeepSeek-V3 shape, bias = 0 (near-uniform routing), seed 0
   profile  T=32, H=7168, E=32, K=8, I=I_shared=2048 (2.8 GB of experts; profiler captures)
+  profile_large  T=4096 with the same 32 experts, bias 0 (prefill-like tiles; captures)
 """
 from __future__ import annotations
 
@@ -58,6 +59,9 @@ WORKLOADS = {
 }
 # small DeepSeek-V3-width case for profiler captures: 32 experts (2.8 GB), same tiles as decode
 WORKLOADS["profile"] = Workload("profile", T=32, H=7168, E=32, K=8, I=2048, Is=2048)
+# ... and its tensor-bound counterpart: 1024 rows per expert, the tiles of prefill
+WORKLOADS["profile_large"] = Workload("profile_large", T=4096, H=7168, E=32, K=8, I=2048,
+                                      Is=2048, bias_range=0.0)
 SWEEP_T = (2, 4, 8, 16, 32, 64, 128, 256)
 for _t in SWEEP_T:
     WORKLOADS[f"sweep{_t}"] = Workload(f"sweep{_t}", T=_t, x_seed=_t, **DSV3)

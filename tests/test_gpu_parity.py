@@ -32,6 +32,9 @@ def test_tiny_layer():
     (300, 192, 40, 5, 192, 64),     # H % 128 == 64, E not a multiple of 32, K = 5
     (130, 128, 8, 8, 64, 0),        # K == E (every expert, order only), no shared expert
     (513, 256, 64, 6, 256, 128),    # several dispatch chunks
+    (513, 256, 8, 6, 128, 128),     # 385 rows per expert: 256-row token tiles
+    (700, 192, 16, 4, 192, 64),     # 256-row tiles, odd weight-tile counts (3 up, 2 down)
+    (128, 128, 16, 2, 128, 0),      # 16 rows per expert: 128-row token tiles
 ])
 def test_ragged_shapes(T, H, E, K, I, Is):
     w = synth.Workload("rag", T=T, H=H, E=E, K=K, I=I, Is=Is, seed=T, x_seed=T + 1)
