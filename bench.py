@@ -132,6 +132,16 @@ def algorithmic(w, n_act: int):
     return b, f, layer_bytes, layer_flops
 
 
+def launches_per_step(T: int, with_affinity: bool) -> int:
+    """Kernels moe_layer_forward launches: router (1 fused, or GEMM + finalise for
+    T > 4096), dispatch (one bookkeeping CTA for T <= 256, else masks, scan, scatter;
+    then the affinity matrix when asked for, and the row gather), the FFN up and down
+    launches, combine."""
+    router = 1 if T <= 4096 else 2
+    dispatch = (1 if T <= 256 else 3) + (1 if with_affinity else 0) + 1
+    return router + dispatch + 2 + 1
+
+
 # ------------------------------------------------------------------- replica helpers
 def replica_workload(name: str, rank: int):
     """The workload a replica runs: rank 0 runs the canonical batch, rank r > 0 the same
@@ -273,7 +283,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(total_tokens / (ms_e2e / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(Xh.numel() * Xh.element_size()),
                 "d2h_bytes_per_step": int(Yh.numel() * Yh.element_size())},
-        "gpu_launches": K * 9,
+        "gpu_launches": K * launches_per_step(w.T, with_affinity=True),
         "roofline": roof,
         "layer_roofline": {"algorithmic_bytes": int(layer_bytes),
                            "hbm_frac": round(layer_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),

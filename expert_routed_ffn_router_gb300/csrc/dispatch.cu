@@ -194,6 +194,90 @@ __global__ void __launch_bounds__(256) affinity_kernel(const uint32_t *__restric
     }
 }
 
+// Small batches (T <= 256, one chunk): masks, counts, scan and stable slots in one CTA --
+// the same popcount formulation as the multi-CTA kernels above.  The masks are also
+// written out for the affinity kernel.
+__global__ void __launch_bounds__(CHUNK) route_small_kernel(const int32_t *__restrict__ idx, int T,
+                                                            int E, int K, int32_t *counts,
+                                                            int32_t *offsets, int32_t *perm,
+                                                            int32_t *slot_pos, uint32_t *smask,
+                                                            int *status)
+{
+    extern __shared__ uint32_t sm[];
+    uint32_t *m_s = sm;                                          // [CW][E]
+    int32_t *base = reinterpret_cast<int32_t *>(sm + CW * E);    // [CW][E]
+    int32_t *off = base + CW * E;                                // [E + 1]
+    __shared__ int warp_tot[CHUNK / 32];
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    for (int i = tid; i < CW * E; i += CHUNK) m_s[i] = 0u;
+    __syncthreads();
+    const bool valid = tid < T;
+    for (int j = 0; j < K; ++j) {
+        int e = valid ? idx[static_cast<size_t>(tid) * K + j] : -1;
+        if (valid && (e < 0 || e >= E)) {
+            report(status, MOE_ERR_INVALID_ARG);
+            e = -1;
+        }
+        const uint32_t peers = __match_any_sync(kFullMask, e);
+        if (e >= 0 && lane == __ffs(peers) - 1) atomicOr(&m_s[w * E + e], peers);
+    }
+    __syncthreads();
+    const int rows = (T + 31) / 32;
+    for (int i = tid; i < rows * E; i += CHUNK) smask[i] = m_s[i];
+    // counts and an exclusive scan over experts: thread tid owns experts [tid*per, +per)
+    const int per = (E + CHUNK - 1) / CHUNK;
+    int local = 0;
+    for (int q = 0; q < per; ++q) {
+        const int e = tid * per + q;
+        if (e >= E) break;
+        int n = 0;
+        for (int r = 0; r < CW; ++r) n += __popc(m_s[r * E + e]);
+        off[e] = n;              // count for now
+        local += n;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFullMask, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_tot[w] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int q = 0; q < w; ++q) before += warp_tot[q];
+    int run = before + incl - local;
+    for (int q = 0; q < per; ++q) {
+        const int e = tid * per + q;
+        if (e >= E) break;
+        const int n = off[e];
+        counts[e] = n;
+        offsets[e] = run;
+        off[e] = run;
+        run += n;
+    }
+    if (tid == CHUNK - 1) { offsets[E] = run; }
+    __syncthreads();
+    // per 32-token row bases, then the stable slot of every (token, j)
+    for (int e = tid; e < E; e += CHUNK) {
+        int r0 = off[e];
+        for (int r = 0; r < CW; ++r) {
+            base[r * E + e] = r0;
+            r0 += __popc(m_s[r * E + e]);
+        }
+    }
+    __syncthreads();
+    if (valid) {
+        const uint32_t below = (1u << lane) - 1u;
+        for (int j = 0; j < K; ++j) {
+            const int e = idx[static_cast<size_t>(tid) * K + j];
+            if (e < 0 || e >= E) continue;
+            const int r = base[w * E + e] + __popc(m_s[w * E + e] & below);
+            slot_pos[static_cast<size_t>(tid) * K + j] = r;
+            perm[r] = tid;
+        }
+    }
+}
+
 }  // namespace
 
 DispatchPlan dispatch_plan(int T, int E)
@@ -216,6 +300,26 @@ cudaError_t launch_dispatch(const void *X, const int32_t *topk_idx, int T, int H
 {
     const size_t m_smem = static_cast<size_t>(CW) * E * sizeof(uint32_t);
     cudaError_t err;
+    if (T <= CHUNK) {
+        const size_t sm = 2 * m_smem + (E + 1) * sizeof(int32_t);
+        err = ensure_smem(reinterpret_cast<const void *>(route_small_kernel), sm);
+        if (err != cudaSuccess) return err;
+        route_small_kernel<<<1, CHUNK, sm, s>>>(topk_idx, T, E, K, counts, offsets, perm,
+                                                slot_pos, scr.smask, status);
+        if (affinity) {
+            dim3 g((E + 31) / 32, (E + 31) / 32);
+            affinity_kernel<<<g, 256, 0, s>>>(scr.smask, plan.n_words, E, affinity);
+        }
+        if (Xp) {
+            const long long rows = static_cast<long long>(T) * K;
+            long long blocks = (rows + 7) / 8;
+            const long long cap = static_cast<long long>(num_sms()) * 8;
+            if (blocks > cap) blocks = cap;
+            gather_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(
+                static_cast<const uint4 *>(X), H, perm, offsets, E, static_cast<uint4 *>(Xp));
+        }
+        return cudaGetLastError();
+    }
     err = ensure_smem(reinterpret_cast<const void *>(masks_kernel), m_smem);
     if (err != cudaSuccess) return err;
     err = ensure_smem(reinterpret_cast<const void *>(scatter_kernel), 2 * m_smem);

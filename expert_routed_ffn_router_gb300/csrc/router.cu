@@ -25,6 +25,7 @@
 //
 // Structure.  A grid (expert tiles, token tiles, K splits) of 256-thread CTAs computes
 // fp32 logit tiles on the CUDA cores into the workspace:
+//   tiny batches (T <= 4):     one warp per expert, all tokens at once;
 //   small batches (T <= 4096): 16 tokens x 256 experts per CTA, 4x4 per thread;
 //   large batches:             128 tokens x 64 experts per CTA, 8x4 per thread.
 // Small batches: the last CTA of a token tile (completion counter) sums the split-K
@@ -58,6 +59,7 @@ struct RouterArgs {
     float *topk_w;
     int *status;
     int max_pairs;   // capacity of the shared-memory refine list
+    int depth;       // additions any product passes through in its logit's summation
 };
 
 // CTA tile: TT tokens x TE experts, TPT x EPT per thread, PF stages of loads in flight.
@@ -226,11 +228,10 @@ __device__ void select_refined(int *pe, const double *pv, int n, int K, const fl
 // Bound constants of the summation tree: gamma_d and the inflation of computed norms.
 struct Bounds {
     float gam, infl;
-    __device__ Bounds(int S, int KS, int H)
+    __device__ Bounds(int depth, int KS, int H)
     {
-        const int ns_max = (S + KS - 1) / KS;
-        const float depth = static_cast<float>(KST + ns_max + KS + 2);
-        gam = depth * kU / (1.f - depth * kU) * 1.0001f;
+        const float d = static_cast<float>(depth);
+        gam = d * kU / (1.f - d * kU) * 1.0001f;
         infl = 1.f + static_cast<float>(H + 16 + KS) * (2.f * kU) + 4.f * kU;
     }
 };
@@ -530,6 +531,84 @@ __device__ void gemm_tile(const RouterArgs &a, unsigned char *smem)
     }
 }
 
+// ----------------------------------------------------------- tiny batches (T <= 4)
+// One warp per expert reads its gate row once and forms the logits of all T tokens; each
+// (token, expert) logit is 8 independent fp32 chains (one per element of a 16-byte vector,
+// H/256 products each) added by a fixed 3-level tree and a 5-level warp tree.
+constexpr int GEMV_TMAX = 4;      // beyond 4 tokens the 16x256 tile path is faster
+
+template <int TB>     // token batch: 1, 2 or 4 (>= T)
+__device__ void gemv_tile(const RouterArgs &a)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * NW + warp;
+    const int T = a.T, nv = a.H / 8;
+    if (e < a.E) {
+        const uint4 *wr = reinterpret_cast<const uint4 *>(a.Wg + static_cast<size_t>(e) * a.H);
+        const uint4 *xr = reinterpret_cast<const uint4 *>(a.X);
+        float acc[TB][8];
+#pragma unroll
+        for (int t = 0; t < TB; ++t)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[t][j] = 0.f;
+        float wsq = 0.f;
+        constexpr int U = TB <= 2 ? 4 : 2;       // vectors per lane in flight
+        for (int v0 = lane; v0 < nv; v0 += 32 * U) {
+            uint4 wv[U], xv[U][TB];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + 32 * u;
+                const bool ok = v < nv;
+                wv[u] = ok ? __ldg(wr + v) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int t = 0; t < TB; ++t)
+                    xv[u][t] = (ok && t < T) ? __ldg(xr + static_cast<size_t>(t) * nv + v)
+                                             : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                float wf[8];
+                unpack8(wv[u], wf);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) wsq = fmaf(wf[j], wf[j], wsq);
+#pragma unroll
+                for (int t = 0; t < TB; ++t) {
+                    float xf[8];
+                    unpack8(xv[u][t], xf);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[t][j] = fmaf(xf[j], wf[j], acc[t][j]);
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < TB; ++t) {
+            float sum = ((acc[t][0] + acc[t][1]) + (acc[t][2] + acc[t][3])) +
+                        ((acc[t][4] + acc[t][5]) + (acc[t][6] + acc[t][7]));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFullMask, sum, off);
+            if (lane == 0 && t < T) a.part[static_cast<size_t>(t) * a.E + e] = sum;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) wsq += __shfl_xor_sync(kFullMask, wsq, off);
+        if (lane == 0) a.wsq[e] = wsq;
+    }
+    if (blockIdx.x == 0 && warp == NW - 1) {     // token norms
+        for (int t = 0; t < T; ++t) {
+            const uint4 *xr = reinterpret_cast<const uint4 *>(a.X + static_cast<size_t>(t) * a.H);
+            float q = 0.f;
+            for (int v = lane; v < nv; v += 32) {
+                float xf[8];
+                unpack8(__ldg(xr + v), xf);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) q = fmaf(xf[j], xf[j], q);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) q += __shfl_xor_sync(kFullMask, q, off);
+            if (lane == 0) a.xsq[t] = q;
+        }
+    }
+}
+
 // Shared-memory layout of the finalise step (after the GEMM tile is done with smem).
 struct FinSmem {
     float *nw, *bias, *nxs, *L;        // [E], [E], [CH], [CH][E]
@@ -585,14 +664,17 @@ __device__ void refine_token_warp(const RouterArgs &a, int t, uint32_t cand, int
 }
 
 // ------------------------------------------------------- fused kernel (small batches)
-template <class C>
+template <class C, int GEMV>   // GEMV = token batch of the tiny-batch path, 0 = tile GEMM
 __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_last, s_npairs, s_npend;
     __shared__ int s_pend[3 * C::TT];     // (token, first pair, pair count) to refine
 
-    gemm_tile<C>(a, smem);
+    if constexpr (GEMV > 0)
+        gemv_tile<GEMV>(a);
+    else
+        gemm_tile<C>(a, smem);
 
     // ---------------------------------------------------------- last CTA finalises
     const int tt = blockIdx.y, tid = threadIdx.x;
@@ -600,7 +682,7 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
     __syncthreads();
     if (tid == 0) {
         const unsigned prev = atomicAdd(&a.cnt[tt], 1u);
-        s_last = (prev == static_cast<unsigned>(gridDim.x * a.KS - 1));
+        s_last = (prev == static_cast<unsigned>(gridDim.x * gridDim.z - 1));
         s_npairs = 0;
         s_npend = 0;
     }
@@ -611,7 +693,7 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
     const int warp = tid >> 5, lane = tid & 31;
     const int E = a.E, KS = a.KS, t0 = tt * C::TT;
     FinSmem S(smem, E, a.max_pairs, warp);
-    const Bounds bd(a.S, KS, a.H);
+    const Bounds bd(a.depth, KS, a.H);
     for (int e = tid; e < E; e += NT) {        // gate-row norms and biases, once per CTA
         float w[16];
 #pragma unroll
@@ -746,7 +828,7 @@ __global__ void __launch_bounds__(NT) router_finalize_kernel(const RouterArgs a,
     double *s64 = reinterpret_cast<double *>((d + 7) & ~static_cast<uintptr_t>(7)) +
                   static_cast<size_t>(warp) * E;
     if (t >= a.T) return;
-    const Bounds bd(a.S, KS, a.H);
+    const Bounds bd(a.depth, KS, a.H);
     const int tt = t / TT;
     const float part_sq = lane < KS ? __ldcg(a.xsq + static_cast<size_t>(lane) * a.T + t) : 0.f;
     float n2 = 0.f;
@@ -795,17 +877,26 @@ RouterPlan router_plan(int T, int H, int E)
 {
     RouterPlan p{};
     const bool small = T <= 4096;
+    p.gemv = 0;                                  // token batch of the tiny-batch path
+    if (T <= GEMV_TMAX)
+        for (p.gemv = 1; p.gemv < T; p.gemv <<= 1) {}
     p.TT = small ? SmallCfg::TT : LargeCfg::TT;
-    p.TE = small ? SmallCfg::TE : LargeCfg::TE;
+    p.TE = p.gemv ? NW : (small ? SmallCfg::TE : LargeCfg::TE);
     p.nTT = (T + p.TT - 1) / p.TT;
     p.nET = (E + p.TE - 1) / p.TE;
     p.S = H / KST;
     const int base = p.nTT * p.nET;
     const int target = 2 * num_sms();
-    // at most 32 stages per split keeps the summation depth (and the error bound) small
-    p.KS = (p.S + 31) / 32;
-    if (p.KS > 16) p.KS = 16;
-    while (p.KS * 2 <= p.S && p.KS * 2 <= 16 && base * p.KS < target) p.KS *= 2;
+    if (p.gemv) {
+        p.KS = 1;
+        p.depth = (H / 8 + 31) / 32 + 3 + 5 + 2;
+    } else {
+        // at most 32 stages per split keeps the summation depth (and the error bound) small
+        p.KS = (p.S + 31) / 32;
+        if (p.KS > 16) p.KS = 16;
+        while (p.KS * 2 <= p.S && p.KS * 2 <= 16 && base * p.KS < target) p.KS *= 2;
+        p.depth = KST + (p.S + p.KS - 1) / p.KS + p.KS + 2;
+    }
     p.max_pairs = 1024;
     auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
     p.part_bytes = al(static_cast<size_t>(p.KS) * T * E * sizeof(float));
@@ -830,14 +921,27 @@ cudaError_t launch_router(const void *X, const void *Wg, const float *bias, int 
     a.part = scr.part; a.xsq = scr.xsq; a.wsq = scr.wsq; a.cnt = scr.cnt;
     a.topk_idx = topk_idx; a.topk_w = topk_w; a.status = status;
     a.max_pairs = plan.max_pairs;
+    a.depth = plan.depth;
     dim3 grid(plan.nET, plan.nTT, plan.KS);
     cudaError_t err;
     if (plan.TT == SmallCfg::TT) {
         err = cudaMemsetAsync(scr.cnt, 0, static_cast<size_t>(plan.nTT) * sizeof(unsigned), s);
         if (err != cudaSuccess) return err;
-        err = ensure_smem(reinterpret_cast<const void *>(router_fused_kernel<SmallCfg>), plan.smem_bytes);
+        const void *fn;
+        switch (plan.gemv) {
+        case 1: fn = reinterpret_cast<const void *>(router_fused_kernel<SmallCfg, 1>); break;
+        case 2: fn = reinterpret_cast<const void *>(router_fused_kernel<SmallCfg, 2>); break;
+        case 4: fn = reinterpret_cast<const void *>(router_fused_kernel<SmallCfg, 4>); break;
+        default: fn = reinterpret_cast<const void *>(router_fused_kernel<SmallCfg, 0>); break;
+        }
+        err = ensure_smem(fn, plan.smem_bytes);
         if (err != cudaSuccess) return err;
-        router_fused_kernel<SmallCfg><<<grid, NT, plan.smem_bytes, s>>>(a);
+        switch (plan.gemv) {
+        case 1: router_fused_kernel<SmallCfg, 1><<<grid, NT, plan.smem_bytes, s>>>(a); break;
+        case 2: router_fused_kernel<SmallCfg, 2><<<grid, NT, plan.smem_bytes, s>>>(a); break;
+        case 4: router_fused_kernel<SmallCfg, 4><<<grid, NT, plan.smem_bytes, s>>>(a); break;
+        default: router_fused_kernel<SmallCfg, 0><<<grid, NT, plan.smem_bytes, s>>>(a); break;
+        }
         return cudaGetLastError();
     }
     err = ensure_smem(reinterpret_cast<const void *>(router_gemm_kernel<LargeCfg>), plan.smem_bytes);
