@@ -66,6 +66,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
+        for _ in range(3):
+            # the aarch64 build of the device front end crashes now and then on a source
+            # that compiles on the next attempt: retry a crash, not a compile error
+            if r.returncode == 0 or "Segmentation fault" not in r.stdout + r.stderr:
+                break
+            r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
         return obj, r.stderr

@@ -55,6 +55,7 @@ def load(build_if_missing: bool = True):
         "moe_read_status": ([P, P], I),
         "moe_debug_set_wait_limit": ([ctypes.c_ulonglong, I], None),
         "moe_debug_set_stage_events": ([P, I], None),
+        "moe_debug_set_ffn_variant": ([I], None),
         "moe_router_topk": ([P, P, P, I, I, I, I, P, P, P, Z, P], I),
         "moe_dispatch": ([P, P, I, I, I, I, P, P, P, P, P, P, P, Z, P], I),
         "moe_expert_ffn": ([P, P, I, I, I, I, P, P, P, P, I, P, Z, P], I),
@@ -107,6 +108,11 @@ def moe_read_status(ws, stream=None) -> int:
 
 def moe_debug_set_wait_limit(limit_ns: int, inject_stall: int = 0) -> None:
     load().moe_debug_set_wait_limit(int(limit_ns), int(inject_stall))
+
+
+def moe_debug_set_ffn_variant(variant: int) -> None:
+    """0: automatic; 1: single-CTA FFN kernel; 2: CTA-pair (2-SM MMA) FFN kernel."""
+    load().moe_debug_set_ffn_variant(int(variant))
 
 
 def moe_debug_set_stage_events(events) -> None:

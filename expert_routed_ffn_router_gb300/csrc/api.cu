@@ -208,6 +208,11 @@ void moe_debug_set_wait_limit(unsigned long long limit_ns, int inject_stall)
     g_inject_stall = inject_stall;
 }
 
+void moe_debug_set_ffn_variant(int variant)
+{
+    moe::set_ffn_variant(variant == 1 || variant == 2 ? variant : 0);
+}
+
 void moe_debug_set_stage_events(void *const *events, int n)
 {
     g_stage_events_on = events != nullptr && n >= 6;

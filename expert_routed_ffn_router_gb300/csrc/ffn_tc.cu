@@ -24,6 +24,16 @@
 // shared-memory ring (full/empty mbarriers) decouples TMA from the MMAs; two TMEM
 // accumulators decouple the MMAs of tile j+1 from the epilogue of tile j.
 //
+// CTA pairs.  Token tiles of 128 rows or more run on clusters of two CTAs that issue
+// 2-SM MMAs (cta_group::2): one 256-row weight tile per pair, each CTA staging 128 weight
+// rows and half of the token rows, the even CTA issuing the MMAs and owning the ring's
+// full barriers (both CTAs' copies complete there), commits multicast to both CTAs.  Per
+// SM this halves the token-tile bytes in shared memory and the L2 reads per flop.
+//
+// Tile order.  Groups that reuse a weight tile across several token tiles (tensor-bound)
+// come first, groups with a single, at most half-full token tile (weight-streaming) after
+// them, and the two sequences are interleaved in proportion over the persistent units.
+//
 // Every wait is bounded (globaltimer): when one runs out the kernel records
 // MOE_ERR_DEVICE_TIMEOUT in the status word, the other roles leave their loops, copies and
 // MMAs in flight are drained with bounded waits, TMEM is freed and the kernel returns.
@@ -42,9 +52,12 @@ constexpr int BK = 64;                    // K per stage = one 128-byte swizzle 
 constexpr int A_BYTES = BM * BK * 2;      // 16 KB: two 64x64 boxes
 constexpr int HALF_A = A_BYTES / 2;
 constexpr int NUM_THREADS = 192;
-constexpr int MAX_GROUPS = 1024;
-constexpr int XCHG_FLOATS = 2 * 16 * 64;  // double-buffered G/U exchange (up epilogue)
+constexpr int MAX_GROUPS = 1024;        // groups of one problem
+constexpr int MAX_CG = 1040;             // groups of all problems of a launch
+constexpr int CW = 32;                    // epilogue chunk: accumulator columns per TMEM load
+constexpr int XCHG_FLOATS = 2 * CW * 64;  // double-buffered G exchange (up epilogue)
 constexpr int MODE_UP = 0, MODE_DOWN = 1;
+constexpr int MAX_STAGES = 12;
 
 struct ProbDev {
     const int32_t *offsets;  // [n_groups + 1] on the device, or nullptr (one dense group)
@@ -91,7 +104,7 @@ __device__ __forceinline__ bool epi_all(bool ok)
     return r != 0;
 }
 
-template <int MODE>
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_constant__ FfnArgs p)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -99,7 +112,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
     const int bn = p.bn, S = p.stages;
-    const int stage_bytes = A_BYTES + bn * 128;
+    const int bn_cta = PAIR ? bn / 2 : bn;    // token rows of B staged in this CTA
+    const int stage_bytes = A_BYTES + bn_cta * 128;
     unsigned char *stage_base = smem;
     float *xbuf = reinterpret_cast<float *>(smem + static_cast<size_t>(S) * stage_bytes);
     uint64_t *full = reinterpret_cast<uint64_t *>(xbuf + XCHG_FLOATS);
@@ -108,12 +122,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    static_assert(BK == 64, "the MMA issuer unrolls four K16 steps per stage");
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    int *goff = reinterpret_cast<int *>(tmem_slot + 4);       // [2][MAX_GROUPS + 1]
-    int *gt = goff + 2 * (MAX_GROUPS + 1);                    // [2][MAX_GROUPS + 1]
+    // groups of all problems, problem 0's first: first row, rows, and the tile order
+    int *n_used_s = reinterpret_cast<int *>(tmem_slot + 2);   // groups with rows
+    int *n_heavy_s = reinterpret_cast<int *>(tmem_slot + 3);  // ... of which heavy
+    int *gstart = reinterpret_cast<int *>(tmem_slot + 4);     // [MAX_CG]
+    int *gm = gstart + MAX_CG;                                // [MAX_CG]
+    int *gord = gm + MAX_CG;                                  // [MAX_CG] group ids, tile order
+    int *gpre = gord + MAX_CG;                                // [MAX_CG + 1] tile prefix
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint64_t tmo = p.timeout_ns;
+    // A CTA pair (cluster of two) computes one 256-row tile: the even CTA issues the MMAs
+    // and owns the full/tempty barriers; each CTA stages half of A and half of B.
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int n_units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -122,7 +148,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 128);
+            mbar_init(&tempty[b], PAIR ? 256 : 128);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -136,30 +162,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
         }
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, static_cast<uint32_t>(p.tmem_cols));
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(tmem_slot, static_cast<uint32_t>(p.tmem_cols));
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, static_cast<uint32_t>(p.tmem_cols));
+            tmem_relinquish();
+        }
     }
     // group row offsets -> shared memory
+    const int n0 = p.prob[0].n_groups;
+    const int n_cg = n0 + (p.n_probs > 1 ? p.prob[1].n_groups : 0);
     for (int pi = 0; pi < p.n_probs; ++pi) {
         const ProbDev &P = p.prob[pi];
-        for (int g = tid; g <= P.n_groups; g += NUM_THREADS)
-            goff[pi * (MAX_GROUPS + 1) + g] =
-                P.offsets ? P.offsets[g] : (g == 0 ? 0 : P.dense_rows);
+        const int base = pi ? n0 : 0;
+        for (int g = tid; g < P.n_groups; g += NUM_THREADS) {
+            const int a = P.offsets ? P.offsets[g] : 0;
+            const int b = P.offsets ? P.offsets[g + 1] : P.dense_rows;
+            gstart[base + g] = a;
+            gm[base + g] = b - a;
+        }
     }
     __syncthreads();
-    // tile prefix per problem: tiles(g) = ceil(m_g / bn) * n_mtiles
-    if (warp < p.n_probs) {
-        const int pi = warp;
-        const ProbDev &P = p.prob[pi];
-        const int *go = goff + pi * (MAX_GROUPS + 1);
-        int *gtp = gt + pi * (MAX_GROUPS + 1);
+    // Tile order.  A group whose rows fit in one token tile at most half full is "light":
+    // its weights are streamed from HBM for little arithmetic.  The other ("heavy") groups
+    // reuse each weight tile across several token tiles and are bound by the tensor
+    // cores.  Heavy groups come first, then light ones (each set in group order), and the
+    // two tile sequences are interleaved in proportion, so that at any time some units
+    // stream weights while the others compute.
+    if (warp == 0) {
+        int n = 0;
+        for (int pass = 0; pass < 2; ++pass) {
+            for (int c0 = 0; c0 < n_cg; c0 += 32) {
+                const int cg = c0 + lane;
+                bool sel = false;
+                if (cg < n_cg) {
+                    const int m = gm[cg];
+                    const bool light = 2 * m <= bn;
+                    sel = m > 0 && (pass == 0 ? !light : light);
+                }
+                const uint32_t bal = __ballot_sync(kFullMask, sel);
+                if (sel) gord[n + __popc(bal & ((1u << lane) - 1u))] = cg;
+                n += __popc(bal);
+            }
+            if (pass == 0 && lane == 0) *n_heavy_s = n;
+        }
+        __syncwarp();
         int running = 0;
-        for (int g0 = 0; g0 < P.n_groups; g0 += 32) {
-            const int g = g0 + lane;
+        for (int k0 = 0; k0 < n; k0 += 32) {
+            const int k = k0 + lane;
             int nt = 0;
-            if (g < P.n_groups) {
-                const int m = go[g + 1] - go[g];
-                nt = m > 0 ? ((m + bn - 1) / bn) * P.n_mtiles : 0;
+            if (k < n) {
+                const int cg = gord[k];
+                nt = ((gm[cg] + bn - 1) / bn) * p.prob[cg >= n0 ? 1 : 0].n_mtiles;
             }
             int incl = nt;
 #pragma unroll
@@ -167,110 +222,156 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
                 const int v = __shfl_up_sync(kFullMask, incl, off);
                 if (lane >= off) incl += v;
             }
-            if (g < P.n_groups) gtp[g] = running + incl - nt;
+            if (k < n) gpre[k] = running + incl - nt;
             running += __shfl_sync(kFullMask, incl, 31);
         }
-        if (lane == 0) gtp[P.n_groups] = running;
+        if (lane == 0) {
+            gpre[n] = running;
+            *n_used_s = n;
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();   // the peer's barriers exist before any remote arrive or copy
     tc_fence_after();
 
     const uint32_t tmem_base = *tmem_slot;
-    const int total0 = gt[p.prob[0].n_groups];
-    const int total = total0 + (p.n_probs > 1 ? gt[(MAX_GROUPS + 1) + p.prob[1].n_groups] : 0);
+    const int n_used = *n_used_s;
+    const int total = gpre[n_used];
+    const int n_heavy_tiles = gpre[*n_heavy_s];
+    const long long n_light_tiles = total - n_heavy_tiles;
 
     auto decode = [&](int t) -> Tile {
-        Tile T;
-        T.pi = (t < total0) ? 0 : 1;
-        const int lt = T.pi ? t - total0 : t;
-        const ProbDev &P = p.prob[T.pi];
-        const int *gtp = gt + T.pi * (MAX_GROUPS + 1);
-        const int *go = goff + T.pi * (MAX_GROUPS + 1);
-        int lo = 0, hi = P.n_groups;   // first index with gtp[i] > lt, minus one
+        // position t of the interleaved order -> index v in the heavy-then-light order
+        const int lt0 = static_cast<int>(n_light_tiles * t / total);
+        const int lt1 = static_cast<int>(n_light_tiles * (t + 1) / total);
+        const int v = lt1 > lt0 ? n_heavy_tiles + lt0 : t - lt0;
+        int lo = 0, hi = n_used - 1;   // last k with gpre[k] <= v
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (gtp[mid] <= lt) lo = mid; else hi = mid - 1;
+            if (gpre[mid] <= v) lo = mid; else hi = mid - 1;
         }
-        T.g = lo;
-        const int m = go[lo + 1] - go[lo];
+        const int cg = gord[lo];
+        Tile T;
+        T.pi = cg >= n0 ? 1 : 0;
+        T.g = cg - (T.pi ? n0 : 0);
+        const int m = gm[cg];
         const int ntn = (m + bn - 1) / bn;
-        const int local = lt - gtp[lo];
+        const int local = v - gpre[lo];
         T.mt = local / ntn;
         const int nt = local - T.mt * ntn;
-        T.row0 = go[lo] + nt * bn;
+        T.row0 = gstart[cg] + nt * bn;
         T.nvalid = min(bn, m - nt * bn);
         return T;
     };
+    // MMA N: the valid rows rounded up to the instruction's granule (a pair splits N
+    // evenly between its two CTAs, 16 rows each at least)
+    auto n_mma_of = [&](const Tile &T) -> int {
+        const int n = PAIR ? (T.nvalid + 31) & ~31 : (T.nvalid + 15) & ~15;
+        return n < bn ? n : bn;
+    };
+    // this CTA's m-tile: a pair tile covers two single-CTA m-tiles
+    auto mt_cta = [&](const Tile &T) -> int { return PAIR ? 2 * T.mt + static_cast<int>(rank) : T.mt; };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && !p.inject) {
             uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            // the three boxes of (tile, K block): two of A (W1 | W3, or two 64-column
+            // halves of W2) and one of B (this CTA's token rows)
+            auto boxes = [&](const Tile &T, int &a0, int &a1, int &brow) {
+                const int mt = mt_cta(T);
+                a0 = MODE == MODE_UP ? mt * 64 : mt * 128;
+                a1 = MODE == MODE_UP ? mt * 64 : mt * 128 + 64;
+                brow = T.row0 + (PAIR && !leader ? n_mma_of(T) / 2 : 0);
+            };
+            uint32_t s = 0, ph = 0;
+            unsigned char *a = stage_base;
+            const uint32_t full_c0 = PAIR ? mapa_shared(smem_u32(full), 0) : 0u;   // even CTA's full[0]
+            for (int t = unit; t < total && ok; t += n_units) {
                 const Tile T = decode(t);
                 const ProbDev &P = p.prob[T.pi];
+                int a0, a1, brow;
+                boxes(T, a0, a1, brow);
+                const CUtensorMap *mA2 = MODE == MODE_UP ? &p.mapA3[T.pi] : &p.mapA[T.pi];
                 for (int kb = 0; kb < P.kblocks; ++kb, ++it) {
-                    const int s = it % S;
-                    const uint32_t ph = (it / S) & 1u;
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, tmo)) { ok = false; break; }
-                    unsigned char *a = stage_base + static_cast<size_t>(s) * stage_bytes;
-                    mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(stage_bytes));
-                    if (MODE == MODE_UP) {
-                        tma_load_3d(a, &p.mapA[T.pi], &full[s], T.mt * 64, kb * BK, T.g);
-                        tma_load_3d(a + HALF_A, &p.mapA3[T.pi], &full[s], T.mt * 64, kb * BK, T.g);
+                    if (!PAIR) {
+                        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(stage_bytes));
+                        tma_load_3d(a, &p.mapA[T.pi], &full[s], a0, kb * BK, T.g);
+                        tma_load_3d(a + HALF_A, mA2, &full[s], a1, kb * BK, T.g);
+                        tma_load_2d(a + A_BYTES, &p.mapB[T.pi], &full[s], kb * BK, brow);
                     } else {
-                        tma_load_3d(a, &p.mapA[T.pi], &full[s], T.mt * 128, kb * BK, T.g);
-                        tma_load_3d(a + HALF_A, &p.mapA[T.pi], &full[s], T.mt * 128 + 64, kb * BK, T.g);
+                        // both CTAs' copies complete on the even CTA's barrier, which
+                        // expects the bytes of both
+                        if (leader) mbar_arrive_expect_tx(&full[s], 2u * static_cast<uint32_t>(stage_bytes));
+                        const uint32_t fb = full_c0 + 8u * s;
+                        tma_load_3d_pair(a, &p.mapA[T.pi], fb, a0, kb * BK, T.g);
+                        tma_load_3d_pair(a + HALF_A, mA2, fb, a1, kb * BK, T.g);
+                        tma_load_2d_pair(a + A_BYTES, &p.mapB[T.pi], fb, kb * BK, brow);
                     }
-                    tma_load_2d(a + A_BYTES, &p.mapB[T.pi], &full[s], kb * BK, T.row0);
+                    if (++s == static_cast<uint32_t>(S)) { s = 0; ph ^= 1u; a = stage_base; } else { a += stage_bytes; }
                 }
             }
             // every copy issued lands before the CTA can exit (a no-op wait in normal runs:
-            // the MMA warp has already waited on each of these phases)
+            // the MMA warp has already waited on each of these phases).  In a pair the
+            // even CTA's barriers count the copies of both CTAs.
             (void)ok;
-            const uint32_t n = it < static_cast<uint32_t>(S) ? it : static_cast<uint32_t>(S);
-            for (uint32_t j = it - n; j < it; ++j) {
-                int dummy_abort = 0;
-                mbar_wait(&full[j % S], (j / S) & 1u, &dummy_abort, nullptr, 20000000ull);
+            if (!PAIR || leader) {
+                const uint32_t n = it < static_cast<uint32_t>(S) ? it : static_cast<uint32_t>(S);
+                for (uint32_t j = it - n; j < it; ++j) {
+                    int dummy_abort = 0;
+                    mbar_wait(&full[j % S], (j / S) & 1u, &dummy_abort, nullptr, 20000000ull);
+                }
             }
         }
     } else if (warp == 1) {
         // -------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            uint32_t it = 0, tc = 0;
+        if (lane == 0 && (!PAIR || leader)) {
+            // The issuing thread's work per stage is kept to a few adds: one stage of MMAs
+            // lasts only ~512 tensor-core cycles, and a longer dependent chain here (index
+            // division, descriptor packing) leaves the tensor pipe idle between stages.
+            const uint32_t ring0 = smem_u32(stage_base);
+            const uint64_t adesc0 = smem_desc_sw128(ring0, HALF_A, 1024);
+            const uint64_t bdesc0 = smem_desc_sw128(ring0 + A_BYTES, 16, 1024);
+            const uint32_t stage16 = static_cast<uint32_t>(stage_bytes) >> 4;  // descriptor units
+            uint32_t s = 0, ph = 0, soff = 0, tc = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
+            for (int t = unit; t < total && ok; t += n_units, ++tc) {
                 const Tile T = decode(t);
                 const ProbDev &P = p.prob[T.pi];
                 const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
                 if (!mbar_wait(&tempty[b], tph ^ 1u, abort_flag, p.status, tmo)) { ok = false; break; }
                 tc_fence_after();
-                int n_mma = (T.nvalid + 15) & ~15;
-                if (n_mma > bn) n_mma = bn;
-                const uint32_t idesc = idesc_bf16_f32(BM, static_cast<uint32_t>(n_mma), true, false);
+                const int n_mma = n_mma_of(T);
+                const uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * BM : BM, static_cast<uint32_t>(n_mma), true, false);
                 const uint32_t d_tmem = tmem_base + b * static_cast<uint32_t>(bn);
-                for (int kb = 0; kb < P.kblocks; ++kb, ++it) {
-                    const int s = it % S;
-                    const uint32_t ph = (it / S) & 1u;
+                for (int kb = 0; kb < P.kblocks; ++kb) {
                     if (!mbar_wait(&full[s], ph, abort_flag, p.status, tmo)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(stage_base + static_cast<size_t>(s) * stage_bytes);
-                    const uint32_t b_addr = a_addr + A_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t adesc = smem_desc_sw128(a_addr + kk * 2048, HALF_A, 1024);
-                        const uint64_t bdesc = smem_desc_sw128(b_addr + kk * 32, 16, 1024);
-                        tc_mma_bf16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    const uint64_t ad = adesc0 + soff, bd = bdesc0 + soff;
+                    // K16 steps: +2048 B along A (MN-major), +32 B along B (K-major)
+                    if (PAIR) {
+                        tc_mma_bf16_pair(d_tmem, ad, bd, idesc, kb != 0 ? 1u : 0u);
+                        tc_mma_bf16_pair(d_tmem, ad + 128, bd + 2, idesc, 1u);
+                        tc_mma_bf16_pair(d_tmem, ad + 256, bd + 4, idesc, 1u);
+                        tc_mma_bf16_pair(d_tmem, ad + 384, bd + 6, idesc, 1u);
+                        tc_commit_pair_mc(&empty[s], 3);
+                    } else {
+                        tc_mma_bf16(d_tmem, ad, bd, idesc, kb != 0 ? 1u : 0u);
+                        tc_mma_bf16(d_tmem, ad + 128, bd + 2, idesc, 1u);
+                        tc_mma_bf16(d_tmem, ad + 256, bd + 4, idesc, 1u);
+                        tc_mma_bf16(d_tmem, ad + 384, bd + 6, idesc, 1u);
+                        tc_commit(&empty[s]);
                     }
-                    tc_commit(&empty[s]);
+                    if (++s == static_cast<uint32_t>(S)) { s = 0; ph ^= 1u; soff = 0; } else { soff += stage16; }
                 }
                 if (!ok) break;
-                tc_commit(&tfull[b]);
+                if (PAIR) tc_commit_pair_mc(&tfull[b], 3); else tc_commit(&tfull[b]);
             }
             // drain: every MMA issued by this thread has completed before TMEM is freed
-            tc_commit(drain);
+            if (PAIR) tc_commit_pair_mc(drain, 1); else tc_commit(drain);
             int dummy_abort = 0;
             mbar_wait(drain, 0, &dummy_abort, nullptr, 20000000ull);
         }
@@ -278,7 +379,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
         // ----------------------------------------------------------------- epilogue
         const int q = warp & 3;                 // TMEM lane quarter of this warp
         uint32_t tc = 0, cc = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
+        for (int t = unit; t < total; t += n_units, ++tc) {
             const Tile T = decode(t);
             const ProbDev &P = p.prob[T.pi];
             const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
@@ -286,53 +387,69 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
             if (!epi_all(ok)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * static_cast<uint32_t>(bn);
-            const int nchunks = (T.nvalid + 15) / 16;
+            const int nchunks = (T.nvalid + CW - 1) / CW;
+            const int mt = mt_cta(T);
+            // one chunk = CW token columns of this warp's 32 accumulator rows (a 16-row
+            // tile has only 16 columns per buffer)
+            auto load_chunk = [&](int c, float (&v)[CW]) {
+                __syncwarp();
+                if (bn >= CW) {
+                    tmem_ld32(tbase + CW * c, v);
+                } else {
+                    float h[16];
+                    tmem_ld16(tbase, h);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) { v[j] = h[j]; v[j + 16] = 0.f; }
+                }
+            };
             if (MODE == MODE_UP) {
-                const int i = T.mt * 64 + (q & 1) * 32 + lane;
+                // G (W1 rows) sits in lanes 0..63 (quarters 0, 1), U (W3 rows) in lanes
+                // 64..127 (quarters 2, 3): the G warps hand their values over through shared
+                // memory and the U warps -- which share no SM sub-partition with the
+                // producer and MMA warps -- compute h = silu(G) * U and store it
+                const int i = mt * 64 + (q & 1) * 32 + lane;
+                const bool col_ok = i < P.out_cols;
                 uint16_t *out = static_cast<uint16_t *>(P.out);
                 for (int c = 0; c < nchunks; ++c, ++cc) {
-                    float v[16];
-                    __syncwarp();
-                    tmem_ld16(tbase + 16 * c, v);
-                    float *xb = xbuf + (cc & 1u) * (16 * 64);
-                    if (q >= 2) {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) xb[j * 64 + (q - 2) * 32 + lane] = v[j];
-                    }
-                    named_bar_sync(1, 128);
+                    float v[CW];
+                    load_chunk(c, v);
+                    float *xb = xbuf + (cc & 1u) * (CW * 64);
                     if (q < 2) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int n = 16 * c + j;
+                        for (int j = 0; j < CW; ++j) xb[j * 64 + q * 32 + lane] = v[j];
+                    }
+                    named_bar_sync(1, 128);
+                    if (q >= 2 && col_ok) {
+#pragma unroll
+                        for (int j = 0; j < CW; ++j) {
+                            const int n = CW * c + j;
                             if (n < T.nvalid) {
-                                const float u = xb[j * 64 + q * 32 + lane];
-                                const float g = v[j];
-                                const float h = g / (1.f + __expf(-g)) * u;
+                                const float g = xb[j * 64 + (q - 2) * 32 + lane];
+                                const float h = g / (1.f + __expf(-g)) * v[j];
                                 out[static_cast<size_t>(T.row0 + n) * P.out_ld + i] = f32_to_bf16_rn(h);
                             }
                         }
                     }
                 }
             } else {
-                const int col = T.mt * 128 + q * 32 + lane;
+                const int col = mt * 128 + q * 32 + lane;
                 const bool col_ok = col < P.out_cols;
                 for (int c = 0; c < nchunks; ++c) {
-                    float v[16];
-                    __syncwarp();
-                    tmem_ld16(tbase + 16 * c, v);
+                    float v[CW];
+                    load_chunk(c, v);
                     if (col_ok) {
                         if (P.out_fp32) {
                             float *out = static_cast<float *>(P.out);
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int n = 16 * c + j;
+                            for (int j = 0; j < CW; ++j) {
+                                const int n = CW * c + j;
                                 if (n < T.nvalid) out[static_cast<size_t>(T.row0 + n) * P.out_ld + col] = v[j];
                             }
                         } else {
                             uint16_t *out = static_cast<uint16_t *>(P.out);
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int n = 16 * c + j;
+                            for (int j = 0; j < CW; ++j) {
+                                const int n = CW * c + j;
                                 if (n < T.nvalid)
                                     out[static_cast<size_t>(T.row0 + n) * P.out_ld + col] = f32_to_bf16_rn(v[j]);
                             }
@@ -341,16 +458,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
                 }
             }
             tc_fence_before();
-            mbar_arrive(&tempty[b]);
+            if (PAIR)
+                mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[b]), 0));
+            else
+                mbar_arrive(&tempty[b]);
         }
     }
 
     tc_fence_before();
+    __syncwarp();
     __syncthreads();
+    // neither CTA of a pair leaves (or frees tensor memory) while the other may still
+    // signal its barriers or the even CTA's MMAs may still write its tensor memory
+    if (PAIR) cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
+        if (PAIR)
+            tmem_dealloc_pair(tmem_base, static_cast<uint32_t>(p.tmem_cols));
+        else
+            tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
     }
 }
 
@@ -391,14 +518,14 @@ bool encode_weight(CUtensorMap *m, const void *base, int n_groups, int rows, int
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D bf16 activation tensor [rows][cols], boxes of 64 columns x bn rows.
-bool encode_act(CUtensorMap *m, const void *base, int rows, int cols, int bn)
+// 2-D bf16 activation tensor [rows][cols], boxes of 64 columns x box_rows rows.
+bool encode_act(CUtensorMap *m, const void *base, int rows, int cols, int box_rows)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(bn)};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -417,32 +544,77 @@ int pick_bn(int avg_rows)
     return bn;
 }
 
-size_t ffn_smem_bytes(int bn, int stages)
+size_t ffn_smem_bytes(int bn_cta, int stages)
 {
-    return 1024 + static_cast<size_t>(stages) * (A_BYTES + bn * 128) + XCHG_FLOATS * 4 +
-           (2 * stages + 5) * 8 + 16 + 4 * (MAX_GROUPS + 1) * 4;
+    return 1024 + static_cast<size_t>(stages) * (A_BYTES + bn_cta * 128) + XCHG_FLOATS * 4 +
+           (2 * stages + 5) * 8 + 16 + (4 * MAX_CG + 1) * 4;
 }
 
-int pick_stages(int bn)
+int pick_stages(int bn_cta)
 {
     const size_t cap = 232448;   // max dynamic shared memory per block on sm_100/sm_103
-    int s = 12;
-    while (s > 2 && ffn_smem_bytes(bn, s) > cap) --s;
+    int s = MAX_STAGES;
+    while (s > 2 && ffn_smem_bytes(bn_cta, s) > cap) --s;
     return s;
 }
 
+// Token tiles of at least this many rows run on CTA pairs (256-row weight tiles, 2-SM
+// MMA): per SM the pair halves the B tile held in shared memory and read by the tensor
+// core, and halves the activation traffic from L2 per flop.
+constexpr int PAIR_MIN_BN = 128;
+int g_variant = 0;   // 0 automatic, 1 single CTA, 2 CTA pair
+
+template <int MODE, bool PAIR>
+cudaError_t launch_one(const FfnArgs &a, size_t smem, cudaStream_t s)
+{
+    const void *fn = reinterpret_cast<const void *>(ffn_kernel<MODE, PAIR>);
+    cudaError_t err = ensure_smem(fn, smem);
+    if (err != cudaSuccess) return err;
+    if (!PAIR) {
+        ffn_kernel<MODE, false><<<num_sms(), NUM_THREADS, smem, s>>>(a);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms() / 2 * 2));
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ffn_kernel<MODE, true>, a);
+}
+
 }  // namespace
+
+void set_ffn_variant(int v) { g_variant = v; }
 
 cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I_pp,
                        int token_hint, int *status, cudaStream_t s,
                        unsigned long long timeout_ns, int inject, cudaEvent_t mid_event)
 {
     if (n_probs < 1 || n_probs > 2) return cudaErrorInvalidValue;
-    const int bn = pick_bn(token_hint);
-    const int stages = pick_stages(bn);
-    const size_t smem = ffn_smem_bytes(bn, stages);
+    int n_cg = 0;
+    for (int pi = 0; pi < n_probs; ++pi) {
+        if (probs[pi].n_groups < 1 || probs[pi].n_groups > MAX_GROUPS) return cudaErrorInvalidValue;
+        n_cg += probs[pi].n_groups;
+    }
+    if (n_cg > MAX_CG) return cudaErrorInvalidValue;
+    int bn = pick_bn(token_hint);
+    bool pair = g_variant == 2 || (g_variant == 0 && bn >= PAIR_MIN_BN);
+    if (pair && bn < 32) bn = 32;           // 16 token rows per CTA at least
+    const int bn_cta = pair ? bn / 2 : bn;
+    const int stages = pick_stages(bn_cta);
+    const size_t smem = ffn_smem_bytes(bn_cta, stages);
     int tcols = 32;
     while (tcols < 2 * bn) tcols <<= 1;
+    const int m_up = pair ? 128 : 64;      // weight columns of one tile
+    const int m_dn = pair ? 256 : 128;
 
     FfnArgs up, dn;
     memset(&up, 0, sizeof up);
@@ -452,16 +624,16 @@ cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I
         const int I = I_pp[pi];
         if (!encode_weight(&up.mapA[pi], P.W1, P.n_groups, H, I) ||
             !encode_weight(&up.mapA3[pi], P.W3, P.n_groups, H, I) ||
-            !encode_act(&up.mapB[pi], P.act, P.rows, H, bn) ||
+            !encode_act(&up.mapB[pi], P.act, P.rows, H, bn_cta) ||
             !encode_weight(&dn.mapA[pi], P.W2, P.n_groups, I, H) ||
-            !encode_act(&dn.mapB[pi], P.h, P.rows, I, bn))
+            !encode_act(&dn.mapB[pi], P.h, P.rows, I, bn_cta))
             return cudaErrorInvalidValue;
         dn.mapA3[pi] = dn.mapA[pi];
         ProbDev u{};
         u.offsets = P.offsets;
         u.n_groups = P.n_groups;
         u.dense_rows = P.dense_rows;
-        u.n_mtiles = I / 64;
+        u.n_mtiles = (I + m_up - 1) / m_up;
         u.kblocks = H / 64;
         u.out_ld = I;
         u.out_cols = I;
@@ -469,7 +641,7 @@ cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I
         u.out = P.h;
         up.prob[pi] = u;
         ProbDev d = u;
-        d.n_mtiles = (H + 127) / 128;
+        d.n_mtiles = (H + m_dn - 1) / m_dn;
         d.kblocks = I / 64;
         d.out_ld = H;
         d.out_cols = H;
@@ -486,18 +658,12 @@ cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I
         a->timeout_ns = timeout_ns;
         a->inject = inject;
     }
-    cudaError_t err;
-    err = ensure_smem(reinterpret_cast<const void *>(ffn_kernel<MODE_UP>), smem);
-    if (err != cudaSuccess) return err;
-    err = ensure_smem(reinterpret_cast<const void *>(ffn_kernel<MODE_DOWN>), smem);
-    if (err != cudaSuccess) return err;
-    const int grid = num_sms();
-    ffn_kernel<MODE_UP><<<grid, NUM_THREADS, smem, s>>>(up);
-    err = cudaGetLastError();
+    cudaError_t err = pair ? launch_one<MODE_UP, true>(up, smem, s)
+                           : launch_one<MODE_UP, false>(up, smem, s);
     if (err != cudaSuccess) return err;
     if (mid_event && (err = cudaEventRecord(mid_event, s)) != cudaSuccess) return err;
-    ffn_kernel<MODE_DOWN><<<grid, NUM_THREADS, smem, s>>>(dn);
-    return cudaGetLastError();
+    return pair ? launch_one<MODE_DOWN, true>(dn, smem, s)
+                : launch_one<MODE_DOWN, false>(dn, smem, s);
 }
 
 }  // namespace moe

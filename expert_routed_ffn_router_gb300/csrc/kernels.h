@@ -73,6 +73,9 @@ struct FfnProblem {
 // Enqueues the up projection (+SwiGLU) and the down projection of up to two problems
 // (the routed experts and the shared expert) that share H; I may differ per problem.
 // `mid_event` (nullable) is recorded on `s` between the up and the down launch.
+// 0 automatic, 1 single-CTA kernel, 2 CTA-pair kernel (testing hook)
+void set_ffn_variant(int v);
+
 cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I_per_prob,
                        int token_hint, int *status, cudaStream_t s,
                        unsigned long long timeout_ns, int inject, cudaEvent_t mid_event);

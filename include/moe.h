@@ -109,6 +109,13 @@ void moe_debug_set_wait_limit(unsigned long long limit_ns, int inject_stall);
  * handles stay owned by the caller and must outlive the recording calls. */
 void moe_debug_set_stage_events(void *const *events, int n);
 
+/* Testing hook: which expert-FFN kernel later moe_expert_ffn and moe_layer_forward calls
+ * of the process launch.  0 (the default) chooses by token tile: tiles of 128 rows or more
+ * run on CTA pairs (256-row weight tiles, 2-SM tensor-core MMA), smaller ones on single
+ * CTAs (128-row weight tiles).  1 forces single CTAs, 2 forces CTA pairs.  Both give the
+ * same results; other values act as 0.  Not for production use. */
+void moe_debug_set_ffn_variant(int variant);
+
 /* Router: gate GEMM, sigmoid scoring, selection bias, top-K, renormalised weights, fused
  * in one kernel ("DeepSeek-V4.1-Flash", Kernels, Mega-Gate; "Lower latency and higher
  * throughput...", MoE Router).

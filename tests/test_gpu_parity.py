@@ -42,6 +42,23 @@ def test_ragged_shapes(T, H, E, K, I, Is):
     check_layer(Problem(w))
 
 
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("T,H,E,K,I,Is", [
+    (37, 256, 16, 2, 128, 128),     # 32-row tiles (a pair splits them 16 + 16)
+    (300, 192, 40, 5, 192, 64),     # pair tiles past the last weight column (I, H % 256)
+    (130, 128, 8, 8, 64, 0),        # I = 64: the odd CTA of every up tile is all padding
+    (513, 256, 8, 6, 128, 128),     # 256-row token tiles, ragged last tile per expert
+    (700, 192, 16, 4, 192, 64),
+])
+def test_ffn_variants_single_cta_and_cta_pair(T, H, E, K, I, Is, variant):
+    w = synth.Workload("var", T=T, H=H, E=E, K=K, I=I, Is=Is, seed=T + 5, x_seed=T + 6)
+    B.moe_debug_set_ffn_variant(variant)
+    try:
+        check_layer(Problem(w))
+    finally:
+        B.moe_debug_set_ffn_variant(0)
+
+
 def test_exact_ties_duplicate_gate_rows():
     w = synth.workload("tiny", T=64)
     r = synth.routing_inputs(w)
