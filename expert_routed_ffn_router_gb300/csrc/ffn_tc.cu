@@ -239,25 +239,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
     const int n_used = *n_used_s;
     const int total = gpre[n_used];
     const int n_heavy_tiles = gpre[*n_heavy_s];
-    const long long n_light_tiles = total - n_heavy_tiles;
-
-    auto decode = [&](int t) -> Tile {
-        // position t of the interleaved order -> index v in the heavy-then-light order
-        const int lt0 = static_cast<int>(n_light_tiles * t / total);
-        const int lt1 = static_cast<int>(n_light_tiles * (t + 1) / total);
-        const int v = lt1 > lt0 ? n_heavy_tiles + lt0 : t - lt0;
-        int lo = 0, hi = n_used - 1;   // last k with gpre[k] <= v
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (gpre[mid] <= v) lo = mid; else hi = mid - 1;
+    const int n_light_tiles = total - n_heavy_tiles;
+    const int n_heavy_groups = *n_heavy_s;
+    // Position t of the interleaved order is a light tile when floor(NL (t+1) / N) >
+    // floor(NL t / N) (NL light tiles of N); its index in the heavy-then-light order is
+    // then NH + floor(NL t / N), otherwise t - floor(NL t / N).  Each role walks its unit's
+    // positions t = unit, unit + n_units, ... with an iterator that keeps floor(NL t / N)
+    // and its remainder up to date by additions, and one group cursor per list (the
+    // indices of each list grow along the walk), so that a tile costs a few adds and
+    // shared-memory reads instead of a 64-bit division and a binary search.
+    const long long step_num = static_cast<long long>(n_light_tiles) * n_units;
+    const int q_step = total ? static_cast<int>(step_num / total) : 0;
+    const int r_step = total ? static_cast<int>(step_num % total) : 0;
+    struct TileIter { int lt, r, kh, kl; };
+    auto iter_at = [&](int t0) -> TileIter {
+        TileIter it;
+        const long long num = static_cast<long long>(n_light_tiles) * t0;
+        it.lt = total ? static_cast<int>(num / total) : 0;
+        it.r = total ? static_cast<int>(num % total) : 0;
+        it.kh = 0;
+        it.kl = n_heavy_groups;
+        return it;
+    };
+    auto take = [&](TileIter &it, int t) -> Tile {
+        const bool light = it.r + n_light_tiles >= total;
+        int v, k;
+        if (light) {
+            v = n_heavy_tiles + it.lt;
+            k = it.kl;
+            while (gpre[k + 1] <= v) ++k;
+            it.kl = k;
+        } else {
+            v = t - it.lt;
+            k = it.kh;
+            while (gpre[k + 1] <= v) ++k;
+            it.kh = k;
         }
-        const int cg = gord[lo];
+        it.lt += q_step;
+        it.r += r_step;
+        if (it.r >= total) { it.r -= total; ++it.lt; }
+        const int cg = gord[k];
         Tile T;
         T.pi = cg >= n0 ? 1 : 0;
         T.g = cg - (T.pi ? n0 : 0);
         const int m = gm[cg];
         const int ntn = (m + bn - 1) / bn;
-        const int local = v - gpre[lo];
+        const int local = v - gpre[k];
         T.mt = local / ntn;
         const int nt = local - T.mt * ntn;
         T.row0 = gstart[cg] + nt * bn;
@@ -289,8 +316,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
             uint32_t s = 0, ph = 0;
             unsigned char *a = stage_base;
             const uint32_t full_c0 = PAIR ? mapa_shared(smem_u32(full), 0) : 0u;   // even CTA's full[0]
+            TileIter iter = iter_at(unit);
             for (int t = unit; t < total && ok; t += n_units) {
-                const Tile T = decode(t);
+                const Tile T = take(iter, t);
                 const ProbDev &P = p.prob[T.pi];
                 int a0, a1, brow;
                 boxes(T, a0, a1, brow);
@@ -338,8 +366,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
             const uint32_t stage16 = static_cast<uint32_t>(stage_bytes) >> 4;  // descriptor units
             uint32_t s = 0, ph = 0, soff = 0, tc = 0;
             bool ok = true;
+            TileIter iter = iter_at(unit);
             for (int t = unit; t < total && ok; t += n_units, ++tc) {
-                const Tile T = decode(t);
+                const Tile T = take(iter, t);
                 const ProbDev &P = p.prob[T.pi];
                 const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
                 if (!mbar_wait(&tempty[b], tph ^ 1u, abort_flag, p.status, tmo)) { ok = false; break; }
@@ -379,8 +408,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
         // ----------------------------------------------------------------- epilogue
         const int q = warp & 3;                 // TMEM lane quarter of this warp
         uint32_t tc = 0, cc = 0;
+        TileIter iter = iter_at(unit);
         for (int t = unit; t < total; t += n_units, ++tc) {
-            const Tile T = decode(t);
+            const Tile T = take(iter, t);
             const ProbDev &P = p.prob[T.pi];
             const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
             const bool ok = mbar_wait(&tfull[b], tph, abort_flag, p.status, tmo);
