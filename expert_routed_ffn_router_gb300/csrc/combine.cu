@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(CT) combine_kernel(const uint4 *__restrict__ Y
                                                      const float4 *__restrict__ Ysh, int H,
                                                      int K, float4 *__restrict__ Y)
 {
+    pdl_wait();
     const int t = blockIdx.x;
     const int c = blockIdx.y * COLS + threadIdx.x * 8;
     if (c >= H) return;
@@ -62,10 +63,8 @@ cudaError_t launch_combine(const void *Yp, const int32_t *slot_pos, const float 
                            const float *Ysh, int T, int H, int K, float *Y, cudaStream_t s)
 {
     dim3 grid(T, (H + COLS - 1) / COLS);
-    combine_kernel<<<grid, CT, 0, s>>>(static_cast<const uint4 *>(Yp), slot_pos, topk_w,
-                                       reinterpret_cast<const float4 *>(Ysh), H, K,
-                                       reinterpret_cast<float4 *>(Y));
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, grid, dim3(CT), 0, s, 1, static_cast<const uint4 *>(Yp), slot_pos,
+                      topk_w, reinterpret_cast<const float4 *>(Ysh), H, K, reinterpret_cast<float4 *>(Y));
 }
 
 }  // namespace moe

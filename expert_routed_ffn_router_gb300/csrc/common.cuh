@@ -45,6 +45,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ------------------------------------------------------- programmatic dependent launch
+// Kernels of the layer are launched with programmatic stream serialization, so that a
+// kernel is scheduled as the previous one drains and runs its prologue (barrier init,
+// tensor-memory allocation, descriptor prefetch) before its inputs are ready.  pdl_wait()
+// blocks until the previous kernel has completed and its writes are visible; every kernel
+// calls it before its first read of data another kernel wrote, so stream order is kept.
+// (Releasing dependents early with griddepcontrol.launch_dependents measured slower: the
+// waiting CTAs of the next kernel then sit on the SMs during the whole previous kernel.)
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // --------------------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {

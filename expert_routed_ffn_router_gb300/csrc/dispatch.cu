@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(CHUNK) masks_kernel(const int32_t *__restrict_
                                                       int E, int K, uint32_t *smask,
                                                       int32_t *chunk_cnt, int *status)
 {
+    pdl_wait();
     extern __shared__ uint32_t m_s[];    // [CW][E]
     const int c = blockIdx.x, tid = threadIdx.x;
     const int w = tid >> 5, lane = tid & 31;
@@ -62,6 +63,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(int E, int n_chunks,
                                                     int32_t *chunk_base, int32_t *counts,
                                                     int32_t *offsets)
 {
+    pdl_wait();
     __shared__ int warp_sums[32];
     const int e = threadIdx.x, lane = e & 31, w = e >> 5;
     int total = 0;
@@ -105,6 +107,7 @@ __global__ void __launch_bounds__(CHUNK) scatter_kernel(const int32_t *__restric
                                                         const int32_t *chunk_base, int32_t *perm,
                                                         int32_t *slot_pos)
 {
+    pdl_wait();
     extern __shared__ uint32_t sh[];
     uint32_t *m_s = sh;                                  // [CW][E]
     int32_t *base = reinterpret_cast<int32_t *>(sh + CW * E);  // [CW][E]
@@ -140,6 +143,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4 *__restrict__ X
                                                      const int32_t *__restrict__ offsets,
                                                      int E, uint4 *__restrict__ Xp)
 {
+    pdl_wait();
     const int n_rows = offsets[E];
     const int vec = H / 8;
     const int lane = threadIdx.x & 31;
@@ -162,6 +166,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4 *__restrict__ X
 __global__ void __launch_bounds__(256) affinity_kernel(const uint32_t *__restrict__ smask,
                                                        int n_words, int E, int32_t *aff)
 {
+    pdl_wait();
     __shared__ uint32_t A[64][33];
     __shared__ uint32_t B[64][33];
     const int i0 = blockIdx.y * 32, j0 = blockIdx.x * 32;
@@ -203,6 +208,7 @@ __global__ void __launch_bounds__(CHUNK) route_small_kernel(const int32_t *__res
                                                             int32_t *slot_pos, uint32_t *smask,
                                                             int *status)
 {
+    pdl_wait();
     extern __shared__ uint32_t sm[];
     uint32_t *m_s = sm;                                          // [CW][E]
     int32_t *base = reinterpret_cast<int32_t *>(sm + CW * E);    // [CW][E]
@@ -304,45 +310,57 @@ cudaError_t launch_dispatch(const void *X, const int32_t *topk_idx, int T, int H
         const size_t sm = 2 * m_smem + (E + 1) * sizeof(int32_t);
         err = ensure_smem(reinterpret_cast<const void *>(route_small_kernel), sm);
         if (err != cudaSuccess) return err;
-        route_small_kernel<<<1, CHUNK, sm, s>>>(topk_idx, T, E, K, counts, offsets, perm,
-                                                slot_pos, scr.smask, status);
+        if ((err = launch_pdl(route_small_kernel, dim3(1), dim3(CHUNK), sm, s, 1, topk_idx, T, E, K,
+                              counts, offsets, perm, slot_pos, scr.smask, status)) != cudaSuccess)
+            return err;
         if (affinity) {
             dim3 g((E + 31) / 32, (E + 31) / 32);
-            affinity_kernel<<<g, 256, 0, s>>>(scr.smask, plan.n_words, E, affinity);
+            if ((err = launch_pdl(affinity_kernel, g, dim3(256), 0, s, 1,
+                                  static_cast<const uint32_t *>(scr.smask), plan.n_words, E, affinity)) != cudaSuccess)
+                return err;
         }
         if (Xp) {
             const long long rows = static_cast<long long>(T) * K;
             long long blocks = (rows + 7) / 8;
             const long long cap = static_cast<long long>(num_sms()) * 8;
             if (blocks > cap) blocks = cap;
-            gather_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(
-                static_cast<const uint4 *>(X), H, perm, offsets, E, static_cast<uint4 *>(Xp));
+            return launch_pdl(gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, 1,
+                              static_cast<const uint4 *>(X), H, static_cast<const int32_t *>(perm),
+                              static_cast<const int32_t *>(offsets), E, static_cast<uint4 *>(Xp));
         }
-        return cudaGetLastError();
+        return cudaSuccess;
     }
     err = ensure_smem(reinterpret_cast<const void *>(masks_kernel), m_smem);
     if (err != cudaSuccess) return err;
     err = ensure_smem(reinterpret_cast<const void *>(scatter_kernel), 2 * m_smem);
     if (err != cudaSuccess) return err;
-    masks_kernel<<<plan.n_chunks, CHUNK, m_smem, s>>>(topk_idx, T, E, K, scr.smask,
-                                                      scr.chunk_cnt, status);
-    scan_kernel<<<1, 1024, 0, s>>>(E, plan.n_chunks, scr.chunk_cnt, scr.chunk_base,
-                                   counts, offsets);
-    scatter_kernel<<<plan.n_chunks, CHUNK, 2 * m_smem, s>>>(topk_idx, T, E, K, scr.smask,
-                                                            scr.chunk_base, perm, slot_pos);
+    if ((err = launch_pdl(masks_kernel, dim3(plan.n_chunks), dim3(CHUNK), m_smem, s, 1, topk_idx, T,
+                          E, K, scr.smask, scr.chunk_cnt, status)) != cudaSuccess)
+        return err;
+    if ((err = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, s, 1, E, plan.n_chunks,
+                          static_cast<const int32_t *>(scr.chunk_cnt), scr.chunk_base, counts,
+                          offsets)) != cudaSuccess)
+        return err;
+    if ((err = launch_pdl(scatter_kernel, dim3(plan.n_chunks), dim3(CHUNK), 2 * m_smem, s, 1,
+                          topk_idx, T, E, K, static_cast<const uint32_t *>(scr.smask),
+                          static_cast<const int32_t *>(scr.chunk_base), perm, slot_pos)) != cudaSuccess)
+        return err;
     if (affinity) {
         dim3 g((E + 31) / 32, (E + 31) / 32);
-        affinity_kernel<<<g, 256, 0, s>>>(scr.smask, plan.n_words, E, affinity);
+        if ((err = launch_pdl(affinity_kernel, g, dim3(256), 0, s, 1,
+                              static_cast<const uint32_t *>(scr.smask), plan.n_words, E, affinity)) != cudaSuccess)
+            return err;
     }
     if (Xp) {
         const long long rows = static_cast<long long>(T) * K;
         long long blocks = (rows + 7) / 8;
         const long long cap = static_cast<long long>(num_sms()) * 8;
         if (blocks > cap) blocks = cap;
-        gather_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(
-            static_cast<const uint4 *>(X), H, perm, offsets, E, static_cast<uint4 *>(Xp));
+        return launch_pdl(gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, 1,
+                          static_cast<const uint4 *>(X), H, static_cast<const int32_t *>(perm),
+                          static_cast<const int32_t *>(offsets), E, static_cast<uint4 *>(Xp));
     }
-    return cudaGetLastError();
+    return cudaSuccess;
 }
 
 }  // namespace moe

@@ -89,6 +89,16 @@ struct Tile {
     int pi, g, mt, row0, nvalid;
 };
 
+// sigmoid(g) = 1 / (1 + e^-g) from the hardware exp2 and reciprocal approximations (a few
+// ulp in fp32; h is rounded to bf16 right after).  e^-g overflows to +inf for g < -88 and
+// the reciprocal of +inf is 0, the limit.
+__device__ __forceinline__ float fast_sigmoid(float g)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + __expf(-g)));
+    return r;
+}
+
 // bar.red.and over the 128 epilogue threads: every thread gets the AND of `ok`.
 __device__ __forceinline__ bool epi_all(bool ok)
 {
@@ -170,6 +180,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
             tmem_relinquish();
         }
     }
+    // everything above overlaps the previous kernel's tail; the group offsets and the
+    // activations are that kernel's (or an earlier one's) output
+    pdl_wait();
     // group row offsets -> shared memory
     const int n0 = p.prob[0].n_groups;
     const int n_cg = n0 + (p.n_probs > 1 ? p.prob[1].n_groups : 0);
@@ -455,7 +468,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
                             const int n = CW * c + j;
                             if (n < T.nvalid) {
                                 const float g = xb[j * 64 + (q - 2) * 32 + lane];
-                                const float h = g / (1.f + __expf(-g)) * v[j];
+                                const float h = g * fast_sigmoid(g) * v[j];
                                 out[static_cast<size_t>(T.row0 + n) * P.out_ld + i] = f32_to_bf16_rn(h);
                             }
                         }
@@ -600,24 +613,8 @@ cudaError_t launch_one(const FfnArgs &a, size_t smem, cudaStream_t s)
     const void *fn = reinterpret_cast<const void *>(ffn_kernel<MODE, PAIR>);
     cudaError_t err = ensure_smem(fn, smem);
     if (err != cudaSuccess) return err;
-    if (!PAIR) {
-        ffn_kernel<MODE, false><<<num_sms(), NUM_THREADS, smem, s>>>(a);
-        return cudaGetLastError();
-    }
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(static_cast<unsigned>(num_sms() / 2 * 2));
-    cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ffn_kernel<MODE, true>, a);
+    if (!PAIR) return launch_pdl(ffn_kernel<MODE, false>, dim3(num_sms()), dim3(NUM_THREADS), smem, s, 1, a);
+    return launch_pdl(ffn_kernel<MODE, true>, dim3(num_sms() / 2 * 2), dim3(NUM_THREADS), smem, s, 2, a);
 }
 
 }  // namespace

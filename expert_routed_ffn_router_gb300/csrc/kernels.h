@@ -73,6 +73,35 @@ struct FfnProblem {
 // Enqueues the up projection (+SwiGLU) and the down projection of up to two problems
 // (the routed experts and the shared expert) that share H; I may differ per problem.
 // `mid_event` (nullable) is recorded on `s` between the up and the down launch.
+// Launch with programmatic stream serialization (the kernel overlaps its prologue with
+// the previous kernel's tail and calls pdl_wait() before reading its inputs) and, with
+// cluster_x > 1, clusters of cluster_x CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, int cluster_x, Args... args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = static_cast<unsigned>(n);
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // 0 automatic, 1 single-CTA kernel, 2 CTA-pair kernel (testing hook)
 void set_ffn_variant(int v);
 

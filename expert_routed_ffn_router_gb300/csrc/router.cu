@@ -667,6 +667,7 @@ __device__ void refine_token_warp(const RouterArgs &a, int t, uint32_t cand, int
 template <class C, int GEMV>   // GEMV = token batch of the tiny-batch path, 0 = tile GEMM
 __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
 {
+    pdl_wait();
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_last, s_npairs, s_npend;
     __shared__ int s_pend[3 * C::TT];     // (token, first pair, pair count) to refine
@@ -807,6 +808,7 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
 template <class C>
 __global__ void __launch_bounds__(NT, 2) router_gemm_kernel(const RouterArgs a)
 {
+    pdl_wait();
     extern __shared__ __align__(16) unsigned char smem[];
     gemm_tile<C>(a, smem);
 }
@@ -814,6 +816,7 @@ __global__ void __launch_bounds__(NT, 2) router_gemm_kernel(const RouterArgs a)
 // One warp per token: split-K sum, scoring, certified top-K, refine when needed.
 __global__ void __launch_bounds__(NT) router_finalize_kernel(const RouterArgs a, int TT)
 {
+    pdl_wait();
     extern __shared__ __align__(16) unsigned char smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * NW + warp;
@@ -937,22 +940,20 @@ cudaError_t launch_router(const void *X, const void *Wg, const float *bias, int 
         err = ensure_smem(fn, plan.smem_bytes);
         if (err != cudaSuccess) return err;
         switch (plan.gemv) {
-        case 1: router_fused_kernel<SmallCfg, 1><<<grid, NT, plan.smem_bytes, s>>>(a); break;
-        case 2: router_fused_kernel<SmallCfg, 2><<<grid, NT, plan.smem_bytes, s>>>(a); break;
-        case 4: router_fused_kernel<SmallCfg, 4><<<grid, NT, plan.smem_bytes, s>>>(a); break;
-        default: router_fused_kernel<SmallCfg, 0><<<grid, NT, plan.smem_bytes, s>>>(a); break;
+        case 1: return launch_pdl(router_fused_kernel<SmallCfg, 1>, grid, dim3(NT), plan.smem_bytes, s, 1, a);
+        case 2: return launch_pdl(router_fused_kernel<SmallCfg, 2>, grid, dim3(NT), plan.smem_bytes, s, 1, a);
+        case 4: return launch_pdl(router_fused_kernel<SmallCfg, 4>, grid, dim3(NT), plan.smem_bytes, s, 1, a);
+        default: return launch_pdl(router_fused_kernel<SmallCfg, 0>, grid, dim3(NT), plan.smem_bytes, s, 1, a);
         }
-        return cudaGetLastError();
     }
     err = ensure_smem(reinterpret_cast<const void *>(router_gemm_kernel<LargeCfg>), plan.smem_bytes);
     if (err != cudaSuccess) return err;
-    router_gemm_kernel<LargeCfg><<<grid, NT, plan.smem_bytes, s>>>(a);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if ((err = launch_pdl(router_gemm_kernel<LargeCfg>, grid, dim3(NT), plan.smem_bytes, s, 1, a)) != cudaSuccess)
+        return err;
     const size_t fs = finalize_smem(E);
     err = ensure_smem(reinterpret_cast<const void *>(router_finalize_kernel), fs);
     if (err != cudaSuccess) return err;
-    router_finalize_kernel<<<(T + NW - 1) / NW, NT, fs, s>>>(a, plan.TT);
-    return cudaGetLastError();
+    return launch_pdl(router_finalize_kernel, dim3((T + NW - 1) / NW), dim3(NT), fs, s, 1, a, plan.TT);
 }
 
 }  // namespace moe
