@@ -30,6 +30,9 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer tokens/s on 1 GB300 (DeepSeek-V3 shape)"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# stage events: before the router, after the router, after dispatch, between the FFN's up-
+# and down-projection launches (small token tiles run both in one launch: then the mark
+# follows it and ffn_down reads ~0), after the FFN, after combine
 STAGES = ("router", "dispatch", "ffn_up", "ffn_down", "combine")
 
 
@@ -114,17 +117,17 @@ def algorithmic(w, n_act: int):
     b = {
         "router": E * H * 2 + T * H * 2 + T * K * 8,
         "dispatch": T * H * 2 + TK * H * 2 + T * K * 4 * 3,
-        "ffn_up": (n_act * 2 * H * I + (2 * H * Is if Is else 0)) * 2 + (TK + T) * H * 2
-                  + (TK * I + T * Is) * 2,
-        "ffn_down": (n_act * I * H + Is * H) * 2 + (TK * I + T * Is) * 2 + TK * H * 2
-                    + (T * H * 4 if Is else 0),
+        # weights of the activated experts (+ shared), token rows in, outputs out; the
+        # intermediate h stays on chip or in L2 between the two projections and is not
+        # counted
+        "ffn": (n_act * 3 * H * I + (3 * H * Is if Is else 0)) * 2 + (TK + T) * H * 2
+               + TK * H * 2 + (T * H * 4 if Is else 0),
         "combine": TK * H * 2 + (T * H * 4 if Is else 0) + T * H * 4 + T * K * 8,
     }
     f = {
         "router": 2 * T * E * H,
         "dispatch": 0,
-        "ffn_up": 2 * (TK * 2 * H * I + T * 2 * H * Is),
-        "ffn_down": 2 * (TK * I * H + T * Is * H),
+        "ffn": 2 * (TK * 3 * H * I + T * 3 * H * Is),
         "combine": 2 * TK * H,
     }
     layer_bytes = (n_act + (1 if Is else 0)) * 3 * H * I * 2 + E * H * 2 + T * H * 2 + T * H * 4
@@ -132,14 +135,21 @@ def algorithmic(w, n_act: int):
     return b, f, layer_bytes, layer_flops
 
 
-def launches_per_step(T: int, with_affinity: bool) -> int:
+def launches_per_step(w, with_affinity: bool) -> int:
     """Kernels moe_layer_forward launches: router (1 fused, or GEMM + finalise for
     T > 4096), dispatch (one bookkeeping CTA for T <= 256, else masks, scan, scatter;
-    then the affinity matrix when asked for, and the row gather), the FFN up and down
-    launches, combine."""
+    then the affinity matrix when asked for, and the row gather), the FFN (one launch for
+    the up and down projections when the token tile is at most 32 rows, else one launch
+    each), combine."""
+    T = w.T
     router = 1 if T <= 4096 else 2
     dispatch = (1 if T <= 256 else 3) + (1 if with_affinity else 0) + 1
-    return router + dispatch + 2 + 1
+    hint = max(1, T * w.K // w.E)        # the token-tile choice of the library
+    bn = 16
+    while bn < 256 and bn < 6 * hint:
+        bn *= 2
+    ffn = 1 if bn <= 32 else 2
+    return router + dispatch + ffn + 1
 
 
 # ------------------------------------------------------------------- replica helpers
@@ -221,6 +231,7 @@ def run_ours(args, rank, world, local_rank):
     stage_ms = {name: statistics.fmean(stage_ev[k][i].elapsed_time(stage_ev[k][i + 1])
                                        for k in range(K))
                 for i, name in enumerate(STAGES)}
+    stage_ms["ffn"] = stage_ms["ffn_up"] + stage_ms["ffn_down"]
     if layer.status() != 0:
         raise RuntimeError("device status word reported an error in the timed region")
 
@@ -249,7 +260,7 @@ def run_ours(args, rank, world, local_rank):
     counts = layer.counts.cpu().numpy()
     n_act = int((counts > 0).sum())
     b, f, layer_bytes, layer_flops = algorithmic(w, n_act)
-    dom = max(("ffn_up", "ffn_down", "router", "combine", "dispatch"), key=lambda s: stage_ms[s])
+    dom = max(("ffn", "router", "combine", "dispatch"), key=lambda s: stage_ms[s])
     t_dom = stage_ms[dom] / 1e3
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     if f[dom] / max(b[dom], 1) > ridge and dom.startswith("ffn"):
@@ -283,7 +294,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(total_tokens / (ms_e2e / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(Xh.numel() * Xh.element_size()),
                 "d2h_bytes_per_step": int(Yh.numel() * Yh.element_size())},
-        "gpu_launches": K * launches_per_step(w.T, with_affinity=True),
+        "gpu_launches": K * launches_per_step(w, with_affinity=True),
         "roofline": roof,
         "layer_roofline": {"algorithmic_bytes": int(layer_bytes),
                            "hbm_frac": round(layer_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),

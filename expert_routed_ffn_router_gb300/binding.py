@@ -59,6 +59,7 @@ def load(build_if_missing: bool = True):
         "moe_router_topk": ([P, P, P, I, I, I, I, P, P, P, Z, P], I),
         "moe_dispatch": ([P, P, I, I, I, I, P, P, P, P, P, P, P, Z, P], I),
         "moe_expert_ffn": ([P, P, I, I, I, I, P, P, P, P, I, P, Z, P], I),
+        "moe_expert_ffn_workspace_bytes": ([I, I, I], Z),
         "moe_combine": ([P, P, P, P, I, I, I, P, P], I),
         "moe_layer_forward": ([ctypes.POINTER(MoeShape), ctypes.POINTER(MoeWeights), P, P, P,
                                P, P, P, P, Z, P], I),
@@ -140,6 +141,10 @@ def moe_dispatch(X, topk_idx, E, counts, offsets, perm, slot_pos, Xp, affinity, 
         _ptr(X), _ptr(topk_idx), T, H, int(E), K, _ptr(counts), _ptr(offsets), _ptr(perm),
         _ptr(slot_pos), _ptr(Xp), _ptr(affinity), _ptr(ws), ws.numel() * ws.element_size(),
         _stream(stream)))
+
+
+def moe_expert_ffn_workspace_bytes(rows: int, n_groups: int, I: int) -> int:
+    return int(load().moe_expert_ffn_workspace_bytes(int(rows), int(n_groups), int(I)))
 
 
 def moe_expert_ffn(Xp, offsets, n_groups, W1, W3, W2, Yp, ws, stream=None):

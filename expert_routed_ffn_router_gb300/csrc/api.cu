@@ -131,6 +131,7 @@ struct LayerLayout {
     int32_t *offsets, *perm, *slot_pos;
     void *Xp, *h, *Yp, *hs;
     float *Ysh;
+    unsigned *ready;
     size_t bytes;
 };
 LayerLayout layer_layout(const moe_shape_t &s, unsigned char *ws)
@@ -149,6 +150,8 @@ LayerLayout layer_layout(const moe_shape_t &s, unsigned char *ws)
     L.Yp = take(TK * s.H * 2);
     L.hs = take(static_cast<size_t>(s.T) * s.I_shared * 2);
     L.Ysh = reinterpret_cast<float *>(take(s.I_shared > 0 ? static_cast<size_t>(s.T) * s.H * 4 : 0));
+    L.ready = reinterpret_cast<unsigned *>(
+        take(ffn_ready_slots(static_cast<long long>(TK) + s.T, s.E + 1) * sizeof(unsigned)));
     L.bytes = o;
     return L;
 }
@@ -253,6 +256,13 @@ int moe_dispatch(const void *X, const int32_t *topk_idx, int T, int H, int E, in
                                        static_cast<cudaStream_t>(stream)));
 }
 
+size_t moe_expert_ffn_workspace_bytes(int rows, int n_groups, int I)
+{
+    if (rows < 0 || n_groups <= 0 || n_groups > 1024 || I <= 0) return 0;
+    return kHeader + al256(static_cast<size_t>(rows) * I * 2) +
+           al256(ffn_ready_slots(rows, n_groups) * sizeof(unsigned));
+}
+
 int moe_expert_ffn(const void *Xp, const int32_t *offsets, int n_groups, int rows, int H, int I,
                    const void *W1, const void *W3, const void *W2, void *Yp, int out_fp32,
                    void *ws, size_t ws_bytes, void *stream)
@@ -263,7 +273,8 @@ int moe_expert_ffn(const void *Xp, const int32_t *offsets, int n_groups, int row
     int rc = check_ptrs({Xp, offsets, W1, W3, W2, Yp});
     if (rc) return rc;
     const size_t hbytes = al256(static_cast<size_t>(rows) * I * 2);
-    if ((rc = check_ws(ws, ws_bytes, kHeader + hbytes))) return rc;
+    const size_t rbytes = al256(ffn_ready_slots(rows, n_groups) * sizeof(unsigned));
+    if ((rc = check_ws(ws, ws_bytes, kHeader + hbytes + rbytes))) return rc;
     if (rows == 0) return MOE_OK;
     FfnProblem P{};
     P.act = Xp;
@@ -275,7 +286,8 @@ int moe_expert_ffn(const void *Xp, const int32_t *offsets, int n_groups, int row
     P.out = Yp;
     P.out_fp32 = out_fp32;
     const int hint = rows / n_groups > 0 ? rows / n_groups : 1;
-    return cuda_status(launch_ffn(&P, 1, H, &I, hint, static_cast<int *>(ws),
+    unsigned *ready = reinterpret_cast<unsigned *>(static_cast<unsigned char *>(ws) + kHeader + hbytes);
+    return cuda_status(launch_ffn(&P, 1, H, &I, hint, ready, static_cast<int *>(ws),
                                   static_cast<cudaStream_t>(stream), g_wait_limit_ns,
                                   g_inject_stall, nullptr));
 }
@@ -348,7 +360,7 @@ int moe_layer_forward(const moe_shape_t *shape, const moe_weights_t *wt, const v
     }
     long long hint = static_cast<long long>(s.T) * s.K / s.E;
     if (hint < 1) hint = 1;
-    e = launch_ffn(P, n_probs, s.H, Ipp, static_cast<int>(hint), status, st, g_wait_limit_ns,
+    e = launch_ffn(P, n_probs, s.H, Ipp, static_cast<int>(hint), L.ready, status, st, g_wait_limit_ns,
                    g_inject_stall, g_stage_events_on ? g_stage_events[3] : nullptr);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     record_stage(4, st);

@@ -70,9 +70,6 @@ struct FfnProblem {
     int out_fp32;
 };
 
-// Enqueues the up projection (+SwiGLU) and the down projection of up to two problems
-// (the routed experts and the shared expert) that share H; I may differ per problem.
-// `mid_event` (nullable) is recorded on `s` between the up and the down launch.
 // Launch with programmatic stream serialization (the kernel overlaps its prologue with
 // the previous kernel's tail and calls pdl_wait() before reading its inputs) and, with
 // cluster_x > 1, clusters of cluster_x CTAs.
@@ -105,9 +102,19 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // 0 automatic, 1 single-CTA kernel, 2 CTA-pair kernel (testing hook)
 void set_ffn_variant(int v);
 
+// Enqueues the up projection (+SwiGLU) and the down projection of up to two problems
+// (the routed experts and the shared expert) that share H; I may differ per problem.  One
+// persistent launch runs the up-projection tiles, then the down-projection tiles; a down
+// tile starts once the h rows of its token tile are complete, tracked by `ready` (device,
+// ffn_ready_slots(...) counters, zeroed here).  `mid_event` (nullable) is recorded after
+// the launch.
 cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I_per_prob,
-                       int token_hint, int *status, cudaStream_t s,
+                       int token_hint, unsigned *ready, int *status, cudaStream_t s,
                        unsigned long long timeout_ns, int inject, cudaEvent_t mid_event);
+
+// Readiness counters launch_ffn needs (unsigned each) for `rows` rows in `n_groups` groups
+// over all its problems.
+size_t ffn_ready_slots(long long rows, int n_groups);
 
 // Raises the dynamic shared-memory limit of `func` to `bytes` once per process and size
 // (a no-op afterwards, so launches stay capturable).

@@ -532,33 +532,44 @@ __device__ void gemm_tile(const RouterArgs &a, unsigned char *smem)
 }
 
 // ----------------------------------------------------------- tiny batches (T <= 4)
-// One warp per expert reads its gate row once and forms the logits of all T tokens; each
-// (token, expert) logit is 8 independent fp32 chains (one per element of a 16-byte vector,
-// H/256 products each) added by a fixed 3-level tree and a 5-level warp tree.
+// GEMV_QW warps share one expert's gate row, each reading a quarter of it once and forming
+// the partial logits of all T tokens; a CTA holds GEMV_EPC experts, so the whole gate
+// matrix is read by E * GEMV_QW warps spread over the GPU (a cold read of 3.7 MB is
+// latency-bound: it needs many loads in flight).  Each partial is 8 independent fp32
+// chains (one per element of a 16-byte vector) added by a fixed 3-level tree and a
+// 5-level warp tree; the quarters are added by a fixed 2-level tree.
 constexpr int GEMV_TMAX = 4;      // beyond 4 tokens the 16x256 tile path is faster
+constexpr int GEMV_QW = 4;        // warps per gate row
+constexpr int GEMV_EPC = NW / GEMV_QW;
 
 template <int TB>     // token batch: 1, 2 or 4 (>= T)
-__device__ void gemv_tile(const RouterArgs &a)
+__device__ void gemv_tile(const RouterArgs &a, unsigned char *smem)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * NW + warp;
+    const int el = warp / GEMV_QW, qw = warp % GEMV_QW;
+    const int e = blockIdx.x * GEMV_EPC + el;
     const int T = a.T, nv = a.H / 8;
+    const int v_beg = nv * qw / GEMV_QW, v_end = nv * (qw + 1) / GEMV_QW;
+    constexpr int RS = 2 * TB + 1;                    // per warp: dots, gate norm, token norms
+    float *red = reinterpret_cast<float *>(smem);     // [NW][RS]
     if (e < a.E) {
         const uint4 *wr = reinterpret_cast<const uint4 *>(a.Wg + static_cast<size_t>(e) * a.H);
         const uint4 *xr = reinterpret_cast<const uint4 *>(a.X);
-        float acc[TB][8];
+        float acc[TB][8], xq[TB];
 #pragma unroll
-        for (int t = 0; t < TB; ++t)
+        for (int t = 0; t < TB; ++t) {
+            xq[t] = 0.f;
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[t][j] = 0.f;
+        }
         float wsq = 0.f;
         constexpr int U = TB <= 2 ? 4 : 2;       // vectors per lane in flight
-        for (int v0 = lane; v0 < nv; v0 += 32 * U) {
+        for (int v0 = v_beg + lane; v0 < v_end; v0 += 32 * U) {
             uint4 wv[U], xv[U][TB];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int v = v0 + 32 * u;
-                const bool ok = v < nv;
+                const bool ok = v < v_end;
                 wv[u] = ok ? __ldg(wr + v) : make_uint4(0, 0, 0, 0);
 #pragma unroll
                 for (int t = 0; t < TB; ++t)
@@ -576,7 +587,10 @@ __device__ void gemv_tile(const RouterArgs &a)
                     float xf[8];
                     unpack8(xv[u][t], xf);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[t][j] = fmaf(xf[j], wf[j], acc[t][j]);
+                    for (int j = 0; j < 8; ++j) {
+                        acc[t][j] = fmaf(xf[j], wf[j], acc[t][j]);
+                        xq[t] = fmaf(xf[j], xf[j], xq[t]);
+                    }
                 }
             }
         }
@@ -584,28 +598,38 @@ __device__ void gemv_tile(const RouterArgs &a)
         for (int t = 0; t < TB; ++t) {
             float sum = ((acc[t][0] + acc[t][1]) + (acc[t][2] + acc[t][3])) +
                         ((acc[t][4] + acc[t][5]) + (acc[t][6] + acc[t][7]));
+            float q = xq[t];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFullMask, sum, off);
-            if (lane == 0 && t < T) a.part[static_cast<size_t>(t) * a.E + e] = sum;
+            for (int off = 16; off > 0; off >>= 1) {
+                sum += __shfl_xor_sync(kFullMask, sum, off);
+                q += __shfl_xor_sync(kFullMask, q, off);
+            }
+            if (lane == 0) {
+                red[warp * RS + t] = sum;
+                red[warp * RS + TB + 1 + t] = q;
+            }
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) wsq += __shfl_xor_sync(kFullMask, wsq, off);
-        if (lane == 0) a.wsq[e] = wsq;
+        if (lane == 0) red[warp * RS + TB] = wsq;
     }
-    if (blockIdx.x == 0 && warp == NW - 1) {     // token norms
-        for (int t = 0; t < T; ++t) {
-            const uint4 *xr = reinterpret_cast<const uint4 *>(a.X + static_cast<size_t>(t) * a.H);
-            float q = 0.f;
-            for (int v = lane; v < nv; v += 32) {
-                float xf[8];
-                unpack8(__ldg(xr + v), xf);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) q = fmaf(xf[j], xf[j], q);
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) q += __shfl_xor_sync(kFullMask, q, off);
-            if (lane == 0) a.xsq[t] = q;
-        }
+    __syncthreads();
+    // quarters -> logits, gate norms and (once, in CTA 0) token norms
+    auto quarters = [&](int elx, int k) {
+        const float *r = red + elx * GEMV_QW * RS + k;
+        return (r[0] + r[RS]) + (r[2 * RS] + r[3 * RS]);
+    };
+    static_assert(GEMV_QW == 4, "the quarter tree adds four partials");
+    const int tid = threadIdx.x;
+    if (tid < GEMV_EPC * TB) {
+        const int elx = tid / TB, t = tid % TB, ex = blockIdx.x * GEMV_EPC + elx;
+        if (ex < a.E && t < T) a.part[static_cast<size_t>(t) * a.E + ex] = quarters(elx, t);
+    } else if (tid < GEMV_EPC * TB + GEMV_EPC) {
+        const int elx = tid - GEMV_EPC * TB, ex = blockIdx.x * GEMV_EPC + elx;
+        if (ex < a.E) a.wsq[ex] = quarters(elx, TB);
+    } else if (blockIdx.x == 0 && tid < GEMV_EPC * TB + GEMV_EPC + TB) {
+        const int t = tid - GEMV_EPC * TB - GEMV_EPC;
+        if (t < T) a.xsq[t] = quarters(0, TB + 1 + t);
     }
 }
 
@@ -673,7 +697,7 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
     __shared__ int s_pend[3 * C::TT];     // (token, first pair, pair count) to refine
 
     if constexpr (GEMV > 0)
-        gemv_tile<GEMV>(a);
+        gemv_tile<GEMV>(a, smem);
     else
         gemm_tile<C>(a, smem);
 
@@ -884,7 +908,7 @@ RouterPlan router_plan(int T, int H, int E)
     if (T <= GEMV_TMAX)
         for (p.gemv = 1; p.gemv < T; p.gemv <<= 1) {}
     p.TT = small ? SmallCfg::TT : LargeCfg::TT;
-    p.TE = p.gemv ? NW : (small ? SmallCfg::TE : LargeCfg::TE);
+    p.TE = p.gemv ? GEMV_EPC : (small ? SmallCfg::TE : LargeCfg::TE);
     p.nTT = (T + p.TT - 1) / p.TT;
     p.nET = (E + p.TE - 1) / p.TE;
     p.S = H / KST;
@@ -892,7 +916,7 @@ RouterPlan router_plan(int T, int H, int E)
     const int target = 2 * num_sms();
     if (p.gemv) {
         p.KS = 1;
-        p.depth = (H / 8 + 31) / 32 + 3 + 5 + 2;
+        p.depth = ((H / 8 + GEMV_QW - 1) / GEMV_QW + 31) / 32 + 3 + 5 + 2 + 2;
     } else {
         // at most 32 stages per split keeps the summation depth (and the error bound) small
         p.KS = (p.S + 31) / 32;

@@ -104,8 +104,9 @@ void moe_debug_set_wait_limit(unsigned long long limit_ns, int inject_stall);
 
 /* Profiling hook: with `events` pointing at n >= 6 cudaEvent_t handles, every later
  * moe_layer_forward records them on its stream: [0] before the router, [1] after the
- * router, [2] after dispatch, [3] after the FFN up-projection launch, [4] after the FFN
- * down-projection launch, [5] after combine.  events == NULL switches recording off.  The
+ * router, [2] after dispatch, [3] between the expert FFN's up- and down-projection
+ * launches (after the FFN when small token tiles run both projections in one launch),
+ * [4] after the FFN, [5] after combine.  events == NULL switches recording off.  The
  * handles stay owned by the caller and must outlive the recording calls. */
 void moe_debug_set_stage_events(void *const *events, int n);
 
@@ -183,8 +184,13 @@ int moe_dispatch(const void *X, const int32_t *topk_idx, int T, int H, int E, in
  *   W1, W3  bf16 [n_groups, H, I];  W2 bf16 [n_groups, I, H]
  *   out Yp  [rows, H], bf16 (out_fp32 == 0) or fp32 (out_fp32 == 1)
  *   rows    upper bound of offsets[n_groups] (sizes the tensor maps and the workspace)
- *   ws / ws_bytes: workspace (holds the bf16 activation h [rows, I]).
+ *   ws / ws_bytes: at least moe_expert_ffn_workspace_bytes(rows, n_groups, I) bytes (the
+ *           bf16 activation h [rows, I] and per-token-tile completion counters).
  * The shared expert is the case n_groups = 1, offsets = {0, T}. */
+/* Workspace bytes moe_expert_ffn needs for `rows` rows in `n_groups` groups of
+ * intermediate size I (0 for invalid arguments).  Not on the pages: a sizing helper. */
+size_t moe_expert_ffn_workspace_bytes(int rows, int n_groups, int I);
+
 int moe_expert_ffn(const void *Xp, const int32_t *offsets, int n_groups, int rows,
                    int H, int I,
                    const void *W1, const void *W3, const void *W2,
