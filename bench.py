@@ -16,6 +16,7 @@ collective on the data path (the timing is reduced with a max over ranks).
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -109,6 +110,25 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------ accounting
+def ffn_traffic(workload: str):
+    """DRAM bytes per step of the FFN launches from the committed ncu record, or None when
+    the record does not cover this workload or the FFN sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "ffn_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        h = hashlib.sha256()
+        for src in rec["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != rec["sources_sha256"]:
+            return None
+        return rec["bytes_per_step"].get(workload)
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+
 def algorithmic(w, n_act: int):
     """Per-launch algorithmic bytes and FLOPs of each stage (what the method must move or
     compute: the weights of the activated experts, the activations in and out)."""
@@ -272,7 +292,7 @@ def run_ours(args, rank, world, local_rank):
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = None
+    roof["traffic"] = ffn_traffic(w.name) if dom == "ffn" else None
     roof["kernel"] = dom
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
     roof["algorithmic_bytes_per_launch"] = int(b[dom])
