@@ -158,12 +158,12 @@ def algorithmic(w, n_act: int):
 def launches_per_step(w, with_affinity: bool) -> int:
     """Kernels moe_layer_forward launches: router (1 fused, or GEMM + finalise for
     T > 4096), dispatch (one bookkeeping CTA for T <= 256, else masks, scan, scatter;
-    then the affinity matrix when asked for, and the row gather), the FFN (one launch for
-    the up and down projections when the token tile is at most 32 rows, else one launch
-    each), combine."""
+    then one launch for the affinity matrix, the row gather and the zeroing of the FFN's
+    counters), the FFN (one launch for the up and down projections when the token tile is
+    at most 32 rows, else one launch each), combine."""
     T = w.T
     router = 1 if T <= 4096 else 2
-    dispatch = (1 if T <= 256 else 3) + (1 if with_affinity else 0) + 1
+    dispatch = (1 if T <= 256 else 3) + 1
     hint = max(1, T * w.K // w.E)        # the token-tile choice of the library
     bn = 16
     while bn < 256 and bn < 6 * hint:

@@ -252,7 +252,7 @@ int moe_dispatch(const void *X, const int32_t *topk_idx, int T, int H, int E, in
     if ((rc = check_ws(ws, ws_bytes, kHeader + L.bytes))) return rc;
     if (T == 0) return MOE_OK;
     return cuda_status(launch_dispatch(X, topk_idx, T, H, E, K, counts, offsets, perm, slot_pos,
-                                       Xp, affinity, L.plan, L.scr, static_cast<int *>(ws),
+                                       Xp, affinity, L.plan, L.scr, nullptr, 0, static_cast<int *>(ws),
                                        static_cast<cudaStream_t>(stream)));
 }
 
@@ -287,7 +287,7 @@ int moe_expert_ffn(const void *Xp, const int32_t *offsets, int n_groups, int row
     P.out_fp32 = out_fp32;
     const int hint = rows / n_groups > 0 ? rows / n_groups : 1;
     unsigned *ready = reinterpret_cast<unsigned *>(static_cast<unsigned char *>(ws) + kHeader + hbytes);
-    return cuda_status(launch_ffn(&P, 1, H, &I, hint, ready, static_cast<int *>(ws),
+    return cuda_status(launch_ffn(&P, 1, H, &I, hint, ready, false, static_cast<int *>(ws),
                                   static_cast<cudaStream_t>(stream), g_wait_limit_ns,
                                   g_inject_stall, nullptr));
 }
@@ -330,8 +330,10 @@ int moe_layer_forward(const moe_shape_t *shape, const moe_weights_t *wt, const v
                                   L.r.plan, L.r.scr, status, st);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     record_stage(1, st);
+    // the dispatch tail also zeroes the FFN's readiness counters
+    const size_t n_ready = ffn_ready_slots(static_cast<long long>(s.T) * s.K + s.T, s.E + 1);
     e = launch_dispatch(X, topk_idx, s.T, s.H, s.E, s.K, counts, L.offsets, L.perm, L.slot_pos,
-                        L.Xp, affinity, L.d.plan, L.d.scr, status, st);
+                        L.Xp, affinity, L.d.plan, L.d.scr, L.ready, n_ready, status, st);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     record_stage(2, st);
 
@@ -360,7 +362,7 @@ int moe_layer_forward(const moe_shape_t *shape, const moe_weights_t *wt, const v
     }
     long long hint = static_cast<long long>(s.T) * s.K / s.E;
     if (hint < 1) hint = 1;
-    e = launch_ffn(P, n_probs, s.H, Ipp, static_cast<int>(hint), L.ready, status, st, g_wait_limit_ns,
+    e = launch_ffn(P, n_probs, s.H, Ipp, static_cast<int>(hint), L.ready, true, status, st, g_wait_limit_ns,
                    g_inject_stall, g_stage_events_on ? g_stage_events[3] : nullptr);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     record_stage(4, st);

@@ -137,18 +137,18 @@ __global__ void __launch_bounds__(CHUNK) scatter_kernel(const int32_t *__restric
     }
 }
 
-// Xp[r] = X[perm[r]] for r < offsets[E]; one warp per row, 16-byte vectors.
-__global__ void __launch_bounds__(256) gather_kernel(const uint4 *__restrict__ X, int H,
-                                                     const int32_t *__restrict__ perm,
-                                                     const int32_t *__restrict__ offsets,
-                                                     int E, uint4 *__restrict__ Xp)
+// Xp[r] = X[perm[r]] for r < offsets[E]; one warp per row, 16-byte vectors; `gb` / `ngb`
+// are this block's index and the block count of the gather part of the launch.
+__device__ __forceinline__ void gather_rows(const uint4 *__restrict__ X, int H,
+                                            const int32_t *__restrict__ perm,
+                                            const int32_t *__restrict__ offsets, int E,
+                                            uint4 *__restrict__ Xp, int gb, int ngb)
 {
-    pdl_wait();
     const int n_rows = offsets[E];
     const int vec = H / 8;
     const int lane = threadIdx.x & 31;
-    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int nw = (gridDim.x * blockDim.x) >> 5;
+    const int gw = (gb * blockDim.x + threadIdx.x) >> 5;
+    const int nw = (ngb * blockDim.x) >> 5;
     for (int r = gw; r < n_rows; r += nw) {
         const uint4 *src = X + static_cast<size_t>(perm[r]) * vec;
         uint4 *dst = Xp + static_cast<size_t>(r) * vec;
@@ -163,13 +163,12 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4 *__restrict__ X
 }
 
 // affinity[i][j] = sum_w popc(smask[w][i] & smask[w][j]) for i != j, 0 on the diagonal.
-__global__ void __launch_bounds__(256) affinity_kernel(const uint32_t *__restrict__ smask,
-                                                       int n_words, int E, int32_t *aff)
+__device__ __forceinline__ void affinity_tile(const uint32_t *__restrict__ smask, int n_words,
+                                              int E, int32_t *aff, int bi, int bj)
 {
-    pdl_wait();
     __shared__ uint32_t A[64][33];
     __shared__ uint32_t B[64][33];
-    const int i0 = blockIdx.y * 32, j0 = blockIdx.x * 32;
+    const int i0 = bi * 32, j0 = bj * 32;
     const int tid = threadIdx.x;
     const int ti = tid >> 3, tj = (tid & 7) * 4;
     int acc[4] = {0, 0, 0, 0};
@@ -197,6 +196,29 @@ __global__ void __launch_bounds__(256) affinity_kernel(const uint32_t *__restric
         const int j = j0 + tj + q;
         if (j < E) aff[static_cast<size_t>(i) * E + j] = (i == j) ? 0 : acc[q];
     }
+}
+
+// The data-parallel tail of dispatch in one launch (no dependency between its parts): the
+// first n_aff blocks compute 32x32 tiles of the affinity matrix, the others gather the
+// permuted rows and zero `zero_n` words of `zero_buf` (the expert FFN's readiness
+// counters, so that its launch needs no separate memset).
+__global__ void __launch_bounds__(256) tail_kernel(const uint32_t *__restrict__ smask, int n_words,
+                                                   int E, int32_t *aff, int n_aff_x, int n_aff,
+                                                   const uint4 *__restrict__ X, int H,
+                                                   const int32_t *__restrict__ perm,
+                                                   const int32_t *__restrict__ offsets,
+                                                   uint4 *__restrict__ Xp, unsigned *zero_buf,
+                                                   int zero_n)
+{
+    pdl_wait();
+    const int b = static_cast<int>(blockIdx.x);
+    if (b < n_aff) {
+        affinity_tile(smask, n_words, E, aff, b / n_aff_x, b % n_aff_x);
+        return;
+    }
+    const int gb = b - n_aff, ngb = static_cast<int>(gridDim.x) - n_aff;
+    for (int i = gb * blockDim.x + threadIdx.x; i < zero_n; i += ngb * blockDim.x) zero_buf[i] = 0u;
+    if (Xp) gather_rows(X, H, perm, offsets, E, Xp, gb, ngb);
 }
 
 // Small batches (T <= 256, one chunk): masks, counts, scan and stable slots in one CTA --
@@ -302,7 +324,7 @@ cudaError_t launch_dispatch(const void *X, const int32_t *topk_idx, int T, int H
                             int K, int32_t *counts, int32_t *offsets, int32_t *perm,
                             int32_t *slot_pos, void *Xp, int32_t *affinity,
                             const DispatchPlan &plan, const DispatchScratch &scr,
-                            int *status, cudaStream_t s)
+                            unsigned *zero_buf, size_t zero_n, int *status, cudaStream_t s)
 {
     const size_t m_smem = static_cast<size_t>(CW) * E * sizeof(uint32_t);
     cudaError_t err;
@@ -313,54 +335,41 @@ cudaError_t launch_dispatch(const void *X, const int32_t *topk_idx, int T, int H
         if ((err = launch_pdl(route_small_kernel, dim3(1), dim3(CHUNK), sm, s, 1, topk_idx, T, E, K,
                               counts, offsets, perm, slot_pos, scr.smask, status)) != cudaSuccess)
             return err;
-        if (affinity) {
-            dim3 g((E + 31) / 32, (E + 31) / 32);
-            if ((err = launch_pdl(affinity_kernel, g, dim3(256), 0, s, 1,
-                                  static_cast<const uint32_t *>(scr.smask), plan.n_words, E, affinity)) != cudaSuccess)
-                return err;
-        }
-        if (Xp) {
-            const long long rows = static_cast<long long>(T) * K;
-            long long blocks = (rows + 7) / 8;
-            const long long cap = static_cast<long long>(num_sms()) * 8;
-            if (blocks > cap) blocks = cap;
-            return launch_pdl(gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, 1,
-                              static_cast<const uint4 *>(X), H, static_cast<const int32_t *>(perm),
-                              static_cast<const int32_t *>(offsets), E, static_cast<uint4 *>(Xp));
-        }
-        return cudaSuccess;
-    }
-    err = ensure_smem(reinterpret_cast<const void *>(masks_kernel), m_smem);
-    if (err != cudaSuccess) return err;
-    err = ensure_smem(reinterpret_cast<const void *>(scatter_kernel), 2 * m_smem);
-    if (err != cudaSuccess) return err;
-    if ((err = launch_pdl(masks_kernel, dim3(plan.n_chunks), dim3(CHUNK), m_smem, s, 1, topk_idx, T,
-                          E, K, scr.smask, scr.chunk_cnt, status)) != cudaSuccess)
-        return err;
-    if ((err = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, s, 1, E, plan.n_chunks,
-                          static_cast<const int32_t *>(scr.chunk_cnt), scr.chunk_base, counts,
-                          offsets)) != cudaSuccess)
-        return err;
-    if ((err = launch_pdl(scatter_kernel, dim3(plan.n_chunks), dim3(CHUNK), 2 * m_smem, s, 1,
-                          topk_idx, T, E, K, static_cast<const uint32_t *>(scr.smask),
-                          static_cast<const int32_t *>(scr.chunk_base), perm, slot_pos)) != cudaSuccess)
-        return err;
-    if (affinity) {
-        dim3 g((E + 31) / 32, (E + 31) / 32);
-        if ((err = launch_pdl(affinity_kernel, g, dim3(256), 0, s, 1,
-                              static_cast<const uint32_t *>(scr.smask), plan.n_words, E, affinity)) != cudaSuccess)
+    } else {
+        err = ensure_smem(reinterpret_cast<const void *>(masks_kernel), m_smem);
+        if (err != cudaSuccess) return err;
+        err = ensure_smem(reinterpret_cast<const void *>(scatter_kernel), 2 * m_smem);
+        if (err != cudaSuccess) return err;
+        if ((err = launch_pdl(masks_kernel, dim3(plan.n_chunks), dim3(CHUNK), m_smem, s, 1, topk_idx, T,
+                              E, K, scr.smask, scr.chunk_cnt, status)) != cudaSuccess)
+            return err;
+        if ((err = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, s, 1, E, plan.n_chunks,
+                              static_cast<const int32_t *>(scr.chunk_cnt), scr.chunk_base, counts,
+                              offsets)) != cudaSuccess)
+            return err;
+        if ((err = launch_pdl(scatter_kernel, dim3(plan.n_chunks), dim3(CHUNK), 2 * m_smem, s, 1,
+                              topk_idx, T, E, K, static_cast<const uint32_t *>(scr.smask),
+                              static_cast<const int32_t *>(scr.chunk_base), perm, slot_pos)) != cudaSuccess)
             return err;
     }
+    // affinity tiles, row gather and counter zeroing: one launch
+    const int n_aff_x = (E + 31) / 32;
+    const int n_aff = affinity ? n_aff_x * n_aff_x : 0;
+    long long gblocks = 0;
     if (Xp) {
-        const long long rows = static_cast<long long>(T) * K;
-        long long blocks = (rows + 7) / 8;
+        gblocks = (static_cast<long long>(T) * K + 7) / 8;
         const long long cap = static_cast<long long>(num_sms()) * 8;
-        if (blocks > cap) blocks = cap;
-        return launch_pdl(gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, 1,
-                          static_cast<const uint4 *>(X), H, static_cast<const int32_t *>(perm),
-                          static_cast<const int32_t *>(offsets), E, static_cast<uint4 *>(Xp));
+        if (gblocks > cap) gblocks = cap;
+    } else if (zero_n) {
+        gblocks = 1;
     }
-    return cudaSuccess;
+    if (zero_n && gblocks < 1) gblocks = 1;
+    if (n_aff + gblocks == 0) return cudaSuccess;
+    return launch_pdl(tail_kernel, dim3(static_cast<unsigned>(n_aff + gblocks)), dim3(256), 0, s, 1,
+                      static_cast<const uint32_t *>(scr.smask), plan.n_words, E, affinity, n_aff_x,
+                      n_aff, static_cast<const uint4 *>(X), H, static_cast<const int32_t *>(perm),
+                      static_cast<const int32_t *>(offsets), static_cast<uint4 *>(Xp), zero_buf,
+                      static_cast<int>(zero_n));
 }
 
 }  // namespace moe

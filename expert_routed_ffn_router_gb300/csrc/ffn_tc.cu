@@ -711,7 +711,7 @@ size_t ffn_ready_slots(long long rows, int n_groups)
 }
 
 cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I_pp,
-                       int token_hint, unsigned *ready, int *status, cudaStream_t s,
+                       int token_hint, unsigned *ready, bool ready_zeroed, int *status, cudaStream_t s,
                        unsigned long long timeout_ns, int inject, cudaEvent_t mid_event)
 {
     if (n_probs < 1 || n_probs > 2 || !ready) return cudaErrorInvalidValue;
@@ -770,8 +770,10 @@ cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I
     a.status = status;
     a.timeout_ns = timeout_ns;
     a.inject = inject;
-    cudaError_t err = cudaMemsetAsync(ready, 0, ffn_ready_slots(rows_total, n_cg) * sizeof(unsigned), s);
-    if (err != cudaSuccess) return err;
+    cudaError_t err;
+    if (!ready_zeroed &&
+        (err = cudaMemsetAsync(ready, 0, ffn_ready_slots(rows_total, n_cg) * sizeof(unsigned), s)) != cudaSuccess)
+        return err;
     const void *fn = pair ? reinterpret_cast<const void *>(ffn_kernel<true>)
                           : reinterpret_cast<const void *>(ffn_kernel<false>);
     if ((err = ensure_smem(fn, smem)) != cudaSuccess) return err;

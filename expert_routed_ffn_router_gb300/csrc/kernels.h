@@ -49,7 +49,7 @@ cudaError_t launch_dispatch(const void *X, const int32_t *topk_idx, int T, int H
                             int K, int32_t *counts, int32_t *offsets, int32_t *perm,
                             int32_t *slot_pos, void *Xp, int32_t *affinity,
                             const DispatchPlan &plan, const DispatchScratch &scr,
-                            int *status, cudaStream_t s);
+                            unsigned *zero_buf, size_t zero_n, int *status, cudaStream_t s);
 
 // -------------------------------------------------------------------------- combine
 cudaError_t launch_combine(const void *Yp, const int32_t *slot_pos, const float *topk_w,
@@ -106,10 +106,10 @@ void set_ffn_variant(int v);
 // (the routed experts and the shared expert) that share H; I may differ per problem.  One
 // persistent launch runs the up-projection tiles, then the down-projection tiles; a down
 // tile starts once the h rows of its token tile are complete, tracked by `ready` (device,
-// ffn_ready_slots(...) counters, zeroed here).  `mid_event` (nullable) is recorded after
+// ffn_ready_slots(...) counters, zeroed here unless `ready_zeroed`).  `mid_event` (nullable) is recorded after
 // the launch.
 cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I_per_prob,
-                       int token_hint, unsigned *ready, int *status, cudaStream_t s,
+                       int token_hint, unsigned *ready, bool ready_zeroed, int *status, cudaStream_t s,
                        unsigned long long timeout_ns, int inject, cudaEvent_t mid_event);
 
 // Readiness counters launch_ffn needs (unsigned each) for `rows` rows in `n_groups` groups
