@@ -137,8 +137,9 @@ __global__ void __launch_bounds__(CHUNK) scatter_kernel(const int32_t *__restric
     }
 }
 
-// Xp[r] = X[perm[r]] for r < offsets[E]; one warp per row, 16-byte vectors; `gb` / `ngb`
-// are this block's index and the block count of the gather part of the launch.
+// Xp[r] = X[perm[r]] for r < offsets[E]; one warp per row, 16-byte vectors (X small enough
+// to stay in L2: many rows in flight).  `gb` / `ngb` are this block's index and the block
+// count of the gather part of the launch.
 __device__ __forceinline__ void gather_rows(const uint4 *__restrict__ X, int H,
                                             const int32_t *__restrict__ perm,
                                             const int32_t *__restrict__ offsets, int E,
@@ -159,6 +160,41 @@ __device__ __forceinline__ void gather_rows(const uint4 *__restrict__ X, int H,
             dst[v] = a0; dst[v + 32] = a1; dst[v + 64] = a2; dst[v + 96] = a3;
         }
         for (; v < vec; v += 32) dst[v] = __ldg(src + v);
+    }
+}
+
+// Xp[slot_pos[t][j]] = X[t] for every token t and slot j < K, token by token: one warp per
+// token reads its row once (16-byte vectors, 2 KB in flight per warp) and writes it to its K
+// destination rows.  Used when X is larger than about half of L2: gathering row by row in
+// Xp order then re-reads each token row K times from HBM.
+__device__ __forceinline__ void gather_tokens(const uint4 *__restrict__ X, int T, int H, int K,
+                                            const int32_t *__restrict__ slot_pos,
+                                            uint4 *__restrict__ Xp, int gb, int ngb)
+{
+    const int vec = H / 8;
+    const int lane = threadIdx.x & 31;
+    const int gw = (gb * blockDim.x + threadIdx.x) >> 5;
+    const int nw = (ngb * blockDim.x) >> 5;
+    for (int t = gw; t < T; t += nw) {
+        const uint4 *src = X + static_cast<size_t>(t) * vec;
+        int dst_row = 0;
+        if (lane < K) dst_row = slot_pos[static_cast<size_t>(t) * K + lane];
+        for (int v0 = 0; v0 < vec; v0 += 128) {
+            uint4 a[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int v = v0 + 32 * u + lane;
+                a[u] = v < vec ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+            }
+            for (int j = 0; j < K; ++j) {
+                uint4 *dst = Xp + static_cast<size_t>(__shfl_sync(kFullMask, dst_row, j)) * vec;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int v = v0 + 32 * u + lane;
+                    if (v < vec) dst[v] = a[u];
+                }
+            }
+        }
     }
 }
 
@@ -204,11 +240,12 @@ __device__ __forceinline__ void affinity_tile(const uint32_t *__restrict__ smask
 // counters, so that its launch needs no separate memset).
 __global__ void __launch_bounds__(256) tail_kernel(const uint32_t *__restrict__ smask, int n_words,
                                                    int E, int32_t *aff, int n_aff_x, int n_aff,
-                                                   const uint4 *__restrict__ X, int H,
+                                                   const uint4 *__restrict__ X, int T, int H, int K,
+                                                   const int32_t *__restrict__ slot_pos,
                                                    const int32_t *__restrict__ perm,
                                                    const int32_t *__restrict__ offsets,
-                                                   uint4 *__restrict__ Xp, unsigned *zero_buf,
-                                                   int zero_n)
+                                                   uint4 *__restrict__ Xp, int by_token,
+                                                   unsigned *zero_buf, int zero_n)
 {
     pdl_wait();
     const int b = static_cast<int>(blockIdx.x);
@@ -218,7 +255,10 @@ __global__ void __launch_bounds__(256) tail_kernel(const uint32_t *__restrict__ 
     }
     const int gb = b - n_aff, ngb = static_cast<int>(gridDim.x) - n_aff;
     for (int i = gb * blockDim.x + threadIdx.x; i < zero_n; i += ngb * blockDim.x) zero_buf[i] = 0u;
-    if (Xp) gather_rows(X, H, perm, offsets, E, Xp, gb, ngb);
+    if (Xp) {
+        if (by_token) gather_tokens(X, T, H, K, slot_pos, Xp, gb, ngb);
+        else gather_rows(X, H, perm, offsets, E, Xp, gb, ngb);
+    }
 }
 
 // Small batches (T <= 256, one chunk): masks, counts, scan and stable slots in one CTA --
@@ -356,8 +396,9 @@ cudaError_t launch_dispatch(const void *X, const int32_t *topk_idx, int T, int H
     const int n_aff_x = (E + 31) / 32;
     const int n_aff = affinity ? n_aff_x * n_aff_x : 0;
     long long gblocks = 0;
+    const bool by_token = static_cast<long long>(T) * H * 2 >= (64ll << 20);
     if (Xp) {
-        gblocks = (static_cast<long long>(T) * K + 7) / 8;
+        gblocks = ((by_token ? static_cast<long long>(T) : static_cast<long long>(T) * K) + 7) / 8;
         const long long cap = static_cast<long long>(num_sms()) * 8;
         if (gblocks > cap) gblocks = cap;
     } else if (zero_n) {
@@ -367,9 +408,10 @@ cudaError_t launch_dispatch(const void *X, const int32_t *topk_idx, int T, int H
     if (n_aff + gblocks == 0) return cudaSuccess;
     return launch_pdl(tail_kernel, dim3(static_cast<unsigned>(n_aff + gblocks)), dim3(256), 0, s, 1,
                       static_cast<const uint32_t *>(scr.smask), plan.n_words, E, affinity, n_aff_x,
-                      n_aff, static_cast<const uint4 *>(X), H, static_cast<const int32_t *>(perm),
-                      static_cast<const int32_t *>(offsets), static_cast<uint4 *>(Xp), zero_buf,
-                      static_cast<int>(zero_n));
+                      n_aff, static_cast<const uint4 *>(X), T, H, K,
+                      static_cast<const int32_t *>(slot_pos), static_cast<const int32_t *>(perm),
+                      static_cast<const int32_t *>(offsets), static_cast<uint4 *>(Xp),
+                      by_token ? 1 : 0, zero_buf, static_cast<int>(zero_n));
 }
 
 }  // namespace moe

@@ -44,3 +44,33 @@ def test_skewed_T8192(dsv3_weights):
     w = synth.workload("skewed")
     r = check_layer(Problem(w, weights_dev=dsv3_weights), tokens=_sample(w.T, 2))
     assert r["disp"]["counts"].max() >= 0.95 * w.T  # the most popular experts: nearly every token
+
+
+def test_dispatch_gathers_token_by_token_at_prefill_size():
+    # X of 16384 x 7168 bf16 (235 MB) is larger than half of L2: the row gather then runs
+    # token by token (each token row read once, written to its K slots)
+    import torch
+    from expert_routed_ffn_router_gb300 import binding as B
+
+    w = synth.workload("prefill")
+    r = synth.routing_inputs(w)
+    to = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(DEV)
+    X, Wg, bias = to(r["X"]), to(r["W_gate"]), torch.from_numpy(r["bias"]).to(DEV)
+    T, H, E, K = w.T, w.H, w.E, w.K
+    ws = torch.zeros(B.moe_workspace_bytes(T, H, E, K, w.I, w.Is), dtype=torch.uint8, device=DEV)
+    idx = torch.empty(T, K, dtype=torch.int32, device=DEV)
+    wt = torch.empty(T, K, dtype=torch.float32, device=DEV)
+    B.moe_router_topk(X, Wg, bias, K, idx, wt, ws)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(T * K, dtype=torch.int32, device=DEV)
+    slot = torch.empty(T, K, dtype=torch.int32, device=DEV)
+    Xp = torch.empty(T * K, H, dtype=torch.bfloat16, device=DEV)
+    B.moe_dispatch(X, idx, E, counts, offsets, perm, slot, Xp, None, ws)
+    torch.cuda.synchronize()
+    assert B.moe_read_status(ws) == 0
+    p = perm.long()
+    assert torch.equal(Xp.view(torch.int16), X.view(torch.int16)[p])
+    # slot_pos is the inverse of perm, and perm lists every (token, slot) once
+    tok = torch.arange(T, device=DEV).unsqueeze(1).expand(T, K)
+    assert torch.equal(p[slot.long()], tok)
