@@ -90,6 +90,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait with acquire at cluster scope: for a barrier another CTA of the cluster arrives
+// on after writing this CTA's shared memory.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Store to the shared memory of a CTA of the cluster (shared::cluster address).
+__device__ __forceinline__ void st_shared_cluster(uint32_t cluster_addr, int v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
 // Bounded wait for the phase of `bar` with parity `parity`.  Gives up when `abort` is
 // raised by another role or after `limit_ns`; then raises `abort`, records
 // MOE_ERR_DEVICE_TIMEOUT and returns false.
@@ -101,6 +122,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            *abort = 1;
+            report(status, MOE_ERR_DEVICE_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// The same with acquire at cluster scope.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity,
+                                                  volatile int *abort, int *status,
+                                                  uint64_t limit_ns)
+{
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
         if (*abort) return false;
         if (globaltimer_ns() - t0 > limit_ns) {
             *abort = 1;

@@ -57,6 +57,7 @@ constexpr int MAX_CG = 1040;              // groups of all problems of a launch
 constexpr int CW = 32;                    // epilogue chunk: accumulator columns per TMEM load
 constexpr int XCHG_FLOATS = 2 * CW * 64;  // double-buffered G exchange (up epilogue)
 constexpr int PH_UP = 0, PH_DOWN = 1;
+constexpr int TQ = 4;                     // depth of the ring that hands claimed tiles to the roles
 constexpr int MAX_STAGES = 8;       // deeper rings measured slower at decode (HBM-bound up projection)
 
 struct ProbDev {
@@ -84,6 +85,7 @@ struct FfnArgs {
     int tmem_cols;
     int tab;                 // stride of the shared-memory group tables (>= groups + 1)
     unsigned *ready;         // per token tile: up-projection weight tiles finished
+    unsigned *next_tile;     // tile counter of this launch (zero at launch)
     int *status;
     unsigned long long timeout_ns;
     int inject;              // 1: the producer never fills a stage (bounded-wait test)
@@ -148,7 +150,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
     uint64_t *tfull = empty + S;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *tqf = drain + 1;                                // [TQ] tile slot written
+    uint64_t *tqe = tqf + TQ;                                 // [TQ] tile slot read by all roles
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tqe + TQ);
     static_assert(BK == 64, "the MMA issuer unrolls four K16 steps per stage");
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     // groups of all problems, problem 0's first: first row, rows, the tile order, the tile
@@ -161,6 +165,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
     int *gpre_up = gord + tab;                                // [tab] up tiles before gord[k]
     int *gpre_dn = gpre_up + tab;                             // [tab] down tiles before gord[k]
     int *ntp = gpre_dn + tab;                                 // [tab] token tiles before group
+    int *tq = ntp + tab;                                      // [TQ][8] claimed tiles
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint64_t tmo = p.timeout_ns;
@@ -168,8 +173,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
     // and owns the full/tempty barriers; each CTA stages half of A and half of B.
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
-    const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-    const int n_units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -181,6 +184,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
             mbar_init(&tempty[b], PAIR ? 256 : 128);
         }
         mbar_init(drain, 1);
+        for (int q = 0; q < TQ; ++q) {
+            mbar_init(&tqf[q], 1);
+            // consumers of a slot: MMA and epilogue (and in a pair the odd CTA's producer
+            // and epilogue, which read their copy of the slot)
+            mbar_init(&tqe[q], PAIR ? 4 : 2);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -305,50 +314,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
     const int light_up = n_up - heavy_up, light_dn = n_dn - heavy_dn;
     // Position t of a phase's interleaved order (N tiles, NL light) is a light tile when
     // floor(NL (t+1) / N) > floor(NL t / N); its index in the heavy-then-light order is
-    // then NH + floor(NL t / N), otherwise t - floor(NL t / N).  Each role walks its unit's
-    // positions t = unit, unit + n_units, ... with an iterator that keeps floor(NL t / N)
-    // and its remainder up to date by additions, and one group cursor per list (the
-    // indices of each list grow along the walk): a tile costs a few adds and shared-memory
-    // reads instead of a 64-bit division and a binary search.
-    struct TileIter { int ph, lt, r, kh, kl, qs, rs; };
-    auto iter_at = [&](int t) -> TileIter {
-        TileIter it;
-        it.ph = t >= n_up ? PH_DOWN : PH_UP;
-        const int N = it.ph ? n_dn : n_up, NL = it.ph ? light_dn : light_up;
-        const int tl = t - (it.ph ? n_up : 0);
-        const long long num = static_cast<long long>(NL) * tl;
-        const long long step = static_cast<long long>(NL) * n_units;
-        it.lt = N ? static_cast<int>(num / N) : 0;
-        it.r = N ? static_cast<int>(num % N) : 0;
-        it.qs = N ? static_cast<int>(step / N) : 0;
-        it.rs = N ? static_cast<int>(step % N) : 0;
-        it.kh = 0;
-        it.kl = n_heavy_groups;
-        return it;
-    };
-    auto take = [&](TileIter &it, int t) -> Tile {
-        if ((t >= n_up ? PH_DOWN : PH_UP) != it.ph) it = iter_at(t);
-        const int ph = it.ph;
+    // then NH + floor(NL t / N), otherwise t - floor(NL t / N).
+    auto decode_at = [&](int t) -> Tile {
+        const int ph = t >= n_up ? PH_DOWN : PH_UP;
         const int N = ph ? n_dn : n_up, NL = ph ? light_dn : light_up, NH = ph ? heavy_dn : heavy_up;
         const int *gpre = ph ? gpre_dn : gpre_up;
         const int tl = t - (ph ? n_up : 0);
-        const bool light = it.r + NL >= N;
-        int v, k;
-        if (light) {
-            v = NH + it.lt;
-            k = it.kl;
-            while (gpre[k + 1] <= v) ++k;
-            it.kl = k;
-        } else {
-            v = tl - it.lt;
-            k = it.kh;
-            while (gpre[k + 1] <= v) ++k;
-            it.kh = k;
+        const int lt0 = static_cast<int>(static_cast<long long>(NL) * tl / N);
+        const int lt1 = static_cast<int>(static_cast<long long>(NL) * (tl + 1) / N);
+        const int v = lt1 > lt0 ? NH + lt0 : tl - lt0;
+        int lo = 0, hi = n_used - 1;   // last k with gpre[k] <= v
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (gpre[mid] <= v) lo = mid; else hi = mid - 1;
         }
-        it.lt += it.qs;
-        it.r += it.rs;
-        if (it.r >= N) { it.r -= N; ++it.lt; }
-        const int cg = gord[k];
+        const int cg = gord[lo];
         Tile T;
         T.ph = ph;
         T.pi = cg >= n0 ? 1 : 0;
@@ -356,13 +336,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
         T.cg = cg;
         const int m = gm[cg];
         const int ntn = (m + bn - 1) / bn;
-        const int local = v - gpre[k];
+        const int local = v - gpre[lo];
         T.mt = local / ntn;
         const int nt = local - T.mt * ntn;
         T.row0 = gstart[cg] + nt * bn;
         T.nvalid = min(bn, m - nt * bn);
         T.nti = ntp[cg] + nt;
         return T;
+    };
+    // Dynamic schedule: the producer of the even CTA claims the next tile of the list from
+    // a global counter and hands it to the other roles -- and to the odd CTA of a pair --
+    // through a TQ-slot ring (tqf: written, tqe: read by every consumer).  Tiles are thus
+    // taken in list order by whichever unit is free, so the token tiles that share a weight
+    // tile are in flight together (L2 serves the second read) and the tail stays balanced.
+    // A tile with ph < 0 ends the list.
+    auto slot_read = [&](int q) -> Tile {
+        const int *e = tq + 8 * q;
+        Tile T;
+        T.ph = e[0]; T.pi = e[1]; T.g = e[2]; T.cg = e[3];
+        T.mt = e[4]; T.row0 = e[5]; T.nvalid = e[6]; T.nti = e[7];
+        return T;
+    };
+    auto tqe_arrive = [&](int q) {
+        if (PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(&tqe[q]), 0));
+        else mbar_arrive(&tqe[q]);
     };
     // MMA N: the valid rows rounded up to the instruction's granule (a pair splits N
     // evenly between its two CTAs, 16 rows each at least)
@@ -381,9 +378,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
             uint32_t s = 0, ph = 0;
             unsigned char *a = stage_base;
             const uint32_t full_c0 = PAIR ? mapa_shared(smem_u32(full), 0) : 0u;   // even CTA's full[0]
-            TileIter iter = iter_at(t_lo + unit);
-            for (int t = t_lo + unit; t < t_hi && ok; t += n_units) {
-                const Tile T = take(iter, t);
+            uint32_t qs = 0, qph = 0;
+            while (ok) {
+                Tile T;
+                if (!PAIR || leader) {
+                    // claim the next tile and publish it to every role (and to the odd CTA)
+                    if (!mbar_wait(&tqe[qs], qph ^ 1u, abort_flag, p.status, tmo)) { ok = false; break; }
+                    const int t = t_lo + static_cast<int>(atomicAdd(p.next_tile, 1u));
+                    if (t < t_hi) {
+                        T = decode_at(t);
+                    } else {
+                        T = Tile{};
+                        T.ph = -1;
+                    }
+                    const int vals[8] = {T.ph, T.pi, T.g, T.cg, T.mt, T.row0, T.nvalid, T.nti};
+                    int *e = tq + 8 * qs;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) e[j] = vals[j];
+                    mbar_arrive(&tqf[qs]);
+                    if (PAIR) {
+                        const uint32_t pe = mapa_shared(smem_u32(e), 1);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) st_shared_cluster(pe + 4u * j, vals[j]);
+                        mbar_arrive_cluster(mapa_shared(smem_u32(&tqf[qs]), 1));
+                    }
+                } else {
+                    // odd CTA of a pair: take the even CTA's claim
+                    if (!mbar_wait_cluster(&tqf[qs], qph, abort_flag, p.status, tmo)) { ok = false; break; }
+                    T = slot_read(qs);
+                    tqe_arrive(qs);
+                }
+                if (++qs == TQ) { qs = 0; qph ^= 1u; }
+                if (T.ph < 0) break;
                 const ProbDev &P = p.prob[T.pi];
                 const int mt = mt_cta(T);
                 const bool up = T.ph == PH_UP;
@@ -461,9 +487,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
             const uint32_t stage16 = static_cast<uint32_t>(stage_bytes) >> 4;  // descriptor units
             uint32_t s = 0, ph = 0, soff = 0, tc = 0;
             bool ok = true;
-            TileIter iter = iter_at(t_lo + unit);
-            for (int t = t_lo + unit; t < t_hi && ok; t += n_units, ++tc) {
-                const Tile T = take(iter, t);
+            uint32_t qs = 0, qph = 0;
+            for (;; ++tc) {
+                if (!mbar_wait(&tqf[qs], qph, abort_flag, p.status, tmo)) { ok = false; break; }
+                const Tile T = slot_read(qs);
+                tqe_arrive(qs);
+                if (++qs == TQ) { qs = 0; qph ^= 1u; }
+                if (T.ph < 0) break;
                 const ProbDev &P = p.prob[T.pi];
                 const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
                 if (!mbar_wait(&tempty[b], tph ^ 1u, abort_flag, p.status, tmo)) { ok = false; break; }
@@ -504,9 +534,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
         // ----------------------------------------------------------------- epilogue
         const int q = warp & 3;                 // TMEM lane quarter of this warp
         uint32_t tc = 0, cc = 0;
-        TileIter iter = iter_at(t_lo + unit);
-        for (int t = t_lo + unit; t < t_hi; t += n_units, ++tc) {
-            const Tile T = take(iter, t);
+        uint32_t qs = 0, qph = 0;
+        for (;; ++tc) {
+            const bool okq = (PAIR && !leader)
+                                 ? mbar_wait_cluster(&tqf[qs], qph, abort_flag, p.status, tmo)
+                                 : mbar_wait(&tqf[qs], qph, abort_flag, p.status, tmo);
+            if (!epi_all(okq)) break;
+            const Tile T = slot_read(qs);
+            named_bar_sync(4, 128);                 // every epilogue thread has read the slot
+            if (warp == 2 && lane == 0) tqe_arrive(qs);
+            if (++qs == TQ) { qs = 0; qph ^= 1u; }
+            if (T.ph < 0) break;
             const ProbDev &P = p.prob[T.pi];
             const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
             const bool ok = mbar_wait(&tfull[b], tph, abort_flag, p.status, tmo);
@@ -682,7 +720,7 @@ int pick_bn(int avg_rows)
 size_t ffn_smem_bytes(int bn_cta, int stages, int tab)
 {
     return 1024 + static_cast<size_t>(stages) * (A_BYTES + bn_cta * 128) + XCHG_FLOATS * 4 +
-           (2 * stages + 5) * 8 + 16 + 6 * static_cast<size_t>(tab) * 4;
+           (2 * stages + 5 + 2 * TQ) * 8 + 16 + (6 * static_cast<size_t>(tab) + 8 * TQ) * 4;
 }
 
 int pick_stages(int bn_cta, int tab)
@@ -777,9 +815,12 @@ cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I
     const void *fn = pair ? reinterpret_cast<const void *>(ffn_kernel<true>)
                           : reinterpret_cast<const void *>(ffn_kernel<false>);
     if ((err = ensure_smem(fn, smem)) != cudaSuccess) return err;
+    // the last two readiness slots are the tile counters of the (one or two) launches
+    unsigned *ctr = ready + ffn_ready_slots(rows_total, n_cg) - 2;
     auto go = [&](int lo, int hi) {
         a.ph_lo = lo;
         a.ph_hi = hi;
+        a.next_tile = ctr + lo;
         return pair ? launch_pdl(ffn_kernel<true>, dim3(num_sms() / 2 * 2), dim3(NUM_THREADS), smem, s, 2, a)
                     : launch_pdl(ffn_kernel<false>, dim3(num_sms()), dim3(NUM_THREADS), smem, s, 1, a);
     };
