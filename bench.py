@@ -31,9 +31,9 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer tokens/s on 1 GB300 (DeepSeek-V3 shape)"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# stage events: before the router, after the router, after dispatch, between the FFN's up-
-# and down-projection launches (small token tiles run both in one launch: then the mark
-# follows it and ffn_down reads ~0), after the FFN, after combine
+# stage events: before the router, after the router, after dispatch, after the FFN launch
+# (its up and down projections are one launch: the next mark is the same point, and
+# "ffn_down" reads ~0), after the FFN, after combine
 STAGES = ("router", "dispatch", "ffn_up", "ffn_down", "combine")
 
 
@@ -159,17 +159,11 @@ def launches_per_step(w, with_affinity: bool) -> int:
     """Kernels moe_layer_forward launches: router (1 fused, or GEMM + finalise for
     T > 4096), dispatch (one bookkeeping CTA for T <= 256, else masks, scan, scatter;
     then one launch for the affinity matrix, the row gather and the zeroing of the FFN's
-    counters), the FFN (one launch for the up and down projections when the token tile is
-    at most 32 rows, else one launch each), combine."""
+    counters), the FFN (up and down projections in one persistent launch), combine."""
     T = w.T
     router = 1 if T <= 4096 else 2
     dispatch = (1 if T <= 256 else 3) + 1
-    hint = max(1, T * w.K // w.E)        # the token-tile choice of the library
-    bn = 16
-    while bn < 256 and bn < 6 * hint:
-        bn *= 2
-    ffn = 1 if bn <= 32 else 2
-    return router + dispatch + ffn + 1
+    return router + dispatch + 1 + 1
 
 
 # ------------------------------------------------------------------- replica helpers

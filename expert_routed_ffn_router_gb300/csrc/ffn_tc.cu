@@ -30,9 +30,14 @@
 // full barriers (both CTAs' copies complete there), commits multicast to both CTAs.  Per
 // SM this halves the token-tile bytes in shared memory and the L2 reads per flop.
 //
-// Tile order.  Groups that reuse a weight tile across several token tiles (tensor-bound)
-// come first, groups with a single, at most half-full token tile (weight-streaming) after
-// them, and the two sequences are interleaved in proportion over the persistent units.
+// Tile list and schedule.  One launch holds the up-projection tiles, then the down-
+// projection tiles of every problem.  Within each phase, groups that reuse a weight tile
+// across several token tiles (tensor-bound) come first, groups with a single, at most
+// half-full token tile (weight-streaming) after them, the two sequences interleaved in
+// proportion.  Units claim tiles in list order from a global counter (dynamic schedule),
+// so the token tiles that share a weight tile are in flight together and L2 serves the
+// second read; a down tile waits (bounded) until the up tiles of its token tile have
+// published their h rows.
 //
 // Every wait is bounded (globaltimer): when one runs out the kernel records
 // MOE_ERR_DEVICE_TIMEOUT in the status word, the other roles leave their loops, copies and
@@ -89,7 +94,6 @@ struct FfnArgs {
     int *status;
     unsigned long long timeout_ns;
     int inject;              // 1: the producer never fills a stage (bounded-wait test)
-    int ph_lo, ph_hi;        // phases this launch runs: [ph_lo, ph_hi) of {up, down}
 };
 
 struct Tile {
@@ -308,8 +312,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
     const int n_used = *n_used_s;
     const int n_heavy_groups = *n_heavy_s;
     const int n_up = gpre_up[n_used], n_dn = gpre_dn[n_used];
-    const int t_lo = p.ph_lo == PH_UP ? 0 : n_up;            // positions of this launch
-    const int t_hi = p.ph_hi == PH_DOWN ? n_up : n_up + n_dn;
+    const int n_tiles = n_up + n_dn;                         // up tiles, then down tiles
     const int heavy_up = gpre_up[n_heavy_groups], heavy_dn = gpre_dn[n_heavy_groups];
     const int light_up = n_up - heavy_up, light_dn = n_dn - heavy_dn;
     // Position t of a phase's interleaved order (N tiles, NL light) is a light tile when
@@ -384,8 +387,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
                 if (!PAIR || leader) {
                     // claim the next tile and publish it to every role (and to the odd CTA)
                     if (!mbar_wait(&tqe[qs], qph ^ 1u, abort_flag, p.status, tmo)) { ok = false; break; }
-                    const int t = t_lo + static_cast<int>(atomicAdd(p.next_tile, 1u));
-                    if (t < t_hi) {
+                    const int t = static_cast<int>(atomicAdd(p.next_tile, 1u));
+                    if (t < n_tiles) {
                         T = decode_at(t);
                     } else {
                         T = Tile{};
@@ -422,9 +425,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
                 const int a1 = up ? mt * 64 : mt * 128 + 64;
                 const int brow = T.row0 + (PAIR && !leader ? n_mma_of(T) / 2 : 0);
                 const int kblocks = up ? P.kb_up : P.kb_dn;
-                if (!up && p.ph_lo == PH_UP) {
-                    // (only when this launch also runs the up projection: a separate launch
-                    // starts after the up-projection launch has completed)
+                if (!up) {
                     // the h rows of this token tile are complete once every up-projection
                     // weight tile of it has been stored (each CTA of a pair stores half)
                     const unsigned need = static_cast<unsigned>(P.mt_up * (PAIR ? 2 : 1));
@@ -595,15 +596,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
                         }
                     }
                 }
-                // publish (when this launch also runs the down projection): this CTA's
-                // columns of the token tile are in h (generic-proxy stores, read later by
-                // other SMs' TMA)
-                if (p.ph_hi == PH_DOWN + 1) {
-                    fence_proxy_async_global();
-                    __threadfence();
-                    named_bar_sync(3, 128);
-                    if (warp == 2 && lane == 0) atomicAdd(p.ready + T.nti, 1u);
-                }
+                // publish: this CTA's columns of the token tile are in h (generic-proxy
+                // stores, read later by other SMs' TMA)
+                fence_proxy_async_global();
+                __threadfence();
+                named_bar_sync(3, 128);
+                if (warp == 2 && lane == 0) atomicAdd(p.ready + T.nti, 1u);
             } else {
                 const int col = mt * 128 + q * 32 + lane;
                 const bool col_ok = col < P.H;
@@ -735,7 +733,6 @@ int pick_stages(int bn_cta, int tab)
 // MMA): per SM the pair halves the B tile held in shared memory and read by the tensor
 // core, and halves the activation traffic from L2 per flop.
 constexpr int PAIR_MIN_BN = 128;
-constexpr int FUSE_MAX_BN = 32;
 int g_variant = 0;   // 0 automatic, 1 single CTA, 2 CTA pair
 
 }  // namespace
@@ -815,28 +812,14 @@ cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I
     const void *fn = pair ? reinterpret_cast<const void *>(ffn_kernel<true>)
                           : reinterpret_cast<const void *>(ffn_kernel<false>);
     if ((err = ensure_smem(fn, smem)) != cudaSuccess) return err;
-    // the last two readiness slots are the tile counters of the (one or two) launches
-    unsigned *ctr = ready + ffn_ready_slots(rows_total, n_cg) - 2;
-    auto go = [&](int lo, int hi) {
-        a.ph_lo = lo;
-        a.ph_hi = hi;
-        a.next_tile = ctr + lo;
-        return pair ? launch_pdl(ffn_kernel<true>, dim3(num_sms() / 2 * 2), dim3(NUM_THREADS), smem, s, 2, a)
-                    : launch_pdl(ffn_kernel<false>, dim3(num_sms()), dim3(NUM_THREADS), smem, s, 1, a);
-    };
-    // Small token tiles (decode) run both projections in one launch: down-projection tiles
-    // fill the up projection's last partial wave and the launch gap disappears (measured
-    // 2-3% faster at T <= 8).  Larger tiles measured the same or slower fused, so they run
-    // the up-projection launch, then the down-projection launch.
-    const bool fuse = !pair && bn <= FUSE_MAX_BN;
-    if (fuse) {
-        if ((err = go(PH_UP, PH_DOWN + 1)) != cudaSuccess) return err;
-        if (mid_event && (err = cudaEventRecord(mid_event, s)) != cudaSuccess) return err;
-        return cudaSuccess;
-    }
-    if ((err = go(PH_UP, PH_DOWN)) != cudaSuccess) return err;
+    // the last readiness slot is the tile counter of the launch
+    a.next_tile = ready + ffn_ready_slots(rows_total, n_cg) - 1;
+    err = pair ? launch_pdl(ffn_kernel<true>, dim3(num_sms() / 2 * 2), dim3(NUM_THREADS), smem, s, 2, a)
+               : launch_pdl(ffn_kernel<false>, dim3(num_sms()), dim3(NUM_THREADS), smem, s, 1, a);
+    if (err != cudaSuccess) return err;
+    // one launch computes both projections: the "between" mark follows it
     if (mid_event && (err = cudaEventRecord(mid_event, s)) != cudaSuccess) return err;
-    return go(PH_DOWN, PH_DOWN + 1);
+    return cudaSuccess;
 }
 
 }  // namespace moe

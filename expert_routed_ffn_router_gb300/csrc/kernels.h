@@ -104,10 +104,11 @@ void set_ffn_variant(int v);
 
 // Enqueues the up projection (+SwiGLU) and the down projection of up to two problems
 // (the routed experts and the shared expert) that share H; I may differ per problem.  One
-// persistent launch runs the up-projection tiles, then the down-projection tiles; a down
-// tile starts once the h rows of its token tile are complete, tracked by `ready` (device,
-// ffn_ready_slots(...) counters, zeroed here unless `ready_zeroed`).  `mid_event` (nullable) is recorded after
-// the launch.
+// persistent launch claims the up-projection tiles, then the down-projection tiles, from
+// a global counter; a down tile starts once the h rows of its token tile are complete,
+// tracked by `ready` (device, ffn_ready_slots(...) counters incl. the tile counter,
+// zeroed here unless `ready_zeroed`).  `mid_event` (nullable) is recorded after the
+// launch.
 cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I_per_prob,
                        int token_hint, unsigned *ready, bool ready_zeroed, int *status, cudaStream_t s,
                        unsigned long long timeout_ns, int inject, cudaEvent_t mid_event);

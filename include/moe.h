@@ -104,9 +104,8 @@ void moe_debug_set_wait_limit(unsigned long long limit_ns, int inject_stall);
 
 /* Profiling hook: with `events` pointing at n >= 6 cudaEvent_t handles, every later
  * moe_layer_forward records them on its stream: [0] before the router, [1] after the
- * router, [2] after dispatch, [3] between the expert FFN's up- and down-projection
- * launches (after the FFN when small token tiles run both projections in one launch),
- * [4] after the FFN, [5] after combine.  events == NULL switches recording off.  The
+ * router, [2] after dispatch, [3] and [4] after the expert FFN (its up and down
+ * projections are one launch), [5] after combine.  events == NULL switches recording off.  The
  * handles stay owned by the caller and must outlive the recording calls. */
 void moe_debug_set_stage_events(void *const *events, int n);
 
