@@ -62,10 +62,13 @@ struct RouterArgs {
     int depth;       // additions any product passes through in its logit's summation
 };
 
-// CTA tile: TT tokens x TE experts, TPT x EPT per thread, PF stages of loads in flight.
-template <int TT_, int TE_, int TPT_, int EPT_, int PF_>
+// CTA tile: TT tokens x TE experts, TPT x EPT per thread, PF stages of loads in flight;
+// X2: paired fp32 FMAs (two tokens per instruction) -- the same correctly rounded
+// operations in the same order, in half the FMA instructions.
+template <int TT_, int TE_, int TPT_, int EPT_, int PF_, int X2_ = 0>
 struct Cfg {
     static constexpr int TT = TT_, TE = TE_, TPT = TPT_, EPT = EPT_, PF = PF_;
+    static constexpr bool X2 = X2_ != 0;
     static constexpr int NTY = TT / TPT, NTX = TE / EPT;
     static constexpr int LY = 4;                          // token groups per warp
     static constexpr int XV = TT * 4, WV = TE * 4;        // 8-element vectors per stage
@@ -75,7 +78,30 @@ struct Cfg {
     static_assert(EPT == 4 && TPT % 4 == 0, "float4 operand reads");
 };
 using SmallCfg = Cfg<16, 256, 4, 4, 2>;
-using LargeCfg = Cfg<128, 64, 8, 4, 2>;
+using LargeCfg = Cfg<128, 64, 8, 4, 2, 1>;
+
+// Two fp32 lanes per 64-bit register: d = a * b + c and d = a + b, each lane correctly
+// rounded (the same results as two fmaf / two fp32 adds).
+__device__ __forceinline__ uint64_t fma_x2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t add_x2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t dup_x2(float w)
+{
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(d) : "f"(w));
+    return d;
+}
 
 __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
 {
@@ -448,6 +474,9 @@ __device__ void gemm_tile(const RouterArgs &a, unsigned char *smem)
     float acc[C::TPT * C::EPT];
 #pragma unroll
     for (int p = 0; p < C::TPT * C::EPT; ++p) acc[p] = 0.f;
+    uint64_t accp[C::X2 ? C::TPT / 2 * C::EPT : 1];     // paired running sums (X2)
+#pragma unroll
+    for (int p = 0; p < (C::X2 ? C::TPT / 2 * C::EPT : 1); ++p) accp[p] = 0ull;
 
 #pragma unroll
     for (int j = 0; j < C::PF; ++j)
@@ -463,31 +492,66 @@ __device__ void gemm_tile(const RouterArgs &a, unsigned char *smem)
                 __syncthreads();
                 // one 32-deep fp32 chain per (token, expert) for this stage, then added to
                 // the running sum of the split
-                float acc_in[C::TPT * C::EPT];
-#pragma unroll
-                for (int p = 0; p < C::TPT * C::EPT; ++p) acc_in[p] = 0.f;
                 const float *xb = xs + buf * KST * C::TT + C::TPT * ty;
                 const float *wb = wsm + buf * KST * C::TE + C::EPT * tx;
+                if constexpr (C::X2) {
+                    // pair pp * 4 + jj = (token 2pp, token 2pp + 1) x expert jj
+                    uint64_t pin[C::TPT / 2 * 4];
+#pragma unroll
+                    for (int q = 0; q < C::TPT / 2 * 4; ++q) pin[q] = 0ull;
 #pragma unroll 4
-                for (int kk = 0; kk < KST; ++kk) {
-                    float xa[C::TPT];
+                    for (int kk = 0; kk < KST; ++kk) {
+                        ulonglong2 xv[C::TPT / 4];
 #pragma unroll
-                    for (int i4 = 0; i4 < C::TPT / 4; ++i4) {
-                        const float4 v = *reinterpret_cast<const float4 *>(xb + kk * C::TT + 4 * i4);
-                        xa[4 * i4] = v.x; xa[4 * i4 + 1] = v.y; xa[4 * i4 + 2] = v.z; xa[4 * i4 + 3] = v.w;
+                        for (int i4 = 0; i4 < C::TPT / 4; ++i4)
+                            xv[i4] = *reinterpret_cast<const ulonglong2 *>(xb + kk * C::TT + 4 * i4);
+                        const float4 wv = *reinterpret_cast<const float4 *>(wb + kk * C::TE);
+                        const uint64_t wp[4] = {dup_x2(wv.x), dup_x2(wv.y), dup_x2(wv.z), dup_x2(wv.w)};
+#pragma unroll
+                        for (int pp = 0; pp < C::TPT / 2; ++pp) {
+                            const uint64_t xp = (pp & 1) ? xv[pp >> 1].y : xv[pp >> 1].x;
+#pragma unroll
+                            for (int jj = 0; jj < 4; ++jj) pin[pp * 4 + jj] = fma_x2(xp, wp[jj], pin[pp * 4 + jj]);
+                        }
                     }
-                    const float4 wv = *reinterpret_cast<const float4 *>(wb + kk * C::TE);
-                    const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-                    for (int i = 0; i < C::TPT; ++i)
+                    for (int q = 0; q < C::TPT / 2 * 4; ++q) accp[q] = add_x2(accp[q], pin[q]);
+                } else {
+                    float acc_in[C::TPT * C::EPT];
 #pragma unroll
-                        for (int jj = 0; jj < 4; ++jj)
-                            acc_in[i * 4 + jj] = fmaf(xa[i], wa[jj], acc_in[i * 4 + jj]);
+                    for (int q = 0; q < C::TPT * C::EPT; ++q) acc_in[q] = 0.f;
+#pragma unroll 4
+                    for (int kk = 0; kk < KST; ++kk) {
+                        float xa[C::TPT];
+#pragma unroll
+                        for (int i4 = 0; i4 < C::TPT / 4; ++i4) {
+                            const float4 v = *reinterpret_cast<const float4 *>(xb + kk * C::TT + 4 * i4);
+                            xa[4 * i4] = v.x; xa[4 * i4 + 1] = v.y; xa[4 * i4 + 2] = v.z; xa[4 * i4 + 3] = v.w;
+                        }
+                        const float4 wv = *reinterpret_cast<const float4 *>(wb + kk * C::TE);
+                        const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                        for (int i = 0; i < C::TPT; ++i)
+#pragma unroll
+                            for (int jj = 0; jj < 4; ++jj)
+                                acc_in[i * 4 + jj] = fmaf(xa[i], wa[jj], acc_in[i * 4 + jj]);
+                    }
+#pragma unroll
+                    for (int q = 0; q < C::TPT * C::EPT; ++q) acc[q] += acc_in[q];
                 }
-#pragma unroll
-                for (int p = 0; p < C::TPT * C::EPT; ++p) acc[p] += acc_in[p];
             }
         }
+    }
+    if constexpr (C::X2) {
+#pragma unroll
+        for (int pp = 0; pp < C::TPT / 2; ++pp)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                float lo, hi;
+                asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(accp[pp * 4 + jj]));
+                acc[(2 * pp) * 4 + jj] = lo;
+                acc[(2 * pp + 1) * 4 + jj] = hi;
+            }
     }
 
 #pragma unroll
