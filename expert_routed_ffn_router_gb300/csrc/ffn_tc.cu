@@ -62,7 +62,8 @@ constexpr int MAX_CG = 1040;              // groups of all problems of a launch
 constexpr int CW = 32;                    // epilogue chunk: accumulator columns per TMEM load
 constexpr int XCHG_FLOATS = 2 * CW * 64;  // double-buffered G exchange (up epilogue)
 constexpr int PH_UP = 0, PH_DOWN = 1;
-constexpr int TQ = 4;                     // depth of the ring that hands claimed tiles to the roles
+constexpr int TQ = 4;
+constexpr int NT_BLOCK = 8;               // token tiles per block of a group's tile order                     // depth of the ring that hands claimed tiles to the roles
 constexpr int MAX_STAGES = 8;       // deeper rings measured slower at decode (HBM-bound up projection)
 
 struct ProbDev {
@@ -340,8 +341,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
         const int m = gm[cg];
         const int ntn = (m + bn - 1) / bn;
         const int local = v - gpre[lo];
-        T.mt = local / ntn;
-        const int nt = local - T.mt * ntn;
+        // A group's tiles are taken in blocks of NT_BLOCK token tiles: for each block, every
+        // weight tile in turn, the block's token tiles innermost.  The weight tile is then
+        // shared by token tiles in flight together, and the block's token rows stay in L2
+        // while the weight tiles pass (a group with many token tiles would otherwise re-read
+        // all of its rows from HBM for every weight tile).
+        const int mtn = ph ? p.prob[T.pi].mt_dn : p.prob[T.pi].mt_up;
+        const int nb = local / (mtn * NT_BLOCK);
+        const int rem = local - nb * (mtn * NT_BLOCK);
+        const int width = min(NT_BLOCK, ntn - nb * NT_BLOCK);
+        T.mt = rem / width;
+        const int nt = nb * NT_BLOCK + (rem - T.mt * width);
         T.row0 = gstart[cg] + nt * bn;
         T.nvalid = min(bn, m - nt * bn);
         T.nti = ntp[cg] + nt;
