@@ -784,14 +784,16 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
     FinSmem S(smem, E, a.max_pairs, warp);
     const Bounds bd(a.depth, KS, a.H);
     for (int e = tid; e < E; e += NT) {        // gate-row norms and biases, once per CTA
-        float w[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q)
-            if (q < KS) w[q] = __ldcg(a.wsq + (static_cast<size_t>(tt) * KS + q) * E + e);
         float nw2 = 0.f;
+        for (int q0 = 0; q0 < KS; q0 += 16) {  // splits in batches of 16 loads, added in order
+            float w[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-            if (q < KS) nw2 += w[q];
+            for (int q = 0; q < 16; ++q)
+                if (q0 + q < KS) w[q] = __ldcg(a.wsq + (static_cast<size_t>(tt) * KS + q0 + q) * E + e);
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                if (q0 + q < KS) nw2 += w[q];
+        }
         S.nw[e] = sqrtf(nw2) * bd.infl;
         S.bias[e] = a.bias[e];
     }
@@ -807,14 +809,17 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
                 const int tl = it / n4, g = it - tl * n4, t = t0 + c0 + tl;
                 if (t >= a.T) continue;
                 const float4 *src = reinterpret_cast<const float4 *>(a.part + static_cast<size_t>(t) * E) + g;
-                float4 w[16];
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int q0 = 0; q0 < KS; q0 += 16) {   // batches of 16 loads, added in order
+                    float4 w[16];
 #pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    if (q < KS) w[q] = __ldcg(src + q * stride);
-                float4 v = w[0];
+                    for (int q = 0; q < 16; ++q)
+                        if (q0 + q < KS) w[q] = __ldcg(src + (q0 + q) * stride);
+                    if (q0 == 0) v = w[0];
 #pragma unroll
-                for (int q = 1; q < 16; ++q)
-                    if (q < KS) { v.x += w[q].x; v.y += w[q].y; v.z += w[q].z; v.w += w[q].w; }
+                    for (int q = 0; q < 16; ++q)
+                        if (q0 + q < KS && q0 + q > 0) { v.x += w[q].x; v.y += w[q].y; v.z += w[q].z; v.w += w[q].w; }
+                }
                 *reinterpret_cast<float4 *>(S.L + tl * E + 4 * g) = v;
             }
         } else {
@@ -926,17 +931,20 @@ __global__ void __launch_bounds__(NT) router_finalize_kernel(const RouterArgs a,
     for (int q = 0; q < KS; ++q) n2 += __shfl_sync(kFullMask, part_sq, q);
     const float nx = sqrtf(n2) * bd.infl;
     for (int e = lane; e < E; e += 32) {
-        float pv[16], pn[16];
+        float v = 0.f, n = 0.f;
+        for (int q0 = 0; q0 < KS; q0 += 16) {   // batches of 16 loads, added in split order
+            float pv[16], pn[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-            if (q < KS) {
-                pv[q] = __ldcg(a.part + (static_cast<size_t>(q) * a.T + t) * E + e);
-                pn[q] = __ldcg(a.wsq + (static_cast<size_t>(tt) * KS + q) * E + e);
-            }
-        float v = pv[0], n = pn[0];
+            for (int q = 0; q < 16; ++q)
+                if (q0 + q < KS) {
+                    pv[q] = __ldcg(a.part + (static_cast<size_t>(q0 + q) * a.T + t) * E + e);
+                    pn[q] = __ldcg(a.wsq + (static_cast<size_t>(tt) * KS + q0 + q) * E + e);
+                }
+            if (q0 == 0) { v = pv[0]; n = pn[0]; }
 #pragma unroll
-        for (int q = 1; q < 16; ++q)
-            if (q < KS) { v += pv[q]; n += pn[q]; }
+            for (int q = 0; q < 16; ++q)
+                if (q0 + q < KS && q0 + q > 0) { v += pv[q]; n += pn[q]; }
+        }
         w_sel[e] = v;
         w_nw[e] = sqrtf(n) * bd.infl;
     }
@@ -984,7 +992,9 @@ RouterPlan router_plan(int T, int H, int E)
     } else {
         // at most 32 stages per split keeps the summation depth (and the error bound) small
         p.KS = (p.S + 31) / 32;
-        if (p.KS > 16) p.KS = 16;
+        // (the finalise reads up to 32 splits; beyond 16 the extra partial reads and the
+        // larger bound -- more tokens to refine -- measured slower at decode)
+        if (p.KS > 32) p.KS = 32;
         while (p.KS * 2 <= p.S && p.KS * 2 <= 16 && base * p.KS < target) p.KS *= 2;
         p.depth = KST + (p.S + p.KS - 1) / p.KS + p.KS + 2;
     }
