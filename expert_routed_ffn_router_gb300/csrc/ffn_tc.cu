@@ -392,36 +392,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
             unsigned char *a = stage_base;
             const uint32_t full_c0 = PAIR ? mapa_shared(smem_u32(full), 0) : 0u;   // even CTA's full[0]
             uint32_t qs = 0, qph = 0;
+            // claim the next tile of the list and publish it to every role (and to the odd CTA)
+            auto claim = [&](Tile &T) -> bool {
+                if (!mbar_wait(&tqe[qs], qph ^ 1u, abort_flag, p.status, tmo)) return false;
+                const int t = static_cast<int>(atomicAdd(p.next_tile, 1u));
+                if (t < n_tiles) {
+                    T = decode_at(t);
+                } else {
+                    T = Tile{};
+                    T.ph = -1;
+                }
+                const int vals[8] = {T.ph, T.pi, T.g, T.cg, T.mt, T.row0, T.nvalid, T.nti};
+                int *e = tq + 8 * qs;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) e[j] = vals[j];
+                mbar_arrive(&tqf[qs]);
+                if (PAIR) {
+                    const uint32_t pe = mapa_shared(smem_u32(e), 1);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) st_shared_cluster(pe + 4u * j, vals[j]);
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&tqf[qs]), 1));
+                }
+                if (++qs == TQ) { qs = 0; qph ^= 1u; }
+                return true;
+            };
+            Tile next_T{};
+            bool have_next = false;
             while (ok) {
                 Tile T;
                 if (!PAIR || leader) {
-                    // claim the next tile and publish it to every role (and to the odd CTA)
-                    if (!mbar_wait(&tqe[qs], qph ^ 1u, abort_flag, p.status, tmo)) { ok = false; break; }
-                    const int t = static_cast<int>(atomicAdd(p.next_tile, 1u));
-                    if (t < n_tiles) {
-                        T = decode_at(t);
-                    } else {
-                        T = Tile{};
-                        T.ph = -1;
+                    if (have_next) {
+                        T = next_T;
+                        have_next = false;
+                    } else if (!claim(T)) {
+                        ok = false;
+                        break;
                     }
-                    const int vals[8] = {T.ph, T.pi, T.g, T.cg, T.mt, T.row0, T.nvalid, T.nti};
-                    int *e = tq + 8 * qs;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) e[j] = vals[j];
-                    mbar_arrive(&tqf[qs]);
-                    if (PAIR) {
-                        const uint32_t pe = mapa_shared(smem_u32(e), 1);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) st_shared_cluster(pe + 4u * j, vals[j]);
-                        mbar_arrive_cluster(mapa_shared(smem_u32(&tqf[qs]), 1));
+                    // CTA pairs claim the following tile before this tile's loads are issued,
+                    // so the global atomic, the decode and the hand-over to the odd CTA
+                    // overlap them instead of stalling the ring at the tile boundary (single-
+                    // CTA decode tiles measured better claiming one tile at a time)
+                    if (PAIR && T.ph >= 0) {
+                        if (!claim(next_T)) { ok = false; break; }
+                        have_next = true;
                     }
                 } else {
                     // odd CTA of a pair: take the even CTA's claim
                     if (!mbar_wait_cluster(&tqf[qs], qph, abort_flag, p.status, tmo)) { ok = false; break; }
                     T = slot_read(qs);
                     tqe_arrive(qs);
+                    if (++qs == TQ) { qs = 0; qph ^= 1u; }
                 }
-                if (++qs == TQ) { qs = 0; qph ^= 1u; }
                 if (T.ph < 0) break;
                 const ProbDev &P = p.prob[T.pi];
                 const int mt = mt_cta(T);
