@@ -18,7 +18,10 @@
  *          matrix A built from co-activation).
  *
  * Readings where the pages are silent (each is also listed in the design notes):
- *   - scoring is the logistic sigmoid s = 1/(1+exp(-l));
+ *   - scoring is the logistic sigmoid s = 1/(1+exp(-l)) (oracle_router_ex also offers
+ *     softmax over the token's E logits, group-limited selection and unnormalised
+ *     weights, the options of the other MoE families one router serves);
+ *   - a group's score is the sum of its group_top largest biased scores sel;
  *   - the per-expert bias only selects: sel = s + b, the weights use the unbiased s;
  *   - order is sel descending, equal sel -> lower expert index first;
  *   - weights are renormalised over the k selected unbiased scores: w_j = s_j / sum s;
@@ -76,11 +79,60 @@ static int ranks_before(const double *sel, int a, int b)
     return a < b;
 }
 
-/* Top-k for one token ([LLHT] "MoE Router": a sort that keeps the indices).
- * k rounds of "take the best expert not yet taken"; the result is in rank order. */
-static void topk_token(const double *sel, int E, int K, int32_t *idx, unsigned char *taken)
+/* Softmax scoring of one token: s[e] = exp(l[e]) / sum_j exp(l[j]) over all E experts,
+ * evaluated as exp(l[e] - m) / sum_j exp(l[j] - m) with m the largest logit (the same
+ * value in exact arithmetic; no overflow).  sel[e] = s[e] + bias[e]. */
+static void softmax_token(const double *l, const float *bias, int E, double *s, double *sel)
 {
-    memset(taken, 0, (size_t)E);
+    double m = l[0];
+    for (int e = 1; e < E; ++e) if (l[e] > m) m = l[e];
+    double sum = 0.0;
+    for (int e = 0; e < E; ++e) { s[e] = exp(l[e] - m); sum += s[e]; }
+    for (int e = 0; e < E; ++e) { s[e] /= sum; sel[e] = s[e] + (double)bias[e]; }
+}
+
+/* Group-limited selection ([LLHT] "MoE Router": DeepSeek routing with expert groups;
+ * Mixtral's is the case of one group that holds every expert).  The E experts form
+ * n_group groups of G = E / n_group consecutive experts.  A group's score is the sum of
+ * its group_top largest sel; the topk_group groups with the largest score (lower group
+ * index first on equal scores) stay eligible, and the experts of the other groups get
+ * taken[e] = 1 so that the top-k passes over them. */
+static void limit_groups(const double *sel, int E, int n_group, int topk_group, int group_top,
+                         unsigned char *taken, double *gscore, unsigned char *gkeep)
+{
+    const int G = E / n_group;
+    for (int g = 0; g < n_group; ++g) {
+        /* group_top rounds of "largest sel of the group not yet counted" */
+        double sum = 0.0;
+        for (int r = 0; r < group_top; ++r) {
+            int best = -1;
+            for (int e = g * G; e < (g + 1) * G; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || ranks_before(sel, e, best)) best = e;
+            }
+            taken[best] = 1;
+            sum += sel[best];
+        }
+        for (int e = g * G; e < (g + 1) * G; ++e) taken[e] = 0;
+        gscore[g] = sum;
+        gkeep[g] = 0;
+    }
+    for (int r = 0; r < topk_group; ++r) {
+        int best = -1;
+        for (int g = 0; g < n_group; ++g) {
+            if (gkeep[g]) continue;
+            if (best < 0 || gscore[g] > gscore[best]) best = g;   /* ties: lower g stays */
+        }
+        gkeep[best] = 1;
+    }
+    for (int e = 0; e < E; ++e) taken[e] = gkeep[e / G] ? 0 : 1;
+}
+
+/* Top-k for one token ([LLHT] "MoE Router": a sort that keeps the indices): k rounds of
+ * "take the best expert not yet taken" over the experts with taken[e] == 0 (the others
+ * are skipped); the result is in rank order. */
+static void topk_eligible(const double *sel, int E, int K, int32_t *idx, unsigned char *taken)
+{
     for (int j = 0; j < K; ++j) {
         int best = -1;
         for (int e = 0; e < E; ++e) {
@@ -92,7 +144,53 @@ static void topk_token(const double *sel, int E, int K, int32_t *idx, unsigned c
     }
 }
 
-/* Router: scores, top-k and renormalised weights for every token.
+/* Router with the routing options of one MoE family:
+ *   scoring     0: s = sigmoid(l) ([V41] Mega-Gate);  1: s = softmax of the token's E logits
+ *   n_group, topk_group, group_top: group-limited selection (limit_groups); n_group = 1
+ *               selects over all experts
+ *   renorm      1: w_j = s_j / sum of the K selected s ([V41]; the bias never enters the
+ *               weights);  0: w_j = s_j
+ * Outputs as oracle_router.  Returns -1 on arguments that do not define a selection. */
+int oracle_router_ex(const uint16_t *X, const uint16_t *Wg, const float *bias,
+                     int T, int H, int E, int K, int scoring, int n_group, int topk_group,
+                     int group_top, int renorm, int32_t *topk_idx, double *topk_w,
+                     double *logits, double *scores, double *sel_out)
+{
+    if (T < 0 || H <= 0 || E <= 0 || K <= 0 || K > E) return -1;
+    if (scoring != 0 && scoring != 1) return -1;
+    if (n_group < 1 || E % n_group != 0 || topk_group < 1 || topk_group > n_group) return -1;
+    if (group_top < 1 || group_top > E / n_group || K > topk_group * (E / n_group)) return -1;
+#pragma omp parallel
+    {
+        double *l = (double *)malloc(sizeof(double) * (size_t)E);
+        double *s = (double *)malloc(sizeof(double) * (size_t)E);
+        double *sel = (double *)malloc(sizeof(double) * (size_t)E);
+        double *gscore = (double *)malloc(sizeof(double) * (size_t)n_group);
+        unsigned char *gkeep = (unsigned char *)malloc((size_t)n_group);
+        unsigned char *taken = (unsigned char *)malloc((size_t)E);
+#pragma omp for schedule(dynamic, 4)
+        for (int t = 0; t < T; ++t) {
+            score_token(X + (size_t)t * H, Wg, bias, H, E, l, s, sel);
+            if (scoring == 1) softmax_token(l, bias, E, s, sel);
+            int32_t *idx = topk_idx + (size_t)t * K;
+            memset(taken, 0, (size_t)E);
+            if (n_group > 1) limit_groups(sel, E, n_group, topk_group, group_top, taken, gscore, gkeep);
+            topk_eligible(sel, E, K, idx, taken);
+            /* weights from the selected, unbiased scores */
+            double denom = 0.0;
+            for (int j = 0; j < K; ++j) denom += s[idx[j]];
+            for (int j = 0; j < K; ++j)
+                topk_w[(size_t)t * K + j] = renorm ? s[idx[j]] / denom : s[idx[j]];
+            if (logits) memcpy(logits + (size_t)t * E, l, sizeof(double) * (size_t)E);
+            if (scores) memcpy(scores + (size_t)t * E, s, sizeof(double) * (size_t)E);
+            if (sel_out) memcpy(sel_out + (size_t)t * E, sel, sizeof(double) * (size_t)E);
+        }
+        free(l); free(s); free(sel); free(gscore); free(gkeep); free(taken);
+    }
+    return 0;
+}
+
+/* Router: sigmoid scores, top-k over all experts and renormalised weights for every token.
  *   topk_idx[T,K] int32 (rank order), topk_w[T,K] double,
  *   logits/scores/sel[T,E] double, each nullable. */
 int oracle_router(const uint16_t *X, const uint16_t *Wg, const float *bias,
@@ -100,29 +198,8 @@ int oracle_router(const uint16_t *X, const uint16_t *Wg, const float *bias,
                   int32_t *topk_idx, double *topk_w,
                   double *logits, double *scores, double *sel_out)
 {
-    if (T < 0 || H <= 0 || E <= 0 || K <= 0 || K > E) return -1;
-#pragma omp parallel
-    {
-        double *l = (double *)malloc(sizeof(double) * (size_t)E);
-        double *s = (double *)malloc(sizeof(double) * (size_t)E);
-        double *sel = (double *)malloc(sizeof(double) * (size_t)E);
-        unsigned char *taken = (unsigned char *)malloc((size_t)E);
-#pragma omp for schedule(dynamic, 4)
-        for (int t = 0; t < T; ++t) {
-            score_token(X + (size_t)t * H, Wg, bias, H, E, l, s, sel);
-            int32_t *idx = topk_idx + (size_t)t * K;
-            topk_token(sel, E, K, idx, taken);
-            /* renormalise over the selected, unbiased scores */
-            double denom = 0.0;
-            for (int j = 0; j < K; ++j) denom += s[idx[j]];
-            for (int j = 0; j < K; ++j) topk_w[(size_t)t * K + j] = s[idx[j]] / denom;
-            if (logits) memcpy(logits + (size_t)t * E, l, sizeof(double) * (size_t)E);
-            if (scores) memcpy(scores + (size_t)t * E, s, sizeof(double) * (size_t)E);
-            if (sel_out) memcpy(sel_out + (size_t)t * E, sel, sizeof(double) * (size_t)E);
-        }
-        free(l); free(s); free(sel); free(taken);
-    }
-    return 0;
+    return oracle_router_ex(X, Wg, bias, T, H, E, K, 0, 1, 1, 1, 1, topk_idx, topk_w, logits,
+                            scores, sel_out);
 }
 
 /* Dispatch bookkeeping ([LLHT] "MoE Router": per-expert aggregated routing info;

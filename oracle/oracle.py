@@ -50,6 +50,8 @@ def _load():
         i = ctypes.c_int
         lib.oracle_router.argtypes = [P, P, P, i, i, i, i, P, P, P, P, P]
         lib.oracle_router.restype = i
+        lib.oracle_router_ex.argtypes = [P, P, P, i, i, i, i, i, i, i, i, i, P, P, P, P, P]
+        lib.oracle_router_ex.restype = i
         lib.oracle_dispatch.argtypes = [P, i, i, i, P, P, P, P, P]
         lib.oracle_dispatch.restype = i
         lib.oracle_expert_rows.argtypes = [P, P, P, P, i, i, i, P]
@@ -101,6 +103,38 @@ def router(X: np.ndarray, W_gate: np.ndarray, bias: np.ndarray, K: int,
                                _p(extra.get("sel")))
     if rc != 0:
         raise ValueError(f"oracle_router rejected its arguments ({rc})")
+    return (idx, w, extra) if want_scores else (idx, w)
+
+
+SCORING = {"sigmoid": 0, "softmax": 1}
+
+
+def router_ex(X: np.ndarray, W_gate: np.ndarray, bias: np.ndarray, K: int,
+              scoring: str = "sigmoid", n_group: int = 1, topk_group: int = 1,
+              group_top: int = 1, renorm: bool = True, want_scores: bool = False):
+    """Router with the options of other MoE families (fp64).
+
+    scoring: "sigmoid" or "softmax" (over the token's E logits); the E experts form
+    n_group groups of E/n_group consecutive experts, a group scores the sum of its
+    group_top largest sel = s + bias, and the top-K is taken inside the topk_group best
+    groups; renorm divides the selected s by their sum (else the weights are s)."""
+    X = _u16(X)
+    W_gate = _u16(W_gate)
+    bias = np.ascontiguousarray(bias, dtype=np.float32)
+    T, H = X.shape
+    E = W_gate.shape[0]
+    assert W_gate.shape == (E, H) and bias.shape == (E,)
+    idx = np.zeros((T, K), np.int32)
+    w = np.zeros((T, K), np.float64)
+    extra = {}
+    if want_scores:
+        extra = {n: np.zeros((T, E), np.float64) for n in ("logits", "scores", "sel")}
+    rc = _load().oracle_router_ex(_p(X), _p(W_gate), _p(bias), T, H, E, K, SCORING[scoring],
+                                  n_group, topk_group, group_top, int(bool(renorm)),
+                                  _p(idx), _p(w), _p(extra.get("logits")),
+                                  _p(extra.get("scores")), _p(extra.get("sel")))
+    if rc != 0:
+        raise ValueError(f"oracle_router_ex rejected its arguments ({rc})")
     return (idx, w, extra) if want_scores else (idx, w)
 
 
@@ -191,12 +225,17 @@ def forward(inp: dict) -> dict:
     """The whole layer for every token of a small problem held in host numpy arrays.
 
     ``inp`` holds X, W_gate, bias, W1, W3, W2 ([E,...] uint16), W1s, W3s, W2s (or None),
-    K.  Returns the routing, dispatch bookkeeping and Y (float64 [T,H])."""
+    K and optionally ``routing`` (keyword options of router_ex).  Returns the routing,
+    dispatch bookkeeping and Y (float64 [T,H])."""
     X, K = inp["X"], int(inp["K"])
     T, H = X.shape
     E, _, I = inp["W1"].shape
     Is = 0 if inp.get("W1s") is None else inp["W1s"].shape[1]
-    idx, w = router(X, inp["W_gate"], inp["bias"], K)
+    routing = inp.get("routing")
+    if routing:
+        idx, w = router_ex(X, inp["W_gate"], inp["bias"], K, **routing)
+    else:
+        idx, w = router(X, inp["W_gate"], inp["bias"], K)
     d = dispatch(idx, E)
     W1 = {e: inp["W1"][e] for e in range(E)}
     W3 = {e: inp["W3"][e] for e in range(E)}

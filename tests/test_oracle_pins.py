@@ -10,7 +10,7 @@ import os
 
 import numpy as np
 import pytest
-from scipy.special import expit
+from scipy.special import expit, softmax
 
 import oracle
 from expert_routed_ffn_router_gb300 import synth
@@ -103,6 +103,97 @@ def test_weights_renormalise_unbiased_scores():
     assert np.all(idx2[:, 0] == 3)
     np.testing.assert_allclose(w2[:, 0], sc2["scores"][:, 3] /
                                np.take_along_axis(sc2["scores"], idx2, 1).sum(1), rtol=1e-15)
+
+
+# ------------------------------------------------------------------ routing variants
+def test_softmax_scores_match_library_softmax():
+    X, Wg, bias = _random_router(9, 96, 16, seed=11)
+    _, _, sc = oracle.router_ex(X, Wg, bias, 3, scoring="softmax", want_scores=True)
+    l_ref = _val(X) @ _val(Wg).T
+    s_ref = softmax(l_ref, axis=1)                # scipy, independent of the oracle
+    np.testing.assert_allclose(sc["scores"], s_ref, rtol=1e-13, atol=0)
+    np.testing.assert_allclose(sc["sel"], s_ref + bias.astype(np.float64), rtol=0, atol=1e-15)
+
+
+def _group_limited_bruteforce(sel, E, K, n_group, topk_group, group_top):
+    """The selection by its definition, every choice found by exhausting the subsets."""
+    G = E // n_group
+    gscore = [max(sum(sel[e] for e in c)
+                  for c in itertools.combinations(range(g * G, (g + 1) * G), group_top))
+              for g in range(n_group)]
+    dom_g = lambda a, b: gscore[a] > gscore[b] or (gscore[a] == gscore[b] and a < b)
+    keep = [S for S in itertools.combinations(range(n_group), topk_group)
+            if all(dom_g(a, b) for a in S for b in range(n_group) if b not in S)]
+    assert len(keep) == 1
+    allowed = [e for e in range(E) if e // G in keep[0]]
+    win = [S for S in itertools.combinations(allowed, K)
+           if all(_dominates(sel, a, b) for a in S for b in allowed if b not in S)]
+    assert len(win) == 1
+    return sorted(win[0], key=lambda e: (-sel[e], e))
+
+
+@pytest.mark.parametrize("scoring", ["sigmoid", "softmax"])
+@pytest.mark.parametrize("E,K,n_group,topk_group,group_top", [
+    (12, 3, 4, 2, 2), (12, 1, 4, 1, 1), (12, 4, 3, 2, 2), (16, 5, 8, 3, 1), (8, 2, 2, 1, 2)])
+def test_group_limited_topk_bruteforce(scoring, E, K, n_group, topk_group, group_top):
+    X, Wg, bias = _random_router(12, 64, E, seed=E * 7 + K + n_group, dup_rows=[(0, E - 1)])
+    idx, _, sc = oracle.router_ex(X, Wg, bias, K, scoring=scoring, n_group=n_group,
+                                  topk_group=topk_group, group_top=group_top, want_scores=True)
+    G = E // n_group
+    for t in range(X.shape[0]):
+        assert list(idx[t]) == _group_limited_bruteforce(sc["sel"][t], E, K, n_group,
+                                                         topk_group, group_top)
+        assert len({int(e) // G for e in idx[t]}) <= topk_group
+
+
+def test_one_group_or_every_group_is_the_plain_router():
+    X, Wg, bias = _random_router(24, 64, 16, seed=12, dup_rows=[(3, 9)])
+    i0, w0 = oracle.router(X, Wg, bias, 4)
+    for kw in (dict(n_group=1), dict(n_group=4, topk_group=4, group_top=2),
+               dict(n_group=16, topk_group=16)):
+        i1, w1 = oracle.router_ex(X, Wg, bias, 4, **kw)
+        assert np.array_equal(i0, i1)
+        np.testing.assert_array_equal(w0, w1)
+
+
+def test_equal_group_scores_go_to_lower_group():
+    # experts 2,3 (group 1) copy experts 4,5 (group 2): the two groups score the same and
+    # a large bias makes them the two best groups; with one group kept, group 1 wins
+    X, Wg, bias = _random_router(16, 64, 8, seed=13, dup_rows=[(4, 2), (5, 3)])
+    bias[2:6] += 2.0
+    idx, _ = oracle.router_ex(X, Wg, bias, 2, n_group=4, topk_group=1, group_top=2)
+    assert set(np.unique(idx)) == {2, 3}
+
+
+def test_mixtral_case_closed_form():
+    # softmax scores, one group, renormalised, no bias: the top-K of the logits, weighted
+    # by the softmax of the selected logits alone
+    X, Wg, _ = _random_router(20, 64, 8, seed=14)
+    zero = np.zeros(8, np.float32)
+    idx, w = oracle.router_ex(X, Wg, zero, 2, scoring="softmax")
+    l_ref = _val(X) @ _val(Wg).T
+    assert np.array_equal(idx, np.argsort(-l_ref, axis=1, kind="stable")[:, :2])
+    lk = np.take_along_axis(l_ref, idx, 1)
+    np.testing.assert_allclose(w, softmax(lk, axis=1), rtol=1e-13)
+
+
+@pytest.mark.parametrize("scoring", ["sigmoid", "softmax"])
+def test_unnormalised_weights_are_the_scores(scoring):
+    X, Wg, bias = _random_router(10, 64, 16, seed=15)
+    idx, w, sc = oracle.router_ex(X, Wg, bias, 4, scoring=scoring, renorm=False,
+                                  n_group=4, topk_group=2, group_top=2, want_scores=True)
+    l_ref = _val(X) @ _val(Wg).T
+    s_ref = expit(l_ref) if scoring == "sigmoid" else softmax(l_ref, axis=1)
+    np.testing.assert_allclose(w, np.take_along_axis(s_ref, idx, 1), rtol=1e-13)
+
+
+def test_router_ex_rejects_undefined_options():
+    X, Wg, bias = _random_router(2, 64, 12, seed=16)
+    for kw in (dict(n_group=5), dict(n_group=4, topk_group=5), dict(n_group=4, group_top=4),
+               dict(n_group=4, topk_group=1, K=4), dict(n_group=0)):
+        K = kw.pop("K", 2)
+        with pytest.raises(ValueError):
+            oracle.router_ex(X, Wg, bias, K, **kw)
 
 
 # -------------------------------------------------------------------------- dispatch
