@@ -35,6 +35,27 @@ class MoeWeights(ctypes.Structure):
                                                "W3s", "W2s")]
 
 
+class MoeRouting(ctypes.Structure):
+    """moe_routing_t: scoring (0 sigmoid, 1 softmax), n_group, topk_group, group_top,
+    renorm.  The defaults are the plain router."""
+    _fields_ = [(n, ctypes.c_int32) for n in ("scoring", "n_group", "topk_group",
+                                              "group_top", "renorm")]
+
+    @classmethod
+    def make(cls, scoring: str = "sigmoid", n_group: int = 1, topk_group: int = 1,
+             group_top: int = 1, renorm: bool = True) -> "MoeRouting":
+        return cls({"sigmoid": 0, "softmax": 1}[scoring], int(n_group), int(topk_group),
+                   int(group_top), int(bool(renorm)))
+
+
+def _routing(routing):
+    if routing is None:
+        return None
+    if isinstance(routing, dict):
+        routing = MoeRouting.make(**routing)
+    return ctypes.byref(routing)
+
+
 def library_path() -> str:
     return _build.LIB
 
@@ -57,12 +78,16 @@ def load(build_if_missing: bool = True):
         "moe_debug_set_stage_events": ([P, I], None),
         "moe_debug_set_ffn_variant": ([I], None),
         "moe_router_topk": ([P, P, P, I, I, I, I, P, P, P, Z, P], I),
+        "moe_router_topk_ex": ([P, P, P, I, I, I, I, ctypes.POINTER(MoeRouting), P, P, P, Z,
+                                P], I),
         "moe_dispatch": ([P, P, I, I, I, I, P, P, P, P, P, P, P, Z, P], I),
         "moe_expert_ffn": ([P, P, I, I, I, I, P, P, P, P, I, P, Z, P], I),
         "moe_expert_ffn_workspace_bytes": ([I, I, I], Z),
         "moe_combine": ([P, P, P, P, I, I, I, P, P], I),
         "moe_layer_forward": ([ctypes.POINTER(MoeShape), ctypes.POINTER(MoeWeights), P, P, P,
                                P, P, P, P, Z, P], I),
+        "moe_layer_forward_ex": ([ctypes.POINTER(MoeShape), ctypes.POINTER(MoeWeights),
+                                  ctypes.POINTER(MoeRouting), P, P, P, P, P, P, P, Z, P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -133,6 +158,15 @@ def moe_router_topk(X, W_gate, bias, K, topk_idx, topk_w, ws, stream=None):
         _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def moe_router_topk_ex(X, W_gate, bias, K, routing, topk_idx, topk_w, ws, stream=None):
+    """routing: MoeRouting, a dict of MoeRouting.make keywords, or None (defaults)."""
+    T, H = X.shape
+    E = W_gate.shape[0]
+    _check("moe_router_topk_ex", load().moe_router_topk_ex(
+        _ptr(X), _ptr(W_gate), _ptr(bias), T, H, E, int(K), _routing(routing), _ptr(topk_idx),
+        _ptr(topk_w), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
 def moe_dispatch(X, topk_idx, E, counts, offsets, perm, slot_pos, Xp, affinity, ws,
                  stream=None):
     T, H = X.shape
@@ -173,14 +207,26 @@ def moe_layer_forward(shape: MoeShape, weights: dict, X, Y, topk_idx, topk_w, co
         _stream(stream)))
 
 
+def moe_layer_forward_ex(shape: MoeShape, weights: dict, routing, X, Y, topk_idx, topk_w,
+                         counts, affinity, ws, stream=None):
+    w = MoeWeights(*[None if weights.get(n) is None else weights[n].data_ptr()
+                     for n in ("W_gate", "bias", "W1", "W3", "W2", "W1s", "W3s", "W2s")])
+    _check("moe_layer_forward_ex", load().moe_layer_forward_ex(
+        ctypes.byref(shape), ctypes.byref(w), _routing(routing), _ptr(X), _ptr(Y),
+        _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(affinity), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
 # ------------------------------------------------------------------- convenience wrapper
 class MoELayer:
     """Holds a layer's weights, outputs and workspace (torch allocations) and runs
     moe_layer_forward.  weights: dict of device tensors W_gate, bias, W1, W3, W2 and
     (optionally) W1s, W3s, W2s."""
 
-    def __init__(self, weights: dict, T: int, K: int, with_affinity: bool = True):
+    def __init__(self, weights: dict, T: int, K: int, with_affinity: bool = True,
+                 routing=None):
         self.w = weights
+        self.routing = routing
         E, H = weights["W_gate"].shape
         I = weights["W1"].shape[-1]
         Is = 0 if weights.get("W1s") is None else weights["W1s"].shape[-1]
@@ -198,8 +244,12 @@ class MoELayer:
         self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
 
     def forward(self, X, stream=None):
-        moe_layer_forward(self.shape, self.w, X, self.Y, self.topk_idx, self.topk_w,
-                          self.counts, self.affinity, self.ws, stream)
+        if self.routing is None:
+            moe_layer_forward(self.shape, self.w, X, self.Y, self.topk_idx, self.topk_w,
+                              self.counts, self.affinity, self.ws, stream)
+        else:
+            moe_layer_forward_ex(self.shape, self.w, self.routing, X, self.Y, self.topk_idx,
+                                 self.topk_w, self.counts, self.affinity, self.ws, stream)
         return self.Y
 
     def status(self, stream=None) -> int:

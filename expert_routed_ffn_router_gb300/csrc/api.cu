@@ -90,6 +90,27 @@ int check_ws(const void *ws, size_t have, size_t need)
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// moe_routing_t (NULL: defaults) -> validated options
+int check_routing(const moe_routing_t *r, int E, int K, RoutingOpts &o)
+{
+    o = RoutingOpts{};
+    if (!r) return MOE_OK;
+    if (r->scoring != 0 && r->scoring != 1) return MOE_ERR_INVALID_ARG;
+    if (r->renorm != 0 && r->renorm != 1) return MOE_ERR_INVALID_ARG;
+    if (r->n_group < 1 || E % r->n_group != 0) return MOE_ERR_INVALID_ARG;
+    const int G = E / r->n_group;
+    if (r->topk_group < 1 || r->topk_group > r->n_group) return MOE_ERR_INVALID_ARG;
+    if (r->group_top < 1 || r->group_top > G) return MOE_ERR_INVALID_ARG;
+    if (static_cast<long long>(K) > static_cast<long long>(r->topk_group) * G) return MOE_ERR_INVALID_ARG;
+    if (r->n_group > 32 || r->group_top > 2) return MOE_ERR_UNSUPPORTED_SHAPE;
+    o.scoring = r->scoring;
+    o.n_group = r->n_group;
+    o.topk_group = r->n_group > 1 ? r->topk_group : 1;
+    o.group_top = r->group_top;
+    o.renorm = r->renorm;
+    return MOE_OK;
+}
+
 struct RouterLayout {
     RouterPlan plan;
     RouterScratch scr;
@@ -227,8 +248,18 @@ int moe_router_topk(const void *X, const void *W_gate, const float *bias, int T,
                     int K, int32_t *topk_idx, float *topk_w, void *ws, size_t ws_bytes,
                     void *stream)
 {
+    return moe_router_topk_ex(X, W_gate, bias, T, H, E, K, nullptr, topk_idx, topk_w, ws,
+                              ws_bytes, stream);
+}
+
+int moe_router_topk_ex(const void *X, const void *W_gate, const float *bias, int T, int H,
+                       int E, int K, const moe_routing_t *routing, int32_t *topk_idx,
+                       float *topk_w, void *ws, size_t ws_bytes, void *stream)
+{
     int rc = check_common(T, H, E, K);
     if (rc) return rc;
+    RoutingOpts ro;
+    if ((rc = check_routing(routing, E, K, ro))) return rc;
     if ((rc = check_ptrs({X, W_gate, bias, topk_idx, topk_w}))) return rc;
     unsigned char *w = static_cast<unsigned char *>(ws);
     const RouterLayout L = router_layout(T, H, E, w ? w + kHeader : nullptr);
@@ -236,7 +267,7 @@ int moe_router_topk(const void *X, const void *W_gate, const float *bias, int T,
     if (T == 0) return MOE_OK;
     return cuda_status(launch_router(X, W_gate, bias, T, H, E, K, topk_idx, topk_w, L.plan,
                                      L.scr, static_cast<int *>(ws),
-                                     static_cast<cudaStream_t>(stream)));
+                                     static_cast<cudaStream_t>(stream), &ro));
 }
 
 int moe_dispatch(const void *X, const int32_t *topk_idx, int T, int H, int E, int K,
@@ -309,8 +340,19 @@ int moe_layer_forward(const moe_shape_t *shape, const moe_weights_t *wt, const v
                       int32_t *topk_idx, float *topk_w, int32_t *counts, int32_t *affinity,
                       void *ws, size_t ws_bytes, void *stream)
 {
+    return moe_layer_forward_ex(shape, wt, nullptr, X, Y, topk_idx, topk_w, counts, affinity,
+                                ws, ws_bytes, stream);
+}
+
+int moe_layer_forward_ex(const moe_shape_t *shape, const moe_weights_t *wt,
+                         const moe_routing_t *routing, const void *X, float *Y,
+                         int32_t *topk_idx, float *topk_w, int32_t *counts, int32_t *affinity,
+                         void *ws, size_t ws_bytes, void *stream)
+{
     int rc = check_shape(shape);
     if (rc) return rc;
+    RoutingOpts ro;
+    if ((rc = check_routing(routing, shape->E, shape->K, ro))) return rc;
     if (!wt) return MOE_ERR_INVALID_ARG;
     const moe_shape_t s = *shape;
     if ((rc = check_ptrs({X, Y, topk_idx, topk_w, counts, wt->W_gate, wt->bias, wt->W1, wt->W3,
@@ -327,7 +369,7 @@ int moe_layer_forward(const moe_shape_t *shape, const moe_weights_t *wt, const v
 
     record_stage(0, st);
     cudaError_t e = launch_router(X, wt->W_gate, wt->bias, s.T, s.H, s.E, s.K, topk_idx, topk_w,
-                                  L.r.plan, L.r.scr, status, st);
+                                  L.r.plan, L.r.scr, status, st, &ro);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     record_stage(1, st);
     // the dispatch tail also zeroes the FFN's readiness counters

@@ -28,10 +28,19 @@ struct RouterScratch {
     float *part, *xsq, *wsq;
     unsigned *cnt;
 };
+// Routing options of other MoE families (moe_routing_t of the public header, validated).
+struct RoutingOpts {
+    int scoring = 0;      // 0 sigmoid, 1 softmax
+    int n_group = 1;      // <= 32, divides E
+    int topk_group = 1;
+    int group_top = 1;    // 1 or 2
+    int renorm = 1;
+    bool is_default() const { return scoring == 0 && n_group == 1 && renorm == 1; }
+};
 cudaError_t launch_router(const void *X, const void *Wg, const float *bias, int T, int H,
                           int E, int K, int32_t *topk_idx, float *topk_w,
                           const RouterPlan &plan, const RouterScratch &scr, int *status,
-                          cudaStream_t s);
+                          cudaStream_t s, const RoutingOpts *ro = nullptr);
 
 // ------------------------------------------------------------------------- dispatch
 struct DispatchPlan {

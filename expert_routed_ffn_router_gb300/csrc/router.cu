@@ -60,6 +60,13 @@ struct RouterArgs {
     int *status;
     int max_pairs;   // capacity of the shared-memory refine list
     int depth;       // additions any product passes through in its logit's summation
+    // routing options (all at their defaults: sigmoid, one group, renormalised weights)
+    int scoring;     // 0 sigmoid, 1 softmax over the token's E logits
+    int n_group;     // groups of E / n_group consecutive experts (<= 32)
+    int topk_group;  // groups kept per token
+    int group_top;   // a group's score: the sum of its group_top (1 or 2) largest sel
+    int renorm;      // 1: weights = selected s / their sum; 0: the selected s
+    int variant;     // any option off its default: the general selection path
 };
 
 // CTA tile: TT tokens x TE experts, TPT x EPT per thread, PF stages of loads in flight;
@@ -378,6 +385,286 @@ __device__ bool score_select(int E, int K, float nx, const float *nw, const floa
     }
     __syncwarp();
     return false;
+}
+
+__device__ __forceinline__ float warp_max_f(float v)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, off));
+    return v;
+}
+
+__device__ __forceinline__ float warp_min_f(float v)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fminf(v, __shfl_xor_sync(kFullMask, v, off));
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(kFullMask, v, off);
+        v = o > v ? o : v;
+    }
+    return v;
+}
+
+// The largest two of a sequence (v1 >= v2), for a group's score.
+__device__ __forceinline__ void top2_push(float v, float &v1, float &v2)
+{
+    if (v > v1) { v2 = v1; v1 = v; } else if (v > v2) { v2 = v; }
+}
+
+// Scores one token with the general routing options (softmax scoring, group-limited
+// selection, unnormalised weights) and selects its top-K in fp32 with certified bounds.
+// Same contract as score_select; when the result is not certified the caller re-scores
+// every expert of the token (softmax needs all of them) and calls select_general64.
+//
+// Softmax bound.  With every logit within beta of its fp32 value, the exact s_e lies
+// within a factor e^{+-2 beta} of exp(l^_e) / sum_j exp(l^_j) (numerator and denominator
+// each move by at most e^{+-beta}).  Its fp32 evaluation exp(l^_e - m) / sum adds
+// u |l^_e - m| for the subtraction in the exponent, 2 ulp (4u) for expf in numerator and
+// every summand, (lane terms + 5 tree levels) u for the positive sum and u for the
+// division.  An absolute 1e-30 covers underflowed terms.
+//
+// Group bound.  A group's score (sum of its n largest sel) is non-decreasing in every sel,
+// so the sums of the n largest lower / upper bounds enclose it.  The kept groups are
+// certified when the smallest lower bound among them exceeds the largest upper bound of
+// the others.
+__device__ bool score_select_general(const RouterArgs &a, float nx, const float *nw,
+                                     const float *bias, float gam, float *w_sel, float *w_bnd,
+                                     float *w_sc, int32_t *oi, float *ow, int lane)
+{
+    const int E = a.E, K = a.K, NI = (E + 31) / 32;
+    if (a.scoring == 0) {
+        for (int i = 0; i < NI; ++i) {
+            const int e = lane + 32 * i;
+            if (e >= E) break;
+            const float l = w_sel[e];
+            const float bl = gam * nx * nw[e] + 1e-30f;
+            const float s = 1.f / (1.f + expf(-l));
+            const float sel = s + bias[e];
+            const float al = fabsf(l);
+            const float D = (al > bl) ? fminf(0.25f, __expf(-(al - bl)) * 1.01f) : 0.25f;
+            w_sel[e] = sel;
+            w_bnd[e] = bl * D + 4.f * kU + fabsf(sel) * (2.f * kU);
+            w_sc[e] = s;
+        }
+    } else {
+        float m = -FLT_MAX, beta = 0.f;
+        for (int i = 0; i < NI; ++i) {
+            const int e = lane + 32 * i;
+            if (e >= E) break;
+            m = fmaxf(m, w_sel[e]);
+            beta = fmaxf(beta, gam * nx * nw[e] + 1e-30f);
+        }
+        m = warp_max_f(m);
+        beta = warp_max_f(beta);
+        float sum = 0.f, spread = 0.f;
+        for (int i = 0; i < NI; ++i) {
+            const int e = lane + 32 * i;
+            if (e >= E) break;
+            const float d = w_sel[e] - m;
+            const float A = expf(d);
+            w_sc[e] = A;
+            sum += A;
+            spread = fmaxf(spread, -d);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFullMask, sum, off);
+        spread = warp_max_f(spread);
+        const float rel = (expm1f(2.f * beta) + kU * (2.f * spread + static_cast<float>(NI) + 14.f)) * 1.02f;
+        for (int i = 0; i < NI; ++i) {
+            const int e = lane + 32 * i;
+            if (e >= E) break;
+            const float sc = w_sc[e] / sum;
+            const float sel = sc + bias[e];
+            w_sc[e] = sc;
+            w_sel[e] = sel;
+            w_bnd[e] = sc * rel + 1e-30f + fabsf(sel) * (2.f * kU);
+        }
+    }
+    __syncwarp();
+
+    // groups kept (bit g), certified against the others
+    uint32_t kmask = kFullMask;
+    int G = E;
+    if (a.n_group > 1) {
+        const int ng = a.n_group;
+        G = E / ng;
+        float glo = -FLT_MAX, ghi = -FLT_MAX;
+        unsigned long long key = 0ull;
+        if (lane < ng) {
+            float s1 = -FLT_MAX, s2 = -FLT_MAX, l1 = -FLT_MAX, l2 = -FLT_MAX, h1 = -FLT_MAX, h2 = -FLT_MAX;
+            for (int e = lane * G; e < (lane + 1) * G; ++e) {
+                const float v = w_sel[e], b = w_bnd[e];
+                top2_push(v, s1, s2);
+                top2_push(__fsub_rd(v, b), l1, l2);
+                top2_push(__fadd_ru(v, b), h1, h2);
+            }
+            const bool two = a.group_top == 2;
+            key = rank_key(two ? s1 + s2 : s1, lane);
+            glo = two ? __fadd_rd(l1, l2) : l1;
+            ghi = two ? __fadd_ru(h1, h2) : h1;
+        }
+        kmask = 0u;
+        for (int r = 0; r < a.topk_group; ++r) {
+            const unsigned long long win = warp_max_u64(key);
+            const int g = static_cast<int>(~static_cast<uint32_t>(win));
+            kmask |= 1u << g;
+            if (lane == g) key = 0ull;
+        }
+        const bool kept = lane < ng && ((kmask >> lane) & 1u);
+        const float klo = warp_min_f(kept ? glo : FLT_MAX);
+        const float ohi = warp_max_f(lane < ng && !kept ? ghi : -FLT_MAX);
+        if (a.topk_group < ng && !(klo > ohi)) return false;
+    }
+
+    // top-K among the experts of the kept groups: each lane keeps its best untaken key
+    auto eligible = [&](int e) { return ((kmask >> (e / G)) & 1u) != 0u; };
+    uint32_t taken = 0;
+    auto lane_best = [&]() {
+        unsigned long long b = 0ull;
+        for (int i = 0; i < NI; ++i) {
+            const int e = lane + 32 * i;
+            if (e >= E) break;
+            if ((taken >> i) & 1u || !eligible(e)) continue;
+            const unsigned long long k = rank_key(w_sel[e], e);
+            b = k > b ? k : b;
+        }
+        return b;
+    };
+    unsigned long long best = lane_best();
+    float lower_min = FLT_MAX, prev_lo = 0.f, my_s = 0.f;
+    int my_e = 0;
+    bool order_ok = true;
+    for (int j = 0; j < K; ++j) {
+        const unsigned long long win = warp_max_u64(best);
+        const int e = static_cast<int>(~static_cast<uint32_t>(win));
+        if ((e & 31) == lane) {
+            taken |= 1u << (e >> 5);
+            best = lane_best();
+        }
+        const float ws = w_sel[e], wb = w_bnd[e];
+        if (lane == j) { my_e = e; my_s = w_sc[e]; }
+        const float lo = __fsub_rd(ws, wb), hi = __fadd_ru(ws, wb);
+        if (j > 0 && !(prev_lo > hi)) order_ok = false;
+        prev_lo = lo;
+        lower_min = fminf(lower_min, lo);
+    }
+    int n_cand = 0;
+    for (int i = 0; i < NI; ++i) {
+        const int e = lane + 32 * i;
+        const bool c = e < E && eligible(e) && __fadd_ru(w_sel[e], w_bnd[e]) >= lower_min;
+        n_cand += __popc(__ballot_sync(kFullMask, c));
+    }
+    if (n_cand != K || !order_ok) {
+        __syncwarp();
+        return false;
+    }
+    float den = 0.f;
+    for (int j = 0; j < K; ++j) den += __shfl_sync(kFullMask, my_s, j);
+    if (lane < K) {
+        oi[lane] = my_e;
+        ow[lane] = a.renorm ? my_s / den : my_s;
+    }
+    __syncwarp();
+    return true;
+}
+
+// The general routing options in fp64 from re-scored logits of EVERY expert of a token:
+// pv[e] holds expert e's logit on entry (pe[e] == e); pv is overwritten with the scores,
+// pe marks taken experts as -1 - e.  Warp-wide.
+__device__ void select_general64(const RouterArgs &a, int *pe, double *pv, int32_t *oi,
+                                 float *ow, int *ord, int lane)
+{
+    const int E = a.E, K = a.K;
+    if (a.scoring == 1) {
+        double m = -DBL_MAX;
+        for (int e = lane; e < E; e += 32) m = fmax(m, pv[e]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = fmax(m, __shfl_xor_sync(kFullMask, m, off));
+        double sum = 0.0;
+        for (int e = lane; e < E; e += 32) {
+            const double v = exp(pv[e] - m);
+            pv[e] = v;
+            sum += v;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFullMask, sum, off);
+        for (int e = lane; e < E; e += 32) pv[e] /= sum;
+    } else {
+        for (int e = lane; e < E; e += 32) pv[e] = 1.0 / (1.0 + exp(-pv[e]));
+    }
+    __syncwarp();
+    uint32_t kmask = kFullMask;
+    int G = E;
+    if (a.n_group > 1) {
+        const int ng = a.n_group;
+        G = E / ng;
+        double gs = -DBL_MAX;
+        if (lane < ng) {
+            double s1 = -DBL_MAX, s2 = -DBL_MAX;
+            for (int e = lane * G; e < (lane + 1) * G; ++e) {
+                const double v = pv[e] + static_cast<double>(a.bias[e]);
+                if (v > s1) { s2 = s1; s1 = v; } else if (v > s2) { s2 = v; }
+            }
+            gs = a.group_top == 2 ? s1 + s2 : s1;
+        }
+        kmask = 0u;
+        bool in = lane < ng;
+        for (int r = 0; r < a.topk_group; ++r) {
+            double bs = in ? gs : -DBL_MAX;
+            int bg = in ? lane : INT_MAX;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const double os = __shfl_xor_sync(kFullMask, bs, off);
+                const int og = __shfl_xor_sync(kFullMask, bg, off);
+                if (og != INT_MAX && (bg == INT_MAX || before64(os, og, bs, bg))) { bs = os; bg = og; }
+            }
+            kmask |= 1u << bg;
+            if (lane == bg) in = false;
+        }
+    }
+    for (int j = 0; j < K; ++j) {
+        double bs = -DBL_MAX;
+        int be = INT_MAX;
+        for (int e = lane; e < E; e += 32) {
+            if (pe[e] < 0 || !((kmask >> (e / G)) & 1u)) continue;
+            const double v = pv[e] + static_cast<double>(a.bias[e]);
+            if (be == INT_MAX || before64(v, e, bs, be)) { bs = v; be = e; }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const double os = __shfl_xor_sync(kFullMask, bs, off);
+            const int oe = __shfl_xor_sync(kFullMask, be, off);
+            if (oe != INT_MAX && (be == INT_MAX || before64(os, oe, bs, be))) { bs = os; be = oe; }
+        }
+        if (lane == 0) ord[j] = be;
+        __syncwarp();
+        if (lane == (be & 31)) pe[be] = -1 - be;
+        __syncwarp();
+    }
+    double den = 0.0;
+    for (int j = 0; j < K; ++j) den += pv[ord[j]];
+    for (int j = lane; j < K; j += 32) {
+        const int e = ord[j];
+        oi[j] = e;
+        ow[j] = static_cast<float>(a.renorm ? pv[e] / den : pv[e]);
+    }
+    __syncwarp();
+}
+
+// Candidate bits of every expert (the general options re-score all of them).
+__device__ __forceinline__ uint32_t all_experts(int E, int lane)
+{
+    const int NI = (E + 31) / 32;
+    uint32_t c = 0;
+    for (int i = 0; i < NI; ++i)
+        if (lane + 32 * i < E) c |= 1u << i;
+    return c;
 }
 
 // Writes the lane-distributed candidate bits of a token as a compact expert list.
@@ -744,11 +1031,16 @@ __device__ void refine_token_warp(const RouterArgs &a, int t, uint32_t cand, int
     for (int q = 0; q < nc; ++q) {
         const int e = ce[q];
         const double l64 = dot_double_word(xrow, a.Wg + static_cast<size_t>(e) * a.H, a.H, lane);
-        if (lane == 0) s64[q] = 1.0 / (1.0 + exp(-l64)) + static_cast<double>(a.bias[e]);
+        if (lane == 0)
+            s64[q] = a.variant ? l64 : 1.0 / (1.0 + exp(-l64)) + static_cast<double>(a.bias[e]);
     }
     __syncwarp();
-    select_refined(ce, s64, nc, a.K, a.bias, a.topk_idx + static_cast<size_t>(t) * a.K,
-                   a.topk_w + static_cast<size_t>(t) * a.K, ord, lane);
+    if (a.variant)
+        select_general64(a, ce, s64, a.topk_idx + static_cast<size_t>(t) * a.K,
+                         a.topk_w + static_cast<size_t>(t) * a.K, ord, lane);
+    else
+        select_refined(ce, s64, nc, a.K, a.bias, a.topk_idx + static_cast<size_t>(t) * a.K,
+                       a.topk_w + static_cast<size_t>(t) * a.K, ord, lane);
 }
 
 // ------------------------------------------------------- fused kernel (small batches)
@@ -849,9 +1141,16 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
             int n_cand;
             int32_t *oi = a.topk_idx + static_cast<size_t>(t) * a.K;
             float *ow = a.topk_w + static_cast<size_t>(t) * a.K;
-            if (score_select(E, a.K, S.nxs[tl], S.nw, S.bias, bd.gam, S.sel, S.bnd, S.sc,
-                             oi, ow, cand, n_cand, lane))
+            if (a.variant) {
+                if (score_select_general(a, S.nxs[tl], S.nw, S.bias, bd.gam, S.sel, S.bnd, S.sc,
+                                         oi, ow, lane))
+                    continue;
+                cand = all_experts(E, lane);
+                n_cand = E;
+            } else if (score_select(E, a.K, S.nxs[tl], S.nw, S.bias, bd.gam, S.sel, S.bnd, S.sc,
+                                    oi, ow, cand, n_cand, lane)) {
                 continue;
+            }
             // not certified: queue the candidates for the CTA-wide double-word refine
             int base = 0;
             if (lane == 0) base = atomicAdd(&s_npairs, n_cand);
@@ -885,15 +1184,21 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
         const int t = t0 + S.p_tok[q];
         const double l64 = dot_double_word(a.X + static_cast<size_t>(t) * a.H,
                                            a.Wg + static_cast<size_t>(e) * a.H, a.H, lane);
-        if (lane == 0) S.p_val[q] = 1.0 / (1.0 + exp(-l64)) + static_cast<double>(a.bias[e]);
+        if (lane == 0)
+            S.p_val[q] = a.variant ? l64 : 1.0 / (1.0 + exp(-l64)) + static_cast<double>(a.bias[e]);
     }
     __syncthreads();
     for (int pi = warp; pi < s_npend; pi += NW) {
         const int tl = s_pend[3 * pi], first = s_pend[3 * pi + 1], cnt = s_pend[3 * pi + 2];
         const int t = t0 + tl;
-        select_refined(S.p_e + first, S.p_val + first, cnt, a.K, a.bias,
-                       a.topk_idx + static_cast<size_t>(t) * a.K,
-                       a.topk_w + static_cast<size_t>(t) * a.K, S.ord, lane);
+        if (a.variant)
+            select_general64(a, S.p_e + first, S.p_val + first,
+                             a.topk_idx + static_cast<size_t>(t) * a.K,
+                             a.topk_w + static_cast<size_t>(t) * a.K, S.ord, lane);
+        else
+            select_refined(S.p_e + first, S.p_val + first, cnt, a.K, a.bias,
+                           a.topk_idx + static_cast<size_t>(t) * a.K,
+                           a.topk_w + static_cast<size_t>(t) * a.K, S.ord, lane);
     }
 }
 
@@ -953,8 +1258,14 @@ __global__ void __launch_bounds__(NT) router_finalize_kernel(const RouterArgs a,
     int n_cand;
     int32_t *oi = a.topk_idx + static_cast<size_t>(t) * a.K;
     float *ow = a.topk_w + static_cast<size_t>(t) * a.K;
-    if (score_select(E, a.K, nx, w_nw, a.bias, bd.gam, w_sel, w_bnd, w_sc, oi, ow, cand, n_cand, lane))
+    if (a.variant) {
+        if (score_select_general(a, nx, w_nw, a.bias, bd.gam, w_sel, w_bnd, w_sc, oi, ow, lane))
+            return;
+        cand = all_experts(E, lane);
+    } else if (score_select(E, a.K, nx, w_nw, a.bias, bd.gam, w_sel, w_bnd, w_sc, oi, ow, cand,
+                            n_cand, lane)) {
         return;
+    }
     refine_token_warp(a, t, cand, ce, s64, ord, lane);
 }
 
@@ -1012,9 +1323,16 @@ RouterPlan router_plan(int T, int H, int E)
 cudaError_t launch_router(const void *X, const void *Wg, const float *bias, int T, int H,
                           int E, int K, int32_t *topk_idx, float *topk_w,
                           const RouterPlan &plan, const RouterScratch &scr, int *status,
-                          cudaStream_t s)
+                          cudaStream_t s, const RoutingOpts *ro)
 {
     RouterArgs a{};
+    const RoutingOpts opts = ro ? *ro : RoutingOpts{};
+    a.scoring = opts.scoring;
+    a.n_group = opts.n_group;
+    a.topk_group = opts.topk_group;
+    a.group_top = opts.group_top;
+    a.renorm = opts.renorm;
+    a.variant = opts.is_default() ? 0 : 1;
     a.X = static_cast<const uint16_t *>(X);
     a.Wg = static_cast<const uint16_t *>(Wg);
     a.bias = bias;

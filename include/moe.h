@@ -133,6 +133,34 @@ int moe_router_topk(const void *X, const void *W_gate, const float *bias,
                     int32_t *topk_idx, float *topk_w,
                     void *ws, size_t ws_bytes, void *stream);
 
+/* Routing options of the other MoE families one router serves ("Lower latency and higher
+ * throughput...", MoE Router: one router for every MoE model, DeepSeek's routing selects
+ * among expert groups and Mixtral's is the case of a single group holding every expert).
+ * The defaults {0, 1, 1, 1, 1} are moe_router_topk's routing.  A NULL moe_routing_t
+ * pointer means the defaults. */
+typedef struct moe_routing {
+    int scoring;     /* 0: s = sigmoid(l); 1: s = softmax of the token's E logits */
+    int n_group;     /* the E experts form n_group groups of E / n_group consecutive
+                        experts (n_group divides E; 1..32; 1 = no group limit) */
+    int topk_group;  /* groups kept per token (1..n_group): those with the largest group
+                        score, equal scores -> lower group first; the top-K is taken among
+                        their experts only */
+    int group_top;   /* a group's score is the sum of its group_top (1 or 2) largest
+                        sel = s + bias */
+    int renorm;      /* 1: topk_w = the selected s divided by their sum; 0: the selected s */
+} moe_routing_t;
+
+/* moe_router_topk with routing options.  Selection order, tie-breaks and exactness as for
+ * moe_router_topk (a token the fp32 bounds cannot certify is re-scored for every expert
+ * in double-word arithmetic).  Errors: MOE_ERR_INVALID_ARG when the options define no
+ * selection (n_group not dividing E, topk_group outside 1..n_group, K > topk_group * E /
+ * n_group, scoring or renorm not 0/1, group_top < 1 or > E / n_group);
+ * MOE_ERR_UNSUPPORTED_SHAPE for n_group > 32 or group_top > 2. */
+int moe_router_topk_ex(const void *X, const void *W_gate, const float *bias,
+                       int T, int H, int E, int K, const moe_routing_t *routing,
+                       int32_t *topk_idx, float *topk_w,
+                       void *ws, size_t ws_bytes, void *stream);
+
 /* Router for callers that cannot allocate device memory.  No counterpart on the pages:
  * this is a convenience of this library.  Same inputs, outputs and results as
  * moe_router_topk, but without a workspace argument: the scratch lives in a fixed 16 MiB
@@ -215,6 +243,14 @@ int moe_layer_forward(const moe_shape_t *shape, const moe_weights_t *weights,
                       int32_t *topk_idx, float *topk_w, int32_t *counts,
                       int32_t *affinity,
                       void *ws, size_t ws_bytes, void *stream);
+
+/* moe_layer_forward with routing options (moe_routing_t; NULL = the defaults, the same
+ * call as moe_layer_forward).  Same workspace; option errors as moe_router_topk_ex. */
+int moe_layer_forward_ex(const moe_shape_t *shape, const moe_weights_t *weights,
+                         const moe_routing_t *routing, const void *X, float *Y,
+                         int32_t *topk_idx, float *topk_w, int32_t *counts,
+                         int32_t *affinity,
+                         void *ws, size_t ws_bytes, void *stream);
 
 #ifdef __cplusplus
 }

@@ -32,8 +32,9 @@ class Problem:
     """One layer problem: host copies of the routing inputs, device copies of everything."""
 
     def __init__(self, w: synth.Workload, routing: dict | None = None, weights_dev=None,
-                 host_weights: bool | None = None):
+                 host_weights: bool | None = None, opts: dict | None = None):
         self.w = w
+        self.opts = opts          # routing options (keywords of oracle.router_ex), or None
         self.routing = routing if routing is not None else synth.routing_inputs(w)
         small = w.E * w.H * w.I < 64 * 1024 * 1024
         if host_weights is None:
@@ -61,7 +62,8 @@ class Problem:
 
     # ---------------------------------------------------------------- CUDA path
     def run_layer(self, with_affinity=True):
-        layer = B.MoELayer(self.dev, self.w.T, self.w.K, with_affinity=with_affinity)
+        layer = B.MoELayer(self.dev, self.w.T, self.w.K, with_affinity=with_affinity,
+                           routing=self.opts)
         layer.forward(self.X)
         torch.cuda.synchronize()
         st = layer.status()
@@ -70,6 +72,9 @@ class Problem:
 
     # ------------------------------------------------------------------- oracle
     def oracle_routing(self):
+        if self.opts:
+            return oracle.router_ex(self.routing["X"], self.routing["W_gate"],
+                                    self.routing["bias"], self.w.K, **self.opts)
         return oracle.router(self.routing["X"], self.routing["W_gate"], self.routing["bias"],
                              self.w.K)
 

@@ -73,3 +73,32 @@ def test_validation_rejects_before_launch(lib):
     assert g(ok, ok, ok, bad, 4, 256, 2, ok, None) == -3                    # Ysh misaligned
     assert g(ok, ok, ok, None, 4, 256, 33, ok, None) == -2                  # K > 32
     assert g(ok, ok, ok, None, 0, 256, 2, ok, None) == 0                    # T == 0: no-op
+
+
+def test_routing_options_are_validated_before_launch(lib):
+    P, I = ctypes.c_void_p, ctypes.c_int
+    f = lib.moe_router_topk_ex
+    f.restype = I
+    f.argtypes = [P, P, P, I, I, I, I, ctypes.POINTER(binding.MoeRouting), P, P, P,
+                  ctypes.c_size_t, P]
+    ok = P(0x10000)            # never dereferenced: every call below fails validation
+    ws = P(0x100000)
+
+    def call(E, K, **kw):
+        r = binding.MoeRouting.make(**kw)
+        return f(ok, ok, ok, 4, 256, E, K, ctypes.byref(r), ok, ok, ws, 16, None)
+
+    # options that define no selection -> MOE_ERR_INVALID_ARG
+    assert call(16, 2, n_group=3) == -1                         # 3 does not divide 16
+    assert call(16, 2, n_group=4, topk_group=5) == -1           # more groups kept than exist
+    assert call(16, 2, n_group=4, topk_group=0) == -1
+    assert call(16, 9, n_group=4, topk_group=2) == -1           # K > 2 groups x 4 experts
+    assert call(16, 2, n_group=4, topk_group=2, group_top=5) == -1
+    r = binding.MoeRouting(2, 1, 1, 1, 1)                       # scoring 2 is undefined
+    assert f(ok, ok, ok, 4, 256, 16, 2, ctypes.byref(r), ok, ok, ws, 16, None) == -1
+    # defined but outside the kernel's support -> MOE_ERR_UNSUPPORTED_SHAPE
+    assert call(128, 2, n_group=64, topk_group=2) == -2
+    assert call(16, 2, n_group=2, topk_group=1, group_top=3) == -2
+    # valid options reach the next check (the 16-byte workspace is too small)
+    assert call(16, 2, n_group=4, topk_group=2, group_top=2, scoring="softmax") == -4
+    assert f(ok, ok, ok, 4, 256, 16, 2, None, ok, ok, ws, 16, None) == -4   # NULL = defaults
