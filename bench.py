@@ -35,6 +35,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (its up and down projections are one launch: the next mark is the same point, and
 # "ffn_down" reads ~0), after the FFN, after combine
 STAGES = ("router", "dispatch", "ffn_up", "ffn_down", "combine")
+# routing options of other MoE families (moe_routing_t); "default" is the plain router
+ROUTINGS = {
+    "default": None,
+    "groups_top2": dict(scoring="sigmoid", n_group=8, topk_group=4, group_top=2),
+    "softmax_groups_max": dict(scoring="softmax", n_group=8, topk_group=3, group_top=1,
+                               renorm=False),
+    "softmax": dict(scoring="softmax"),
+}
 
 
 def load_peaks():
@@ -204,7 +212,8 @@ def run_ours(args, rank, world, local_rank):
     weights["bias"] = torch.from_numpy(routing["bias"]).to(dev)
     X_host = torch.from_numpy(routing["X"].view(np.int16)).view(torch.bfloat16)
     X = X_host.to(dev)
-    layer = B.MoELayer(weights, w.T, w.K, with_affinity=True)
+    opts = ROUTINGS[args.routing]
+    layer = B.MoELayer(weights, w.T, w.K, with_affinity=True, routing=opts)
     peaks, peak_src = load_peaks()
 
     def barrier():
@@ -305,6 +314,7 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "inputs larger than L2: the activated experts' weights "
                          f"({layer_bytes / 1e9:.1f} GB) stream from HBM every step",
                    "n_active_experts": n_act},
+        **({"routing": {"name": args.routing, **opts}} if opts else {}),
         "e2e": {"value": round(total_tokens / (ms_e2e / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(Xh.numel() * Xh.element_size()),
                 "d2h_bytes_per_step": int(Yh.numel() * Yh.element_size())},
@@ -319,19 +329,24 @@ def run_ours(args, rank, world, local_rank):
         "clocks": sampler.summary(t_wall0, t_wall1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(w, routing, weights, budget_s=args.cpu_budget)
+        out["cpu_baseline"] = cpu_baseline(w, routing, weights, budget_s=args.cpu_budget,
+                                           opts=opts)
     return out
 
 
 # --------------------------------------------------------------------- oracle (CPU)
-def _oracle_step(w, routing, weights, tokens, host_cache):
-    """One oracle pass over `tokens`: router for those tokens + their experts + shared."""
-    import numpy as np
-
+def _oracle_route(w, routing, X, opts):
     import oracle
+    if opts:
+        return oracle.router_ex(X, routing["W_gate"], routing["bias"], w.K, **opts)
+    return oracle.router(X, routing["W_gate"], routing["bias"], w.K)
+
+
+def _oracle_step(w, routing, weights, tokens, host_cache, opts=None):
+    """One oracle pass over `tokens`: router for those tokens + their experts + shared."""
     from expert_routed_ffn_router_gb300 import synth
     X = routing["X"][tokens]
-    idx, wt = oracle.router(X, routing["W_gate"], routing["bias"], w.K)
+    idx, wt = _oracle_route(w, routing, X, opts)
     used = sorted({int(e) for e in idx.ravel()})
     for e in used:
         if e not in host_cache:
@@ -341,13 +356,13 @@ def _oracle_step(w, routing, weights, tokens, host_cache):
     return X, idx, wt, used
 
 
-def _oracle_timed(w, routing, weights, tokens, host_cache):
+def _oracle_timed(w, routing, weights, tokens, host_cache, opts=None):
     import numpy as np
 
     import oracle
-    X, idx, wt, used = _oracle_step(w, routing, weights, tokens, host_cache)
+    X, idx, wt, used = _oracle_step(w, routing, weights, tokens, host_cache, opts)
     t0 = time.perf_counter()
-    idx, wt = oracle.router(X, routing["W_gate"], routing["bias"], w.K)
+    idx, wt = _oracle_route(w, routing, X, opts)
     sh = host_cache.get("shared", (None, None, None))
     oracle.layer_tokens(X, idx, wt, {e: host_cache[e][0] for e in used},
                         {e: host_cache[e][1] for e in used}, {e: host_cache[e][2] for e in used},
@@ -355,18 +370,18 @@ def _oracle_timed(w, routing, weights, tokens, host_cache):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(w, routing, weights, budget_s=12.0):
+def cpu_baseline(w, routing, weights, budget_s=12.0, opts=None):
     import numpy as np
 
     import oracle
     cores = oracle.num_threads()
     cache = {}
     n1 = cores
-    t1 = _oracle_timed(w, routing, weights, np.arange(n1) % w.T, cache)
+    t1 = _oracle_timed(w, routing, weights, np.arange(n1) % w.T, cache, opts)
     per_tok = t1 / n1
     n = int(min(w.T, max(n1, round(budget_s / max(per_tok, 1e-6)))))
     tokens = np.arange(n) % w.T
-    t = _oracle_timed(w, routing, weights, tokens, cache)
+    t = _oracle_timed(w, routing, weights, tokens, cache, opts)
     return {"value": round(n / t, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"first {n} of the {w.T} tokens of the workload: fp64 router over all "
                       f"{w.E} experts + the {w.K} routed experts and the shared expert of each "
@@ -386,24 +401,26 @@ def run_reference(args):
     cores = oracle.num_threads()
     cache = {}
     # size each step so that warm-up + timed steps take about two minutes
-    t1 = _oracle_timed(w, routing, weights, np.arange(cores) % w.T, cache)
+    opts = ROUTINGS[args.routing]
+    t1 = _oracle_timed(w, routing, weights, np.arange(cores) % w.T, cache, opts)
     per_tok = t1 / cores
     budget = 120.0 / max(1, args.steps + args.warmup)
     n = int(max(1, min(w.T, round(budget / max(per_tok, 1e-6)))))
     rng = np.random.default_rng(0)
     steps_tok = [rng.choice(w.T, size=n, replace=False) for _ in range(args.warmup + args.steps)]
     for k in range(args.warmup):
-        _oracle_timed(w, routing, weights, steps_tok[k], cache)
+        _oracle_timed(w, routing, weights, steps_tok[k], cache, opts)
     tt = 0.0
     for k in range(args.steps):
-        tt += _oracle_timed(w, routing, weights, steps_tok[args.warmup + k], cache)
+        tt += _oracle_timed(w, routing, weights, steps_tok[args.warmup + k], cache, opts)
     value = n * args.steps / tt
     return {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tt / args.steps * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)", "impl": "reference",
-        "config": {"workload": f"{w.name}: DeepSeek-V3-shaped MoE layer forward, T={w.T}"},
+        "config": {"workload": f"{w.name}: DeepSeek-V3-shaped MoE layer forward, T={w.T}",
+                   **({"routing": {"name": args.routing, **opts}} if opts else {})},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{n} random tokens of the {w.T}-token workload per step"},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -419,6 +436,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="decode",
                     help="decode (default), tiny, sweep2..sweep256, prefill, skewed")
+    ap.add_argument("--routing", choices=sorted(ROUTINGS), default="default",
+                    help="routing options of other MoE families (default: the plain router)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()

@@ -222,7 +222,7 @@ __device__ double dot_double_word(const uint16_t *x, const uint16_t *w, int H, i
 // writes the experts and their renormalised weights.  Warp-wide; pairs live in shared
 // memory; taken pairs are marked by storing -1 - expert.
 __device__ void select_refined(int *pe, const double *pv, int n, int K, const float *bias,
-                               int32_t *oi, float *ow, int *ord, int lane)
+                               int32_t *oi, float *ow, int *ord, int lane, int renorm = 1)
 {
     for (int j = 0; j < K; ++j) {
         double bs = -DBL_MAX;
@@ -253,7 +253,8 @@ __device__ void select_refined(int *pe, const double *pv, int n, int K, const fl
     for (int j = lane; j < K; j += 32) {
         const int q = ord[j], e = -1 - pe[q];
         oi[j] = e;
-        ow[j] = static_cast<float>((pv[q] - static_cast<double>(bias[e])) / den);
+        const double sc = pv[q] - static_cast<double>(bias[e]);
+        ow[j] = static_cast<float>(renorm ? sc / den : sc);
     }
     __syncwarp();
 }
@@ -419,8 +420,12 @@ __device__ __forceinline__ void top2_push(float v, float &v1, float &v2)
 
 // Scores one token with the general routing options (softmax scoring, group-limited
 // selection, unnormalised weights) and selects its top-K in fp32 with certified bounds.
-// Same contract as score_select; when the result is not certified the caller re-scores
-// every expert of the token (softmax needs all of them) and calls select_general64.
+// Returns 1 when the result is certified and written.  Returns 0 when the kept groups are
+// certified but not the top-K among them and the scores are sigmoids: `cand` / `n_cand`
+// then hold the candidates (kept-group experts whose upper bound reaches the K-th lower
+// bound), to be re-scored and passed to select_candidates64.  Returns -1 otherwise: the
+// caller re-scores every expert of the token (softmax needs all of them, and so does an
+// uncertain group choice) and calls select_general64.
 //
 // Softmax bound.  With every logit within beta of its fp32 value, the exact s_e lies
 // within a factor e^{+-2 beta} of exp(l^_e) / sum_j exp(l^_j) (numerator and denominator
@@ -433,9 +438,10 @@ __device__ __forceinline__ void top2_push(float v, float &v1, float &v2)
 // so the sums of the n largest lower / upper bounds enclose it.  The kept groups are
 // certified when the smallest lower bound among them exceeds the largest upper bound of
 // the others.
-__device__ bool score_select_general(const RouterArgs &a, float nx, const float *nw,
-                                     const float *bias, float gam, float *w_sel, float *w_bnd,
-                                     float *w_sc, int32_t *oi, float *ow, int lane)
+__device__ int score_select_general(const RouterArgs &a, float nx, const float *nw,
+                                    const float *bias, float gam, float *w_sel, float *w_bnd,
+                                    float *w_sc, int32_t *oi, float *ow, uint32_t &cand,
+                                    int &n_cand, int lane)
 {
     const int E = a.E, K = a.K, NI = (E + 31) / 32;
     if (a.scoring == 0) {
@@ -519,7 +525,7 @@ __device__ bool score_select_general(const RouterArgs &a, float nx, const float 
         const bool kept = lane < ng && ((kmask >> lane) & 1u);
         const float klo = warp_min_f(kept ? glo : FLT_MAX);
         const float ohi = warp_max_f(lane < ng && !kept ? ghi : -FLT_MAX);
-        if (a.topk_group < ng && !(klo > ohi)) return false;
+        if (a.topk_group < ng && !(klo > ohi)) return -1;
     }
 
     // top-K among the experts of the kept groups: each lane keeps its best untaken key
@@ -554,15 +560,17 @@ __device__ bool score_select_general(const RouterArgs &a, float nx, const float 
         prev_lo = lo;
         lower_min = fminf(lower_min, lo);
     }
-    int n_cand = 0;
+    n_cand = 0;
+    cand = 0;
     for (int i = 0; i < NI; ++i) {
         const int e = lane + 32 * i;
         const bool c = e < E && eligible(e) && __fadd_ru(w_sel[e], w_bnd[e]) >= lower_min;
+        if (c) cand |= 1u << i;
         n_cand += __popc(__ballot_sync(kFullMask, c));
     }
     if (n_cand != K || !order_ok) {
         __syncwarp();
-        return false;
+        return a.scoring == 0 ? 0 : -1;
     }
     float den = 0.f;
     for (int j = 0; j < K; ++j) den += __shfl_sync(kFullMask, my_s, j);
@@ -571,7 +579,18 @@ __device__ bool score_select_general(const RouterArgs &a, float nx, const float 
         ow[lane] = a.renorm ? my_s / den : my_s;
     }
     __syncwarp();
-    return true;
+    return 1;
+}
+
+// Top-K among re-scored sigmoid candidates (all in the certified kept groups): pv[q] holds
+// the fp64 logit of expert pe[q] on entry and is turned into sel = sigmoid + bias here.
+__device__ void select_candidates64(const RouterArgs &a, int *pe, double *pv, int n,
+                                    int32_t *oi, float *ow, int *ord, int lane)
+{
+    for (int q = lane; q < n; q += 32)
+        pv[q] = 1.0 / (1.0 + exp(-pv[q])) + static_cast<double>(a.bias[pe[q]]);
+    __syncwarp();
+    select_refined(pe, pv, n, a.K, a.bias, oi, ow, ord, lane, a.renorm);
 }
 
 // The general routing options in fp64 from re-scored logits of EVERY expert of a token:
@@ -1024,7 +1043,7 @@ struct FinSmem {
 // Refines one token with its warp alone (used when the shared list is full, and by the
 // one-warp-per-token finaliser).
 __device__ void refine_token_warp(const RouterArgs &a, int t, uint32_t cand, int *ce,
-                                  double *s64, int *ord, int lane)
+                                  double *s64, int *ord, int lane, bool every = false)
 {
     const int nc = list_candidates(cand, a.E, ce, lane);
     const uint16_t *xrow = a.X + static_cast<size_t>(t) * a.H;
@@ -1035,9 +1054,12 @@ __device__ void refine_token_warp(const RouterArgs &a, int t, uint32_t cand, int
             s64[q] = a.variant ? l64 : 1.0 / (1.0 + exp(-l64)) + static_cast<double>(a.bias[e]);
     }
     __syncwarp();
-    if (a.variant)
+    if (a.variant && every)
         select_general64(a, ce, s64, a.topk_idx + static_cast<size_t>(t) * a.K,
                          a.topk_w + static_cast<size_t>(t) * a.K, ord, lane);
+    else if (a.variant)
+        select_candidates64(a, ce, s64, nc, a.topk_idx + static_cast<size_t>(t) * a.K,
+                            a.topk_w + static_cast<size_t>(t) * a.K, ord, lane);
     else
         select_refined(ce, s64, nc, a.K, a.bias, a.topk_idx + static_cast<size_t>(t) * a.K,
                        a.topk_w + static_cast<size_t>(t) * a.K, ord, lane);
@@ -1141,12 +1163,16 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
             int n_cand;
             int32_t *oi = a.topk_idx + static_cast<size_t>(t) * a.K;
             float *ow = a.topk_w + static_cast<size_t>(t) * a.K;
+            bool every = false;
             if (a.variant) {
-                if (score_select_general(a, S.nxs[tl], S.nw, S.bias, bd.gam, S.sel, S.bnd, S.sc,
-                                         oi, ow, lane))
-                    continue;
-                cand = all_experts(E, lane);
-                n_cand = E;
+                const int r = score_select_general(a, S.nxs[tl], S.nw, S.bias, bd.gam, S.sel,
+                                                   S.bnd, S.sc, oi, ow, cand, n_cand, lane);
+                if (r > 0) continue;
+                if (r < 0) {
+                    every = true;
+                    cand = all_experts(E, lane);
+                    n_cand = E;
+                }
             } else if (score_select(E, a.K, S.nxs[tl], S.nw, S.bias, bd.gam, S.sel, S.bnd, S.sc,
                                     oi, ow, cand, n_cand, lane)) {
                 continue;
@@ -1162,7 +1188,7 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
                     const int pi = atomicAdd(&s_npend, 1);
                     s_pend[3 * pi] = c0 + tl;
                     s_pend[3 * pi + 1] = base;
-                    s_pend[3 * pi + 2] = n_cand;
+                    s_pend[3 * pi + 2] = every ? -n_cand : n_cand;   // < 0: every expert
                 }
                 __syncwarp();
                 continue;
@@ -1171,7 +1197,7 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
             // refine this token with the warp alone
             for (int q = base + lane; q < a.max_pairs; q += 32) S.p_e[q] = -1;
             __syncwarp();
-            refine_token_warp(a, t, cand, S.ce, S.s64, S.ord, lane);
+            refine_token_warp(a, t, cand, S.ce, S.s64, S.ord, lane, every);
         }
     }
     __syncthreads();
@@ -1191,10 +1217,14 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
     for (int pi = warp; pi < s_npend; pi += NW) {
         const int tl = s_pend[3 * pi], first = s_pend[3 * pi + 1], cnt = s_pend[3 * pi + 2];
         const int t = t0 + tl;
-        if (a.variant)
+        if (a.variant && cnt < 0)
             select_general64(a, S.p_e + first, S.p_val + first,
                              a.topk_idx + static_cast<size_t>(t) * a.K,
                              a.topk_w + static_cast<size_t>(t) * a.K, S.ord, lane);
+        else if (a.variant)
+            select_candidates64(a, S.p_e + first, S.p_val + first, cnt,
+                                a.topk_idx + static_cast<size_t>(t) * a.K,
+                                a.topk_w + static_cast<size_t>(t) * a.K, S.ord, lane);
         else
             select_refined(S.p_e + first, S.p_val + first, cnt, a.K, a.bias,
                            a.topk_idx + static_cast<size_t>(t) * a.K,
@@ -1258,15 +1288,20 @@ __global__ void __launch_bounds__(NT) router_finalize_kernel(const RouterArgs a,
     int n_cand;
     int32_t *oi = a.topk_idx + static_cast<size_t>(t) * a.K;
     float *ow = a.topk_w + static_cast<size_t>(t) * a.K;
+    bool every = false;
     if (a.variant) {
-        if (score_select_general(a, nx, w_nw, a.bias, bd.gam, w_sel, w_bnd, w_sc, oi, ow, lane))
-            return;
-        cand = all_experts(E, lane);
+        const int r = score_select_general(a, nx, w_nw, a.bias, bd.gam, w_sel, w_bnd, w_sc, oi,
+                                           ow, cand, n_cand, lane);
+        if (r > 0) return;
+        if (r < 0) {
+            every = true;
+            cand = all_experts(E, lane);
+        }
     } else if (score_select(E, a.K, nx, w_nw, a.bias, bd.gam, w_sel, w_bnd, w_sc, oi, ow, cand,
                             n_cand, lane)) {
         return;
     }
-    refine_token_warp(a, t, cand, ce, s64, ord, lane);
+    refine_token_warp(a, t, cand, ce, s64, ord, lane, every);
 }
 
 size_t fused_smem(int TT, int TE, int E, int max_pairs)
