@@ -420,12 +420,14 @@ __device__ __forceinline__ void top2_push(float v, float &v1, float &v2)
 
 // Scores one token with the general routing options (softmax scoring, group-limited
 // selection, unnormalised weights) and selects its top-K in fp32 with certified bounds.
-// Returns 1 when the result is certified and written.  Returns 0 when the kept groups are
-// certified but not the top-K among them and the scores are sigmoids: `cand` / `n_cand`
-// then hold the candidates (kept-group experts whose upper bound reaches the K-th lower
-// bound), to be re-scored and passed to select_candidates64.  Returns -1 otherwise: the
-// caller re-scores every expert of the token (softmax needs all of them, and so does an
-// uncertain group choice) and calls select_general64.
+// Returns 1 when the result is certified and written.  With sigmoid scores, returns 0
+// when it is not: `cand` / `n_cand` hold the experts to re-score and `ck` / `ug` the
+// groups certainly kept / still undecided (bit g), for select_candidates64.  The
+// candidates are the members of undecided groups that may be among their group's
+// group_top best (upper bound >= the group's group_top-th lower bound) and the experts of
+// kept or undecided groups whose upper bound reaches the K-th largest lower bound among
+// the experts of the certainly kept groups.  With softmax scores returns -1 instead: the
+// caller re-scores every expert (the normaliser needs all of them) for select_general64.
 //
 // Softmax bound.  With every logit within beta of its fp32 value, the exact s_e lies
 // within a factor e^{+-2 beta} of exp(l^_e) / sum_j exp(l^_j) (numerator and denominator
@@ -441,7 +443,7 @@ __device__ __forceinline__ void top2_push(float v, float &v1, float &v2)
 __device__ int score_select_general(const RouterArgs &a, float nx, const float *nw,
                                     const float *bias, float gam, float *w_sel, float *w_bnd,
                                     float *w_sc, int32_t *oi, float *ow, uint32_t &cand,
-                                    int &n_cand, int lane)
+                                    int &n_cand, uint32_t &ck, uint32_t &ug, int lane)
 {
     const int E = a.E, K = a.K, NI = (E + 31) / 32;
     if (a.scoring == 0) {
@@ -497,13 +499,17 @@ __device__ int score_select_general(const RouterArgs &a, float nx, const float *
     // groups kept (bit g), certified against the others
     uint32_t kmask = kFullMask;
     int G = E;
+    bool groups_ok = true;
+    float nth_lo = -FLT_MAX;       // lane g: the group_top-th largest lower bound of group g
+    ck = kFullMask;
+    ug = 0u;
     if (a.n_group > 1) {
         const int ng = a.n_group;
         G = E / ng;
         float glo = -FLT_MAX, ghi = -FLT_MAX;
         unsigned long long key = 0ull;
+        float s1 = -FLT_MAX, s2 = -FLT_MAX, l1 = -FLT_MAX, l2 = -FLT_MAX, h1 = -FLT_MAX, h2 = -FLT_MAX;
         if (lane < ng) {
-            float s1 = -FLT_MAX, s2 = -FLT_MAX, l1 = -FLT_MAX, l2 = -FLT_MAX, h1 = -FLT_MAX, h2 = -FLT_MAX;
             for (int e = lane * G; e < (lane + 1) * G; ++e) {
                 const float v = w_sel[e], b = w_bnd[e];
                 top2_push(v, s1, s2);
@@ -525,7 +531,61 @@ __device__ int score_select_general(const RouterArgs &a, float nx, const float *
         const bool kept = lane < ng && ((kmask >> lane) & 1u);
         const float klo = warp_min_f(kept ? glo : FLT_MAX);
         const float ohi = warp_max_f(lane < ng && !kept ? ghi : -FLT_MAX);
-        if (a.topk_group < ng && !(klo > ohi)) return -1;
+        ck = kmask;
+        if (a.topk_group < ng && !(klo > ohi)) {
+            if (a.scoring != 0) return -1;
+            // a kept group above every other group's upper bound is kept for certain, an
+            // other group below every kept group's lower bound is dropped for certain
+            groups_ok = false;
+            ck = __ballot_sync(kFullMask, kept && glo > ohi);
+            ug = __ballot_sync(kFullMask, lane < ng && !(kept && glo > ohi) && !(!kept && ghi < klo));
+            nth_lo = a.group_top == 2 ? l2 : l1;
+        }
+    }
+
+    if (!groups_ok) {
+        // K-th largest lower bound among the experts of the certainly kept groups
+        uint32_t tk = 0;
+        auto best_lo = [&]() {
+            unsigned long long b = 0ull;
+            for (int i = 0; i < NI; ++i) {
+                const int e = lane + 32 * i;
+                if (e >= E) break;
+                if ((tk >> i) & 1u || !((ck >> (e / G)) & 1u)) continue;
+                const unsigned long long k = rank_key(__fsub_rd(w_sel[e], w_bnd[e]), e);
+                b = k > b ? k : b;
+            }
+            return b;
+        };
+        unsigned long long b = best_lo();
+        float L = FLT_MAX;
+        for (int j = 0; j < K; ++j) {
+            const unsigned long long win = warp_max_u64(b);
+            if (win == 0ull) { L = -FLT_MAX; break; }     // fewer than K such experts
+            const int e = static_cast<int>(~static_cast<uint32_t>(win));
+            if ((e & 31) == lane) {
+                tk |= 1u << (e >> 5);
+                b = best_lo();
+            }
+            L = fminf(L, __fsub_rd(w_sel[e], w_bnd[e]));
+        }
+        n_cand = 0;
+        cand = 0;
+        for (int i = 0; i < NI; ++i) {
+            const int e = lane + 32 * i;
+            const int g = e < E ? e / G : 0;
+            const float gth = __shfl_sync(kFullMask, nth_lo, g);
+            bool c = false;
+            if (e < E) {
+                const float hi = __fadd_ru(w_sel[e], w_bnd[e]);
+                const bool live = ((ck | ug) >> g) & 1u;
+                c = (live && hi >= L) || (((ug >> g) & 1u) && hi >= gth);
+            }
+            if (c) cand |= 1u << i;
+            n_cand += __popc(__ballot_sync(kFullMask, c));
+        }
+        __syncwarp();
+        return 0;
     }
 
     // top-K among the experts of the kept groups: each lane keeps its best untaken key
@@ -582,13 +642,50 @@ __device__ int score_select_general(const RouterArgs &a, float nx, const float *
     return 1;
 }
 
-// Top-K among re-scored sigmoid candidates (all in the certified kept groups): pv[q] holds
-// the fp64 logit of expert pe[q] on entry and is turned into sel = sigmoid + bias here.
+// The selection from re-scored sigmoid candidates (score_select_general's 0 case): pv[q]
+// holds the fp64 logit of expert pe[q] on entry and is turned into sel = sigmoid + bias.
+// Undecided groups (bit g of ug) are scored by the group_top best sel of their candidates
+// -- every member that can be among them is a candidate -- and the best of them join the
+// certainly kept groups (ck) up to topk_group (equal scores: lower group first); the top-K
+// is then taken among the candidates of the kept groups.
 __device__ void select_candidates64(const RouterArgs &a, int *pe, double *pv, int n,
-                                    int32_t *oi, float *ow, int *ord, int lane)
+                                    uint32_t ck, uint32_t ug, int32_t *oi, float *ow, int *ord,
+                                    int lane)
 {
     for (int q = lane; q < n; q += 32)
         pv[q] = 1.0 / (1.0 + exp(-pv[q])) + static_cast<double>(a.bias[pe[q]]);
+    __syncwarp();
+    const int G = a.E / a.n_group;
+    uint32_t kept = ck;
+    if (ug) {
+        double gs = -DBL_MAX;
+        bool in = ((ug >> lane) & 1u) != 0u;
+        if (in) {
+            double s1 = -DBL_MAX, s2 = -DBL_MAX;
+            for (int q = 0; q < n; ++q) {
+                if (pe[q] / G != lane) continue;
+                const double v = pv[q];
+                if (v > s1) { s2 = s1; s1 = v; } else if (v > s2) { s2 = v; }
+            }
+            gs = a.group_top == 2 ? s1 + s2 : s1;
+        }
+        const int more = a.topk_group - __popc(ck);
+        for (int r = 0; r < more; ++r) {
+            double bs = in ? gs : -DBL_MAX;
+            int bg = in ? lane : INT_MAX;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const double os = __shfl_xor_sync(kFullMask, bs, off);
+                const int og = __shfl_xor_sync(kFullMask, bg, off);
+                if (og != INT_MAX && (bg == INT_MAX || before64(os, og, bs, bg))) { bs = os; bg = og; }
+            }
+            kept |= 1u << bg;
+            if (lane == bg) in = false;
+        }
+    }
+    __syncwarp();
+    for (int q = lane; q < n; q += 32)
+        if (!((kept >> (pe[q] / G)) & 1u)) pe[q] = -1 - pe[q];
     __syncwarp();
     select_refined(pe, pv, n, a.K, a.bias, oi, ow, ord, lane, a.renorm);
 }
@@ -1043,7 +1140,8 @@ struct FinSmem {
 // Refines one token with its warp alone (used when the shared list is full, and by the
 // one-warp-per-token finaliser).
 __device__ void refine_token_warp(const RouterArgs &a, int t, uint32_t cand, int *ce,
-                                  double *s64, int *ord, int lane, bool every = false)
+                                  double *s64, int *ord, int lane, bool every = false,
+                                  uint32_t ck = kFullMask, uint32_t ug = 0u)
 {
     const int nc = list_candidates(cand, a.E, ce, lane);
     const uint16_t *xrow = a.X + static_cast<size_t>(t) * a.H;
@@ -1058,7 +1156,7 @@ __device__ void refine_token_warp(const RouterArgs &a, int t, uint32_t cand, int
         select_general64(a, ce, s64, a.topk_idx + static_cast<size_t>(t) * a.K,
                          a.topk_w + static_cast<size_t>(t) * a.K, ord, lane);
     else if (a.variant)
-        select_candidates64(a, ce, s64, nc, a.topk_idx + static_cast<size_t>(t) * a.K,
+        select_candidates64(a, ce, s64, nc, ck, ug, a.topk_idx + static_cast<size_t>(t) * a.K,
                             a.topk_w + static_cast<size_t>(t) * a.K, ord, lane);
     else
         select_refined(ce, s64, nc, a.K, a.bias, a.topk_idx + static_cast<size_t>(t) * a.K,
@@ -1072,7 +1170,7 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
     pdl_wait();
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_last, s_npairs, s_npend;
-    __shared__ int s_pend[3 * C::TT];     // (token, first pair, pair count) to refine
+    __shared__ int s_pend[5 * C::TT];     // (token, first pair, pair count, ck, ug) to refine
 
     if constexpr (GEMV > 0)
         gemv_tile<GEMV>(a, smem);
@@ -1164,9 +1262,11 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
             int32_t *oi = a.topk_idx + static_cast<size_t>(t) * a.K;
             float *ow = a.topk_w + static_cast<size_t>(t) * a.K;
             bool every = false;
+            uint32_t ck = kFullMask, ug = 0u;
             if (a.variant) {
                 const int r = score_select_general(a, S.nxs[tl], S.nw, S.bias, bd.gam, S.sel,
-                                                   S.bnd, S.sc, oi, ow, cand, n_cand, lane);
+                                                   S.bnd, S.sc, oi, ow, cand, n_cand, ck, ug,
+                                                   lane);
                 if (r > 0) continue;
                 if (r < 0) {
                     every = true;
@@ -1186,9 +1286,11 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
                 for (int q = lane; q < n_cand; q += 32) S.p_tok[base + q] = c0 + tl;
                 if (lane == 0) {
                     const int pi = atomicAdd(&s_npend, 1);
-                    s_pend[3 * pi] = c0 + tl;
-                    s_pend[3 * pi + 1] = base;
-                    s_pend[3 * pi + 2] = every ? -n_cand : n_cand;   // < 0: every expert
+                    s_pend[5 * pi] = c0 + tl;
+                    s_pend[5 * pi + 1] = base;
+                    s_pend[5 * pi + 2] = every ? -n_cand : n_cand;   // < 0: every expert
+                    s_pend[5 * pi + 3] = static_cast<int>(ck);
+                    s_pend[5 * pi + 4] = static_cast<int>(ug);
                 }
                 __syncwarp();
                 continue;
@@ -1197,7 +1299,7 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
             // refine this token with the warp alone
             for (int q = base + lane; q < a.max_pairs; q += 32) S.p_e[q] = -1;
             __syncwarp();
-            refine_token_warp(a, t, cand, S.ce, S.s64, S.ord, lane, every);
+            refine_token_warp(a, t, cand, S.ce, S.s64, S.ord, lane, every, ck, ug);
         }
     }
     __syncthreads();
@@ -1215,14 +1317,16 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
     }
     __syncthreads();
     for (int pi = warp; pi < s_npend; pi += NW) {
-        const int tl = s_pend[3 * pi], first = s_pend[3 * pi + 1], cnt = s_pend[3 * pi + 2];
+        const int tl = s_pend[5 * pi], first = s_pend[5 * pi + 1], cnt = s_pend[5 * pi + 2];
+        const uint32_t ck = static_cast<uint32_t>(s_pend[5 * pi + 3]);
+        const uint32_t ug = static_cast<uint32_t>(s_pend[5 * pi + 4]);
         const int t = t0 + tl;
         if (a.variant && cnt < 0)
             select_general64(a, S.p_e + first, S.p_val + first,
                              a.topk_idx + static_cast<size_t>(t) * a.K,
                              a.topk_w + static_cast<size_t>(t) * a.K, S.ord, lane);
         else if (a.variant)
-            select_candidates64(a, S.p_e + first, S.p_val + first, cnt,
+            select_candidates64(a, S.p_e + first, S.p_val + first, cnt, ck, ug,
                                 a.topk_idx + static_cast<size_t>(t) * a.K,
                                 a.topk_w + static_cast<size_t>(t) * a.K, S.ord, lane);
         else
@@ -1289,9 +1393,10 @@ __global__ void __launch_bounds__(NT) router_finalize_kernel(const RouterArgs a,
     int32_t *oi = a.topk_idx + static_cast<size_t>(t) * a.K;
     float *ow = a.topk_w + static_cast<size_t>(t) * a.K;
     bool every = false;
+    uint32_t ck = kFullMask, ug = 0u;
     if (a.variant) {
         const int r = score_select_general(a, nx, w_nw, a.bias, bd.gam, w_sel, w_bnd, w_sc, oi,
-                                           ow, cand, n_cand, lane);
+                                           ow, cand, n_cand, ck, ug, lane);
         if (r > 0) return;
         if (r < 0) {
             every = true;
@@ -1301,7 +1406,7 @@ __global__ void __launch_bounds__(NT) router_finalize_kernel(const RouterArgs a,
                             n_cand, lane)) {
         return;
     }
-    refine_token_warp(a, t, cand, ce, s64, ord, lane, every);
+    refine_token_warp(a, t, cand, ce, s64, ord, lane, every, ck, ug);
 }
 
 size_t fused_smem(int TT, int TE, int E, int max_pairs)

@@ -91,6 +91,23 @@ def test_groups_tie_on_score_lower_group_wins():
     assert np.all((idx >= 32) & (idx < 64))
 
 
+@pytest.mark.parametrize("topk_group", [1, 2, 4])
+def test_groups_near_tie_is_decided_exactly(topk_group):
+    # group 5 copies group 1 with one bf16 ulp added to one element of every row: the two
+    # group scores differ far inside the fp32 bound, so the group choice is left to the
+    # re-scored candidates
+    w = synth.workload("decode", T=80, x_seed=10)
+    r = synth.routing_inputs(w)
+    r["W_gate"][160:192] = r["W_gate"][32:64]
+    r["W_gate"][160:192, 7] += 1
+    r["bias"][160:192] = r["bias"][32:64]
+    r["bias"][32:64] += 0.3
+    r["bias"][160:192] += 0.3
+    for group_top in (1, 2):
+        opts = dict(scoring="sigmoid", n_group=8, topk_group=topk_group, group_top=group_top)
+        _check_router(r, w.K, opts)
+
+
 @pytest.mark.parametrize("name", ["groups_top2", "softmax_groups_max"])
 def test_layer_forward_with_routing_options(name):
     w = synth.Workload("rt", T=150, H=256, E=32, K=4, I=128, Is=128, seed=21, x_seed=22)
