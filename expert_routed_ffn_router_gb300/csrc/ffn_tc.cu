@@ -62,8 +62,8 @@ constexpr int MAX_CG = 1040;              // groups of all problems of a launch
 constexpr int CW = 32;                    // epilogue chunk: accumulator columns per TMEM load
 constexpr int XCHG_FLOATS = 2 * CW * 64;  // double-buffered G exchange (up epilogue)
 constexpr int PH_UP = 0, PH_DOWN = 1;
-constexpr int TQ = 4;
-constexpr int NT_BLOCK = 8;               // token tiles per block of a group's tile order                     // depth of the ring that hands claimed tiles to the roles
+constexpr int TQ = 4;                     // depth of the ring that hands claimed tiles to the roles
+constexpr int NT_BLOCK = 8;               // token tiles per block of a group's tile order
 constexpr int MAX_STAGES = 8;       // deeper rings measured slower at decode (HBM-bound up projection)
 
 struct ProbDev {
