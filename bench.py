@@ -282,6 +282,14 @@ def run_ours(args, rank, world, local_rank):
 
     counts = layer.counts.cpu().numpy()
     n_act = int((counts > 0).sum())
+    # GRACE-MoE placement for expert parallelism over 8 GPUs (4 per node), planned on the
+    # host from this step's counts and co-activation matrix (outside the timed regions)
+    A = layer.affinity.cpu().numpy()
+    t_plan = time.perf_counter()
+    plan = B.moe_grace_choose_r(A, 8, [0.0, 0.125, 0.25, 0.375, 0.5])
+    rep = B.moe_grace_replicate(counts, plan["group_of"], 8)
+    B.moe_grace_route_table(rep, 4)
+    ms_plan = (time.perf_counter() - t_plan) * 1e3
     b, f, layer_bytes, layer_flops = algorithmic(w, n_act)
     dom = max(("ffn", "router", "combine", "dispatch"), key=lambda s: stage_ms[s])
     t_dom = stage_ms[dom] / 1e3
@@ -326,6 +334,11 @@ def run_ours(args, rank, world, local_rank):
                            "tensor_frac": round(layer_flops / (ms / 1e3) / 1e12 /
                                                 peaks["bf16_tflops"], 4)},
         "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "grace_plan": {"gpus": 8, "gpus_per_node": 4, "r": plan["r"],
+                       "U": round(float(plan["U"][plan["knee"]]), 4),
+                       "S": round(float(plan["S"][plan["knee"]]), 4),
+                       "rho": round(rep["rho"], 4), "n_replica": rep["n_replica"],
+                       "n_hot": len(rep["hot"]), "planner_ms": round(ms_plan, 1)},
         "clocks": sampler.summary(t_wall0, t_wall1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -1,8 +1,8 @@
 """Builds the CUDA library in-tree: expert_routed_ffn_router_gb300/_lib/libmoe_gb300.so.
 
-nvcc compiles every translation unit of csrc/ for sm_103a (one -gencode) in parallel and
-links a shared library with the CUDA runtime linked statically, so the library has no
-dependency on the runtime that PyTorch ships.
+nvcc compiles every translation unit of csrc/ (CUDA for sm_103a, one -gencode; host C++)
+in parallel and links a shared library with the CUDA runtime linked statically, so the
+library has no dependency on the runtime that PyTorch ships.
 """
 from __future__ import annotations
 
@@ -33,7 +33,9 @@ def _nvcc() -> str:
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    # CUDA translation units and the host-only C++ ones (nvcc hands those to the host
+    # compiler)
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _digest() -> str:
@@ -61,7 +63,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(LIBDIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(LIBDIR, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [nvcc, *ARCH, *CFLAGS, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")

@@ -48,6 +48,12 @@ class MoeRouting(ctypes.Structure):
                    int(group_top), int(bool(renorm)))
 
 
+class MoeGraceReplication(ctypes.Structure):
+    _fields_ = [("heaviest", ctypes.c_int32), ("n_replica", ctypes.c_int32),
+                ("n_hot", ctypes.c_int32), ("rho", ctypes.c_double), ("W_mean", ctypes.c_double),
+                ("W_max", ctypes.c_longlong), ("W_r", ctypes.c_longlong)]
+
+
 def _routing(routing):
     if routing is None:
         return None
@@ -88,6 +94,11 @@ def load(build_if_missing: bool = True):
                                P, P, P, P, Z, P], I),
         "moe_layer_forward_ex": ([ctypes.POINTER(MoeShape), ctypes.POINTER(MoeWeights),
                                   ctypes.POINTER(MoeRouting), P, P, P, P, P, P, P, Z, P], I),
+        "moe_grace_metrics": ([P, I, P, I, P, P], I),
+        "moe_grace_group": ([P, I, I, ctypes.c_double, P], I),
+        "moe_grace_choose_r": ([P, I, I, P, I, P, P, P, P], I),
+        "moe_grace_replicate": ([P, I, P, I, P, P, P, ctypes.POINTER(MoeGraceReplication)], I),
+        "moe_grace_route_table": ([P, I, ctypes.POINTER(MoeGraceReplication), P, I, P, P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -254,3 +265,72 @@ class MoELayer:
 
     def status(self, stream=None) -> int:
         return moe_read_status(self.ws, stream)
+
+
+# ------------------------------------------------------ GRACE-MoE placement (host arrays)
+def _np(a, dtype):
+    import numpy as np
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _hp(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def moe_grace_metrics(affinity, group_of, D: int):
+    import numpy as np
+    A = _np(affinity, np.int32)
+    g = _np(group_of, np.int32)
+    U, S = ctypes.c_double(), ctypes.c_double()
+    _check("moe_grace_metrics", load().moe_grace_metrics(_hp(A), A.shape[0], _hp(g), int(D),
+                                                         ctypes.byref(U), ctypes.byref(S)))
+    return U.value, S.value
+
+
+def moe_grace_group(affinity, D: int, r: float):
+    import numpy as np
+    A = _np(affinity, np.int32)
+    g = np.zeros(A.shape[0], np.int32)
+    _check("moe_grace_group", load().moe_grace_group(_hp(A), A.shape[0], int(D), float(r), _hp(g)))
+    return g
+
+
+def moe_grace_choose_r(affinity, D: int, r_grid):
+    import numpy as np
+    A = _np(affinity, np.int32)
+    r = _np(r_grid, np.float64)
+    U, S = np.zeros(len(r)), np.zeros(len(r))
+    g = np.zeros(A.shape[0], np.int32)
+    k = ctypes.c_int()
+    _check("moe_grace_choose_r", load().moe_grace_choose_r(
+        _hp(A), A.shape[0], int(D), _hp(r), len(r), _hp(U), _hp(S), ctypes.byref(k), _hp(g)))
+    return dict(U=U, S=S, knee=k.value, r=float(r[k.value]), group_of=g)
+
+
+def moe_grace_replicate(counts, group_of, D: int):
+    import numpy as np
+    c = _np(counts, np.int32)
+    g = _np(group_of, np.int32)
+    W = np.zeros(D, np.int64)
+    hot = np.zeros(len(c), np.int32)
+    rg = np.zeros(max(D - 1, 1), np.int32)
+    rep = MoeGraceReplication()
+    _check("moe_grace_replicate", load().moe_grace_replicate(
+        _hp(c), len(c), _hp(g), int(D), _hp(W), _hp(hot), _hp(rg), ctypes.byref(rep)))
+    return dict(W=W.tolist(), W_mean=rep.W_mean, W_max=rep.W_max, heaviest=rep.heaviest,
+                rho=rep.rho, n_replica=rep.n_replica, hot=hot[:rep.n_hot].tolist(),
+                W_r=rep.W_r, replica_gpus=rg[:rep.n_replica].tolist(), _struct=rep)
+
+
+def moe_grace_route_table(rep: dict, gpus_per_node: int):
+    import numpy as np
+    W = _np(rep["W"], np.int64)
+    D = len(W)
+    st = rep["_struct"]
+    rg = _np(rep["replica_gpus"] or [0], np.int32)
+    n = 1 + st.n_replica
+    pred = np.zeros(n)
+    table = np.zeros((D, n))
+    _check("moe_grace_route_table", load().moe_grace_route_table(
+        _hp(W), D, ctypes.byref(st), _hp(rg), int(gpus_per_node), _hp(pred), _hp(table)))
+    return dict(instances=[st.heaviest] + list(rep["replica_gpus"]), predicted=pred, table=table)

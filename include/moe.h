@@ -252,6 +252,65 @@ int moe_layer_forward_ex(const moe_shape_t *shape, const moe_weights_t *weights,
                          int32_t *affinity,
                          void *ws, size_t ws_bytes, void *stream);
 
+/* ------------------------------------------------------------------------------------
+ * GRACE-MoE placement planner ("GRACE-MoE" notes, Core Idea 1-3).  Host code on HOST
+ * pointers: it consumes the counts and the affinity matrix moe_layer_forward produces
+ * (copied to the host by the caller) and plans where experts go for expert parallelism
+ * over D GPUs.  Plain C arrays in, plain C arrays out; the planner allocates host memory
+ * for its own scratch only, never device memory.  All calls validate their arguments and
+ * return MOE_ERR_INVALID_ARG without writing anything when they do not hold.
+ * ------------------------------------------------------------------------------------ */
+
+/* Core Idea 1: U = affinity inside groups / all affinity, over the pairs i < j of the
+ * symmetric affinity [E, E]; S = sqrt(mean over the D groups of (|C_d| - E/D)^2).
+ * group_of [E] holds group ids 0..D-1. */
+int moe_grace_metrics(const int32_t *affinity, int E, const int32_t *group_of, int D,
+                      double *U, double *S);
+
+/* Core Idea 1: spectral grouping of the E experts into D groups whose sizes stay within
+ * [ceil(E/D - delta), floor(E/D + delta)], delta = (E/D) r (r >= 0; the bounds must admit
+ * a partition).  Normalised spectral embedding (the D leading eigenvectors of
+ * Deg^-1/2 A Deg^-1/2, rows scaled to unit length) and a size-bounded k-means from
+ * farthest-point seeds.  out group_of [E].  E <= 4096 (cost O(E^3)). */
+int moe_grace_group(const int32_t *affinity, int E, int D, double r, int32_t *group_of);
+
+/* Core Idea 1: moe_grace_group at every r of the increasing grid r_grid [n_r]; out U, S
+ * [n_r] (the metrics of each grouping), *knee (the grid index where U and r scaled to
+ * [0, 1] differ most: beyond it a looser size bound buys less affinity than on average)
+ * and group_of [E] (the grouping at the knee). */
+int moe_grace_choose_r(const int32_t *affinity, int E, int D, const double *r_grid, int n_r,
+                       double *U, double *S, int *knee, int32_t *group_of);
+
+/* Core Idea 2: replication of the heaviest group's hot experts. */
+typedef struct moe_grace_replication {
+    int heaviest;        /* group (GPU) with the largest load W_max; ties -> lower id */
+    int n_replica;       /* min(max(1, floor(rho)), D - 1) */
+    int n_hot;           /* hot experts written to hot[0 .. n_hot) */
+    double rho;          /* W_max / W_mean */
+    double W_mean;
+    long long W_max;
+    long long W_r;       /* load of the hot experts */
+} moe_grace_replication_t;
+
+/* counts [E] (expert loads, e.g. moe_layer_forward's counts), group_of [E] (D >= 2 groups);
+ * out W [D] (group loads), hot [E] (the heaviest group's experts by load, descending, ties
+ * -> lower index, until their cumulative load exceeds W_max * n_replica / (1 + n_replica)),
+ * replica_gpus [D - 1] (the first n_replica written: the least-loaded other GPUs, ties ->
+ * lower id), *out. */
+int moe_grace_replicate(const int32_t *counts, int E, const int32_t *group_of, int D,
+                        long long *W, int32_t *hot, int32_t *replica_gpus,
+                        moe_grace_replication_t *out);
+
+/* Core Idea 3: instance weights of a hot expert.  Instances: [rep->heaviest] followed by
+ * replica_gpus[0 .. n_replica).  out predicted [1 + n_replica]: W_max - W_r + W_p for the
+ * original, W_i + W_p for a copy on GPU i, W_p = W_r / (1 + n_replica).  out table
+ * [D][1 + n_replica]: for a token on GPU src, the probability of each instance -- weights
+ * proportional to 1 / predicted, over the instances on src if any, else those on src's
+ * node (gpus_per_node consecutive GPU ids per node), else all instances. */
+int moe_grace_route_table(const long long *W, int D, const moe_grace_replication_t *rep,
+                          const int32_t *replica_gpus, int gpus_per_node, double *predicted,
+                          double *table);
+
 #ifdef __cplusplus
 }
 #endif

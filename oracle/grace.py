@@ -19,12 +19,13 @@ Source: the "GRACE-MoE" notes, section "Core Idea":
 
 Readings where the notes leave a step open (also listed in the design notes):
   * spectral clustering is the normalised form: the D leading eigenvectors of
-    Deg^-1/2 A Deg^-1/2 (an expert with no co-activation gets degree 1), rows scaled to
-    unit length, then a size-bounded k-means on the rows;
+    Deg^-1/2 A Deg^-1/2 (an expert with no co-activation gets degree 1 and keeps a zero
+    row), rows scaled to unit length, then a size-bounded k-means on the rows;
   * the integer size bounds are lo = ceil(ebar - delta) and hi = floor(ebar + delta);
   * k-means starts from the farthest-point seeds (first: the expert of largest degree),
-    assigns greedily in increasing distance under the upper bound, then fills groups below
-    lo with the cheapest moves from groups above lo; ties go to the lower index;
+    assigns greedily in increasing distance under the upper bound, puts each expert with
+    no co-activation into the smallest group (it carries no affinity), then fills groups
+    below lo with the cheapest moves from groups above lo; ties go to the lower index;
   * the knee is taken on U(r) over the grid of r (S(r) is reported beside it): with r and
     U scaled to [0, 1], the r where U_scaled - r_scaled is largest -- beyond it a looser
     size bound buys less affinity than on average;
@@ -77,20 +78,27 @@ def embedding(A: np.ndarray, D: int) -> np.ndarray:
     w, V = np.linalg.eigh(M)                      # ascending eigenvalues
     Y = V[:, ::-1][:, :D].copy()
     norm = np.linalg.norm(Y, axis=1)
-    norm[norm == 0] = 1.0
+    # an expert with no co-activation has a zero row (up to rounding): it stays at zero
+    Y[norm < 1e-9] = 0.0
+    norm[norm < 1e-9] = 1.0
     return Y / norm[:, None]
 
 
-def _assign(Y, C, lo, hi):
+def _assign(Y, C, lo, hi, iso):
     n, D = Y.shape[0], C.shape[0]
     d2 = ((Y[:, None, :] - C[None, :, :]) ** 2).sum(-1)          # [n, D]
-    order = sorted(((d2[i, k], i, k) for i in range(n) for k in range(D)))
+    order = sorted(((d2[i, k], i, k) for i in range(n) for k in range(D) if not iso[i]))
     g = np.full(n, -1, np.int64)
     size = np.zeros(D, np.int64)
     for _, i, k in order:
         if g[i] < 0 and size[k] < hi:
             g[i] = k
             size[k] += 1
+    # experts with no co-activation: each to the smallest group (lowest id on ties)
+    for i in np.nonzero(iso)[0]:
+        k = min((kk for kk in range(D) if size[kk] < hi), key=lambda kk: (size[kk], kk))
+        g[i] = k
+        size[k] += 1
     # groups below lo take the cheapest experts from groups above lo
     while True:
         under = [k for k in range(D) if size[k] < lo]
@@ -131,10 +139,11 @@ def group(A: np.ndarray, D: int, r: float, max_iter: int = 50) -> np.ndarray:
         seeds.append(s)
         dmin = np.minimum(dmin, ((Y - Y[s]) ** 2).sum(1))
     C = Y[seeds].copy()
-    g = _assign(Y, C, lo, hi)
+    iso = deg == 0
+    g = _assign(Y, C, lo, hi, iso)
     for _ in range(max_iter):
         C = np.stack([Y[g == k].mean(0) if np.any(g == k) else C[k] for k in range(D)])
-        g2 = _assign(Y, C, lo, hi)
+        g2 = _assign(Y, C, lo, hi, iso)
         if np.array_equal(g2, g):
             break
         g = g2
