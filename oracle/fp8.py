@@ -12,7 +12,8 @@ Readings where the page leaves a step open (also listed in the design notes):
   * the FP8 format is E4M3 (largest finite value 448, subnormal step 2^-9), rounding to
     nearest with ties to even;
   * a block's scale is a power of two: the smallest 2^k with amax <= 448 * 2^k (k = 0 for
-    an all-zero block), so that every quantised value times its scale is exact in bf16;
+    an all-zero block), k kept within [-124, 127], so that every quantised value times its
+    scale is exact in bf16 (down to its subnormals) and k fits one signed byte;
   * the activations quantised are the inputs of the two GEMMs of an expert: the token
     rows x (blocks of 128 along H) and h = silu(x W1) * (x W3) after it is rounded to bf16
     (blocks of 128 along I); the GEMMs then run on the dequantised values (q * 2^k) with
@@ -60,12 +61,16 @@ def e4m3_round(v: np.ndarray) -> np.ndarray:
     return np.where(v < 0, -r, r)
 
 
+K_MIN, K_MAX = -124, 127
+
+
 def scale_exponent(amax: float) -> int:
-    """Smallest k with amax <= 448 * 2^k (0 for amax == 0)."""
+    """Smallest k with amax <= 448 * 2^k (0 for amax == 0), kept within [-124, 127]."""
     if amax == 0:
         return 0
     m, e = np.frexp(float(amax))                  # amax = m 2^e, m in [0.5, 1)
-    return int(e - 9) if m <= 0.875 else int(e - 8)   # 448 = 0.875 * 2^9
+    k = int(e - 9) if m <= 0.875 else int(e - 8)  # 448 = 0.875 * 2^9
+    return min(max(k, K_MIN), K_MAX)
 
 
 def quantize_tile(x: np.ndarray):

@@ -38,6 +38,9 @@ def test_scale_exponent_worked_values():
     assert fp8.scale_exponent(1.75) == -8
     assert fp8.scale_exponent(1.7578125) == -7
     assert fp8.scale_exponent(0.0) == 0
+    assert fp8.scale_exponent(2.0 ** -130) == -124                  # clamped: tiny blocks
+    assert fp8.scale_exponent(2.0 ** -116) == -124
+    assert fp8.scale_exponent(2.0 ** -115) == -123
     rng = np.random.default_rng(1)
     for a in rng.uniform(1e-6, 1e4, 2000):
         k = fp8.scale_exponent(a)
