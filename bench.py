@@ -137,9 +137,10 @@ def ffn_traffic(workload: str):
 
 
 
-def algorithmic(w, n_act: int):
+def algorithmic(w, n_act: int, wbytes: int = 2):
     """Per-launch algorithmic bytes and FLOPs of each stage (what the method must move or
-    compute: the weights of the activated experts, the activations in and out)."""
+    compute: the weights of the activated experts, the activations in and out).  wbytes:
+    bytes per expert weight (2 bf16, 1 FP8; the FP8 tile scales add 1 byte per 16384)."""
     T, H, E, K, I, Is = w.T, w.H, w.E, w.K, w.I, w.Is
     TK = T * K
     b = {
@@ -148,7 +149,7 @@ def algorithmic(w, n_act: int):
         # weights of the activated experts (+ shared), token rows in, outputs out; the
         # intermediate h stays on chip or in L2 between the two projections and is not
         # counted
-        "ffn": (n_act * 3 * H * I + (3 * H * Is if Is else 0)) * 2 + (TK + T) * H * 2
+        "ffn": (n_act * 3 * H * I + (3 * H * Is if Is else 0)) * wbytes + (TK + T) * H * 2
                + TK * H * 2 + (T * H * 4 if Is else 0),
         "combine": TK * H * 2 + (T * H * 4 if Is else 0) + T * H * 4 + T * K * 8,
     }
@@ -158,20 +159,24 @@ def algorithmic(w, n_act: int):
         "ffn": 2 * (TK * 3 * H * I + T * 3 * H * Is),
         "combine": 2 * TK * H,
     }
-    layer_bytes = (n_act + (1 if Is else 0)) * 3 * H * I * 2 + E * H * 2 + T * H * 2 + T * H * 4
+    layer_bytes = ((n_act + (1 if Is else 0)) * 3 * H * I * wbytes + E * H * 2 + T * H * 2
+                   + T * H * 4)
     layer_flops = 2 * T * (K * 3 * H * I + 3 * H * Is) + 2 * T * E * H
     return b, f, layer_bytes, layer_flops
 
 
-def launches_per_step(w, with_affinity: bool) -> int:
+def launches_per_step(w, with_affinity: bool, fp8: bool = False) -> int:
     """Kernels moe_layer_forward launches: router (1 fused, or GEMM + finalise for
     T > 4096), dispatch (one bookkeeping CTA for T <= 256, else masks, scan, scatter;
     then one launch for the affinity matrix, the row gather and the zeroing of the FFN's
-    counters), the FFN (up and down projections in one persistent launch), combine."""
+    counters), the FFN (up and down projections in one persistent launch), combine.  FP8
+    experts add the token-row quantisation, split the FFN into its up and down launches
+    and quantise h (and the shared expert's h) between them."""
     T = w.T
     router = 1 if T <= 4096 else 2
     dispatch = (1 if T <= 256 else 3) + 1
-    return router + dispatch + 1 + 1
+    ffn = 1 if not fp8 else 1 + 2 + (2 if w.Is else 1)
+    return router + dispatch + ffn + 1
 
 
 # ------------------------------------------------------------------- replica helpers
@@ -213,7 +218,8 @@ def run_ours(args, rank, world, local_rank):
     X_host = torch.from_numpy(routing["X"].view(np.int16)).view(torch.bfloat16)
     X = X_host.to(dev)
     opts = ROUTINGS[args.routing]
-    layer = B.MoELayer(weights, w.T, w.K, with_affinity=True, routing=opts)
+    fp8 = args.precision == "fp8"
+    layer = B.MoELayer(weights, w.T, w.K, with_affinity=True, routing=opts, fp8=fp8)
     peaks, peak_src = load_peaks()
 
     def barrier():
@@ -290,7 +296,7 @@ def run_ours(args, rank, world, local_rank):
     rep = B.moe_grace_replicate(counts, plan["group_of"], 8)
     B.moe_grace_route_table(rep, 4)
     ms_plan = (time.perf_counter() - t_plan) * 1e3
-    b, f, layer_bytes, layer_flops = algorithmic(w, n_act)
+    b, f, layer_bytes, layer_flops = algorithmic(w, n_act, 1 if fp8 else 2)
     dom = max(("ffn", "router", "combine", "dispatch"), key=lambda s: stage_ms[s])
     t_dom = stage_ms[dom] / 1e3
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
@@ -303,7 +309,7 @@ def run_ours(args, rank, world, local_rank):
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = ffn_traffic(w.name) if dom == "ffn" else None
+    roof["traffic"] = ffn_traffic(w.name) if dom == "ffn" and not fp8 else None
     roof["kernel"] = dom
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
     roof["algorithmic_bytes_per_launch"] = int(b[dom])
@@ -314,7 +320,8 @@ def run_ours(args, rank, world, local_rank):
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8-e4m3 experts (128x128 / 1x128 block scales), bf16 activations" if fp8 else "bf16",
         "data": "synthetic (seeded; random-init weights of the DeepSeek-V3 MoE shape)",
         "config": {"workload": f"{w.name}: DeepSeek-V3-shaped MoE layer forward, T={w.T} "
                                f"tokens, H={w.H}, E={w.E}, top-{w.K}, I={w.I}, shared I={w.Is}",
@@ -326,7 +333,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(total_tokens / (ms_e2e / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(Xh.numel() * Xh.element_size()),
                 "d2h_bytes_per_step": int(Yh.numel() * Yh.element_size())},
-        "gpu_launches": K * launches_per_step(w, with_affinity=True),
+        "gpu_launches": K * launches_per_step(w, with_affinity=True, fp8=fp8),
         "roofline": roof,
         "layer_roofline": {"algorithmic_bytes": int(layer_bytes),
                            "hbm_frac": round(layer_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
@@ -341,7 +348,7 @@ def run_ours(args, rank, world, local_rank):
                        "n_hot": len(rep["hot"]), "planner_ms": round(ms_plan, 1)},
         "clocks": sampler.summary(t_wall0, t_wall1),
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
         out["cpu_baseline"] = cpu_baseline(w, routing, weights, budget_s=args.cpu_budget,
                                            opts=opts)
     return out
@@ -451,6 +458,8 @@ def main():
                     help="decode (default), tiny, sweep2..sweep256, prefill, skewed")
     ap.add_argument("--routing", choices=sorted(ROUTINGS), default="default",
                     help="routing options of other MoE families (default: the plain router)")
+    ap.add_argument("--precision", choices=("bf16", "fp8"), default="bf16",
+                    help="expert weights: bf16 (default) or FP8 E4M3 with 128x128 block scales")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()

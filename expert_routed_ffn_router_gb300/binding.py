@@ -48,6 +48,11 @@ class MoeRouting(ctypes.Structure):
                    int(group_top), int(bool(renorm)))
 
 
+class MoeWeightsFp8(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("W_gate", "bias", "W1", "W3", "W2", "S1", "S3",
+                                               "S2", "W1s", "W3s", "W2s", "S1s", "S3s", "S2s")]
+
+
 class MoeGraceReplication(ctypes.Structure):
     _fields_ = [("heaviest", ctypes.c_int32), ("n_replica", ctypes.c_int32),
                 ("n_hot", ctypes.c_int32), ("rho", ctypes.c_double), ("W_mean", ctypes.c_double),
@@ -94,6 +99,10 @@ def load(build_if_missing: bool = True):
                                P, P, P, P, Z, P], I),
         "moe_layer_forward_ex": ([ctypes.POINTER(MoeShape), ctypes.POINTER(MoeWeights),
                                   ctypes.POINTER(MoeRouting), P, P, P, P, P, P, P, Z, P], I),
+        "moe_quantize_weight_fp8": ([P, I, I, I, P, P, P], I),
+        "moe_quantize_rows_fp8": ([P, ctypes.c_longlong, I, P, P], I),
+        "moe_layer_forward_fp8": ([ctypes.POINTER(MoeShape), ctypes.POINTER(MoeWeightsFp8),
+                                   ctypes.POINTER(MoeRouting), P, P, P, P, P, P, P, Z, P], I),
         "moe_grace_metrics": ([P, I, P, I, P, P], I),
         "moe_grace_group": ([P, I, I, ctypes.c_double, P], I),
         "moe_grace_choose_r": ([P, I, I, P, I, P, P, P, P], I),
@@ -228,6 +237,51 @@ def moe_layer_forward_ex(shape: MoeShape, weights: dict, routing, X, Y, topk_idx
         ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def moe_quantize_weight_fp8(W, stream=None):
+    """W bf16 [G, R, C] or [R, C] (device) -> (E4M3 bytes uint8, same shape; int32 scale
+    exponents [G, R/128, C/128] or [R/128, C/128])."""
+    shape = W.shape
+    G, R, C = (1,) + tuple(shape) if W.dim() == 2 else tuple(shape)
+    Wq = torch.empty(shape, dtype=torch.uint8, device=W.device)
+    S = torch.empty(shape[:-2] + (R // 128, C // 128), dtype=torch.int32, device=W.device)
+    _check("moe_quantize_weight_fp8", load().moe_quantize_weight_fp8(
+        _ptr(W), G, R, C, _ptr(Wq), _ptr(S), _stream(stream)))
+    return Wq, S
+
+
+def moe_quantize_rows_fp8(x, out=None, stream=None):
+    rows, n = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    _check("moe_quantize_rows_fp8", load().moe_quantize_rows_fp8(
+        _ptr(x), rows, n, _ptr(out), _stream(stream)))
+    return out
+
+
+def quantize_expert_weights_fp8(weights: dict, stream=None) -> dict:
+    """bf16 layer weights (W_gate, bias, W1, W3, W2[, W1s, W3s, W2s]) -> the FP8 layer's
+    weights (E4M3 bytes and tile scale exponents); W_gate and bias are kept."""
+    out = {"W_gate": weights["W_gate"], "bias": weights["bias"]}
+    for w, sc in (("W1", "S1"), ("W3", "S3"), ("W2", "S2"), ("W1s", "S1s"), ("W3s", "S3s"),
+                  ("W2s", "S2s")):
+        if weights.get(w) is None:
+            out[w] = out[sc] = None
+            continue
+        out[w], out[sc] = moe_quantize_weight_fp8(weights[w], stream)
+    return out
+
+
+def moe_layer_forward_fp8(shape: MoeShape, weights8: dict, routing, X, Y, topk_idx, topk_w,
+                          counts, affinity, ws, stream=None):
+    w = MoeWeightsFp8(*[None if weights8.get(n) is None else weights8[n].data_ptr()
+                        for n in ("W_gate", "bias", "W1", "W3", "W2", "S1", "S3", "S2", "W1s",
+                                  "W3s", "W2s", "S1s", "S3s", "S2s")])
+    _check("moe_layer_forward_fp8", load().moe_layer_forward_fp8(
+        ctypes.byref(shape), ctypes.byref(w), _routing(routing), _ptr(X), _ptr(Y),
+        _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(affinity), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
 # ------------------------------------------------------------------- convenience wrapper
 class MoELayer:
     """Holds a layer's weights, outputs and workspace (torch allocations) and runs
@@ -235,9 +289,11 @@ class MoELayer:
     (optionally) W1s, W3s, W2s."""
 
     def __init__(self, weights: dict, T: int, K: int, with_affinity: bool = True,
-                 routing=None):
+                 routing=None, fp8: bool = False):
         self.w = weights
         self.routing = routing
+        # FP8 experts: the weights are quantised once here (static, 128 x 128 tiles)
+        self.w8 = quantize_expert_weights_fp8(weights) if fp8 else None
         E, H = weights["W_gate"].shape
         I = weights["W1"].shape[-1]
         Is = 0 if weights.get("W1s") is None else weights["W1s"].shape[-1]
@@ -255,7 +311,10 @@ class MoELayer:
         self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
 
     def forward(self, X, stream=None):
-        if self.routing is None:
+        if self.w8 is not None:
+            moe_layer_forward_fp8(self.shape, self.w8, self.routing, X, self.Y, self.topk_idx,
+                                  self.topk_w, self.counts, self.affinity, self.ws, stream)
+        elif self.routing is None:
             moe_layer_forward(self.shape, self.w, X, self.Y, self.topk_idx, self.topk_w,
                               self.counts, self.affinity, self.ws, stream)
         else:

@@ -150,7 +150,7 @@ struct LayerLayout {
     RouterLayout r;
     DispatchLayout d;
     int32_t *offsets, *perm, *slot_pos;
-    void *Xp, *h, *Yp, *hs;
+    void *Xp, *h, *Yp, *hs, *Xq;
     float *Ysh;
     unsigned *ready;
     size_t bytes;
@@ -170,6 +170,7 @@ LayerLayout layer_layout(const moe_shape_t &s, unsigned char *ws)
     L.h = take(TK * s.I * 2);
     L.Yp = take(TK * s.H * 2);
     L.hs = take(static_cast<size_t>(s.T) * s.I_shared * 2);
+    L.Xq = take(static_cast<size_t>(s.T) * s.H * 2);   // FP8 weights: quantised token rows
     L.Ysh = reinterpret_cast<float *>(take(s.I_shared > 0 ? static_cast<size_t>(s.T) * s.H * 4 : 0));
     L.ready = reinterpret_cast<unsigned *>(
         take(ffn_ready_slots(static_cast<long long>(TK) + s.T, s.E + 1) * sizeof(unsigned)));
@@ -185,6 +186,114 @@ int check_shape(const moe_shape_t *s)
     if (s->I <= 0 || s->I_shared < 0) return MOE_ERR_INVALID_ARG;
     if (s->I % 64 != 0 || s->I_shared % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
     return MOE_OK;
+}
+
+// The layer on bf16 expert weights (wt) or FP8 ones (w8: E4M3 with 128 x 128 power-of-two
+// block scales; the token rows and h are then quantised on the fly in vectors of 128).
+int layer_forward(const moe_shape_t *shape, const moe_weights_t *wt, const moe_weights_fp8_t *w8,
+                  const moe_routing_t *routing, const void *X, float *Y, int32_t *topk_idx,
+                  float *topk_w, int32_t *counts, int32_t *affinity, void *ws, size_t ws_bytes,
+                  void *stream)
+{
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    const moe_shape_t s = *shape;
+    RoutingOpts ro;
+    if ((rc = check_routing(routing, s.E, s.K, ro))) return rc;
+    const bool fp8 = w8 != nullptr;
+    const void *W_gate = fp8 ? w8->W_gate : wt->W_gate;
+    const float *bias = fp8 ? w8->bias : static_cast<const float *>(wt->bias);
+    const void *W1 = fp8 ? w8->W1 : wt->W1, *W3 = fp8 ? w8->W3 : wt->W3, *W2 = fp8 ? w8->W2 : wt->W2;
+    const void *W1s = fp8 ? w8->W1s : wt->W1s, *W3s = fp8 ? w8->W3s : wt->W3s,
+               *W2s = fp8 ? w8->W2s : wt->W2s;
+    if ((rc = check_ptrs({X, Y, topk_idx, topk_w, counts, W_gate, bias, W1, W3, W2}))) return rc;
+    if (s.I_shared > 0 && (rc = check_ptrs({W1s, W3s, W2s}))) return rc;
+    if (fp8) {
+        if (s.H % 128 || s.I % 128 || s.I_shared % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+        if (s.H > 16384 || s.I > 16384 || s.I_shared > 16384) return MOE_ERR_UNSUPPORTED_SHAPE;
+        if (!w8->S1 || !w8->S3 || !w8->S2) return MOE_ERR_INVALID_ARG;
+        if (s.I_shared > 0 && (!w8->S1s || !w8->S3s || !w8->S2s)) return MOE_ERR_INVALID_ARG;
+    }
+    if ((rc = check_opt(affinity))) return rc;
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    const LayerLayout L = layer_layout(s, w);
+    if ((rc = check_ws(ws, ws_bytes, L.bytes))) return rc;
+    if (s.T == 0) return MOE_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int *status = static_cast<int *>(ws);
+
+    record_stage(0, st);
+    cudaError_t e = launch_router(X, W_gate, bias, s.T, s.H, s.E, s.K, topk_idx, topk_w,
+                                  L.r.plan, L.r.scr, status, st, &ro);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    record_stage(1, st);
+    // FP8: the expert FFNs read the token rows quantised in vectors of 128 along H
+    const void *Xin = X;
+    if (fp8) {
+        if ((e = launch_quant_rows(X, s.T, s.H, L.Xq, st)) != cudaSuccess) return MOE_ERR_CUDA;
+        Xin = L.Xq;
+    }
+    // the dispatch tail also zeroes the FFN's readiness counters
+    const size_t n_ready = ffn_ready_slots(static_cast<long long>(s.T) * s.K + s.T, s.E + 1);
+    e = launch_dispatch(Xin, topk_idx, s.T, s.H, s.E, s.K, counts, L.offsets, L.perm, L.slot_pos,
+                        L.Xp, affinity, L.d.plan, L.d.scr, L.ready, n_ready, status, st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    record_stage(2, st);
+
+    FfnProblem P[2]{};
+    int Ipp[2] = {s.I, s.I_shared};
+    P[0].act = L.Xp;
+    P[0].offsets = L.offsets;
+    P[0].n_groups = s.E;
+    P[0].rows = s.T * s.K;
+    P[0].W1 = W1; P[0].W3 = W3; P[0].W2 = W2;
+    P[0].h = L.h;
+    P[0].out = L.Yp;
+    P[0].out_fp32 = 0;
+    if (fp8) {
+        P[0].fp8 = 1;
+        P[0].S1 = w8->S1; P[0].S3 = w8->S3; P[0].S2 = w8->S2;
+    }
+    int n_probs = 1;
+    if (s.I_shared > 0) {
+        P[1].act = Xin;
+        P[1].offsets = nullptr;
+        P[1].n_groups = 1;
+        P[1].rows = s.T;
+        P[1].dense_rows = s.T;
+        P[1].W1 = W1s; P[1].W3 = W3s; P[1].W2 = W2s;
+        P[1].h = L.hs;
+        P[1].out = L.Ysh;
+        P[1].out_fp32 = 1;
+        if (fp8) {
+            P[1].fp8 = 1;
+            P[1].S1 = w8->S1s; P[1].S3 = w8->S3s; P[1].S2 = w8->S2s;
+        }
+        n_probs = 2;
+    }
+    long long hint = static_cast<long long>(s.T) * s.K / s.E;
+    if (hint < 1) hint = 1;
+    if (!fp8) {
+        e = launch_ffn(P, n_probs, s.H, Ipp, static_cast<int>(hint), L.ready, true, status, st,
+                       g_wait_limit_ns, g_inject_stall, g_stage_events_on ? g_stage_events[3] : nullptr);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    } else {
+        // up projections, h quantised in vectors of 128 along I, then the down projections
+        e = launch_ffn(P, n_probs, s.H, Ipp, static_cast<int>(hint), L.ready, true, status, st,
+                       g_wait_limit_ns, g_inject_stall, nullptr, 0);
+        if (e == cudaSuccess) e = launch_quant_rows(L.h, static_cast<long long>(s.T) * s.K, s.I, L.h, st);
+        if (e == cudaSuccess && s.I_shared > 0) e = launch_quant_rows(L.hs, s.T, s.I_shared, L.hs, st);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        record_stage(3, st);
+        e = launch_ffn(P, n_probs, s.H, Ipp, static_cast<int>(hint), L.ready, true, status, st,
+                       g_wait_limit_ns, g_inject_stall, nullptr, 1);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    record_stage(4, st);
+    e = launch_combine(L.Yp, L.slot_pos, topk_w, s.I_shared > 0 ? L.Ysh : nullptr, s.T, s.H,
+                       s.K, Y, st);
+    record_stage(5, st);
+    return cuda_status(e);
 }
 
 }  // namespace
@@ -349,69 +458,42 @@ int moe_layer_forward_ex(const moe_shape_t *shape, const moe_weights_t *wt,
                          int32_t *topk_idx, float *topk_w, int32_t *counts, int32_t *affinity,
                          void *ws, size_t ws_bytes, void *stream)
 {
-    int rc = check_shape(shape);
-    if (rc) return rc;
-    RoutingOpts ro;
-    if ((rc = check_routing(routing, shape->E, shape->K, ro))) return rc;
     if (!wt) return MOE_ERR_INVALID_ARG;
-    const moe_shape_t s = *shape;
-    if ((rc = check_ptrs({X, Y, topk_idx, topk_w, counts, wt->W_gate, wt->bias, wt->W1, wt->W3,
-                          wt->W2})))
-        return rc;
-    if (s.I_shared > 0 && (rc = check_ptrs({wt->W1s, wt->W3s, wt->W2s}))) return rc;
-    if ((rc = check_opt(affinity))) return rc;
-    unsigned char *w = static_cast<unsigned char *>(ws);
-    const LayerLayout L = layer_layout(s, w);
-    if ((rc = check_ws(ws, ws_bytes, L.bytes))) return rc;
-    if (s.T == 0) return MOE_OK;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    int *status = static_cast<int *>(ws);
+    return layer_forward(shape, wt, nullptr, routing, X, Y, topk_idx, topk_w, counts, affinity,
+                         ws, ws_bytes, stream);
+}
 
-    record_stage(0, st);
-    cudaError_t e = launch_router(X, wt->W_gate, wt->bias, s.T, s.H, s.E, s.K, topk_idx, topk_w,
-                                  L.r.plan, L.r.scr, status, st, &ro);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    record_stage(1, st);
-    // the dispatch tail also zeroes the FFN's readiness counters
-    const size_t n_ready = ffn_ready_slots(static_cast<long long>(s.T) * s.K + s.T, s.E + 1);
-    e = launch_dispatch(X, topk_idx, s.T, s.H, s.E, s.K, counts, L.offsets, L.perm, L.slot_pos,
-                        L.Xp, affinity, L.d.plan, L.d.scr, L.ready, n_ready, status, st);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    record_stage(2, st);
+int moe_layer_forward_fp8(const moe_shape_t *shape, const moe_weights_fp8_t *w8,
+                          const moe_routing_t *routing, const void *X, float *Y,
+                          int32_t *topk_idx, float *topk_w, int32_t *counts, int32_t *affinity,
+                          void *ws, size_t ws_bytes, void *stream)
+{
+    if (!w8) return MOE_ERR_INVALID_ARG;
+    return layer_forward(shape, nullptr, w8, routing, X, Y, topk_idx, topk_w, counts, affinity,
+                         ws, ws_bytes, stream);
+}
 
-    FfnProblem P[2]{};
-    int Ipp[2] = {s.I, s.I_shared};
-    P[0].act = L.Xp;
-    P[0].offsets = L.offsets;
-    P[0].n_groups = s.E;
-    P[0].rows = s.T * s.K;
-    P[0].W1 = wt->W1; P[0].W3 = wt->W3; P[0].W2 = wt->W2;
-    P[0].h = L.h;
-    P[0].out = L.Yp;
-    P[0].out_fp32 = 0;
-    int n_probs = 1;
-    if (s.I_shared > 0) {
-        P[1].act = X;
-        P[1].offsets = nullptr;
-        P[1].n_groups = 1;
-        P[1].rows = s.T;
-        P[1].dense_rows = s.T;
-        P[1].W1 = wt->W1s; P[1].W3 = wt->W3s; P[1].W2 = wt->W2s;
-        P[1].h = L.hs;
-        P[1].out = L.Ysh;
-        P[1].out_fp32 = 1;
-        n_probs = 2;
-    }
-    long long hint = static_cast<long long>(s.T) * s.K / s.E;
-    if (hint < 1) hint = 1;
-    e = launch_ffn(P, n_probs, s.H, Ipp, static_cast<int>(hint), L.ready, true, status, st, g_wait_limit_ns,
-                   g_inject_stall, g_stage_events_on ? g_stage_events[3] : nullptr);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    record_stage(4, st);
-    e = launch_combine(L.Yp, L.slot_pos, topk_w, s.I_shared > 0 ? L.Ysh : nullptr, s.T, s.H,
-                       s.K, Y, st);
-    record_stage(5, st);
-    return cuda_status(e);
+int moe_quantize_weight_fp8(const void *W, int G, int R, int C, void *Wq, int32_t *S,
+                            void *stream)
+{
+    if (G < 0 || R <= 0 || C <= 0) return MOE_ERR_INVALID_ARG;
+    if (R % 128 || C % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    int rc = check_ptrs({W, Wq});
+    if (rc) return rc;
+    if (!S) return MOE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(S) % 4) return MOE_ERR_MISALIGNED;
+    if (G == 0) return MOE_OK;
+    return cuda_status(launch_quant_weight(W, G, R, C, Wq, S, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_quantize_rows_fp8(const void *in, long long rows, int n, void *out, void *stream)
+{
+    if (rows < 0 || n <= 0) return MOE_ERR_INVALID_ARG;
+    if (n % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    int rc = check_ptrs({in, out});
+    if (rc) return rc;
+    if (rows == 0) return MOE_OK;
+    return cuda_status(launch_quant_rows(in, rows, n, out, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

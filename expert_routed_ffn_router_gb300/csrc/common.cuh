@@ -25,6 +25,79 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f)
     return static_cast<uint16_t>(u >> 16);
 }
 
+// ------------------------------------------------------------------------------- fp8
+// E4M3 block quantisation with power-of-two scales 2^k: k is the smallest integer with
+// amax <= 448 * 2^k, kept within [-124, 127] so that every dequantised value q * 2^k is
+// exact in bf16 (and k fits an int8).
+constexpr int kFp8MinExp = -124;
+constexpr int kFp8MaxExp = 127;
+
+__device__ __forceinline__ int fp8_scale_exp(float amax)
+{
+    if (!(amax > 0.f)) return 0;
+    int e;
+    const float m = frexpf(amax, &e);      // amax = m 2^e, m in [0.5, 1); 448 = 0.875 * 2^9
+    const int k = m <= 0.875f ? e - 9 : e - 8;
+    return k < kFp8MinExp ? kFp8MinExp : (k > kFp8MaxExp ? kFp8MaxExp : k);
+}
+
+// 2^e as an fp32 (e in [-149, 127]; subnormal below -126): multiplying by it is exact
+// whenever the product is representable.
+__device__ __forceinline__ float pow2f(int e)
+{
+    return e >= -126 ? __int_as_float((e + 127) << 23) : __int_as_float(1 << (e + 149));
+}
+
+// Two fp32 values -> two E4M3 bytes (round to nearest even, saturating), hi in the upper byte.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float hi, float lo)
+{
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Two E4M3 bytes (upper byte -> .y) -> two exact fp32 values.
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t v)
+{
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+    uint16_t lo, hi;
+    asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(h2));
+    float a, b;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(a) : "h"(lo));
+    asm("cvt.f32.f16 %0, %1;" : "=f"(b) : "h"(hi));
+    return make_float2(a, b);
+}
+
+// Four E4M3 bytes (byte i = element i) -> two bf16x2 words of the elements times 2^-120:
+// each byte's sign, exponent and mantissa bits move into bf16's sign bit, the low four
+// bits of its exponent field and the top three mantissa bits, so E4M3's exponent bias 7
+// becomes bf16's 127 and E4M3 subnormals become bf16 subnormals -- exactly 2^-120 times the
+// value in both cases.
+__device__ __forceinline__ void e4m3x4_to_bf16x2_shifted(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    const uint32_t d0 = __byte_perm(w, 0u, 0x1404u);   // b1 << 24 | b0 << 8
+    const uint32_t d1 = __byte_perm(w, 0u, 0x3424u);   // b3 << 24 | b2 << 8
+    lo = (d0 & 0x80008000u) | ((d0 >> 4) & 0x07F007F0u);
+    hi = (d1 & 0x80008000u) | ((d1 >> 4) & 0x07F007F0u);
+}
+
+// Packed bf16x2 product (round to nearest even).
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Two fp32 values -> packed bf16x2 (round to nearest even; exact for dequantised values).
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float hi, float lo)
+{
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
 // ------------------------------------------------------------------------ status word
 // The first int of every workspace records device-side conditions (bounded waits that ran
 // out, indices out of range).  The first error wins.

@@ -56,7 +56,14 @@ constexpr int BM = 128;                   // MMA M (weight rows)
 constexpr int BK = 64;                    // K per stage = one 128-byte swizzle row of bf16
 constexpr int A_BYTES = BM * BK * 2;      // 16 KB: two 64x64 boxes
 constexpr int HALF_A = A_BYTES / 2;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 192;          // producer, MMA, 4 epilogue warps
+constexpr int CONV_WARPS = 8;             // warps that dequantise the FP8 weight tiles
+constexpr int NUM_THREADS_FP8 = NUM_THREADS + 32 * CONV_WARPS;
+constexpr int A8_BYTES = BM * BK;          // 8 KB: the stage's weight tile as E4M3 bytes
+constexpr int FP8_END = 1 << 20;          // scale slot value that tells the converters to stop
+constexpr int FP8_SB = 3;                 // FP8: slots of dequantised weight tiles
+constexpr int TSC = 128;                  // FP8: scale-table entries per box (H, I <= 16384)
+constexpr int MAX_STAGES_FP8 = 24;        // FP8: the E4M3 ring is deeper (its stages are small)
 constexpr int MAX_GROUPS = 1024;          // groups of one problem
 constexpr int MAX_CG = 1040;              // groups of all problems of a launch
 constexpr int CW = 32;                    // epilogue chunk: accumulator columns per TMEM load
@@ -76,6 +83,9 @@ struct ProbDev {
     int out_fp32;
     void *h;                 // bf16 [rows, I]
     void *out;               // [rows, H] bf16 or fp32
+    // FP8 weights: scale exponents per 128 x 128 tile, [groups][H/128][I/128] for W1 and W3,
+    // [groups][I/128][H/128] for W2
+    const int32_t *s1, *s3, *s2;
 };
 
 struct FfnArgs {
@@ -95,6 +105,7 @@ struct FfnArgs {
     int *status;
     unsigned long long timeout_ns;
     int inject;              // 1: the producer never fills a stage (bounded-wait test)
+    int phase_only;          // -1: up and down tiles; 0: only up tiles; 1: only down tiles
 };
 
 struct Tile {
@@ -138,18 +149,31 @@ __device__ __forceinline__ void fence_proxy_async_global()
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-template <bool PAIR>
-__global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_constant__ FfnArgs p)
+// generic-proxy shared-memory stores -> later async-proxy (tensor core) reads
+__device__ __forceinline__ void fence_proxy_async_shared()
 {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <bool PAIR, bool FP8>
+__global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
+    ffn_kernel(const __grid_constant__ FfnArgs p)
+{
+    constexpr int NT = FP8 ? NUM_THREADS_FP8 : NUM_THREADS;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
     const int bn = p.bn, S = p.stages, tab = p.tab;
     const int bn_cta = PAIR ? bn / 2 : bn;    // token rows of B staged in this CTA
-    const int stage_bytes = A_BYTES + bn_cta * 128;
+    // stage: weight tile (bf16, SW128) | token rows.  With FP8 weights the ring's stages hold
+    // token rows | E4M3 weight bytes, and the dequantised weight tiles have a ring of their
+    // own (FP8_SB slots), so the E4M3 ring can be deep enough to keep HBM busy
+    const int stage_bytes = FP8 ? bn_cta * 128 + A8_BYTES : A_BYTES + bn_cta * 128;
+    const int b_off = FP8 ? 0 : A_BYTES;                      // token rows within a stage
     unsigned char *stage_base = smem;
-    float *xbuf = reinterpret_cast<float *>(smem + static_cast<size_t>(S) * stage_bytes);
+    unsigned char *abf_base = smem + static_cast<size_t>(S) * stage_bytes;   // FP8 only
+    float *xbuf = reinterpret_cast<float *>(abf_base + (FP8 ? FP8_SB * A_BYTES : 0));
     uint64_t *full = reinterpret_cast<uint64_t *>(xbuf + XCHG_FLOATS);
     uint64_t *empty = full + S;
     uint64_t *tfull = empty + S;
@@ -157,7 +181,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
     uint64_t *drain = tempty + 2;
     uint64_t *tqf = drain + 1;                                // [TQ] tile slot written
     uint64_t *tqe = tqf + TQ;                                 // [TQ] tile slot read by all roles
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tqe + TQ);
+    uint64_t *cvt = tqe + TQ;                                 // [FP8_SB] FP8: slot dequantised
+    uint64_t *cempty = cvt + (FP8 ? FP8_SB : 0);              // [FP8_SB] FP8: slot consumed
+    int *sc8 = reinterpret_cast<int *>(cempty + (FP8 ? FP8_SB : 0));   // [S][2] box scale exponents
+    int *tsc = sc8 + (FP8 ? 2 * S : 0);                       // [2][TSC] FP8: the tile's scales
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tsc + (FP8 ? 2 * TSC : 0));
     static_assert(BK == 64, "the MMA issuer unrolls four K16 steps per stage");
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     // groups of all problems, problem 0's first: first row, rows, the tile order, the tile
@@ -195,6 +223,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
             // and epilogue, which read their copy of the slot)
             mbar_init(&tqe[q], PAIR ? 4 : 2);
         }
+        if (FP8)
+            for (int q = 0; q < FP8_SB; ++q) {
+                mbar_init(&cvt[q], PAIR ? 2 * CONV_WARPS : CONV_WARPS);
+                mbar_init(&cempty[q], 1);
+            }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -225,7 +258,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
     for (int pi = 0; pi < p.n_probs; ++pi) {
         const ProbDev &P = p.prob[pi];
         const int base = pi ? n0 : 0;
-        for (int g = tid; g < P.n_groups; g += NUM_THREADS) {
+        for (int g = tid; g < P.n_groups; g += NT) {
             const int a = P.offsets ? P.offsets[g] : 0;
             const int b = P.offsets ? P.offsets[g + 1] : P.dense_rows;
             gstart[base + g] = a;
@@ -314,6 +347,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
     const int n_heavy_groups = *n_heavy_s;
     const int n_up = gpre_up[n_used], n_dn = gpre_dn[n_used];
     const int n_tiles = n_up + n_dn;                         // up tiles, then down tiles
+    // a launch may take only one phase: [t_begin, t_end) of the list
+    const int t_begin = p.phase_only == 1 ? n_up : 0;
+    const int t_end = p.phase_only == 0 ? n_up : n_tiles;
     const int heavy_up = gpre_up[n_heavy_groups], heavy_dn = gpre_dn[n_heavy_groups];
     const int light_up = n_up - heavy_up, light_dn = n_dn - heavy_dn;
     // Position t of a phase's interleaved order (N tiles, NL light) is a light tile when
@@ -395,8 +431,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
             // claim the next tile of the list and publish it to every role (and to the odd CTA)
             auto claim = [&](Tile &T) -> bool {
                 if (!mbar_wait(&tqe[qs], qph ^ 1u, abort_flag, p.status, tmo)) return false;
-                const int t = static_cast<int>(atomicAdd(p.next_tile, 1u));
-                if (t < n_tiles) {
+                const int t = t_begin + static_cast<int>(atomicAdd(p.next_tile, 1u));
+                if (t < t_end) {
                     T = decode_at(t);
                 } else {
                     T = Tile{};
@@ -456,6 +492,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
                 const int a1 = up ? mt * 64 : mt * 128 + 64;
                 const int brow = T.row0 + (PAIR && !leader ? n_mma_of(T) / 2 : 0);
                 const int kblocks = up ? P.kb_up : P.kb_dn;
+                // FP8: scale exponents of the two weight boxes of stage kb (a box past the
+                // last weight column reads zeros: any tile's scale does, so its index is
+                // clamped to the last tile of the row)
+                // The tile's scales (one per 128 K rows and box) are copied into a shared
+                // table when the tile starts (asynchronous 4-byte copies, all in flight
+                // together), so the per-stage loop reads them from shared memory.
+                if (FP8) {
+                    const int nkq = (kblocks * BK + 127) / 128;
+                    const int nc = (up ? P.I : P.H) / 128;
+                    const int nr = (up ? P.H : P.I) / 128;
+                    for (int box = 0; box < 2; ++box) {
+                        const int c = min((box ? a1 : a0) / 128, nc - 1);
+                        const int32_t *src = (up ? (box ? P.s3 : P.s1) : P.s2) +
+                                             static_cast<size_t>(T.g) * nr * nc + c;
+                        for (int q = 0; q < nkq; ++q)
+                            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;"
+                                         ::"r"(smem_u32(tsc + box * TSC + q)),
+                                           "l"(reinterpret_cast<uint64_t>(src + static_cast<size_t>(q) * nc))
+                                         : "memory");
+                    }
+                    asm volatile("cp.async.commit_group;" ::: "memory");
+                    asm volatile("cp.async.wait_group 0;" ::: "memory");
+                }
                 if (!up) {
                     // the h rows of this token tile are complete once every up-projection
                     // weight tile of it has been stored (each CTA of a pair stores half)
@@ -479,7 +538,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
                 }
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, tmo)) { ok = false; break; }
-                    if (!PAIR) {
+                    if (FP8) {
+                        // E4M3 weight boxes into the stage's byte area, token rows as usual;
+                        // each CTA's copies complete on its own barrier, where its converter
+                        // warps wait (they then tell the MMA issuer)
+                        sc8[2 * s] = tsc[(kb * BK) / 128];
+                        sc8[2 * s + 1] = tsc[TSC + (kb * BK) / 128];
+                        unsigned char *a8 = a + bn_cta * 128;
+                        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(A8_BYTES + bn_cta * 128));
+                        tma_load_3d(a8, mA, &full[s], a0, kb * BK, T.g);
+                        tma_load_3d(a8 + A8_BYTES / 2, mA2, &full[s], a1, kb * BK, T.g);
+                        tma_load_2d(a, mB, &full[s], kb * BK, brow);
+                    } else if (!PAIR) {
                         mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(stage_bytes));
                         tma_load_3d(a, mA, &full[s], a0, kb * BK, T.g);
                         tma_load_3d(a + HALF_A, mA2, &full[s], a1, kb * BK, T.g);
@@ -498,12 +568,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
             }
             // every copy issued lands before the CTA can exit (a no-op wait in normal runs:
             // the MMA warp has already waited on each of these phases).  In a pair the
-            // even CTA's barriers count the copies of both CTAs.
-            if (!PAIR || leader) {
+            // even CTA's barriers count the copies of both CTAs (with FP8 weights each CTA's
+            // count its own).
+            if (!PAIR || leader || FP8) {
                 const uint32_t n = it < static_cast<uint32_t>(S) ? it : static_cast<uint32_t>(S);
                 for (uint32_t j = it - n; j < it; ++j) {
                     int dummy_abort = 0;
                     mbar_wait(&full[j % S], (j / S) & 1u, &dummy_abort, nullptr, 20000000ull);
+                }
+            }
+            if (FP8 && ok) {
+                // the converter warps stop at a stage whose scale slot says so (after the
+                // drain above: this arrival moves the stage's barrier one phase on)
+                if (mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, tmo)) {
+                    sc8[2 * s] = FP8_END;
+                    mbar_arrive(&full[s]);
                 }
             }
         }
@@ -514,10 +593,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
             // lasts only ~512 tensor-core cycles, and a longer dependent chain here (index
             // division, descriptor packing) leaves the tensor pipe idle between stages.
             const uint32_t ring0 = smem_u32(stage_base);
-            const uint64_t adesc0 = smem_desc_sw128(ring0, HALF_A, 1024);
-            const uint64_t bdesc0 = smem_desc_sw128(ring0 + A_BYTES, 16, 1024);
+            const uint64_t adesc0 = smem_desc_sw128(FP8 ? smem_u32(abf_base) : ring0, HALF_A, 1024);
+            const uint64_t bdesc0 = smem_desc_sw128(ring0 + b_off, 16, 1024);
             const uint32_t stage16 = static_cast<uint32_t>(stage_bytes) >> 4;  // descriptor units
             uint32_t s = 0, ph = 0, soff = 0, tc = 0;
+            uint32_t sb = 0, pb = 0, aoff = 0;          // FP8: slot of the dequantised tile
             bool ok = true;
             uint32_t qs = 0, qph = 0;
             for (;; ++tc) {
@@ -535,9 +615,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
                 const uint32_t d_tmem = tmem_base + b * static_cast<uint32_t>(bn);
                 const int kblocks = T.ph == PH_UP ? P.kb_up : P.kb_dn;
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    if (!mbar_wait(&full[s], ph, abort_flag, p.status, tmo)) { ok = false; break; }
+                    // FP8: the stage is ready once every converter warp (of both CTAs of a
+                    // pair) has written its dequantised weight tile (after the stage's copies)
+                    const bool got = !FP8 ? mbar_wait(&full[s], ph, abort_flag, p.status, tmo)
+                                     : PAIR ? mbar_wait_cluster(&cvt[sb], pb, abort_flag, p.status, tmo)
+                                            : mbar_wait(&cvt[sb], pb, abort_flag, p.status, tmo);
+                    if (!got) { ok = false; break; }
                     tc_fence_after();
-                    const uint64_t ad = adesc0 + soff, bd = bdesc0 + soff;
+                    const uint64_t ad = adesc0 + (FP8 ? aoff : soff), bd = bdesc0 + soff;
                     // K16 steps: +2048 B along A (MN-major), +32 B along B (K-major)
                     if (PAIR) {
                         tc_mma_bf16_pair(d_tmem, ad, bd, idesc, kb != 0 ? 1u : 0u);
@@ -545,14 +630,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
                         tc_mma_bf16_pair(d_tmem, ad + 256, bd + 4, idesc, 1u);
                         tc_mma_bf16_pair(d_tmem, ad + 384, bd + 6, idesc, 1u);
                         tc_commit_pair_mc(&empty[s], 3);
+                        if (FP8) tc_commit_pair_mc(&cempty[sb], 3);
                     } else {
                         tc_mma_bf16(d_tmem, ad, bd, idesc, kb != 0 ? 1u : 0u);
                         tc_mma_bf16(d_tmem, ad + 128, bd + 2, idesc, 1u);
                         tc_mma_bf16(d_tmem, ad + 256, bd + 4, idesc, 1u);
                         tc_mma_bf16(d_tmem, ad + 384, bd + 6, idesc, 1u);
                         tc_commit(&empty[s]);
+                        if (FP8) tc_commit(&cempty[sb]);
                     }
                     if (++s == static_cast<uint32_t>(S)) { s = 0; ph ^= 1u; soff = 0; } else { soff += stage16; }
+                    if (FP8) {
+                        if (++sb == static_cast<uint32_t>(FP8_SB)) { sb = 0; pb ^= 1u; aoff = 0; }
+                        else { aoff += static_cast<uint32_t>(A_BYTES) >> 4; }
+                    }
                 }
                 if (!ok) break;
                 if (PAIR) tc_commit_pair_mc(&tfull[b], 3); else tc_commit(&tfull[b]);
@@ -561,6 +652,80 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ffn_kernel(const __grid_consta
             if (PAIR) tc_commit_pair_mc(drain, 1); else tc_commit(drain);
             int dummy_abort = 0;
             mbar_wait(drain, 0, &dummy_abort, nullptr, 20000000ull);
+        }
+    } else if (FP8 && warp >= 6) {
+        // ------------------------------------------------------- FP8 weight converters
+        // Each stage's two E4M3 boxes (64 K rows x 64 weight columns, 64-byte rows) become
+        // the bf16 weight tile in the swizzled layout TMA gives bf16 boxes (128-byte rows,
+        // 16-byte chunk c of row r at chunk c ^ (r & 7)), times the box's scale 2^k (exact).
+        // 16-byte chunks of E4M3 spread over the converter threads; then a proxy fence so
+        // the tensor core sees the generic stores, and one arrival per warp.
+        const int ct = tid - NUM_THREADS;
+        const uint32_t cvt_c0 = PAIR ? mapa_shared(smem_u32(cvt), 0) : 0u;   // even CTA's cvt[0]
+        uint32_t s = 0, ph = 0, sb = 0, pb = 0;
+        for (;;) {
+            if (!mbar_wait(&full[s], ph, abort_flag, p.status, tmo)) break;
+            const int k0 = sc8[2 * s], k1 = sc8[2 * s + 1];
+            if (k0 == FP8_END) break;
+            if (!mbar_wait(&cempty[sb], pb ^ 1u, abort_flag, p.status, tmo)) break;
+            const uint32_t abf = smem_u32(abf_base) + sb * static_cast<uint32_t>(A_BYTES);
+            const uint32_t a8 = smem_u32(stage_base) + s * static_cast<uint32_t>(stage_bytes) +
+                                static_cast<uint32_t>(bn_cta) * 128u;
+            // every chunk's bytes first (independent shared loads), then the conversions
+            constexpr int NCH = 16 / CONV_WARPS;
+            uint32_t w[NCH][4];
+#pragma unroll
+            for (int j = 0; j < NCH; ++j) {
+                const uint32_t addr = a8 + 16u * static_cast<uint32_t>(ct + 32 * CONV_WARPS * j);
+                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(w[j][0]), "=r"(w[j][1]), "=r"(w[j][2]), "=r"(w[j][3]) : "r"(addr));
+            }
+            // bit moves (x 2^-120) then one packed multiply by 2^(120 + k): a power of two,
+            // so exact, and the results are normal bf16 for -117 <= k <= 7; other scales go
+            // through fp32 (exact power-of-two products)
+            const bool fast = k0 >= -117 && k0 <= 7 && k1 >= -117 && k1 <= 7;
+            const uint32_t e0 = static_cast<uint32_t>(247 + k0) << 7, e1 = static_cast<uint32_t>(247 + k1) << 7;
+            const uint32_t sc_a = e0 | (e0 << 16), sc_b = e1 | (e1 << 16);
+#pragma unroll
+            for (int j = 0; j < NCH; ++j) {
+                const int chunk = ct + 32 * CONV_WARPS * j;   // 0..511 over the two 4 KB boxes
+                const int box = chunk >> 8, r = (chunk >> 2) & 63, cq = chunk & 3;
+                uint32_t o[8];
+                if (fast) {
+                    const uint32_t sc2 = box ? sc_b : sc_a;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t x, y;
+                        e4m3x4_to_bf16x2_shifted(w[j][i], x, y);
+                        o[2 * i] = bf16x2_mul(x, sc2);
+                        o[2 * i + 1] = bf16x2_mul(y, sc2);
+                    }
+                } else {
+                    const float sc = pow2f(box ? k1 : k0);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 f0 = e4m3x2_to_f32x2(static_cast<uint16_t>(w[j][i] & 0xffffu));
+                        const float2 f1 = e4m3x2_to_f32x2(static_cast<uint16_t>(w[j][i] >> 16));
+                        o[2 * i] = f32x2_to_bf16x2(f0.y * sc, f0.x * sc);
+                        o[2 * i + 1] = f32x2_to_bf16x2(f1.y * sc, f1.x * sc);
+                    }
+                }
+                const uint32_t row = abf + static_cast<uint32_t>(box * HALF_A + r * 128);
+                const uint32_t d0 = row + ((static_cast<uint32_t>(2 * cq) ^ static_cast<uint32_t>(r & 7)) << 4);
+                const uint32_t d1 = row + ((static_cast<uint32_t>(2 * cq + 1) ^ static_cast<uint32_t>(r & 7)) << 4);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
+                             ::"r"(d0), "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]) : "memory");
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
+                             ::"r"(d1), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7]) : "memory");
+            }
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+                if (PAIR) mbar_arrive_cluster(cvt_c0 + 8u * sb);
+                else mbar_arrive(&cvt[sb]);
+            }
+            if (++s == static_cast<uint32_t>(S)) { s = 0; ph ^= 1u; }
+            if (++sb == static_cast<uint32_t>(FP8_SB)) { sb = 0; pb ^= 1u; }
         }
     } else {
         // ----------------------------------------------------------------- epilogue
@@ -704,19 +869,23 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 3-D bf16 weight tensor [n_groups][rows][cols] (cols contiguous), 64 x 64 boxes.
-bool encode_weight(CUtensorMap *m, const void *base, int n_groups, int rows, int cols)
+// 3-D weight tensor [n_groups][rows][cols] (cols contiguous), 64 x 64 boxes: bf16 into the
+// 128-byte swizzle the MMA reads, or E4M3 bytes (fp8) as plain 64-byte rows.
+bool encode_weight(CUtensorMap *m, const void *base, int n_groups, int rows, int cols,
+                   bool fp8 = false)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
+    const cuuint64_t esz = fp8 ? 1 : 2;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
                           static_cast<cuuint64_t>(n_groups)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2,
-                             static_cast<cuuint64_t>(cols) * rows * 2};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * esz,
+                             static_cast<cuuint64_t>(cols) * rows * esz};
     cuuint32_t box[3] = {64, 64, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    return fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -746,17 +915,20 @@ int pick_bn(int avg_rows)
     return bn;
 }
 
-size_t ffn_smem_bytes(int bn_cta, int stages, int tab)
+size_t ffn_smem_bytes(int bn_cta, int stages, int tab, bool fp8)
 {
-    return 1024 + static_cast<size_t>(stages) * (A_BYTES + bn_cta * 128) + XCHG_FLOATS * 4 +
-           (2 * stages + 5 + 2 * TQ) * 8 + 16 + (6 * static_cast<size_t>(tab) + 8 * TQ) * 4;
+    const size_t stage = fp8 ? static_cast<size_t>(bn_cta) * 128 + A8_BYTES
+                             : static_cast<size_t>(A_BYTES) + bn_cta * 128;
+    return 1024 + stages * stage + (fp8 ? static_cast<size_t>(FP8_SB) * A_BYTES : 0) +
+           XCHG_FLOATS * 4 + (2 * stages + 5 + 2 * TQ) * 8 + (fp8 ? 2 * FP8_SB * 8 + stages * 8 + 2 * TSC * 4 : 0) +
+           16 + (6 * static_cast<size_t>(tab) + 8 * TQ) * 4;
 }
 
-int pick_stages(int bn_cta, int tab)
+int pick_stages(int bn_cta, int tab, bool fp8)
 {
     const size_t cap = 232448;   // max dynamic shared memory per block on sm_100/sm_103
-    int s = MAX_STAGES;
-    while (s > 2 && ffn_smem_bytes(bn_cta, s, tab) > cap) --s;
+    int s = fp8 ? MAX_STAGES_FP8 : MAX_STAGES;
+    while (s > 2 && ffn_smem_bytes(bn_cta, s, tab, fp8) > cap) --s;
     return s;
 }
 
@@ -778,13 +950,20 @@ size_t ffn_ready_slots(long long rows, int n_groups)
 
 cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I_pp,
                        int token_hint, unsigned *ready, bool ready_zeroed, int *status, cudaStream_t s,
-                       unsigned long long timeout_ns, int inject, cudaEvent_t mid_event)
+                       unsigned long long timeout_ns, int inject, cudaEvent_t mid_event,
+                       int phase_only)
 {
-    if (n_probs < 1 || n_probs > 2 || !ready) return cudaErrorInvalidValue;
+    if (n_probs < 1 || n_probs > 2 || !ready || phase_only < -1 || phase_only > 1)
+        return cudaErrorInvalidValue;
     int n_cg = 0;
     long long rows_total = 0;
+    const bool fp8 = probs[0].fp8 != 0;
     for (int pi = 0; pi < n_probs; ++pi) {
         if (probs[pi].n_groups < 1 || probs[pi].n_groups > MAX_GROUPS) return cudaErrorInvalidValue;
+        if ((probs[pi].fp8 != 0) != fp8) return cudaErrorInvalidValue;
+        if (fp8 && (!probs[pi].S1 || !probs[pi].S3 || !probs[pi].S2 || H % 128 || I_pp[pi] % 128 ||
+                    H > 128 * TSC || I_pp[pi] > 128 * TSC))
+            return cudaErrorInvalidValue;
         n_cg += probs[pi].n_groups;
         rows_total += probs[pi].rows;
     }
@@ -794,8 +973,8 @@ cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I
     if (pair && bn < 32) bn = 32;           // 16 token rows per CTA at least
     const int bn_cta = pair ? bn / 2 : bn;
     const int tab = (n_cg + 1 + 3) & ~3;
-    const int stages = pick_stages(bn_cta, tab);
-    const size_t smem = ffn_smem_bytes(bn_cta, stages, tab);
+    const int stages = pick_stages(bn_cta, tab, fp8);
+    const size_t smem = ffn_smem_bytes(bn_cta, stages, tab, fp8);
     int tcols = 32;
     while (tcols < 2 * bn) tcols <<= 1;
     const int m_up = pair ? 128 : 64;      // weight columns of one tile
@@ -806,10 +985,10 @@ cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I
     for (int pi = 0; pi < n_probs; ++pi) {
         const FfnProblem &P = probs[pi];
         const int I = I_pp[pi];
-        if (!encode_weight(&a.upA[pi], P.W1, P.n_groups, H, I) ||
-            !encode_weight(&a.upA3[pi], P.W3, P.n_groups, H, I) ||
+        if (!encode_weight(&a.upA[pi], P.W1, P.n_groups, H, I, fp8) ||
+            !encode_weight(&a.upA3[pi], P.W3, P.n_groups, H, I, fp8) ||
             !encode_act(&a.upB[pi], P.act, P.rows, H, bn_cta) ||
-            !encode_weight(&a.dnA[pi], P.W2, P.n_groups, I, H) ||
+            !encode_weight(&a.dnA[pi], P.W2, P.n_groups, I, H, fp8) ||
             !encode_act(&a.dnB[pi], P.h, P.rows, I, bn_cta))
             return cudaErrorInvalidValue;
         ProbDev d{};
@@ -825,6 +1004,9 @@ cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I
         d.out_fp32 = P.out_fp32;
         d.h = P.h;
         d.out = P.out;
+        d.s1 = P.S1;
+        d.s3 = P.S3;
+        d.s2 = P.S2;
         a.prob[pi] = d;
     }
     a.n_probs = n_probs;
@@ -836,17 +1018,27 @@ cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I
     a.status = status;
     a.timeout_ns = timeout_ns;
     a.inject = inject;
+    a.phase_only = phase_only;
+    const size_t slots = ffn_ready_slots(rows_total, n_cg);
     cudaError_t err;
-    if (!ready_zeroed &&
-        (err = cudaMemsetAsync(ready, 0, ffn_ready_slots(rows_total, n_cg) * sizeof(unsigned), s)) != cudaSuccess)
+    if (!ready_zeroed && (err = cudaMemsetAsync(ready, 0, slots * sizeof(unsigned), s)) != cudaSuccess)
         return err;
-    const void *fn = pair ? reinterpret_cast<const void *>(ffn_kernel<true>)
-                          : reinterpret_cast<const void *>(ffn_kernel<false>);
+    const void *fn = fp8 ? (pair ? reinterpret_cast<const void *>(ffn_kernel<true, true>)
+                                 : reinterpret_cast<const void *>(ffn_kernel<false, true>))
+                         : (pair ? reinterpret_cast<const void *>(ffn_kernel<true, false>)
+                                 : reinterpret_cast<const void *>(ffn_kernel<false, false>));
     if ((err = ensure_smem(fn, smem)) != cudaSuccess) return err;
-    // the last readiness slot is the tile counter of the launch
-    a.next_tile = ready + ffn_ready_slots(rows_total, n_cg) - 1;
-    err = pair ? launch_pdl(ffn_kernel<true>, dim3(num_sms() / 2 * 2), dim3(NUM_THREADS), smem, s, 2, a)
-               : launch_pdl(ffn_kernel<false>, dim3(num_sms()), dim3(NUM_THREADS), smem, s, 1, a);
+    // the tile counters of a launch: the last readiness slot, the one before it for a
+    // launch of the down tiles alone (the up tiles' launch ran first with the last slot)
+    a.next_tile = ready + slots - (phase_only == 1 ? 2 : 1);
+    const dim3 block(fp8 ? NUM_THREADS_FP8 : NUM_THREADS);
+    const dim3 grid_pair(num_sms() / 2 * 2), grid_one(num_sms());
+    if (fp8)
+        err = pair ? launch_pdl(ffn_kernel<true, true>, grid_pair, block, smem, s, 2, a)
+                   : launch_pdl(ffn_kernel<false, true>, grid_one, block, smem, s, 1, a);
+    else
+        err = pair ? launch_pdl(ffn_kernel<true, false>, grid_pair, block, smem, s, 2, a)
+                   : launch_pdl(ffn_kernel<false, false>, grid_one, block, smem, s, 1, a);
     if (err != cudaSuccess) return err;
     // one launch computes both projections: the "between" mark follows it
     if (mid_event && (err = cudaEventRecord(mid_event, s)) != cudaSuccess) return err;

@@ -60,6 +60,15 @@ cudaError_t launch_dispatch(const void *X, const int32_t *topk_idx, int T, int H
                             const DispatchPlan &plan, const DispatchScratch &scr,
                             unsigned *zero_buf, size_t zero_n, int *status, cudaStream_t s);
 
+// ------------------------------------------------------------------------------ fp8
+// Static E4M3 quantisation of W [G][R][C] bf16 (R, C multiples of 128) into Wq [G][R][C]
+// bytes and the scale exponents S [G][R/128][C/128] (scale 2^S).
+cudaError_t launch_quant_weight(const void *W, int G, int R, int C, void *Wq, int32_t *S,
+                                cudaStream_t s);
+// Quantise-dequantise bf16 rows [rows][n] (n a multiple of 128) in vectors of 128 into out
+// (may alias in).
+cudaError_t launch_quant_rows(const void *in, long long rows, int n, void *out, cudaStream_t s);
+
 // -------------------------------------------------------------------------- combine
 cudaError_t launch_combine(const void *Yp, const int32_t *slot_pos, const float *topk_w,
                            const float *Ysh, int T, int H, int K, float *Y, cudaStream_t s);
@@ -77,6 +86,11 @@ struct FfnProblem {
     void *h;                // bf16 [rows, I] activation scratch
     void *out;              // [rows, H] bf16 or fp32
     int out_fp32;
+    // FP8 weights: W1, W3, W2 hold E4M3 bytes and S1, S3 [n_groups][H/128][I/128], S2
+    // [n_groups][I/128][H/128] the scale exponents of their 128 x 128 tiles (H, I multiples
+    // of 128).  Every problem of a launch uses the same weight format.
+    int fp8;
+    const int32_t *S1, *S3, *S2;
 };
 
 // Launch with programmatic stream serialization (the kernel overlaps its prologue with
@@ -118,9 +132,12 @@ void set_ffn_variant(int v);
 // tracked by `ready` (device, ffn_ready_slots(...) counters incl. the tile counter,
 // zeroed here unless `ready_zeroed`).  `mid_event` (nullable) is recorded after the
 // launch.
+// phase_only: -1 both projections; 0 the up projections alone; 1 the down projections alone
+// (after a phase-0 launch of the same problems and the same readiness counters).
 cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I_per_prob,
                        int token_hint, unsigned *ready, bool ready_zeroed, int *status, cudaStream_t s,
-                       unsigned long long timeout_ns, int inject, cudaEvent_t mid_event);
+                       unsigned long long timeout_ns, int inject, cudaEvent_t mid_event,
+                       int phase_only = -1);
 
 // Readiness counters launch_ffn needs (unsigned each) for `rows` rows in `n_groups` groups
 // over all its problems.

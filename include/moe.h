@@ -83,6 +83,22 @@ typedef struct moe_weights {
     const void *W1s, *W3s, *W2s;
 } moe_weights_t;
 
+/* Layer weights with FP8 experts ("Lower latency and higher throughput...", Quantization:
+ * weights quantised ahead of time with one scale per 128 x 128 tile).  W_gate and bias as in
+ * moe_weights_t (the router is not quantised).  W1, W3, W2 (and W1s, W3s, W2s) hold E4M3
+ * bytes in the layouts of moe_weights_t; S1, S3 int32 [E, H/128, I/128] and S2 int32
+ * [E, I/128, H/128] (S1s, S3s [H/128, I_shared/128], S2s [I_shared/128, H/128]) hold the
+ * scale exponents: a weight is its E4M3 value times 2^S of its tile.
+ * moe_quantize_weight_fp8 produces both from bf16 weights. */
+typedef struct moe_weights_fp8 {
+    const void *W_gate;
+    const float *bias;
+    const void *W1, *W3, *W2;
+    const int32_t *S1, *S3, *S2;
+    const void *W1s, *W3s, *W2s;
+    const int32_t *S1s, *S3s, *S2s;
+} moe_weights_fp8_t;
+
 /* Bytes of workspace that moe_layer_forward needs for `shape`; it also suffices for every
  * other entry point called with the same or smaller sizes.  Returns 0 for an invalid shape. */
 size_t moe_workspace_bytes(const moe_shape_t *shape);
@@ -251,6 +267,39 @@ int moe_layer_forward_ex(const moe_shape_t *shape, const moe_weights_t *weights,
                          int32_t *topk_idx, float *topk_w, int32_t *counts,
                          int32_t *affinity,
                          void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------------------
+ * FP8 experts ("Lower latency and higher throughput...", Quantization: FP8 with block-wise
+ * scales, weights per 128 x 128 tile ahead of time, activations per 128-element vector on
+ * the fly).  Format E4M3 (largest finite 448), round to nearest even; a block's scale is
+ * the power of two 2^k with k the smallest integer such that amax <= 448 * 2^k (0 for an
+ * all-zero block), clamped to [-124, 127], so every dequantised value q * 2^k is exact in
+ * bf16.
+ * ------------------------------------------------------------------------------------ */
+
+/* Static weight quantisation: W bf16 [G, R, C] (R, C multiples of 128, else
+ * MOE_ERR_UNSUPPORTED_SHAPE) -> Wq E4M3 bytes [G, R, C] and S int32 [G, R/128, C/128] (the
+ * tile's k).  Device pointers, enqueued on `stream`. */
+int moe_quantize_weight_fp8(const void *W, int G, int R, int C, void *Wq, int32_t *S,
+                            void *stream);
+
+/* Activation quantisation as the FP8 layer applies it: every row of `in` bf16 [rows, n]
+ * (n a multiple of 128) in vectors of 128, quantised to E4M3 and dequantised back, into
+ * `out` bf16 [rows, n] (out may equal in).  Device pointers, enqueued on `stream`. */
+int moe_quantize_rows_fp8(const void *in, long long rows, int n, void *out, void *stream);
+
+/* The layer with FP8 experts: as moe_layer_forward_ex, with the expert FFNs (routed and
+ * shared) computed from the dequantised E4M3 weights on token rows quantised in vectors
+ * of 128 along H and on h = silu(x W1) * (x W3), rounded to bf16, quantised in vectors of
+ * 128 along I.  The GEMMs sum the exact products of the dequantised values in fp32 -- what
+ * an FP8 GEMM with these block scales computes.  H, I and I_shared must be multiples of
+ * 128 and at most 16384 (else MOE_ERR_UNSUPPORTED_SHAPE).  Same workspace as
+ * moe_layer_forward. */
+int moe_layer_forward_fp8(const moe_shape_t *shape, const moe_weights_fp8_t *weights,
+                          const moe_routing_t *routing, const void *X, float *Y,
+                          int32_t *topk_idx, float *topk_w, int32_t *counts,
+                          int32_t *affinity,
+                          void *ws, size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------------------------
  * GRACE-MoE placement planner ("GRACE-MoE" notes, Core Idea 1-3).  Host code on HOST

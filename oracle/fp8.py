@@ -51,12 +51,9 @@ def e4m3_round(v: np.ndarray) -> np.ndarray:
     a = np.abs(v)
     if np.any(a > E4M3_MAX):
         raise ValueError("value outside the E4M3 range")
-    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
-    # guard the floor of log2 against rounding at exact powers of two
-    e = np.where(2.0 ** e > a, e - 1, e)
-    e = np.where(2.0 ** (e + 1) <= a, e + 1, e)
-    e = np.maximum(e, -6.0)                       # below 2^-6 the grid step is 2^-9
-    step = 2.0 ** (e - 3)
+    e = np.frexp(np.where(a > 0, a, 1.0))[1] - 1  # a in [2^e, 2^(e+1)): exact
+    e = np.maximum(e, -6)                         # below 2^-6 the grid step is 2^-9
+    step = np.ldexp(1.0, e - 3)
     r = np.round(a / step) * step                 # numpy rounds halves to even
     return np.where(v < 0, -r, r)
 
@@ -80,22 +77,22 @@ def quantize_tile(x: np.ndarray):
     return e4m3_round(x / 2.0 ** k), k
 
 
+def _scale_exponents(amax: np.ndarray) -> np.ndarray:
+    return np.vectorize(scale_exponent, otypes=[np.int64])(amax)
+
+
 def quantize_weight(W: np.ndarray):
     """W [..., R, C] (R, C multiples of 128) -> q (same shape, E4M3 values as float64) and
-    k [..., R/128, C/128] (int)."""
+    k [..., R/128, C/128] (int): each 128 x 128 tile on its own."""
     W = np.asarray(W, dtype=np.float64)
     R, C = W.shape[-2:]
     lead = W.shape[:-2]
-    q = np.empty_like(W)
-    k = np.empty(lead + (R // BLOCK, C // BLOCK), np.int64)
-    for idx in np.ndindex(*lead) if lead else [()]:
-        for i in range(R // BLOCK):
-            for j in range(C // BLOCK):
-                blk = W[idx + (slice(i * BLOCK, (i + 1) * BLOCK), slice(j * BLOCK, (j + 1) * BLOCK))]
-                qq, kk = quantize_tile(blk)
-                q[idx + (slice(i * BLOCK, (i + 1) * BLOCK), slice(j * BLOCK, (j + 1) * BLOCK))] = qq
-                k[idx + (i, j)] = kk
-    return q, k
+    tiles = W.reshape(lead + (R // BLOCK, BLOCK, C // BLOCK, BLOCK))
+    amax = np.abs(tiles).max(axis=(-3, -1))                     # [..., R/128, C/128]
+    k = _scale_exponents(amax)
+    scale = 2.0 ** k.astype(np.float64)
+    q = e4m3_round(tiles / scale[..., :, None, :, None])
+    return q.reshape(W.shape), k
 
 
 def dequantize_weight(q: np.ndarray, k: np.ndarray) -> np.ndarray:
@@ -106,15 +103,11 @@ def dequantize_weight(q: np.ndarray, k: np.ndarray) -> np.ndarray:
 def fake_quant_rows(x: np.ndarray) -> np.ndarray:
     """Quantise then dequantise every row of x [..., n] in blocks of 128 along the row."""
     x = np.asarray(x, dtype=np.float64)
-    out = np.empty_like(x)
     n = x.shape[-1]
-    flat = x.reshape(-1, n)
-    o = out.reshape(-1, n)
-    for r in range(flat.shape[0]):
-        for j in range(0, n, BLOCK):
-            q, k = quantize_tile(flat[r, j:j + BLOCK])
-            o[r, j:j + BLOCK] = q * 2.0 ** k
-    return out
+    v = x.reshape(x.shape[:-1] + (n // BLOCK, BLOCK))
+    k = _scale_exponents(np.abs(v).max(axis=-1))
+    scale = 2.0 ** k.astype(np.float64)[..., None]
+    return (e4m3_round(v / scale) * scale).reshape(x.shape)
 
 
 def round_bf16(x: np.ndarray) -> np.ndarray:
