@@ -39,6 +39,12 @@
 // second read; a down tile waits (bounded) until the up tiles of its token tile have
 // published their h rows.
 //
+// FP8 weights (ffn_kernel<PAIR, true>).  The weights arrive as E4M3 bytes with one
+// power-of-two scale per 128 x 128 tile ("Lower latency and higher throughput...",
+// Quantization).  The ring then holds token rows and E4M3 weight boxes; eight more warps
+// dequantise each box into the bf16 tile the MMA reads (exact: q * 2^k fits bf16) in a
+// separate small ring of tiles.  The MMAs and the epilogue are those of the bf16 kernel.
+//
 // Every wait is bounded (globaltimer): when one runs out the kernel records
 // MOE_ERR_DEVICE_TIMEOUT in the status word, the other roles leave their loops, copies and
 // MMAs in flight are drained with bounded waits, TMEM is freed and the kernel returns.
