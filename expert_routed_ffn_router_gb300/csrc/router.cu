@@ -25,7 +25,7 @@
 //
 // Structure.  A grid (expert tiles, token tiles, K splits) of 256-thread CTAs computes
 // fp32 logit tiles on the CUDA cores into the workspace:
-//   tiny batches (T <= 4):     one warp per expert, all tokens at once;
+//   tiny batches (T <= 8):     four warps per expert, all tokens at once;
 //   small batches (T <= 4096): 16 tokens x 256 experts per CTA, 4x4 per thread;
 //   large batches:             128 tokens x 64 experts per CTA, 8x4 per thread.
 // Small batches: the last CTA of a token tile (completion counter) sums the split-K
@@ -998,18 +998,19 @@ __device__ void gemm_tile(const RouterArgs &a, unsigned char *smem)
     }
 }
 
-// ----------------------------------------------------------- tiny batches (T <= 4)
+// ----------------------------------------------------------- tiny batches (T <= 8)
 // GEMV_QW warps share one expert's gate row, each reading a quarter of it once and forming
 // the partial logits of all T tokens; a CTA holds GEMV_EPC experts, so the whole gate
 // matrix is read by E * GEMV_QW warps spread over the GPU (a cold read of 3.7 MB is
 // latency-bound: it needs many loads in flight).  Each partial is 8 independent fp32
 // chains (one per element of a 16-byte vector) added by a fixed 3-level tree and a
 // 5-level warp tree; the quarters are added by a fixed 2-level tree.
-constexpr int GEMV_TMAX = 4;      // beyond 4 tokens the 16x256 tile path is faster
+constexpr int GEMV_TMAX = 8;      // up to 8 tokens (5..8: 87 -> 65 us per router stage than the
+                                  // 16x256 tile path, which has one CTA per split here)
 constexpr int GEMV_QW = 4;        // warps per gate row
 constexpr int GEMV_EPC = NW / GEMV_QW;
 
-template <int TB>     // token batch: 1, 2 or 4 (>= T)
+template <int TB>     // token batch: 1, 2, 4 or 8 (>= T)
 __device__ void gemv_tile(const RouterArgs &a, unsigned char *smem)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1030,7 +1031,7 @@ __device__ void gemv_tile(const RouterArgs &a, unsigned char *smem)
             for (int j = 0; j < 8; ++j) acc[t][j] = 0.f;
         }
         float wsq = 0.f;
-        constexpr int U = TB <= 2 ? 4 : 2;       // vectors per lane in flight
+        constexpr int U = TB <= 2 ? 4 : (TB <= 4 ? 2 : 1);   // vectors per lane in flight
         for (int v0 = v_beg + lane; v0 < v_end; v0 += 32 * U) {
             uint4 wv[U], xv[U][TB];
 #pragma unroll
@@ -1446,7 +1447,8 @@ RouterPlan router_plan(int T, int H, int E)
         // (the finalise reads up to 32 splits; beyond 16 the extra partial reads and the
         // larger bound -- more tokens to refine -- measured slower at decode)
         if (p.KS > 32) p.KS = 32;
-        while (p.KS * 2 <= p.S && p.KS * 2 <= 16 && base * p.KS < target) p.KS *= 2;
+        // (up to 32 splits when there are at most 4 token tiles: too few CTAs otherwise)
+        while (p.KS * 2 <= p.S && p.KS * 2 <= (p.nTT <= 4 ? 32 : 16) && base * p.KS < target) p.KS *= 2;
         p.depth = KST + (p.S + p.KS - 1) / p.KS + p.KS + 2;
     }
     p.max_pairs = 1024;
@@ -1491,6 +1493,7 @@ cudaError_t launch_router(const void *X, const void *Wg, const float *bias, int 
         case 1: fn = reinterpret_cast<const void *>(router_fused_kernel<SmallCfg, 1>); break;
         case 2: fn = reinterpret_cast<const void *>(router_fused_kernel<SmallCfg, 2>); break;
         case 4: fn = reinterpret_cast<const void *>(router_fused_kernel<SmallCfg, 4>); break;
+        case 8: fn = reinterpret_cast<const void *>(router_fused_kernel<SmallCfg, 8>); break;
         default: fn = reinterpret_cast<const void *>(router_fused_kernel<SmallCfg, 0>); break;
         }
         err = ensure_smem(fn, plan.smem_bytes);
@@ -1499,6 +1502,7 @@ cudaError_t launch_router(const void *X, const void *Wg, const float *bias, int 
         case 1: return launch_pdl(router_fused_kernel<SmallCfg, 1>, grid, dim3(NT), plan.smem_bytes, s, 1, a);
         case 2: return launch_pdl(router_fused_kernel<SmallCfg, 2>, grid, dim3(NT), plan.smem_bytes, s, 1, a);
         case 4: return launch_pdl(router_fused_kernel<SmallCfg, 4>, grid, dim3(NT), plan.smem_bytes, s, 1, a);
+        case 8: return launch_pdl(router_fused_kernel<SmallCfg, 8>, grid, dim3(NT), plan.smem_bytes, s, 1, a);
         default: return launch_pdl(router_fused_kernel<SmallCfg, 0>, grid, dim3(NT), plan.smem_bytes, s, 1, a);
         }
     }

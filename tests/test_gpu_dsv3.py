@@ -26,7 +26,7 @@ def test_decode_T128(dsv3_weights):
     check_layer(Problem(w, weights_dev=dsv3_weights), tokens=_sample(w.T, 4))
 
 
-@pytest.mark.parametrize("T", [2, 64])
+@pytest.mark.parametrize("T", [2, 8, 64])
 def test_batch_sweep(dsv3_weights, T):
     w = synth.workload(f"sweep{T}")
     r = check_layer(Problem(w, weights_dev=dsv3_weights),

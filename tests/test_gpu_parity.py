@@ -29,6 +29,7 @@ def test_tiny_layer():
 @pytest.mark.parametrize("T,H,E,K,I,Is", [
     (1, 256, 16, 2, 128, 128),      # a single token: 14 experts receive nothing
     (3, 256, 16, 2, 128, 128),      # tiny batch: 3 of a 4-token router batch
+    (6, 256, 16, 2, 128, 128),      # 6 of an 8-token router batch
     (37, 256, 16, 2, 128, 128),     # ragged token tail
     (300, 192, 40, 5, 192, 64),     # H % 128 == 64, E not a multiple of 32, K = 5
     (130, 128, 8, 8, 64, 0),        # K == E (every expert, order only), no shared expert

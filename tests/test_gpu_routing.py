@@ -53,7 +53,7 @@ def _check_router(r, K, opts):
 
 
 @pytest.mark.parametrize("name", sorted(OPTS))
-@pytest.mark.parametrize("T", [1, 3, 200, 4100])
+@pytest.mark.parametrize("T", [1, 3, 7, 200, 4100])
 def test_router_options_dsv3_shape(name, T):
     w = synth.workload("decode", T=T, x_seed=T + 11)
     _check_router(synth.routing_inputs(w), w.K, OPTS[name])
