@@ -289,11 +289,12 @@ class MoELayer:
     (optionally) W1s, W3s, W2s."""
 
     def __init__(self, weights: dict, T: int, K: int, with_affinity: bool = True,
-                 routing=None, fp8: bool = False):
+                 routing=None, fp8: bool = False, weights8: dict | None = None):
         self.w = weights
         self.routing = routing
-        # FP8 experts: the weights are quantised once here (static, 128 x 128 tiles)
-        self.w8 = quantize_expert_weights_fp8(weights) if fp8 else None
+        # FP8 experts: the weights are quantised once here (static, 128 x 128 tiles), unless
+        # another layer's quantised weights are passed in
+        self.w8 = (weights8 if weights8 is not None else quantize_expert_weights_fp8(weights)) if fp8 else None
         E, H = weights["W_gate"].shape
         I = weights["W1"].shape[-1]
         Is = 0 if weights.get("W1s") is None else weights["W1s"].shape[-1]
