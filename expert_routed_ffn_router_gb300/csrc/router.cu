@@ -18,16 +18,19 @@
 // additions, so |l_fp32 - l| <= gamma_d * sum|x_h w_h| <= gamma_d * ||x|| * ||w||
 // (Cauchy-Schwarz), gamma_d = d u / (1 - d u), u = 2^-24.  Propagating that bound through
 // the sigmoid and the bias add gives an interval per expert.  When the intervals certify
-// both the chosen set and its order, the fp32 result is exact; otherwise every expert
-// whose interval reaches the k-th lower bound is re-scored in double-word fp32 arithmetic
-// (error-free TwoSum accumulation of the exact products, ~2^-48 relative) with an fp64
-// sigmoid, and the top-k is taken again among those candidates.
+// both the chosen set and its order, the fp32 result is exact; otherwise the candidates
+// are the experts whose interval reaches the k-th lower bound, and those whose interval
+// meets another candidate's (every candidate, under the other routing options) are
+// re-scored in double-word fp32 arithmetic (error-free TwoSum accumulation of the exact
+// products, ~2^-48 relative) with an fp64 sigmoid; the top-k is taken again among the
+// candidates (the others keep their fp32 sel, which orders exactly since their intervals
+// are disjoint from every other candidate's).
 //
 // Structure.  A grid (expert tiles, token tiles, K splits) of 256-thread CTAs computes
 // fp32 logit tiles on the CUDA cores into the workspace:
 //   tiny batches (T <= 8):     four warps per expert, all tokens at once;
 //   small batches (T <= 4096): 16 tokens x 256 experts per CTA, 4x4 per thread;
-//   large batches:             128 tokens x 64 experts per CTA, 8x4 per thread.
+//   large batches:             128 tokens x 128 experts per CTA, 8x8 per thread.
 // Small batches: the last CTA of a token tile (completion counter) sums the split-K
 // partials in a fixed order, scores, selects and writes the outputs -- one launch.
 // Large batches: a second launch finalises, one warp per token, so the selection of
@@ -71,10 +74,11 @@ struct RouterArgs {
 
 // CTA tile: TT tokens x TE experts, TPT x EPT per thread, PF stages of loads in flight;
 // X2: paired fp32 FMAs (two tokens per instruction) -- the same correctly rounded
-// operations in the same order, in half the FMA instructions.
-template <int TT_, int TE_, int TPT_, int EPT_, int PF_, int X2_ = 0>
+// operations in the same order, in half the FMA instructions; MINB: resident CTAs per SM
+// the registers are sized for.
+template <int TT_, int TE_, int TPT_, int EPT_, int PF_, int X2_ = 0, int MINB_ = 2>
 struct Cfg {
-    static constexpr int TT = TT_, TE = TE_, TPT = TPT_, EPT = EPT_, PF = PF_;
+    static constexpr int TT = TT_, TE = TE_, TPT = TPT_, EPT = EPT_, PF = PF_, MINB = MINB_;
     static constexpr bool X2 = X2_ != 0;
     static constexpr int NTY = TT / TPT, NTX = TE / EPT;
     static constexpr int LY = 4;                          // token groups per warp
@@ -82,10 +86,13 @@ struct Cfg {
     static constexpr int XPT = (XV + NT - 1) / NT, WPT = (WV + NT - 1) / NT;
     static_assert(NTX * NTY == NT, "one output micro-tile per thread");
     static_assert(NTY % LY == 0 && NTX % (32 / LY) == 0, "warp layout");
-    static_assert(EPT == 4 && TPT % 4 == 0, "float4 operand reads");
+    static_assert(EPT % 4 == 0 && TPT % 4 == 0 && (EPT == 4 || X2), "float4 operand reads");
 };
 using SmallCfg = Cfg<16, 256, 4, 4, 2>;
-using LargeCfg = Cfg<128, 64, 8, 4, 2, 1>;
+// 8 x 8 outputs a thread: 16 operands read from shared memory per 64 FMAs (the 8 x 4 tile
+// read 12 per 32 and was bound by shared-memory bandwidth); one CTA per SM holds the
+// 64 paired running sums.
+using LargeCfg = Cfg<128, 128, 8, 8, 2, 1, 1>;
 
 // Two fp32 lanes per 64-bit register: d = a * b + c and d = a + b, each lane correctly
 // rounded (the same results as two fmaf / two fp32 adds).
@@ -870,10 +877,17 @@ __device__ void gemm_tile(const RouterArgs &a, unsigned char *smem)
         }
     };
 
-    // output micro-tile of this thread: tokens TPT*ty.., experts EPT*tx..
+    // output micro-tile of this thread: TPT tokens and EPT experts, each in groups of four
+    // interleaved over the warp's lane rows (LY) and lane columns (LX): token group g of
+    // lane row r is wtok + 4 (LY g + r) ..+3, expert group g of lane column c is
+    // wexp + 4 (LX g + c) ..+3, so each 16-byte operand read covers one contiguous span of
+    // the stage across the warp
     constexpr int WY = C::NTY / C::LY;
-    const int ty = (warp % WY) * C::LY + (lane % C::LY);
-    const int tx = (warp / WY) * (32 / C::LY) + lane / C::LY;
+    constexpr int LX = 32 / C::LY;
+    const int wtok = (warp % WY) * (C::LY * C::TPT) + 4 * (lane % C::LY);
+    const int wexp = (warp / WY) * (LX * C::EPT) + 4 * (lane / C::LY);
+    auto tok = [&](int i) { return wtok + (i >> 2) * (4 * C::LY) + (i & 3); };
+    auto exq = [&](int j) { return wexp + (j >> 2) * (4 * LX) + (j & 3); };
     float acc[C::TPT * C::EPT];
 #pragma unroll
     for (int p = 0; p < C::TPT * C::EPT; ++p) acc[p] = 0.f;
@@ -895,30 +909,38 @@ __device__ void gemm_tile(const RouterArgs &a, unsigned char *smem)
                 __syncthreads();
                 // one 32-deep fp32 chain per (token, expert) for this stage, then added to
                 // the running sum of the split
-                const float *xb = xs + buf * KST * C::TT + C::TPT * ty;
-                const float *wb = wsm + buf * KST * C::TE + C::EPT * tx;
+                const float *xb = xs + buf * KST * C::TT + wtok;
+                const float *wb = wsm + buf * KST * C::TE + wexp;
                 if constexpr (C::X2) {
-                    // pair pp * 4 + jj = (token 2pp, token 2pp + 1) x expert jj
-                    uint64_t pin[C::TPT / 2 * 4];
+                    // pair pp * EPT + jj = (token 2pp, token 2pp + 1) x expert jj
+                    uint64_t pin[C::TPT / 2 * C::EPT];
 #pragma unroll
-                    for (int q = 0; q < C::TPT / 2 * 4; ++q) pin[q] = 0ull;
+                    for (int q = 0; q < C::TPT / 2 * C::EPT; ++q) pin[q] = 0ull;
 #pragma unroll 4
                     for (int kk = 0; kk < KST; ++kk) {
                         ulonglong2 xv[C::TPT / 4];
 #pragma unroll
                         for (int i4 = 0; i4 < C::TPT / 4; ++i4)
-                            xv[i4] = *reinterpret_cast<const ulonglong2 *>(xb + kk * C::TT + 4 * i4);
-                        const float4 wv = *reinterpret_cast<const float4 *>(wb + kk * C::TE);
-                        const uint64_t wp[4] = {dup_x2(wv.x), dup_x2(wv.y), dup_x2(wv.z), dup_x2(wv.w)};
+                            xv[i4] = *reinterpret_cast<const ulonglong2 *>(xb + kk * C::TT + 4 * C::LY * i4);
+                        uint64_t wp[C::EPT];
+#pragma unroll
+                        for (int g = 0; g < C::EPT / 4; ++g) {
+                            const float4 wv = *reinterpret_cast<const float4 *>(wb + kk * C::TE + 4 * LX * g);
+                            wp[4 * g] = dup_x2(wv.x);
+                            wp[4 * g + 1] = dup_x2(wv.y);
+                            wp[4 * g + 2] = dup_x2(wv.z);
+                            wp[4 * g + 3] = dup_x2(wv.w);
+                        }
 #pragma unroll
                         for (int pp = 0; pp < C::TPT / 2; ++pp) {
                             const uint64_t xp = (pp & 1) ? xv[pp >> 1].y : xv[pp >> 1].x;
 #pragma unroll
-                            for (int jj = 0; jj < 4; ++jj) pin[pp * 4 + jj] = fma_x2(xp, wp[jj], pin[pp * 4 + jj]);
+                            for (int jj = 0; jj < C::EPT; ++jj)
+                                pin[pp * C::EPT + jj] = fma_x2(xp, wp[jj], pin[pp * C::EPT + jj]);
                         }
                     }
 #pragma unroll
-                    for (int q = 0; q < C::TPT / 2 * 4; ++q) accp[q] = add_x2(accp[q], pin[q]);
+                    for (int q = 0; q < C::TPT / 2 * C::EPT; ++q) accp[q] = add_x2(accp[q], pin[q]);
                 } else {
                     float acc_in[C::TPT * C::EPT];
 #pragma unroll
@@ -928,7 +950,7 @@ __device__ void gemm_tile(const RouterArgs &a, unsigned char *smem)
                         float xa[C::TPT];
 #pragma unroll
                         for (int i4 = 0; i4 < C::TPT / 4; ++i4) {
-                            const float4 v = *reinterpret_cast<const float4 *>(xb + kk * C::TT + 4 * i4);
+                            const float4 v = *reinterpret_cast<const float4 *>(xb + kk * C::TT + 4 * C::LY * i4);
                             xa[4 * i4] = v.x; xa[4 * i4 + 1] = v.y; xa[4 * i4 + 2] = v.z; xa[4 * i4 + 3] = v.w;
                         }
                         const float4 wv = *reinterpret_cast<const float4 *>(wb + kk * C::TE);
@@ -949,27 +971,30 @@ __device__ void gemm_tile(const RouterArgs &a, unsigned char *smem)
 #pragma unroll
         for (int pp = 0; pp < C::TPT / 2; ++pp)
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
+            for (int jj = 0; jj < C::EPT; ++jj) {
                 float lo, hi;
-                asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(accp[pp * 4 + jj]));
-                acc[(2 * pp) * 4 + jj] = lo;
-                acc[(2 * pp + 1) * 4 + jj] = hi;
+                asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(accp[pp * C::EPT + jj]));
+                acc[(2 * pp) * C::EPT + jj] = lo;
+                acc[(2 * pp + 1) * C::EPT + jj] = hi;
             }
     }
 
 #pragma unroll
     for (int i = 0; i < C::TPT; ++i) {
-        const int t = t0 + C::TPT * ty + i;
+        const int t = t0 + tok(i);
         if (t >= a.T) continue;
         float *dst = a.part + (static_cast<size_t>(ks) * a.T + t) * a.E;
-        const int e = e0 + C::EPT * tx;
-        if ((a.E & 3) == 0 && e + 3 < a.E) {
-            *reinterpret_cast<float4 *>(dst + e) =
-                make_float4(acc[i * 4], acc[i * 4 + 1], acc[i * 4 + 2], acc[i * 4 + 3]);
-        } else {
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj)
-                if (e + jj < a.E) dst[e + jj] = acc[i * 4 + jj];
+        for (int g = 0; g < C::EPT / 4; ++g) {
+            const int e = e0 + exq(4 * g);
+            const float *v = acc + i * C::EPT + 4 * g;
+            if ((a.E & 3) == 0 && e + 3 < a.E) {
+                *reinterpret_cast<float4 *>(dst + e) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    if (e + jj < a.E) dst[e + jj] = v[jj];
+            }
         }
     }
 
@@ -1164,6 +1189,47 @@ __device__ void refine_token_warp(const RouterArgs &a, int t, uint32_t cand, int
                        a.topk_w + static_cast<size_t>(t) * a.K, ord, lane);
 }
 
+// Re-scores only the candidates whose interval [sel - bound, sel + bound] meets another
+// candidate's; every other candidate keeps its fp32 sel, which lies in its own interval
+// and that interval is disjoint from all the others, so it orders against any candidate
+// exactly as the exact value would.  Writes the token's outputs; returns false (nothing
+// written) for more than 32 candidates.  Default routing options only.
+__device__ bool meets_another(const int *ce, int nc, const float *w_sel, const float *w_bnd, int lane)
+{
+    const int e = lane < nc ? ce[lane] : 0;
+    const float lo = lane < nc ? __fsub_rd(w_sel[e], w_bnd[e]) : FLT_MAX;
+    const float hi = lane < nc ? __fadd_ru(w_sel[e], w_bnd[e]) : -FLT_MAX;
+    bool meets = false;
+    for (int r = 0; r < nc; ++r) {
+        const float olo = __shfl_sync(kFullMask, lo, r), ohi = __shfl_sync(kFullMask, hi, r);
+        meets |= r != lane && lo <= ohi && olo <= hi;
+    }
+    return meets;
+}
+
+__device__ bool refine_overlapping(const RouterArgs &a, int t, uint32_t cand, const float *w_sel,
+                                   const float *w_bnd, int *ce, double *s64, int *ord, int lane)
+{
+    const int nc = list_candidates(cand, a.E, ce, lane);
+    if (nc > 32) return false;
+    const int e = lane < nc ? ce[lane] : 0;
+    const bool meets = meets_another(ce, nc, w_sel, w_bnd, lane);
+    uint32_t need = __ballot_sync(kFullMask, meets);
+    if (lane < nc && !meets) s64[lane] = static_cast<double>(w_sel[e]);
+    const uint16_t *xrow = a.X + static_cast<size_t>(t) * a.H;
+    while (need) {
+        const int q = __ffs(need) - 1;
+        need &= need - 1;
+        const int eq = ce[q];
+        const double l64 = dot_double_word(xrow, a.Wg + static_cast<size_t>(eq) * a.H, a.H, lane);
+        if (lane == 0) s64[q] = 1.0 / (1.0 + exp(-l64)) + static_cast<double>(a.bias[eq]);
+    }
+    __syncwarp();
+    select_refined(ce, s64, nc, a.K, a.bias, a.topk_idx + static_cast<size_t>(t) * a.K,
+                   a.topk_w + static_cast<size_t>(t) * a.K, ord, lane);
+    return true;
+}
+
 // ------------------------------------------------------- fused kernel (small batches)
 template <class C, int GEMV>   // GEMV = token batch of the tiny-batch path, 0 = tile GEMM
 __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
@@ -1284,7 +1350,15 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
             base = __shfl_sync(kFullMask, base, 0);
             if (base + n_cand <= a.max_pairs) {
                 list_candidates(cand, E, S.p_e + base, lane);
-                for (int q = lane; q < n_cand; q += 32) S.p_tok[base + q] = c0 + tl;
+                // default options: only candidates whose interval meets another's are
+                // re-scored (p_tok < 0 marks the others, which keep their fp32 sel)
+                const bool some = !a.variant && n_cand <= 32;
+                const bool meets = some ? meets_another(S.p_e + base, n_cand, S.sel, S.bnd, lane) : true;
+                for (int q = lane; q < n_cand; q += 32) {
+                    const bool need = !some || meets;
+                    S.p_tok[base + q] = need ? c0 + tl : -1 - (c0 + tl);
+                    if (!need) S.p_val[base + q] = static_cast<double>(S.sel[S.p_e[base + q]]);
+                }
                 if (lane == 0) {
                     const int pi = atomicAdd(&s_npend, 1);
                     s_pend[5 * pi] = c0 + tl;
@@ -1309,7 +1383,7 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
     const int npairs = min(s_npairs, a.max_pairs);
     for (int q = warp; q < npairs; q += NW) {
         const int e = S.p_e[q];
-        if (e < 0) continue;
+        if (e < 0 || S.p_tok[q] < 0) continue;
         const int t = t0 + S.p_tok[q];
         const double l64 = dot_double_word(a.X + static_cast<size_t>(t) * a.H,
                                            a.Wg + static_cast<size_t>(e) * a.H, a.H, lane);
@@ -1339,14 +1413,15 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
 
 // ------------------------------------------- GEMM-only kernel + finaliser (large batches)
 template <class C>
-__global__ void __launch_bounds__(NT, 2) router_gemm_kernel(const RouterArgs a)
+__global__ void __launch_bounds__(NT, C::MINB) router_gemm_kernel(const RouterArgs a)
 {
     pdl_wait();
     extern __shared__ __align__(16) unsigned char smem[];
     gemm_tile<C>(a, smem);
 }
 
-// One warp per token: split-K sum, scoring, certified top-K, refine when needed.
+// One warp per token: split-K sum, scoring, certified top-K, refine when needed.  The
+// CTA's tokens lie in one token tile (TT % NW == 0), whose gate-row norms it forms once.
 __global__ void __launch_bounds__(NT) router_finalize_kernel(const RouterArgs a, int TT)
 {
     pdl_wait();
@@ -1355,38 +1430,50 @@ __global__ void __launch_bounds__(NT) router_finalize_kernel(const RouterArgs a,
     const int t = blockIdx.x * NW + warp;
     const int E = a.E, KS = a.KS;
     float *fb = reinterpret_cast<float *>(smem);
-    float *w_sel = fb + static_cast<size_t>(warp) * 4 * E;
-    float *w_bnd = w_sel + E, *w_sc = w_bnd + E, *w_nw = w_sc + E;
-    int *ib = reinterpret_cast<int *>(fb + static_cast<size_t>(NW) * 4 * E);
+    float *w_nw = fb;                                       // [E], shared by the CTA
+    float *w_sel = fb + E + static_cast<size_t>(warp) * 3 * E;
+    float *w_bnd = w_sel + E, *w_sc = w_bnd + E;
+    int *ib = reinterpret_cast<int *>(fb + E + static_cast<size_t>(NW) * 3 * E);
     int *ce = ib + static_cast<size_t>(warp) * E;
     int *ord = ib + static_cast<size_t>(NW) * E + warp * 32;
     const uintptr_t d = reinterpret_cast<uintptr_t>(ib + static_cast<size_t>(NW) * E + NW * 32);
     double *s64 = reinterpret_cast<double *>((d + 7) & ~static_cast<uintptr_t>(7)) +
                   static_cast<size_t>(warp) * E;
-    if (t >= a.T) return;
     const Bounds bd(a.depth, KS, a.H);
-    const int tt = t / TT;
+    const int tt = (blockIdx.x * NW) / TT;
+    for (int e = threadIdx.x; e < E; e += NT) {
+        float n = 0.f;
+        for (int q0 = 0; q0 < KS; q0 += 16) {   // batches of 16 loads, added in split order
+            float pn[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                if (q0 + q < KS) pn[q] = __ldcg(a.wsq + (static_cast<size_t>(tt) * KS + q0 + q) * E + e);
+            if (q0 == 0) n = pn[0];
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                if (q0 + q < KS && q0 + q > 0) n += pn[q];
+        }
+        w_nw[e] = sqrtf(n) * bd.infl;
+    }
+    __syncthreads();
+    if (t >= a.T) return;
     const float part_sq = lane < KS ? __ldcg(a.xsq + static_cast<size_t>(lane) * a.T + t) : 0.f;
     float n2 = 0.f;
     for (int q = 0; q < KS; ++q) n2 += __shfl_sync(kFullMask, part_sq, q);
     const float nx = sqrtf(n2) * bd.infl;
     for (int e = lane; e < E; e += 32) {
-        float v = 0.f, n = 0.f;
+        float v = 0.f;
         for (int q0 = 0; q0 < KS; q0 += 16) {   // batches of 16 loads, added in split order
-            float pv[16], pn[16];
+            float pv[16];
 #pragma unroll
             for (int q = 0; q < 16; ++q)
-                if (q0 + q < KS) {
-                    pv[q] = __ldcg(a.part + (static_cast<size_t>(q0 + q) * a.T + t) * E + e);
-                    pn[q] = __ldcg(a.wsq + (static_cast<size_t>(tt) * KS + q0 + q) * E + e);
-                }
-            if (q0 == 0) { v = pv[0]; n = pn[0]; }
+                if (q0 + q < KS) pv[q] = __ldcg(a.part + (static_cast<size_t>(q0 + q) * a.T + t) * E + e);
+            if (q0 == 0) v = pv[0];
 #pragma unroll
             for (int q = 0; q < 16; ++q)
-                if (q0 + q < KS && q0 + q > 0) { v += pv[q]; n += pn[q]; }
+                if (q0 + q < KS && q0 + q > 0) v += pv[q];
         }
         w_sel[e] = v;
-        w_nw[e] = sqrtf(n) * bd.infl;
     }
     __syncwarp();
     uint32_t cand;
@@ -1406,6 +1493,8 @@ __global__ void __launch_bounds__(NT) router_finalize_kernel(const RouterArgs a,
     } else if (score_select(E, a.K, nx, w_nw, a.bias, bd.gam, w_sel, w_bnd, w_sc, oi, ow, cand,
                             n_cand, lane)) {
         return;
+    } else if (refine_overlapping(a, t, cand, w_sel, w_bnd, ce, s64, ord, lane)) {
+        return;
     }
     refine_token_warp(a, t, cand, ce, s64, ord, lane, every, ck, ug);
 }
@@ -1419,7 +1508,8 @@ size_t fused_smem(int TT, int TE, int E, int max_pairs)
 
 size_t finalize_smem(int E)
 {
-    return static_cast<size_t>(NW) * 5 * E * 4 + NW * 32 * 4 + 8 + static_cast<size_t>(NW) * E * 8;
+    return static_cast<size_t>(E) * 4 + static_cast<size_t>(NW) * 4 * E * 4 + NW * 32 * 4 + 8 +
+           static_cast<size_t>(NW) * E * 8;
 }
 
 }  // namespace
@@ -1437,7 +1527,7 @@ RouterPlan router_plan(int T, int H, int E)
     p.nET = (E + p.TE - 1) / p.TE;
     p.S = H / KST;
     const int base = p.nTT * p.nET;
-    const int target = 2 * num_sms();
+    const int target = (small ? SmallCfg::MINB : LargeCfg::MINB) * num_sms();
     if (p.gemv) {
         p.KS = 1;
         p.depth = ((H / 8 + GEMV_QW - 1) / GEMV_QW + 31) / 32 + 3 + 5 + 2 + 2;

@@ -113,3 +113,13 @@ def test_layer_forward_with_routing_options(name):
     w = synth.Workload("rt", T=150, H=256, E=32, K=4, I=128, Is=128, seed=21, x_seed=22)
     opts = dict(OPTS[name], n_group=4, topk_group=2)
     check_layer(Problem(w, opts=opts))
+
+
+@pytest.mark.parametrize("opts", [{}, OPTS["groups_top2"]])
+def test_large_batch_tiles_with_ragged_edges(opts):
+    # the 128-token x 64-expert tile GEMM of batches above 4096 tokens: a partial last
+    # token tile (4300 = 33 x 128 + 76), a partial last expert tile (72 = 64 + 8) and a
+    # K split that does not divide the 15 stages of H = 960
+    w = synth.Workload("large_ragged", T=4300, H=960, E=72 if not opts else 64, K=6,
+                       I=64, Is=0, seed=21, x_seed=22)
+    _check_router(synth.routing_inputs(w), w.K, opts)
