@@ -3,6 +3,7 @@
 // nothing here allocates, frees or synchronises (moe_read_status excepted).
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/moe.h"
 #include "kernels.h"
@@ -51,6 +52,39 @@ unsigned long long g_wait_limit_ns = 1000000000ull;
 int g_inject_stall = 0;
 cudaEvent_t g_stage_events[6] = {};
 bool g_stage_events_on = false;
+int g_shared_side = -1;   // shared expert on the side stream: -1 by batch size, 0 never, 1 always
+
+// Up to this many tokens the router and the dispatch leave most of the GPU idle (their
+// kernels wait on latency, not on SMs or HBM): the shared expert, which needs no routing,
+// then runs beside them on half of the SMs.
+constexpr int kSideMaxTokens = 128;
+
+// A stream of the library per device for the shared expert, forked from and joined back
+// into the caller's stream with two events (capturable: the side stream joins a capture
+// through the fork event).
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    bool tried = false;
+};
+
+SideStream *side_stream()
+{
+    static SideStream tab[64];
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    SideStream &ss = tab[dev];
+    if (!ss.tried) {
+        ss.tried = true;
+        if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
+            ss.s = nullptr;
+    }
+    return ss.s ? &ss : nullptr;
+}
 
 void record_stage(int i, cudaStream_t s)
 {
@@ -152,7 +186,7 @@ struct LayerLayout {
     int32_t *offsets, *perm, *slot_pos;
     void *Xp, *h, *Yp, *hs, *Xq;
     float *Ysh;
-    unsigned *ready;
+    unsigned *ready, *ready_sh;   // readiness counters: the FFN launch, the side launch
     size_t bytes;
 };
 LayerLayout layer_layout(const moe_shape_t &s, unsigned char *ws)
@@ -174,6 +208,8 @@ LayerLayout layer_layout(const moe_shape_t &s, unsigned char *ws)
     L.Ysh = reinterpret_cast<float *>(take(s.I_shared > 0 ? static_cast<size_t>(s.T) * s.H * 4 : 0));
     L.ready = reinterpret_cast<unsigned *>(
         take(ffn_ready_slots(static_cast<long long>(TK) + s.T, s.E + 1) * sizeof(unsigned)));
+    L.ready_sh = reinterpret_cast<unsigned *>(
+        take(s.I_shared > 0 ? ffn_ready_slots(s.T, 1) * sizeof(unsigned) : 0));
     L.bytes = o;
     return L;
 }
@@ -221,28 +257,10 @@ int layer_forward(const moe_shape_t *shape, const moe_weights_t *wt, const moe_w
     if (s.T == 0) return MOE_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int *status = static_cast<int *>(ws);
-
-    record_stage(0, st);
-    cudaError_t e = launch_router(X, W_gate, bias, s.T, s.H, s.E, s.K, topk_idx, topk_w,
-                                  L.r.plan, L.r.scr, status, st, &ro);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    record_stage(1, st);
-    // FP8: the expert FFNs read the token rows quantised in vectors of 128 along H
-    const void *Xin = X;
-    if (fp8) {
-        if ((e = launch_quant_rows(X, s.T, s.H, L.Xq, st)) != cudaSuccess) return MOE_ERR_CUDA;
-        Xin = L.Xq;
-    }
-    // the dispatch tail also zeroes the FFN's readiness counters
-    const size_t n_ready = ffn_ready_slots(static_cast<long long>(s.T) * s.K + s.T, s.E + 1);
-    e = launch_dispatch(Xin, topk_idx, s.T, s.H, s.E, s.K, counts, L.offsets, L.perm, L.slot_pos,
-                        L.Xp, affinity, L.d.plan, L.d.scr, L.ready, n_ready, status, st);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    record_stage(2, st);
+    const void *Xin = X;   // FP8: the token rows quantised in vectors of 128 along H
 
     FfnProblem P[2]{};
     int Ipp[2] = {s.I, s.I_shared};
-    P[0].act = L.Xp;
     P[0].offsets = L.offsets;
     P[0].n_groups = s.E;
     P[0].rows = s.T * s.K;
@@ -256,7 +274,6 @@ int layer_forward(const moe_shape_t *shape, const moe_weights_t *wt, const moe_w
     }
     int n_probs = 1;
     if (s.I_shared > 0) {
-        P[1].act = Xin;
         P[1].offsets = nullptr;
         P[1].n_groups = 1;
         P[1].rows = s.T;
@@ -271,6 +288,41 @@ int layer_forward(const moe_shape_t *shape, const moe_weights_t *wt, const moe_w
         }
         n_probs = 2;
     }
+
+    // shared expert beside the router and the dispatch (bf16 weights, small batches)
+    SideStream *side = nullptr;
+    if (!fp8 && s.I_shared > 0 && (g_shared_side == 1 || (g_shared_side < 0 && s.T <= kSideMaxTokens)))
+        side = side_stream();
+    if (side) {
+        P[1].act = X;
+        if (cudaEventRecord(side->fork, st) != cudaSuccess ||
+            cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (launch_ffn(&P[1], 1, s.H, &Ipp[1], s.T, L.ready_sh, false, status, side->s,
+                       g_wait_limit_ns, g_inject_stall, nullptr, -1, num_sms() / 2) != cudaSuccess ||
+            cudaEventRecord(side->join, side->s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        n_probs = 1;
+    }
+
+    record_stage(0, st);
+    cudaError_t e = launch_router(X, W_gate, bias, s.T, s.H, s.E, s.K, topk_idx, topk_w,
+                                  L.r.plan, L.r.scr, status, st, &ro);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    record_stage(1, st);
+    if (fp8) {
+        if ((e = launch_quant_rows(X, s.T, s.H, L.Xq, st)) != cudaSuccess) return MOE_ERR_CUDA;
+        Xin = L.Xq;
+    }
+    // the dispatch tail also zeroes the FFN's readiness counters
+    const size_t n_ready = ffn_ready_slots(static_cast<long long>(s.T) * s.K + s.T, s.E + 1);
+    e = launch_dispatch(Xin, topk_idx, s.T, s.H, s.E, s.K, counts, L.offsets, L.perm, L.slot_pos,
+                        L.Xp, affinity, L.d.plan, L.d.scr, L.ready, n_ready, status, st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    record_stage(2, st);
+
+    P[0].act = L.Xp;
+    if (s.I_shared > 0 && !side) P[1].act = Xin;
     long long hint = static_cast<long long>(s.T) * s.K / s.E;
     if (hint < 1) hint = 1;
     if (!fp8) {
@@ -290,6 +342,7 @@ int layer_forward(const moe_shape_t *shape, const moe_weights_t *wt, const moe_w
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
     record_stage(4, st);
+    if (side && cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess) return MOE_ERR_CUDA;
     e = launch_combine(L.Yp, L.slot_pos, topk_w, s.I_shared > 0 ? L.Ysh : nullptr, s.T, s.H,
                        s.K, Y, st);
     record_stage(5, st);
@@ -339,6 +392,11 @@ void moe_debug_set_wait_limit(unsigned long long limit_ns, int inject_stall)
 {
     g_wait_limit_ns = limit_ns ? limit_ns : 1000000000ull;
     g_inject_stall = inject_stall;
+}
+
+void moe_debug_set_shared_side(int mode)
+{
+    g_shared_side = mode == 0 || mode == 1 ? mode : -1;
 }
 
 void moe_debug_set_ffn_variant(int variant)

@@ -957,7 +957,7 @@ size_t ffn_ready_slots(long long rows, int n_groups)
 cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I_pp,
                        int token_hint, unsigned *ready, bool ready_zeroed, int *status, cudaStream_t s,
                        unsigned long long timeout_ns, int inject, cudaEvent_t mid_event,
-                       int phase_only)
+                       int phase_only, int max_ctas)
 {
     if (n_probs < 1 || n_probs > 2 || !ready || phase_only < -1 || phase_only > 1)
         return cudaErrorInvalidValue;
@@ -1038,7 +1038,8 @@ cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I
     // launch of the down tiles alone (the up tiles' launch ran first with the last slot)
     a.next_tile = ready + slots - (phase_only == 1 ? 2 : 1);
     const dim3 block(fp8 ? NUM_THREADS_FP8 : NUM_THREADS);
-    const dim3 grid_pair(num_sms() / 2 * 2), grid_one(num_sms());
+    const int n_cta = max_ctas > 0 && max_ctas < num_sms() ? max_ctas : num_sms();
+    const dim3 grid_pair(n_cta / 2 > 0 ? n_cta / 2 * 2 : 2), grid_one(n_cta);
     if (fp8)
         err = pair ? launch_pdl(ffn_kernel<true, true>, grid_pair, block, smem, s, 2, a)
                    : launch_pdl(ffn_kernel<false, true>, grid_one, block, smem, s, 1, a);

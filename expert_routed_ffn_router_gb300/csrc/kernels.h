@@ -134,10 +134,12 @@ void set_ffn_variant(int v);
 // launch.
 // phase_only: -1 both projections; 0 the up projections alone; 1 the down projections alone
 // (after a phase-0 launch of the same problems and the same readiness counters).
+// max_ctas > 0 caps the persistent grid (the rest of the GPU stays free for kernels of
+// other streams); 0 takes one CTA (or CTA pair) per SM.
 cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I_per_prob,
                        int token_hint, unsigned *ready, bool ready_zeroed, int *status, cudaStream_t s,
                        unsigned long long timeout_ns, int inject, cudaEvent_t mid_event,
-                       int phase_only = -1);
+                       int phase_only = -1, int max_ctas = 0);
 
 // Readiness counters launch_ffn needs (unsigned each) for `rows` rows in `n_groups` groups
 // over all its problems.

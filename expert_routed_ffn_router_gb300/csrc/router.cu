@@ -277,6 +277,16 @@ struct Bounds {
     }
 };
 
+// Warp-wide maximum of 64-bit keys: the high words' maximum, then the low words' maximum
+// among the lanes holding it (two hardware reductions instead of five 64-bit shuffles).
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
+{
+    const uint32_t hi = static_cast<uint32_t>(v >> 32), lo = static_cast<uint32_t>(v);
+    const uint32_t mh = __reduce_max_sync(kFullMask, hi);
+    const uint32_t ml = __reduce_max_sync(kFullMask, hi == mh ? lo : 0u);
+    return (static_cast<unsigned long long>(mh) << 32) | ml;
+}
+
 // Compare-and-swap for a descending order of 64-bit keys.
 __device__ __forceinline__ void cas_desc(unsigned long long &a, unsigned long long &b)
 {
@@ -341,12 +351,7 @@ __device__ bool score_select(int E, int K, float nx, const float *nw, const floa
     for (int j = 0; j < K; ++j) {
         // tournament over the lanes' heads (fast path: a lane's keys are kept sorted)
         const unsigned long long head = fast ? key[0] : best;
-        unsigned long long win = head;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const unsigned long long o = __shfl_xor_sync(kFullMask, win, off);
-            win = o > win ? o : win;
-        }
+        const unsigned long long win = warp_max_u64(head);
         const int e = static_cast<int>(~static_cast<uint32_t>(win));
         if (fast) {
             if (head == win) {                 // pop the winner's head
@@ -409,15 +414,6 @@ __device__ __forceinline__ float warp_min_f(float v)
     return v;
 }
 
-__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
-{
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const unsigned long long o = __shfl_xor_sync(kFullMask, v, off);
-        v = o > v ? o : v;
-    }
-    return v;
-}
 
 // The largest two of a sequence (v1 >= v2), for a group's score.
 __device__ __forceinline__ void top2_push(float v, float &v1, float &v2)

@@ -92,7 +92,28 @@ def test_one_expert_takes_every_token():
     assert res["disp"]["counts"][3] == w.T
 
 
-def test_deterministic_and_graph_capture():
+@pytest.mark.parametrize("side", [0, 1])
+def test_deterministic_and_graph_capture(side):
+    # side = 1: the shared expert on the library's side stream, which joins the capture
+    B.moe_debug_set_shared_side(side)
+    try:
+        _deterministic_and_graph_capture()
+    finally:
+        B.moe_debug_set_shared_side(-1)
+
+
+@pytest.mark.parametrize("side", [0, 1])
+@pytest.mark.parametrize("T", [3, 40, 300])
+def test_shared_expert_in_the_routed_launch_or_beside_the_router(side, T):
+    w = synth.Workload("side", T=T, H=256, E=16, K=4, I=128, Is=192, seed=T + 51, x_seed=T + 52)
+    B.moe_debug_set_shared_side(side)
+    try:
+        check_layer(Problem(w))
+    finally:
+        B.moe_debug_set_shared_side(-1)
+
+
+def _deterministic_and_graph_capture():
     p = Problem(synth.workload("tiny", T=77))
     layer = B.MoELayer(p.dev, p.w.T, p.w.K)
     layer.forward(p.X)
