@@ -137,28 +137,39 @@ def ffn_traffic(workload: str):
 
 
 
-def algorithmic(w, n_act: int, wbytes: int = 2):
+def shared_on_side(w, fp8: bool = False) -> bool:
+    """moe_layer_forward runs the shared expert as its own launch on a side stream (bf16
+    weights, up to 128 tokens); otherwise it is a second problem of the routed FFN launch."""
+    return bool(w.Is) and not fp8 and w.T <= 128
+
+
+def algorithmic(w, n_act: int, wbytes: int = 2, side: bool = False):
     """Per-launch algorithmic bytes and FLOPs of each stage (what the method must move or
     compute: the weights of the activated experts, the activations in and out).  wbytes:
-    bytes per expert weight (2 bf16, 1 FP8; the FP8 tile scales add 1 byte per 16384)."""
+    bytes per expert weight (2 bf16, 1 FP8; the FP8 tile scales add 1 byte per 16384).
+    side: the shared expert is its own launch ("ffn_shared"), not part of "ffn"."""
     T, H, E, K, I, Is = w.T, w.H, w.E, w.K, w.I, w.Is
     TK = T * K
+    # weights, token rows in and fp32 outputs of the shared expert
+    sh_bytes = 3 * H * Is * wbytes + T * H * 2 + T * H * 4 if Is else 0
+    sh_flops = 2 * T * 3 * H * Is
     b = {
         "router": E * H * 2 + T * H * 2 + T * K * 8,
         "dispatch": T * H * 2 + TK * H * 2 + T * K * 4 * 3,
         # weights of the activated experts (+ shared), token rows in, outputs out; the
         # intermediate h stays on chip or in L2 between the two projections and is not
         # counted
-        "ffn": (n_act * 3 * H * I + (3 * H * Is if Is else 0)) * wbytes + (TK + T) * H * 2
-               + TK * H * 2 + (T * H * 4 if Is else 0),
+        "ffn": n_act * 3 * H * I * wbytes + TK * H * 2 + TK * H * 2 + (0 if side else sh_bytes),
         "combine": TK * H * 2 + (T * H * 4 if Is else 0) + T * H * 4 + T * K * 8,
     }
     f = {
         "router": 2 * T * E * H,
         "dispatch": 0,
-        "ffn": 2 * (TK * 3 * H * I + T * 3 * H * Is),
+        "ffn": 2 * TK * 3 * H * I + (0 if side else sh_flops),
         "combine": 2 * TK * H,
     }
+    if side:
+        b["ffn_shared"], f["ffn_shared"] = sh_bytes, sh_flops
     layer_bytes = ((n_act + (1 if Is else 0)) * 3 * H * I * wbytes + E * H * 2 + T * H * 2
                    + T * H * 4)
     layer_flops = 2 * T * (K * 3 * H * I + 3 * H * Is) + 2 * T * E * H
@@ -178,7 +189,7 @@ def launches_per_step(w, with_affinity: bool, fp8: bool = False) -> int:
     router = 1 if T <= 4096 else 2
     dispatch = (1 if T <= 256 else 3) + 1
     ffn = 1 if not fp8 else 1 + 2 + (2 if w.Is else 1)
-    side = 1 if (not fp8 and w.Is and T <= 128) else 0
+    side = 1 if shared_on_side(w, fp8) else 0
     return router + dispatch + ffn + side + 1
 
 
@@ -325,7 +336,8 @@ def run_ours(args, rank, world, local_rank):
     rep = B.moe_grace_replicate(counts, plan["group_of"], 8)
     B.moe_grace_route_table(rep, 4)
     ms_plan = (time.perf_counter() - t_plan) * 1e3
-    b, f, layer_bytes, layer_flops = algorithmic(w, n_act, 1 if fp8 else 2)
+    b, f, layer_bytes, layer_flops = algorithmic(w, n_act, 1 if fp8 else 2,
+                                                 shared_on_side(w, fp8))
     dom = max(("ffn", "router", "combine", "dispatch"), key=lambda s: stage_ms[s])
     t_dom = stage_ms[dom] / 1e3
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
@@ -357,7 +369,10 @@ def run_ours(args, rank, world, local_rank):
                    "tokens_per_gpu": w.T, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2: the activated experts' weights "
                          f"({layer_bytes / 1e9:.1f} GB) stream from HBM every step",
-                   "n_active_experts": n_act},
+                   "n_active_experts": n_act,
+                   "shared_expert": ("own FFN launch on a side stream beside the router and "
+                                     "the dispatch" if shared_on_side(w, fp8) else
+                                     "second problem of the routed FFN launch")},
         **({"routing": {"name": args.routing, **opts}} if opts else {}),
         "e2e": {"value": round(total_tokens / (ms_e2e / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(Xh.numel() * Xh.element_size()),
