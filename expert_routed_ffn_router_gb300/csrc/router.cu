@@ -30,7 +30,9 @@
 // fp32 logit tiles on the CUDA cores into the workspace:
 //   tiny batches (T <= 8):     four warps per expert, all tokens at once;
 //   small batches (T <= 4096): 16 tokens x 256 experts per CTA, 4x4 per thread;
-//   large batches:             128 tokens x 128 experts per CTA, 8x8 per thread.
+//   large batches:             128 tokens x 128 experts per CTA, 8x8 per thread on eight
+//                              compute warps, fed through a 4-stage fp32 ring by four
+//                              producer warps (cp.async staging, bf16 -> fp32, norms).
 // Small batches: the last CTA of a token tile (completion counter) sums the split-K
 // partials in a fixed order, scores, selects and writes the outputs -- one launch.
 // Large batches: a second launch finalises, one warp per token, so the selection of
@@ -125,8 +127,13 @@ __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
     f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
 }
 
+// Order of (score, expert): larger score first, then lower expert index.  A NaN score
+// (non-finite inputs) orders below every number, so the order stays total and the lanes of
+// a warp reduction agree on its winner.
 __device__ __forceinline__ bool before64(double a, int ea, double b, int eb)
 {
+    a = a == a ? a : -INFINITY;
+    b = b == b ? b : -INFINITY;
     return a > b || (a == b && ea < eb);
 }
 
@@ -249,16 +256,25 @@ __device__ void select_refined(int *pe, const double *pv, int n, int K, const fl
         }
         if (lane == 0) ord[j] = bp;
         __syncwarp();
-        if (lane == (bp & 31)) pe[bp] = -1 - be;
+        if (bp >= 0 && lane == (bp & 31)) pe[bp] = -1 - be;
         __syncwarp();
     }
+    // (callers pass at least K candidates; a round that found none writes expert 0 with
+    // weight 0 rather than an index outside the list)
+    auto expert_of = [&](int q) { return pe[q] < 0 ? -1 - pe[q] : pe[q]; };
     double den = 0.0;
     for (int j = 0; j < K; ++j) {
-        const int q = ord[j], e = -1 - pe[q];
-        den += pv[q] - static_cast<double>(bias[e]);
+        const int q = ord[j];
+        if (q >= 0) den += pv[q] - static_cast<double>(bias[expert_of(q)]);
     }
     for (int j = lane; j < K; j += 32) {
-        const int q = ord[j], e = -1 - pe[q];
+        const int q = ord[j];
+        if (q < 0) {
+            oi[j] = 0;
+            ow[j] = 0.f;
+            continue;
+        }
+        const int e = expert_of(q);
         oi[j] = e;
         const double sc = pv[q] - static_cast<double>(bias[e]);
         ow[j] = static_cast<float>(renorm ? sc / den : sc);
@@ -527,6 +543,7 @@ __device__ int score_select_general(const RouterArgs &a, float nx, const float *
         kmask = 0u;
         for (int r = 0; r < a.topk_group; ++r) {
             const unsigned long long win = warp_max_u64(key);
+            if (win == 0ull) break;        // (topk_group <= n_group: not reached)
             const int g = static_cast<int>(~static_cast<uint32_t>(win));
             kmask |= 1u << g;
             if (lane == g) key = 0ull;
@@ -682,6 +699,7 @@ __device__ void select_candidates64(const RouterArgs &a, int *pe, double *pv, in
                 const int og = __shfl_xor_sync(kFullMask, bg, off);
                 if (og != INT_MAX && (bg == INT_MAX || before64(os, og, bs, bg))) { bs = os; bg = og; }
             }
+            if (bg == INT_MAX) break;      // no undecided group left
             kept |= 1u << bg;
             if (lane == bg) in = false;
         }
@@ -743,6 +761,7 @@ __device__ void select_general64(const RouterArgs &a, int *pe, double *pv, int32
                 const int og = __shfl_xor_sync(kFullMask, bg, off);
                 if (og != INT_MAX && (bg == INT_MAX || before64(os, og, bs, bg))) { bs = os; bg = og; }
             }
+            if (bg == INT_MAX) break;          // (topk_group <= n_group: not reached)
             kmask |= 1u << bg;
             if (lane == bg) in = false;
         }
@@ -761,6 +780,7 @@ __device__ void select_general64(const RouterArgs &a, int *pe, double *pv, int32
             const int oe = __shfl_xor_sync(kFullMask, be, off);
             if (oe != INT_MAX && (be == INT_MAX || before64(os, oe, bs, be))) { bs = os; be = oe; }
         }
+        if (be == INT_MAX) be = 0;        // (no candidate left: cannot happen for K <= E)
         if (lane == 0) ord[j] = be;
         __syncwarp();
         if (lane == (be & 31)) pe[be] = -1 - be;
@@ -1016,6 +1036,229 @@ __device__ void gemm_tile(const RouterArgs &a, unsigned char *smem)
     for (int r = tid; r < C::TE; r += NT) {
         const float sw = ((rws[r] + rws[C::TE + r]) + rws[2 * C::TE + r]) + rws[3 * C::TE + r];
         if (e0 + r < a.E) a.wsq[(static_cast<size_t>(tt) * a.KS + ks) * a.E + e0 + r] = sw;
+    }
+}
+
+// ------------------------------------------------- warp-specialised tile GEMM (large)
+// The large-batch tile with its operand traffic taken off the compute warps: four producer
+// warps load the bf16 token and gate-row slices of each stage, convert them to fp32 into
+// a ring of WS stages (the same transposed layout) and keep the slices' squared norms; the
+// eight compute warps only run the 32-deep chains (the same operations in the same order
+// as gemm_tile, so the logits and the bound are unchanged).  full[s] / empty[s] mbarriers
+// hand the stages over; every wait is bounded and, on expiry, records
+// MOE_ERR_DEVICE_TIMEOUT and makes both roles leave their loops.
+constexpr int WS = 4;              // fp32 stages in the ring
+constexpr int WSB = 4;             // bf16 stages in the staging ring
+constexpr int NPW = 4;             // producer warps (one per SM sub-partition)
+constexpr int NT_WS = NT + 32 * NPW;   // eight compute warps + the producer warps
+constexpr unsigned long long kWsWaitNs = 1000000000ull;
+
+template <class C>
+__host__ __device__ constexpr size_t ws_smem_bytes()
+{
+    return static_cast<size_t>(WS) * KST * (C::TT + C::TE) * sizeof(float) +
+           static_cast<size_t>(WSB) * KST * (C::TT + C::TE) * 2 + 2 * WS * 8 + 16;
+}
+
+// 16-byte global -> shared copy, zero-filled when !valid (src must still be addressable).
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, bool valid)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+
+template <class C>
+__device__ void gemm_tile_ws(const RouterArgs &a, unsigned char *smem)
+{
+    static_assert(C::X2 && C::TT % (8 * NPW) == 0 && C::TE % (8 * NPW) == 0, "warp-specialised tile");
+    constexpr int PT = 32 * NPW;                                // producer threads
+    constexpr int XI = C::TT * 4 / PT, WI = C::TE * 4 / PT;   // 8-element vectors a thread
+    const int et = blockIdx.x, tt = blockIdx.y, ks = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = tt * C::TT, e0 = et * C::TE;
+    const int s_beg = static_cast<int>(static_cast<long long>(ks) * a.S / a.KS);
+    const int s_end = static_cast<int>(static_cast<long long>(ks + 1) * a.S / a.KS);
+    const int n_st = s_end - s_beg;
+
+    float *xs = reinterpret_cast<float *>(smem);                  // [WS][KST][TT]
+    float *wsm = xs + WS * KST * C::TT;                           // [WS][KST][TE]
+    uint4 *stg = reinterpret_cast<uint4 *>(wsm + WS * KST * C::TE);   // [WSB][XI + WI][PT]
+    uint64_t *full = reinterpret_cast<uint64_t *>(stg + WSB * (XI + WI) * PT);
+    uint64_t *empty = full + WS;
+    int *abort_flag = reinterpret_cast<int *>(empty + WS);
+    if (tid == 0) {
+        for (int s = 0; s < WS; ++s) {
+            mbar_init(&full[s], PT);
+            mbar_init(&empty[s], NW);
+        }
+        *abort_flag = 0;
+    }
+    __syncthreads();
+    volatile int *abort_v = abort_flag;
+
+    float xsq[XI], wsq[WI];
+    constexpr int WY = C::NTY / C::LY;
+    constexpr int LX = 32 / C::LY;
+    const int wtok = (warp % WY) * (C::LY * C::TPT) + 4 * (lane % C::LY);
+    const int wexp = (warp / WY) * (LX * C::EPT) + 4 * (lane / C::LY);
+    auto tok = [&](int i) { return wtok + (i >> 2) * (4 * C::LY) + (i & 3); };
+    auto exq = [&](int j) { return wexp + (j >> 2) * (4 * LX) + (j & 3); };
+    uint64_t accp[C::TPT / 2 * C::EPT];
+
+    const int ptid = tid - NT;   // producer thread index (>= 0 in the producer warps)
+    if (warp >= NW) {
+        // ----------------------------------------------------------- producer warps
+        // vector v = ptid + PT i: row v % TT (consecutive threads, consecutive rows, so the
+        // transposed stores do not conflict), 8-element group v / TT
+#pragma unroll
+        for (int i = 0; i < XI; ++i) xsq[i] = 0.f;
+#pragma unroll
+        for (int i = 0; i < WI; ++i) wsq[i] = 0.f;
+        // raw bf16 slices land in a staging ring by cp.async, WSB - 1 stages ahead; each
+        // thread converts the 16-byte vectors it copied itself
+        auto copy_stage = [&](int n) {
+            if (n < n_st) {
+                const int st = s_beg + n;
+                uint4 *sb = stg + (n % WSB) * (XI + WI) * PT;
+#pragma unroll
+                for (int i = 0; i < XI; ++i) {
+                    const int v = ptid + PT * i, row = t0 + v % C::TT;
+                    const uint4 *src = reinterpret_cast<const uint4 *>(a.X + static_cast<size_t>(row < a.T ? row : 0) * a.H) + st * 4 + v / C::TT;
+                    cp_async16(sb + v, src, row < a.T);
+                }
+#pragma unroll
+                for (int i = 0; i < WI; ++i) {
+                    const int v = ptid + PT * i, row = e0 + v % C::TE;
+                    const uint4 *src = reinterpret_cast<const uint4 *>(a.Wg + static_cast<size_t>(row < a.E ? row : 0) * a.H) + st * 4 + v / C::TE;
+                    cp_async16(sb + XI * PT + v, src, row < a.E);
+                }
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+#pragma unroll
+        for (int n = 0; n < WSB - 1; ++n) copy_stage(n);
+        for (int n = 0; n < n_st; ++n) {
+            const int slot = n % WS;
+            copy_stage(n + WSB - 1);
+            asm volatile("cp.async.wait_group %0;" ::"n"(WSB - 1) : "memory");
+            // (warp-uniform: a lane that gave up takes the whole warp out of the loop)
+            if (n >= WS && !__all_sync(kFullMask, mbar_wait(&empty[slot], ((n / WS) - 1) & 1, abort_v,
+                                                             a.status, kWsWaitNs)))
+                break;
+            const uint4 *sb = stg + (n % WSB) * (XI + WI) * PT;
+            float *xd = xs + slot * KST * C::TT;
+            float *wd = wsm + slot * KST * C::TE;
+#pragma unroll
+            for (int i = 0; i < XI; ++i) {
+                const int v = ptid + PT * i;
+                float f[8];
+                unpack8(sb[v], f);
+                float *d = xd + ((v / C::TT) * 8) * C::TT + v % C::TT;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) { d[e * C::TT] = f[e]; xsq[i] = fmaf(f[e], f[e], xsq[i]); }
+            }
+#pragma unroll
+            for (int i = 0; i < WI; ++i) {
+                const int v = ptid + PT * i;
+                float f[8];
+                unpack8(sb[XI * PT + v], f);
+                float *d = wd + ((v / C::TE) * 8) * C::TE + v % C::TE;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) { d[e * C::TE] = f[e]; wsq[i] = fmaf(f[e], f[e], wsq[i]); }
+            }
+            mbar_arrive(&full[slot]);
+        }
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+    } else {
+        // ------------------------------------------------------------ compute warps
+#pragma unroll
+        for (int q = 0; q < C::TPT / 2 * C::EPT; ++q) accp[q] = 0ull;
+        for (int n = 0; n < n_st; ++n) {
+            const int slot = n % WS;
+            if (!__all_sync(kFullMask, mbar_wait(&full[slot], (n / WS) & 1, abort_v, a.status, kWsWaitNs)))
+                break;
+            const float *xb = xs + slot * KST * C::TT + wtok;
+            const float *wb = wsm + slot * KST * C::TE + wexp;
+            // pair pp * EPT + jj = (token 2pp, token 2pp + 1) x expert jj
+            uint64_t pin[C::TPT / 2 * C::EPT];
+#pragma unroll
+            for (int q = 0; q < C::TPT / 2 * C::EPT; ++q) pin[q] = 0ull;
+#pragma unroll 4
+            for (int kk = 0; kk < KST; ++kk) {
+                ulonglong2 xv[C::TPT / 4];
+#pragma unroll
+                for (int i4 = 0; i4 < C::TPT / 4; ++i4)
+                    xv[i4] = *reinterpret_cast<const ulonglong2 *>(xb + kk * C::TT + 4 * C::LY * i4);
+                uint64_t wp[C::EPT];
+#pragma unroll
+                for (int g = 0; g < C::EPT / 4; ++g) {
+                    const float4 wv = *reinterpret_cast<const float4 *>(wb + kk * C::TE + 4 * LX * g);
+                    wp[4 * g] = dup_x2(wv.x);
+                    wp[4 * g + 1] = dup_x2(wv.y);
+                    wp[4 * g + 2] = dup_x2(wv.z);
+                    wp[4 * g + 3] = dup_x2(wv.w);
+                }
+#pragma unroll
+                for (int pp = 0; pp < C::TPT / 2; ++pp) {
+                    const uint64_t xp = (pp & 1) ? xv[pp >> 1].y : xv[pp >> 1].x;
+#pragma unroll
+                    for (int jj = 0; jj < C::EPT; ++jj)
+                        pin[pp * C::EPT + jj] = fma_x2(xp, wp[jj], pin[pp * C::EPT + jj]);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < C::TPT / 2 * C::EPT; ++q) accp[q] = add_x2(accp[q], pin[q]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+    }
+    __syncthreads();
+
+    if (warp < NW) {
+        float *part_t = a.part + static_cast<size_t>(ks) * a.T * a.E;
+#pragma unroll
+        for (int pp = 0; pp < C::TPT / 2; ++pp) {
+            const int tA = t0 + tok(2 * pp), tB = t0 + tok(2 * pp + 1);
+#pragma unroll
+            for (int g = 0; g < C::EPT / 4; ++g) {
+                const int e = e0 + exq(4 * g);
+                float lo[4], hi[4];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo[jj]), "=f"(hi[jj]) : "l"(accp[pp * C::EPT + 4 * g + jj]));
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int t = h ? tB : tA;
+                    const float *v = h ? hi : lo;
+                    if (t >= a.T) continue;
+                    float *dst = part_t + static_cast<size_t>(t) * a.E;
+                    if ((a.E & 3) == 0 && e + 3 < a.E) {
+                        *reinterpret_cast<float4 *>(dst + e) = make_float4(v[0], v[1], v[2], v[3]);
+                    } else {
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj)
+                            if (e + jj < a.E) dst[e + jj] = v[jj];
+                    }
+                }
+            }
+        }
+    } else {
+        // squared norms of this slice, reduced over the four 8-element groups of a row
+        float *rxs = xs;                   // [4][TT]
+        float *rws = xs + 4 * C::TT;       // [4][TE]
+#pragma unroll
+        for (int i = 0; i < XI; ++i) rxs[ptid + PT * i] = xsq[i];
+#pragma unroll
+        for (int i = 0; i < WI; ++i) rws[ptid + PT * i] = wsq[i];
+        asm volatile("bar.sync 1, %0;" ::"n"(PT) : "memory");   // the producer warps only
+        for (int r = ptid; r < C::TT; r += PT) {
+            const float sx = ((rxs[r] + rxs[C::TT + r]) + rxs[2 * C::TT + r]) + rxs[3 * C::TT + r];
+            if (et == 0 && t0 + r < a.T) a.xsq[static_cast<size_t>(ks) * a.T + t0 + r] = sx;
+        }
+        for (int r = ptid; r < C::TE; r += PT) {
+            const float sw = ((rws[r] + rws[C::TE + r]) + rws[2 * C::TE + r]) + rws[3 * C::TE + r];
+            if (e0 + r < a.E) a.wsq[(static_cast<size_t>(tt) * a.KS + ks) * a.E + e0 + r] = sw;
+        }
     }
 }
 
@@ -1340,6 +1583,11 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
                                     oi, ow, cand, n_cand, lane)) {
                 continue;
             }
+            if (!every && n_cand < a.K) {   // non-finite scores: re-score every expert
+                every = true;
+                cand = all_experts(E, lane);
+                n_cand = E;
+            }
             // not certified: queue the candidates for the CTA-wide double-word refine
             int base = 0;
             if (lane == 0) base = atomicAdd(&s_npairs, n_cand);
@@ -1401,7 +1649,7 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
                                 a.topk_idx + static_cast<size_t>(t) * a.K,
                                 a.topk_w + static_cast<size_t>(t) * a.K, S.ord, lane);
         else
-            select_refined(S.p_e + first, S.p_val + first, cnt, a.K, a.bias,
+            select_refined(S.p_e + first, S.p_val + first, cnt < 0 ? -cnt : cnt, a.K, a.bias,
                            a.topk_idx + static_cast<size_t>(t) * a.K,
                            a.topk_w + static_cast<size_t>(t) * a.K, S.ord, lane);
     }
@@ -1409,11 +1657,11 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
 
 // ------------------------------------------- GEMM-only kernel + finaliser (large batches)
 template <class C>
-__global__ void __launch_bounds__(NT, C::MINB) router_gemm_kernel(const RouterArgs a)
+__global__ void __launch_bounds__(NT_WS, 1) router_gemm_kernel(const RouterArgs a)
 {
     pdl_wait();
     extern __shared__ __align__(16) unsigned char smem[];
-    gemm_tile<C>(a, smem);
+    gemm_tile_ws<C>(a, smem);
 }
 
 // One warp per token: split-K sum, scoring, certified top-K, refine when needed.  The
@@ -1489,7 +1737,11 @@ __global__ void __launch_bounds__(NT) router_finalize_kernel(const RouterArgs a,
     } else if (score_select(E, a.K, nx, w_nw, a.bias, bd.gam, w_sel, w_bnd, w_sc, oi, ow, cand,
                             n_cand, lane)) {
         return;
-    } else if (refine_overlapping(a, t, cand, w_sel, w_bnd, ce, s64, ord, lane)) {
+    }
+    if (!every && n_cand < a.K) {           // non-finite scores: re-score every expert
+        every = true;
+        cand = all_experts(E, lane);
+    } else if (!a.variant && refine_overlapping(a, t, cand, w_sel, w_bnd, ce, s64, ord, lane)) {
         return;
     }
     refine_token_warp(a, t, cand, ce, s64, ord, lane, every, ck, ug);
@@ -1543,8 +1795,7 @@ RouterPlan router_plan(int T, int H, int E)
     p.xsq_bytes = al(static_cast<size_t>(p.KS) * T * sizeof(float));
     p.wsq_bytes = al(static_cast<size_t>(p.nTT) * p.KS * E * sizeof(float));
     p.cnt_bytes = al(static_cast<size_t>(p.nTT) * sizeof(unsigned));
-    p.smem_bytes = small ? fused_smem(p.TT, p.TE, E, p.max_pairs)
-                         : 2 * KST * static_cast<size_t>(p.TT + p.TE) * sizeof(float) + 16;
+    p.smem_bytes = small ? fused_smem(p.TT, p.TE, E, p.max_pairs) : ws_smem_bytes<LargeCfg>();
     return p;
 }
 
@@ -1594,7 +1845,7 @@ cudaError_t launch_router(const void *X, const void *Wg, const float *bias, int 
     }
     err = ensure_smem(reinterpret_cast<const void *>(router_gemm_kernel<LargeCfg>), plan.smem_bytes);
     if (err != cudaSuccess) return err;
-    if ((err = launch_pdl(router_gemm_kernel<LargeCfg>, grid, dim3(NT), plan.smem_bytes, s, 1, a)) != cudaSuccess)
+    if ((err = launch_pdl(router_gemm_kernel<LargeCfg>, grid, dim3(NT_WS), plan.smem_bytes, s, 1, a)) != cudaSuccess)
         return err;
     const size_t fs = finalize_smem(E);
     err = ensure_smem(reinterpret_cast<const void *>(router_finalize_kernel), fs);

@@ -123,3 +123,25 @@ def test_large_batch_tiles_with_ragged_edges(opts):
     w = synth.Workload("large_ragged", T=4300, H=960, E=72 if not opts else 64, K=6,
                        I=64, Is=0, seed=21, x_seed=22)
     _check_router(synth.routing_inputs(w), w.K, opts)
+
+
+@pytest.mark.parametrize("opts", [{}, OPTS["groups_top2"]])
+@pytest.mark.parametrize("T", [5, 40, 4200])
+def test_non_finite_scores_still_give_valid_indices(opts, T):
+    # rows of X with a NaN, an infinity, or magnitudes whose fp32 products overflow: the
+    # exact top-k is undefined there, but the router must still write K distinct in-range
+    # experts per token (the certified selection falls back to re-scoring every expert)
+    w = synth.workload("decode", T=T, x_seed=T + 17)
+    r = synth.routing_inputs(w)
+    big = synth.f32_to_bf16_bits(np.full(w.H, 3.0e38, dtype=np.float32))
+    r["X"][0, 5] = synth.f32_to_bf16_bits(np.array([np.nan], dtype=np.float32))[0]
+    r["X"][1, 7] = synth.f32_to_bf16_bits(np.array([np.inf], dtype=np.float32))[0]
+    r["X"][T - 1] = big
+    idx, wt = _run_router(r, w.K, opts)
+    assert idx.min() >= 0 and idx.max() < w.E
+    assert all(len(set(row)) == w.K for row in idx.tolist())
+    # the finite rows are unaffected
+    ok = np.ones(T, bool)
+    ok[[0, 1, T - 1]] = False
+    idx_o, w_o = oracle.router_ex(r["X"][ok], r["W_gate"], r["bias"], w.K, **opts)
+    assert np.array_equal(idx[ok], idx_o)
