@@ -1070,9 +1070,11 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, bool vali
 template <class C>
 __device__ void gemm_tile_ws(const RouterArgs &a, unsigned char *smem)
 {
-    static_assert(C::X2 && C::TT % (8 * NPW) == 0 && C::TE % (8 * NPW) == 0, "warp-specialised tile");
     constexpr int PT = 32 * NPW;                                // producer threads
-    constexpr int XI = C::TT * 4 / PT, WI = C::TE * 4 / PT;   // 8-element vectors a thread
+    // producer units: 4 consecutive rows x one 8-element group of a stage
+    static_assert(C::X2 && C::TT % PT == 0 && C::TE % PT == 0, "warp-specialised tile");
+    constexpr int XU = C::TT / PT, WU = C::TE / PT;            // units a producer thread
+    constexpr int XI = 4 * XU, WI = 4 * WU;                     // 16-byte vectors a thread
     const int et = blockIdx.x, tt = blockIdx.y, ks = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t0 = tt * C::TT, e0 = et * C::TE;
@@ -1096,7 +1098,7 @@ __device__ void gemm_tile_ws(const RouterArgs &a, unsigned char *smem)
     __syncthreads();
     volatile int *abort_v = abort_flag;
 
-    float xsq[XI], wsq[WI];
+    float xsq[XI], wsq[WI];        // producer: squared norms of (row, group) slices
     constexpr int WY = C::NTY / C::LY;
     constexpr int LX = 32 / C::LY;
     const int wtok = (warp % WY) * (C::LY * C::TPT) + 4 * (lane % C::LY);
@@ -1108,8 +1110,9 @@ __device__ void gemm_tile_ws(const RouterArgs &a, unsigned char *smem)
     const int ptid = tid - NT;   // producer thread index (>= 0 in the producer warps)
     if (warp >= NW) {
         // ----------------------------------------------------------- producer warps
-        // vector v = ptid + PT i: row v % TT (consecutive threads, consecutive rows, so the
-        // transposed stores do not conflict), 8-element group v / TT
+        // unit u = ptid + PT i: rows 4 (u % (TT / 4)) ..+3, 8-element group u / (TT / 4);
+        // consecutive threads take consecutive row quads, so the 16-byte transposed stores
+        // (four rows at one k) of a warp cover one contiguous span
 #pragma unroll
         for (int i = 0; i < XI; ++i) xsq[i] = 0.f;
 #pragma unroll
@@ -1121,19 +1124,39 @@ __device__ void gemm_tile_ws(const RouterArgs &a, unsigned char *smem)
                 const int st = s_beg + n;
                 uint4 *sb = stg + (n % WSB) * (XI + WI) * PT;
 #pragma unroll
-                for (int i = 0; i < XI; ++i) {
-                    const int v = ptid + PT * i, row = t0 + v % C::TT;
-                    const uint4 *src = reinterpret_cast<const uint4 *>(a.X + static_cast<size_t>(row < a.T ? row : 0) * a.H) + st * 4 + v / C::TT;
-                    cp_async16(sb + v, src, row < a.T);
+                for (int i = 0; i < XU; ++i) {
+                    const int u = ptid + PT * i, r0 = 4 * (u % (C::TT / 4)), g = u / (C::TT / 4);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int row = t0 + r0 + q;
+                        const uint4 *src = reinterpret_cast<const uint4 *>(a.X + static_cast<size_t>(row < a.T ? row : 0) * a.H) + st * 4 + g;
+                        cp_async16(sb + (4 * i + q) * PT + ptid, src, row < a.T);
+                    }
                 }
 #pragma unroll
-                for (int i = 0; i < WI; ++i) {
-                    const int v = ptid + PT * i, row = e0 + v % C::TE;
-                    const uint4 *src = reinterpret_cast<const uint4 *>(a.Wg + static_cast<size_t>(row < a.E ? row : 0) * a.H) + st * 4 + v / C::TE;
-                    cp_async16(sb + XI * PT + v, src, row < a.E);
+                for (int i = 0; i < WU; ++i) {
+                    const int u = ptid + PT * i, r0 = 4 * (u % (C::TE / 4)), g = u / (C::TE / 4);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int row = e0 + r0 + q;
+                        const uint4 *src = reinterpret_cast<const uint4 *>(a.Wg + static_cast<size_t>(row < a.E ? row : 0) * a.H) + st * 4 + g;
+                        cp_async16(sb + (XI + 4 * i + q) * PT + ptid, src, row < a.E);
+                    }
                 }
             }
             asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        // four rows of one group -> eight 16-byte stores (one per k) and the rows' norms
+        auto convert = [&](const uint4 *sv, float *dst, int ld, float *nrm) {
+            float f[4][8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) unpack8(sv[q * PT], f[q]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                *reinterpret_cast<float4 *>(dst + k * ld) = make_float4(f[0][k], f[1][k], f[2][k], f[3][k]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) nrm[q] = fmaf(f[q][k], f[q][k], nrm[q]);
+            }
         };
 #pragma unroll
         for (int n = 0; n < WSB - 1; ++n) copy_stage(n);
@@ -1145,26 +1168,18 @@ __device__ void gemm_tile_ws(const RouterArgs &a, unsigned char *smem)
             if (n >= WS && !__all_sync(kFullMask, mbar_wait(&empty[slot], ((n / WS) - 1) & 1, abort_v,
                                                              a.status, kWsWaitNs)))
                 break;
-            const uint4 *sb = stg + (n % WSB) * (XI + WI) * PT;
+            const uint4 *sb = stg + (n % WSB) * (XI + WI) * PT + ptid;
             float *xd = xs + slot * KST * C::TT;
             float *wd = wsm + slot * KST * C::TE;
 #pragma unroll
-            for (int i = 0; i < XI; ++i) {
-                const int v = ptid + PT * i;
-                float f[8];
-                unpack8(sb[v], f);
-                float *d = xd + ((v / C::TT) * 8) * C::TT + v % C::TT;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) { d[e * C::TT] = f[e]; xsq[i] = fmaf(f[e], f[e], xsq[i]); }
+            for (int i = 0; i < XU; ++i) {
+                const int u = ptid + PT * i, r0 = 4 * (u % (C::TT / 4)), g = u / (C::TT / 4);
+                convert(sb + 4 * i * PT, xd + g * 8 * C::TT + r0, C::TT, xsq + 4 * i);
             }
 #pragma unroll
-            for (int i = 0; i < WI; ++i) {
-                const int v = ptid + PT * i;
-                float f[8];
-                unpack8(sb[XI * PT + v], f);
-                float *d = wd + ((v / C::TE) * 8) * C::TE + v % C::TE;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) { d[e * C::TE] = f[e]; wsq[i] = fmaf(f[e], f[e], wsq[i]); }
+            for (int i = 0; i < WU; ++i) {
+                const int u = ptid + PT * i, r0 = 4 * (u % (C::TE / 4)), g = u / (C::TE / 4);
+                convert(sb + (XI + 4 * i) * PT, wd + g * 8 * C::TE + r0, C::TE, wsq + 4 * i);
             }
             mbar_arrive(&full[slot]);
         }
@@ -1247,9 +1262,17 @@ __device__ void gemm_tile_ws(const RouterArgs &a, unsigned char *smem)
         float *rxs = xs;                   // [4][TT]
         float *rws = xs + 4 * C::TT;       // [4][TE]
 #pragma unroll
-        for (int i = 0; i < XI; ++i) rxs[ptid + PT * i] = xsq[i];
+        for (int i = 0; i < XU; ++i) {
+            const int u = ptid + PT * i, r0 = 4 * (u % (C::TT / 4)), g = u / (C::TT / 4);
 #pragma unroll
-        for (int i = 0; i < WI; ++i) rws[ptid + PT * i] = wsq[i];
+            for (int q = 0; q < 4; ++q) rxs[g * C::TT + r0 + q] = xsq[4 * i + q];
+        }
+#pragma unroll
+        for (int i = 0; i < WU; ++i) {
+            const int u = ptid + PT * i, r0 = 4 * (u % (C::TE / 4)), g = u / (C::TE / 4);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) rws[g * C::TE + r0 + q] = wsq[4 * i + q];
+        }
         asm volatile("bar.sync 1, %0;" ::"n"(PT) : "memory");   // the producer warps only
         for (int r = ptid; r < C::TT; r += PT) {
             const float sx = ((rxs[r] + rxs[C::TT + r]) + rxs[2 * C::TT + r]) + rxs[3 * C::TT + r];
