@@ -3,7 +3,6 @@
 // nothing here allocates, frees or synchronises (moe_read_status excepted).
 #include <cstdint>
 #include <cstring>
-#include <mutex>
 
 #include "../../include/moe.h"
 #include "kernels.h"
@@ -59,9 +58,11 @@ int g_shared_side = -1;   // shared expert on the side stream: -1 by batch size,
 // then runs beside them on half of the SMs.
 constexpr int kSideMaxTokens = 128;
 
-// A stream of the library per device for the shared expert, forked from and joined back
-// into the caller's stream with two events (capturable: the side stream joins a capture
-// through the fork event).
+// A stream of the library for the shared expert, forked from and joined back into the
+// caller's stream with two events (capturable: the side stream joins a capture through the
+// fork event).  One per host thread and device, created on first use and kept for the
+// process: calls from different threads (on different workspaces) never share the events,
+// and the calls of one thread are sequential.
 struct SideStream {
     cudaStream_t s = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
@@ -70,11 +71,9 @@ struct SideStream {
 
 SideStream *side_stream()
 {
-    static SideStream tab[64];
-    static std::mutex mu;
+    thread_local SideStream tab[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
     SideStream &ss = tab[dev];
     if (!ss.tried) {
         ss.tried = true;

@@ -27,7 +27,11 @@
  *   - Row-major layouts; "bf16" arrays hold IEEE bfloat16 values (2 bytes each).
  *   - `stream` is a cudaStream_t (0 = legacy default stream).  All work is enqueued on it;
  *     no call synchronises the host, allocates or frees memory, so calls can be captured
- *     in a CUDA graph.  Outputs are valid once the stream reaches them.
+ *     in a CUDA graph.  Outputs are valid once the stream reaches them.  (One exception,
+ *     moe_layer_forward on bf16 weights up to 128 tokens: it forks the shared expert onto a
+ *     side stream of the library and joins it back before the combine; that stream and
+ *     its two events are created by the first such call of a host thread on a device and
+ *     kept for the process.)
  *   - `ws` is a caller-owned device workspace of at least moe_workspace_bytes() bytes
  *     (256-byte aligned).  Its first 4 bytes are the status word: zero them once after
  *     allocating (e.g. cudaMemset); moe_read_status() resets the word after reading it.
@@ -259,6 +263,8 @@ int moe_combine(const void *Yp, const int32_t *slot_pos, const float *topk_w,
                 const float *Ysh, int T, int H, int K, float *Y, void *stream);
 
 /* Whole layer: router -> dispatch -> grouped expert FFN and shared expert -> combine.
+ * Up to 128 tokens on bf16 weights the shared expert runs on the library's side stream
+ * beside the router and the dispatch (joined back into `stream` before the combine).
  *   X bf16 [T, H]; out Y fp32 [T, H]
  *   out topk_idx int32 [T, K], topk_w fp32 [T, K], counts int32 [E] (required)
  *   out affinity int32 [E, E] (nullable: skipped when NULL)

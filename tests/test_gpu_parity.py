@@ -113,6 +113,42 @@ def test_shared_expert_in_the_routed_launch_or_beside_the_router(side, T):
         B.moe_debug_set_shared_side(-1)
 
 
+def test_concurrent_calls_from_two_host_threads():
+    # two host threads, each with its own layer (workspace) and stream, run the layer at the
+    # same time; each thread's shared expert takes its own side stream, so the results are
+    # those of the calls run one after the other
+    import threading
+    p = Problem(synth.workload("tiny", T=40))
+    layers = [B.MoELayer(p.dev, p.w.T, p.w.K) for _ in range(2)]
+    Xs = [p.X, p.X.flip(0).contiguous()]
+    ref = []
+    for layer, X in zip(layers, Xs):
+        layer.forward(X)
+        torch.cuda.synchronize()
+        ref.append(layer.Y.clone())
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    errors = []
+
+    def run(i):
+        try:
+            torch.cuda.set_device(0)
+            for _ in range(50):
+                layers[i].forward(Xs[i], stream=streams[i])
+        except Exception as exc:          # reported below, on the main thread
+            errors.append(exc)
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for layer, r in zip(layers, ref):
+        assert torch.equal(layer.Y, r)
+        assert layer.status() == 0
+
+
 def _deterministic_and_graph_capture():
     p = Problem(synth.workload("tiny", T=77))
     layer = B.MoELayer(p.dev, p.w.T, p.w.K)
