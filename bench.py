@@ -178,16 +178,17 @@ def algorithmic(w, n_act: int, wbytes: int = 2, side: bool = False):
 
 def launches_per_step(w, with_affinity: bool, fp8: bool = False) -> int:
     """Kernels moe_layer_forward launches: router (1 fused, or GEMM + finalise for
-    T > 4096), dispatch (one bookkeeping CTA for T <= 256, else masks, scan, scatter;
-    then one launch for the affinity matrix, the row gather and the zeroing of the FFN's
-    counters), the FFN (up and down projections in one persistent launch), combine.  On
+    T > 4096), dispatch (for T <= 256 one launch whose CTAs each form the bookkeeping and
+    then compute the affinity matrix, gather the rows and zero the FFN's counters; else
+    masks, scan, scatter and one launch for the affinity, the gather and the zeroing), the
+    FFN (up and down projections in one persistent launch), combine.  On
     bf16 weights up to 128 tokens the shared expert is a second FFN launch, on a side
     stream beside the router and the dispatch.  FP8 experts add the token-row
     quantisation, split the FFN into its up and down launches and quantise h (and the
     shared expert's h) between them."""
     T = w.T
     router = 1 if T <= 4096 else 2
-    dispatch = (1 if T <= 256 else 3) + 1
+    dispatch = 1 if T <= 256 else 4
     ffn = 1 if not fp8 else 1 + 2 + (2 if w.Is else 1)
     side = 1 if shared_on_side(w, fp8) else 0
     return router + dispatch + ffn + side + 1

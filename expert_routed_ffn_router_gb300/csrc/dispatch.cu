@@ -261,20 +261,16 @@ __global__ void __launch_bounds__(256) tail_kernel(const uint32_t *__restrict__ 
     }
 }
 
-// Small batches (T <= 256, one chunk): masks, counts, scan and stable slots in one CTA --
-// the same popcount formulation as the multi-CTA kernels above.  The masks are also
-// written out for the affinity kernel.
-__global__ void __launch_bounds__(CHUNK) route_small_kernel(const int32_t *__restrict__ idx, int T,
-                                                            int E, int K, int32_t *counts,
-                                                            int32_t *offsets, int32_t *perm,
-                                                            int32_t *slot_pos, uint32_t *smask,
-                                                            int *status)
+// Small batches (T <= 256, one chunk): masks, counts, scan and stable slots of the whole
+// batch in one CTA's shared memory -- the same popcount formulation as the multi-CTA
+// kernels above.  m_s [CW][E] masks, off [E + 1] exclusive offsets (off[E] = rows),
+// perm_s [T K] the token of every row.  With `out` the CTA also writes counts, offsets,
+// perm, slot_pos and the masks to global memory.
+__device__ void small_routing(const int32_t *__restrict__ idx, int T, int E, int K, uint32_t *m_s,
+                              int32_t *base, int32_t *off, int32_t *perm_s, bool out,
+                              int32_t *counts, int32_t *offsets, int32_t *perm,
+                              int32_t *slot_pos, uint32_t *smask, int *status)
 {
-    pdl_wait();
-    extern __shared__ uint32_t sm[];
-    uint32_t *m_s = sm;                                          // [CW][E]
-    int32_t *base = reinterpret_cast<int32_t *>(sm + CW * E);    // [CW][E]
-    int32_t *off = base + CW * E;                                // [E + 1]
     __shared__ int warp_tot[CHUNK / 32];
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     for (int i = tid; i < CW * E; i += CHUNK) m_s[i] = 0u;
@@ -291,7 +287,8 @@ __global__ void __launch_bounds__(CHUNK) route_small_kernel(const int32_t *__res
     }
     __syncthreads();
     const int rows = (T + 31) / 32;
-    for (int i = tid; i < rows * E; i += CHUNK) smask[i] = m_s[i];
+    if (out)
+        for (int i = tid; i < rows * E; i += CHUNK) smask[i] = m_s[i];
     // counts and an exclusive scan over experts: thread tid owns experts [tid*per, +per)
     const int per = (E + CHUNK - 1) / CHUNK;
     int local = 0;
@@ -318,12 +315,17 @@ __global__ void __launch_bounds__(CHUNK) route_small_kernel(const int32_t *__res
         const int e = tid * per + q;
         if (e >= E) break;
         const int n = off[e];
-        counts[e] = n;
-        offsets[e] = run;
+        if (out) {
+            counts[e] = n;
+            offsets[e] = run;
+        }
         off[e] = run;
         run += n;
     }
-    if (tid == CHUNK - 1) { offsets[E] = run; }
+    if (tid == CHUNK - 1) {
+        off[E] = run;
+        if (out) offsets[E] = run;
+    }
     __syncthreads();
     // per 32-token row bases, then the stable slot of every (token, j)
     for (int e = tid; e < E; e += CHUNK) {
@@ -340,10 +342,42 @@ __global__ void __launch_bounds__(CHUNK) route_small_kernel(const int32_t *__res
             const int e = idx[static_cast<size_t>(tid) * K + j];
             if (e < 0 || e >= E) continue;
             const int r = base[w * E + e] + __popc(m_s[w * E + e] & below);
-            slot_pos[static_cast<size_t>(tid) * K + j] = r;
-            perm[r] = tid;
+            perm_s[r] = tid;
+            if (out) {
+                slot_pos[static_cast<size_t>(tid) * K + j] = r;
+                perm[r] = tid;
+            }
         }
     }
+    __syncthreads();
+}
+
+// The whole dispatch of a small batch in one launch: every CTA forms the bookkeeping in its
+// own shared memory (at most 256 x K entries), CTA 0 writes it out, the first n_aff CTAs
+// then compute 32x32 affinity tiles from their masks and the others gather the permuted
+// rows (from their own copy of perm) and zero the FFN's readiness counters.
+__global__ void __launch_bounds__(CHUNK) small_dispatch_kernel(
+    const int32_t *__restrict__ idx, int T, int E, int K, int32_t *counts, int32_t *offsets,
+    int32_t *perm, int32_t *slot_pos, uint32_t *smask, int *status, int32_t *aff, int n_aff_x,
+    int n_aff, const uint4 *__restrict__ X, int H, uint4 *__restrict__ Xp, unsigned *zero_buf,
+    int zero_n)
+{
+    pdl_wait();
+    extern __shared__ uint32_t sm[];
+    uint32_t *m_s = sm;                                          // [CW][E]
+    int32_t *base = reinterpret_cast<int32_t *>(sm + CW * E);    // [CW][E]
+    int32_t *off = base + CW * E;                                // [E + 1]
+    int32_t *perm_s = off + E + 1;                               // [T K]
+    const int b = static_cast<int>(blockIdx.x);
+    small_routing(idx, T, E, K, m_s, base, off, perm_s, b == 0, counts, offsets, perm, slot_pos,
+                  smask, status);
+    if (b < n_aff) {
+        affinity_tile(m_s, (T + 31) / 32, E, aff, b / n_aff_x, b % n_aff_x);
+        return;
+    }
+    const int gb = b - n_aff, ngb = static_cast<int>(gridDim.x) - n_aff;
+    for (int i = gb * blockDim.x + threadIdx.x; i < zero_n; i += ngb * blockDim.x) zero_buf[i] = 0u;
+    if (Xp) gather_rows(X, H, perm_s, off, E, Xp, gb, ngb);
 }
 
 }  // namespace
@@ -368,33 +402,39 @@ cudaError_t launch_dispatch(const void *X, const int32_t *topk_idx, int T, int H
 {
     const size_t m_smem = static_cast<size_t>(CW) * E * sizeof(uint32_t);
     cudaError_t err;
-    if (T <= CHUNK) {
-        const size_t sm = 2 * m_smem + (E + 1) * sizeof(int32_t);
-        err = ensure_smem(reinterpret_cast<const void *>(route_small_kernel), sm);
-        if (err != cudaSuccess) return err;
-        if ((err = launch_pdl(route_small_kernel, dim3(1), dim3(CHUNK), sm, s, 1, topk_idx, T, E, K,
-                              counts, offsets, perm, slot_pos, scr.smask, status)) != cudaSuccess)
-            return err;
-    } else {
-        err = ensure_smem(reinterpret_cast<const void *>(masks_kernel), m_smem);
-        if (err != cudaSuccess) return err;
-        err = ensure_smem(reinterpret_cast<const void *>(scatter_kernel), 2 * m_smem);
-        if (err != cudaSuccess) return err;
-        if ((err = launch_pdl(masks_kernel, dim3(plan.n_chunks), dim3(CHUNK), m_smem, s, 1, topk_idx, T,
-                              E, K, scr.smask, scr.chunk_cnt, status)) != cudaSuccess)
-            return err;
-        if ((err = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, s, 1, E, plan.n_chunks,
-                              static_cast<const int32_t *>(scr.chunk_cnt), scr.chunk_base, counts,
-                              offsets)) != cudaSuccess)
-            return err;
-        if ((err = launch_pdl(scatter_kernel, dim3(plan.n_chunks), dim3(CHUNK), 2 * m_smem, s, 1,
-                              topk_idx, T, E, K, static_cast<const uint32_t *>(scr.smask),
-                              static_cast<const int32_t *>(scr.chunk_base), perm, slot_pos)) != cudaSuccess)
-            return err;
-    }
-    // affinity tiles, row gather and counter zeroing: one launch
     const int n_aff_x = (E + 31) / 32;
     const int n_aff = affinity ? n_aff_x * n_aff_x : 0;
+    if (T <= CHUNK) {
+        // one launch: bookkeeping in every CTA, affinity tiles, row gather, counter zeroing
+        long long gblocks = Xp ? (static_cast<long long>(T) * K + 7) / 8 : 1;
+        const long long cap = static_cast<long long>(num_sms()) * 8;
+        if (gblocks > cap) gblocks = cap;
+        if (gblocks < 1) gblocks = 1;
+        const size_t sm = 2 * m_smem + (E + 1 + static_cast<size_t>(T) * K) * sizeof(int32_t);
+        err = ensure_smem(reinterpret_cast<const void *>(small_dispatch_kernel), sm);
+        if (err != cudaSuccess) return err;
+        return launch_pdl(small_dispatch_kernel, dim3(static_cast<unsigned>(n_aff + gblocks)),
+                          dim3(CHUNK), sm, s, 1, topk_idx, T, E, K, counts, offsets, perm,
+                          slot_pos, scr.smask, status, affinity, n_aff_x, n_aff,
+                          static_cast<const uint4 *>(X), H, static_cast<uint4 *>(Xp), zero_buf,
+                          static_cast<int>(zero_n));
+    }
+    err = ensure_smem(reinterpret_cast<const void *>(masks_kernel), m_smem);
+    if (err != cudaSuccess) return err;
+    err = ensure_smem(reinterpret_cast<const void *>(scatter_kernel), 2 * m_smem);
+    if (err != cudaSuccess) return err;
+    if ((err = launch_pdl(masks_kernel, dim3(plan.n_chunks), dim3(CHUNK), m_smem, s, 1, topk_idx, T,
+                          E, K, scr.smask, scr.chunk_cnt, status)) != cudaSuccess)
+        return err;
+    if ((err = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, s, 1, E, plan.n_chunks,
+                          static_cast<const int32_t *>(scr.chunk_cnt), scr.chunk_base, counts,
+                          offsets)) != cudaSuccess)
+        return err;
+    if ((err = launch_pdl(scatter_kernel, dim3(plan.n_chunks), dim3(CHUNK), 2 * m_smem, s, 1,
+                          topk_idx, T, E, K, static_cast<const uint32_t *>(scr.smask),
+                          static_cast<const int32_t *>(scr.chunk_base), perm, slot_pos)) != cudaSuccess)
+        return err;
+    // affinity tiles, row gather and counter zeroing: one launch
     long long gblocks = 0;
     const bool by_token = static_cast<long long>(T) * H * 2 >= (64ll << 20);
     if (Xp) {
