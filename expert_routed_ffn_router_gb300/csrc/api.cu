@@ -69,13 +69,18 @@ struct SideStream {
     bool tried = false;
 };
 
-SideStream *side_stream()
+SideStream *side_stream(cudaStream_t caller)
 {
     thread_local SideStream tab[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     SideStream &ss = tab[dev];
     if (!ss.tried) {
+        // not created while the caller's stream is being captured (the call then keeps the
+        // shared expert in the routed launch; a later call outside a capture creates it)
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(caller, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+            return nullptr;
         ss.tried = true;
         if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess ||
             cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
@@ -291,7 +296,7 @@ int layer_forward(const moe_shape_t *shape, const moe_weights_t *wt, const moe_w
     // shared expert beside the router and the dispatch (bf16 weights, small batches)
     SideStream *side = nullptr;
     if (!fp8 && s.I_shared > 0 && (g_shared_side == 1 || (g_shared_side < 0 && s.T <= kSideMaxTokens)))
-        side = side_stream();
+        side = side_stream(st);
     if (side) {
         P[1].act = X;
         if (cudaEventRecord(side->fork, st) != cudaSuccess ||

@@ -149,6 +149,47 @@ def test_concurrent_calls_from_two_host_threads():
         assert layer.status() == 0
 
 
+def test_first_call_of_a_host_thread_inside_a_graph_capture():
+    # a host thread whose first layer call is captured: its side stream is not created
+    # during the capture (that call keeps the shared expert in the routed launch), and the
+    # replay gives what an ordinary call gives
+    import threading
+    p = Problem(synth.workload("tiny", T=24))
+    layer = B.MoELayer(p.dev, p.w.T, p.w.K)
+    layer.forward(p.X)                      # shared-memory limits raised outside the capture
+    B.moe_debug_set_shared_side(0)          # the reference in the placement the capture takes
+    try:
+        layer.forward(p.X)
+        torch.cuda.synchronize()
+    finally:
+        B.moe_debug_set_shared_side(-1)
+    ref = layer.Y.clone()
+    out = {}
+
+    def run():
+        try:
+            torch.cuda.set_device(0)
+            s = torch.cuda.Stream()
+            X2 = p.X.clone()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    layer.forward(X2, stream=s)
+                layer.Y.zero_()
+                g.replay()
+            torch.cuda.synchronize()
+            out["y"] = layer.Y.clone()
+        except Exception as exc:          # reported below, on the main thread
+            out["err"] = exc
+
+    th = threading.Thread(target=run)
+    th.start()
+    th.join()
+    assert "err" not in out, out.get("err")
+    assert torch.equal(out["y"], ref)
+    assert layer.status() == 0
+
+
 def _deterministic_and_graph_capture():
     p = Problem(synth.workload("tiny", T=77))
     layer = B.MoELayer(p.dev, p.w.T, p.w.K)
