@@ -74,27 +74,37 @@ struct RouterArgs {
     int variant;     // any option off its default: the general selection path
 };
 
-// CTA tile: TT tokens x TE experts, TPT x EPT per thread, PF stages of loads in flight;
-// X2: paired fp32 FMAs (two tokens per instruction) -- the same correctly rounded
-// operations in the same order, in half the FMA instructions; MINB: resident CTAs per SM
-// the registers are sized for.
-template <int TT_, int TE_, int TPT_, int EPT_, int PF_, int X2_ = 0, int MINB_ = 2>
+// Two-stage CTA tile (gemm_tile): TT tokens x TE experts, TPT x EPT per thread, PF stages
+// of loads in flight in registers.
+template <int TT_, int TE_, int TPT_, int EPT_, int PF_>
 struct Cfg {
-    static constexpr int TT = TT_, TE = TE_, TPT = TPT_, EPT = EPT_, PF = PF_, MINB = MINB_;
-    static constexpr bool X2 = X2_ != 0;
+    static constexpr int TT = TT_, TE = TE_, TPT = TPT_, EPT = EPT_, PF = PF_;
     static constexpr int NTY = TT / TPT, NTX = TE / EPT;
     static constexpr int LY = 4;                          // token groups per warp
     static constexpr int XV = TT * 4, WV = TE * 4;        // 8-element vectors per stage
     static constexpr int XPT = (XV + NT - 1) / NT, WPT = (WV + NT - 1) / NT;
     static_assert(NTX * NTY == NT, "one output micro-tile per thread");
     static_assert(NTY % LY == 0 && NTX % (32 / LY) == 0, "warp layout");
-    static_assert(EPT % 4 == 0 && TPT % 4 == 0 && (EPT == 4 || X2), "float4 operand reads");
+    static_assert(EPT == 4 && TPT % 4 == 0, "float4 operand reads");
 };
 using SmallCfg = Cfg<16, 256, 4, 4, 2>;
+
+// Warp-specialised CTA tile (gemm_tile_ws): TT x TE on the eight compute warps, TPT x EPT
+// outputs a thread in paired fp32 FMAs (two tokens per instruction -- the same correctly
+// rounded operations in the same order as two fmaf, in half the FMA instructions).
+template <int TT_, int TE_, int TPT_, int EPT_>
+struct WsCfg {
+    static constexpr int TT = TT_, TE = TE_, TPT = TPT_, EPT = EPT_;
+    static constexpr int NTY = TT / TPT, NTX = TE / EPT;
+    static constexpr int LY = 4;                          // token groups per warp
+    static_assert(NTX * NTY == NT, "one output micro-tile per compute thread");
+    static_assert(NTY % LY == 0 && NTX % (32 / LY) == 0, "warp layout");
+    static_assert(EPT % 4 == 0 && TPT % 4 == 0, "float4 operand reads");
+};
 // 8 x 8 outputs a thread: 16 operands read from shared memory per 64 FMAs (the 8 x 4 tile
 // read 12 per 32 and was bound by shared-memory bandwidth); one CTA per SM holds the
 // 64 paired running sums.
-using LargeCfg = Cfg<128, 128, 8, 8, 2, 1, 1>;
+using LargeCfg = WsCfg<128, 128, 8, 8>;
 
 // Two fp32 lanes per 64-bit register: d = a * b + c and d = a + b, each lane correctly
 // rounded (the same results as two fmaf / two fp32 adds).
@@ -907,9 +917,6 @@ __device__ void gemm_tile(const RouterArgs &a, unsigned char *smem)
     float acc[C::TPT * C::EPT];
 #pragma unroll
     for (int p = 0; p < C::TPT * C::EPT; ++p) acc[p] = 0.f;
-    uint64_t accp[C::X2 ? C::TPT / 2 * C::EPT : 1];     // paired running sums (X2)
-#pragma unroll
-    for (int p = 0; p < (C::X2 ? C::TPT / 2 * C::EPT : 1); ++p) accp[p] = 0ull;
 
 #pragma unroll
     for (int j = 0; j < C::PF; ++j)
@@ -927,72 +934,29 @@ __device__ void gemm_tile(const RouterArgs &a, unsigned char *smem)
                 // the running sum of the split
                 const float *xb = xs + buf * KST * C::TT + wtok;
                 const float *wb = wsm + buf * KST * C::TE + wexp;
-                if constexpr (C::X2) {
-                    // pair pp * EPT + jj = (token 2pp, token 2pp + 1) x expert jj
-                    uint64_t pin[C::TPT / 2 * C::EPT];
+                float acc_in[C::TPT * C::EPT];
 #pragma unroll
-                    for (int q = 0; q < C::TPT / 2 * C::EPT; ++q) pin[q] = 0ull;
+                for (int q = 0; q < C::TPT * C::EPT; ++q) acc_in[q] = 0.f;
 #pragma unroll 4
-                    for (int kk = 0; kk < KST; ++kk) {
-                        ulonglong2 xv[C::TPT / 4];
+                for (int kk = 0; kk < KST; ++kk) {
+                    float xa[C::TPT];
 #pragma unroll
-                        for (int i4 = 0; i4 < C::TPT / 4; ++i4)
-                            xv[i4] = *reinterpret_cast<const ulonglong2 *>(xb + kk * C::TT + 4 * C::LY * i4);
-                        uint64_t wp[C::EPT];
-#pragma unroll
-                        for (int g = 0; g < C::EPT / 4; ++g) {
-                            const float4 wv = *reinterpret_cast<const float4 *>(wb + kk * C::TE + 4 * LX * g);
-                            wp[4 * g] = dup_x2(wv.x);
-                            wp[4 * g + 1] = dup_x2(wv.y);
-                            wp[4 * g + 2] = dup_x2(wv.z);
-                            wp[4 * g + 3] = dup_x2(wv.w);
-                        }
-#pragma unroll
-                        for (int pp = 0; pp < C::TPT / 2; ++pp) {
-                            const uint64_t xp = (pp & 1) ? xv[pp >> 1].y : xv[pp >> 1].x;
-#pragma unroll
-                            for (int jj = 0; jj < C::EPT; ++jj)
-                                pin[pp * C::EPT + jj] = fma_x2(xp, wp[jj], pin[pp * C::EPT + jj]);
-                        }
+                    for (int i4 = 0; i4 < C::TPT / 4; ++i4) {
+                        const float4 v = *reinterpret_cast<const float4 *>(xb + kk * C::TT + 4 * C::LY * i4);
+                        xa[4 * i4] = v.x; xa[4 * i4 + 1] = v.y; xa[4 * i4 + 2] = v.z; xa[4 * i4 + 3] = v.w;
                     }
+                    const float4 wv = *reinterpret_cast<const float4 *>(wb + kk * C::TE);
+                    const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-                    for (int q = 0; q < C::TPT / 2 * C::EPT; ++q) accp[q] = add_x2(accp[q], pin[q]);
-                } else {
-                    float acc_in[C::TPT * C::EPT];
+                    for (int i = 0; i < C::TPT; ++i)
 #pragma unroll
-                    for (int q = 0; q < C::TPT * C::EPT; ++q) acc_in[q] = 0.f;
-#pragma unroll 4
-                    for (int kk = 0; kk < KST; ++kk) {
-                        float xa[C::TPT];
-#pragma unroll
-                        for (int i4 = 0; i4 < C::TPT / 4; ++i4) {
-                            const float4 v = *reinterpret_cast<const float4 *>(xb + kk * C::TT + 4 * C::LY * i4);
-                            xa[4 * i4] = v.x; xa[4 * i4 + 1] = v.y; xa[4 * i4 + 2] = v.z; xa[4 * i4 + 3] = v.w;
-                        }
-                        const float4 wv = *reinterpret_cast<const float4 *>(wb + kk * C::TE);
-                        const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-                        for (int i = 0; i < C::TPT; ++i)
-#pragma unroll
-                            for (int jj = 0; jj < 4; ++jj)
-                                acc_in[i * 4 + jj] = fmaf(xa[i], wa[jj], acc_in[i * 4 + jj]);
-                    }
-#pragma unroll
-                    for (int q = 0; q < C::TPT * C::EPT; ++q) acc[q] += acc_in[q];
+                        for (int jj = 0; jj < 4; ++jj)
+                            acc_in[i * 4 + jj] = fmaf(xa[i], wa[jj], acc_in[i * 4 + jj]);
                 }
+#pragma unroll
+                for (int q = 0; q < C::TPT * C::EPT; ++q) acc[q] += acc_in[q];
             }
         }
-    }
-    if constexpr (C::X2) {
-#pragma unroll
-        for (int pp = 0; pp < C::TPT / 2; ++pp)
-#pragma unroll
-            for (int jj = 0; jj < C::EPT; ++jj) {
-                float lo, hi;
-                asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(accp[pp * C::EPT + jj]));
-                acc[(2 * pp) * C::EPT + jj] = lo;
-                acc[(2 * pp + 1) * C::EPT + jj] = hi;
-            }
     }
 
 #pragma unroll
@@ -1072,7 +1036,7 @@ __device__ void gemm_tile_ws(const RouterArgs &a, unsigned char *smem)
 {
     constexpr int PT = 32 * NPW;                                // producer threads
     // producer units: 4 consecutive rows x one 8-element group of a stage
-    static_assert(C::X2 && C::TT % PT == 0 && C::TE % PT == 0, "warp-specialised tile");
+    static_assert(C::TT % PT == 0 && C::TE % PT == 0, "warp-specialised tile");
     constexpr int XU = C::TT / PT, WU = C::TE / PT;            // units a producer thread
     constexpr int XI = 4 * XU, WI = 4 * WU;                     // 16-byte vectors a thread
     const int et = blockIdx.x, tt = blockIdx.y, ks = blockIdx.z;
@@ -1798,7 +1762,7 @@ RouterPlan router_plan(int T, int H, int E)
     p.nET = (E + p.TE - 1) / p.TE;
     p.S = H / KST;
     const int base = p.nTT * p.nET;
-    const int target = (small ? SmallCfg::MINB : LargeCfg::MINB) * num_sms();
+    const int target = (small ? 2 : 1) * num_sms();   // resident CTAs per SM: 2 small, 1 large
     if (p.gemv) {
         p.KS = 1;
         p.depth = ((H / 8 + GEMV_QW - 1) / GEMV_QW + 31) / 32 + 3 + 5 + 2 + 2;
