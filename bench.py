@@ -177,8 +177,8 @@ def algorithmic(w, n_act: int, wbytes: int = 2, side: bool = False):
 
 
 def launches_per_step(w, with_affinity: bool, fp8: bool = False) -> int:
-    """Kernels moe_layer_forward launches: router (1 fused, or GEMM + finalise for
-    T > 4096), dispatch (for T <= 256 one launch whose CTAs each form the bookkeeping and
+    """Kernels moe_layer_forward launches: router (GEMM + finalise for 16 <= T <= 2048
+    and T > 4096, else one fused launch), dispatch (for T <= 256 one launch whose CTAs each form the bookkeeping and
     then compute the affinity matrix, gather the rows and zero the FFN's counters; else
     masks, scan, scatter and one launch for the affinity, the gather and the zeroing), the
     FFN (up and down projections in one persistent launch), combine.  On
@@ -187,7 +187,7 @@ def launches_per_step(w, with_affinity: bool, fp8: bool = False) -> int:
     quantisation, split the FFN into its up and down launches and quantise h (and the
     shared expert's h) between them."""
     T = w.T
-    router = 1 if T <= 4096 else 2
+    router = 2 if (16 <= T <= 2048 or T > 4096) else 1
     dispatch = 1 if T <= 256 else 4
     ffn = 1 if not fp8 else 1 + 2 + (2 if w.Is else 1)
     side = 1 if shared_on_side(w, fp8) else 0

@@ -17,8 +17,10 @@ struct RouterPlan {
     int TT, TE, nTT, nET, KS, S;  // token tile, expert tile, tiles, split-K, 32-wide stages
     int max_pairs;                // shared-memory refine list capacity
     int depth;                    // summation depth of one logit (error bound)
-    int gemv;                     // tiny batches: token batch (1,2,4) of the one-warp-per-
+    int gemv;                     // tiny batches: token batch (1,2,4,8) of the one-warp-per-
                                   // expert path; 0 = tile GEMM
+    int split;                    // small tile GEMM, then the one-warp-per-token finalise
+                                  // launch (instead of the last CTA of a token tile)
     size_t part_bytes, xsq_bytes, wsq_bytes, cnt_bytes, smem_bytes;
     size_t total() const { return part_bytes + xsq_bytes + wsq_bytes + cnt_bytes; }
 };
