@@ -26,14 +26,14 @@
 // candidates (the others keep their fp32 sel, which orders exactly since their intervals
 // are disjoint from every other candidate's).
 //
-// Structure.  A grid (expert tiles, token tiles, K splits) of 256-thread CTAs computes
-// fp32 logit tiles on the CUDA cores into the workspace:
+// Structure.  A grid (expert tiles, token tiles, K splits) of CTAs (256 threads; 384 for
+// large batches) computes fp32 logit tiles on the CUDA cores into the workspace:
 //   tiny batches (T <= 8):     four warps per expert, all tokens at once;
 //   small batches (T <= 4096): 16 tokens x 256 experts per CTA, 4x4 per thread;
 //   large batches:             128 tokens x 128 experts per CTA, 8x8 per thread on eight
 //                              compute warps, fed through a 4-stage fp32 ring by four
 //                              producer warps (cp.async staging, bf16 -> fp32, norms).
-// Tiny batches and small batches above 2048 tokens: the last CTA of a token tile
+// Batches of up to 15 tokens and of 2049 to 4096 tokens: the last CTA of a token tile
 // (completion counter) sums the split-K partials in a fixed order, scores, selects and
 // writes the outputs -- one launch.  From 16 to 2048 tokens and for large batches a second
 // launch finalises, one warp per token, so the selection is spread over the whole GPU
