@@ -1,0 +1,35 @@
+"""Host-side accounting of bench.py (CPU only): the algorithmic bytes and FLOPs of the FFN
+stage when the shared expert runs in its own launch add up to those of the single launch,
+and the launch count per step follows the library's launch structure."""
+import bench
+from expert_routed_ffn_router_gb300 import synth
+
+
+def test_shared_expert_split_keeps_the_totals():
+    for name in ("sweep2", "decode", "prefill"):
+        w = synth.workload(name)
+        n_act = min(w.E, w.T * w.K)
+        b1, f1, lb1, lf1 = bench.algorithmic(w, n_act, 2, side=False)
+        b2, f2, lb2, lf2 = bench.algorithmic(w, n_act, 2, side=True)
+        assert b2["ffn"] + b2["ffn_shared"] == b1["ffn"]
+        assert f2["ffn"] + f2["ffn_shared"] == f1["ffn"]
+        assert (lb1, lf1) == (lb2, lf2)
+        # the shared expert's weights: 3 H Is bf16 values
+        assert b2["ffn_shared"] >= 3 * w.H * w.Is * 2
+
+
+def test_side_stream_placement_rule():
+    assert bench.shared_on_side(synth.workload("decode"))            # T = 128
+    assert bench.shared_on_side(synth.workload("sweep2"))
+    assert not bench.shared_on_side(synth.workload("prefill"))
+    assert not bench.shared_on_side(synth.workload("decode"), fp8=True)
+
+
+def test_launches_per_step_by_batch_size():
+    expect = {2: 5, 8: 5, 16: 6, 128: 6, 200: 5, 512: 8, 3000: 7, 16384: 8}
+    for T, n in expect.items():
+        assert bench.launches_per_step(synth.workload("decode", T=T), True) == n, T
+    # FP8 experts at 128 tokens: router tile + finalise, dispatch, then token-row
+    # quantisation, up launch, two h quantisations, down launch, and combine
+    w = synth.workload("decode")
+    assert bench.launches_per_step(w, True, fp8=True) == 2 + 1 + 5 + 1
