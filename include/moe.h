@@ -155,6 +155,9 @@ void moe_debug_set_shared_side(int mode);
  *       bias, in descending sel order, equal sel -> lower index first.  The selection is
  *       the one exact arithmetic gives: fp32 scores carry a rigorous error bound and any
  *       token whose order the bound cannot certify is re-scored in double-word arithmetic.
+ *       A token whose row of X (or a gate row) holds a NaN, an infinity or values whose
+ *       products overflow has no defined selection; it still gets K distinct experts in
+ *       [0, E) (its weights may be NaN), and the call does not fail.
  *   out topk_w fp32 [T, K]: s_j / sum_j s_j over the selected unbiased scores s.
  *   ws / ws_bytes: workspace (split-K partial logits, completion counters). */
 int moe_router_topk(const void *X, const void *W_gate, const float *bias,
