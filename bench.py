@@ -8,7 +8,12 @@ bf16 weights (22.5 GB of routed experts) and activations, fp32 output.  Inputs a
 synthetic tensors already resident in HBM; the activated experts' weights (13.2 GB per
 step at T=128) are far larger than L2, so every step streams them from HBM.
 
-One JSON line on rank 0.  `--impl reference` times the fp64 CPU oracle instead (the
+One JSON line on rank 0.  Beside the decode headline, the same line carries a `workloads`
+table measured in the same process on the same weights: the batch sweep T = 2 ... 256
+(memory-bound: target >= 70% of 8 TB/s up to 64 tokens), the skewed 8192-token batch and
+the 16384-token prefill (tensor-bound: target >= 60% of the bf16 burst rate).  Each row is
+timed like the headline (bare calls between CUDA events) and gets its per-stage times from
+a separate instrumented pass.  `--impl reference` times the fp64 CPU oracle instead (the
 reference arm), on a bounded sample of the same workload.
 Multi-GPU (torchrun): independent replicas, one per GPU, each with its own tokens; no
 collective on the data path (the timing is reduced with a max over ranks).
@@ -73,7 +78,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -97,12 +102,8 @@ class ClockSampler:
         if self.thread is not None:
             self.thread.join(timeout=5)
 
-    def summary(self, t0: float, t1: float):
-        win = [p for (t, p) in self.samples if t0 <= t <= t1] or [p for (_, p) in self.samples]
-        if not win:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
-                    "samples": 0}
-
+    @staticmethod
+    def _stats(win):
         def num(x):
             try:
                 return float(x)
@@ -110,11 +111,31 @@ class ClockSampler:
                 return None
         sm = [num(p[0]) for p in win if num(p[0]) is not None]
         mx = [num(p[1]) for p in win if num(p[1]) is not None]
+        pw = [num(p[2]) for p in win if num(p[2]) is not None]
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         reasons = sorted({names[i] for p in win for i in range(4) if p[4 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "sm_min_mhz": min(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "reasons": reasons,
                 "samples": len(win)}
+
+    def summary(self, t0: float, t1: float, b0: float | None = None, b1: float | None = None):
+        """Clocks over the timed region [t0, t1] and, when given, over the busy window
+        [b0, b1] around it (warm-up, timed and instrumented passes of the same workload):
+        a timed region of a few tens of milliseconds holds one or two 20 ms samples."""
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        timed = [p for (t, p) in self.samples if t0 <= t <= t1]
+        out = self._stats(timed) if timed else {"samples": 0}
+        if b0 is not None:
+            busy = [p for (t, p) in self.samples if b0 <= t <= b1]
+            if busy:
+                wb = self._stats(busy)
+                out = {**wb, "timed_region": out, "window": "busy window of this workload "
+                       f"({b1 - b0:.2f} s: warm-up, timed and instrumented passes)"}
+        return out
 
 
 # ------------------------------------------------------------------------ accounting
@@ -215,8 +236,153 @@ def max_over_ranks(x: float, device=None) -> float:
 
 
 # ----------------------------------------------------------------------------- our arm
-def run_ours(args, rank, world, local_rank):
+# Workloads measured beside the headline in the same process (same expert weights): the
+# batch sweep of the memory-bound regime and the two tensor-bound batches.
+SIDE_WORKLOADS = ("sweep2", "sweep4", "sweep8", "sweep16", "sweep32", "sweep64", "sweep256",
+                  "skewed", "prefill")
+HBM_TARGET = 0.70      # of 8 TB/s, batches of up to 64 tokens
+TENSOR_TARGET = 0.60   # of the bf16 burst rate, batches of 8192 tokens and more
+
+
+def _layer_for(w, routing, weights, dev, opts, fp8, weights8=None):
     import numpy as np
+    import torch
+
+    from expert_routed_ffn_router_gb300 import binding as B
+    wts = dict(weights)
+    wts["W_gate"] = torch.from_numpy(routing["W_gate"].view(np.int16)).view(torch.bfloat16).to(dev)
+    wts["bias"] = torch.from_numpy(routing["bias"]).to(dev)
+    X_host = torch.from_numpy(routing["X"].view(np.int16)).view(torch.bfloat16)
+    layer = B.MoELayer(wts, w.T, w.K, with_affinity=True, routing=opts, fp8=fp8,
+                       weights8=weights8)
+    return layer, wts, X_host, X_host.to(dev)
+
+
+def _timed(layer, X, K, stream, barrier):
+    """Device time per step of K bare layer calls (CUDA events on the launching stream)."""
+    import torch
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    ev0.record(stream)
+    for _ in range(K):
+        layer.forward(X)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier()
+    return ev0.elapsed_time(ev1) / K, t0, t1
+
+
+def _stage_pass(layer, X, K, stream):
+    """Per-stage device times: a separate pass of K calls that record the library's stage
+    events (the headline's timed region runs the bare call)."""
+    import torch
+
+    from expert_routed_ffn_router_gb300 import binding as B
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for evs in stage_ev:
+        for ev in evs:
+            ev.record(stream)          # materialise the handles
+    torch.cuda.synchronize()
+    for k in range(K):
+        B.moe_debug_set_stage_events(stage_ev[k])
+        layer.forward(X)
+    torch.cuda.synchronize()
+    B.moe_debug_set_stage_events(None)
+    stage_ms = {name: statistics.fmean(stage_ev[k][i].elapsed_time(stage_ev[k][i + 1])
+                                       for k in range(K))
+                for i, name in enumerate(STAGES)}
+    stage_ms["ffn"] = stage_ms["ffn_up"] + stage_ms["ffn_down"]
+    return stage_ms
+
+
+def dominant_roofline(w, n_act, stage_ms, peaks, peak_src, fp8, workload_name):
+    b, f, _, _ = algorithmic(w, n_act, 1 if fp8 else 2, shared_on_side(w, fp8))
+    dom = max(("ffn", "router", "combine", "dispatch"), key=lambda s: stage_ms[s])
+    t_dom = stage_ms[dom] / 1e3
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if f[dom] / max(b[dom], 1) > ridge and dom.startswith("ffn"):
+        ach = f[dom] / t_dom / 1e12
+        roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    else:
+        ach = b[dom] / t_dom / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = ffn_traffic(workload_name) if dom == "ffn" and not fp8 else None
+    roof["kernel"] = dom
+    roof["peak_source"] = (f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured"
+                           else "fallback")
+    roof["algorithmic_bytes_per_launch"] = int(b[dom])
+    roof["algorithmic_flops_per_launch"] = int(f[dom])
+    roof["launch_ms"] = round(stage_ms[dom], 4)
+    return roof
+
+
+def layer_roofline(w, n_act, ms, peaks, fp8=False):
+    _, _, layer_bytes, layer_flops = algorithmic(w, n_act, 1 if fp8 else 2, shared_on_side(w, fp8))
+    sec = ms / 1e3
+    return {"algorithmic_bytes": int(layer_bytes), "algorithmic_flops": int(layer_flops),
+            "hbm_gbs": round(layer_bytes / sec / 1e9, 1),
+            "hbm_frac": round(layer_bytes / sec / 1e9 / peaks["hbm_gbs"], 4),
+            "hbm_frac_of_8TBs": round(layer_bytes / sec / 8e12, 4),
+            "tensor_tflops": round(layer_flops / sec / 1e12, 2),
+            "tensor_frac": round(layer_flops / sec / 1e12 / peaks["bf16_tflops"], 4),
+            "tensor_frac_sustained": round(layer_flops / sec / 1e12 /
+                                           peaks["bf16_tflops_sustained"], 4)}
+
+
+def target_of(w):
+    """The layer-level target of a DeepSeek-V3-shaped batch: >= 70% of 8 TB/s up to 64
+    tokens, >= 60% of the bf16 burst rate from 8192 tokens; none in between."""
+    if w.T <= 64:
+        return "hbm_frac_of_8TBs", HBM_TARGET
+    if w.T >= 8192:
+        return "tensor_frac", TENSOR_TARGET
+    return None, None
+
+
+def measure_side_workload(name, weights, dev, args, sampler, peaks, peak_src, barrier):
+    """One row of the workloads table: the same call as the headline on another batch."""
+    import torch
+
+    from expert_routed_ffn_router_gb300 import synth
+    w = synth.workload(name)
+    routing = synth.routing_inputs(w)
+    layer, _, _, X = _layer_for(w, routing, weights, dev, None, False)
+    stream = torch.cuda.current_stream()
+    t_busy0 = time.time()
+    for _ in range(args.warmup):
+        layer.forward(X)
+    torch.cuda.synchronize()
+    if layer.status() != 0:
+        raise RuntimeError(f"device status word reported an error during warm-up ({name})")
+    ms, t0, t1 = _timed(layer, X, args.steps, stream, barrier)
+    stage_ms = _stage_pass(layer, X, args.steps, stream)
+    t_busy1 = time.time()
+    if layer.status() != 0:
+        raise RuntimeError(f"device status word reported an error ({name})")
+    counts = layer.counts.cpu().numpy()
+    n_act = int((counts > 0).sum())
+    lr = layer_roofline(w, n_act, ms, peaks)
+    key, tgt = target_of(w)
+    row = {"T": w.T, "ms_per_step": round(ms, 4), "tokens_per_s": round(w.T / (ms / 1e3), 1),
+           "n_active_experts": n_act, **lr,
+           "dominant_kernel": dominant_roofline(w, n_act, stage_ms, peaks, peak_src, False, name),
+           "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+           "gpu_launches": args.steps * launches_per_step(w, with_affinity=True),
+           "clocks": sampler.summary(t0, t1, t_busy0, t_busy1)}
+    if key:
+        row["target"] = {"metric": key, "min": tgt, "met": bool(lr[key] >= tgt)}
+    del layer
+    torch.cuda.empty_cache()
+    return row
+
+
+def run_ours(args, rank, world, local_rank):
     import torch
 
     from expert_routed_ffn_router_gb300 import binding as B
@@ -228,13 +394,9 @@ def run_ours(args, rank, world, local_rank):
     w = replica_workload(args.workload, rank)
     routing = synth.routing_inputs(w)
     weights = synth.expert_weights_device(w, dev)
-    weights["W_gate"] = torch.from_numpy(routing["W_gate"].view(np.int16)).view(torch.bfloat16).to(dev)
-    weights["bias"] = torch.from_numpy(routing["bias"]).to(dev)
-    X_host = torch.from_numpy(routing["X"].view(np.int16)).view(torch.bfloat16)
-    X = X_host.to(dev)
     opts = ROUTINGS[args.routing]
     fp8 = args.precision == "fp8"
-    layer = B.MoELayer(weights, w.T, w.K, with_affinity=True, routing=opts, fp8=fp8)
+    layer, wts, X_host, X = _layer_for(w, routing, weights, dev, opts, fp8)
     peaks, peak_src = load_peaks()
 
     def barrier():
@@ -245,39 +407,21 @@ def run_ours(args, rank, world, local_rank):
                            else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank]))
     sampler.start()
     stream = torch.cuda.current_stream()
+    t_busy0 = time.time()
     for _ in range(args.warmup):
         layer.forward(X)
     torch.cuda.synchronize()
     if layer.status() != 0:
         raise RuntimeError("device status word reported an error during warm-up")
 
-    # ---- device-resident timed region (per-stage events recorded inside every step)
+    # ---- device-resident timed region: the bare layer call, inputs already in HBM
     K = args.steps
-    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
-    for evs in stage_ev:
-        for ev in evs:
-            ev.record(stream)          # materialise the handles
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
-    t_wall0 = time.time()
-    ev0.record(stream)
-    for k in range(K):
-        B.moe_debug_set_stage_events(stage_ev[k])
-        layer.forward(X)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    t_wall1 = time.time()
-    B.moe_debug_set_stage_events(None)
-    ms = max_over_ranks(ev0.elapsed_time(ev1) / K, dev)
-    stage_ms = {name: statistics.fmean(stage_ev[k][i].elapsed_time(stage_ev[k][i + 1])
-                                       for k in range(K))
-                for i, name in enumerate(STAGES)}
-    stage_ms["ffn"] = stage_ms["ffn_up"] + stage_ms["ffn_down"]
+    ms_rank, t_wall0, t_wall1 = _timed(layer, X, K, stream, barrier)
+    ms = max_over_ranks(ms_rank, dev)
     if layer.status() != 0:
         raise RuntimeError("device status word reported an error in the timed region")
+    # ---- per-stage times (a separate, instrumented pass)
+    stage_ms = _stage_pass(layer, X, K, stream)
 
     # ---- end to end: pinned host input -> layer -> pinned host output, every step.  The
     # copies run on their own stream and overlap the neighbouring steps' compute: step k's
@@ -286,7 +430,7 @@ def run_ours(args, rank, world, local_rank):
     Xh = X_host.pin_memory()
     Yh = [torch.empty(w.T, w.H, dtype=torch.float32).pin_memory() for _ in range(2)]
     Xd = [torch.empty_like(X) for _ in range(2)]
-    layers = [layer, B.MoELayer(weights, w.T, w.K, with_affinity=True, routing=opts, fp8=fp8,
+    layers = [layer, B.MoELayer(wts, w.T, w.K, with_affinity=True, routing=opts, fp8=fp8,
                                 weights8=layer.w8)]
     copy_s = torch.cuda.Stream(device=dev)
 
@@ -321,11 +465,12 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    sampler.stop()
+    t_busy1 = time.time()
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / K, dev)
     if any(l.status() != 0 for l in layers):
         raise RuntimeError("device status word reported an error in the end-to-end region")
     del layers[1]
+    clocks = sampler.summary(t_wall0, t_wall1, t_busy0, t_busy1)
 
     counts = layer.counts.cpu().numpy()
     n_act = int((counts > 0).sum())
@@ -337,25 +482,8 @@ def run_ours(args, rank, world, local_rank):
     rep = B.moe_grace_replicate(counts, plan["group_of"], 8)
     B.moe_grace_route_table(rep, 4)
     ms_plan = (time.perf_counter() - t_plan) * 1e3
-    b, f, layer_bytes, layer_flops = algorithmic(w, n_act, 1 if fp8 else 2,
-                                                 shared_on_side(w, fp8))
-    dom = max(("ffn", "router", "combine", "dispatch"), key=lambda s: stage_ms[s])
-    t_dom = stage_ms[dom] / 1e3
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if f[dom] / max(b[dom], 1) > ridge and dom.startswith("ffn"):
-        ach = f[dom] / t_dom / 1e12
-        roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s"}
-    else:
-        ach = b[dom] / t_dom / 1e9
-        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s"}
-    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = ffn_traffic(w.name) if dom == "ffn" and not fp8 else None
-    roof["kernel"] = dom
-    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
-    roof["algorithmic_bytes_per_launch"] = int(b[dom])
-    roof["launch_ms"] = round(stage_ms[dom], 4)
+    roof = dominant_roofline(w, n_act, stage_ms, peaks, peak_src, fp8, w.name)
+    lr = layer_roofline(w, n_act, ms, peaks, fp8)
 
     total_tokens = w.T * world
     value = total_tokens / (ms / 1e3)
@@ -369,7 +497,7 @@ def run_ours(args, rank, world, local_rank):
                                f"tokens, H={w.H}, E={w.E}, top-{w.K}, I={w.I}, shared I={w.Is}",
                    "tokens_per_gpu": w.T, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2: the activated experts' weights "
-                         f"({layer_bytes / 1e9:.1f} GB) stream from HBM every step",
+                         f"({lr['algorithmic_bytes'] / 1e9:.1f} GB) stream from HBM every step",
                    "n_active_experts": n_act,
                    "shared_expert": ("own FFN launch on a side stream beside the router and "
                                      "the dispatch" if shared_on_side(w, fp8) else
@@ -381,19 +509,31 @@ def run_ours(args, rank, world, local_rank):
                 "copies": "own stream, overlapping the neighbouring steps' compute"},
         "gpu_launches": K * launches_per_step(w, with_affinity=True, fp8=fp8),
         "roofline": roof,
-        "layer_roofline": {"algorithmic_bytes": int(layer_bytes),
-                           "hbm_frac": round(layer_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
-                           "hbm_frac_of_8TBs": round(layer_bytes / (ms / 1e3) / 8e12, 4),
-                           "tensor_frac": round(layer_flops / (ms / 1e3) / 1e12 /
-                                                peaks["bf16_tflops"], 4)},
+        "layer_roofline": lr,
         "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "stages_note": "from a separate pass of the same calls with the library's stage "
+                       "events recorded; the timed region runs the bare call",
         "grace_plan": {"gpus": 8, "gpus_per_node": 4, "r": plan["r"],
                        "U": round(float(plan["U"][plan["knee"]]), 4),
                        "S": round(float(plan["S"][plan["knee"]]), 4),
                        "rho": round(rep["rho"], 4), "n_replica": rep["n_replica"],
                        "n_hot": len(rep["hot"]), "planner_ms": round(ms_plan, 1)},
-        "clocks": sampler.summary(t_wall0, t_wall1),
+        "clocks": clocks,
     }
+    del layer
+    torch.cuda.empty_cache()
+    if (world == 1 and args.workload == "decode" and not fp8 and opts is None
+            and not args.no_workloads):
+        rows = {}
+        for name in SIDE_WORKLOADS:
+            rows[name] = measure_side_workload(name, weights, dev, args, sampler, peaks,
+                                               peak_src, barrier)
+        rows["decode"] = {"T": w.T, "ms_per_step": round(ms, 4),
+                          "tokens_per_s": round(value, 1), "n_active_experts": n_act, **lr,
+                          "note": "the headline above"}
+        out["workloads"] = rows
+        out["targets"] = {n: r["target"] for n, r in rows.items() if "target" in r}
+    sampler.stop()
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
         out["cpu_baseline"] = cpu_baseline(w, routing, weights, budget_s=args.cpu_budget,
                                            opts=opts)
@@ -507,6 +647,9 @@ def main():
     ap.add_argument("--precision", choices=("bf16", "fp8"), default="bf16",
                     help="expert weights: bf16 (default) or FP8 E4M3 with 128x128 block scales")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="measure the headline workload only (skip the sweep, skewed and "
+                         "prefill rows measured beside the decode headline)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -515,6 +658,10 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.gpus != world:
+        # one process per GPU: N GPUs need N ranks (torch.distributed.run --nproc-per-node N)
+        sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; launch one process per "
+                 "GPU with torch.distributed.run --nproc-per-node N")
 
     if args.impl == "reference":
         if rank != 0:

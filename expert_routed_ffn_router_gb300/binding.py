@@ -35,6 +35,12 @@ class MoeWeights(ctypes.Structure):
                                                "W3s", "W2s")]
 
 
+class MoeWorkspaceLayout(ctypes.Structure):
+    """moe_workspace_layout_t: byte offsets of the layer's intermediates in the workspace."""
+    _fields_ = [(n, ctypes.c_size_t) for n in ("offsets", "perm", "slot_pos", "Xp", "h", "Yp",
+                                               "Ysh", "bytes")]
+
+
 class MoeRouting(ctypes.Structure):
     """moe_routing_t: scoring (0 sigmoid, 1 softmax), n_group, topk_group, group_top,
     renorm.  The defaults are the plain router."""
@@ -83,6 +89,7 @@ def load(build_if_missing: bool = True):
     P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     sig = {
         "moe_workspace_bytes": ([ctypes.POINTER(MoeShape)], Z),
+        "moe_workspace_layout": ([ctypes.POINTER(MoeShape), ctypes.POINTER(MoeWorkspaceLayout)], I),
         "moe_error_string": ([I], ctypes.c_char_p),
         "moe_read_status": ([P, P], I),
         "moe_debug_set_wait_limit": ([ctypes.c_ulonglong, I], None),
@@ -92,6 +99,8 @@ def load(build_if_missing: bool = True):
         "moe_router_topk": ([P, P, P, I, I, I, I, P, P, P, Z, P], I),
         "moe_router_topk_ex": ([P, P, P, I, I, I, I, ctypes.POINTER(MoeRouting), P, P, P, Z,
                                 P], I),
+        "moe_router_topk_noalloc": ([P, P, P, I, I, I, I, P, P, P], I),
+        "moe_router_topk_noalloc_status": ([P], I),
         "moe_dispatch": ([P, P, I, I, I, I, P, P, P, P, P, P, P, Z, P], I),
         "moe_expert_ffn": ([P, P, I, I, I, I, P, P, P, P, I, P, Z, P], I),
         "moe_expert_ffn_workspace_bytes": ([I, I, I], Z),
@@ -149,6 +158,15 @@ def moe_workspace_bytes(T, H, E, K, I, I_shared) -> int:
     return int(load().moe_workspace_bytes(ctypes.byref(s)))
 
 
+def moe_workspace_layout(T, H, E, K, I, I_shared) -> dict:
+    """Byte offsets of offsets, perm, slot_pos, Xp, h, Yp and Ysh inside the layer's
+    workspace, and its size ("bytes")."""
+    s = MoeShape(T, H, E, K, I, I_shared)
+    lay = MoeWorkspaceLayout()
+    _check("moe_workspace_layout", load().moe_workspace_layout(ctypes.byref(s), ctypes.byref(lay)))
+    return {n: int(getattr(lay, n)) for n, _ in MoeWorkspaceLayout._fields_}
+
+
 def moe_read_status(ws, stream=None) -> int:
     return int(load().moe_read_status(_ptr(ws), _stream(stream)))
 
@@ -191,6 +209,19 @@ def moe_router_topk_ex(X, W_gate, bias, K, routing, topk_idx, topk_w, ws, stream
     _check("moe_router_topk_ex", load().moe_router_topk_ex(
         _ptr(X), _ptr(W_gate), _ptr(bias), T, H, E, int(K), _routing(routing), _ptr(topk_idx),
         _ptr(topk_w), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_router_topk_noalloc(X, W_gate, bias, K, topk_idx, topk_w, stream=None):
+    """The router without a workspace (its scratch is a fixed array of the library)."""
+    T, H = X.shape
+    E = W_gate.shape[0]
+    _check("moe_router_topk_noalloc", load().moe_router_topk_noalloc(
+        _ptr(X), _ptr(W_gate), _ptr(bias), T, H, E, int(K), _ptr(topk_idx), _ptr(topk_w),
+        _stream(stream)))
+
+
+def moe_router_topk_noalloc_status(stream=None) -> int:
+    return int(load().moe_router_topk_noalloc_status(_stream(stream)))
 
 
 def moe_dispatch(X, topk_idx, E, counts, offsets, perm, slot_pos, Xp, affinity, ws,
@@ -331,6 +362,21 @@ class MoELayer:
 
     def status(self, stream=None) -> int:
         return moe_read_status(self.ws, stream)
+
+    def intermediates(self) -> dict:
+        """Views (no copies) of the last forward's offsets [E+1], perm [T*K], slot_pos
+        [T,K] and Xp [T*K,H] inside the workspace (moe_workspace_layout)."""
+        s = self.shape
+        lay = moe_workspace_layout(s.T, s.H, s.E, s.K, s.I, s.I_shared)
+        TK = s.T * s.K
+
+        def view(off, n, dtype, shape):
+            nbytes = n * torch.empty((), dtype=dtype).element_size()
+            return self.ws[off:off + nbytes].view(dtype).view(*shape)
+        return dict(offsets=view(lay["offsets"], s.E + 1, torch.int32, (s.E + 1,)),
+                    perm=view(lay["perm"], TK, torch.int32, (TK,)),
+                    slot_pos=view(lay["slot_pos"], TK, torch.int32, (s.T, s.K)),
+                    Xp=view(lay["Xp"], TK * s.H, torch.bfloat16, (TK, s.H)))
 
 
 # ------------------------------------------------------ GRACE-MoE placement (host arrays)

@@ -1,8 +1,10 @@
 // api.cu -- the C ABI of include/moe.h: argument validation, workspace layout and the
 // kernel sequence of each entry point.  Everything is enqueued on the caller's stream;
 // nothing here allocates, frees or synchronises (moe_read_status excepted).
+#include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/moe.h"
 #include "kernels.h"
@@ -11,28 +13,31 @@ namespace moe {
 
 int num_sms()
 {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];   // zero-initialised (static storage)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (cache[dev] == 0) {
-        int n = 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
             n = 148;
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
 }
 
 cudaError_t ensure_smem(const void *func, size_t bytes)
 {
-    // small table of (function, device) -> largest limit set so far
+    // small table of (function, device) -> largest limit set so far; host threads making
+    // their first calls at the same time share it, hence the lock
     struct Entry { const void *f; int dev; size_t bytes; };
     static Entry tab[64];
     static int n = 0;
+    static std::mutex mu;
     if (bytes <= 48 * 1024) return cudaSuccess;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < n; ++i)
         if (tab[i].f == func && tab[i].dev == dev && tab[i].bytes >= bytes) return cudaSuccess;
     e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -60,18 +65,34 @@ constexpr int kSideMaxTokens = 128;
 
 // A stream of the library for the shared expert, forked from and joined back into the
 // caller's stream with two events (capturable: the side stream joins a capture through the
-// fork event).  One per host thread and device, created on first use and kept for the
-// process: calls from different threads (on different workspaces) never share the events,
-// and the calls of one thread are sequential.
+// fork event).  One per host thread and device, created on first use and kept until the
+// thread exits: calls from different threads (on different workspaces) never share the
+// events, and the calls of one thread are sequential.
 struct SideStream {
     cudaStream_t s = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
     bool tried = false;
 };
 
+// The side streams of one host thread; released when the thread exits (work still queued
+// on a stream completes first: cudaStreamDestroy defers the release).  Errors are ignored:
+// at process exit the runtime may already be gone.
+struct SideStreams {
+    SideStream tab[64];
+    ~SideStreams()
+    {
+        for (SideStream &ss : tab) {
+            if (ss.fork) cudaEventDestroy(ss.fork);
+            if (ss.join) cudaEventDestroy(ss.join);
+            if (ss.s) cudaStreamDestroy(ss.s);
+        }
+    }
+};
+
 SideStream *side_stream(cudaStream_t caller)
 {
-    thread_local SideStream tab[64];
+    thread_local SideStreams streams;
+    SideStream *tab = streams.tab;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     SideStream &ss = tab[dev];
@@ -191,6 +212,7 @@ struct LayerLayout {
     void *Xp, *h, *Yp, *hs, *Xq;
     float *Ysh;
     unsigned *ready, *ready_sh;   // readiness counters: the FFN launch, the side launch
+    moe_workspace_layout_t at;    // byte offsets of the intermediates inside the workspace
     size_t bytes;
 };
 LayerLayout layer_layout(const moe_shape_t &s, unsigned char *ws)
@@ -200,21 +222,35 @@ LayerLayout layer_layout(const moe_shape_t &s, unsigned char *ws)
     size_t o = kHeader;
     L.r = router_layout(s.T, s.H, s.E, ws ? ws + o : nullptr); o += L.r.bytes;
     L.d = dispatch_layout(s.T, s.E, ws ? ws + o : nullptr); o += L.d.bytes;
-    auto take = [&](size_t b) { unsigned char *p = ws ? ws + o : nullptr; o += al256(b); return p; };
+    size_t at = 0;
+    auto take = [&](size_t b) {
+        unsigned char *p = ws ? ws + o : nullptr;
+        at = o;
+        o += al256(b);
+        return p;
+    };
     L.offsets = reinterpret_cast<int32_t *>(take((s.E + 1) * sizeof(int32_t)));
+    L.at.offsets = at;
     L.perm = reinterpret_cast<int32_t *>(take(TK * sizeof(int32_t)));
+    L.at.perm = at;
     L.slot_pos = reinterpret_cast<int32_t *>(take(TK * sizeof(int32_t)));
+    L.at.slot_pos = at;
     L.Xp = take(TK * s.H * 2);
+    L.at.Xp = at;
     L.h = take(TK * s.I * 2);
+    L.at.h = at;
     L.Yp = take(TK * s.H * 2);
+    L.at.Yp = at;
     L.hs = take(static_cast<size_t>(s.T) * s.I_shared * 2);
     L.Xq = take(static_cast<size_t>(s.T) * s.H * 2);   // FP8 weights: quantised token rows
     L.Ysh = reinterpret_cast<float *>(take(s.I_shared > 0 ? static_cast<size_t>(s.T) * s.H * 4 : 0));
+    L.at.Ysh = at;
     L.ready = reinterpret_cast<unsigned *>(
         take(ffn_ready_slots(static_cast<long long>(TK) + s.T, s.E + 1) * sizeof(unsigned)));
     L.ready_sh = reinterpret_cast<unsigned *>(
         take(s.I_shared > 0 ? ffn_ready_slots(s.T, 1) * sizeof(unsigned) : 0));
     L.bytes = o;
+    L.at.bytes = o;
     return L;
 }
 
@@ -364,6 +400,15 @@ size_t moe_workspace_bytes(const moe_shape_t *shape)
 {
     if (check_shape(shape) != MOE_OK) return 0;
     return layer_layout(*shape, nullptr).bytes;
+}
+
+int moe_workspace_layout(const moe_shape_t *shape, moe_workspace_layout_t *out)
+{
+    if (!out) return MOE_ERR_INVALID_ARG;
+    const int rc = check_shape(shape);
+    if (rc) return rc;
+    *out = layer_layout(*shape, nullptr).at;
+    return MOE_OK;
 }
 
 const char *moe_error_string(int status)

@@ -13,7 +13,10 @@
 // kRouterScratchBytes bytes.  In host code the array's name is only a stand-in for the
 // device object, so its device address is looked up with cudaGetSymbolAddress, once per
 // device, with that device current, on the first call made on that device; the kernel is
-// then given that address.  No call here allocates or frees memory.
+// then given that address.  The address belongs to the device's current CUDA context: if
+// the context is destroyed and created again (cudaDeviceReset), the module is loaded again
+// and the array may move, so the cache also remembers the context's unique id and repeats
+// the lookup when it changes.  No call here allocates or frees memory.
 #include <mutex>
 
 #include "../../include/moe.h"
@@ -28,24 +31,60 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_router_scratch[kRouterScratchBytes];
 
-std::mutex g_setup_mutex;
-unsigned char *g_scratch_addr[kMaxDevices] = {};
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
 
-// Device address of g_router_scratch on the current device (looked up on first use).
+// Unique id of the calling thread's current context (driver entry points looked up once).
+bool current_context_id(unsigned long long *id)
+{
+    static const CtxGetCurrentFn get_current = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        return (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                                 &q) == cudaSuccess && q == cudaDriverEntryPointSuccess)
+                   ? reinterpret_cast<CtxGetCurrentFn>(p) : nullptr;
+    }();
+    static const CtxGetIdFn get_id = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        return (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault,
+                                                 &q) == cudaSuccess && q == cudaDriverEntryPointSuccess)
+                   ? reinterpret_cast<CtxGetIdFn>(p) : nullptr;
+    }();
+    CUcontext ctx = nullptr;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+std::mutex g_setup_mutex;
+struct ScratchAddr {
+    unsigned long long ctx_id = 0;
+    unsigned char *addr = nullptr;
+};
+ScratchAddr g_scratch[kMaxDevices];
+
+// Device address of g_router_scratch on the current device (looked up on first use, and
+// again whenever the device's context changed since).
 cudaError_t scratch_address(unsigned char **out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);   // false before the runtime set up the context
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_addr[dev]) {
+    ScratchAddr &sa = g_scratch[dev];
+    if (!have_id || !sa.addr || sa.ctx_id != id) {
         void *p = nullptr;
+        // (also makes the device's primary context current when the runtime has not yet)
         e = cudaGetSymbolAddress(&p, g_router_scratch);
         if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = static_cast<unsigned char *>(p);
+        if (!current_context_id(&id)) return cudaErrorDeviceUninitialized;
+        sa.addr = static_cast<unsigned char *>(p);
+        sa.ctx_id = id;
     }
-    *out = g_scratch_addr[dev];
+    *out = sa.addr;
     return cudaSuccess;
 }
 
@@ -82,4 +121,17 @@ extern "C" int moe_router_topk_noalloc(const void *X, const void *W_gate, const 
                                         reinterpret_cast<int *>(base),
                                         static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" int moe_router_topk_noalloc_status(void *stream)
+{
+    using namespace moe;
+    unsigned char *base = nullptr;
+    if (scratch_address(&base) != cudaSuccess) return MOE_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaMemcpyAsync(&v, base, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(base, 0, sizeof v, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return v;
 }

@@ -31,7 +31,7 @@
  *     moe_layer_forward on bf16 weights up to 128 tokens: it forks the shared expert onto a
  *     side stream of the library and joins it back before the combine; that stream and
  *     its two events are created by the first such call of a host thread on a device and
- *     kept for the process.)
+ *     released when that thread exits.)
  *   - `ws` is a caller-owned device workspace of at least moe_workspace_bytes() bytes
  *     (256-byte aligned).  Its first 4 bytes are the status word: zero them once after
  *     allocating (e.g. cudaMemset); moe_read_status() resets the word after reading it.
@@ -106,6 +106,21 @@ typedef struct moe_weights_fp8 {
 /* Bytes of workspace that moe_layer_forward needs for `shape`; it also suffices for every
  * other entry point called with the same or smaller sizes.  Returns 0 for an invalid shape. */
 size_t moe_workspace_bytes(const moe_shape_t *shape);
+
+/* Where moe_layer_forward keeps its intermediate results inside the workspace: byte
+ * offsets from `ws` of offsets int32 [E + 1], perm int32 [T*K], slot_pos int32 [T, K] (the
+ * dispatch bookkeeping, as moe_dispatch defines it), Xp bf16 [T*K, H] (the permuted token
+ * rows), h bf16 [T*K, I] (the SwiGLU activations), Yp bf16 [T*K, H] (the expert outputs)
+ * and Ysh fp32 [T, H] (the shared expert's output; 0 when I_shared == 0), and `bytes` =
+ * moe_workspace_bytes(shape).  They hold what the last layer call on that workspace left
+ * there, once its stream has reached the end of the call (with FP8 experts, Xp and h hold
+ * the rows after their quantisation to E4M3 and back).  For inspection and testing; not on
+ * the pages.  Returns MOE_OK, or MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED_SHAPE for a
+ * shape moe_workspace_bytes rejects. */
+typedef struct moe_workspace_layout {
+    size_t offsets, perm, slot_pos, Xp, h, Yp, Ysh, bytes;
+} moe_workspace_layout_t;
+int moe_workspace_layout(const moe_shape_t *shape, moe_workspace_layout_t *out);
 
 /* Static, NUL-terminated description of a moe_status_t value. */
 const char *moe_error_string(int status);
@@ -201,17 +216,29 @@ int moe_router_topk_ex(const void *X, const void *W_gate, const float *bias,
  * whose host application owns all device memory and hands out only the input and output
  * buffers, or a path whose allocator is frozen after start-up.
  *   - The first call on a device looks up the array's device address (with that device
- *     current) and caches it; make that first call before any stream capture.
+ *     current) and caches it together with the id of the device's context; make that
+ *     first call before any stream capture.  If the context is destroyed and created again
+ *     (cudaDeviceReset), the next call sees the new context id and looks the address up
+ *     again.
  *   - Allocates and frees nothing.  Shapes whose router scratch does not fit in 16 MiB
  *     return MOE_ERR_UNSUPPORTED_SHAPE before anything is enqueued (every T <= 2048 with
  *     E <= 256 and H <= 7168 fits).
  *   - All calls on a device share the one array and it keeps what the last call left;
  *     the part that must start at zero is cleared on `stream` by every call.  Calls whose
  *     work overlaps on the GPU (other streams, other host threads) race on the array:
- *     serialise them. */
+ *     serialise them.
+ *   - Conditions found on the device (a bounded wait of the large-batch router kernel that
+ *     ran out: MOE_ERR_DEVICE_TIMEOUT) go to a status word inside the array, which only
+ *     moe_router_topk_noalloc_status reads. */
 int moe_router_topk_noalloc(const void *X, const void *W_gate, const float *bias,
                             int T, int H, int E, int K,
                             int32_t *topk_idx, float *topk_w, void *stream);
+
+/* Status word of moe_router_topk_noalloc on the current device: synchronises `stream`,
+ * returns what the word held (MOE_OK or MOE_ERR_DEVICE_TIMEOUT; MOE_ERR_CUDA if the copy
+ * failed) and resets it to MOE_OK.  Like moe_read_status, but for the library's own array
+ * (no workspace); allocates nothing.  Not on the pages. */
+int moe_router_topk_noalloc_status(void *stream);
 
 /* Dispatch: the single-GPU counterpart of the AllToAll Dispatch ("Lower latency and higher
  * throughput...", Expert Parallelism; MoE Router: per-expert aggregated routing info).

@@ -204,6 +204,48 @@ def layer_tokens(X: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray,
     return Y
 
 
+def layer_tokens_by_expert(X: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray,
+                           fetch_expert, shared, tokens, I: int, Is: int,
+                           experts_per_pass: int = 16) -> np.ndarray:
+    """The same Y as ``layer_tokens`` (fp64), evaluated expert by expert so that only a few
+    experts' weights need to be on the host at a time.
+
+    fetch_expert(e) returns the bf16 (W1 [H,I], W3 [H,I], W2 [I,H]) arrays of expert e;
+    shared is (W1s, W3s, W2s) or None.  The (token, slot) pairs of the listed tokens are
+    grouped by expert; each pass fetches `experts_per_pass` experts and evaluates all their
+    pairs (``expert_rows``).  Then Y[q] = sum_j w[t,j] y[q,j] + y_shared[q], j ascending,
+    for t = tokens[q]."""
+    X = _u16(X)
+    H = X.shape[1]
+    K = topk_idx.shape[1]
+    tokens = np.asarray(tokens, dtype=np.int64)
+    n = len(tokens)
+    ysel = np.zeros((n, K, H), np.float64)
+    pairs = {}
+    for q, t in enumerate(tokens):
+        for j in range(K):
+            pairs.setdefault(int(topk_idx[t, j]), []).append((q, j))
+    experts = sorted(pairs)
+    for c in range(0, len(experts), experts_per_pass):
+        chunk = experts[c:c + experts_per_pass]
+        weights = {e: fetch_expert(e) for e in chunk}
+        rows = [(e, q, j) for e in chunk for (q, j) in pairs[e]]
+        y = expert_rows([X[tokens[q]] for (_, q, _) in rows],
+                        [weights[e][0] for (e, _, _) in rows],
+                        [weights[e][1] for (e, _, _) in rows],
+                        [weights[e][2] for (e, _, _) in rows], H, I)
+        for r, (_, q, j) in enumerate(rows):
+            ysel[q, j] = y[r]
+        del weights
+    Y = np.zeros((n, H), np.float64)
+    for j in range(K):
+        Y += topk_w[tokens, j][:, None] * ysel[:, j]
+    if shared is not None and Is > 0:
+        W1s, W3s, W2s = shared
+        Y += expert_rows([X[t] for t in tokens], [W1s] * n, [W3s] * n, [W2s] * n, H, Is)
+    return Y
+
+
 def combine(Yp: np.ndarray, slot_pos: np.ndarray, topk_w: np.ndarray,
             Ysh: np.ndarray | None = None) -> np.ndarray:
     """Y[t] = sum_j topk_w[t,j] * Yp[slot_pos[t,j]] (+ Ysh[t]); Yp bf16 bits [rows,H]."""

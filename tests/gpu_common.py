@@ -79,20 +79,53 @@ class Problem:
                              self.w.K)
 
     def oracle_Y(self, idx, wts, tokens) -> np.ndarray:
-        used = sorted({int(e) for t in tokens for e in idx[t]})
-        W1 = {e: self.expert_host("W1", e) for e in used}
-        W3 = {e: self.expert_host("W3", e) for e in used}
-        W2 = {e: self.expert_host("W2", e) for e in used}
-        sh = [None] * 3
+        """Y of the listed tokens, evaluated by the oracle expert by expert (only a few
+        experts' weights are copied to the host at a time)."""
+        sh = None
         if self.w.Is > 0:
-            sh = [self.expert_host(n) for n in ("W1s", "W3s", "W2s")]
-        return oracle.layer_tokens(self.routing["X"], idx, wts, W1, W3, W2, *sh, tokens,
-                                   self.w.I, self.w.Is)
+            sh = tuple(self.expert_host(n) for n in ("W1s", "W3s", "W2s"))
+        fetch = lambda e: tuple(self.expert_host(n, e) for n in ("W1", "W3", "W2"))
+        return oracle.layer_tokens_by_expert(self.routing["X"], idx, wts, fetch, sh, tokens,
+                                             self.w.I, self.w.Is)
 
 
-def check_layer(p: Problem, tokens=None, check_affinity=True):
-    """Full-layer parity: routing, counts and affinity bit-exact over all tokens; Y on
-    `tokens` (all tokens when None) within the stated tolerances."""
+def covering_tokens(idx: np.ndarray, n: int) -> list:
+    """At least n tokens (all of them when T <= n) such that every expert some token chose
+    appears: for each chosen expert, in increasing order, the first token choosing it;
+    then evenly spaced tokens up to n, plus the first and the last token."""
+    T = idx.shape[0]
+    if T <= n:
+        return list(range(T))
+    first = {}
+    for t in range(T):
+        for e in idx[t]:
+            first.setdefault(int(e), t)
+    chosen = set(first.values()) | {0, T - 1}
+    for t in np.linspace(0, T - 1, n).astype(int):
+        if len(chosen) >= n:
+            break
+        chosen.add(int(t))
+    return sorted(chosen)
+
+
+def check_dispatch(layer, X: torch.Tensor, d: dict):
+    """The layer's own dispatch results (offsets, perm, slot_pos and Xp in its workspace)
+    against the oracle's dispatch of the same routing: bit-exact."""
+    inter = layer.intermediates()
+    assert np.array_equal(inter["offsets"].cpu().numpy(), d["offsets"]), "offsets differ"
+    perm_g = inter["perm"].cpu().numpy()
+    bad = np.nonzero(perm_g != d["perm"])[0]
+    assert bad.size == 0, f"perm differs at rows {bad[:10]}"
+    slot_g = inter["slot_pos"].cpu().numpy()
+    assert np.array_equal(slot_g, d["slot_pos"]), "slot_pos differs"
+    perm_o = torch.from_numpy(d["perm"].astype(np.int64)).to(X.device)
+    assert torch.equal(inter["Xp"].view(torch.int16), X.view(torch.int16)[perm_o]), "Xp != X[perm]"
+
+
+def check_layer(p: Problem, tokens=None, check_affinity=True, n_cover=None):
+    """Full-layer parity: routing, counts, the dispatch bookkeeping (offsets, perm,
+    slot_pos, Xp) and affinity bit-exact over all tokens; Y on `tokens` (all tokens when
+    None, or with n_cover set, covering_tokens(n_cover)) within the stated tolerances."""
     layer = p.run_layer(with_affinity=check_affinity)
     idx_o, w_o = p.oracle_routing()
     idx_g = layer.topk_idx.cpu().numpy()
@@ -102,9 +135,12 @@ def check_layer(p: Problem, tokens=None, check_affinity=True):
     assert w_err <= W_MAX_ABS, w_err
     d = oracle.dispatch(idx_o, p.w.E, want_affinity=check_affinity)
     assert np.array_equal(layer.counts.cpu().numpy(), d["counts"])
+    check_dispatch(layer, p.X, d)
     if check_affinity:
         assert np.array_equal(layer.affinity.cpu().numpy(), d["affinity"])
-    if tokens is None:
+    if n_cover is not None:
+        tokens = covering_tokens(idx_o, n_cover)
+    elif tokens is None:
         tokens = np.arange(p.w.T)
     tokens = np.asarray(tokens)
     Y_o = p.oracle_Y(idx_o, w_o, tokens)
@@ -112,4 +148,4 @@ def check_layer(p: Problem, tokens=None, check_affinity=True):
     rf = rel_frob(Y_g, Y_o)
     ma = float(np.abs(Y_g - Y_o).max())
     assert rf <= Y_REL_FROB and ma <= Y_MAX_ABS, (rf, ma)
-    return dict(layer=layer, rel_frob=rf, max_abs=ma, idx=idx_o, w=w_o, disp=d)
+    return dict(layer=layer, rel_frob=rf, max_abs=ma, idx=idx_o, w=w_o, disp=d, tokens=tokens)

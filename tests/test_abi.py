@@ -102,3 +102,26 @@ def test_routing_options_are_validated_before_launch(lib):
     # valid options reach the next check (the 16-byte workspace is too small)
     assert call(16, 2, n_group=4, topk_group=2, group_top=2, scoring="softmax") == -4
     assert f(ok, ok, ok, 4, 256, 16, 2, None, ok, ok, ws, 16, None) == -4   # NULL = defaults
+
+
+@pytest.mark.parametrize("shape", [(128, 7168, 256, 8, 2048, 2048), (16, 256, 16, 2, 128, 128),
+                                   (1, 64, 1, 1, 64, 0), (16384, 7168, 256, 8, 2048, 2048)])
+def test_workspace_layout_lies_inside_the_workspace(shape):
+    T, H, E, K, I, Is = shape
+    lay = binding.moe_workspace_layout(*shape)
+    assert lay["bytes"] == binding.moe_workspace_bytes(*shape)
+    ends = [("offsets", (E + 1) * 4), ("perm", T * K * 4), ("slot_pos", T * K * 4),
+            ("Xp", T * K * H * 2), ("h", T * K * I * 2), ("Yp", T * K * H * 2)]
+    prev_end = 256                      # the status header comes first
+    for name, nbytes in ends:
+        assert lay[name] % 256 == 0, name
+        assert lay[name] >= prev_end, name
+        prev_end = lay[name] + nbytes
+    assert prev_end <= lay["bytes"]
+    if Is:
+        assert lay["Ysh"] % 256 == 0 and lay["Ysh"] + T * H * 4 <= lay["bytes"]
+
+
+def test_workspace_layout_rejects_what_the_size_query_rejects():
+    with pytest.raises(binding.MoeError):
+        binding.moe_workspace_layout(1, 100, 16, 2, 128, 0)       # H % 64 != 0

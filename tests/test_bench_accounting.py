@@ -33,3 +33,40 @@ def test_launches_per_step_by_batch_size():
     # quantisation, up launch, two h quantisations, down launch, and combine
     w = synth.workload("decode")
     assert bench.launches_per_step(w, True, fp8=True) == 2 + 1 + 5 + 1
+
+
+def test_targets_by_batch_size():
+    assert bench.target_of(synth.workload("sweep2")) == ("hbm_frac_of_8TBs", 0.70)
+    assert bench.target_of(synth.workload("sweep64")) == ("hbm_frac_of_8TBs", 0.70)
+    assert bench.target_of(synth.workload("decode")) == (None, None)
+    assert bench.target_of(synth.workload("skewed")) == ("tensor_frac", 0.60)
+    assert bench.target_of(synth.workload("prefill")) == ("tensor_frac", 0.60)
+
+
+def test_layer_roofline_fractions():
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0}
+    w = synth.workload("sweep2")
+    n_act = 16
+    _, _, lb, lf = bench.algorithmic(w, n_act, 2, bench.shared_on_side(w))
+    ms = lb / 8e12 * 1e3          # a step moving the algorithmic bytes at exactly 8 TB/s
+    r = bench.layer_roofline(w, n_act, ms, peaks)
+    assert abs(r["hbm_frac_of_8TBs"] - 1.0) < 1e-3
+    assert abs(r["hbm_frac"] - 8000.0 / 6000.0) < 1e-3
+    assert abs(r["tensor_frac"] * 2000.0 - r["tensor_frac_sustained"] * 1600.0) < 1e-3 * 2000
+
+
+def test_every_side_workload_exists_and_shares_the_weights():
+    base = synth.workload("decode")
+    for name in bench.SIDE_WORKLOADS:
+        w = synth.workload(name)
+        assert (w.H, w.E, w.K, w.I, w.Is, w.seed) == (base.H, base.E, base.K, base.I, base.Is,
+                                                      base.seed)
+
+
+def test_gpus_flag_must_match_world_size(monkeypatch):
+    import pytest
+    monkeypatch.setattr("sys.argv", ["bench.py", "--gpus", "2"])
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    with pytest.raises(SystemExit) as e:
+        bench.main()
+    assert e.value.code not in (0, None)

@@ -196,3 +196,39 @@ def test_route_table_rows_are_distributions():
     t = grace.route_table(rep, gpus_per_node=4)["table"]
     np.testing.assert_allclose(t.sum(1), 1.0, atol=1e-14)
     assert np.all(t >= 0)
+
+
+# ------------------------------------------------- experts with no co-activation at all
+def _blocks_and_isolated(block_sizes, n_isolated, v=10):
+    n = sum(block_sizes) + n_isolated
+    A = np.zeros((n, n), np.int32)
+    start = 0
+    for b in block_sizes:
+        A[start:start + b, start:start + b] = v
+        start += b
+    np.fill_diagonal(A, 0)
+    return A
+
+
+@pytest.mark.parametrize("block_sizes,r,expected", [
+    # blocks {0,1,2} and {3,4,5}; isolated 6 and 7.  Both groups hold 3 experts when the
+    # isolated ones are placed: 6 goes to the lower group id, then 7 to the other group
+    ((3, 3), 0.5, [0, 0, 0, 1, 1, 1, 0, 1]),
+    # blocks {0,1,2,3} and {4,5}: the smaller group takes both isolated experts
+    ((4, 2), 0.5, [0, 0, 0, 0, 1, 1, 1, 1]),
+    ((4, 2), 0.0, [0, 0, 0, 0, 1, 1, 1, 1]),
+])
+def test_isolated_experts_join_the_smallest_group(block_sizes, r, expected):
+    # An expert that no token co-activates with another has a zero row in A: its spectral
+    # embedding row is zero (rounding noise only), so its position carries no affinity.
+    # The grouping's reading places each such expert, in index order, into the group that
+    # is smallest at that moment (lower group id on ties).  Worked by hand: the D = 2
+    # leading eigenvectors span the two blocks' indicator vectors, every block maps to one
+    # unit vector and the blocks become the groups (first seed: the expert of largest
+    # degree, i.e. expert 0; second: the farthest point, a member of the other block).
+    A = _blocks_and_isolated(block_sizes, 2)
+    g = grace.group(A, 2, r)
+    assert _same_partition(g, np.array(expected)), g.tolist()
+    assert g[6] != g[7] if block_sizes == (3, 3) else g[6] == g[7] == g[4]
+    U, _ = grace.metrics(A, g, 2)
+    assert U == 1.0                      # every co-activation stays inside a group

@@ -114,3 +114,19 @@ def test_skewed_routing_groups_follow_the_clusters():
     assert lib["knee"] > 0 and lib["U"][lib["knee"]] >= U_clusters - 0.02
     rep = B.moe_grace_replicate(counts, lib["group_of"], 8)
     assert rep["hot"] == grace.replicate(counts, lib["group_of"], 8)["hot"]
+
+
+@pytest.mark.parametrize("block_sizes,r", [((3, 3), 0.5), ((4, 2), 0.5), ((4, 2), 0.0)])
+def test_isolated_experts_are_placed_like_the_oracle(block_sizes, r):
+    # experts with no co-activation (zero rows of A) go to the smallest group, as the
+    # oracle's reading places them (pinned by hand in test_grace_oracle)
+    n = sum(block_sizes) + 2
+    A = np.zeros((n, n), np.int32)
+    s = 0
+    for b in block_sizes:
+        A[s:s + b, s:s + b] = 10
+        s += b
+    np.fill_diagonal(A, 0)
+    g_lib = B.moe_grace_group(A, 2, r)
+    g_ref = grace.group(A, 2, r)
+    assert _same_partition(g_lib, g_ref), (g_lib.tolist(), g_ref.tolist())

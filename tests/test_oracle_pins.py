@@ -288,6 +288,34 @@ def test_ffn_matches_library_matmul():
     np.testing.assert_allclose(out["Y"], Y, rtol=1e-12, atol=1e-13)
 
 
+@pytest.mark.parametrize("per_pass,shared", [(1, True), (3, True), (16, False)])
+def test_expert_by_expert_evaluation_matches_library_matmul(per_pass, shared):
+    # layer_tokens_by_expert (the form the DeepSeek-V3-sized parity tests use, fetching a
+    # few experts at a time) against numpy float64 matmuls, on a token subset
+    w, inp = _tiny_layer(7)
+    idx, wts = oracle.router(inp["X"], inp["W_gate"], inp["bias"], w.K)
+    X = _val(inp["X"])
+    W1, W3, W2 = (_val(inp[n]) for n in ("W1", "W3", "W2"))
+    tokens = [w.T - 1, 0, 5, 5, 3]
+    fetched = []
+
+    def fetch(e):
+        fetched.append(e)
+        return inp["W1"][e], inp["W3"][e], inp["W2"][e]
+    sh = (inp["W1s"], inp["W3s"], inp["W2s"]) if shared else None
+    Y = oracle.layer_tokens_by_expert(inp["X"], idx, wts, fetch, sh, tokens, w.I, w.Is,
+                                      experts_per_pass=per_pass)
+    used = sorted({int(e) for t in tokens for e in idx[t]})
+    assert fetched == used                      # every needed expert once, in order
+    for q, t in enumerate(tokens):
+        ref = _np_ffn(X[t], _val(inp["W1s"]), _val(inp["W3s"]), _val(inp["W2s"])) if shared \
+            else np.zeros(w.H)
+        for j in range(w.K):
+            e = idx[t, j]
+            ref = ref + wts[t, j] * _np_ffn(X[t], W1[e], W3[e], W2[e])
+        np.testing.assert_allclose(Y[q], ref, rtol=1e-12, atol=1e-13)
+
+
 def test_identical_experts_collapse():
     w, inp = _tiny_layer(3)
     for n in ("W1", "W3", "W2"):
