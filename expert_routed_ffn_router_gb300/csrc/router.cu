@@ -93,9 +93,10 @@ using SmallCfg = Cfg<16, 256, 4, 4, 2>;
 // Warp-specialised CTA tile (gemm_tile_ws): TT x TE on the eight compute warps, TPT x EPT
 // outputs a thread in paired fp32 FMAs (two tokens per instruction -- the same correctly
 // rounded operations in the same order as two fmaf, in half the FMA instructions).
-template <int TT_, int TE_, int TPT_, int EPT_>
+template <int TT_, int TE_, int TPT_, int EPT_, int RING_ = 4, int STG_ = 4>
 struct WsCfg {
     static constexpr int TT = TT_, TE = TE_, TPT = TPT_, EPT = EPT_;
+    static constexpr int RING = RING_, STG = STG_;        // fp32 ring and bf16 staging stages
     static constexpr int NTY = TT / TPT, NTX = TE / EPT;
     static constexpr int LY = 4;                          // token groups per warp
     static_assert(NTX * NTY == NT, "one output micro-tile per compute thread");
@@ -106,6 +107,9 @@ struct WsCfg {
 // read 12 per 32 and was bound by shared-memory bandwidth); one CTA per SM holds the
 // 64 paired running sums.
 using LargeCfg = WsCfg<128, 128, 8, 8>;
+// 16 tokens x 256 experts, 4 x 4 outputs a thread, for batches of 16 to 2048 tokens: one
+// CTA per SM (four-stage fp32 and staging rings).
+using SmallWsCfg = WsCfg<16, 256, 4, 4, 4, 4>;
 
 // Two fp32 lanes per 64-bit register: d = a * b + c and d = a + b, each lane correctly
 // rounded (the same results as two fmaf / two fp32 adds).
@@ -243,54 +247,114 @@ __device__ double dot_double_word(const uint16_t *x, const uint16_t *w, int H, i
     return static_cast<double>(h) + static_cast<double>(l);
 }
 
+// Monotone 64-bit key of an fp64 score: a larger score gives a larger key; -0 and +0 give
+// the same key; NaN gives the key of -infinity (it orders below every number).
+__device__ __forceinline__ unsigned long long key64(double v)
+{
+    v = v == v ? v + 0.0 : -INFINITY;
+    const unsigned long long u = static_cast<unsigned long long>(__double_as_longlong(v));
+    return (u & 0x8000000000000000ull) ? ~u : (u | 0x8000000000000000ull);
+}
+
 // Top-K of a token among `n` candidate (expert, sel64) pairs by (sel64 desc, expert asc);
 // writes the experts and their renormalised weights.  Warp-wide; pairs live in shared
-// memory; taken pairs are marked by storing -1 - expert.
+// memory; taken pairs are marked by storing -1 - expert.  The order is the one before64
+// defines, decided on integer keys: every lane keeps its best untaken pair as (key64 of
+// the score, ~expert), and a round's winner is the lane maximum of the score keys, then of
+// ~expert among the lanes that hold that key (hardware reductions, no fp64 compares).
 __device__ void select_refined(int *pe, const double *pv, int n, int K, const float *bias,
                                int32_t *oi, float *ow, int *ord, int lane, int renorm = 1)
 {
+    // lists of up to 32 candidates (the usual case): each lane's key in registers
+    const bool reg = n <= 32;
+    const unsigned long long rk = (reg && lane < n) ? key64(pv[lane]) : 0ull;
     for (int j = 0; j < K; ++j) {
-        double bs = -DBL_MAX;
-        int be = INT_MAX, bp = -1;
-        for (int q = lane; q < n; q += 32) {
-            const int e = pe[q];
-            if (e < 0) continue;
-            const double v = pv[q];
-            if (be == INT_MAX || before64(v, e, bs, be)) { bs = v; be = e; bp = q; }
+        unsigned long long bk = 0ull;     // 0: no untaken pair (every real key is larger)
+        uint32_t bi = 0u;                 // ~expert of the lane's best
+        int bp = -1;
+        if (reg) {
+            if (lane < n && pe[lane] >= 0) { bk = rk; bi = ~static_cast<uint32_t>(pe[lane]); bp = lane; }
+        } else {
+            for (int q = lane; q < n; q += 32) {
+                const int e = pe[q];
+                if (e < 0) continue;
+                const unsigned long long k = key64(pv[q]);
+                const uint32_t ie = ~static_cast<uint32_t>(e);
+                if (k > bk || (k == bk && ie > bi)) { bk = k; bi = ie; bp = q; }
+            }
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const double os = __shfl_xor_sync(kFullMask, bs, off);
-            const int oe = __shfl_xor_sync(kFullMask, be, off);
-            const int op = __shfl_xor_sync(kFullMask, bp, off);
-            if (oe != INT_MAX && (be == INT_MAX || before64(os, oe, bs, be))) { bs = os; be = oe; bp = op; }
-        }
-        if (lane == 0) ord[j] = bp;
+        const uint32_t kh = static_cast<uint32_t>(bk >> 32), kl = static_cast<uint32_t>(bk);
+        const uint32_t mh = __reduce_max_sync(kFullMask, kh);
+        const uint32_t ml = __reduce_max_sync(kFullMask, kh == mh ? kl : 0u);
+        const bool top = kh == mh && kl == ml;
+        const uint32_t mi = __reduce_max_sync(kFullMask, top ? bi : 0u);
+        const uint32_t win = __ballot_sync(kFullMask, top && bi == mi && bp >= 0);
+        const int wp = win ? __shfl_sync(kFullMask, bp, __ffs(win) - 1) : -1;
+        if (lane == 0) ord[j] = wp;
         __syncwarp();
-        if (bp >= 0 && lane == (bp & 31)) pe[bp] = -1 - be;
+        if (wp >= 0 && lane == (wp & 31)) pe[wp] = -1 - pe[wp];
         __syncwarp();
     }
-    // (callers pass at least K candidates; a round that found none writes expert 0 with
-    // weight 0 rather than an index outside the list)
-    auto expert_of = [&](int q) { return pe[q] < 0 ? -1 - pe[q] : pe[q]; };
-    double den = 0.0;
-    for (int j = 0; j < K; ++j) {
-        const int q = ord[j];
-        if (q >= 0) den += pv[q] - static_cast<double>(bias[expert_of(q)]);
+    // weights: the selected unbiased scores (fp64 minus the bias), renormalised in fp32
+    // (a relative error of a few 1e-7); lane j < K holds slot j.  A round that found no
+    // pair (callers pass at least K candidates) writes expert 0 with weight 0 rather than
+    // an index outside the list.
+    int e = 0;
+    float sc = 0.f;
+    const int q = lane < K ? ord[lane] : -1;
+    if (q >= 0) {
+        e = pe[q] < 0 ? -1 - pe[q] : pe[q];
+        sc = static_cast<float>(pv[q] - static_cast<double>(bias[e]));
     }
-    for (int j = lane; j < K; j += 32) {
-        const int q = ord[j];
-        if (q < 0) {
-            oi[j] = 0;
-            ow[j] = 0.f;
-            continue;
-        }
-        const int e = expert_of(q);
-        oi[j] = e;
-        const double sc = pv[q] - static_cast<double>(bias[e]);
-        ow[j] = static_cast<float>(renorm ? sc / den : sc);
+    float den = 0.f;
+    for (int j = 0; j < K; ++j) den += __shfl_sync(kFullMask, sc, j);
+    if (lane < K) {
+        oi[lane] = e;
+        ow[lane] = q < 0 ? 0.f : (renorm ? sc / den : sc);
     }
     __syncwarp();
+}
+
+// Double-word partial dot product of a token row and a gate row over the 8-element
+// vectors [v0, v1), reduced over the warp in a fixed order (every lane gets (h, l)).  A
+// group of warps splits one dot into such ranges and merges the partials in rank order.
+__device__ void dot_dw_range(const uint16_t *x, const uint16_t *w, int v0, int v1, int lane,
+                             float &h, float &l)
+{
+    constexpr int U = 4;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x);
+    const uint4 *wr = reinterpret_cast<const uint4 *>(w);
+    float hi[U], lo[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) { hi[u] = 0.f; lo[u] = 0.f; }
+    for (int v = v0 + lane; v < v1; v += 32 * U) {
+        uint4 xa[U], wa[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const bool ok = v + 32 * u < v1;
+            xa[u] = ok ? __ldg(xr + v + 32 * u) : make_uint4(0, 0, 0, 0);
+            wa[u] = ok ? __ldg(wr + v + 32 * u) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float xf[8], wf[8];
+            unpack8(xa[u], xf);
+            unpack8(wa[u], wf);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dw_add(hi[u], lo[u], __fmul_rn(xf[i], wf[i]));  // exact product
+        }
+    }
+    dw_merge(hi[0], lo[0], hi[1], lo[1]);
+    dw_merge(hi[2], lo[2], hi[3], lo[3]);
+    dw_merge(hi[0], lo[0], hi[2], lo[2]);
+    h = hi[0];
+    l = lo[0];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float ohi = __shfl_xor_sync(kFullMask, h, off);
+        const float olo = __shfl_xor_sync(kFullMask, l, off);
+        dw_merge(h, l, ohi, olo);
+    }
 }
 
 // Bound constants of the summation tree: gamma_d and the inflation of computed norms.
@@ -333,14 +397,27 @@ __device__ __forceinline__ void sort8_desc(unsigned long long (&k)[8])
     cas_desc(k[1], k[2]); cas_desc(k[3], k[4]); cas_desc(k[5], k[6]);
 }
 
-// Scores one token held by one warp and selects its top-K in fp32 with the certified
-// error bound.  `w_sel` holds the token's fp32 logits on entry (lane owns e = lane + 32i);
-// it is overwritten with sel, and w_bnd / w_sc receive the bound and the sigmoid.
-// Returns true when the result is certified and written; otherwise `cand` holds the
-// lane's candidate bits and `n_cand` their warp-wide count.
-__device__ bool score_select(int E, int K, float nx, const float *nw, const float *bias,
-                             float gam, float *w_sel, float *w_bnd, float *w_sc,
-                             int32_t *oi, float *ow, uint32_t &cand, int &n_cand, int lane)
+// Score, selection key and error bound of one expert of a token: l is the fp32 logit,
+// bl = gam ||x|| ||w_e|| bounds its summation error; s = sigmoid(l) and sel = s + b carry
+// the bound propagated through the sigmoid (|sigmoid'| <= min(1/4, e^-(|l| - bl))) plus the
+// fp32 rounding of the sigmoid and of the add.
+__device__ __forceinline__ void score_expert(float l, float bl, float b, float &sel, float &bnd,
+                                             float &s)
+{
+    s = 1.f / (1.f + expf(-l));
+    sel = s + b;
+    const float al = fabsf(l);
+    const float D = (al > bl) ? fminf(0.25f, __expf(-(al - bl)) * 1.01f) : 0.25f;
+    bnd = bl * D + 4.f * kU + fabsf(sel) * (2.f * kU);
+}
+
+// Selects the top-K of one token held by one warp from its scored experts (w_sel, w_bnd,
+// w_sc as score_expert leaves them; lane owns e = lane + 32i) in fp32 with the certified
+// error bound.  Returns true when the result is certified and written; otherwise `cand`
+// holds the lane's candidate bits and `n_cand` their warp-wide count.
+__device__ bool select_scored(int E, int K, const float *w_sel, const float *w_bnd,
+                              const float *w_sc, int32_t *oi, float *ow, uint32_t &cand,
+                              int &n_cand, int lane)
 {
     const int NI = (E + 31) / 32;
     const bool fast = NI <= 8;                // keys of <= 256 experts fit in registers
@@ -348,28 +425,21 @@ __device__ bool score_select(int E, int K, float nx, const float *nw, const floa
 #pragma unroll
     for (int i = 0; i < 8; ++i) key[i] = 0ull;
     unsigned long long best = 0ull;           // generic path: lane's best untaken key
-    for (int i = 0; i < NI; ++i) {
-        const int e = lane + 32 * i;
-        if (e >= E) break;
-        const float l = w_sel[e];
-        const float bl = gam * nx * nw[e] + 1e-30f;
-        const float s = 1.f / (1.f + expf(-l));
-        const float sel = s + bias[e];
-        const float al = fabsf(l);
-        const float D = (al > bl) ? fminf(0.25f, __expf(-(al - bl)) * 1.01f) : 0.25f;
-        w_sel[e] = sel;
-        w_bnd[e] = bl * D + 4.f * kU + fabsf(sel) * (2.f * kU);
-        w_sc[e] = s;
-        const unsigned long long k = rank_key(sel, e);
-        if (fast) {
+    if (fast) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (u == i) key[u] = k;
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane + 32 * i;
+            if (i < NI && e < E) key[i] = rank_key(w_sel[e], e);
         }
-        best = k > best ? k : best;
+        sort8_desc(key);
+    } else {
+        for (int i = 0; i < NI; ++i) {
+            const int e = lane + 32 * i;
+            if (e >= E) break;
+            const unsigned long long k = rank_key(w_sel[e], e);
+            best = k > best ? k : best;
+        }
     }
-    if (fast) sort8_desc(key);
-    __syncwarp();
 
     uint32_t taken = 0;
     float lower_min = FLT_MAX, prev_lo = 0.f, my_s = 0.f;
@@ -425,6 +495,24 @@ __device__ bool score_select(int E, int K, float nx, const float *nw, const floa
     }
     __syncwarp();
     return false;
+}
+
+// Scores one token held by one warp (`w_sel` holds its fp32 logits on entry and receives
+// sel; w_bnd / w_sc receive the bound and the sigmoid) and selects its top-K as
+// select_scored does.
+__device__ bool score_select(int E, int K, float nx, const float *nw, const float *bias,
+                             float gam, float *w_sel, float *w_bnd, float *w_sc,
+                             int32_t *oi, float *ow, uint32_t &cand, int &n_cand, int lane)
+{
+    for (int e = lane; e < E; e += 32) {
+        float sel, bnd, sc;
+        score_expert(w_sel[e], gam * nx * nw[e] + 1e-30f, bias[e], sel, bnd, sc);
+        w_sel[e] = sel;
+        w_bnd[e] = bnd;
+        w_sc[e] = sc;
+    }
+    __syncwarp();
+    return select_scored(E, K, w_sel, w_bnd, w_sc, oi, ow, cand, n_cand, lane);
 }
 
 __device__ __forceinline__ float warp_max_f(float v)
@@ -1012,8 +1100,6 @@ __device__ void gemm_tile(const RouterArgs &a, unsigned char *smem)
 // as gemm_tile, so the logits and the bound are unchanged).  full[s] / empty[s] mbarriers
 // hand the stages over; every wait is bounded and, on expiry, records
 // MOE_ERR_DEVICE_TIMEOUT and makes both roles leave their loops.
-constexpr int WS = 4;              // fp32 stages in the ring
-constexpr int WSB = 4;             // bf16 stages in the staging ring
 constexpr int NPW = 4;             // producer warps (one per SM sub-partition)
 constexpr int NT_WS = NT + 32 * NPW;   // eight compute warps + the producer warps
 constexpr unsigned long long kWsWaitNs = 1000000000ull;
@@ -1021,8 +1107,11 @@ constexpr unsigned long long kWsWaitNs = 1000000000ull;
 template <class C>
 __host__ __device__ constexpr size_t ws_smem_bytes()
 {
-    return static_cast<size_t>(WS) * KST * (C::TT + C::TE) * sizeof(float) +
-           static_cast<size_t>(WSB) * KST * (C::TT + C::TE) * 2 + 2 * WS * 8 + 16;
+    constexpr int PT = 32 * NPW;
+    constexpr int XI = 4 * ((C::TT + PT - 1) / PT), WI = 4 * ((C::TE + PT - 1) / PT);
+    constexpr int XP = C::TT < PT ? C::TT : PT;       // producer threads with token units
+    return static_cast<size_t>(C::RING) * KST * (C::TT + C::TE) * sizeof(float) +
+           static_cast<size_t>(C::STG) * (XI * XP + WI * PT) * 16 + 2 * C::RING * 8 + 16;
 }
 
 // 16-byte global -> shared copy, zero-filled when !valid (src must still be addressable).
@@ -1036,10 +1125,14 @@ template <class C>
 __device__ void gemm_tile_ws(const RouterArgs &a, unsigned char *smem)
 {
     constexpr int PT = 32 * NPW;                                // producer threads
-    // producer units: 4 consecutive rows x one 8-element group of a stage
-    static_assert(C::TT % PT == 0 && C::TE % PT == 0, "warp-specialised tile");
-    constexpr int XU = C::TT / PT, WU = C::TE / PT;            // units a producer thread
+    constexpr int WS = C::RING, WSB = C::STG;
+    // producer units: 4 consecutive rows x one 8-element group of a stage (TT units for
+    // the token slice, TE for the gate rows; a tile smaller than PT leaves threads idle)
+    static_assert((C::TT % PT == 0 || C::TT < PT) && C::TE % PT == 0, "warp-specialised tile");
+    constexpr int XU = (C::TT + PT - 1) / PT, WU = C::TE / PT;  // units a producer thread
     constexpr int XI = 4 * XU, WI = 4 * WU;                     // 16-byte vectors a thread
+    constexpr int XP = C::TT < PT ? C::TT : PT;                 // threads with token units
+    constexpr int SV = XI * XP + WI * PT;                       // staged vectors a stage
     const int et = blockIdx.x, tt = blockIdx.y, ks = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t0 = tt * C::TT, e0 = et * C::TE;
@@ -1049,8 +1142,9 @@ __device__ void gemm_tile_ws(const RouterArgs &a, unsigned char *smem)
 
     float *xs = reinterpret_cast<float *>(smem);                  // [WS][KST][TT]
     float *wsm = xs + WS * KST * C::TT;                           // [WS][KST][TE]
-    uint4 *stg = reinterpret_cast<uint4 *>(wsm + WS * KST * C::TE);   // [WSB][XI + WI][PT]
-    uint64_t *full = reinterpret_cast<uint64_t *>(stg + WSB * (XI + WI) * PT);
+    // staging ring: per stage [XI][XP] token vectors, then [WI][PT] gate-row vectors
+    uint4 *stg = reinterpret_cast<uint4 *>(wsm + WS * KST * C::TE);
+    uint64_t *full = reinterpret_cast<uint64_t *>(stg + WSB * SV);
     uint64_t *empty = full + WS;
     int *abort_flag = reinterpret_cast<int *>(empty + WS);
     if (tid == 0) {
@@ -1087,15 +1181,16 @@ __device__ void gemm_tile_ws(const RouterArgs &a, unsigned char *smem)
         auto copy_stage = [&](int n) {
             if (n < n_st) {
                 const int st = s_beg + n;
-                uint4 *sb = stg + (n % WSB) * (XI + WI) * PT;
+                uint4 *sb = stg + (n % WSB) * SV;
 #pragma unroll
                 for (int i = 0; i < XU; ++i) {
                     const int u = ptid + PT * i, r0 = 4 * (u % (C::TT / 4)), g = u / (C::TT / 4);
+                    if (u >= C::TT) break;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int row = t0 + r0 + q;
                         const uint4 *src = reinterpret_cast<const uint4 *>(a.X + static_cast<size_t>(row < a.T ? row : 0) * a.H) + st * 4 + g;
-                        cp_async16(sb + (4 * i + q) * PT + ptid, src, row < a.T);
+                        cp_async16(sb + (4 * i + q) * XP + ptid, src, row < a.T);
                     }
                 }
 #pragma unroll
@@ -1105,17 +1200,17 @@ __device__ void gemm_tile_ws(const RouterArgs &a, unsigned char *smem)
                     for (int q = 0; q < 4; ++q) {
                         const int row = e0 + r0 + q;
                         const uint4 *src = reinterpret_cast<const uint4 *>(a.Wg + static_cast<size_t>(row < a.E ? row : 0) * a.H) + st * 4 + g;
-                        cp_async16(sb + (XI + 4 * i + q) * PT + ptid, src, row < a.E);
+                        cp_async16(sb + XI * XP + (4 * i + q) * PT + ptid, src, row < a.E);
                     }
                 }
             }
             asm volatile("cp.async.commit_group;" ::: "memory");
         };
         // four rows of one group -> eight 16-byte stores (one per k) and the rows' norms
-        auto convert = [&](const uint4 *sv, float *dst, int ld, float *nrm) {
+        auto convert = [&](const uint4 *sv, int sstride, float *dst, int ld, float *nrm) {
             float f[4][8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) unpack8(sv[q * PT], f[q]);
+            for (int q = 0; q < 4; ++q) unpack8(sv[q * sstride], f[q]);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 *reinterpret_cast<float4 *>(dst + k * ld) = make_float4(f[0][k], f[1][k], f[2][k], f[3][k]);
@@ -1133,18 +1228,18 @@ __device__ void gemm_tile_ws(const RouterArgs &a, unsigned char *smem)
             if (n >= WS && !__all_sync(kFullMask, mbar_wait(&empty[slot], ((n / WS) - 1) & 1, abort_v,
                                                              a.status, kWsWaitNs)))
                 break;
-            const uint4 *sb = stg + (n % WSB) * (XI + WI) * PT + ptid;
+            const uint4 *sb = stg + (n % WSB) * SV + ptid;
             float *xd = xs + slot * KST * C::TT;
             float *wd = wsm + slot * KST * C::TE;
 #pragma unroll
             for (int i = 0; i < XU; ++i) {
                 const int u = ptid + PT * i, r0 = 4 * (u % (C::TT / 4)), g = u / (C::TT / 4);
-                convert(sb + 4 * i * PT, xd + g * 8 * C::TT + r0, C::TT, xsq + 4 * i);
+                if (u < C::TT) convert(sb + 4 * i * XP, XP, xd + g * 8 * C::TT + r0, C::TT, xsq + 4 * i);
             }
 #pragma unroll
             for (int i = 0; i < WU; ++i) {
                 const int u = ptid + PT * i, r0 = 4 * (u % (C::TE / 4)), g = u / (C::TE / 4);
-                convert(sb + (XI + 4 * i) * PT, wd + g * 8 * C::TE + r0, C::TE, wsq + 4 * i);
+                convert(sb + XI * XP + 4 * i * PT, PT, wd + g * 8 * C::TE + r0, C::TE, wsq + 4 * i);
             }
             mbar_arrive(&full[slot]);
         }
@@ -1229,6 +1324,7 @@ __device__ void gemm_tile_ws(const RouterArgs &a, unsigned char *smem)
 #pragma unroll
         for (int i = 0; i < XU; ++i) {
             const int u = ptid + PT * i, r0 = 4 * (u % (C::TT / 4)), g = u / (C::TT / 4);
+            if (u >= C::TT) break;
 #pragma unroll
             for (int q = 0; q < 4; ++q) rxs[g * C::TT + r0 + q] = xsq[4 * i + q];
         }
@@ -1416,11 +1512,10 @@ __device__ void refine_token_warp(const RouterArgs &a, int t, uint32_t cand, int
                        a.topk_w + static_cast<size_t>(t) * a.K, ord, lane);
 }
 
-// Re-scores only the candidates whose interval [sel - bound, sel + bound] meets another
-// candidate's; every other candidate keeps its fp32 sel, which lies in its own interval
-// and that interval is disjoint from all the others, so it orders against any candidate
-// exactly as the exact value would.  Writes the token's outputs; returns false (nothing
-// written) for more than 32 candidates.  Default routing options only.
+// Whether the lane's candidate (of at most 32) has an interval [sel - bound, sel + bound]
+// that meets another candidate's.  Only those need re-scoring: a candidate whose interval
+// is disjoint from all the others keeps its fp32 sel, which lies in that interval, so it
+// orders against any candidate exactly as the exact value would.  Default routing options.
 __device__ bool meets_another(const int *ce, int nc, const float *w_sel, const float *w_bnd, int lane)
 {
     const int e = lane < nc ? ce[lane] : 0;
@@ -1432,29 +1527,6 @@ __device__ bool meets_another(const int *ce, int nc, const float *w_sel, const f
         meets |= r != lane && lo <= ohi && olo <= hi;
     }
     return meets;
-}
-
-__device__ bool refine_overlapping(const RouterArgs &a, int t, uint32_t cand, const float *w_sel,
-                                   const float *w_bnd, int *ce, double *s64, int *ord, int lane)
-{
-    const int nc = list_candidates(cand, a.E, ce, lane);
-    if (nc > 32) return false;
-    const int e = lane < nc ? ce[lane] : 0;
-    const bool meets = meets_another(ce, nc, w_sel, w_bnd, lane);
-    uint32_t need = __ballot_sync(kFullMask, meets);
-    if (lane < nc && !meets) s64[lane] = static_cast<double>(w_sel[e]);
-    const uint16_t *xrow = a.X + static_cast<size_t>(t) * a.H;
-    while (need) {
-        const int q = __ffs(need) - 1;
-        need &= need - 1;
-        const int eq = ce[q];
-        const double l64 = dot_double_word(xrow, a.Wg + static_cast<size_t>(eq) * a.H, a.H, lane);
-        if (lane == 0) s64[q] = 1.0 / (1.0 + exp(-l64)) + static_cast<double>(a.bias[eq]);
-    }
-    __syncwarp();
-    select_refined(ce, s64, nc, a.K, a.bias, a.topk_idx + static_cast<size_t>(t) * a.K,
-                   a.topk_w + static_cast<size_t>(t) * a.K, ord, lane);
-    return true;
 }
 
 // ------------------------------------------------------- fused kernel (small batches)
@@ -1644,15 +1716,6 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
 }
 
 // ------------------------------------------- GEMM-only kernels + finaliser
-// Small tiles whose selection runs in the finalise launch (one warp per token over the
-// whole GPU rather than the last CTA of each token tile).
-__global__ void __launch_bounds__(NT, 2) router_tile_kernel(const RouterArgs a)
-{
-    pdl_wait();
-    extern __shared__ __align__(16) unsigned char smem[];
-    gemm_tile<SmallCfg>(a, smem);
-}
-
 template <class C>
 __global__ void __launch_bounds__(NT_WS, 1) router_gemm_kernel(const RouterArgs a)
 {
@@ -1661,87 +1724,295 @@ __global__ void __launch_bounds__(NT_WS, 1) router_gemm_kernel(const RouterArgs 
     gemm_tile_ws<C>(a, smem);
 }
 
-// One warp per token: split-K sum, scoring, certified top-K, refine when needed.  The
-// CTA's tokens lie in one token tile (TT % NW == 0), whose gate-row norms it forms once.
-__global__ void __launch_bounds__(NT) router_finalize_kernel(const RouterArgs a, int TT)
+// Shared-memory layout of the finalise launch: one CTA finalises NW consecutive tokens
+// (one warp each), then re-scores the uncertified candidates of all of them together.
+struct FinCta {
+    float *nw, *bias, *L, *bnd, *sc, *nxs;   // [E] x 2, [NW][E] x 3 (logits -> sel), [NW]
+    int *ce, *ord;                     // [NW][E] (per-warp fallback), [NW][32]
+    int *p_e, *p_tok, *need;           // refine list [MP] x 3
+    double *p_val, *s64;               // [MP], [NW][E] (per-warp fallback)
+    float2 *dwp;                       // [NW] partial double-word dot of each warp
+
+    __host__ __device__ static int pairs(int E) { return E > 512 ? 1024 : 2048; }
+    __device__ FinCta(unsigned char *smem, int E)
+    {
+        const int MP = pairs(E);
+        float *f = reinterpret_cast<float *>(smem);
+        dwp = reinterpret_cast<float2 *>(f); f += 2 * NW;   // (first: 8-byte aligned)
+        nw = f; f += E;
+        bias = f; f += E;
+        L = f; f += NW * E;                                  // (16-byte aligned when E % 4 == 0)
+        bnd = f; f += NW * E;
+        sc = f; f += NW * E;
+        nxs = f; f += NW;
+        int *i = reinterpret_cast<int *>(f);
+        ce = i; i += NW * E;
+        ord = i; i += NW * 32;
+        p_e = i; i += MP;
+        p_tok = i; i += MP;
+        need = i; i += MP;
+        const uintptr_t d = (reinterpret_cast<uintptr_t>(i) + 7) & ~static_cast<uintptr_t>(7);
+        p_val = reinterpret_cast<double *>(d);
+        s64 = p_val + MP;
+    }
+    static size_t bytes(int E)
+    {
+        const size_t MP = pairs(E);
+        return (2 * static_cast<size_t>(E) + 3 * NW * static_cast<size_t>(E) + NW + 2 * NW) * 4 +
+               (static_cast<size_t>(NW) * E + NW * 32 + 3 * MP) * 4 + 8 +
+               (MP + static_cast<size_t>(NW) * E) * 8;
+    }
+};
+
+// Split-K sum, scoring, certified top-K and refine of `tpc` (1, 2, 4 or 8) consecutive
+// tokens per CTA (the CTA's tokens lie in one token tile of TT tokens, whose gate-row norms
+// it forms).  Small batches take one token per CTA: the partial sums are read by many SMs
+// at once (one SM keeps only so many loads in flight), and the CTA's eight warps are free
+// to split that token's re-scores among them.
+//   1. The whole CTA sums the split-K partials of its tokens, every split's float4 loads
+//      of an element in flight together, added in split order.
+//   2. One warp per token scores it and takes the certified top-K; a token the bounds do
+//      not certify queues its candidates in a CTA-wide list (default options: only those
+//      whose interval meets another candidate's need re-scoring).
+//   3. The CTA re-scores the listed (token, expert) pairs in double-word arithmetic; with
+//      few pairs, each dot product is split over a group of warps (ranges of H merged in
+//      rank order), so one re-score costs about one memory round trip.
+//   4. One warp per queued token selects among its re-scored candidates.
+__global__ void __launch_bounds__(NT) router_finalize_kernel(const RouterArgs a, int TT, int tpc)
 {
     pdl_wait();
     extern __shared__ __align__(16) unsigned char smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * NW + warp;
-    const int E = a.E, KS = a.KS;
-    float *fb = reinterpret_cast<float *>(smem);
-    float *w_nw = fb;                                       // [E], shared by the CTA
-    float *w_sel = fb + E + static_cast<size_t>(warp) * 3 * E;
-    float *w_bnd = w_sel + E, *w_sc = w_bnd + E;
-    int *ib = reinterpret_cast<int *>(fb + E + static_cast<size_t>(NW) * 3 * E);
-    int *ce = ib + static_cast<size_t>(warp) * E;
-    int *ord = ib + static_cast<size_t>(NW) * E + warp * 32;
-    const uintptr_t d = reinterpret_cast<uintptr_t>(ib + static_cast<size_t>(NW) * E + NW * 32);
-    double *s64 = reinterpret_cast<double *>((d + 7) & ~static_cast<uintptr_t>(7)) +
-                  static_cast<size_t>(warp) * E;
+    __shared__ int s_npairs, s_npend, s_nneed;
+    __shared__ int s_pend[5 * NW];      // (token, first pair, pair count, ck, ug) to select
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int E = a.E, KS = a.KS, MP = FinCta::pairs(E);
+    const int t0 = blockIdx.x * tpc;
+    const int ntok = min(tpc, a.T - t0);
+    FinCta S(smem, E);
     const Bounds bd(a.depth, KS, a.H);
-    const int tt = (blockIdx.x * NW) / TT;
-    for (int e = threadIdx.x; e < E; e += NT) {
+    const int tt = t0 / TT;
+    if (tid == 0) { s_npairs = 0; s_npend = 0; s_nneed = 0; }
+
+    // ---- 1. gate-row norms, token norms and the logits of the CTA's tokens
+    for (int e = tid; e < E; e += NT) {
         float n = 0.f;
-        for (int q0 = 0; q0 < KS; q0 += 16) {   // batches of 16 loads, added in split order
-            float pn[16];
+        for (int q0 = 0; q0 < KS; q0 += 32) {   // up to 32 loads in flight, in split order
+            float pn[32];
 #pragma unroll
-            for (int q = 0; q < 16; ++q)
+            for (int q = 0; q < 32; ++q)
                 if (q0 + q < KS) pn[q] = __ldcg(a.wsq + (static_cast<size_t>(tt) * KS + q0 + q) * E + e);
             if (q0 == 0) n = pn[0];
 #pragma unroll
-            for (int q = 0; q < 16; ++q)
+            for (int q = 0; q < 32; ++q)
                 if (q0 + q < KS && q0 + q > 0) n += pn[q];
         }
-        w_nw[e] = sqrtf(n) * bd.infl;
+        S.nw[e] = sqrtf(n) * bd.infl;
+        S.bias[e] = a.bias[e];
+    }
+    if (warp == NW - 1 && lane < ntok) {   // token norms: every split's load in flight
+        float n2 = 0.f;
+        for (int q0 = 0; q0 < KS; q0 += 32) {
+            float pq[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q)
+                if (q0 + q < KS) pq[q] = __ldcg(a.xsq + static_cast<size_t>(q0 + q) * a.T + t0 + lane);
+#pragma unroll
+            for (int q = 0; q < 32; ++q)
+                if (q0 + q < KS) n2 += pq[q];
+        }
+        S.nxs[lane] = sqrtf(n2) * bd.infl;
+    }
+    if ((E & 3) == 0) {
+        // The partials of split q for the CTA's tokens are one contiguous block of `items`
+        // float4.  With few tokens per CTA the splits are divided among G thread groups
+        // (every warp carries loads, at most 8 in flight per thread): group g sums its
+        // consecutive splits in order, then the G group sums are added in group order --
+        // a chain no deeper than KS, as the error bound assumes.
+        const int items = ntok * (E / 4);
+        int G = 1;
+        while (E >= 128 && 2 * G * items <= NT && 2 * G <= KS && G < 8) G *= 2;   // (stage fits)
+        const size_t stride4 = static_cast<size_t>(a.T) * E / 4;
+        const float4 *base = reinterpret_cast<const float4 *>(a.part) + static_cast<size_t>(t0) * (E / 4);
+        float4 *stage = reinterpret_cast<float4 *>(S.bnd);      // [G][items] (free until step 2)
+        for (int it0 = 0; it0 < items; it0 += NT / G) {
+            const int it = it0 + tid % (NT / G), g = tid / (NT / G);
+            if (it < items) {
+                const int qb = g * KS / G, qe = (g + 1) * KS / G;
+                const float4 *src = base + it;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int q0 = qb; q0 < qe; q0 += 8) {     // 8 loads in flight, in split order
+                    float4 w[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        if (q0 + q < qe) w[q] = __ldcg(src + static_cast<size_t>(q0 + q) * stride4);
+                    if (q0 == qb) v = w[0];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        if (q0 + q < qe && q0 + q > qb) { v.x += w[q].x; v.y += w[q].y; v.z += w[q].z; v.w += w[q].w; }
+                }
+                if (G == 1) *reinterpret_cast<float4 *>(S.L + 4 * static_cast<size_t>(it)) = v;
+                else stage[static_cast<size_t>(g) * (NT / G) + (it - it0)] = v;
+            }
+            if (G > 1) {
+                __syncthreads();
+                if (tid < NT / G && it < items) {
+                    float4 v = stage[tid];
+                    for (int h = 1; h < G; ++h) {
+                        const float4 o = stage[static_cast<size_t>(h) * (NT / G) + tid];
+                        v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+                    }
+                    *reinterpret_cast<float4 *>(S.L + 4 * static_cast<size_t>(it)) = v;
+                }
+                __syncthreads();
+            }
+        }
+    } else {
+        for (int it = tid; it < ntok * E; it += NT) {
+            const int tl = it / E, e = it - tl * E;
+            const float *src = a.part + static_cast<size_t>(t0 + tl) * E + e;
+            float v = __ldcg(src);
+            for (int q = 1; q < KS; ++q) v += __ldcg(src + static_cast<size_t>(q) * a.T * E);
+            S.L[it] = v;
+        }
     }
     __syncthreads();
-    if (t >= a.T) return;
-    const float part_sq = lane < KS ? __ldcg(a.xsq + static_cast<size_t>(lane) * a.T + t) : 0.f;
-    float n2 = 0.f;
-    for (int q = 0; q < KS; ++q) n2 += __shfl_sync(kFullMask, part_sq, q);
-    const float nx = sqrtf(n2) * bd.infl;
-    for (int e = lane; e < E; e += 32) {
-        float v = 0.f;
-        for (int q0 = 0; q0 < KS; q0 += 16) {   // batches of 16 loads, added in split order
-            float pv[16];
-#pragma unroll
-            for (int q = 0; q < 16; ++q)
-                if (q0 + q < KS) pv[q] = __ldcg(a.part + (static_cast<size_t>(q0 + q) * a.T + t) * E + e);
-            if (q0 == 0) v = pv[0];
-#pragma unroll
-            for (int q = 0; q < 16; ++q)
-                if (q0 + q < KS && q0 + q > 0) v += pv[q];
+
+    // ---- 2. scoring (default options: every thread takes (token, expert) pairs), then one
+    // warp per token: the certified top-K, else its candidates are queued
+    if (!a.variant) {
+        for (int i = tid; i < ntok * E; i += NT) {
+            const int tl = i / E, e = i - tl * E;
+            float sel, bnd, sc;
+            score_expert(S.L[i], bd.gam * S.nxs[tl] * S.nw[e] + 1e-30f, S.bias[e], sel, bnd, sc);
+            S.L[i] = sel;
+            S.bnd[i] = bnd;
+            S.sc[i] = sc;
         }
-        w_sel[e] = v;
+        __syncthreads();
     }
-    __syncwarp();
-    uint32_t cand;
-    int n_cand;
-    int32_t *oi = a.topk_idx + static_cast<size_t>(t) * a.K;
-    float *ow = a.topk_w + static_cast<size_t>(t) * a.K;
-    bool every = false;
-    uint32_t ck = kFullMask, ug = 0u;
-    if (a.variant) {
-        const int r = score_select_general(a, nx, w_nw, a.bias, bd.gam, w_sel, w_bnd, w_sc, oi,
-                                           ow, cand, n_cand, ck, ug, lane);
-        if (r > 0) return;
-        if (r < 0) {
-            every = true;
-            cand = all_experts(E, lane);
+    if (warp < ntok) {
+        const int t = t0 + warp;
+        float *w_sel = S.L + static_cast<size_t>(warp) * E;
+        float *w_bnd = S.bnd + static_cast<size_t>(warp) * E, *w_sc = S.sc + static_cast<size_t>(warp) * E;
+        int32_t *oi = a.topk_idx + static_cast<size_t>(t) * a.K;
+        float *ow = a.topk_w + static_cast<size_t>(t) * a.K;
+        uint32_t cand = 0u, ck = kFullMask, ug = 0u;
+        int n_cand = 0;
+        bool every = false, done = false;
+        if (a.variant) {
+            const int r = score_select_general(a, S.nxs[warp], S.nw, S.bias, bd.gam, w_sel, w_bnd,
+                                               w_sc, oi, ow, cand, n_cand, ck, ug, lane);
+            done = r > 0;
+            if (r < 0) every = true;
+        } else {
+            done = select_scored(E, a.K, w_sel, w_bnd, w_sc, oi, ow, cand, n_cand, lane);
         }
-    } else if (score_select(E, a.K, nx, w_nw, a.bias, bd.gam, w_sel, w_bnd, w_sc, oi, ow, cand,
-                            n_cand, lane)) {
-        return;
+        if (!done && !every && n_cand < a.K) every = true;   // non-finite scores
+        if (!done) {
+            if (every) {
+                cand = all_experts(E, lane);
+                n_cand = E;
+            }
+            int base = 0;
+            if (lane == 0) base = atomicAdd(&s_npairs, n_cand);
+            base = __shfl_sync(kFullMask, base, 0);
+            if (base + n_cand <= MP) {
+                list_candidates(cand, E, S.p_e + base, lane);
+                // default options: only candidates whose interval meets another's are
+                // re-scored (p_tok < 0 marks the others, which keep their fp32 sel)
+                const bool some = !a.variant && !every && n_cand <= 32;
+                const bool meets = some ? meets_another(S.p_e + base, n_cand, w_sel, w_bnd, lane) : true;
+                for (int q = lane; q < n_cand; q += 32) {
+                    const bool need = !some || meets;
+                    S.p_tok[base + q] = need ? warp : -1 - warp;
+                    if (!need) S.p_val[base + q] = static_cast<double>(w_sel[S.p_e[base + q]]);
+                }
+                if (lane == 0) {
+                    const int pi = atomicAdd(&s_npend, 1);
+                    s_pend[5 * pi] = warp;
+                    s_pend[5 * pi + 1] = base;
+                    s_pend[5 * pi + 2] = every ? -n_cand : n_cand;   // < 0: every expert
+                    s_pend[5 * pi + 3] = static_cast<int>(ck);
+                    s_pend[5 * pi + 4] = static_cast<int>(ug);
+                }
+                __syncwarp();
+            } else {
+                // list full (pathological ties): retire the reserved in-range slots, then
+                // refine this token with the warp alone
+                for (int q = base + lane; q < MP; q += 32) S.p_e[q] = -1;
+                __syncwarp();
+                refine_token_warp(a, t, cand, S.ce + static_cast<size_t>(warp) * E,
+                                  S.s64 + static_cast<size_t>(warp) * E, S.ord + warp * 32, lane,
+                                  every, ck, ug);
+            }
+        }
     }
-    if (!every && n_cand < a.K) {           // non-finite scores: re-score every expert
-        every = true;
-        cand = all_experts(E, lane);
-    } else if (!a.variant && refine_overlapping(a, t, cand, w_sel, w_bnd, ce, s64, ord, lane)) {
-        return;
+    __syncthreads();
+
+    // ---- 3. the pairs to re-score, in list order
+    const int npairs = min(s_npairs, MP);
+    if (warp == 0) {
+        int n = 0;
+        for (int q0 = 0; q0 < npairs; q0 += 32) {
+            const int q = q0 + lane;
+            const bool nd = q < npairs && S.p_e[q] >= 0 && S.p_tok[q] >= 0;
+            const uint32_t m = __ballot_sync(kFullMask, nd);
+            if (nd) S.need[n + __popc(m & ((1u << lane) - 1u))] = q;
+            n += __popc(m);
+        }
+        if (lane == 0) s_nneed = n;
     }
-    refine_token_warp(a, t, cand, ce, s64, ord, lane, every, ck, ug);
+    __syncthreads();
+    const int nneed = s_nneed;
+    if (nneed > 0) {
+        // group size: 8 warps on one pair, 4 on each of two, 2 on each of four, else one
+        const int G = nneed >= NW ? 1 : (nneed >= NW / 2 ? 2 : (nneed >= 2 ? 4 : 8));
+        const int rank = warp % G, slot = warp / G, per_round = NW / G;
+        const int nv = a.H / 8;
+        const int v0 = rank * nv / G, v1 = (rank + 1) * nv / G;
+        for (int r0 = 0; r0 < nneed; r0 += per_round) {
+            const int i = r0 + slot;
+            if (i < nneed) {
+                const int q = S.need[i];
+                const int e = S.p_e[q], t = t0 + S.p_tok[q];
+                float h, l;
+                dot_dw_range(a.X + static_cast<size_t>(t) * a.H, a.Wg + static_cast<size_t>(e) * a.H,
+                             v0, v1, lane, h, l);
+                if (lane == 0) S.dwp[warp] = make_float2(h, l);
+            }
+            __syncthreads();
+            if (i < nneed && rank == 0 && lane == 0) {
+                float h = S.dwp[warp].x, l = S.dwp[warp].y;
+                for (int g = 1; g < G; ++g) dw_merge(h, l, S.dwp[warp + g].x, S.dwp[warp + g].y);
+                const double l64 = static_cast<double>(h) + static_cast<double>(l);
+                const int q = S.need[i];
+                const int e = S.p_e[q];
+                S.p_val[q] = a.variant ? l64 : 1.0 / (1.0 + exp(-l64)) + static_cast<double>(S.bias[e]);
+            }
+            __syncthreads();
+        }
+    }
+
+    // ---- 4. selection among the re-scored candidates, one warp per queued token
+    for (int pi = warp; pi < s_npend; pi += NW) {
+        const int tl = s_pend[5 * pi], first = s_pend[5 * pi + 1], cnt = s_pend[5 * pi + 2];
+        const uint32_t ck = static_cast<uint32_t>(s_pend[5 * pi + 3]);
+        const uint32_t ug = static_cast<uint32_t>(s_pend[5 * pi + 4]);
+        const int t = t0 + tl;
+        int *ord = S.ord + warp * 32;
+        if (a.variant && cnt < 0)
+            select_general64(a, S.p_e + first, S.p_val + first,
+                             a.topk_idx + static_cast<size_t>(t) * a.K,
+                             a.topk_w + static_cast<size_t>(t) * a.K, ord, lane);
+        else if (a.variant)
+            select_candidates64(a, S.p_e + first, S.p_val + first, cnt, ck, ug,
+                                a.topk_idx + static_cast<size_t>(t) * a.K,
+                                a.topk_w + static_cast<size_t>(t) * a.K, ord, lane);
+        else
+            select_refined(S.p_e + first, S.p_val + first, cnt < 0 ? -cnt : cnt, a.K, S.bias,
+                           a.topk_idx + static_cast<size_t>(t) * a.K,
+                           a.topk_w + static_cast<size_t>(t) * a.K, ord, lane);
+    }
 }
 
 size_t fused_smem(int TT, int TE, int E, int max_pairs)
@@ -1751,11 +2022,7 @@ size_t fused_smem(int TT, int TE, int E, int max_pairs)
     return (g > f ? g : f) + 16;
 }
 
-size_t finalize_smem(int E)
-{
-    return static_cast<size_t>(E) * 4 + static_cast<size_t>(NW) * 4 * E * 4 + NW * 32 * 4 + 8 +
-           static_cast<size_t>(NW) * E * 8;
-}
+size_t finalize_smem(int E) { return FinCta::bytes(E) + 16; }
 
 }  // namespace
 
@@ -1778,21 +2045,32 @@ RouterPlan router_plan(int T, int H, int E)
     p.nET = (E + p.TE - 1) / p.TE;
     p.S = H / KST;
     const int base = p.nTT * p.nET;
-    const int target = (small ? 2 : 1) * num_sms();   // resident CTAs per SM: 2 small, 1 large
+    const bool split = !p.gemv && small && T >= kSplitMinTokens && T <= kSplitMaxTokens;
+    // resident CTAs per SM: 2 for the two-stage small tile, 1 for the warp-specialised ones
+    const int target = (small && !split ? 2 : 1) * num_sms();
     if (p.gemv) {
         p.KS = 1;
         p.depth = ((H / 8 + GEMV_QW - 1) / GEMV_QW + 31) / 32 + 3 + 5 + 2 + 2;
     } else {
         // at most 32 stages per split keeps the summation depth (and the error bound) small
         p.KS = (p.S + 31) / 32;
-        // (the finalise reads up to 32 splits; beyond 16 the extra partial reads and the
-        // larger bound -- more tokens to refine -- measured slower at decode)
+        // (the finalise sums at most 32 splits in one batch of loads)
         if (p.KS > 32) p.KS = 32;
-        // (up to 32 splits when there are at most 4 token tiles: too few CTAs otherwise)
-        while (p.KS * 2 <= p.S && p.KS * 2 <= (p.nTT <= 4 ? 32 : 16) && base * p.KS < target) p.KS *= 2;
+        // split tiles (16 to 2048 tokens): as many splits as fill one wave of resident CTAs
+        // (one per SM), at most 32 -- the finalise launch reads every split's partials
+        // with their loads in flight together, so more splits cost it little.  Otherwise:
+        // doubled while the grid stays below one wave.
+        if (split) {
+            // (at least enough splits for 64 stages each, so the summation depth stays small)
+            const int ks = target / base, ks_min = (p.S + 63) / 64;
+            p.KS = ks > 32 ? 32 : (ks > ks_min ? ks : ks_min);
+            if (p.KS > p.S) p.KS = p.S;
+        } else {
+            while (p.KS * 2 <= p.S && p.KS * 2 <= 32 && base * p.KS < target) p.KS *= 2;
+        }
         p.depth = KST + (p.S + p.KS - 1) / p.KS + p.KS + 2;
     }
-    p.split = (!p.gemv && small && T >= kSplitMinTokens && T <= kSplitMaxTokens) ? 1 : 0;
+    p.split = split ? 1 : 0;
     p.max_pairs = 1024;
     auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
     p.part_bytes = al(static_cast<size_t>(p.KS) * T * E * sizeof(float));
@@ -1800,7 +2078,7 @@ RouterPlan router_plan(int T, int H, int E)
     p.wsq_bytes = al(static_cast<size_t>(p.nTT) * p.KS * E * sizeof(float));
     p.cnt_bytes = al(static_cast<size_t>(p.nTT) * sizeof(unsigned));
     p.smem_bytes = !small ? ws_smem_bytes<LargeCfg>()
-                 : p.split ? 2 * KST * static_cast<size_t>(p.TT + p.TE) * sizeof(float) + 16
+                 : p.split ? ws_smem_bytes<SmallWsCfg>()
                            : fused_smem(p.TT, p.TE, E, p.max_pairs);
     return p;
 }
@@ -1829,9 +2107,9 @@ cudaError_t launch_router(const void *X, const void *Wg, const float *bias, int 
     dim3 grid(plan.nET, plan.nTT, plan.KS);
     cudaError_t err;
     if (plan.split) {
-        err = ensure_smem(reinterpret_cast<const void *>(router_tile_kernel), plan.smem_bytes);
+        err = ensure_smem(reinterpret_cast<const void *>(router_gemm_kernel<SmallWsCfg>), plan.smem_bytes);
         if (err != cudaSuccess) return err;
-        if ((err = launch_pdl(router_tile_kernel, grid, dim3(NT), plan.smem_bytes, s, 1, a)) != cudaSuccess)
+        if ((err = launch_pdl(router_gemm_kernel<SmallWsCfg>, grid, dim3(NT_WS), plan.smem_bytes, s, 1, a)) != cudaSuccess)
             return err;
     } else if (plan.TT == SmallCfg::TT) {
         err = cudaMemsetAsync(scr.cnt, 0, static_cast<size_t>(plan.nTT) * sizeof(unsigned), s);
@@ -1862,7 +2140,12 @@ cudaError_t launch_router(const void *X, const void *Wg, const float *bias, int 
     const size_t fs = finalize_smem(E);
     err = ensure_smem(reinterpret_cast<const void *>(router_finalize_kernel), fs);
     if (err != cudaSuccess) return err;
-    return launch_pdl(router_finalize_kernel, dim3((T + NW - 1) / NW), dim3(NT), fs, s, 1, a, plan.TT);
+    // tokens per finalise CTA: the fewest that keep the grid within one CTA per SM (its
+    // registers allow one resident CTA)
+    const int sms = num_sms();
+    const int tpc = T <= sms ? 1 : (T <= 2 * sms ? 2 : (T <= 4 * sms ? 4 : NW));
+    return launch_pdl(router_finalize_kernel, dim3((T + tpc - 1) / tpc), dim3(NT), fs, s, 1, a,
+                      plan.TT, tpc);
 }
 
 }  // namespace moe

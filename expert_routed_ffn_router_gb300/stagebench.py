@@ -2,10 +2,11 @@
 
     python -m expert_routed_ffn_router_gb300.stagebench --stage router --workload prefill
 
-Stages: router (moe_router_topk), dispatch (moe_dispatch on the router's output), layer
-(moe_layer_forward).  The router and dispatch stages allocate only their own inputs, so
-they run at full token counts without the 22.5 GB of expert weights -- small enough for
-profiler captures.  Prints one JSON line with the mean milliseconds per call.
+Stages: router (moe_router_topk), dispatch (moe_dispatch on the router's output), combine
+(moe_combine on seeded expert outputs Yp and the router's routing), layer
+(moe_layer_forward).  The router, dispatch and combine stages allocate only their own
+inputs, so they run at full token counts without the 22.5 GB of expert weights -- small
+enough for profiler captures.  Prints one JSON line with the mean milliseconds per call.
 """
 from __future__ import annotations
 
@@ -21,7 +22,8 @@ from . import synth
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--stage", choices=("router", "dispatch", "layer"), default="router")
+    ap.add_argument("--stage", choices=("router", "dispatch", "combine", "layer"),
+                    default="router")
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--T", type=int, default=0, help="override the token count")
     ap.add_argument("--iters", type=int, default=20)
@@ -52,6 +54,22 @@ def main(argv=None):
 
         def run():
             B.moe_dispatch(X, idx, E, counts, offsets, perm, slot, Xp, aff, ws)
+    elif args.stage == "combine":
+        B.moe_router_topk(X, Wg, bias, K, idx, wt, ws)
+        counts = torch.empty(E, dtype=torch.int32, device=dev)
+        offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        perm = torch.empty(T * K, dtype=torch.int32, device=dev)
+        slot = torch.empty(T, K, dtype=torch.int32, device=dev)
+        Xp = torch.empty(T * K, H, dtype=torch.bfloat16, device=dev)
+        B.moe_dispatch(X, idx, E, counts, offsets, perm, slot, Xp, None, ws)
+        g = torch.Generator(device=dev)
+        g.manual_seed(12345)
+        Yp = torch.randn(T * K, H, generator=g, device=dev).to(torch.bfloat16)
+        Ysh = torch.randn(T, H, generator=g, device=dev)
+        Y = torch.empty(T, H, dtype=torch.float32, device=dev)
+
+        def run():
+            B.moe_combine(Yp, slot, wt, Ysh, Y)
     else:
         weights = synth.expert_weights_device(w, dev)
         weights["W_gate"], weights["bias"] = Wg, bias
