@@ -26,30 +26,49 @@ __global__ void __launch_bounds__(CT) combine_kernel(const uint4 *__restrict__ Y
                                                      int K, float4 *__restrict__ Y)
 {
     pdl_wait();
+    // the token's K (<= 32) row numbers and weights, staged once, so that every row load of
+    // a thread is issued together (one round trip instead of two per row)
+    __shared__ int r_s[32];
+    __shared__ float w_s[32];
     const int t = blockIdx.x;
+    if (threadIdx.x < K) {
+        r_s[threadIdx.x] = __ldg(slot_pos + static_cast<size_t>(t) * K + threadIdx.x);
+        w_s[threadIdx.x] = __ldg(topk_w + static_cast<size_t>(t) * K + threadIdx.x);
+    }
+    __syncthreads();
     const int c = blockIdx.y * COLS + threadIdx.x * 8;
     if (c >= H) return;
     const int vec = H / 8;
     const int cv = c / 8;
+    const size_t o = (static_cast<size_t>(t) * H + c) / 4;
+    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+    if (Ysh) {
+        s0 = __ldg(Ysh + o);
+        s1 = __ldg(Ysh + o + 1);
+    }
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    for (int j = 0; j < K; ++j) {
-        const int r = __ldg(slot_pos + static_cast<size_t>(t) * K + j);
-        const float w = __ldg(topk_w + static_cast<size_t>(t) * K + j);
-        const uint4 v = __ldg(Yp + static_cast<size_t>(r) * vec + cv);
-        acc[0] = fmaf(w, bf16_lo(v.x), acc[0]);
-        acc[1] = fmaf(w, bf16_hi(v.x), acc[1]);
-        acc[2] = fmaf(w, bf16_lo(v.y), acc[2]);
-        acc[3] = fmaf(w, bf16_hi(v.y), acc[3]);
-        acc[4] = fmaf(w, bf16_lo(v.z), acc[4]);
-        acc[5] = fmaf(w, bf16_hi(v.z), acc[5]);
-        acc[6] = fmaf(w, bf16_lo(v.w), acc[6]);
-        acc[7] = fmaf(w, bf16_hi(v.w), acc[7]);
+    for (int j0 = 0; j0 < K; j0 += 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (j0 + u < K) v[u] = __ldg(Yp + static_cast<size_t>(r_s[j0 + u]) * vec + cv);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (j0 + u >= K) break;
+            const float w = w_s[j0 + u];
+            acc[0] = fmaf(w, bf16_lo(v[u].x), acc[0]);
+            acc[1] = fmaf(w, bf16_hi(v[u].x), acc[1]);
+            acc[2] = fmaf(w, bf16_lo(v[u].y), acc[2]);
+            acc[3] = fmaf(w, bf16_hi(v[u].y), acc[3]);
+            acc[4] = fmaf(w, bf16_lo(v[u].z), acc[4]);
+            acc[5] = fmaf(w, bf16_hi(v[u].z), acc[5]);
+            acc[6] = fmaf(w, bf16_lo(v[u].w), acc[6]);
+            acc[7] = fmaf(w, bf16_hi(v[u].w), acc[7]);
+        }
     }
-    const size_t o = (static_cast<size_t>(t) * H + c) / 4;
     if (Ysh) {
-        const float4 s0 = __ldg(Ysh + o), s1 = __ldg(Ysh + o + 1);
         acc[0] += s0.x; acc[1] += s0.y; acc[2] += s0.z; acc[3] += s0.w;
         acc[4] += s1.x; acc[5] += s1.y; acc[6] += s1.z; acc[7] += s1.w;
     }

@@ -24,6 +24,16 @@ namespace {
 
 constexpr int CHUNK = 256;            // tokens per chunk (8 warps x 32)
 constexpr int CW = CHUNK / 32;        // mask rows per chunk
+constexpr int KMAX = 32;              // largest top-K
+
+// The K (<= 32) expert indices of token t, all loads issued before any is used (-1 for an
+// invalid token); one memory round trip instead of K.
+__device__ __forceinline__ void load_topk(const int32_t *__restrict__ idx, int t, bool valid,
+                                          int K, int (&ev)[KMAX])
+{
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) ev[j] = (valid && j < K) ? idx[static_cast<size_t>(t) * K + j] : -1;
+}
 
 __global__ void __launch_bounds__(CHUNK) masks_kernel(const int32_t *__restrict__ idx, int T,
                                                       int E, int K, uint32_t *smask,
@@ -37,8 +47,12 @@ __global__ void __launch_bounds__(CHUNK) masks_kernel(const int32_t *__restrict_
     __syncthreads();
     const int t = c * CHUNK + tid;
     const bool valid = t < T;
-    for (int j = 0; j < K; ++j) {
-        int e = valid ? idx[static_cast<size_t>(t) * K + j] : -1;
+    int ev[KMAX];
+    load_topk(idx, t, valid, K, ev);
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        if (j >= K) break;
+        int e = ev[j];
         if (valid && (e < 0 || e >= E)) {
             report(status, MOE_ERR_INVALID_ARG);
             e = -1;
@@ -128,8 +142,12 @@ __global__ void __launch_bounds__(CHUNK) scatter_kernel(const int32_t *__restric
     const int t = c * CHUNK + tid;
     if (t >= T) return;
     const uint32_t below = (1u << lane) - 1u;
-    for (int j = 0; j < K; ++j) {
-        const int e = idx[static_cast<size_t>(t) * K + j];
+    int ev[KMAX];
+    load_topk(idx, t, true, K, ev);
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        if (j >= K) break;
+        const int e = ev[j];
         if (e < 0 || e >= E) continue;   // reported by masks_kernel
         const int r = base[w * E + e] + __popc(m_s[w * E + e] & below);
         slot_pos[static_cast<size_t>(t) * K + j] = r;
@@ -276,8 +294,12 @@ __device__ void small_routing(const int32_t *__restrict__ idx, int T, int E, int
     for (int i = tid; i < CW * E; i += CHUNK) m_s[i] = 0u;
     __syncthreads();
     const bool valid = tid < T;
-    for (int j = 0; j < K; ++j) {
-        int e = valid ? idx[static_cast<size_t>(tid) * K + j] : -1;
+    int ev[KMAX];
+    load_topk(idx, tid, valid, K, ev);
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        if (j >= K) break;
+        int e = ev[j];
         if (valid && (e < 0 || e >= E)) {
             report(status, MOE_ERR_INVALID_ARG);
             e = -1;
@@ -338,8 +360,10 @@ __device__ void small_routing(const int32_t *__restrict__ idx, int T, int E, int
     __syncthreads();
     if (valid) {
         const uint32_t below = (1u << lane) - 1u;
-        for (int j = 0; j < K; ++j) {
-            const int e = idx[static_cast<size_t>(tid) * K + j];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            if (j >= K) break;
+            const int e = ev[j];
             if (e < 0 || e >= E) continue;
             const int r = base[w * E + e] + __popc(m_s[w * E + e] & below);
             perm_s[r] = tid;

@@ -321,7 +321,7 @@ __device__ void select_refined(int *pe, const double *pv, int n, int K, const fl
 __device__ void dot_dw_range(const uint16_t *x, const uint16_t *w, int v0, int v1, int lane,
                              float &h, float &l)
 {
-    constexpr int U = 4;
+    constexpr int U = 8;
     const uint4 *xr = reinterpret_cast<const uint4 *>(x);
     const uint4 *wr = reinterpret_cast<const uint4 *>(w);
     float hi[U], lo[U];
@@ -344,9 +344,10 @@ __device__ void dot_dw_range(const uint16_t *x, const uint16_t *w, int v0, int v
             for (int i = 0; i < 8; ++i) dw_add(hi[u], lo[u], __fmul_rn(xf[i], wf[i]));  // exact product
         }
     }
-    dw_merge(hi[0], lo[0], hi[1], lo[1]);
-    dw_merge(hi[2], lo[2], hi[3], lo[3]);
-    dw_merge(hi[0], lo[0], hi[2], lo[2]);
+#pragma unroll
+    for (int step = 1; step < U; step <<= 1)
+#pragma unroll
+        for (int u = 0; u + step < U; u += 2 * step) dw_merge(hi[u], lo[u], hi[u + step], lo[u + step]);
     h = hi[0];
     l = lo[0];
 #pragma unroll
@@ -1379,7 +1380,9 @@ __device__ void gemv_tile(const RouterArgs &a, unsigned char *smem)
             for (int j = 0; j < 8; ++j) acc[t][j] = 0.f;
         }
         float wsq = 0.f;
-        constexpr int U = TB <= 2 ? 4 : (TB <= 4 ? 2 : 1);   // vectors per lane in flight
+        // vectors per lane in flight: a quarter row of DeepSeek-V3's gate (224 vectors) in
+        // one round trip for one or two tokens
+        constexpr int U = TB <= 2 ? 8 : (TB <= 4 ? 4 : 2);
         for (int v0 = v_beg + lane; v0 < v_end; v0 += 32 * U) {
             uint4 wv[U], xv[U][TB];
 #pragma unroll
@@ -1449,17 +1452,71 @@ __device__ void gemv_tile(const RouterArgs &a, unsigned char *smem)
     }
 }
 
+// Re-scores the listed (token, expert) pairs of a CTA -- p_tok[q] >= 0 a token relative to
+// t0, p_e[q] >= 0 an expert; other entries are skipped -- in double-word arithmetic with all
+// of the CTA's warps, and writes p_val[q]: the fp64 logit (routing options) or sigmoid +
+// bias.  With fewer pairs than warps, each dot product is split over a group of 2, 4 or 8
+// warps (ranges of H, partials merged in rank order), so a re-score costs about one memory
+// round trip.  CTA-wide: every thread calls it.  Scratch: need [npairs] ints, dwp [NW],
+// s_n one shared int.
+__device__ void rescore_pairs(const RouterArgs &a, const int *p_e, const int *p_tok, int npairs,
+                              int t0, const float *bias, int *need, float2 *dwp, double *p_val,
+                              int *s_n, int warp, int lane)
+{
+    if (warp == 0) {
+        int n = 0;
+        for (int q0 = 0; q0 < npairs; q0 += 32) {
+            const int q = q0 + lane;
+            const bool nd = q < npairs && p_e[q] >= 0 && p_tok[q] >= 0;
+            const uint32_t m = __ballot_sync(kFullMask, nd);
+            if (nd) need[n + __popc(m & ((1u << lane) - 1u))] = q;
+            n += __popc(m);
+        }
+        if (lane == 0) *s_n = n;
+    }
+    __syncthreads();
+    const int nneed = *s_n;
+    if (nneed == 0) return;
+    // group size: 8 warps on one pair, 4 on each of two, 2 on each of four, else one
+    const int G = nneed >= NW ? 1 : (nneed >= NW / 2 ? 2 : (nneed >= 2 ? 4 : 8));
+    const int rank = warp % G, slot = warp / G, per_round = NW / G;
+    const int nv = a.H / 8;
+    const int v0 = rank * nv / G, v1 = (rank + 1) * nv / G;
+    for (int r0 = 0; r0 < nneed; r0 += per_round) {
+        const int i = r0 + slot;
+        if (i < nneed) {
+            const int q = need[i];
+            const int e = p_e[q], t = t0 + p_tok[q];
+            float h, l;
+            dot_dw_range(a.X + static_cast<size_t>(t) * a.H, a.Wg + static_cast<size_t>(e) * a.H,
+                         v0, v1, lane, h, l);
+            if (lane == 0) dwp[warp] = make_float2(h, l);
+        }
+        __syncthreads();
+        if (i < nneed && rank == 0 && lane == 0) {
+            float h = dwp[warp].x, l = dwp[warp].y;
+            for (int g = 1; g < G; ++g) dw_merge(h, l, dwp[warp + g].x, dwp[warp + g].y);
+            const double l64 = static_cast<double>(h) + static_cast<double>(l);
+            const int q = need[i];
+            p_val[q] = a.variant ? l64 : 1.0 / (1.0 + exp(-l64)) + static_cast<double>(bias[p_e[q]]);
+        }
+        __syncthreads();
+    }
+}
+
 // Shared-memory layout of the finalise step (after the GEMM tile is done with smem).
 struct FinSmem {
     float *nw, *bias, *nxs, *L;        // [E], [E], [CH], [CH][E]
     float *sel, *bnd, *sc;             // per warp [E] each
     int *ord, *ce;                     // per warp [32], [E]
-    int *p_e, *p_tok;                  // refine list [max_pairs]
+    int *p_e, *p_tok, *need;           // refine list [max_pairs] x 3
     double *p_val, *s64;               // [max_pairs], per warp [E]
+    float2 *dwp;                       // [NW] partial double-word dots
 
     __device__ FinSmem(unsigned char *smem, int E, int max_pairs, int warp)
     {
         float *f = reinterpret_cast<float *>(smem);
+        dwp = reinterpret_cast<float2 *>(f); f += 2 * NW;   // (first: 8-byte aligned)
         nw = f; f += E;
         bias = f; f += E;
         nxs = f; f += CH;
@@ -1473,15 +1530,16 @@ struct FinSmem {
         ce = i + static_cast<size_t>(warp) * E; i += NW * E;
         p_e = i; i += max_pairs;
         p_tok = i; i += max_pairs;
+        need = i; i += max_pairs;
         const uintptr_t d = (reinterpret_cast<uintptr_t>(i) + 7) & ~static_cast<uintptr_t>(7);
         p_val = reinterpret_cast<double *>(d);
         s64 = p_val + max_pairs + static_cast<size_t>(warp) * E;
     }
     static size_t bytes(int E, int max_pairs)
     {
-        return (2 * static_cast<size_t>(E) + CH + static_cast<size_t>(CH) * E +
+        return (2 * NW + 2 * static_cast<size_t>(E) + CH + static_cast<size_t>(CH) * E +
                 static_cast<size_t>(NW) * 3 * E) * 4 +
-               (NW * 32 + static_cast<size_t>(NW) * E + 2 * static_cast<size_t>(max_pairs)) * 4 + 8 +
+               (NW * 32 + static_cast<size_t>(NW) * E + 3 * static_cast<size_t>(max_pairs)) * 4 + 8 +
                (static_cast<size_t>(max_pairs) + static_cast<size_t>(NW) * E) * 8;
     }
 };
@@ -1535,7 +1593,7 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
 {
     pdl_wait();
     extern __shared__ __align__(16) unsigned char smem[];
-    __shared__ int s_last, s_npairs, s_npend;
+    __shared__ int s_last, s_npairs, s_npend, s_nneed;
     __shared__ int s_pend[5 * C::TT];     // (token, first pair, pair count, ck, ug) to refine
 
     if constexpr (GEMV > 0)
@@ -1683,18 +1741,9 @@ __global__ void __launch_bounds__(NT, 2) router_fused_kernel(const RouterArgs a)
     }
     __syncthreads();
 
-    // CTA-wide refine: every warp takes (token, expert) pairs of the queued tokens
-    const int npairs = min(s_npairs, a.max_pairs);
-    for (int q = warp; q < npairs; q += NW) {
-        const int e = S.p_e[q];
-        if (e < 0 || S.p_tok[q] < 0) continue;
-        const int t = t0 + S.p_tok[q];
-        const double l64 = dot_double_word(a.X + static_cast<size_t>(t) * a.H,
-                                           a.Wg + static_cast<size_t>(e) * a.H, a.H, lane);
-        if (lane == 0)
-            S.p_val[q] = a.variant ? l64 : 1.0 / (1.0 + exp(-l64)) + static_cast<double>(a.bias[e]);
-    }
-    __syncthreads();
+    // CTA-wide refine of the queued tokens' (token, expert) pairs
+    rescore_pairs(a, S.p_e, S.p_tok, min(s_npairs, a.max_pairs), t0, S.bias, S.need, S.dwp,
+                  S.p_val, &s_nneed, warp, lane);
     for (int pi = warp; pi < s_npend; pi += NW) {
         const int tl = s_pend[5 * pi], first = s_pend[5 * pi + 1], cnt = s_pend[5 * pi + 2];
         const uint32_t ck = static_cast<uint32_t>(s_pend[5 * pi + 3]);
@@ -1949,49 +1998,9 @@ __global__ void __launch_bounds__(NT) router_finalize_kernel(const RouterArgs a,
     }
     __syncthreads();
 
-    // ---- 3. the pairs to re-score, in list order
-    const int npairs = min(s_npairs, MP);
-    if (warp == 0) {
-        int n = 0;
-        for (int q0 = 0; q0 < npairs; q0 += 32) {
-            const int q = q0 + lane;
-            const bool nd = q < npairs && S.p_e[q] >= 0 && S.p_tok[q] >= 0;
-            const uint32_t m = __ballot_sync(kFullMask, nd);
-            if (nd) S.need[n + __popc(m & ((1u << lane) - 1u))] = q;
-            n += __popc(m);
-        }
-        if (lane == 0) s_nneed = n;
-    }
-    __syncthreads();
-    const int nneed = s_nneed;
-    if (nneed > 0) {
-        // group size: 8 warps on one pair, 4 on each of two, 2 on each of four, else one
-        const int G = nneed >= NW ? 1 : (nneed >= NW / 2 ? 2 : (nneed >= 2 ? 4 : 8));
-        const int rank = warp % G, slot = warp / G, per_round = NW / G;
-        const int nv = a.H / 8;
-        const int v0 = rank * nv / G, v1 = (rank + 1) * nv / G;
-        for (int r0 = 0; r0 < nneed; r0 += per_round) {
-            const int i = r0 + slot;
-            if (i < nneed) {
-                const int q = S.need[i];
-                const int e = S.p_e[q], t = t0 + S.p_tok[q];
-                float h, l;
-                dot_dw_range(a.X + static_cast<size_t>(t) * a.H, a.Wg + static_cast<size_t>(e) * a.H,
-                             v0, v1, lane, h, l);
-                if (lane == 0) S.dwp[warp] = make_float2(h, l);
-            }
-            __syncthreads();
-            if (i < nneed && rank == 0 && lane == 0) {
-                float h = S.dwp[warp].x, l = S.dwp[warp].y;
-                for (int g = 1; g < G; ++g) dw_merge(h, l, S.dwp[warp + g].x, S.dwp[warp + g].y);
-                const double l64 = static_cast<double>(h) + static_cast<double>(l);
-                const int q = S.need[i];
-                const int e = S.p_e[q];
-                S.p_val[q] = a.variant ? l64 : 1.0 / (1.0 + exp(-l64)) + static_cast<double>(S.bias[e]);
-            }
-            __syncthreads();
-        }
-    }
+    // ---- 3. the listed pairs re-scored by the whole CTA
+    rescore_pairs(a, S.p_e, S.p_tok, min(s_npairs, MP), t0, S.bias, S.need, S.dwp, S.p_val,
+                  &s_nneed, warp, lane);
 
     // ---- 4. selection among the re-scored candidates, one warp per queued token
     for (int pi = warp; pi < s_npend; pi += NW) {
@@ -2056,15 +2065,20 @@ RouterPlan router_plan(int T, int H, int E)
         p.KS = (p.S + 31) / 32;
         // (the finalise sums at most 32 splits in one batch of loads)
         if (p.KS > 32) p.KS = 32;
-        // split tiles (16 to 2048 tokens): as many splits as fill one wave of resident CTAs
-        // (one per SM), at most 32 -- the finalise launch reads every split's partials
-        // with their loads in flight together, so more splits cost it little.  Otherwise:
-        // doubled while the grid stays below one wave.
+        // split tiles (16 to 2048 tokens, one CTA per SM): the split count with the least
+        // modelled time, waves x (stages of a split + the per-CTA overhead, ~0.7 of a
+        // stage, measured at the DeepSeek-V3 shape), from 64 stages a split down to 32
+        // splits -- the finalise launch reads every split's partials with their loads in
+        // flight together, so more splits cost it little.  Otherwise: doubled while the
+        // grid stays below one wave.
         if (split) {
-            // (at least enough splits for 64 stages each, so the summation depth stays small)
-            const int ks = target / base, ks_min = (p.S + 63) / 64;
-            p.KS = ks > 32 ? 32 : (ks > ks_min ? ks : ks_min);
-            if (p.KS > p.S) p.KS = p.S;
+            long long best = -1;
+            const int ks_hi = p.S < 32 ? p.S : 32;
+            for (int ks = (p.S + 63) / 64; ks <= ks_hi; ++ks) {
+                const long long waves = (static_cast<long long>(base) * ks + target - 1) / target;
+                const long long cost = waves * (((p.S + ks - 1) / ks) * 11 + 8);
+                if (best < 0 || cost < best) { best = cost; p.KS = ks; }
+            }
         } else {
             while (p.KS * 2 <= p.S && p.KS * 2 <= 32 && base * p.KS < target) p.KS *= 2;
         }
