@@ -275,11 +275,12 @@ def moe_layer_forward_ex(shape: MoeShape, weights: dict, routing, X, Y, topk_idx
 
 
 def moe_quantize_weight_fp8(W, stream=None):
-    """W bf16 [G, R, C] or [R, C] (device) -> (E4M3 bytes uint8, same shape; int32 scale
-    exponents [G, R/128, C/128] or [R/128, C/128])."""
+    """W bf16 [G, R, C] or [R, C] (device; R the reduction dimension) -> (E4M3 bytes uint8,
+    transposed: [G, C, R] or [C, R]; int32 scale exponents [G, R/128, C/128] or
+    [R/128, C/128])."""
     shape = W.shape
     G, R, C = (1,) + tuple(shape) if W.dim() == 2 else tuple(shape)
-    Wq = torch.empty(shape, dtype=torch.uint8, device=W.device)
+    Wq = torch.empty(shape[:-2] + (C, R), dtype=torch.uint8, device=W.device)
     S = torch.empty(shape[:-2] + (R // 128, C // 128), dtype=torch.int32, device=W.device)
     _check("moe_quantize_weight_fp8", load().moe_quantize_weight_fp8(
         _ptr(W), G, R, C, _ptr(Wq), _ptr(S), _stream(stream)))

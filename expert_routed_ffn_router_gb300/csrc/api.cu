@@ -209,8 +209,12 @@ struct LayerLayout {
     RouterLayout r;
     DispatchLayout d;
     int32_t *offsets, *perm, *slot_pos;
-    void *Xp, *h, *Yp, *hs, *Xq;
+    void *Xp, *h, *Yp, *hs;
     float *Ysh;
+    // FP8 experts: E4M3 operands of the expert GEMMs and their block scales (fp32 2^k,
+    // [blocks][fp8_scale_pitch(rows)]): permuted rows, token rows (shared expert), h, hs
+    void *Xp8, *X8, *h8, *hs8;
+    float *XpsT, *XsT, *hsT, *hssT;
     unsigned *ready, *ready_sh;   // readiness counters: the FFN launch, the side launch
     moe_workspace_layout_t at;    // byte offsets of the intermediates inside the workspace
     size_t bytes;
@@ -242,9 +246,22 @@ LayerLayout layer_layout(const moe_shape_t &s, unsigned char *ws)
     L.Yp = take(TK * s.H * 2);
     L.at.Yp = at;
     L.hs = take(static_cast<size_t>(s.T) * s.I_shared * 2);
-    L.Xq = take(static_cast<size_t>(s.T) * s.H * 2);   // FP8 weights: quantised token rows
     L.Ysh = reinterpret_cast<float *>(take(s.I_shared > 0 ? static_cast<size_t>(s.T) * s.H * 4 : 0));
     L.at.Ysh = at;
+    {
+        const size_t pT = static_cast<size_t>(fp8_scale_pitch(s.T));
+        const size_t pTK = static_cast<size_t>(fp8_scale_pitch(static_cast<long long>(TK)));
+        const size_t bH = (s.H + 127) / 128, bI = (s.I + 127) / 128, bIs = (s.I_shared + 127) / 128;
+        L.Xp8 = take(TK * s.H);
+        L.XpsT = reinterpret_cast<float *>(take(bH * pTK * 4));
+        L.X8 = take(static_cast<size_t>(s.T) * s.H);
+        L.XsT = reinterpret_cast<float *>(take(bH * pT * 4));
+        L.h8 = take(TK * s.I);
+        L.hsT = reinterpret_cast<float *>(take(bI * pTK * 4));
+        L.hs8 = take(static_cast<size_t>(s.T) * s.I_shared);
+        L.hssT = reinterpret_cast<float *>(take(bIs * pT * 4));
+    }
+    
     L.ready = reinterpret_cast<unsigned *>(
         take(ffn_ready_slots(static_cast<long long>(TK) + s.T, s.E + 1) * sizeof(unsigned)));
     L.ready_sh = reinterpret_cast<unsigned *>(
@@ -297,7 +314,6 @@ int layer_forward(const moe_shape_t *shape, const moe_weights_t *wt, const moe_w
     if (s.T == 0) return MOE_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int *status = static_cast<int *>(ws);
-    const void *Xin = X;   // FP8: the token rows quantised in vectors of 128 along H
 
     FfnProblem P[2]{};
     int Ipp[2] = {s.I, s.I_shared};
@@ -311,6 +327,9 @@ int layer_forward(const moe_shape_t *shape, const moe_weights_t *wt, const moe_w
     if (fp8) {
         P[0].fp8 = 1;
         P[0].S1 = w8->S1; P[0].S3 = w8->S3; P[0].S2 = w8->S2;
+        P[0].act_s = L.XpsT;
+        P[0].h8 = L.h8;
+        P[0].h_s = L.hsT;
     }
     int n_probs = 1;
     if (s.I_shared > 0) {
@@ -325,6 +344,9 @@ int layer_forward(const moe_shape_t *shape, const moe_weights_t *wt, const moe_w
         if (fp8) {
             P[1].fp8 = 1;
             P[1].S1 = w8->S1s; P[1].S3 = w8->S3s; P[1].S2 = w8->S2s;
+            P[1].act_s = L.XsT;
+            P[1].h8 = L.hs8;
+            P[1].h_s = L.hssT;
         }
         n_probs = 2;
     }
@@ -350,19 +372,24 @@ int layer_forward(const moe_shape_t *shape, const moe_weights_t *wt, const moe_w
                                   L.r.plan, L.r.scr, status, st, &ro);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     record_stage(1, st);
-    if (fp8) {
-        if ((e = launch_quant_rows(X, s.T, s.H, L.Xq, st)) != cudaSuccess) return MOE_ERR_CUDA;
-        Xin = L.Xq;
-    }
     // the dispatch tail also zeroes the FFN's readiness counters
     const size_t n_ready = ffn_ready_slots(static_cast<long long>(s.T) * s.K + s.T, s.E + 1);
-    e = launch_dispatch(Xin, topk_idx, s.T, s.H, s.E, s.K, counts, L.offsets, L.perm, L.slot_pos,
+    e = launch_dispatch(X, topk_idx, s.T, s.H, s.E, s.K, counts, L.offsets, L.perm, L.slot_pos,
                         L.Xp, affinity, L.d.plan, L.d.scr, L.ready, n_ready, status, st);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
+    const long long TK = static_cast<long long>(s.T) * s.K;
+    if (fp8) {
+        // the expert GEMMs' inputs as E4M3 rows with a scale per 128 along H: the permuted
+        // rows and (shared expert) the token rows
+        e = launch_quant_rows_e4m3(L.Xp, TK, s.H, L.Xp8, L.XpsT, fp8_scale_pitch(TK), st);
+        if (e == cudaSuccess && s.I_shared > 0)
+            e = launch_quant_rows_e4m3(X, s.T, s.H, L.X8, L.XsT, fp8_scale_pitch(s.T), st);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
     record_stage(2, st);
 
-    P[0].act = L.Xp;
-    if (s.I_shared > 0 && !side) P[1].act = Xin;
+    P[0].act = fp8 ? L.Xp8 : L.Xp;
+    if (s.I_shared > 0 && !side) P[1].act = fp8 ? L.X8 : X;
     long long hint = static_cast<long long>(s.T) * s.K / s.E;
     if (hint < 1) hint = 1;
     if (!fp8) {
@@ -370,11 +397,13 @@ int layer_forward(const moe_shape_t *shape, const moe_weights_t *wt, const moe_w
                        g_wait_limit_ns, g_inject_stall, g_stage_events_on ? g_stage_events[3] : nullptr);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     } else {
-        // up projections, h quantised in vectors of 128 along I, then the down projections
+        // up projections, h (bf16) quantised to E4M3 in vectors of 128 along I, then the down
+        // projections
         e = launch_ffn(P, n_probs, s.H, Ipp, static_cast<int>(hint), L.ready, true, status, st,
                        g_wait_limit_ns, g_inject_stall, nullptr, 0);
-        if (e == cudaSuccess) e = launch_quant_rows(L.h, static_cast<long long>(s.T) * s.K, s.I, L.h, st);
-        if (e == cudaSuccess && s.I_shared > 0) e = launch_quant_rows(L.hs, s.T, s.I_shared, L.hs, st);
+        if (e == cudaSuccess) e = launch_quant_rows_e4m3(L.h, TK, s.I, L.h8, L.hsT, fp8_scale_pitch(TK), st);
+        if (e == cudaSuccess && s.I_shared > 0)
+            e = launch_quant_rows_e4m3(L.hs, s.T, s.I_shared, L.hs8, L.hssT, fp8_scale_pitch(s.T), st);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
         record_stage(3, st);
         e = launch_ffn(P, n_probs, s.H, Ipp, static_cast<int>(hint), L.ready, true, status, st,

@@ -39,11 +39,20 @@
 // second read; a down tile waits (bounded) until the up tiles of its token tile have
 // published their h rows.
 //
-// FP8 weights (ffn_kernel<PAIR, true>).  The weights arrive as E4M3 bytes with one
-// power-of-two scale per 128 x 128 tile ("Lower latency and higher throughput...",
-// Quantization).  The ring then holds token rows and E4M3 weight boxes; eight more warps
-// dequantise each box into the bf16 tile the MMA reads (exact: q * 2^k fits bf16) in a
-// separate small ring of tiles.  The MMAs and the epilogue are those of the bf16 kernel.
+// FP8 (ffn_kernel<false, true>).  Weights and activations arrive as E4M3 bytes with
+// power-of-two block scales ("Lower latency and higher throughput...", Quantization: one
+// scale per 128 x 128 weight tile, one per 128-element activation vector): the weights
+// transposed to K-major rows ([g][n][k]), the activation rows with their scales in a
+// transposed table ([k/128][rows], fp32 2^k).  A stage holds one 128-wide K block: the
+// E4M3 weight tile and the token rows; the block's scales (the token rows' and the two
+// weight boxes') go to a separate, deeper ring of small slots, so that a stage is free
+// again as soon as its MMAs are done.  The tensor cores multiply the E4M3 bytes
+// (tcgen05.mma kind::f8f6f4, both operands K-major) into a fresh fp32 partial in TMEM (up
+// to eight partials in flight), and the epilogue adds each partial times the block's
+// weight scale and token scale into accumulators held in registers ("promotion" per K
+// block, taken in batches of partials); at the end of the tile it applies SwiGLU (up) or
+// stores (down) as the bf16 kernel does.  Single-CTA tiles of at most 64 token rows
+// (larger groups take several token tiles).
 //
 // Every wait is bounded (globaltimer): when one runs out the kernel records
 // MOE_ERR_DEVICE_TIMEOUT in the status word, the other roles leave their loops, copies and
@@ -63,13 +72,13 @@ constexpr int BK = 64;                    // K per stage = one 128-byte swizzle 
 constexpr int A_BYTES = BM * BK * 2;      // 16 KB: two 64x64 boxes
 constexpr int HALF_A = A_BYTES / 2;
 constexpr int NUM_THREADS = 192;          // producer, MMA, 4 epilogue warps
-constexpr int CONV_WARPS = 8;             // warps that dequantise the FP8 weight tiles
-constexpr int NUM_THREADS_FP8 = NUM_THREADS + 32 * CONV_WARPS;
-constexpr int A8_BYTES = BM * BK;          // 8 KB: the stage's weight tile as E4M3 bytes
-constexpr int FP8_END = 1 << 20;          // scale slot value that tells the converters to stop
-constexpr int FP8_SB = 3;                 // FP8: slots of dequantised weight tiles
+constexpr int NUM_THREADS_FP8 = 224;      // FP8: + the scale producer warp
+constexpr int BK8 = 128;                  // FP8: K per stage = one 128-byte row of E4M3
+constexpr int A8_BYTES = BM * BK8;        // FP8: 16 KB, two 64-row boxes of E4M3 weights
+constexpr int BN8_MAX = 64;               // FP8: token rows per tile (register accumulators)
+constexpr int NPB_MAX = 8;                // FP8: TMEM partial buffers (512 columns at 64 rows)
+constexpr int SR = 32;                    // FP8: slots of the scale ring (one per K block)
 constexpr int TSC = 128;                  // FP8: scale-table entries per box (H, I <= 16384)
-constexpr int MAX_STAGES_FP8 = 24;        // FP8: the E4M3 ring is deeper (its stages are small)
 constexpr int MAX_GROUPS = 1024;          // groups of one problem
 constexpr int MAX_CG = 1040;              // groups of all problems of a launch
 constexpr int CW = 32;                    // epilogue chunk: accumulator columns per TMEM load
@@ -100,6 +109,8 @@ struct FfnArgs {
     CUtensorMap upB[2];      // per problem: activation rows [rows, H]
     CUtensorMap dnA[2];      // per problem: W2
     CUtensorMap dnB[2];      // per problem: h [rows, I]
+    CUtensorMap upS[2];      // FP8, per problem: activation scales [H/128, rows] (fp32)
+    CUtensorMap dnS[2];      // FP8, per problem: h scales [I/128, rows] (fp32)
     ProbDev prob[2];
     int n_probs;
     int bn;                  // token tile: multiple of 16, <= 256
@@ -155,43 +166,43 @@ __device__ __forceinline__ void fence_proxy_async_global()
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// generic-proxy shared-memory stores -> later async-proxy (tensor core) reads
-__device__ __forceinline__ void fence_proxy_async_shared()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 template <bool PAIR, bool FP8>
 __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     ffn_kernel(const __grid_constant__ FfnArgs p)
 {
+    static_assert(!(PAIR && FP8), "FP8 tiles run on single CTAs");
     constexpr int NT = FP8 ? NUM_THREADS_FP8 : NUM_THREADS;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
     const int bn = p.bn, S = p.stages, tab = p.tab;
+    // FP8: partial buffers in TMEM (every K block's MMAs go to the next one)
+    const uint32_t npb = FP8 ? static_cast<uint32_t>(p.tmem_cols / bn) : 2u;
     const int bn_cta = PAIR ? bn / 2 : bn;    // token rows of B staged in this CTA
-    // stage: weight tile (bf16, SW128) | token rows.  With FP8 weights the ring's stages hold
-    // token rows | E4M3 weight bytes, and the dequantised weight tiles have a ring of their
-    // own (FP8_SB slots), so the E4M3 ring can be deep enough to keep HBM busy
-    const int stage_bytes = FP8 ? bn_cta * 128 + A8_BYTES : A_BYTES + bn_cta * 128;
-    const int b_off = FP8 ? 0 : A_BYTES;                      // token rows within a stage
+    // stage: weight tile (SW128) | token rows (SW128)
+    const int b_off = FP8 ? A8_BYTES : A_BYTES;               // token rows within a stage
+    const int stage_bytes = b_off + bn_cta * 128;
     unsigned char *stage_base = smem;
-    unsigned char *abf_base = smem + static_cast<size_t>(S) * stage_bytes;   // FP8 only
-    float *xbuf = reinterpret_cast<float *>(abf_base + (FP8 ? FP8_SB * A_BYTES : 0));
+    // FP8 scale ring: per slot the token rows' scales of one K block (bn + 4 fp32, the copy
+    // starting at a multiple of 4 rows) and the exponents of the stage's two weight boxes
+    const int sl_ints = ((bn + 4) * 4 + 15) & ~15;            // byte offset of the exponents
+    const int sl_bytes = FP8 ? ((sl_ints + 8 + 127) & ~127) : 0;
+    unsigned char *sring = smem + static_cast<size_t>(S) * stage_bytes;
+    float *xbuf = reinterpret_cast<float *>(sring + static_cast<size_t>(FP8 ? SR : 0) * sl_bytes);
     uint64_t *full = reinterpret_cast<uint64_t *>(xbuf + XCHG_FLOATS);
     uint64_t *empty = full + S;
+    // accumulator handoff MMA -> epilogue: bf16 two per-tile buffers, FP8 npb per-K-block
+    // partials
     uint64_t *tfull = empty + S;
-    uint64_t *tempty = tfull + 2;
-    uint64_t *drain = tempty + 2;
+    uint64_t *tempty = tfull + NPB_MAX;
+    uint64_t *drain = tempty + NPB_MAX;
     uint64_t *tqf = drain + 1;                                // [TQ] tile slot written
     uint64_t *tqe = tqf + TQ;                                 // [TQ] tile slot read by all roles
-    uint64_t *cvt = tqe + TQ;                                 // [FP8_SB] FP8: slot dequantised
-    uint64_t *cempty = cvt + (FP8 ? FP8_SB : 0);              // [FP8_SB] FP8: slot consumed
-    int *sc8 = reinterpret_cast<int *>(cempty + (FP8 ? FP8_SB : 0));   // [S][2] box scale exponents
-    int *tsc = sc8 + (FP8 ? 2 * S : 0);                       // [2][TSC] FP8: the tile's scales
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tsc + (FP8 ? 2 * TSC : 0));
+    uint64_t *sfull = tqe + TQ;                               // FP8: [SR] scale slot written
+    uint64_t *sempty = sfull + (FP8 ? SR : 0);                // FP8: [SR] scale slot read
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sempty + (FP8 ? SR : 0));
     static_assert(BK == 64, "the MMA issuer unrolls four K16 steps per stage");
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     // groups of all problems, problem 0's first: first row, rows, the tile order, the tile
@@ -218,7 +229,12 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        if (FP8)
+            for (int r = 0; r < SR; ++r) {
+                mbar_init(&sfull[r], 1);
+                mbar_init(&sempty[r], 128);   // the epilogue threads
+            }
+        for (int b = 0; b < NPB_MAX; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], PAIR ? 256 : 128);
         }
@@ -226,14 +242,9 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         for (int q = 0; q < TQ; ++q) {
             mbar_init(&tqf[q], 1);
             // consumers of a slot: MMA and epilogue (and in a pair the odd CTA's producer
-            // and epilogue, which read their copy of the slot)
-            mbar_init(&tqe[q], PAIR ? 4 : 2);
+            // and epilogue, which read their copy of the slot; with FP8 the scale producer)
+            mbar_init(&tqe[q], PAIR ? 4 : (FP8 ? 3 : 2));
         }
-        if (FP8)
-            for (int q = 0; q < FP8_SB; ++q) {
-                mbar_init(&cvt[q], PAIR ? 2 * CONV_WARPS : CONV_WARPS);
-                mbar_init(&cempty[q], 1);
-            }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -244,6 +255,10 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             prefetch_tmap(&p.upB[pi]);
             prefetch_tmap(&p.dnA[pi]);
             prefetch_tmap(&p.dnB[pi]);
+            if (FP8) {
+                prefetch_tmap(&p.upS[pi]);
+                prefetch_tmap(&p.dnS[pi]);
+            }
         }
     }
     if (warp == 1) {
@@ -435,9 +450,19 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             const uint32_t full_c0 = PAIR ? mapa_shared(smem_u32(full), 0) : 0u;   // even CTA's full[0]
             uint32_t qs = 0, qph = 0;
             // claim the next tile of the list and publish it to every role (and to the odd CTA)
+            // FP8: the counter's next value is fetched one claim ahead, so the atomic's round
+            // trip overlaps a tile's loads instead of stalling the ring at the tile boundary
+            unsigned pend = FP8 ? atomicAdd(p.next_tile, 1u) : 0u;
             auto claim = [&](Tile &T) -> bool {
                 if (!mbar_wait(&tqe[qs], qph ^ 1u, abort_flag, p.status, tmo)) return false;
-                const int t = t_begin + static_cast<int>(atomicAdd(p.next_tile, 1u));
+                unsigned ticket;
+                if (FP8) {
+                    ticket = pend;
+                    pend = atomicAdd(p.next_tile, 1u);
+                } else {
+                    ticket = atomicAdd(p.next_tile, 1u);
+                }
+                const int t = t_begin + static_cast<int>(ticket);
                 if (t < t_end) {
                     T = decode_at(t);
                 } else {
@@ -470,11 +495,12 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    // CTA pairs claim the following tile before this tile's loads are issued,
-                    // so the global atomic, the decode and the hand-over to the odd CTA
-                    // overlap them instead of stalling the ring at the tile boundary (single-
-                    // CTA decode tiles measured better claiming one tile at a time)
-                    if (PAIR && T.ph >= 0) {
+                    // CTA pairs and FP8 tiles claim the following tile before this tile's
+                    // loads are issued, so the global atomic, the decode (the hand-over to the
+                    // odd CTA, the FP8 scale table) overlap them instead of stalling the ring
+                    // at the tile boundary (bf16 single-CTA decode tiles measured better
+                    // claiming one tile at a time)
+                    if ((PAIR || FP8) && T.ph >= 0) {
                         if (!claim(next_T)) { ok = false; break; }
                         have_next = true;
                     }
@@ -498,32 +524,11 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                 const int a1 = up ? mt * 64 : mt * 128 + 64;
                 const int brow = T.row0 + (PAIR && !leader ? n_mma_of(T) / 2 : 0);
                 const int kblocks = up ? P.kb_up : P.kb_dn;
-                // FP8: scale exponents of the two weight boxes of stage kb (a box past the
-                // last weight column reads zeros: any tile's scale does, so its index is
-                // clamped to the last tile of the row)
-                // The tile's scales (one per 128 K rows and box) are copied into a shared
-                // table when the tile starts (asynchronous 4-byte copies, all in flight
-                // together), so the per-stage loop reads them from shared memory.
-                if (FP8) {
-                    const int nkq = (kblocks * BK + 127) / 128;
-                    const int nc = (up ? P.I : P.H) / 128;
-                    const int nr = (up ? P.H : P.I) / 128;
-                    for (int box = 0; box < 2; ++box) {
-                        const int c = min((box ? a1 : a0) / 128, nc - 1);
-                        const int32_t *src = (up ? (box ? P.s3 : P.s1) : P.s2) +
-                                             static_cast<size_t>(T.g) * nr * nc + c;
-                        for (int q = 0; q < nkq; ++q)
-                            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;"
-                                         ::"r"(smem_u32(tsc + box * TSC + q)),
-                                           "l"(reinterpret_cast<uint64_t>(src + static_cast<size_t>(q) * nc))
-                                         : "memory");
-                    }
-                    asm volatile("cp.async.commit_group;" ::: "memory");
-                    asm volatile("cp.async.wait_group 0;" ::: "memory");
-                }
-                if (!up) {
+                if (!up && p.phase_only != 1) {
                     // the h rows of this token tile are complete once every up-projection
-                    // weight tile of it has been stored (each CTA of a pair stores half)
+                    // weight tile of it has been stored (each CTA of a pair stores half); a
+                    // launch of the down projections alone follows the up projections' launch
+                    // on the stream, which already orders h before it
                     const unsigned need = static_cast<unsigned>(P.mt_up * (PAIR ? 2 : 1));
                     const unsigned *flag = p.ready + T.nti;
                     if (ld_acquire(flag) < need) {
@@ -545,16 +550,11 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, tmo)) { ok = false; break; }
                     if (FP8) {
-                        // E4M3 weight boxes into the stage's byte area, token rows as usual;
-                        // each CTA's copies complete on its own barrier, where its converter
-                        // warps wait (they then tell the MMA issuer)
-                        sc8[2 * s] = tsc[(kb * BK) / 128];
-                        sc8[2 * s + 1] = tsc[TSC + (kb * BK) / 128];
-                        unsigned char *a8 = a + bn_cta * 128;
+                        // the two K-major E4M3 weight boxes and the token rows
                         mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(A8_BYTES + bn_cta * 128));
-                        tma_load_3d(a8, mA, &full[s], a0, kb * BK, T.g);
-                        tma_load_3d(a8 + A8_BYTES / 2, mA2, &full[s], a1, kb * BK, T.g);
-                        tma_load_2d(a, mB, &full[s], kb * BK, brow);
+                        tma_load_3d(a, mA, &full[s], kb * BK8, a0, T.g);
+                        tma_load_3d(a + A8_BYTES / 2, mA2, &full[s], kb * BK8, a1, T.g);
+                        tma_load_2d(a + b_off, mB, &full[s], kb * BK8, brow);
                     } else if (!PAIR) {
                         mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(stage_bytes));
                         tma_load_3d(a, mA, &full[s], a0, kb * BK, T.g);
@@ -583,14 +583,6 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                     mbar_wait(&full[j % S], (j / S) & 1u, &dummy_abort, nullptr, 20000000ull);
                 }
             }
-            if (FP8 && ok) {
-                // the converter warps stop at a stage whose scale slot says so (after the
-                // drain above: this arrival moves the stage's barrier one phase on)
-                if (mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, tmo)) {
-                    sc8[2 * s] = FP8_END;
-                    mbar_arrive(&full[s]);
-                }
-            }
         }
     } else if (warp == 1) {
         // -------------------------------------------------------------- MMA issuer
@@ -599,11 +591,15 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             // lasts only ~512 tensor-core cycles, and a longer dependent chain here (index
             // division, descriptor packing) leaves the tensor pipe idle between stages.
             const uint32_t ring0 = smem_u32(stage_base);
-            const uint64_t adesc0 = smem_desc_sw128(FP8 ? smem_u32(abf_base) : ring0, HALF_A, 1024);
+            // A: bf16 MN-major (LBO = the 64-column half), FP8 K-major (128-byte rows)
+            const uint64_t adesc0 = FP8 ? smem_desc_sw128(ring0, 16, 1024) : smem_desc_sw128(ring0, HALF_A, 1024);
             const uint64_t bdesc0 = smem_desc_sw128(ring0 + b_off, 16, 1024);
             const uint32_t stage16 = static_cast<uint32_t>(stage_bytes) >> 4;  // descriptor units
+            // per K step: bf16 K16 = +2048 B along A (MN-major), +32 B along B; FP8 K32 =
+            // +32 B along both
+            constexpr uint32_t ASTEP = FP8 ? 2u : 128u;
             uint32_t s = 0, ph = 0, soff = 0, tc = 0;
-            uint32_t sb = 0, pb = 0, aoff = 0;          // FP8: slot of the dequantised tile
+            uint32_t pb = 0, pph = 0;                   // FP8: partial buffer
             bool ok = true;
             uint32_t qs = 0, qph = 0;
             for (;; ++tc) {
@@ -614,130 +610,119 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                 if (T.ph < 0) break;
                 const ProbDev &P = p.prob[T.pi];
                 const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
-                if (!mbar_wait(&tempty[b], tph ^ 1u, abort_flag, p.status, tmo)) { ok = false; break; }
-                tc_fence_after();
+                if (!FP8) {
+                    if (!mbar_wait(&tempty[b], tph ^ 1u, abort_flag, p.status, tmo)) { ok = false; break; }
+                    tc_fence_after();
+                }
                 const int n_mma = n_mma_of(T);
-                const uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * BM : BM, static_cast<uint32_t>(n_mma), true, false);
-                const uint32_t d_tmem = tmem_base + b * static_cast<uint32_t>(bn);
+                const uint32_t idesc = FP8 ? idesc_e4m3_f32(BM, static_cast<uint32_t>(n_mma))
+                                           : idesc_bf16_f32(PAIR ? 2 * BM : BM, static_cast<uint32_t>(n_mma), true, false);
                 const int kblocks = T.ph == PH_UP ? P.kb_up : P.kb_dn;
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    // FP8: the stage is ready once every converter warp (of both CTAs of a
-                    // pair) has written its dequantised weight tile (after the stage's copies)
-                    const bool got = !FP8 ? mbar_wait(&full[s], ph, abort_flag, p.status, tmo)
-                                     : PAIR ? mbar_wait_cluster(&cvt[sb], pb, abort_flag, p.status, tmo)
-                                            : mbar_wait(&cvt[sb], pb, abort_flag, p.status, tmo);
-                    if (!got) { ok = false; break; }
+                    if (!mbar_wait(&full[s], ph, abort_flag, p.status, tmo)) { ok = false; break; }
+                    // FP8: every K block goes to a fresh partial the epilogue has emptied
+                    if (FP8 && !mbar_wait(&tempty[pb], pph ^ 1u, abort_flag, p.status, tmo)) { ok = false; break; }
                     tc_fence_after();
-                    const uint64_t ad = adesc0 + (FP8 ? aoff : soff), bd = bdesc0 + soff;
-                    // K16 steps: +2048 B along A (MN-major), +32 B along B (K-major)
-                    if (PAIR) {
-                        tc_mma_bf16_pair(d_tmem, ad, bd, idesc, kb != 0 ? 1u : 0u);
-                        tc_mma_bf16_pair(d_tmem, ad + 128, bd + 2, idesc, 1u);
-                        tc_mma_bf16_pair(d_tmem, ad + 256, bd + 4, idesc, 1u);
-                        tc_mma_bf16_pair(d_tmem, ad + 384, bd + 6, idesc, 1u);
-                        tc_commit_pair_mc(&empty[s], 3);
-                        if (FP8) tc_commit_pair_mc(&cempty[sb], 3);
-                    } else {
-                        tc_mma_bf16(d_tmem, ad, bd, idesc, kb != 0 ? 1u : 0u);
-                        tc_mma_bf16(d_tmem, ad + 128, bd + 2, idesc, 1u);
-                        tc_mma_bf16(d_tmem, ad + 256, bd + 4, idesc, 1u);
-                        tc_mma_bf16(d_tmem, ad + 384, bd + 6, idesc, 1u);
+                    const uint64_t ad = adesc0 + soff, bd = bdesc0 + soff;
+                    if (FP8) {
+                        const uint32_t d = tmem_base + pb * static_cast<uint32_t>(bn);
+                        tc_mma_f8(d, ad, bd, idesc, 0u);
+                        tc_mma_f8(d, ad + ASTEP, bd + 2, idesc, 1u);
+                        tc_mma_f8(d, ad + 2 * ASTEP, bd + 4, idesc, 1u);
+                        tc_mma_f8(d, ad + 3 * ASTEP, bd + 6, idesc, 1u);
                         tc_commit(&empty[s]);
-                        if (FP8) tc_commit(&cempty[sb]);
+                        tc_commit(&tfull[pb]);
+                        if (++pb == npb) { pb = 0; pph ^= 1u; }
+                    } else if (PAIR) {
+                        const uint32_t d_tmem = tmem_base + b * static_cast<uint32_t>(bn);
+                        tc_mma_bf16_pair(d_tmem, ad, bd, idesc, kb != 0 ? 1u : 0u);
+                        tc_mma_bf16_pair(d_tmem, ad + ASTEP, bd + 2, idesc, 1u);
+                        tc_mma_bf16_pair(d_tmem, ad + 2 * ASTEP, bd + 4, idesc, 1u);
+                        tc_mma_bf16_pair(d_tmem, ad + 3 * ASTEP, bd + 6, idesc, 1u);
+                        tc_commit_pair_mc(&empty[s], 3);
+                    } else {
+                        const uint32_t d_tmem = tmem_base + b * static_cast<uint32_t>(bn);
+                        tc_mma_bf16(d_tmem, ad, bd, idesc, kb != 0 ? 1u : 0u);
+                        tc_mma_bf16(d_tmem, ad + ASTEP, bd + 2, idesc, 1u);
+                        tc_mma_bf16(d_tmem, ad + 2 * ASTEP, bd + 4, idesc, 1u);
+                        tc_mma_bf16(d_tmem, ad + 3 * ASTEP, bd + 6, idesc, 1u);
+                        tc_commit(&empty[s]);
                     }
                     if (++s == static_cast<uint32_t>(S)) { s = 0; ph ^= 1u; soff = 0; } else { soff += stage16; }
-                    if (FP8) {
-                        if (++sb == static_cast<uint32_t>(FP8_SB)) { sb = 0; pb ^= 1u; aoff = 0; }
-                        else { aoff += static_cast<uint32_t>(A_BYTES) >> 4; }
-                    }
                 }
                 if (!ok) break;
-                if (PAIR) tc_commit_pair_mc(&tfull[b], 3); else tc_commit(&tfull[b]);
+                if (!FP8) {
+                    if (PAIR) tc_commit_pair_mc(&tfull[b], 3); else tc_commit(&tfull[b]);
+                }
             }
             // drain: every MMA issued by this thread has completed before TMEM is freed
             if (PAIR) tc_commit_pair_mc(drain, 1); else tc_commit(drain);
             int dummy_abort = 0;
             mbar_wait(drain, 0, &dummy_abort, nullptr, 20000000ull);
         }
-    } else if (FP8 && warp >= 6) {
-        // ------------------------------------------------------- FP8 weight converters
-        // Each stage's two E4M3 boxes (64 K rows x 64 weight columns, 64-byte rows) become
-        // the bf16 weight tile in the swizzled layout TMA gives bf16 boxes (128-byte rows,
-        // 16-byte chunk c of row r at chunk c ^ (r & 7)), times the box's scale 2^k (exact).
-        // 16-byte chunks of E4M3 spread over the converter threads; then a proxy fence so
-        // the tensor core sees the generic stores, and one arrival per warp.
-        const int ct = tid - NUM_THREADS;
-        const uint32_t cvt_c0 = PAIR ? mapa_shared(smem_u32(cvt), 0) : 0u;   // even CTA's cvt[0]
-        uint32_t s = 0, ph = 0, sb = 0, pb = 0;
-        for (;;) {
-            if (!mbar_wait(&full[s], ph, abort_flag, p.status, tmo)) break;
-            const int k0 = sc8[2 * s], k1 = sc8[2 * s + 1];
-            if (k0 == FP8_END) break;
-            if (!mbar_wait(&cempty[sb], pb ^ 1u, abort_flag, p.status, tmo)) break;
-            const uint32_t abf = smem_u32(abf_base) + sb * static_cast<uint32_t>(A_BYTES);
-            const uint32_t a8 = smem_u32(stage_base) + s * static_cast<uint32_t>(stage_bytes) +
-                                static_cast<uint32_t>(bn_cta) * 128u;
-            // every chunk's bytes first (independent shared loads), then the conversions
-            constexpr int NCH = 16 / CONV_WARPS;
-            uint32_t w[NCH][4];
-#pragma unroll
-            for (int j = 0; j < NCH; ++j) {
-                const uint32_t addr = a8 + 16u * static_cast<uint32_t>(ct + 32 * CONV_WARPS * j);
-                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(w[j][0]), "=r"(w[j][1]), "=r"(w[j][2]), "=r"(w[j][3]) : "r"(addr));
-            }
-            // bit moves (x 2^-120) then one packed multiply by 2^(120 + k): a power of two,
-            // so exact, and the results are normal bf16 for -117 <= k <= 7; other scales go
-            // through fp32 (exact power-of-two products)
-            const bool fast = k0 >= -117 && k0 <= 7 && k1 >= -117 && k1 <= 7;
-            const uint32_t e0 = static_cast<uint32_t>(247 + k0) << 7, e1 = static_cast<uint32_t>(247 + k1) << 7;
-            const uint32_t sc_a = e0 | (e0 << 16), sc_b = e1 | (e1 << 16);
-#pragma unroll
-            for (int j = 0; j < NCH; ++j) {
-                const int chunk = ct + 32 * CONV_WARPS * j;   // 0..511 over the two 4 KB boxes
-                const int box = chunk >> 8, r = (chunk >> 2) & 63, cq = chunk & 3;
-                uint32_t o[8];
-                if (fast) {
-                    const uint32_t sc2 = box ? sc_b : sc_a;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint32_t x, y;
-                        e4m3x4_to_bf16x2_shifted(w[j][i], x, y);
-                        o[2 * i] = bf16x2_mul(x, sc2);
-                        o[2 * i + 1] = bf16x2_mul(y, sc2);
-                    }
-                } else {
-                    const float sc = pow2f(box ? k1 : k0);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 f0 = e4m3x2_to_f32x2(static_cast<uint16_t>(w[j][i] & 0xffffu));
-                        const float2 f1 = e4m3x2_to_f32x2(static_cast<uint16_t>(w[j][i] >> 16));
-                        o[2 * i] = f32x2_to_bf16x2(f0.y * sc, f0.x * sc);
-                        o[2 * i + 1] = f32x2_to_bf16x2(f1.y * sc, f1.x * sc);
-                    }
+    } else if (FP8 && warp == 6) {
+        // ------------------------------------------------------- FP8 scale producer
+        // For every K block of every tile, in the order of the other roles: the token rows'
+        // scales (a TMA copy from row0 rounded down to a multiple of 4 rows: a TMA copy's
+        // innermost coordinate must be 16-byte aligned) and the exponents of the tile's two
+        // weight boxes (asynchronous 4-byte copies whose completion the slot barrier
+        // tracks) into the next slot of the scale ring.  Kept off the TMA producer's thread,
+        // whose per-stage work sets the pace of the weight stream.
+        if (lane == 0 && !p.inject) {
+            uint32_t r = 0, rph = 0, n_sc = 0, qs = 0, qph = 0;
+            bool ok = true;
+            while (ok) {
+                if (!mbar_wait(&tqf[qs], qph, abort_flag, p.status, tmo)) break;
+                const Tile T = slot_read(qs);
+                tqe_arrive(qs);
+                if (++qs == TQ) { qs = 0; qph ^= 1u; }
+                if (T.ph < 0) break;
+                const ProbDev &P = p.prob[T.pi];
+                const bool up = T.ph == PH_UP;
+                const int a0 = up ? T.mt * 64 : T.mt * 128, a1 = up ? T.mt * 64 : T.mt * 128 + 64;
+                // the boxes' exponents, one per K block (row stride nc of the [g][K/128][N/128]
+                // table; a box past the last weight column reads zeros: any tile's scale
+                // does, so its index is clamped)
+                const int nc = (up ? P.I : P.H) / 128, nr = (up ? P.H : P.I) / 128;
+                const int32_t *src[2];
+                for (int box = 0; box < 2; ++box) {
+                    const int c = min((box ? a1 : a0) / 128, nc - 1);
+                    src[box] = (up ? (box ? P.s3 : P.s1) : P.s2) + static_cast<size_t>(T.g) * nr * nc + c;
                 }
-                const uint32_t row = abf + static_cast<uint32_t>(box * HALF_A + r * 128);
-                const uint32_t d0 = row + ((static_cast<uint32_t>(2 * cq) ^ static_cast<uint32_t>(r & 7)) << 4);
-                const uint32_t d1 = row + ((static_cast<uint32_t>(2 * cq + 1) ^ static_cast<uint32_t>(r & 7)) << 4);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
-                             ::"r"(d0), "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]) : "memory");
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
-                             ::"r"(d1), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7]) : "memory");
+                const CUtensorMap *mS = up ? &p.upS[T.pi] : &p.dnS[T.pi];
+                const int kblocks = up ? P.kb_up : P.kb_dn;
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait(&sempty[r], rph ^ 1u, abort_flag, p.status, tmo)) { ok = false; break; }
+                    unsigned char *sl = sring + static_cast<size_t>(r) * sl_bytes;
+                    const uint32_t ex = smem_u32(sl + sl_ints);
+                    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;"
+                                 ::"r"(ex), "l"(reinterpret_cast<uint64_t>(src[0] + static_cast<size_t>(kb) * nc))
+                                 : "memory");
+                    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;"
+                                 ::"r"(ex + 4u), "l"(reinterpret_cast<uint64_t>(src[1] + static_cast<size_t>(kb) * nc))
+                                 : "memory");
+                    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];"
+                                 ::"r"(smem_u32(&sfull[r])) : "memory");
+                    mbar_arrive_expect_tx(&sfull[r], static_cast<uint32_t>((bn + 4) * 4));
+                    tma_load_2d(sl, mS, &sfull[r], T.row0 & ~3, kb);
+                    ++n_sc;
+                    if (++r == static_cast<uint32_t>(SR)) { r = 0; rph ^= 1u; }
+                }
             }
-            fence_proxy_async_shared();
-            __syncwarp();
-            if (lane == 0) {
-                if (PAIR) mbar_arrive_cluster(cvt_c0 + 8u * sb);
-                else mbar_arrive(&cvt[sb]);
+            // every copy issued lands before the CTA can exit
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            const uint32_t n = n_sc < static_cast<uint32_t>(SR) ? n_sc : static_cast<uint32_t>(SR);
+            for (uint32_t j = n_sc - n; j < n_sc; ++j) {
+                int dummy_abort = 0;
+                mbar_wait(&sfull[j % SR], (j / SR) & 1u, &dummy_abort, nullptr, 20000000ull);
             }
-            if (++s == static_cast<uint32_t>(S)) { s = 0; ph ^= 1u; }
-            if (++sb == static_cast<uint32_t>(FP8_SB)) { sb = 0; pb ^= 1u; }
         }
     } else {
         // ----------------------------------------------------------------- epilogue
         const int q = warp & 3;                 // TMEM lane quarter of this warp
         uint32_t tc = 0, cc = 0;
         uint32_t qs = 0, qph = 0;
+        uint32_t es = 0, eph = 0, epb = 0, epph = 0;   // FP8: scale slot and partial buffer
         for (;; ++tc) {
             const bool okq = (PAIR && !leader)
                                  ? mbar_wait_cluster(&tqf[qs], qph, abort_flag, p.status, tmo)
@@ -750,23 +735,141 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             if (T.ph < 0) break;
             const ProbDev &P = p.prob[T.pi];
             const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
-            const bool ok = mbar_wait(&tfull[b], tph, abort_flag, p.status, tmo);
-            if (!epi_all(ok)) break;
-            tc_fence_after();
-            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * static_cast<uint32_t>(bn);
             const int nchunks = (T.nvalid + CW - 1) / CW;
             const int mt = mt_cta(T);
-            // one chunk = CW token columns of this warp's 32 accumulator rows (a 16-row
-            // tile has only 16 columns per buffer)
-            auto load_chunk = [&](int c, float (&v)[CW]) {
+            // 32 lanes x 16 or 32 columns of TMEM (a 16-row tile has 16 columns per buffer)
+            auto tmem_cols = [&](uint32_t taddr, float (&v)[CW]) {
                 __syncwarp();
                 if (bn >= CW) {
-                    tmem_ld32(tbase + CW * c, v);
+                    tmem_ld32(taddr, v);
                 } else {
                     float h[16];
-                    tmem_ld16(tbase, h);
+                    tmem_ld16(taddr, h);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) { v[j] = h[j]; v[j + 16] = 0.f; }
+                }
+            };
+            float acc[2][CW];   // FP8: the tile's accumulators, at most 64 token columns
+            if (FP8) {
+                // promotion: every K block's partial times 2^(weight tile exponent) times
+                // the token row's 2^(exponent), added in K-block order.  The partials are
+                // taken in batches of 128 TMEM columns (4 K blocks of 32 rows, 2 of 64, 8
+                // of 16): one round of waits, one barrier and one load latency per batch.
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int j = 0; j < CW; ++j) acc[c][j] = 0.f;
+                const int kblocks = T.ph == PH_UP ? P.kb_up : P.kb_dn;
+                const int box = (T.ph == PH_UP && q >= 2) ? 1 : 0;   // U (W3) rows: lanes 64..127
+                const int per_batch = bn == 16 ? 4 : 128 / bn;       // K blocks a batch
+                const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
+                bool got_all = true;
+                int kb0 = 0;
+                while (kb0 < kblocks) {
+                    // K blocks of this batch: within the tile and the partial ring
+                    int nb = kblocks - kb0;
+                    if (nb > per_batch) nb = per_batch;
+                    if (nb > static_cast<int>(npb - epb)) nb = static_cast<int>(npb - epb);
+                    bool got = true;
+                    {
+                        uint32_t si = es, phi = eph;
+                        for (int i = 0; i < nb; ++i) {
+                            got = got && mbar_wait(&sfull[si], phi, abort_flag, p.status, tmo) &&
+                                  mbar_wait(&tfull[epb + i], epph, abort_flag, p.status, tmo);
+                            if (++si == static_cast<uint32_t>(SR)) { si = 0; phi ^= 1u; }
+                        }
+                    }
+                    if (!epi_all(got)) { got_all = false; break; }
+                    tc_fence_after();
+                    __syncwarp();
+                    float v[128];
+                    const uint32_t pb0 = tmem_base + lane_off + epb * static_cast<uint32_t>(bn);
+                    if (bn == 16) {
+                        uint32_t ad[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) ad[i] = pb0 + 16u * static_cast<uint32_t>(i < nb ? i : 0);
+                        tmem_ld16x8(ad, v);
+                    } else {
+                        // 32 columns a load: (K block i, chunk c) -> load i * nck + c
+                        const int nck = bn / CW;           // 1 or 2
+                        uint32_t ad[4];
+#pragma unroll
+                        for (int l = 0; l < 4; ++l) {
+                            const int i = l / nck, c = l - i * nck;
+                            ad[l] = i < nb ? pb0 + static_cast<uint32_t>(i * bn + CW * c) : pb0;
+                        }
+                        tmem_ld32x4(ad[0], ad[1], ad[2], ad[3], v);
+                    }
+                    // the scales of K block i sit in scale slot es + i
+                    auto stage_scales = [&](int i, float &sw, const float *&xs) {
+                        uint32_t si = es + static_cast<uint32_t>(i);
+                        if (si >= static_cast<uint32_t>(SR)) si -= static_cast<uint32_t>(SR);
+                        const unsigned char *sl = sring + static_cast<size_t>(si) * sl_bytes;
+                        sw = pow2f(reinterpret_cast<const int *>(sl + sl_ints)[box]);
+                        xs = reinterpret_cast<const float *>(sl) + (T.row0 & 3);
+                    };
+                    if (bn == 16) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            if (i < nb) {
+                                float sw;
+                                const float *xs;
+                                stage_scales(i, sw, xs);
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) acc[0][j] = fmaf(v[16 * i + j], sw * xs[j], acc[0][j]);
+                            }
+                        }
+                    } else if (bn == 32) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            if (i < nb) {
+                                float sw;
+                                const float *xs;
+                                stage_scales(i, sw, xs);
+#pragma unroll
+                                for (int j = 0; j < CW; ++j) acc[0][j] = fmaf(v[32 * i + j], sw * xs[j], acc[0][j]);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            if (i < nb) {
+                                float sw;
+                                const float *xs;
+                                stage_scales(i, sw, xs);
+#pragma unroll
+                                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                                    for (int j = 0; j < CW; ++j)
+                                        acc[c][j] = fmaf(v[64 * i + 32 * c + j], sw * xs[CW * c + j], acc[c][j]);
+                            }
+                        }
+                    }
+                    // release the batch's partials and scale slots
+                    tc_fence_before();
+                    for (int i = 0; i < nb; ++i) {
+                        mbar_arrive(&tempty[epb + i]);
+                        mbar_arrive(&sempty[es]);
+                        if (++es == static_cast<uint32_t>(SR)) { es = 0; eph ^= 1u; }
+                    }
+                    epb += static_cast<uint32_t>(nb);
+                    if (epb == npb) { epb = 0; epph ^= 1u; }
+                    kb0 += nb;
+                }
+                if (!got_all) break;
+            } else {
+                const bool ok = mbar_wait(&tfull[b], tph, abort_flag, p.status, tmo);
+                if (!epi_all(ok)) break;
+                tc_fence_after();
+            }
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * static_cast<uint32_t>(bn);
+            // one chunk = CW token columns of this warp's 32 accumulator rows
+            auto load_chunk = [&](int c, float (&v)[CW]) {
+                if (FP8) {
+#pragma unroll
+                    for (int j = 0; j < CW; ++j) v[j] = c ? acc[1][j] : acc[0][j];
+                } else {
+                    tmem_cols(tbase + CW * c, v);
                 }
             };
             if (T.ph == PH_UP) {
@@ -799,11 +902,15 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                     }
                 }
                 // publish: this CTA's columns of the token tile are in h (generic-proxy
-                // stores, read later by other SMs' TMA)
-                fence_proxy_async_global();
-                __threadfence();
-                named_bar_sync(3, 128);
-                if (warp == 2 && lane == 0) atomicAdd(p.ready + T.nti, 1u);
+                // stores, read later by other SMs' TMA).  A launch of the up projections
+                // alone is followed on the stream by the launch that reads h, which orders
+                // the stores without fences or counters.
+                if (p.phase_only != 0) {
+                    fence_proxy_async_global();
+                    __threadfence();
+                    named_bar_sync(3, 128);
+                    if (warp == 2 && lane == 0) atomicAdd(p.ready + T.nti, 1u);
+                }
             } else {
                 const int col = mt * 128 + q * 32 + lane;
                 const bool col_ok = col < P.H;
@@ -830,11 +937,13 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                     }
                 }
             }
-            tc_fence_before();
-            if (PAIR)
-                mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[b]), 0));
-            else
-                mbar_arrive(&tempty[b]);
+            if (!FP8) {
+                tc_fence_before();
+                if (PAIR)
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[b]), 0));
+                else
+                    mbar_arrive(&tempty[b]);
+            }
         }
     }
 
@@ -877,24 +986,66 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 3-D weight tensor [n_groups][rows][cols] (cols contiguous), 64 x 64 boxes: bf16 into the
-// 128-byte swizzle the MMA reads, or E4M3 bytes (fp8) as plain 64-byte rows.
-bool encode_weight(CUtensorMap *m, const void *base, int n_groups, int rows, int cols,
-                   bool fp8 = false)
+// 3-D bf16 weight tensor [n_groups][rows][cols] (cols contiguous), 64 x 64 boxes in the
+// 128-byte swizzle the MMA reads (MN-major operand).
+bool encode_weight(CUtensorMap *m, const void *base, int n_groups, int rows, int cols)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t esz = fp8 ? 1 : 2;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
                           static_cast<cuuint64_t>(n_groups)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * esz,
-                             static_cast<cuuint64_t>(cols) * rows * esz};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2,
+                             static_cast<cuuint64_t>(cols) * rows * 2};
     cuuint32_t box[3] = {64, 64, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D E4M3 weight tensor [n_groups][n][k] (k contiguous: K-major rows), boxes of 128 k x 64
+// rows in the 128-byte swizzle.
+bool encode_weight8(CUtensorMap *m, const void *base, int n_groups, int n, int k)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(n),
+                          static_cast<cuuint64_t>(n_groups)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(k) * n};
+    cuuint32_t box[3] = {128, 64, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D E4M3 activation rows [rows][k], boxes of 128 k x box_rows rows (128-byte swizzle).
+bool encode_act8(CUtensorMap *m, const void *base, int rows, int k, int box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(k)};
+    cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D fp32 scale table [blocks][pitch] (rows valid of each pitch), boxes of box_rows x 1.
+bool encode_scales(CUtensorMap *m, const float *base, int rows, long long pitch, int blocks,
+                   int box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(blocks)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch) * 4};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 2-D bf16 activation tensor [rows][cols], boxes of 64 columns x box_rows rows.
@@ -925,17 +1076,17 @@ int pick_bn(int avg_rows)
 
 size_t ffn_smem_bytes(int bn_cta, int stages, int tab, bool fp8)
 {
-    const size_t stage = fp8 ? static_cast<size_t>(bn_cta) * 128 + A8_BYTES
-                             : static_cast<size_t>(A_BYTES) + bn_cta * 128;
-    return 1024 + stages * stage + (fp8 ? static_cast<size_t>(FP8_SB) * A_BYTES : 0) +
-           XCHG_FLOATS * 4 + (2 * stages + 5 + 2 * TQ) * 8 + (fp8 ? 2 * FP8_SB * 8 + stages * 8 + 2 * TSC * 4 : 0) +
-           16 + (6 * static_cast<size_t>(tab) + 8 * TQ) * 4;
+    const size_t stage = static_cast<size_t>(fp8 ? A8_BYTES : A_BYTES) + bn_cta * 128;
+    const size_t slot = ((((bn_cta + 4) * 4 + 15) & ~static_cast<size_t>(15)) + 8 + 127) & ~static_cast<size_t>(127);
+    return 1024 + stages * stage + (fp8 ? SR * slot : 0) + XCHG_FLOATS * 4 +
+           (2 * stages + 2 * NPB_MAX + 1 + 2 * TQ) * 8 + (fp8 ? 2 * SR * 8 : 0) + 16 +
+           (6 * static_cast<size_t>(tab) + 8 * TQ) * 4;
 }
 
 int pick_stages(int bn_cta, int tab, bool fp8)
 {
     const size_t cap = 232448;   // max dynamic shared memory per block on sm_100/sm_103
-    int s = fp8 ? MAX_STAGES_FP8 : MAX_STAGES;
+    int s = MAX_STAGES;
     while (s > 2 && ffn_smem_bytes(bn_cta, s, tab, fp8) > cap) --s;
     return s;
 }
@@ -969,7 +1120,8 @@ cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I
     for (int pi = 0; pi < n_probs; ++pi) {
         if (probs[pi].n_groups < 1 || probs[pi].n_groups > MAX_GROUPS) return cudaErrorInvalidValue;
         if ((probs[pi].fp8 != 0) != fp8) return cudaErrorInvalidValue;
-        if (fp8 && (!probs[pi].S1 || !probs[pi].S3 || !probs[pi].S2 || H % 128 || I_pp[pi] % 128 ||
+        if (fp8 && (!probs[pi].S1 || !probs[pi].S3 || !probs[pi].S2 || !probs[pi].act_s ||
+                    !probs[pi].h8 || !probs[pi].h_s || H % 128 || I_pp[pi] % 128 ||
                     H > 128 * TSC || I_pp[pi] > 128 * TSC))
             return cudaErrorInvalidValue;
         n_cg += probs[pi].n_groups;
@@ -977,14 +1129,16 @@ cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I
     }
     if (n_cg > MAX_CG) return cudaErrorInvalidValue;
     int bn = pick_bn(token_hint);
-    bool pair = g_variant == 2 || (g_variant == 0 && bn >= PAIR_MIN_BN);
+    if (fp8 && bn > BN8_MAX) bn = BN8_MAX;     // FP8: register accumulators, single CTAs
+    bool pair = !fp8 && (g_variant == 2 || (g_variant == 0 && bn >= PAIR_MIN_BN));
     if (pair && bn < 32) bn = 32;           // 16 token rows per CTA at least
     const int bn_cta = pair ? bn / 2 : bn;
     const int tab = (n_cg + 1 + 3) & ~3;
     const int stages = pick_stages(bn_cta, tab, fp8);
     const size_t smem = ffn_smem_bytes(bn_cta, stages, tab, fp8);
+    // TMEM columns: two accumulators of bn columns; FP8: NPB_MAX partials of bn (at most 512)
     int tcols = 32;
-    while (tcols < 2 * bn) tcols <<= 1;
+    while (tcols < (fp8 ? NPB_MAX : 2) * bn && tcols < 512) tcols <<= 1;
     const int m_up = pair ? 128 : 64;      // weight columns of one tile
     const int m_dn = pair ? 256 : 128;
 
@@ -993,20 +1147,31 @@ cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I
     for (int pi = 0; pi < n_probs; ++pi) {
         const FfnProblem &P = probs[pi];
         const int I = I_pp[pi];
-        if (!encode_weight(&a.upA[pi], P.W1, P.n_groups, H, I, fp8) ||
-            !encode_weight(&a.upA3[pi], P.W3, P.n_groups, H, I, fp8) ||
-            !encode_act(&a.upB[pi], P.act, P.rows, H, bn_cta) ||
-            !encode_weight(&a.dnA[pi], P.W2, P.n_groups, I, H, fp8) ||
-            !encode_act(&a.dnB[pi], P.h, P.rows, I, bn_cta))
+        if (fp8) {
+            const long long pitch = fp8_scale_pitch(P.rows);
+            if (!encode_weight8(&a.upA[pi], P.W1, P.n_groups, I, H) ||
+                !encode_weight8(&a.upA3[pi], P.W3, P.n_groups, I, H) ||
+                !encode_act8(&a.upB[pi], P.act, P.rows, H, bn) ||
+                !encode_scales(&a.upS[pi], P.act_s, P.rows, pitch, H / 128, bn + 4) ||
+                !encode_weight8(&a.dnA[pi], P.W2, P.n_groups, H, I) ||
+                !encode_act8(&a.dnB[pi], P.h8, P.rows, I, bn) ||
+                !encode_scales(&a.dnS[pi], P.h_s, P.rows, pitch, I / 128, bn + 4))
+                return cudaErrorInvalidValue;
+        } else if (!encode_weight(&a.upA[pi], P.W1, P.n_groups, H, I) ||
+                   !encode_weight(&a.upA3[pi], P.W3, P.n_groups, H, I) ||
+                   !encode_act(&a.upB[pi], P.act, P.rows, H, bn_cta) ||
+                   !encode_weight(&a.dnA[pi], P.W2, P.n_groups, I, H) ||
+                   !encode_act(&a.dnB[pi], P.h, P.rows, I, bn_cta)) {
             return cudaErrorInvalidValue;
+        }
         ProbDev d{};
         d.offsets = P.offsets;
         d.n_groups = P.n_groups;
         d.dense_rows = P.dense_rows;
         d.mt_up = (I + m_up - 1) / m_up;
         d.mt_dn = (H + m_dn - 1) / m_dn;
-        d.kb_up = H / 64;
-        d.kb_dn = I / 64;
+        d.kb_up = H / (fp8 ? BK8 : BK);
+        d.kb_dn = I / (fp8 ? BK8 : BK);
         d.I = I;
         d.H = H;
         d.out_fp32 = P.out_fp32;
@@ -1031,8 +1196,7 @@ cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I
     cudaError_t err;
     if (!ready_zeroed && (err = cudaMemsetAsync(ready, 0, slots * sizeof(unsigned), s)) != cudaSuccess)
         return err;
-    const void *fn = fp8 ? (pair ? reinterpret_cast<const void *>(ffn_kernel<true, true>)
-                                 : reinterpret_cast<const void *>(ffn_kernel<false, true>))
+    const void *fn = fp8 ? reinterpret_cast<const void *>(ffn_kernel<false, true>)
                          : (pair ? reinterpret_cast<const void *>(ffn_kernel<true, false>)
                                  : reinterpret_cast<const void *>(ffn_kernel<false, false>));
     if ((err = ensure_smem(fn, smem)) != cudaSuccess) return err;
@@ -1043,8 +1207,7 @@ cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I
     const int n_cta = max_ctas > 0 && max_ctas < num_sms() ? max_ctas : num_sms();
     const dim3 grid_pair(n_cta / 2 > 0 ? n_cta / 2 * 2 : 2), grid_one(n_cta);
     if (fp8)
-        err = pair ? launch_pdl(ffn_kernel<true, true>, grid_pair, block, smem, s, 2, a)
-                   : launch_pdl(ffn_kernel<false, true>, grid_one, block, smem, s, 1, a);
+        err = launch_pdl(ffn_kernel<false, true>, grid_one, block, smem, s, 1, a);
     else
         err = pair ? launch_pdl(ffn_kernel<true, false>, grid_pair, block, smem, s, 2, a)
                    : launch_pdl(ffn_kernel<false, false>, grid_one, block, smem, s, 1, a);

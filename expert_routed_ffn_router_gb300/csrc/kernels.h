@@ -63,13 +63,18 @@ cudaError_t launch_dispatch(const void *X, const int32_t *topk_idx, int T, int H
                             unsigned *zero_buf, size_t zero_n, int *status, cudaStream_t s);
 
 // ------------------------------------------------------------------------------ fp8
-// Static E4M3 quantisation of W [G][R][C] bf16 (R, C multiples of 128) into Wq [G][R][C]
-// bytes and the scale exponents S [G][R/128][C/128] (scale 2^S).
+// Static E4M3 quantisation of W [G][R][C] bf16 (R, C multiples of 128; R the reduction
+// dimension) into Wq [G][C][R] bytes (transposed: K-major rows for the FP8 MMA) and the
+// scale exponents S [G][R/128][C/128] (scale 2^S).
 cudaError_t launch_quant_weight(const void *W, int G, int R, int C, void *Wq, int32_t *S,
                                 cudaStream_t s);
 // Quantise-dequantise bf16 rows [rows][n] (n a multiple of 128) in vectors of 128 into out
 // (may alias in).
 cudaError_t launch_quant_rows(const void *in, long long rows, int n, void *out, cudaStream_t s);
+// bf16 rows [rows][n] in vectors of 128 -> E4M3 bytes out [rows][n] and the scales 2^k as
+// fp32 sT [n / 128][rows].
+cudaError_t launch_quant_rows_e4m3(const void *in, long long rows, int n, void *out, float *sT,
+                                   long long ld_sT, cudaStream_t s);
 
 // -------------------------------------------------------------------------- combine
 cudaError_t launch_combine(const void *Yp, const int32_t *slot_pos, const float *topk_w,
@@ -88,12 +93,23 @@ struct FfnProblem {
     void *h;                // bf16 [rows, I] activation scratch
     void *out;              // [rows, H] bf16 or fp32
     int out_fp32;
-    // FP8 weights: W1, W3, W2 hold E4M3 bytes and S1, S3 [n_groups][H/128][I/128], S2
-    // [n_groups][I/128][H/128] the scale exponents of their 128 x 128 tiles (H, I multiples
-    // of 128).  Every problem of a launch uses the same weight format.
+    // FP8: W1, W3 hold E4M3 bytes [n_groups, I, H] and W2 [n_groups, H, I] (K-major rows),
+    // S1, S3 [n_groups][H/128][I/128], S2 [n_groups][I/128][H/128] the scale exponents of
+    // their 128 x 128 tiles (H, I multiples of 128); `act` holds E4M3 rows [rows, H] with
+    // their scales 2^k in act_s [H/128][fp8_scale_pitch(rows)] (fp32); the up projection
+    // writes h (bf16) and the down projection reads its E4M3 quantisation h8 [rows, I] with
+    // scales h_s [I/128][fp8_scale_pitch(rows)].  Every problem of a launch uses the same
+    // format.
     int fp8;
     const int32_t *S1, *S3, *S2;
+    const float *act_s;
+    const void *h8;
+    const float *h_s;
 };
+
+// Row pitch (in scales) of an FP8 scale table [blocks][rows]: a multiple of 4 rows, so that
+// the table's row stride is a multiple of 16 bytes (a TMA requirement).
+inline long long fp8_scale_pitch(long long rows) { return (rows + 3) & ~3ll; }
 
 // Launch with programmatic stream serialization (the kernel overlaps its prologue with
 // the previous kernel's tail and calls pdl_wait() before reading its inputs) and, with

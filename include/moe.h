@@ -89,11 +89,14 @@ typedef struct moe_weights {
 
 /* Layer weights with FP8 experts ("Lower latency and higher throughput...", Quantization:
  * weights quantised ahead of time with one scale per 128 x 128 tile).  W_gate and bias as in
- * moe_weights_t (the router is not quantised).  W1, W3, W2 (and W1s, W3s, W2s) hold E4M3
- * bytes in the layouts of moe_weights_t; S1, S3 int32 [E, H/128, I/128] and S2 int32
+ * moe_weights_t (the router is not quantised).  W1, W3 hold E4M3 bytes [E, I, H] and W2
+ * [E, H, I] (W1s, W3s [I_shared, H], W2s [H, I_shared]): each matrix of moe_weights_t
+ * TRANSPOSED, so that every output column's reduction values are contiguous (the K-major
+ * rows the FP8 tensor-core MMA reads).  S1, S3 int32 [E, H/128, I/128] and S2 int32
  * [E, I/128, H/128] (S1s, S3s [H/128, I_shared/128], S2s [I_shared/128, H/128]) hold the
- * scale exponents: a weight is its E4M3 value times 2^S of its tile.
- * moe_quantize_weight_fp8 produces both from bf16 weights. */
+ * scale exponents, indexed as the untransposed matrices' 128 x 128 tiles: a weight is its
+ * E4M3 value times 2^S of its tile.  moe_quantize_weight_fp8 produces both from bf16
+ * weights. */
 typedef struct moe_weights_fp8 {
     const void *W_gate;
     const float *bias;
@@ -113,9 +116,9 @@ size_t moe_workspace_bytes(const moe_shape_t *shape);
  * rows), h bf16 [T*K, I] (the SwiGLU activations), Yp bf16 [T*K, H] (the expert outputs)
  * and Ysh fp32 [T, H] (the shared expert's output; 0 when I_shared == 0), and `bytes` =
  * moe_workspace_bytes(shape).  They hold what the last layer call on that workspace left
- * there, once its stream has reached the end of the call (with FP8 experts, Xp and h hold
- * the rows after their quantisation to E4M3 and back).  For inspection and testing; not on
- * the pages.  Returns MOE_OK, or MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED_SHAPE for a
+ * there, once its stream has reached the end of the call (with FP8 experts, h and Yp hold
+ * the bf16 activations and outputs the FP8 GEMMs read and wrote; their E4M3 operands live
+ * elsewhere in the workspace).  For inspection and testing; not on the pages.  Returns MOE_OK, or MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED_SHAPE for a
  * shape moe_workspace_bytes rejects. */
 typedef struct moe_workspace_layout {
     size_t offsets, perm, slot_pos, Xp, h, Yp, Ysh, bytes;
@@ -323,8 +326,9 @@ int moe_layer_forward_ex(const moe_shape_t *shape, const moe_weights_t *weights,
  * ------------------------------------------------------------------------------------ */
 
 /* Static weight quantisation: W bf16 [G, R, C] (R, C multiples of 128, else
- * MOE_ERR_UNSUPPORTED_SHAPE) -> Wq E4M3 bytes [G, R, C] and S int32 [G, R/128, C/128] (the
- * tile's k).  Device pointers, enqueued on `stream`. */
+ * MOE_ERR_UNSUPPORTED_SHAPE; R is the reduction dimension: H for W1 / W3, I for W2) -> Wq
+ * E4M3 bytes [G, C, R] (transposed) and S int32 [G, R/128, C/128] (the tile's k).  Device
+ * pointers, enqueued on `stream`. */
 int moe_quantize_weight_fp8(const void *W, int G, int R, int C, void *Wq, int32_t *S,
                             void *stream);
 
@@ -334,12 +338,13 @@ int moe_quantize_weight_fp8(const void *W, int G, int R, int C, void *Wq, int32_
 int moe_quantize_rows_fp8(const void *in, long long rows, int n, void *out, void *stream);
 
 /* The layer with FP8 experts: as moe_layer_forward_ex, with the expert FFNs (routed and
- * shared) computed from the dequantised E4M3 weights on token rows quantised in vectors
- * of 128 along H and on h = silu(x W1) * (x W3), rounded to bf16, quantised in vectors of
- * 128 along I.  The GEMMs sum the exact products of the dequantised values in fp32 -- what
- * an FP8 GEMM with these block scales computes.  H, I and I_shared must be multiples of
- * 128 and at most 16384 (else MOE_ERR_UNSUPPORTED_SHAPE).  Same workspace as
- * moe_layer_forward. */
+ * shared) computed from the E4M3 weights and their tile scales on token rows quantised in
+ * vectors of 128 along H and on h = silu(x W1) * (x W3), rounded to bf16, quantised in
+ * vectors of 128 along I.  The tensor cores multiply the E4M3 values (FP8 MMA) one
+ * 128-wide block of the reduction at a time; each block's fp32 partial sum is scaled by
+ * the block's weight and activation scales (powers of two) and added in fp32.  H, I and
+ * I_shared must be multiples of 128 and at most 16384 (else MOE_ERR_UNSUPPORTED_SHAPE).
+ * Same workspace as moe_layer_forward. */
 int moe_layer_forward_fp8(const moe_shape_t *shape, const moe_weights_fp8_t *weights,
                           const moe_routing_t *routing, const void *X, float *Y,
                           int32_t *topk_idx, float *topk_w, int32_t *counts,

@@ -37,7 +37,9 @@ def test_weight_quantisation_is_bit_exact():
     torch.cuda.synchronize()
     q_ref, k_ref = ofp8.quantize_weight(synth.bf16_bits_to_f32(Wb).astype(np.float64))
     assert np.array_equal(S.cpu().numpy().astype(np.int64), k_ref)
-    np.testing.assert_array_equal(_e4m3_bytes_to_values(Wq), q_ref)
+    # the bytes are stored transposed ([G, C, R]: K-major rows for the FP8 tensor-core MMA)
+    assert tuple(Wq.shape) == (3, 384, 256)
+    np.testing.assert_array_equal(_e4m3_bytes_to_values(Wq), np.swapaxes(q_ref, -1, -2))
 
 
 @pytest.mark.parametrize("rows,n", [(1, 128), (37, 512), (300, 7168)])
