@@ -87,6 +87,7 @@ constexpr int PH_UP = 0, PH_DOWN = 1;
 constexpr int TQ = 4;                     // depth of the ring that hands claimed tiles to the roles
 constexpr int NT_BLOCK = 8;               // token tiles per block of a group's tile order
 constexpr int MAX_STAGES = 8;       // deeper rings measured slower at decode (HBM-bound up projection)
+constexpr int MAX_STAGES_FP8 = 8;   // FP8 (10 measured the same at decode)
 
 struct ProbDev {
     const int32_t *offsets;  // [n_groups + 1] on the device, or nullptr (one dense group)
@@ -1086,7 +1087,7 @@ size_t ffn_smem_bytes(int bn_cta, int stages, int tab, bool fp8)
 int pick_stages(int bn_cta, int tab, bool fp8)
 {
     const size_t cap = 232448;   // max dynamic shared memory per block on sm_100/sm_103
-    int s = MAX_STAGES;
+    int s = fp8 ? MAX_STAGES_FP8 : MAX_STAGES;
     while (s > 2 && ffn_smem_bytes(bn_cta, s, tab, fp8) > cap) --s;
     return s;
 }
