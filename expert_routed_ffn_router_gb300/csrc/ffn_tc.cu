@@ -52,7 +52,10 @@
 // weight scale and token scale into accumulators held in registers ("promotion" per K
 // block, taken in batches of partials); at the end of the tile it applies SwiGLU (up) or
 // stores (down) as the bf16 kernel does.  Single-CTA tiles of at most 64 token rows
-// (larger groups take several token tiles).
+// (larger groups take several token tiles).  FP8 tiles are 256 weight rows, as two MMAs of
+// M = 128 into two TMEM regions: an up tile covers 128 columns of I (its W1 rows in region
+// 0, its W3 rows in region 1, so each epilogue thread holds both G and U of its column),
+// a down tile 256 rows of H -- twice the weight bytes of a stage.
 //
 // Every wait is bounded (globaltimer): when one runs out the kernel records
 // MOE_ERR_DEVICE_TIMEOUT in the status word, the other roles leave their loops, copies and
@@ -74,8 +77,8 @@ constexpr int HALF_A = A_BYTES / 2;
 constexpr int NUM_THREADS = 192;          // producer, MMA, 4 epilogue warps
 constexpr int NUM_THREADS_FP8 = 224;      // FP8: + the scale producer warp
 constexpr int BK8 = 128;                  // FP8: K per stage = one 128-byte row of E4M3
-constexpr int A8_BYTES = BM * BK8;        // FP8: 16 KB, two 64-row boxes of E4M3 weights
-constexpr int BN8_MAX = 64;               // FP8: token rows per tile (register accumulators)
+constexpr int A8_BYTES = BM * BK8;        // FP8: 16 KB, one 128-row region (two 64-row boxes)
+constexpr int BN8_MAX = 32;               // FP8: token rows per tile (register accumulators)
 constexpr int NPB_MAX = 8;                // FP8: TMEM partial buffers (512 columns at 64 rows)
 constexpr int SR = 32;                    // FP8: slots of the scale ring (one per K block)
 constexpr int TSC = 128;                  // FP8: scale-table entries per box (H, I <= 16384)
@@ -179,11 +182,12 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
     const int bn = p.bn, S = p.stages, tab = p.tab;
-    // FP8: partial buffers in TMEM (every K block's MMAs go to the next one)
-    const uint32_t npb = FP8 ? static_cast<uint32_t>(p.tmem_cols / bn) : 2u;
+    // FP8: partial buffers in TMEM (every K block's MMAs go to the next one), each two
+    // regions of bn columns
+    const uint32_t npb = FP8 ? static_cast<uint32_t>(p.tmem_cols / (2 * bn)) : 2u;
     const int bn_cta = PAIR ? bn / 2 : bn;    // token rows of B staged in this CTA
     // stage: weight tile (SW128) | token rows (SW128)
-    const int b_off = FP8 ? A8_BYTES : A_BYTES;               // token rows within a stage
+    const int b_off = FP8 ? 2 * A8_BYTES : A_BYTES;           // token rows within a stage
     const int stage_bytes = b_off + bn_cta * 128;
     unsigned char *stage_base = smem;
     // FP8 scale ring: per slot the token rows' scales of one K block (bn + 4 fp32, the copy
@@ -192,7 +196,7 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     const int sl_bytes = FP8 ? ((sl_ints + 8 + 127) & ~127) : 0;
     unsigned char *sring = smem + static_cast<size_t>(S) * stage_bytes;
     float *xbuf = reinterpret_cast<float *>(sring + static_cast<size_t>(FP8 ? SR : 0) * sl_bytes);
-    uint64_t *full = reinterpret_cast<uint64_t *>(xbuf + XCHG_FLOATS);
+    uint64_t *full = reinterpret_cast<uint64_t *>(xbuf + (FP8 ? 0 : XCHG_FLOATS));   // (FP8: no exchange)
     uint64_t *empty = full + S;
     // accumulator handoff MMA -> epilogue: bf16 two per-tile buffers, FP8 npb per-K-block
     // partials
@@ -523,6 +527,7 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                 // CTA's token rows)
                 const int a0 = up ? mt * 64 : mt * 128;
                 const int a1 = up ? mt * 64 : mt * 128 + 64;
+                const int a8 = up ? mt * 128 : mt * 256;   // FP8: the tile's first weight row
                 const int brow = T.row0 + (PAIR && !leader ? n_mma_of(T) / 2 : 0);
                 const int kblocks = up ? P.kb_up : P.kb_dn;
                 if (!up && p.phase_only != 1) {
@@ -551,10 +556,15 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, tmo)) { ok = false; break; }
                     if (FP8) {
-                        // the two K-major E4M3 weight boxes and the token rows
-                        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(A8_BYTES + bn_cta * 128));
-                        tma_load_3d(a, mA, &full[s], kb * BK8, a0, T.g);
-                        tma_load_3d(a + A8_BYTES / 2, mA2, &full[s], kb * BK8, a1, T.g);
+                        // four K-major E4M3 weight boxes (region 0: rows a8, a8 + 64 of W1 or
+                        // W2; region 1: the same rows of W3, or rows a8 + 128, a8 + 192 of W2)
+                        // and the token rows
+                        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * A8_BYTES + bn_cta * 128));
+                        const int r1 = up ? a8 : a8 + 128;
+                        tma_load_3d(a, mA, &full[s], kb * BK8, a8, T.g);
+                        tma_load_3d(a + A8_BYTES / 2, mA, &full[s], kb * BK8, a8 + 64, T.g);
+                        tma_load_3d(a + A8_BYTES, mA2, &full[s], kb * BK8, r1, T.g);
+                        tma_load_3d(a + 3 * A8_BYTES / 2, mA2, &full[s], kb * BK8, r1 + 64, T.g);
                         tma_load_2d(a + b_off, mB, &full[s], kb * BK8, brow);
                     } else if (!PAIR) {
                         mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(stage_bytes));
@@ -626,11 +636,15 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                     tc_fence_after();
                     const uint64_t ad = adesc0 + soff, bd = bdesc0 + soff;
                     if (FP8) {
-                        const uint32_t d = tmem_base + pb * static_cast<uint32_t>(bn);
-                        tc_mma_f8(d, ad, bd, idesc, 0u);
-                        tc_mma_f8(d, ad + ASTEP, bd + 2, idesc, 1u);
-                        tc_mma_f8(d, ad + 2 * ASTEP, bd + 4, idesc, 1u);
-                        tc_mma_f8(d, ad + 3 * ASTEP, bd + 6, idesc, 1u);
+                        // region 0 (A rows 0..127) and region 1 (A rows 128..255, 16 KB on)
+                        const uint32_t d = tmem_base + pb * 2u * static_cast<uint32_t>(bn);
+                        const uint32_t d1 = d + static_cast<uint32_t>(bn);
+                        constexpr uint64_t AR1 = static_cast<uint64_t>(A8_BYTES) >> 4;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            tc_mma_f8(d, ad + k * ASTEP, bd + 2 * k, idesc, k ? 1u : 0u);
+                            tc_mma_f8(d1, ad + AR1 + k * ASTEP, bd + 2 * k, idesc, k ? 1u : 0u);
+                        }
                         tc_commit(&empty[s]);
                         tc_commit(&tfull[pb]);
                         if (++pb == npb) { pb = 0; pph ^= 1u; }
@@ -680,10 +694,12 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                 if (T.ph < 0) break;
                 const ProbDev &P = p.prob[T.pi];
                 const bool up = T.ph == PH_UP;
-                const int a0 = up ? T.mt * 64 : T.mt * 128, a1 = up ? T.mt * 64 : T.mt * 128 + 64;
-                // the boxes' exponents, one per K block (row stride nc of the [g][K/128][N/128]
-                // table; a box past the last weight column reads zeros: any tile's scale
-                // does, so its index is clamped)
+                // the two regions' first weight rows: up, the tile's 128 columns of W1 and
+                // of W3; down, two 128-row halves of the tile's 256 rows of W2
+                const int a0 = up ? T.mt * 128 : T.mt * 256, a1 = up ? T.mt * 128 : T.mt * 256 + 128;
+                // the regions' exponents, one per K block (row stride nc of the
+                // [g][K/128][N/128] table; a region past the last weight column reads zeros:
+                // any tile's scale does, so its index is clamped)
                 const int nc = (up ? P.I : P.H) / 128, nr = (up ? P.H : P.I) / 128;
                 const int32_t *src[2];
                 for (int box = 0; box < 2; ++box) {
@@ -750,19 +766,20 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                     for (int j = 0; j < 16; ++j) { v[j] = h[j]; v[j + 16] = 0.f; }
                 }
             };
-            float acc[2][CW];   // FP8: the tile's accumulators, at most 64 token columns
+            // FP8: the tile's accumulators, region r (0: W1 / first W2 half, 1: W3 / second
+            // W2 half) x token column j (at most 32)
+            float acc[2][CW];
             if (FP8) {
                 // promotion: every K block's partial times 2^(weight tile exponent) times
                 // the token row's 2^(exponent), added in K-block order.  The partials are
-                // taken in batches of 128 TMEM columns (4 K blocks of 32 rows, 2 of 64, 8
-                // of 16): one round of waits, one barrier and one load latency per batch.
+                // taken in batches of 128 TMEM columns (2 K blocks x 2 regions of 32 rows, or
+                // 4 x 2 of 16): one round of waits, one barrier and one load latency per batch.
 #pragma unroll
-                for (int c = 0; c < 2; ++c)
+                for (int r = 0; r < 2; ++r)
 #pragma unroll
-                    for (int j = 0; j < CW; ++j) acc[c][j] = 0.f;
+                    for (int j = 0; j < CW; ++j) acc[r][j] = 0.f;
                 const int kblocks = T.ph == PH_UP ? P.kb_up : P.kb_dn;
-                const int box = (T.ph == PH_UP && q >= 2) ? 1 : 0;   // U (W3) rows: lanes 64..127
-                const int per_batch = bn == 16 ? 4 : 128 / bn;       // K blocks a batch
+                const int per_batch = bn == 16 ? 4 : 2;              // K blocks a batch
                 const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
                 bool got_all = true;
                 int kb0 = 0;
@@ -783,66 +800,57 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                     if (!epi_all(got)) { got_all = false; break; }
                     tc_fence_after();
                     __syncwarp();
+                    // K block i, region r of the batch: columns (2 i + r) bn on from the first
+                    // partial
                     float v[128];
-                    const uint32_t pb0 = tmem_base + lane_off + epb * static_cast<uint32_t>(bn);
+                    const uint32_t pb0 = tmem_base + lane_off + epb * 2u * static_cast<uint32_t>(bn);
                     if (bn == 16) {
                         uint32_t ad[8];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) ad[i] = pb0 + 16u * static_cast<uint32_t>(i < nb ? i : 0);
+                        for (int l = 0; l < 8; ++l) ad[l] = pb0 + 16u * static_cast<uint32_t>((l >> 1) < nb ? l : 0);
                         tmem_ld16x8(ad, v);
                     } else {
-                        // 32 columns a load: (K block i, chunk c) -> load i * nck + c
-                        const int nck = bn / CW;           // 1 or 2
                         uint32_t ad[4];
 #pragma unroll
-                        for (int l = 0; l < 4; ++l) {
-                            const int i = l / nck, c = l - i * nck;
-                            ad[l] = i < nb ? pb0 + static_cast<uint32_t>(i * bn + CW * c) : pb0;
-                        }
+                        for (int l = 0; l < 4; ++l) ad[l] = pb0 + 32u * static_cast<uint32_t>((l >> 1) < nb ? l : 0);
                         tmem_ld32x4(ad[0], ad[1], ad[2], ad[3], v);
                     }
                     // the scales of K block i sit in scale slot es + i
-                    auto stage_scales = [&](int i, float &sw, const float *&xs) {
+                    auto block_scales = [&](int i, float &sw0, float &sw1, const float *&xs) {
                         uint32_t si = es + static_cast<uint32_t>(i);
                         if (si >= static_cast<uint32_t>(SR)) si -= static_cast<uint32_t>(SR);
                         const unsigned char *sl = sring + static_cast<size_t>(si) * sl_bytes;
-                        sw = pow2f(reinterpret_cast<const int *>(sl + sl_ints)[box]);
+                        const int *ex = reinterpret_cast<const int *>(sl + sl_ints);
+                        sw0 = pow2f(ex[0]);
+                        sw1 = pow2f(ex[1]);
                         xs = reinterpret_cast<const float *>(sl) + (T.row0 & 3);
                     };
                     if (bn == 16) {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            if (i < nb) {
-                                float sw;
-                                const float *xs;
-                                stage_scales(i, sw, xs);
-#pragma unroll
-                                for (int j = 0; j < 16; ++j) acc[0][j] = fmaf(v[16 * i + j], sw * xs[j], acc[0][j]);
-                            }
-                        }
-                    } else if (bn == 32) {
-#pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             if (i < nb) {
-                                float sw;
+                                float sw0, sw1;
                                 const float *xs;
-                                stage_scales(i, sw, xs);
+                                block_scales(i, sw0, sw1, xs);
 #pragma unroll
-                                for (int j = 0; j < CW; ++j) acc[0][j] = fmaf(v[32 * i + j], sw * xs[j], acc[0][j]);
+                                for (int j = 0; j < 16; ++j) {
+                                    acc[0][j] = fmaf(v[32 * i + j], sw0 * xs[j], acc[0][j]);
+                                    acc[1][j] = fmaf(v[32 * i + 16 + j], sw1 * xs[j], acc[1][j]);
+                                }
                             }
                         }
                     } else {
 #pragma unroll
                         for (int i = 0; i < 2; ++i) {
                             if (i < nb) {
-                                float sw;
+                                float sw0, sw1;
                                 const float *xs;
-                                stage_scales(i, sw, xs);
+                                block_scales(i, sw0, sw1, xs);
 #pragma unroll
-                                for (int c = 0; c < 2; ++c)
-#pragma unroll
-                                    for (int j = 0; j < CW; ++j)
-                                        acc[c][j] = fmaf(v[64 * i + 32 * c + j], sw * xs[CW * c + j], acc[c][j]);
+                                for (int j = 0; j < CW; ++j) {
+                                    acc[0][j] = fmaf(v[64 * i + j], sw0 * xs[j], acc[0][j]);
+                                    acc[1][j] = fmaf(v[64 * i + 32 + j], sw1 * xs[j], acc[1][j]);
+                                }
                             }
                         }
                     }
@@ -858,6 +866,35 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                     kb0 += nb;
                 }
                 if (!got_all) break;
+                // output: up, h = silu(G) * U of column i for every token (G and U of the
+                // same column sit in the same thread); down, the thread's two rows of Yp
+                if (T.ph == PH_UP) {
+                    const int i = T.mt * 128 + 32 * q + lane;
+                    if (i < P.I) {
+                        uint16_t *out = static_cast<uint16_t *>(P.h);
+#pragma unroll
+                        for (int j = 0; j < CW; ++j) {
+                            if (j < T.nvalid) {
+                                const float g = acc[0][j];
+                                out[static_cast<size_t>(T.row0 + j) * P.I + i] = f32_to_bf16_rn(g * fast_sigmoid(g) * acc[1][j]);
+                            }
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int col = T.mt * 256 + 128 * r + 32 * q + lane;
+                        if (col >= P.H) continue;
+#pragma unroll
+                        for (int j = 0; j < CW; ++j) {
+                            if (j >= T.nvalid) continue;
+                            const size_t o = static_cast<size_t>(T.row0 + j) * P.H + col;
+                            if (P.out_fp32) static_cast<float *>(P.out)[o] = acc[r][j];
+                            else static_cast<uint16_t *>(P.out)[o] = f32_to_bf16_rn(acc[r][j]);
+                        }
+                    }
+                }
+                continue;   // (FP8 tiles have no per-tile TMEM accumulator to release)
             } else {
                 const bool ok = mbar_wait(&tfull[b], tph, abort_flag, p.status, tmo);
                 if (!epi_all(ok)) break;
@@ -865,14 +902,7 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             }
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * static_cast<uint32_t>(bn);
             // one chunk = CW token columns of this warp's 32 accumulator rows
-            auto load_chunk = [&](int c, float (&v)[CW]) {
-                if (FP8) {
-#pragma unroll
-                    for (int j = 0; j < CW; ++j) v[j] = c ? acc[1][j] : acc[0][j];
-                } else {
-                    tmem_cols(tbase + CW * c, v);
-                }
-            };
+            auto load_chunk = [&](int c, float (&v)[CW]) { tmem_cols(tbase + CW * c, v); };
             if (T.ph == PH_UP) {
                 // G (W1 rows) sits in lanes 0..63 (quarters 0, 1), U (W3 rows) in lanes
                 // 64..127 (quarters 2, 3): the G warps hand their values over through shared
@@ -1077,9 +1107,9 @@ int pick_bn(int avg_rows)
 
 size_t ffn_smem_bytes(int bn_cta, int stages, int tab, bool fp8)
 {
-    const size_t stage = static_cast<size_t>(fp8 ? A8_BYTES : A_BYTES) + bn_cta * 128;
+    const size_t stage = static_cast<size_t>(fp8 ? 2 * A8_BYTES : A_BYTES) + bn_cta * 128;
     const size_t slot = ((((bn_cta + 4) * 4 + 15) & ~static_cast<size_t>(15)) + 8 + 127) & ~static_cast<size_t>(127);
-    return 1024 + stages * stage + (fp8 ? SR * slot : 0) + XCHG_FLOATS * 4 +
+    return 1024 + stages * stage + (fp8 ? SR * slot : XCHG_FLOATS * 4) +
            (2 * stages + 2 * NPB_MAX + 1 + 2 * TQ) * 8 + (fp8 ? 2 * SR * 8 : 0) + 16 +
            (6 * static_cast<size_t>(tab) + 8 * TQ) * 4;
 }
@@ -1137,9 +1167,10 @@ cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I
     const int tab = (n_cg + 1 + 3) & ~3;
     const int stages = pick_stages(bn_cta, tab, fp8);
     const size_t smem = ffn_smem_bytes(bn_cta, stages, tab, fp8);
-    // TMEM columns: two accumulators of bn columns; FP8: NPB_MAX partials of bn (at most 512)
+    // TMEM columns: two accumulators of bn columns; FP8: NPB_MAX partials of two regions
+    // of bn columns (at most 512)
     int tcols = 32;
-    while (tcols < (fp8 ? NPB_MAX : 2) * bn && tcols < 512) tcols <<= 1;
+    while (tcols < (fp8 ? 2 * NPB_MAX : 2) * bn && tcols < 512) tcols <<= 1;
     const int m_up = pair ? 128 : 64;      // weight columns of one tile
     const int m_dn = pair ? 256 : 128;
 
@@ -1169,8 +1200,9 @@ cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I
         d.offsets = P.offsets;
         d.n_groups = P.n_groups;
         d.dense_rows = P.dense_rows;
-        d.mt_up = (I + m_up - 1) / m_up;
-        d.mt_dn = (H + m_dn - 1) / m_dn;
+        // FP8 tiles: 128 columns of I (up), 256 rows of H (down)
+        d.mt_up = fp8 ? (I + 127) / 128 : (I + m_up - 1) / m_up;
+        d.mt_dn = fp8 ? (H + 255) / 256 : (H + m_dn - 1) / m_dn;
         d.kb_up = H / (fp8 ? BK8 : BK);
         d.kb_dn = I / (fp8 ? BK8 : BK);
         d.I = I;
