@@ -253,6 +253,9 @@ def _layer_for(w, routing, weights, dev, opts, fp8, weights8=None):
     wts["W_gate"] = torch.from_numpy(routing["W_gate"].view(np.int16)).view(torch.bfloat16).to(dev)
     wts["bias"] = torch.from_numpy(routing["bias"]).to(dev)
     X_host = torch.from_numpy(routing["X"].view(np.int16)).view(torch.bfloat16)
+    if weights8 is not None:
+        # pre-quantised experts: this workload's gate rows and bias (the router is bf16)
+        weights8 = {**weights8, "W_gate": wts["W_gate"], "bias": wts["bias"]}
     layer = B.MoELayer(wts, w.T, w.K, with_affinity=True, routing=opts, fp8=fp8,
                        weights8=weights8)
     return layer, wts, X_host, X_host.to(dev)
@@ -345,14 +348,17 @@ def target_of(w):
     return None, None
 
 
-def measure_side_workload(name, weights, dev, args, sampler, peaks, peak_src, barrier):
-    """One row of the workloads table: the same call as the headline on another batch."""
+def measure_side_workload(name, weights, dev, args, sampler, peaks, peak_src, barrier,
+                          weights8=None):
+    """One row of the workloads table: the same call as the headline on another batch (with
+    weights8, the FP8 layer on those pre-quantised experts)."""
     import torch
 
     from expert_routed_ffn_router_gb300 import synth
+    fp8 = weights8 is not None
     w = synth.workload(name)
     routing = synth.routing_inputs(w)
-    layer, _, _, X = _layer_for(w, routing, weights, dev, None, False)
+    layer, _, _, X = _layer_for(w, routing, weights, dev, None, fp8, weights8)
     stream = torch.cuda.current_stream()
     t_busy0 = time.time()
     for _ in range(args.warmup):
@@ -367,14 +373,17 @@ def measure_side_workload(name, weights, dev, args, sampler, peaks, peak_src, ba
         raise RuntimeError(f"device status word reported an error ({name})")
     counts = layer.counts.cpu().numpy()
     n_act = int((counts > 0).sum())
-    lr = layer_roofline(w, n_act, ms, peaks)
-    key, tgt = target_of(w)
+    lr = layer_roofline(w, n_act, ms, peaks, fp8)
+    key, tgt = target_of(w) if not fp8 else (None, None)
     row = {"T": w.T, "ms_per_step": round(ms, 4), "tokens_per_s": round(w.T / (ms / 1e3), 1),
            "n_active_experts": n_act, **lr,
-           "dominant_kernel": dominant_roofline(w, n_act, stage_ms, peaks, peak_src, False, name),
+           "dominant_kernel": dominant_roofline(w, n_act, stage_ms, peaks, peak_src, fp8, name),
            "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
-           "gpu_launches": args.steps * launches_per_step(w, with_affinity=True),
+           "gpu_launches": args.steps * launches_per_step(w, with_affinity=True, fp8=fp8),
            "clocks": sampler.summary(t0, t1, t_busy0, t_busy1)}
+    if fp8:
+        row["precision"] = ("FP8 E4M3 experts, 128 x 128 weight / 1 x 128 activation block "
+                            "scales, on the FP8 tensor cores")
     if key:
         row["target"] = {"metric": key, "min": tgt, "met": bool(lr[key] >= tgt)}
     del layer
@@ -531,6 +540,14 @@ def run_ours(args, rank, world, local_rank):
         rows["decode"] = {"T": w.T, "ms_per_step": round(ms, 4),
                           "tokens_per_s": round(value, 1), "n_active_experts": n_act, **lr,
                           "note": "the headline above"}
+        # the same decode step with FP8 experts (the pages' serving precision; the experts
+        # quantised once, outside every timed region)
+        weights8 = B.quantize_expert_weights_fp8({**weights, "W_gate": None, "bias": None})
+        torch.cuda.synchronize()
+        rows["decode_fp8"] = measure_side_workload("decode", weights, dev, args, sampler, peaks,
+                                                   peak_src, barrier, weights8=weights8)
+        del weights8
+        torch.cuda.empty_cache()
         out["workloads"] = rows
         out["targets"] = {n: r["target"] for n, r in rows.items() if "target" in r}
     sampler.stop()

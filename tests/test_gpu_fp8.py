@@ -148,6 +148,14 @@ def test_fp8_layer_dsv3_two_tokens():
     check_layer_fp8(Problem(w, host_weights=False))
 
 
+def test_fp8_layer_dsv3_decode():
+    # DeepSeek-V3 decode step (128 tokens, 32-row FP8 token tiles, 256-row weight tiles):
+    # routing, counts and affinity bit-exact over every token; Y on four tokens spread over
+    # the batch (the oracle quantises each of their ~30 experts' weights in numpy)
+    w = synth.workload("decode")
+    check_layer_fp8(Problem(w, host_weights=False), tokens=[0, 37, 77, 127])
+
+
 def test_fp8_rejects_shapes_off_the_128_grid():
     w = synth.Workload("f8bad", T=8, H=192, E=8, K=2, I=128, Is=0, seed=1, x_seed=2)
     p = Problem(w)
