@@ -204,13 +204,13 @@ def launches_per_step(w, with_affinity: bool, fp8: bool = False) -> int:
     masks, scan, scatter and one launch for the affinity, the gather and the zeroing), the
     FFN (up and down projections in one persistent launch), combine.  On
     bf16 weights up to 128 tokens the shared expert is a second FFN launch, on a side
-    stream beside the router and the dispatch.  FP8 experts add the token-row
-    quantisation, split the FFN into its up and down launches and quantise h (and the
-    shared expert's h) between them."""
+    stream beside the router and the dispatch.  FP8 experts quantise the permuted rows (and
+    the token rows for the shared expert), split the FFN into its up and down launches and
+    quantise h (and the shared expert's h) between them."""
     T = w.T
     router = 2 if (16 <= T <= 2048 or T > 4096) else 1
     dispatch = 1 if T <= 256 else 4
-    ffn = 1 if not fp8 else 1 + 2 + (2 if w.Is else 1)
+    ffn = 1 if not fp8 else 2 + (4 if w.Is else 2)
     side = 1 if shared_on_side(w, fp8) else 0
     return router + dispatch + ffn + side + 1
 

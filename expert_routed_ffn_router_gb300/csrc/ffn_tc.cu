@@ -51,7 +51,7 @@
 // to eight partials in flight), and the epilogue adds each partial times the block's
 // weight scale and token scale into accumulators held in registers ("promotion" per K
 // block, taken in batches of partials); at the end of the tile it applies SwiGLU (up) or
-// stores (down) as the bf16 kernel does.  Single-CTA tiles of at most 64 token rows
+// stores (down) as the bf16 kernel does.  Single-CTA tiles of at most 32 token rows
 // (larger groups take several token tiles).  FP8 tiles are 256 weight rows, as two MMAs of
 // M = 128 into two TMEM regions: an up tile covers 128 columns of I (its W1 rows in region
 // 0, its W3 rows in region 1, so each epilogue thread holds both G and U of its column),
@@ -79,7 +79,7 @@ constexpr int NUM_THREADS_FP8 = 224;      // FP8: + the scale producer warp
 constexpr int BK8 = 128;                  // FP8: K per stage = one 128-byte row of E4M3
 constexpr int A8_BYTES = BM * BK8;        // FP8: 16 KB, one 128-row region (two 64-row boxes)
 constexpr int BN8_MAX = 32;               // FP8: token rows per tile (register accumulators)
-constexpr int NPB_MAX = 8;                // FP8: TMEM partial buffers (512 columns at 64 rows)
+constexpr int NPB_MAX = 8;                // FP8: TMEM partial buffers (2 regions x 32 columns each)
 constexpr int SR = 32;                    // FP8: slots of the scale ring (one per K block)
 constexpr int TSC = 128;                  // FP8: scale-table entries per box (H, I <= 16384)
 constexpr int MAX_GROUPS = 1024;          // groups of one problem

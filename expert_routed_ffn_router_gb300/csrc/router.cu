@@ -27,17 +27,20 @@
 // are disjoint from every other candidate's).
 //
 // Structure.  A grid (expert tiles, token tiles, K splits) of CTAs (256 threads; 384 for
-// large batches) computes fp32 logit tiles on the CUDA cores into the workspace:
-//   tiny batches (T <= 8):     four warps per expert, all tokens at once;
-//   small batches (T <= 4096): 16 tokens x 256 experts per CTA, 4x4 per thread;
-//   large batches:             128 tokens x 128 experts per CTA, 8x8 per thread on eight
-//                              compute warps, fed through a 4-stage fp32 ring by four
-//                              producer warps (cp.async staging, bf16 -> fp32, norms).
-// Batches of up to 15 tokens and of 2049 to 4096 tokens: the last CTA of a token tile
-// (completion counter) sums the split-K partials in a fixed order, scores, selects and
-// writes the outputs -- one launch.  From 16 to 2048 tokens and for large batches a second
-// launch finalises, one warp per token, so the selection is spread over the whole GPU
-// instead of one CTA per token tile.
+// the warp-specialised tiles) computes fp32 logit tiles on the CUDA cores:
+//   tiny batches (T <= 8):       four warps per expert, all tokens at once;
+//   9 to 15 and 2049 to 4096:    16 tokens x 256 experts per CTA, 4x4 per thread;
+//   16 to 2048 tokens:           16 tokens x 256 experts per CTA, 4x4 per thread on eight
+//                                compute warps, fed through a 4-stage fp32 ring by four
+//                                producer warps (cp.async staging, bf16 -> fp32, norms);
+//   large batches (T > 4096):    128 tokens x 128 experts per CTA, 8x8 per thread, the
+//                                same warp-specialised structure.
+// Up to 15 tokens and from 2049 to 4096 tokens the last CTA of a token tile (completion
+// counter) sums the split-K partials in a fixed order, scores, selects and writes the
+// outputs -- one launch.  From 16 to 2048 tokens and for large batches a second launch
+// finalises 1 to 8 tokens a CTA (split-K sum, scoring and certified top-K, then the
+// CTA-wide re-score of the uncertified candidates), so the selection is spread over the
+// whole GPU instead of one CTA per token tile.
 #include <cfloat>
 #include <climits>
 
@@ -1773,8 +1776,9 @@ __global__ void __launch_bounds__(NT_WS, 1) router_gemm_kernel(const RouterArgs 
     gemm_tile_ws<C>(a, smem);
 }
 
-// Shared-memory layout of the finalise launch: one CTA finalises NW consecutive tokens
-// (one warp each), then re-scores the uncertified candidates of all of them together.
+// Shared-memory layout of the finalise launch: one CTA finalises up to NW consecutive
+// tokens (one warp each for scoring and selection), then re-scores the uncertified
+// candidates of all of them together.
 struct FinCta {
     float *nw, *bias, *L, *bnd, *sc, *nxs;   // [E] x 2, [NW][E] x 3 (logits -> sel), [NW]
     int *ce, *ord;                     // [NW][E] (per-warp fallback), [NW][32]
@@ -2035,8 +2039,8 @@ size_t finalize_smem(int E) { return FinCta::bytes(E) + 16; }
 
 }  // namespace
 
-// Small-tile batches of 16 to 2048 tokens select in the finalise launch (one warp per
-// token over the whole GPU) rather than in the last CTA of each 16-token tile: 71.6 -> 63.1
+// Small-tile batches of 16 to 2048 tokens select in the finalise launch (1 to 8 tokens a
+// CTA over the whole GPU) rather than in the last CTA of each 16-token tile: 71.6 -> 63.1
 // us at 128 tokens, 6 us less from 16 to 2048 tokens; at 4096 the last-CTA selection is
 // ahead (654 vs 662 us).
 constexpr int kSplitMinTokens = 16, kSplitMaxTokens = 2048;

@@ -1,6 +1,8 @@
 """Host-side accounting of bench.py (CPU only): the algorithmic bytes and FLOPs of the FFN
 stage when the shared expert runs in its own launch add up to those of the single launch,
 and the launch count per step follows the library's launch structure."""
+import dataclasses
+
 import bench
 from expert_routed_ffn_router_gb300 import synth
 
@@ -29,10 +31,13 @@ def test_launches_per_step_by_batch_size():
     expect = {2: 5, 8: 5, 16: 6, 128: 6, 200: 5, 512: 8, 3000: 7, 16384: 8}
     for T, n in expect.items():
         assert bench.launches_per_step(synth.workload("decode", T=T), True) == n, T
-    # FP8 experts at 128 tokens: router tile + finalise, dispatch, then token-row
-    # quantisation, up launch, two h quantisations, down launch, and combine
+    # FP8 experts at 128 tokens: router tile + finalise, dispatch, then the quantisation of
+    # the permuted rows and of the token rows, up launch, two h quantisations, down launch,
+    # and combine (ten launches a step in the ncu launch list of FP8 decode)
     w = synth.workload("decode")
-    assert bench.launches_per_step(w, True, fp8=True) == 2 + 1 + 5 + 1
+    assert bench.launches_per_step(w, True, fp8=True) == 2 + 1 + 6 + 1
+    # without a shared expert: no token-row and no shared-h quantisation
+    assert bench.launches_per_step(dataclasses.replace(w, Is=0), True, fp8=True) == 2 + 1 + 4 + 1
 
 
 def test_targets_by_batch_size():
