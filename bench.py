@@ -139,9 +139,10 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------ accounting
-def ffn_traffic(workload: str):
-    """DRAM bytes per step of the FFN launches from the committed ncu record, or None when
-    the record does not cover this workload or the FFN sources changed since it was taken."""
+def ffn_traffic(workload: str, fp8: bool = False):
+    """DRAM bytes per step of the FFN launches from the committed ncu record (bf16 weights:
+    the routed launch; FP8 weights: the up and the down launch), or None when the record
+    does not cover this workload or the FFN sources changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "ffn_traffic.json")
     try:
         with open(path) as f:
@@ -152,7 +153,7 @@ def ffn_traffic(workload: str):
                 h.update(f.read())
         if h.hexdigest() != rec["sources_sha256"]:
             return None
-        return rec["bytes_per_step"].get(workload)
+        return rec["bytes_per_step_fp8" if fp8 else "bytes_per_step"].get(workload)
     except (OSError, KeyError, ValueError):
         return None
 
@@ -241,6 +242,9 @@ def max_over_ranks(x: float, device=None) -> float:
 SIDE_WORKLOADS = ("sweep2", "sweep4", "sweep8", "sweep16", "sweep32", "sweep64", "sweep256",
                   "skewed", "prefill")
 HBM_TARGET = 0.70      # of 8 TB/s, batches of up to 64 tokens
+# dense FP8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s nominal): FP8 contractions are measured
+# against the measured bf16 peak times this ratio
+FP8_OVER_BF16 = 2.0
 TENSOR_TARGET = 0.60   # of the bf16 burst rate, batches of 8192 tokens and more
 
 
@@ -305,20 +309,24 @@ def dominant_roofline(w, n_act, stage_ms, peaks, peak_src, fp8, workload_name):
     b, f, _, _ = algorithmic(w, n_act, 1 if fp8 else 2, shared_on_side(w, fp8))
     dom = max(("ffn", "router", "combine", "dispatch"), key=lambda s: stage_ms[s])
     t_dom = stage_ms[dom] / 1e3
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if f[dom] / max(b[dom], 1) > ridge and dom.startswith("ffn"):
+    tpeak = peaks["bf16_tflops"] * (FP8_OVER_BF16 if fp8 else 1.0)   # the FFN's own dtype
+    ridge = tpeak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    tensor = f[dom] / max(b[dom], 1) > ridge and dom.startswith("ffn")
+    if tensor:
         ach = f[dom] / t_dom / 1e12
-        roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"],
+        roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": round(tpeak, 1),
                 "unit": "TFLOP/s"}
     else:
         ach = b[dom] / t_dom / 1e9
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = ffn_traffic(workload_name) if dom == "ffn" and not fp8 else None
+    roof["traffic"] = ffn_traffic(workload_name, fp8) if dom == "ffn" else None
     roof["kernel"] = dom
     roof["peak_source"] = (f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured"
                            else "fallback")
+    if tensor and fp8:
+        roof["peak_source"] += f": bf16 x {FP8_OVER_BF16:g}, the nominal dense FP8 / bf16 ratio"
     roof["algorithmic_bytes_per_launch"] = int(b[dom])
     roof["algorithmic_flops_per_launch"] = int(f[dom])
     roof["launch_ms"] = round(stage_ms[dom], 4)
@@ -326,16 +334,21 @@ def dominant_roofline(w, n_act, stage_ms, peaks, peak_src, fp8, workload_name):
 
 
 def layer_roofline(w, n_act, ms, peaks, fp8=False):
+    """The whole layer against the measured copy bandwidth, 8 TB/s and the tensor rate of
+    the expert GEMMs' dtype (bf16, or for FP8 experts bf16 x FP8_OVER_BF16; the layer's
+    flops are counted alike whatever units run them)."""
     _, _, layer_bytes, layer_flops = algorithmic(w, n_act, 1 if fp8 else 2, shared_on_side(w, fp8))
     sec = ms / 1e3
+    k = FP8_OVER_BF16 if fp8 else 1.0
     return {"algorithmic_bytes": int(layer_bytes), "algorithmic_flops": int(layer_flops),
             "hbm_gbs": round(layer_bytes / sec / 1e9, 1),
             "hbm_frac": round(layer_bytes / sec / 1e9 / peaks["hbm_gbs"], 4),
             "hbm_frac_of_8TBs": round(layer_bytes / sec / 8e12, 4),
             "tensor_tflops": round(layer_flops / sec / 1e12, 2),
-            "tensor_frac": round(layer_flops / sec / 1e12 / peaks["bf16_tflops"], 4),
+            "tensor_frac": round(layer_flops / sec / 1e12 / (k * peaks["bf16_tflops"]), 4),
             "tensor_frac_sustained": round(layer_flops / sec / 1e12 /
-                                           peaks["bf16_tflops_sustained"], 4)}
+                                           (k * peaks["bf16_tflops_sustained"]), 4),
+            "tensor_dtype": "fp8" if fp8 else "bf16"}
 
 
 def target_of(w):

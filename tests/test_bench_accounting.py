@@ -58,6 +58,22 @@ def test_layer_roofline_fractions():
     assert abs(r["hbm_frac_of_8TBs"] - 1.0) < 1e-3
     assert abs(r["hbm_frac"] - 8000.0 / 6000.0) < 1e-3
     assert abs(r["tensor_frac"] * 2000.0 - r["tensor_frac_sustained"] * 1600.0) < 1e-3 * 2000
+    # FP8 experts: the same step measured against the FP8 rate (bf16 x the nominal ratio)
+    r8 = bench.layer_roofline(w, n_act, ms, peaks, fp8=True)
+    assert r8["tensor_dtype"] == "fp8"
+    assert abs(r8["tensor_frac"] * bench.FP8_OVER_BF16 - r["tensor_frac"]) <= 2e-4
+
+
+def test_fp8_dominant_kernel_takes_the_fp8_peak():
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0}
+    w = synth.workload("prefill")
+    stage_ms = {"router": 1.0, "dispatch": 0.5, "ffn_up": 10.0, "ffn_down": 0.0, "combine": 0.4,
+                "ffn": 10.0}
+    r16 = bench.dominant_roofline(w, w.E, stage_ms, peaks, "measured", False, "prefill")
+    r8 = bench.dominant_roofline(w, w.E, stage_ms, peaks, "measured", True, "prefill")
+    assert r16["bound"] == r8["bound"] == "tensor"
+    assert r16["peak"] == 2000.0 and r8["peak"] == 2000.0 * bench.FP8_OVER_BF16
+    assert "ratio" in r8["peak_source"] and "ratio" not in r16["peak_source"]
 
 
 def test_every_side_workload_exists_and_shares_the_weights():

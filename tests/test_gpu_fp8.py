@@ -11,7 +11,7 @@ from oracle import fp8 as ofp8
 from expert_routed_ffn_router_gb300 import binding as B
 from expert_routed_ffn_router_gb300 import synth
 
-from gpu_common import (DEV, W_MAX_ABS, Y_MAX_ABS, Y_REL_FROB, Problem, bits,
+from gpu_common import (DEV, W_MAX_ABS, Y_MAX_ABS, Y_REL_FROB, Problem, bits, check_dispatch,
                         host_to_device_bf16, rel_frob)
 
 pytestmark = pytest.mark.gpu
@@ -89,6 +89,7 @@ def check_layer_fp8(p: Problem, tokens=None):
     d = oracle.dispatch(idx_o, p.w.E)
     assert np.array_equal(layer.counts.cpu().numpy(), d["counts"])
     assert np.array_equal(layer.affinity.cpu().numpy(), d["affinity"])
+    check_dispatch(layer, p.X, d)     # offsets, perm, slot_pos and Xp = X[perm], bit-exact
     tokens = np.arange(p.w.T) if tokens is None else np.asarray(tokens)
     Y_o = _oracle_Y_fp8(p, idx_o, w_o, tokens)
     Y_g = layer.Y.cpu().numpy()[tokens].astype(np.float64)
