@@ -60,8 +60,11 @@ int g_shared_side = -1;   // shared expert on the side stream: -1 by batch size,
 
 // Up to this many tokens the router and the dispatch leave most of the GPU idle (their
 // kernels wait on latency, not on SMs or HBM): the shared expert, which needs no routing,
-// then runs beside them on half of the SMs.
+// then runs beside them on a quarter of the SMs.  (The routed experts' launch takes the
+// other SMs as soon as the dispatch is done; a quarter measured best of 1/8 .. 1: T=2
+// 0.2458 ms with half of the SMs -> 0.2431 ms, T=64 1.618 -> 1.610, T=128 1.862 -> 1.855.)
 constexpr int kSideMaxTokens = 128;
+int side_ctas() { return num_sms() / 4 > 0 ? num_sms() / 4 : 1; }
 
 // A stream of the library for the shared expert, forked from and joined back into the
 // caller's stream with two events (capturable: the side stream joins a capture through the
@@ -361,7 +364,7 @@ int layer_forward(const moe_shape_t *shape, const moe_weights_t *wt, const moe_w
             cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess)
             return MOE_ERR_CUDA;
         if (launch_ffn(&P[1], 1, s.H, &Ipp[1], s.T, L.ready_sh, false, status, side->s,
-                       g_wait_limit_ns, g_inject_stall, nullptr, -1, num_sms() / 2) != cudaSuccess ||
+                       g_wait_limit_ns, g_inject_stall, nullptr, -1, side_ctas()) != cudaSuccess ||
             cudaEventRecord(side->join, side->s) != cudaSuccess)
             return MOE_ERR_CUDA;
         n_probs = 1;

@@ -156,7 +156,7 @@ void moe_debug_set_ffn_variant(int variant);
 
 /* Testing hook: where later moe_layer_forward calls on bf16 weights run the shared expert.
  * -1 (the default) chooses by batch size: up to 128 tokens it runs as its own FFN launch on
- * half of the SMs, on a side stream of the library forked from the caller's stream before
+ * a quarter of the SMs, on a side stream of the library forked from the caller's stream before
  * the router and joined back before the combine, so that it overlaps the router and the
  * dispatch; larger batches run it in the routed experts' launch.  0 always takes the
  * routed experts' launch, 1 always the side stream.  Same results either way; other
