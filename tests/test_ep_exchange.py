@@ -94,6 +94,51 @@ def test_exchange_matches_the_single_gpu_dispatch_gloo_world2(owner_kind):
     assert sorted(seen) == list(range(E))         # every expert has exactly one owner
 
 
+def _grace_worker(rank, world, port, group_of, out):
+    import torch.distributed as dist
+
+    from expert_routed_ffn_router_gb300 import ep
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        idx = _routing(rank)
+        d = oracle.dispatch(idx, E, want_affinity=False)
+        gtok = torch.from_numpy(d["perm"].astype(np.float64) + rank * T_LOCAL)
+        plan = ep.plan_exchange(torch.from_numpy(d["offsets"]), ep.grouping_owner(group_of, world))
+        rows = ep.dispatch_rows(gtok[:, None], plan)
+        back = ep.combine_rows(rows * 2.0, plan, int(d["offsets"][-1]))
+        out[rank] = dict(mine=plan.mine.tolist(), local_offsets=plan.local_offsets.numpy(),
+                         rows=rows[:, 0].numpy(), gtok=gtok.numpy(), back=back[:, 0].numpy())
+    finally:
+        dist.destroy_process_group()
+
+
+def test_exchange_over_a_grace_grouping_gloo_world3():
+    """Three ranks own the groups of a GRACE-MoE placement computed by the library's planner
+    from the co-activation matrix of all ranks' routing (GRACE notes, Core Idea 1: group d
+    on GPU d): every rank receives exactly its experts' rows of the single-GPU dispatch,
+    and every row comes back to its source."""
+    from expert_routed_ffn_router_gb300 import binding as B
+    world = 3
+    idx_all = np.concatenate([_routing(r) for r in range(world)])
+    g = oracle.dispatch(idx_all, E)
+    group_of = B.moe_grace_group(g["affinity"], world, 0.5)
+    assert sorted(set(group_of.tolist())) == list(range(world))
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_grace_worker, args=(world, port, group_of.tolist(), out), nprocs=world, join=True)
+        res = dict(out)
+    for r in range(world):
+        R = res[r]
+        assert R["mine"] == [e for e in range(E) if group_of[e] == r]
+        for j, e in enumerate(R["mine"]):
+            a, b = R["local_offsets"][j], R["local_offsets"][j + 1]
+            np.testing.assert_array_equal(R["rows"][a:b], g["perm"][g["offsets"][e]:g["offsets"][e + 1]])
+        np.testing.assert_array_equal(R["back"], 2.0 * R["gtok"])
+
+
 def test_owner_helpers():
     from expert_routed_ffn_router_gb300 import ep
     assert ep.contiguous_owner(8, 4).tolist() == [0, 0, 1, 1, 2, 2, 3, 3]
