@@ -2044,13 +2044,18 @@ size_t finalize_smem(int E) { return FinCta::bytes(E) + 16; }
 // us at 128 tokens, 6 us less from 16 to 2048 tokens; at 4096 the last-CTA selection is
 // ahead (654 vs 662 us).
 constexpr int kSplitMinTokens = 16, kSplitMaxTokens = 2048;
+constexpr size_t kMaxSmemPerCta = 232448;   // dynamic shared memory a CTA may opt in to
 
 RouterPlan router_plan(int T, int H, int E)
 {
     RouterPlan p{};
     const bool small = T <= 4096;
+    // the one-launch paths finalise in one CTA whose shared memory holds E-wide arrays per
+    // warp: past what a CTA may hold (E above ~800) the batch takes the tile GEMM and the
+    // finalise launch instead
+    const bool fused_ok = fused_smem(SmallCfg::TT, SmallCfg::TE, E, 1024) <= kMaxSmemPerCta;
     p.gemv = 0;                                  // token batch of the tiny-batch path
-    if (T <= GEMV_TMAX)
+    if (T <= GEMV_TMAX && fused_ok)
         for (p.gemv = 1; p.gemv < T; p.gemv <<= 1) {}
     p.TT = small ? SmallCfg::TT : LargeCfg::TT;
     p.TE = p.gemv ? GEMV_EPC : (small ? SmallCfg::TE : LargeCfg::TE);
@@ -2058,7 +2063,8 @@ RouterPlan router_plan(int T, int H, int E)
     p.nET = (E + p.TE - 1) / p.TE;
     p.S = H / KST;
     const int base = p.nTT * p.nET;
-    const bool split = !p.gemv && small && T >= kSplitMinTokens && T <= kSplitMaxTokens;
+    const bool split = !p.gemv && small &&
+                       ((T >= kSplitMinTokens && T <= kSplitMaxTokens) || !fused_ok);
     // resident CTAs per SM: 2 for the two-stage small tile, 1 for the warp-specialised ones
     const int target = (small && !split ? 2 : 1) * num_sms();
     if (p.gemv) {

@@ -37,6 +37,12 @@ def test_tiny_layer():
     (513, 256, 8, 6, 128, 128),     # 385 rows per expert: 256-row token tiles
     (700, 192, 16, 4, 192, 64),     # 256-row tiles, odd weight-tile counts (3 up, 2 down)
     (128, 128, 16, 2, 128, 0),      # 16 rows per expert: 128-row token tiles
+    (50, 128, 8, 1, 64, 64),        # top-1 routing
+    (20, 64, 1, 1, 64, 0),          # a single expert (E = K = 1), H = I = 64
+    (5, 128, 1024, 8, 64, 0),       # the largest E: a batch the one-launch router would
+                                    # take, whose finalising CTA cannot hold 1024 experts
+    (40, 128, 1024, 4, 64, 64),     # the largest E on the tile + finalise path
+    (2100, 64, 1024, 2, 64, 0),     # the largest E at a size of the one-launch 16-token tile
 ])
 def test_ragged_shapes(T, H, E, K, I, Is):
     w = synth.Workload("rag", T=T, H=H, E=E, K=K, I=I, Is=Is, seed=T, x_seed=T + 1)
