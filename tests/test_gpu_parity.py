@@ -43,6 +43,8 @@ def test_tiny_layer():
                                     # take, whose finalising CTA cannot hold 1024 experts
     (40, 128, 1024, 4, 64, 64),     # the largest E on the tile + finalise path
     (2100, 64, 1024, 2, 64, 0),     # the largest E at a size of the one-launch 16-token tile
+    (100, 128, 64, 32, 64, 0),      # the largest K
+    (30, 128, 48, 32, 64, 64),      # the largest K, E not a multiple of 32
 ])
 def test_ragged_shapes(T, H, E, K, I, Is):
     w = synth.Workload("rag", T=T, H=H, E=E, K=K, I=I, Is=Is, seed=T, x_seed=T + 1)
