@@ -361,6 +361,44 @@ def target_of(w):
     return None, None
 
 
+def measure_tiny(dev, steps: int, flush_bytes: int = 512 << 20) -> dict:
+    """The tiny configuration (T=16, H=256, E=16, top-2, I=Is=128; 3.3 MB of expert
+    weights): microseconds a layer call, warm (weights and activations left in L2 by the
+    previous call) and cold (L2 flushed before every call by writing a buffer larger than
+    it, the call alone timed with events around it)."""
+    import torch
+
+    from expert_routed_ffn_router_gb300 import binding as B
+    from expert_routed_ffn_router_gb300 import synth
+    w = synth.workload("tiny")
+    routing = synth.routing_inputs(w)
+    weights = {k: (None if v is None else torch.from_numpy(v.view("int16")).view(torch.bfloat16).to(dev))
+               for k, v in synth.expert_weights_host(w).items()}
+    layer, _, _, X = _layer_for(w, routing, weights, dev, None, False)
+    stream = torch.cuda.current_stream()
+    for _ in range(10):
+        layer.forward(X)
+    torch.cuda.synchronize()
+    ms_warm, _, _ = _timed(layer, X, steps, stream, lambda: None)
+    flush = torch.empty(flush_bytes, dtype=torch.uint8, device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for e0, e1 in ev:
+        flush.fill_(1)                       # evicts the layer's data from the 129 MB L2
+        e0.record(stream)
+        layer.forward(X)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms_cold = sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+    if layer.status() != 0:
+        raise RuntimeError("device status word reported an error (tiny)")
+    return {"T": w.T, "shape": {"H": w.H, "E": w.E, "K": w.K, "I": w.I, "I_shared": w.Is},
+            "us_per_call_warm": round(ms_warm * 1e3, 2),
+            "us_per_call_cold_l2": round(ms_cold * 1e3, 2),
+            "l2": f"cold: a {flush_bytes >> 20} MB buffer written before every call",
+            "gpu_launches_per_call": launches_per_step(w, with_affinity=True)}
+
+
 def measure_side_workload(name, weights, dev, args, sampler, peaks, peak_src, barrier,
                           weights8=None):
     """One row of the workloads table: the same call as the headline on another batch (with
@@ -561,6 +599,7 @@ def run_ours(args, rank, world, local_rank):
                                                    peak_src, barrier, weights8=weights8)
         del weights8
         torch.cuda.empty_cache()
+        rows["tiny"] = measure_tiny(dev, args.steps)
         out["workloads"] = rows
         out["targets"] = {n: r["target"] for n, r in rows.items() if "target" in r}
     sampler.stop()
