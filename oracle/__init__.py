@@ -6,4 +6,4 @@ import this package.  It shares no code with the CUDA library in
 """
 from .oracle import (build_oracle, combine, dispatch, expert_rows, forward, layer_tokens,  # noqa: F401
                      layer_tokens_by_expert,
-                     num_threads, router, router_ex)
+                     num_threads, router, router_ex, set_num_threads)

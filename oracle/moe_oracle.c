@@ -370,3 +370,17 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/* Threads for the calling thread's later oracle calls (n >= 1); returns the previous
+ * count.  For timing the oracle on one core beside all of them. */
+int oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    const int prev = omp_get_max_threads();
+    if (n >= 1) omp_set_num_threads(n);
+    return prev;
+#else
+    (void)n;
+    return 1;
+#endif
+}

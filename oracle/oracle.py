@@ -62,6 +62,8 @@ def _load():
         lib.oracle_combine.restype = i
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i
+        lib.oracle_set_num_threads.argtypes = [i]
+        lib.oracle_set_num_threads.restype = i
         _lib = lib
     return _lib
 
@@ -79,6 +81,11 @@ def _u16(a) -> np.ndarray:
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> int:
+    """Threads for this thread's later oracle calls; returns the previous count."""
+    return int(_load().oracle_set_num_threads(int(n)))
 
 
 def router(X: np.ndarray, W_gate: np.ndarray, bias: np.ndarray, K: int,

@@ -91,3 +91,19 @@ def test_gpus_flag_must_match_world_size(monkeypatch):
     with pytest.raises(SystemExit) as e:
         bench.main()
     assert e.value.code not in (0, None)
+
+
+def test_cpu_baseline_reports_all_cores_and_one_core():
+    # the oracle timed on the tiny workload's CPU-resident weights: the all-core rate and
+    # the one-core rate, each with its sample, and the thread count restored afterwards
+    import torch
+
+    import oracle
+    w = synth.workload("tiny")
+    r = synth.routing_inputs(w)
+    wt = synth.expert_weights_device(w, torch.device("cpu"))
+    before = oracle.num_threads()
+    out = bench.cpu_baseline(w, r, wt, budget_s=0.2)
+    assert out["kind"] == "oracle" and out["cores"] == before and out["value"] > 0
+    assert out["one_core"]["cores"] == 1 and out["one_core"]["value"] > 0
+    assert oracle.num_threads() == before
