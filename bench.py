@@ -437,9 +437,29 @@ def measure_side_workload(name, weights, dev, args, sampler, peaks, peak_src, ba
                             "scales, on the FP8 tensor cores")
     if key:
         row["target"] = {"metric": key, "min": tgt, "met": bool(lr[key] >= tgt)}
+    if name == "skewed":
+        row["routing_stats"] = skew_stats(counts, layer.affinity.cpu().numpy(), w.T)
     del layer
     torch.cuda.empty_cache()
     return row
+
+
+def skew_stats(counts, affinity, T: int, cluster: int = 32) -> dict:
+    """What the skewed recipe aims at, read off the layer's own counts and co-activation
+    matrix: the log-log slope of count against popularity rank (ranks >= 3, the two
+    capped at T left out) and the share of co-activations inside a cluster of 32 experts."""
+    import numpy as np
+    c = np.sort(np.asarray(counts, dtype=np.float64))[::-1]
+    r = np.arange(1, c.size + 1)
+    m = (c > 0) & (r >= 3)
+    slope = float(np.polyfit(np.log(r[m]), np.log(c[m]), 1)[0]) if m.sum() >= 2 else None
+    A = np.asarray(affinity, dtype=np.int64)
+    g = np.arange(A.shape[0]) // cluster
+    tot = int(A.sum())
+    within = float(A[g[:, None] == g[None, :]].sum() / tot) if tot else None
+    return {"zipf_slope": None if slope is None else round(slope, 3),
+            "within_cluster_coactivation": None if within is None else round(within, 4),
+            "top_counts": [int(x) for x in c[:3]], "cap": int(T)}
 
 
 def run_ours(args, rank, world, local_rank):

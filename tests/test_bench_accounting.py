@@ -107,3 +107,19 @@ def test_cpu_baseline_reports_all_cores_and_one_core():
     assert out["kind"] == "oracle" and out["cores"] == before and out["value"] > 0
     assert out["one_core"]["cores"] == 1 and out["one_core"]["value"] > 0
     assert oracle.num_threads() == before
+
+
+def test_skew_stats_on_a_planted_routing():
+    # counts exactly c_r = 1000 r^-1.2 and co-activations only inside clusters of 32: the
+    # slope and the within-cluster share come back as planted
+    import numpy as np
+    E = 64
+    c = np.rint(1000.0 * np.arange(1, E + 1) ** -1.2)
+    A = np.zeros((E, E), np.int64)
+    for k in range(E // 32):
+        A[32 * k:32 * k + 32, 32 * k:32 * k + 32] = 3
+    np.fill_diagonal(A, 0)
+    s = bench.skew_stats(np.random.default_rng(0).permutation(c), A, T=10_000)
+    assert abs(s["zipf_slope"] + 1.2) < 0.02
+    assert s["within_cluster_coactivation"] == 1.0
+    assert s["top_counts"][0] == 1000
