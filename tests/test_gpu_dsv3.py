@@ -122,3 +122,29 @@ def test_dispatch_of_concentrated_routing(T, hot):
         assert np.array_equal(got.cpu().numpy(), d[name]), name
     p = torch.from_numpy(d["perm"].astype(np.int64)).to(DEV)
     assert torch.equal(Xp.view(torch.int16), X.view(torch.int16)[p])
+
+
+@pytest.mark.parametrize("name,T,fp8,reps", [("decode", None, False, 40), ("decode", None, True, 40),
+                                             ("decode", 4100, False, 12)])
+def test_repeated_calls_are_bit_identical(dsv3_weights, name, T, fp8, reps):
+    """The layer repeated on the same inputs gives bit-identical outputs every time: a race
+    between the persistent FFN's units (tile claims, the up -> down readiness counters, the
+    FP8 scale ring) or in the router's CTA-wide re-score would show as an occasional
+    difference.  DeepSeek-V3 decode (bf16 and FP8 experts) and 4100 tokens (CTA-pair tiles,
+    the multi-launch dispatch)."""
+    w = synth.workload(name) if T is None else synth.workload(name, T=T, x_seed=T)
+    r = synth.routing_inputs(w)
+    X = host_to_device_bf16(r["X"])
+    weights = dict(dsv3_weights)
+    weights["W_gate"] = host_to_device_bf16(r["W_gate"])
+    weights["bias"] = torch.from_numpy(r["bias"]).to(DEV)
+    layer = B.MoELayer(weights, w.T, w.K, fp8=fp8)
+    layer.forward(X)
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in (layer.Y, layer.topk_idx, layer.topk_w, layer.counts, layer.affinity)]
+    for i in range(reps):
+        layer.forward(X)
+        outs = (layer.Y, layer.topk_idx, layer.topk_w, layer.counts, layer.affinity)
+        for got, want in zip(outs, ref):
+            assert torch.equal(got, want), f"call {i + 2} differs"
+    assert layer.status() == 0
