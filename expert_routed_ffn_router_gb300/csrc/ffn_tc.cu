@@ -432,8 +432,12 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         T.mt = e[4]; T.row0 = e[5]; T.nvalid = e[6]; T.nti = e[7];
         return T;
     };
+    // The even CTA's own roles arrive locally; the odd CTA's arrive on the even CTA's
+    // barrier with release at cluster scope, so the even CTA's waits on tqe and tempty
+    // acquire at cluster scope (the odd CTA's reads of its slot copy and of its tensor
+    // memory are then ordered before the even CTA overwrites them).
     auto tqe_arrive = [&](int q) {
-        if (PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(&tqe[q]), 0));
+        if (PAIR && !leader) mbar_arrive_cluster(mapa_shared(smem_u32(&tqe[q]), 0));
         else mbar_arrive(&tqe[q]);
     };
     // MMA N: the valid rows rounded up to the instruction's granule (a pair splits N
@@ -459,7 +463,9 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             // trip overlaps a tile's loads instead of stalling the ring at the tile boundary
             unsigned pend = FP8 ? atomicAdd(p.next_tile, 1u) : 0u;
             auto claim = [&](Tile &T) -> bool {
-                if (!mbar_wait(&tqe[qs], qph ^ 1u, abort_flag, p.status, tmo)) return false;
+                if (!(PAIR ? mbar_wait_cluster(&tqe[qs], qph ^ 1u, abort_flag, p.status, tmo)
+                           : mbar_wait(&tqe[qs], qph ^ 1u, abort_flag, p.status, tmo)))
+                    return false;
                 unsigned ticket;
                 if (FP8) {
                     ticket = pend;
@@ -622,7 +628,8 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                 const ProbDev &P = p.prob[T.pi];
                 const uint32_t b = tc & 1u, tph = (tc >> 1) & 1u;
                 if (!FP8) {
-                    if (!mbar_wait(&tempty[b], tph ^ 1u, abort_flag, p.status, tmo)) { ok = false; break; }
+                    if (!(PAIR ? mbar_wait_cluster(&tempty[b], tph ^ 1u, abort_flag, p.status, tmo)
+                               : mbar_wait(&tempty[b], tph ^ 1u, abort_flag, p.status, tmo))) { ok = false; break; }
                     tc_fence_after();
                 }
                 const int n_mma = n_mma_of(T);
@@ -970,7 +977,7 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             }
             if (!FP8) {
                 tc_fence_before();
-                if (PAIR)
+                if (PAIR && !leader)
                     mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[b]), 0));
                 else
                     mbar_arrive(&tempty[b]);
