@@ -139,11 +139,20 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------ accounting
-def ffn_traffic(workload: str, fp8: bool = False):
-    """DRAM bytes per step of the FFN launches from the committed ncu record (bf16 weights:
-    the routed launch; FP8 weights: the up and the down launch), or None when the record
-    does not cover this workload or the FFN sources changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", "ffn_traffic.json")
+TRAFFIC_MAX_TOKENS = 256
+
+
+def ffn_traffic(w, fp8: bool, alg_bytes: int, path: str | None = None):
+    """DRAM bytes per step of the FFN launches (bf16 weights: the routed launch; FP8: the up
+    and the down launch) for batches of up to TRAFFIC_MAX_TOKENS tokens, where every
+    activated expert is one token tile that streams its weights once: the step's
+    algorithmic bytes times the DRAM / algorithmic ratio ncu measured on small cases of the
+    same regime (profiles/ffn_traffic.json, taken on the current FFN sources).  None for
+    larger batches (their token tiles' L2 reuse depends on the routing, so the small cases
+    do not scale to them), or when the FFN sources changed since the record was taken."""
+    if w.T > TRAFFIC_MAX_TOKENS:
+        return None
+    path = path or os.path.join(ROOT, "profiles", "ffn_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
@@ -153,10 +162,9 @@ def ffn_traffic(workload: str, fp8: bool = False):
                 h.update(f.read())
         if h.hexdigest() != rec["sources_sha256"]:
             return None
-        return rec["bytes_per_step_fp8" if fp8 else "bytes_per_step"].get(workload)
-    except (OSError, KeyError, ValueError):
+        return int(round(rec["ratio"]["fp8" if fp8 else "bf16"] * alg_bytes))
+    except (OSError, KeyError, ValueError, TypeError):
         return None
-
 
 
 def shared_on_side(w, fp8: bool = False) -> bool:
@@ -305,7 +313,7 @@ def _stage_pass(layer, X, K, stream):
     return stage_ms
 
 
-def dominant_roofline(w, n_act, stage_ms, peaks, peak_src, fp8, workload_name):
+def dominant_roofline(w, n_act, stage_ms, peaks, peak_src, fp8):
     b, f, _, _ = algorithmic(w, n_act, 1 if fp8 else 2, shared_on_side(w, fp8))
     dom = max(("ffn", "router", "combine", "dispatch"), key=lambda s: stage_ms[s])
     t_dom = stage_ms[dom] / 1e3
@@ -321,7 +329,11 @@ def dominant_roofline(w, n_act, stage_ms, peaks, peak_src, fp8, workload_name):
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = ffn_traffic(workload_name, fp8) if dom == "ffn" else None
+    roof["traffic"] = ffn_traffic(w, fp8, b[dom]) if dom == "ffn" else None
+    if roof["traffic"] is not None:
+        roof["traffic_source"] = ("algorithmic bytes x the DRAM / algorithmic ratio of ncu "
+                                  "captures of small weight-streaming cases "
+                                  "(profiles/ffn_traffic.json)")
     roof["kernel"] = dom
     roof["peak_source"] = (f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured"
                            else "fallback")
@@ -428,7 +440,7 @@ def measure_side_workload(name, weights, dev, args, sampler, peaks, peak_src, ba
     key, tgt = target_of(w) if not fp8 else (None, None)
     row = {"T": w.T, "ms_per_step": round(ms, 4), "tokens_per_s": round(w.T / (ms / 1e3), 1),
            "n_active_experts": n_act, **lr,
-           "dominant_kernel": dominant_roofline(w, n_act, stage_ms, peaks, peak_src, fp8, name),
+           "dominant_kernel": dominant_roofline(w, n_act, stage_ms, peaks, peak_src, fp8),
            "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
            "gpu_launches": args.steps * launches_per_step(w, with_affinity=True, fp8=fp8),
            "clocks": sampler.summary(t0, t1, t_busy0, t_busy1)}
@@ -562,7 +574,7 @@ def run_ours(args, rank, world, local_rank):
     rep = B.moe_grace_replicate(counts, plan["group_of"], 8)
     B.moe_grace_route_table(rep, 4)
     ms_plan = (time.perf_counter() - t_plan) * 1e3
-    roof = dominant_roofline(w, n_act, stage_ms, peaks, peak_src, fp8, w.name)
+    roof = dominant_roofline(w, n_act, stage_ms, peaks, peak_src, fp8)
     lr = layer_roofline(w, n_act, ms, peaks, fp8)
 
     total_tokens = w.T * world

@@ -28,6 +28,7 @@ def main(argv=None):
     ap.add_argument("--T", type=int, default=0, help="override the token count")
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--fp8", action="store_true", help="layer stage: E4M3 expert weights")
     args = ap.parse_args(argv)
 
     dev = torch.device("cuda", 0)
@@ -73,7 +74,7 @@ def main(argv=None):
     else:
         weights = synth.expert_weights_device(w, dev)
         weights["W_gate"], weights["bias"] = Wg, bias
-        layer = B.MoELayer(weights, T, K)
+        layer = B.MoELayer(weights, T, K, fp8=args.fp8)
 
         def run():
             layer.forward(X)
@@ -87,9 +88,15 @@ def main(argv=None):
         run()
     e1.record()
     torch.cuda.synchronize()
-    st = B.moe_read_status(ws)
-    print(json.dumps({"stage": args.stage, "workload": w.name, "T": T,
-                      "ms": round(e0.elapsed_time(e1) / args.iters, 4), "status": st}))
+    out = {"stage": args.stage, "workload": w.name, "T": T,
+           "ms": round(e0.elapsed_time(e1) / args.iters, 4)}
+    if args.stage == "layer":
+        # the layer's own workspace and by-products: status word, activated experts
+        out.update(fp8=args.fp8, status=layer.status(),
+                   n_active=int((layer.counts > 0).sum().item()))
+    else:
+        out["status"] = B.moe_read_status(ws)
+    print(json.dumps(out))
 
 
 if __name__ == "__main__":

@@ -2,6 +2,7 @@
 stage when the shared expert runs in its own launch add up to those of the single launch,
 and the launch count per step follows the library's launch structure."""
 import dataclasses
+import os
 
 import bench
 from expert_routed_ffn_router_gb300 import synth
@@ -69,8 +70,8 @@ def test_fp8_dominant_kernel_takes_the_fp8_peak():
     w = synth.workload("prefill")
     stage_ms = {"router": 1.0, "dispatch": 0.5, "ffn_up": 10.0, "ffn_down": 0.0, "combine": 0.4,
                 "ffn": 10.0}
-    r16 = bench.dominant_roofline(w, w.E, stage_ms, peaks, "measured", False, "prefill")
-    r8 = bench.dominant_roofline(w, w.E, stage_ms, peaks, "measured", True, "prefill")
+    r16 = bench.dominant_roofline(w, w.E, stage_ms, peaks, "measured", False)
+    r8 = bench.dominant_roofline(w, w.E, stage_ms, peaks, "measured", True)
     assert r16["bound"] == r8["bound"] == "tensor"
     assert r16["peak"] == 2000.0 and r8["peak"] == 2000.0 * bench.FP8_OVER_BF16
     assert "ratio" in r8["peak_source"] and "ratio" not in r16["peak_source"]
@@ -123,3 +124,27 @@ def test_skew_stats_on_a_planted_routing():
     assert abs(s["zipf_slope"] + 1.2) < 0.02
     assert s["within_cluster_coactivation"] == 1.0
     assert s["top_counts"][0] == 1000
+
+
+def test_ffn_traffic_scales_small_case_ratio_only_for_weight_streaming_batches(tmp_path):
+    import hashlib
+    import json
+    srcs = ["expert_routed_ffn_router_gb300/csrc/ffn_tc.cu",
+            "expert_routed_ffn_router_gb300/csrc/common.cuh"]
+    h = hashlib.sha256()
+    for s in srcs:
+        with open(os.path.join(bench.ROOT, s), "rb") as f:
+            h.update(f.read())
+    rec = {"sources": srcs, "sources_sha256": h.hexdigest(), "ratio": {"bf16": 1.01, "fp8": 1.02}}
+    p = tmp_path / "t.json"
+    p.write_text(json.dumps(rec))
+    dec, pre = synth.workload("decode"), synth.workload("prefill")
+    assert bench.ffn_traffic(dec, False, 10**9, str(p)) == 1_010_000_000
+    assert bench.ffn_traffic(dec, True, 10**9, str(p)) == 1_020_000_000
+    assert bench.ffn_traffic(synth.workload("sweep256"), False, 100, str(p)) == 101
+    # larger batches: the small cases do not scale to them
+    assert bench.ffn_traffic(pre, False, 10**9, str(p)) is None
+    # a record taken on other sources is not reported
+    rec["sources_sha256"] = "0" * 64
+    p.write_text(json.dumps(rec))
+    assert bench.ffn_traffic(dec, False, 10**9, str(p)) is None
