@@ -73,18 +73,20 @@ def plan_exchange(offsets: torch.Tensor, owner: torch.Tensor, group=None) -> Exc
     """Steps 2 and the bookkeeping of 3-5 from this rank's dispatch offsets [E + 1] (rows of
     expert e are offsets[e] .. offsets[e+1] of Xp).  Collective: every rank calls it."""
     world, rank = _world(group)
+    # the counts travel on the offsets' device (NCCL exchanges device tensors only, gloo
+    # host ones); the bookkeeping below is host work on a few integers per expert
+    dev = offsets.device
     offsets = offsets.to(torch.int64).cpu()
     owner = owner.to(torch.int64).cpu()
-    E = owner.numel()
     counts = offsets[1:] - offsets[:-1]
     experts_of = [torch.nonzero(owner == d).flatten() for d in range(world)]
     mine = experts_of[rank]
     # 2. counts exchange: to rank d, the counts of d's experts (ascending)
-    send_c = torch.cat([counts[experts_of[d]] for d in range(world)])
-    recv_c = torch.empty(world * mine.numel(), dtype=torch.int64)
+    send_c = torch.cat([counts[experts_of[d]] for d in range(world)]).to(dev)
+    recv_c = torch.empty(world * mine.numel(), dtype=torch.int64, device=dev)
     dist.all_to_all_single(recv_c, send_c, [mine.numel()] * world,
                            [experts_of[d].numel() for d in range(world)], group=group)
-    recv_counts = recv_c.view(world, mine.numel())
+    recv_counts = recv_c.cpu().view(world, mine.numel())
     # 3. send order: by destination, then by expert (the expert's Xp rows in order)
     order = []
     send_splits = []
