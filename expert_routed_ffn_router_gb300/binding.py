@@ -127,14 +127,47 @@ def load(build_if_missing: bool = True):
     return lib
 
 
-def _ptr(t):
+BF16, F32, I32, U8 = torch.bfloat16, torch.float32, torch.int32, torch.uint8
+
+
+def _chk(t, dtype=None, numel=None, name="tensor"):
+    """The C ABI takes bare pointers: a tensor of another element type, or smaller than the
+    sizes passed beside it, would be misread (or read past its end) by the kernels."""
+    if t is None:
+        return
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name}: {t.numel()} elements, expected {numel}")
+
+
+def _ptr(t, dtype=None, numel=None, name="tensor"):
+    """Device pointer of a contiguous CUDA tensor (None stays NULL), after _chk."""
     if t is None:
         return None
+    _chk(t, dtype, numel, name)
     if not t.is_cuda:
-        raise ValueError("device tensors are required")
+        raise ValueError(f"{name}: device tensors are required")
     if not t.is_contiguous():
-        raise ValueError("contiguous tensors are required")
+        raise ValueError(f"{name}: contiguous tensors are required")
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _ptrs(*specs):
+    """Pointers of (tensor, dtype, numel, name) arguments: every element type and size is
+    checked before any device check."""
+    for spec in specs:
+        _chk(*spec)
+    return [_ptr(*spec) for spec in specs]
+
+
+def _wstruct(cls, weights: dict, specs, io_specs):
+    """A weights structure from (name, dtype, numel) specs (a missing name stays NULL), with
+    the layer's input / output tensors (io_specs): every type and size is checked first."""
+    ws = [(weights.get(n), dt, k, n) for n, dt, k in specs]
+    for spec in ws + list(io_specs):
+        _chk(*spec)
+    return cls(*[None if t is None else _ptr(t, dt, k, n).value for t, dt, k, n in ws])
 
 
 def _stream(stream):
@@ -194,30 +227,32 @@ def moe_debug_set_stage_events(events) -> None:
     load().moe_debug_set_stage_events(ctypes.cast(arr, ctypes.c_void_p), len(events))
 
 
-def moe_router_topk(X, W_gate, bias, K, topk_idx, topk_w, ws, stream=None):
+def _router_args(X, W_gate, bias, K, topk_idx, topk_w):
     T, H = X.shape
-    E = W_gate.shape[0]
+    E, K = W_gate.shape[0], int(K)
+    x, wg, b, i, w = _ptrs((X, BF16, T * H, "X"), (W_gate, BF16, E * H, "W_gate"),
+                           (bias, F32, E, "bias"), (topk_idx, I32, T * K, "topk_idx"),
+                           (topk_w, F32, T * K, "topk_w"))
+    return (x, wg, b, T, H, E, K), (i, w)
+
+
+def moe_router_topk(X, W_gate, bias, K, topk_idx, topk_w, ws, stream=None):
+    a, o = _router_args(X, W_gate, bias, K, topk_idx, topk_w)
     _check("moe_router_topk", load().moe_router_topk(
-        _ptr(X), _ptr(W_gate), _ptr(bias), T, H, E, int(K), _ptr(topk_idx), _ptr(topk_w),
-        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+        *a, *o, _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def moe_router_topk_ex(X, W_gate, bias, K, routing, topk_idx, topk_w, ws, stream=None):
     """routing: MoeRouting, a dict of MoeRouting.make keywords, or None (defaults)."""
-    T, H = X.shape
-    E = W_gate.shape[0]
+    a, o = _router_args(X, W_gate, bias, K, topk_idx, topk_w)
     _check("moe_router_topk_ex", load().moe_router_topk_ex(
-        _ptr(X), _ptr(W_gate), _ptr(bias), T, H, E, int(K), _routing(routing), _ptr(topk_idx),
-        _ptr(topk_w), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+        *a, _routing(routing), *o, _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def moe_router_topk_noalloc(X, W_gate, bias, K, topk_idx, topk_w, stream=None):
     """The router without a workspace (its scratch is a fixed array of the library)."""
-    T, H = X.shape
-    E = W_gate.shape[0]
-    _check("moe_router_topk_noalloc", load().moe_router_topk_noalloc(
-        _ptr(X), _ptr(W_gate), _ptr(bias), T, H, E, int(K), _ptr(topk_idx), _ptr(topk_w),
-        _stream(stream)))
+    a, o = _router_args(X, W_gate, bias, K, topk_idx, topk_w)
+    _check("moe_router_topk_noalloc", load().moe_router_topk_noalloc(*a, *o, _stream(stream)))
 
 
 def moe_router_topk_noalloc_status(stream=None) -> int:
@@ -227,10 +262,14 @@ def moe_router_topk_noalloc_status(stream=None) -> int:
 def moe_dispatch(X, topk_idx, E, counts, offsets, perm, slot_pos, Xp, affinity, ws,
                  stream=None):
     T, H = X.shape
-    K = topk_idx.shape[1]
+    K, E = topk_idx.shape[1], int(E)
+    x, i, c, o, pm, sp, xp, af = _ptrs(
+        (X, BF16, T * H, "X"), (topk_idx, I32, T * K, "topk_idx"), (counts, I32, E, "counts"),
+        (offsets, I32, E + 1, "offsets"), (perm, I32, T * K, "perm"),
+        (slot_pos, I32, T * K, "slot_pos"), (Xp, BF16, T * K * H, "Xp"),
+        (affinity, I32, E * E, "affinity"))
     _check("moe_dispatch", load().moe_dispatch(
-        _ptr(X), _ptr(topk_idx), T, H, int(E), K, _ptr(counts), _ptr(offsets), _ptr(perm),
-        _ptr(slot_pos), _ptr(Xp), _ptr(affinity), _ptr(ws), ws.numel() * ws.element_size(),
+        x, i, T, H, E, K, c, o, pm, sp, xp, af, _ptr(ws), ws.numel() * ws.element_size(),
         _stream(stream)))
 
 
@@ -240,37 +279,55 @@ def moe_expert_ffn_workspace_bytes(rows: int, n_groups: int, I: int) -> int:
 
 def moe_expert_ffn(Xp, offsets, n_groups, W1, W3, W2, Yp, ws, stream=None):
     rows, H = Xp.shape
-    I = W1.shape[-1]
+    I, G = W1.shape[-1], int(n_groups)
     out_fp32 = 1 if Yp.dtype == torch.float32 else 0
+    xp, o, w1, w3, w2, yp = _ptrs(
+        (Xp, BF16, rows * H, "Xp"), (offsets, I32, G + 1, "offsets"),
+        (W1, BF16, G * H * I, "W1"), (W3, BF16, G * H * I, "W3"), (W2, BF16, G * I * H, "W2"),
+        (Yp, F32 if out_fp32 else BF16, rows * H, "Yp"))
     _check("moe_expert_ffn", load().moe_expert_ffn(
-        _ptr(Xp), _ptr(offsets), int(n_groups), rows, H, I, _ptr(W1), _ptr(W3), _ptr(W2),
-        _ptr(Yp), out_fp32, _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+        xp, o, G, rows, H, I, w1, w3, w2, yp, out_fp32, _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def moe_combine(Yp, slot_pos, topk_w, Ysh, Y, stream=None):
     T, K = slot_pos.shape
     H = Y.shape[1]
-    _check("moe_combine", load().moe_combine(
-        _ptr(Yp), _ptr(slot_pos), _ptr(topk_w), _ptr(Ysh), T, H, K, _ptr(Y), _stream(stream)))
+    yp, sp, w, ysh, y = _ptrs((Yp, BF16, T * K * H, "Yp"), (slot_pos, I32, T * K, "slot_pos"),
+                              (topk_w, F32, T * K, "topk_w"), (Ysh, F32, T * H, "Ysh"),
+                              (Y, F32, T * H, "Y"))
+    _check("moe_combine", load().moe_combine(yp, sp, w, ysh, T, H, K, y, _stream(stream)))
+
+
+def _io_specs(shape: MoeShape, X, Y, topk_idx, topk_w, counts, affinity):
+    T, H, E, K = shape.T, shape.H, shape.E, shape.K
+    return [(X, BF16, T * H, "X"), (Y, F32, T * H, "Y"), (topk_idx, I32, T * K, "topk_idx"),
+            (topk_w, F32, T * K, "topk_w"), (counts, I32, E, "counts"),
+            (affinity, I32, E * E, "affinity")]
+
+
+def _layer_args(shape: MoeShape, weights: dict, io):
+    H, E, I, Is = shape.H, shape.E, shape.I, shape.I_shared
+    w = _wstruct(MoeWeights, weights,
+                 (("W_gate", BF16, E * H), ("bias", F32, E), ("W1", BF16, E * H * I),
+                  ("W3", BF16, E * H * I), ("W2", BF16, E * I * H), ("W1s", BF16, H * Is),
+                  ("W3s", BF16, H * Is), ("W2s", BF16, Is * H)), io)
+    return w, _ptrs(*io)
 
 
 def moe_layer_forward(shape: MoeShape, weights: dict, X, Y, topk_idx, topk_w, counts,
                       affinity, ws, stream=None):
-    w = MoeWeights(*[None if weights.get(n) is None else weights[n].data_ptr()
-                     for n in ("W_gate", "bias", "W1", "W3", "W2", "W1s", "W3s", "W2s")])
+    w, io = _layer_args(shape, weights, _io_specs(shape, X, Y, topk_idx, topk_w, counts, affinity))
     _check("moe_layer_forward", load().moe_layer_forward(
-        ctypes.byref(shape), ctypes.byref(w), _ptr(X), _ptr(Y), _ptr(topk_idx), _ptr(topk_w),
-        _ptr(counts), _ptr(affinity), _ptr(ws), ws.numel() * ws.element_size(),
+        ctypes.byref(shape), ctypes.byref(w), *io, _ptr(ws), ws.numel() * ws.element_size(),
         _stream(stream)))
 
 
 def moe_layer_forward_ex(shape: MoeShape, weights: dict, routing, X, Y, topk_idx, topk_w,
                          counts, affinity, ws, stream=None):
-    w = MoeWeights(*[None if weights.get(n) is None else weights[n].data_ptr()
-                     for n in ("W_gate", "bias", "W1", "W3", "W2", "W1s", "W3s", "W2s")])
+    w, io = _layer_args(shape, weights, _io_specs(shape, X, Y, topk_idx, topk_w, counts, affinity))
     _check("moe_layer_forward_ex", load().moe_layer_forward_ex(
-        ctypes.byref(shape), ctypes.byref(w), _routing(routing), _ptr(X), _ptr(Y),
-        _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(affinity), _ptr(ws),
+        ctypes.byref(shape), ctypes.byref(w), _routing(routing), *io, _ptr(ws),
         ws.numel() * ws.element_size(), _stream(stream)))
 
 
@@ -283,7 +340,7 @@ def moe_quantize_weight_fp8(W, stream=None):
     Wq = torch.empty(shape[:-2] + (C, R), dtype=torch.uint8, device=W.device)
     S = torch.empty(shape[:-2] + (R // 128, C // 128), dtype=torch.int32, device=W.device)
     _check("moe_quantize_weight_fp8", load().moe_quantize_weight_fp8(
-        _ptr(W), G, R, C, _ptr(Wq), _ptr(S), _stream(stream)))
+        _ptr(W, BF16, name="W"), G, R, C, _ptr(Wq), _ptr(S), _stream(stream)))
     return Wq, S
 
 
@@ -311,12 +368,17 @@ def quantize_expert_weights_fp8(weights: dict, stream=None) -> dict:
 
 def moe_layer_forward_fp8(shape: MoeShape, weights8: dict, routing, X, Y, topk_idx, topk_w,
                           counts, affinity, ws, stream=None):
-    w = MoeWeightsFp8(*[None if weights8.get(n) is None else weights8[n].data_ptr()
-                        for n in ("W_gate", "bias", "W1", "W3", "W2", "S1", "S3", "S2", "W1s",
-                                  "W3s", "W2s", "S1s", "S3s", "S2s")])
+    H, E, I, Is = shape.H, shape.E, shape.I, shape.I_shared
+    tiles, tiles_s = (H // 128) * (I // 128), (H // 128) * (Is // 128)
+    io = _io_specs(shape, X, Y, topk_idx, topk_w, counts, affinity)
+    w = _wstruct(MoeWeightsFp8, weights8,
+                 (("W_gate", BF16, E * H), ("bias", F32, E), ("W1", U8, E * H * I),
+                  ("W3", U8, E * H * I), ("W2", U8, E * I * H), ("S1", I32, E * tiles),
+                  ("S3", I32, E * tiles), ("S2", I32, E * tiles), ("W1s", U8, H * Is),
+                  ("W3s", U8, H * Is), ("W2s", U8, Is * H), ("S1s", I32, tiles_s),
+                  ("S3s", I32, tiles_s), ("S2s", I32, tiles_s)), io)
     _check("moe_layer_forward_fp8", load().moe_layer_forward_fp8(
-        ctypes.byref(shape), ctypes.byref(w), _routing(routing), _ptr(X), _ptr(Y),
-        _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(affinity), _ptr(ws),
+        ctypes.byref(shape), ctypes.byref(w), _routing(routing), *_ptrs(*io), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(stream)))
 
 

@@ -125,3 +125,33 @@ def test_workspace_layout_lies_inside_the_workspace(shape):
 def test_workspace_layout_rejects_what_the_size_query_rejects():
     with pytest.raises(binding.MoeError):
         binding.moe_workspace_layout(1, 100, 16, 2, 128, 0)       # H % 64 != 0
+
+
+def test_binding_checks_element_types_and_sizes_before_the_call():
+    # the C ABI takes bare pointers: the binding rejects a tensor of another element type,
+    # or one smaller than the sizes passed beside it (which a kernel would read past),
+    # before anything is called (CPU tensors: the checks come before the device check)
+    import torch
+    T, H, E, K = 4, 64, 8, 2
+    X = torch.zeros(T, H, dtype=torch.bfloat16)
+    Wg = torch.zeros(E, H, dtype=torch.bfloat16)
+    bias = torch.zeros(E, dtype=torch.float32)
+    idx = torch.zeros(T, K, dtype=torch.int32)
+    wt = torch.zeros(T, K, dtype=torch.float32)
+    ws = torch.zeros(1024, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="X: dtype"):
+        binding.moe_router_topk(X.float(), Wg, bias, K, idx, wt, ws)
+    with pytest.raises(ValueError, match="W_gate: 256 elements, expected 512"):
+        binding.moe_router_topk(X, Wg[:, :32].contiguous(), bias, K, idx, wt, ws)
+    with pytest.raises(ValueError, match="topk_idx: dtype"):
+        binding.moe_router_topk(X, Wg, bias, K, idx.long(), wt, ws)
+    with pytest.raises(ValueError, match="device tensors"):
+        binding.moe_router_topk(X, Wg, bias, K, idx, wt, ws)
+    # the layer: a routed weight with fewer experts than the shape says
+    shape = binding.MoeShape(T, H, E, K, 64, 0)
+    W = {"W_gate": Wg, "bias": bias, "W1": torch.zeros(E - 1, H, 64, dtype=torch.bfloat16),
+         "W3": torch.zeros(E, H, 64, dtype=torch.bfloat16),
+         "W2": torch.zeros(E, 64, H, dtype=torch.bfloat16)}
+    with pytest.raises(ValueError, match="W1: "):
+        binding.moe_layer_forward(shape, W, X, torch.zeros(T, H), idx, wt,
+                                  torch.zeros(E, dtype=torch.int32), None, ws)
