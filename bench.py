@@ -167,6 +167,13 @@ def ffn_traffic(w, fp8: bool, alg_bytes: int, path: str | None = None):
         return None
 
 
+def workload_desc(w) -> str:
+    """The config's workload string, the same on both arms."""
+    dsv3 = (w.H, w.E, w.K, w.I, w.Is) == (7168, 256, 8, 2048, 2048)
+    return (f"{w.name}: {'DeepSeek-V3-shaped ' if dsv3 else ''}MoE layer forward, T={w.T} "
+            f"tokens, H={w.H}, E={w.E}, top-{w.K}, I={w.I}, shared I={w.Is}")
+
+
 def shared_on_side(w, fp8: bool = False) -> bool:
     """moe_layer_forward runs the shared expert as its own launch on a side stream (bf16
     weights, up to 128 tokens); otherwise it is a second problem of the routed FFN launch."""
@@ -585,8 +592,7 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8-e4m3 experts (128x128 / 1x128 block scales), bf16 activations" if fp8 else "bf16",
         "data": "synthetic (seeded; random-init weights of the DeepSeek-V3 MoE shape)",
-        "config": {"workload": f"{w.name}: DeepSeek-V3-shaped MoE layer forward, T={w.T} "
-                               f"tokens, H={w.H}, E={w.E}, top-{w.K}, I={w.I}, shared I={w.Is}",
+        "config": {"workload": workload_desc(w),
                    "tokens_per_gpu": w.T, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2: the activated experts' weights "
                          f"({lr['algorithmic_bytes'] / 1e9:.1f} GB) stream from HBM every step",
@@ -741,7 +747,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tt / args.steps * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)", "impl": "reference",
-        "config": {"workload": f"{w.name}: DeepSeek-V3-shaped MoE layer forward, T={w.T}",
+        "config": {"workload": workload_desc(w), "tokens_per_gpu": w.T,
                    **({"routing": {"name": args.routing, **opts}} if opts else {})},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{n} random tokens of the {w.T}-token workload per step"},
