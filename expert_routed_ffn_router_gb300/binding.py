@@ -96,6 +96,7 @@ def load(build_if_missing: bool = True):
         "moe_debug_set_stage_events": ([P, I], None),
         "moe_debug_set_ffn_variant": ([I], None),
         "moe_debug_set_shared_side": ([I], None),
+        "moe_debug_set_sync_status": ([I], None),
         "moe_router_topk": ([P, P, P, I, I, I, I, P, P, P, Z, P], I),
         "moe_router_topk_ex": ([P, P, P, I, I, I, I, ctypes.POINTER(MoeRouting), P, P, P, Z,
                                 P], I),
@@ -211,6 +212,12 @@ def moe_debug_set_wait_limit(limit_ns: int, inject_stall: int = 0) -> None:
 def moe_debug_set_ffn_variant(variant: int) -> None:
     """0: automatic; 1: single-CTA FFN kernel; 2: CTA-pair (2-SM MMA) FFN kernel."""
     load().moe_debug_set_ffn_variant(int(variant))
+
+
+def moe_debug_set_sync_status(on: bool) -> None:
+    """Debug mode: calls synchronise and return their workspace's status word (a device-side
+    error then raises MoeError from the call itself)."""
+    load().moe_debug_set_sync_status(1 if on else 0)
 
 
 def moe_debug_set_shared_side(mode: int) -> None:

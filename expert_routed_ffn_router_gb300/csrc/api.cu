@@ -57,6 +57,7 @@ int g_inject_stall = 0;
 cudaEvent_t g_stage_events[6] = {};
 bool g_stage_events_on = false;
 int g_shared_side = -1;   // shared expert on the side stream: -1 by batch size, 0 never, 1 always
+std::atomic<int> g_sync_status{0};   // debug mode: calls return their workspace's status word
 
 // Up to this many tokens the router and the dispatch leave most of the GPU idle (their
 // kernels wait on latency, not on SMs or HBM): the shared expert, which needs no routing,
@@ -469,6 +470,26 @@ int moe_read_status(void *ws, void *stream)
     return v;
 }
 
+void moe_debug_set_sync_status(int on)
+{
+    g_sync_status.store(on ? 1 : 0, std::memory_order_relaxed);
+}
+
+// Debug mode: after a call enqueued work without error, synchronise its stream and return
+// the workspace's status word (read and reset as by moe_read_status) -- unless nothing was
+// enqueued (an empty batch) or the stream is being captured into a graph, which cannot be
+// synchronised.
+static int debug_status(int rc, void *ws, void *stream, bool enqueued = true)
+{
+    if (rc != MOE_OK || !enqueued || g_sync_status.load(std::memory_order_relaxed) == 0)
+        return rc;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone) return rc;
+    return moe_read_status(ws, stream);
+}
+
 void moe_debug_set_wait_limit(unsigned long long limit_ns, int inject_stall)
 {
     g_wait_limit_ns = limit_ns ? limit_ns : 1000000000ull;
@@ -513,9 +534,10 @@ int moe_router_topk_ex(const void *X, const void *W_gate, const float *bias, int
     const RouterLayout L = router_layout(T, H, E, w ? w + kHeader : nullptr);
     if ((rc = check_ws(ws, ws_bytes, kHeader + L.bytes))) return rc;
     if (T == 0) return MOE_OK;
-    return cuda_status(launch_router(X, W_gate, bias, T, H, E, K, topk_idx, topk_w, L.plan,
-                                     L.scr, static_cast<int *>(ws),
-                                     static_cast<cudaStream_t>(stream), &ro));
+    return debug_status(cuda_status(launch_router(X, W_gate, bias, T, H, E, K, topk_idx, topk_w,
+                                                  L.plan, L.scr, static_cast<int *>(ws),
+                                                  static_cast<cudaStream_t>(stream), &ro)),
+                        ws, stream);
 }
 
 int moe_dispatch(const void *X, const int32_t *topk_idx, int T, int H, int E, int K,
@@ -530,9 +552,11 @@ int moe_dispatch(const void *X, const int32_t *topk_idx, int T, int H, int E, in
     const DispatchLayout L = dispatch_layout(T, E, w ? w + kHeader : nullptr);
     if ((rc = check_ws(ws, ws_bytes, kHeader + L.bytes))) return rc;
     if (T == 0) return MOE_OK;
-    return cuda_status(launch_dispatch(X, topk_idx, T, H, E, K, counts, offsets, perm, slot_pos,
-                                       Xp, affinity, L.plan, L.scr, nullptr, 0, static_cast<int *>(ws),
-                                       static_cast<cudaStream_t>(stream)));
+    return debug_status(cuda_status(launch_dispatch(X, topk_idx, T, H, E, K, counts, offsets,
+                                                    perm, slot_pos, Xp, affinity, L.plan, L.scr,
+                                                    nullptr, 0, static_cast<int *>(ws),
+                                                    static_cast<cudaStream_t>(stream))),
+                        ws, stream);
 }
 
 size_t moe_expert_ffn_workspace_bytes(int rows, int n_groups, int I)
@@ -566,9 +590,11 @@ int moe_expert_ffn(const void *Xp, const int32_t *offsets, int n_groups, int row
     P.out_fp32 = out_fp32;
     const int hint = rows / n_groups > 0 ? rows / n_groups : 1;
     unsigned *ready = reinterpret_cast<unsigned *>(static_cast<unsigned char *>(ws) + kHeader + hbytes);
-    return cuda_status(launch_ffn(&P, 1, H, &I, hint, ready, false, static_cast<int *>(ws),
-                                  static_cast<cudaStream_t>(stream), g_wait_limit_ns,
-                                  g_inject_stall, nullptr));
+    return debug_status(cuda_status(launch_ffn(&P, 1, H, &I, hint, ready, false,
+                                               static_cast<int *>(ws),
+                                               static_cast<cudaStream_t>(stream), g_wait_limit_ns,
+                                               g_inject_stall, nullptr)),
+                        ws, stream);
 }
 
 int moe_combine(const void *Yp, const int32_t *slot_pos, const float *topk_w, const float *Ysh,
@@ -598,8 +624,9 @@ int moe_layer_forward_ex(const moe_shape_t *shape, const moe_weights_t *wt,
                          void *ws, size_t ws_bytes, void *stream)
 {
     if (!wt) return MOE_ERR_INVALID_ARG;
-    return layer_forward(shape, wt, nullptr, routing, X, Y, topk_idx, topk_w, counts, affinity,
-                         ws, ws_bytes, stream);
+    return debug_status(layer_forward(shape, wt, nullptr, routing, X, Y, topk_idx, topk_w, counts,
+                                      affinity, ws, ws_bytes, stream),
+                        ws, stream, shape && shape->T > 0);
 }
 
 int moe_layer_forward_fp8(const moe_shape_t *shape, const moe_weights_fp8_t *w8,
@@ -608,8 +635,9 @@ int moe_layer_forward_fp8(const moe_shape_t *shape, const moe_weights_fp8_t *w8,
                           void *ws, size_t ws_bytes, void *stream)
 {
     if (!w8) return MOE_ERR_INVALID_ARG;
-    return layer_forward(shape, nullptr, w8, routing, X, Y, topk_idx, topk_w, counts, affinity,
-                         ws, ws_bytes, stream);
+    return debug_status(layer_forward(shape, nullptr, w8, routing, X, Y, topk_idx, topk_w, counts,
+                                      affinity, ws, ws_bytes, stream),
+                        ws, stream, shape && shape->T > 0);
 }
 
 int moe_quantize_weight_fp8(const void *W, int G, int R, int C, void *Wq, int32_t *S,

@@ -53,7 +53,9 @@ __global__ void __launch_bounds__(CT) combine_kernel(const uint4 *__restrict__ Y
         uint4 v[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-            if (j0 + u < K) v[u] = __ldg(Yp + static_cast<size_t>(r_s[j0 + u]) * vec + cv);
+            if (j0 + u < K)   // slot -1: a pair the dispatch rejected, no contribution
+                v[u] = r_s[j0 + u] >= 0 ? __ldg(Yp + static_cast<size_t>(r_s[j0 + u]) * vec + cv)
+                                        : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             if (j0 + u >= K) break;

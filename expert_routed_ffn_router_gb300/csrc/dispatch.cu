@@ -148,7 +148,10 @@ __global__ void __launch_bounds__(CHUNK) scatter_kernel(const int32_t *__restric
     for (int j = 0; j < KMAX; ++j) {
         if (j >= K) break;
         const int e = ev[j];
-        if (e < 0 || e >= E) continue;   // reported by masks_kernel
+        if (e < 0 || e >= E) {           // reported by masks_kernel; no row for this pair
+            slot_pos[static_cast<size_t>(t) * K + j] = -1;
+            continue;
+        }
         const int r = base[w * E + e] + __popc(m_s[w * E + e] & below);
         slot_pos[static_cast<size_t>(t) * K + j] = r;
         perm[r] = t;
@@ -205,7 +208,9 @@ __device__ __forceinline__ void gather_tokens(const uint4 *__restrict__ X, int T
                 a[u] = v < vec ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
             }
             for (int j = 0; j < K; ++j) {
-                uint4 *dst = Xp + static_cast<size_t>(__shfl_sync(kFullMask, dst_row, j)) * vec;
+                const int row = __shfl_sync(kFullMask, dst_row, j);
+                if (row < 0) continue;   // a pair with an out-of-range expert: no row
+                uint4 *dst = Xp + static_cast<size_t>(row) * vec;
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int v = v0 + 32 * u + lane;
@@ -364,7 +369,10 @@ __device__ void small_routing(const int32_t *__restrict__ idx, int T, int E, int
         for (int j = 0; j < KMAX; ++j) {
             if (j >= K) break;
             const int e = ev[j];
-            if (e < 0 || e >= E) continue;
+            if (e < 0 || e >= E) {       // reported above; no row for this pair
+                if (out) slot_pos[static_cast<size_t>(tid) * K + j] = -1;
+                continue;
+            }
             const int r = base[w * E + e] + __popc(m_s[w * E + e] & below);
             perm_s[r] = tid;
             if (out) {

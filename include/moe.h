@@ -129,9 +129,20 @@ int moe_workspace_layout(const moe_shape_t *shape, moe_workspace_layout_t *out);
 const char *moe_error_string(int status);
 
 /* Reads the device status word of workspace `ws` (synchronising `stream`), resets it to
- * MOE_OK and returns what it held: MOE_OK or MOE_ERR_DEVICE_TIMEOUT; MOE_ERR_CUDA if the
- * copy itself failed. */
+ * MOE_OK and returns what it held: MOE_OK, MOE_ERR_DEVICE_TIMEOUT (a bounded device-side
+ * wait ran out) or MOE_ERR_INVALID_ARG (the dispatch met an expert index outside [0, E));
+ * MOE_ERR_CUDA if the copy itself failed. */
 int moe_read_status(void *ws, void *stream);
+
+/* Debugging hook: with on = 1, every later call that records device-side conditions in a
+ * workspace status word (moe_router_topk, moe_router_topk_ex, moe_dispatch,
+ * moe_expert_ffn, moe_layer_forward, moe_layer_forward_ex, moe_layer_forward_fp8)
+ * synchronises its stream after enqueueing its work and returns that word, read and reset
+ * as by moe_read_status, in place of MOE_OK -- except for an empty batch and inside a stream
+ * capture (a capture cannot be synchronised).  on = 0 (the default) restores the
+ * asynchronous calls.  Process-wide; not for production use: it serialises the host with
+ * the GPU. */
+void moe_debug_set_sync_status(int on);
 
 /* Testing hook: sets the limit of the bounded device-side waits of the tensor-core FFN
  * kernels (0 restores the default of one second) and, with inject_stall = 1, makes their
@@ -255,7 +266,10 @@ int moe_router_topk_noalloc_status(void *stream);
  *   out Xp       bf16 [T*K, H]  Xp[r] = X[perm[r]]
  *   out affinity int32 [E, E]   (nullable) tokens whose top-K holds both i and j, zero
  *                               diagonal ("GRACE-MoE", Expert Grouping, matrix A)
- *   ws / ws_bytes: workspace (per-token-group expert bit masks and counts). */
+ *   ws / ws_bytes: workspace (per-token-group expert bit masks and counts).
+ * An index outside [0, E) is recorded as MOE_ERR_INVALID_ARG in the workspace's status word
+ * (moe_read_status); its pair gets no row (slot_pos = -1, left out of counts, perm, Xp and
+ * affinity, so offsets[E] < T*K) and nothing is written out of bounds. */
 int moe_dispatch(const void *X, const int32_t *topk_idx, int T, int H, int E, int K,
                  int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *slot_pos,
                  void *Xp, int32_t *affinity,
@@ -291,7 +305,8 @@ int moe_expert_ffn(const void *Xp, const int32_t *offsets, int n_groups, int row
  * expert's result).
  *     Y[t] = sum_j topk_w[t, j] * Yp[slot_pos[t, j]]  (+ Ysh[t] when Ysh != NULL)
  *   Yp bf16 [T*K, H], slot_pos int32 [T, K], topk_w fp32 [T, K], Ysh fp32 [T, H] or NULL
- *   out Y fp32 [T, H].  Summation order is fixed (j ascending, then Ysh). */
+ *   out Y fp32 [T, H].  Summation order is fixed (j ascending, then Ysh).  A slot_pos entry
+ * of -1 (a pair moe_dispatch rejected) contributes nothing. */
 int moe_combine(const void *Yp, const int32_t *slot_pos, const float *topk_w,
                 const float *Ysh, int T, int H, int K, float *Y, void *stream);
 
