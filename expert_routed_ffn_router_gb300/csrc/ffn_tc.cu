@@ -96,6 +96,7 @@ struct ProbDev {
     const int32_t *offsets;  // [n_groups + 1] on the device, or nullptr (one dense group)
     int n_groups;
     int dense_rows;
+    int rows;                // rows of the activation and output buffers (offsets' bound)
     int mt_up, mt_dn;        // weight tiles per token tile: up, down
     int kb_up, kb_dn;        // K blocks: H / 64, I / 64
     int I, H;                // row lengths of h (up output) and of the down output
@@ -281,17 +282,25 @@ __global__ void __launch_bounds__(FP8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     // group row offsets -> shared memory
     const int n0 = p.prob[0].n_groups;
     const int n_cg = n0 + (p.n_probs > 1 ? p.prob[1].n_groups : 0);
+    // (offsets that are not non-decreasing within [0, rows] would send tiles past the
+    // buffers: the launch then records MOE_ERR_INVALID_ARG and runs no tile)
+    int bad = 0;
     for (int pi = 0; pi < p.n_probs; ++pi) {
         const ProbDev &P = p.prob[pi];
         const int base = pi ? n0 : 0;
         for (int g = tid; g < P.n_groups; g += NT) {
             const int a = P.offsets ? P.offsets[g] : 0;
             const int b = P.offsets ? P.offsets[g + 1] : P.dense_rows;
+            bad |= a < 0 || b < a || b > P.rows;
             gstart[base + g] = a;
             gm[base + g] = b - a;
         }
     }
-    __syncthreads();
+    if (__syncthreads_or(bad)) {
+        for (int cg = tid; cg < n_cg; cg += NT) gm[cg] = 0;
+        if (tid == 0) report(p.status, MOE_ERR_INVALID_ARG);
+        __syncthreads();
+    }
     // Tile order, per phase (all up-projection tiles, then all down-projection tiles).  A
     // group whose rows fit in one token tile at most half full is "light": its weights
     // are streamed from HBM for little arithmetic.  The other ("heavy") groups reuse each
@@ -1207,6 +1216,7 @@ cudaError_t launch_ffn(const FfnProblem *probs, int n_probs, int H, const int *I
         d.offsets = P.offsets;
         d.n_groups = P.n_groups;
         d.dense_rows = P.dense_rows;
+        d.rows = P.rows;
         // FP8 tiles: 128 columns of I (up), 256 rows of H (down)
         d.mt_up = fp8 ? (I + 127) / 128 : (I + m_up - 1) / m_up;
         d.mt_dn = fp8 ? (H + 255) / 256 : (H + m_dn - 1) / m_dn;

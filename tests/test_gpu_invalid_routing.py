@@ -113,3 +113,34 @@ def test_debug_mode_returns_the_status_word_from_the_call():
         B.moe_debug_set_sync_status(False)
     torch.cuda.synchronize()
     assert layer.status() == 0
+
+
+@pytest.mark.parametrize("bad", ["decreasing", "past_rows", "negative"])
+def test_expert_ffn_rejects_offsets_outside_its_rows(bad):
+    # moe_expert_ffn reads the group offsets on the device only: offsets that are not
+    # non-decreasing within [0, rows] make the launch record MOE_ERR_INVALID_ARG and run no
+    # tile (nothing written), and the next valid call on the same buffers runs normally
+    w = synth.workload("tiny", T=40)
+    p = Problem(w)
+    T, H, E, K, I = w.T, w.H, w.E, w.K, w.I
+    rows = T * K
+    good = np.linspace(0, rows, E + 1).astype(np.int32)
+    off = good.copy()
+    if bad == "decreasing":
+        off[3], off[4] = good[4], good[3]
+    elif bad == "past_rows":
+        off[-1] = rows + 64
+    else:
+        off[0] = -16
+    rng = np.random.default_rng(2)
+    Xp = host_to_device_bf16(synth.f32_to_bf16_bits(rng.standard_normal((rows, H)).astype(np.float32)))
+    Yp = torch.full((rows, H), 7.0, dtype=torch.float32, device=DEV)
+    ws = torch.zeros(B.moe_expert_ffn_workspace_bytes(rows, E, I), dtype=torch.uint8, device=DEV)
+    B.moe_expert_ffn(Xp, torch.from_numpy(off).to(DEV), E, p.dev["W1"], p.dev["W3"], p.dev["W2"],
+                     Yp, ws)
+    assert B.moe_read_status(ws) == MOE_ERR_INVALID_ARG
+    assert bool(torch.all(Yp == 7.0))
+    B.moe_expert_ffn(Xp, torch.from_numpy(good).to(DEV), E, p.dev["W1"], p.dev["W3"],
+                     p.dev["W2"], Yp, ws)
+    assert B.moe_read_status(ws) == 0
+    assert not bool(torch.any(Yp == 7.0))
