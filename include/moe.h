@@ -283,7 +283,9 @@ int moe_dispatch(const void *X, const int32_t *topk_idx, int T, int H, int E, in
  * tcgen05 tensor cores with fp32 accumulation; the activation h is rounded to bf16.
  *   Xp      bf16 [rows, H]
  *   offsets int32 [n_groups + 1] on the device, non-decreasing, offsets[0] = 0,
- *           offsets[n_groups] <= rows; read by the kernels, never by the host
+ *           offsets[n_groups] <= rows; read by the kernels, never by the host (offsets
+ *           that decrease or leave [0, rows] are recorded as MOE_ERR_INVALID_ARG in the
+ *           status word and no tile runs: nothing is written)
  *   W1, W3  bf16 [n_groups, H, I];  W2 bf16 [n_groups, I, H]
  *   out Yp  [rows, H], bf16 (out_fp32 == 0) or fp32 (out_fp32 == 1)
  *   rows    upper bound of offsets[n_groups] (sizes the tensor maps and the workspace)
