@@ -38,6 +38,7 @@ __global__ void __launch_bounds__(CT) combine_kernel(const uint4 *__restrict__ Y
     __syncthreads();
     const int c = blockIdx.y * COLS + threadIdx.x * 8;
     if (c >= H) return;
+    const unsigned n_rows = gridDim.x * static_cast<unsigned>(K);   // rows of Yp: T*K
     const int vec = H / 8;
     const int cv = c / 8;
     const size_t o = (static_cast<size_t>(t) * H + c) / 4;
@@ -53,9 +54,11 @@ __global__ void __launch_bounds__(CT) combine_kernel(const uint4 *__restrict__ Y
         uint4 v[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-            if (j0 + u < K)   // slot -1: a pair the dispatch rejected, no contribution
-                v[u] = r_s[j0 + u] >= 0 ? __ldg(Yp + static_cast<size_t>(r_s[j0 + u]) * vec + cv)
-                                        : make_uint4(0, 0, 0, 0);
+            if (j0 + u < K)   // a row outside [0, T*K) (-1: a pair the dispatch rejected)
+                              // contributes nothing
+                v[u] = static_cast<unsigned>(r_s[j0 + u]) < n_rows
+                           ? __ldg(Yp + static_cast<size_t>(r_s[j0 + u]) * vec + cv)
+                           : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             if (j0 + u >= K) break;

@@ -308,7 +308,7 @@ int moe_expert_ffn(const void *Xp, const int32_t *offsets, int n_groups, int row
  *     Y[t] = sum_j topk_w[t, j] * Yp[slot_pos[t, j]]  (+ Ysh[t] when Ysh != NULL)
  *   Yp bf16 [T*K, H], slot_pos int32 [T, K], topk_w fp32 [T, K], Ysh fp32 [T, H] or NULL
  *   out Y fp32 [T, H].  Summation order is fixed (j ascending, then Ysh).  A slot_pos entry
- * of -1 (a pair moe_dispatch rejected) contributes nothing. */
+ * outside [0, T*K) -- -1 marks a pair moe_dispatch rejected -- contributes nothing. */
 int moe_combine(const void *Yp, const int32_t *slot_pos, const float *topk_w,
                 const float *Ysh, int T, int H, int K, float *Y, void *stream);
 

@@ -144,3 +144,24 @@ def test_expert_ffn_rejects_offsets_outside_its_rows(bad):
                      p.dev["W2"], Yp, ws)
     assert B.moe_read_status(ws) == 0
     assert not bool(torch.any(Yp == 7.0))
+
+
+def test_combine_skips_rows_outside_its_inputs():
+    # slot_pos entries outside [0, T*K) (here past the end and far past it) contribute
+    # nothing; the other slots are summed as usual
+    T, H, K = 45, 256, 2
+    rng = np.random.default_rng(8)
+    slot = rng.permutation(T * K).astype(np.int32).reshape(T, K)
+    slot[3, 0], slot[17, 1], slot[44, 0] = T * K + 5, 1 << 30, -2
+    keep = (slot >= 0) & (slot < T * K)
+    Yp_h = synth.f32_to_bf16_bits(rng.standard_normal((T * K, H)).astype(np.float32))
+    wt = rng.random((T, K)).astype(np.float32)
+    Y = torch.empty(T, H, dtype=torch.float32, device=DEV)
+    B.moe_combine(host_to_device_bf16(Yp_h), torch.from_numpy(slot).to(DEV),
+                  torch.from_numpy(wt).to(DEV), None, Y)
+    Yp64 = synth.bf16_bits_to_f32(Yp_h).astype(np.float64)
+    Y_ref = np.zeros((T, H))
+    for j in range(K):
+        m = keep[:, j]
+        Y_ref[m] += wt[m, j, None].astype(np.float64) * Yp64[slot[m, j]]
+    assert np.abs(Y.cpu().numpy() - Y_ref).max() <= 1e-4
