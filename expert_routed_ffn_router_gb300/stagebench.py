@@ -4,9 +4,11 @@
 
 Stages: router (moe_router_topk), dispatch (moe_dispatch on the router's output), combine
 (moe_combine on seeded expert outputs Yp and the router's routing), layer
-(moe_layer_forward).  The router, dispatch and combine stages allocate only their own
-inputs, so they run at full token counts without the 22.5 GB of expert weights -- small
-enough for profiler captures.  Prints one JSON line with the mean milliseconds per call.
+(moe_layer_forward; with --fp8 the FP8 layer on E4M3 experts).  The router, dispatch and
+combine stages allocate only their own inputs, so they run at full token counts without the
+22.5 GB of expert weights -- small enough for profiler captures.  Prints one JSON line with
+the mean milliseconds per call and the call's status word (for the layer also the number of
+activated experts).
 """
 from __future__ import annotations
 
