@@ -155,3 +155,28 @@ def test_binding_checks_element_types_and_sizes_before_the_call():
     with pytest.raises(ValueError, match="W1: "):
         binding.moe_layer_forward(shape, W, X, torch.zeros(T, H), idx, wt,
                                   torch.zeros(E, dtype=torch.int32), None, ws)
+
+
+def test_binding_checks_the_dispatch_ffn_and_combine_arguments():
+    import torch
+    T, H, E, K, I = 4, 64, 8, 2, 64
+    X = torch.zeros(T, H, dtype=torch.bfloat16)
+    idx = torch.zeros(T, K, dtype=torch.int32)
+    i32 = lambda n: torch.zeros(n, dtype=torch.int32)
+    ws = torch.zeros(1024, dtype=torch.uint8)
+    Xp = torch.zeros(T * K, H, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="perm: dtype"):
+        binding.moe_dispatch(X, idx, E, i32(E), i32(E + 1), torch.zeros(T * K, dtype=torch.int64),
+                             i32(T * K), Xp, None, ws)
+    with pytest.raises(ValueError, match="offsets: 8 elements, expected 9"):
+        binding.moe_dispatch(X, idx, E, i32(E), i32(E), i32(T * K), i32(T * K), Xp, None, ws)
+    W = torch.zeros(E, H, I, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="Yp: dtype"):
+        binding.moe_expert_ffn(Xp, i32(E + 1), E, W, W, W.transpose(1, 2).contiguous(),
+                               torch.zeros(T * K, H, dtype=torch.float16), ws)
+    with pytest.raises(ValueError, match="W2: "):
+        binding.moe_expert_ffn(Xp, i32(E + 1), E, W, W, W[:-1].contiguous(),
+                               torch.zeros(T * K, H, dtype=torch.float32), ws)
+    with pytest.raises(ValueError, match="slot_pos: dtype"):
+        binding.moe_combine(Xp, torch.zeros(T, K, dtype=torch.int64),
+                            torch.zeros(T, K), None, torch.zeros(T, H))
