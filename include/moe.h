@@ -26,8 +26,9 @@
  *     Host structs (moe_shape_t, moe_weights_t) are read during the call only.
  *   - Row-major layouts; "bf16" arrays hold IEEE bfloat16 values (2 bytes each).
  *   - `stream` is a cudaStream_t (0 = legacy default stream).  All work is enqueued on it;
- *     no call synchronises the host, allocates or frees memory, so calls can be captured
- *     in a CUDA graph.  Outputs are valid once the stream reaches them.  (One exception,
+ *     no call synchronises the host (moe_read_status, and every call in the debug mode of
+ *     moe_debug_set_sync_status, excepted), allocates or frees memory, so calls can be
+ *     captured in a CUDA graph.  Outputs are valid once the stream reaches them.  (One exception,
  *     moe_layer_forward on bf16 weights up to 128 tokens: it forks the shared expert onto a
  *     side stream of the library and joins it back before the combine; that stream and
  *     its two events are created by the first such call of a host thread on a device and
@@ -38,8 +39,10 @@
  *     Calls that share a workspace must be serialised by the caller.
  *   - Arguments are validated on the host before anything is enqueued: an invalid call
  *     returns a negative moe_status_t and has no effect.  A failing launch returns
- *     MOE_ERR_CUDA.  Conditions found on the device (a bounded wait that ran out) are
- *     recorded in the workspace's status word; read them with moe_read_status().
+ *     MOE_ERR_CUDA.  Conditions found on the device (a bounded wait that ran out, an
+ *     expert index outside [0, E) given to moe_dispatch, group offsets outside [0, rows]
+ *     given to moe_expert_ffn) are recorded in the workspace's status word and never lead
+ *     to an access out of bounds; read them with moe_read_status().
  *   - Supported shapes: 1 <= E <= 1024, 1 <= K <= min(E, 32), H and I multiples of 64,
  *     T >= 0 (T == 0 enqueues nothing and returns MOE_OK), T*K < 2^31.
  */
@@ -57,7 +60,8 @@ extern "C" {
 
 typedef enum moe_status {
     MOE_OK = 0,
-    MOE_ERR_INVALID_ARG = -1,        /* null pointer, negative size, K > E, ...            */
+    MOE_ERR_INVALID_ARG = -1,        /* null pointer, negative size, K > E, ...; on the
+                                        device: out-of-range expert index or offsets      */
     MOE_ERR_UNSUPPORTED_SHAPE = -2,  /* H or I not a multiple of 64, E > 1024, K > 32, ... */
     MOE_ERR_MISALIGNED = -3,         /* a pointer is not 16-byte aligned (ws: 256-byte)     */
     MOE_ERR_WORKSPACE_TOO_SMALL = -4,
@@ -130,8 +134,9 @@ const char *moe_error_string(int status);
 
 /* Reads the device status word of workspace `ws` (synchronising `stream`), resets it to
  * MOE_OK and returns what it held: MOE_OK, MOE_ERR_DEVICE_TIMEOUT (a bounded device-side
- * wait ran out) or MOE_ERR_INVALID_ARG (the dispatch met an expert index outside [0, E));
- * MOE_ERR_CUDA if the copy itself failed. */
+ * wait ran out) or MOE_ERR_INVALID_ARG (the dispatch met an expert index outside [0, E),
+ * or the expert FFN group offsets outside [0, rows]); MOE_ERR_CUDA if the copy itself
+ * failed. */
 int moe_read_status(void *ws, void *stream);
 
 /* Debugging hook: with on = 1, every later call that records device-side conditions in a
