@@ -182,7 +182,8 @@ void moe_debug_set_shared_side(int mode);
 /* Router: gate GEMM, sigmoid scoring, selection bias, top-K, renormalised weights
  * ("DeepSeek-V4.1-Flash", Kernels, Mega-Gate: fused into one kernel; "Lower latency and
  * higher throughput...", MoE Router).  One launch up to 15 tokens and from 2049 to 4096
- * tokens (the last CTA of each token tile selects); other batch sizes take a tile-GEMM
+ * tokens (the last CTA of each token tile selects; up to ~800 experts, whose per-warp
+ * arrays fit that CTA's shared memory); other batches take a tile-GEMM
  * launch that leaves split-K partial logits in the workspace and a finalise launch that
  * sums, scores and selects them (the scores themselves are never stored).
  *   X      bf16 [T, H]      token activations
